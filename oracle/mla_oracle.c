@@ -1,0 +1,230 @@
+/*
+ * Reference (oracle) for paged FP8 MLA decode: plain, slow, fp64 CPU code.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  It shares no code,
+ * header, table or constant generator with the CUDA path.
+ *
+ * What it computes (the plain definition; the split-KV method reaches the same
+ * result up to rounding because it is an exact refactoring of softmax):
+ *
+ *   Geometry, from "CuTe DSL FP8 MLA decode regression" (TensorRT-LLM issue
+ *   #20510, section "Setup"): each KV row is 576 E4M3 values, 512 latent + 64
+ *   rope; K is the whole row and V is its first 512 values (same issue,
+ *   "Analysis": the V operand is the latent part of the rows K already read).
+ *   Page size 32: token j of request b sits in slot j % 32 of page
+ *   page_table[b][j / 32].
+ *
+ *   For query row (b, qi, h):
+ *     q   = q_scale  * dec(Q[b][qi][h][0:576])
+ *     k_j = kv_scale * dec(KV row of token j),   v_j = k_j[0:512]
+ *     n   = L_b - q_len + qi + 1 if causal (MTP verify: query token i sees keys
+ *           [0, L - q_len + i], inclusive), else L_b
+ *     s_j = softmax_scale * (q . k_j),           j < n
+ *     M = max_j s_j,  Z = sum_j exp(s_j - M)
+ *     O = sum_j exp(s_j - M) v_j / Z,  LSE = M + ln Z   (natural log)
+ *
+ *   dec() is the exact E4M3 ("FN", no infinities) decode: sign s, 4-bit
+ *   exponent e with bias 7, 3-bit mantissa m; e == 0 is subnormal m/8 * 2^-6;
+ *   e == 15 && m == 7 is NaN; otherwise (1 + m/8) * 2^(e-7).
+ *
+ *   Partials: for a key range, (m, l, O) with m = max_j s_j * log2(e) (log2
+ *   units), l = sum_j 2^(t_j - m), O = sum_j 2^(t_j - m) v_j, t_j = s_j log2(e);
+ *   an empty range gives (-inf, 0, 0).  The merge ("fmhaReductionKernel",
+ *   TensorRT-LLM PR #20380, "Description"): M = max_s m_s,
+ *   w_s = 2^(m_s - M), O = sum_s w_s O_s / sum_s w_s l_s,
+ *   LSE = ln 2 * (M + log2 sum_s w_s l_s); empty partials contribute nothing.
+ *
+ * Two passes over stored scores per row; no online rescaling, no blocking.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_HEAD_DIM 576
+#define ORC_LATENT_DIM 512
+#define ORC_PAGE 32
+
+/* Exact E4M3 decode from its bit fields. */
+double mla_oracle_e4m3_decode(uint8_t code) {
+  int sign = (code >> 7) & 1;
+  int e = (code >> 3) & 15;
+  int m = code & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) {
+    v = ldexp((double)m / 8.0, -6);
+  } else {
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  }
+  return sign ? -v : v;
+}
+
+static void build_lut(double lut[256]) {
+  for (int c = 0; c < 256; ++c) lut[c] = mla_oracle_e4m3_decode((uint8_t)c);
+}
+
+int mla_oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Visible key range of one row, intersected with [tok_begin, tok_end). */
+static void row_range(int32_t L, int32_t q_len, int32_t qi, int32_t causal,
+                      int64_t tok_begin, int64_t tok_end, int64_t* lo, int64_t* hi) {
+  int64_t n = causal ? (int64_t)L - q_len + qi + 1 : (int64_t)L;
+  if (n < 0) n = 0;
+  int64_t a = tok_begin < 0 ? 0 : tok_begin;
+  int64_t b = (tok_end < 0 || tok_end > n) ? n : tok_end;
+  if (b < a) b = a;
+  *lo = a;
+  *hi = b;
+}
+
+static const uint8_t* key_row(const uint8_t* kv, const int32_t* page_table, int32_t max_pages,
+                              int32_t b, int64_t j) {
+  int64_t page = page_table[(int64_t)b * max_pages + j / ORC_PAGE];
+  return kv + ((page * ORC_PAGE) + (j % ORC_PAGE)) * ORC_HEAD_DIM;
+}
+
+/*
+ * Decode rows.  rows[i] is the flat row id (b*q_len + qi)*num_heads + h.
+ * Keys are restricted to [tok_begin, tok_end) when those are >= 0.
+ * mode 0: final outputs: out[i][512] = O, lse[i] = LSE (natural log);
+ *         an empty row gives O = 0, LSE = -inf.
+ * mode 1: partials: out[i][512] = unnormalised O, m_out[i] = m (log2 units),
+ *         l_out[i] = l.
+ * Returns 0, or -1 on an out-of-range page id, -2 on allocation failure.
+ */
+int mla_oracle_decode_rows(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
+                           const int32_t* page_table, int32_t max_pages,
+                           const int32_t* kv_lens, int32_t batch, int32_t q_len,
+                           int32_t num_heads, int32_t causal, double q_scale,
+                           double kv_scale, double softmax_scale, const int64_t* rows,
+                           int64_t n_rows, int64_t tok_begin, int64_t tok_end, int32_t mode,
+                           double* out, double* lse, double* m_out, double* l_out,
+                           int32_t n_threads) {
+  double lut[256];
+  int status = 0;
+  build_lut(lut);
+  (void)batch;
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+  (void)n_threads;
+#endif
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n_rows; ++i) {
+    int64_t r = rows[i];
+    int32_t h = (int32_t)(r % num_heads);
+    int32_t qi = (int32_t)((r / num_heads) % q_len);
+    int32_t b = (int32_t)(r / ((int64_t)num_heads * q_len));
+    double qd[ORC_HEAD_DIM];
+    double* o = out + i * ORC_LATENT_DIM;
+    int64_t lo, hi;
+    (void)h;
+    for (int d = 0; d < ORC_HEAD_DIM; ++d) qd[d] = q_scale * lut[q[r * ORC_HEAD_DIM + d]];
+    row_range(kv_lens[b], q_len, qi, causal, tok_begin, tok_end, &lo, &hi);
+    for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] = 0.0;
+    if (hi <= lo) {
+      if (mode == 0) {
+        lse[i] = -INFINITY;
+      } else {
+        m_out[i] = -INFINITY;
+        l_out[i] = 0.0;
+      }
+      continue;
+    }
+    double* s = (double*)malloc(sizeof(double) * (size_t)(hi - lo));
+    if (!s) {
+#pragma omp atomic write
+      status = -2;
+      continue;
+    }
+    int bad = 0;
+    /* Pass 1: scores. */
+    for (int64_t j = lo; j < hi; ++j) {
+      int64_t page = page_table[(int64_t)b * max_pages + j / ORC_PAGE];
+      if (page < 0 || page >= num_pages) {
+        bad = 1;
+        s[j - lo] = 0.0;
+        continue;
+      }
+      const uint8_t* k = key_row(kv, page_table, max_pages, b, j);
+      double dot = 0.0;
+      for (int d = 0; d < ORC_HEAD_DIM; ++d) dot += qd[d] * (kv_scale * lut[k[d]]);
+      s[j - lo] = softmax_scale * dot;
+    }
+    double M = -INFINITY;
+    for (int64_t j = lo; j < hi; ++j)
+      if (s[j - lo] > M) M = s[j - lo];
+    /* Pass 2: weights and the weighted sum of values. */
+    double Z = 0.0;
+    for (int64_t j = lo; j < hi; ++j) {
+      double w = exp(s[j - lo] - M);
+      const uint8_t* k;
+      int64_t page = page_table[(int64_t)b * max_pages + j / ORC_PAGE];
+      Z += w;
+      if (page < 0 || page >= num_pages) continue;
+      k = key_row(kv, page_table, max_pages, b, j);
+      for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] += w * (kv_scale * lut[k[d]]);
+    }
+    free(s);
+    if (bad) {
+#pragma omp atomic write
+      status = -1;
+    }
+    if (mode == 0) {
+      for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] /= Z;
+      lse[i] = M + log(Z);
+    } else {
+      m_out[i] = M * (1.0 / log(2.0));
+      l_out[i] = Z;
+    }
+  }
+  return status;
+}
+
+/*
+ * Merge split partials (closed form).  ml: [rows][S][2] = (m, l);
+ * o: [rows][S][512]; fp64 throughout (float32 partials widen exactly).
+ * An empty slot (l == 0 or m == -inf) is skipped.  A row with no non-empty
+ * slot gives O = 0 and LSE = -inf.
+ */
+void mla_oracle_merge(const double* ml, const double* o, int64_t rows, int32_t S, double* out,
+                      double* lse) {
+  for (int64_t r = 0; r < rows; ++r) {
+    double M = -INFINITY;
+    for (int32_t s = 0; s < S; ++s) {
+      double m = ml[(r * S + s) * 2 + 0];
+      double l = ml[(r * S + s) * 2 + 1];
+      if (l > 0.0 && m > M) M = m;
+    }
+    double* dst = out + r * ORC_LATENT_DIM;
+    for (int d = 0; d < ORC_LATENT_DIM; ++d) dst[d] = 0.0;
+    if (M == -INFINITY) {
+      lse[r] = -INFINITY;
+      continue;
+    }
+    double den = 0.0;
+    for (int32_t s = 0; s < S; ++s) {
+      double m = ml[(r * S + s) * 2 + 0];
+      double l = ml[(r * S + s) * 2 + 1];
+      if (!(l > 0.0) || m == -INFINITY) continue;
+      double w = exp2(m - M);
+      den += w * l;
+      const double* src = o + (r * S + s) * ORC_LATENT_DIM;
+      for (int d = 0; d < ORC_LATENT_DIM; ++d) dst[d] += w * src[d];
+    }
+    for (int d = 0; d < ORC_LATENT_DIM; ++d) dst[d] /= den;
+    lse[r] = log(2.0) * (M + log2(den));
+  }
+}

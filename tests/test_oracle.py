@@ -1,0 +1,256 @@
+"""Pins for the fp64 oracle, checked against things other than itself.
+
+Each test names what fixes the expected value: a library routine (torch's
+float8 widening, torch's float64 attention), a closed form, or an invariance
+of the method (split-KV is an exact refactoring of softmax; pages are only an
+indirection; the MTP-verify mask truncates the key range).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import HEAD_DIM, LATENT_DIM, PAGE_SIZE, SOFTMAX_SCALE, decode_inputs, merge_partials
+
+
+def _gather_keys(inp, b):
+    """Dense [L, 576] uint8 keys of request b, gathered page by page in Python."""
+    L = int(inp.kv_lens[b])
+    pages = inp.page_table[b].cpu()
+    rows = []
+    for j in range(L):
+        rows.append(inp.kv[int(pages[j // PAGE_SIZE]), j % PAGE_SIZE])
+    return torch.stack(rows) if rows else torch.empty((0, HEAD_DIM), dtype=torch.uint8)
+
+
+def _widen(u8):
+    return u8.view(torch.float8_e4m3fn).to(torch.float64)
+
+
+# --- (1) E4M3 codec ---------------------------------------------------------
+
+def test_e4m3_all_codes_match_torch_widening():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert set(np.nonzero(nan)[0].tolist()) == {0x7F, 0xFF}
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # Signed zero is kept.
+    assert math.copysign(1.0, ours[0x80]) == -1.0
+
+
+def test_e4m3_landmarks():
+    # Largest finite, smallest normal, smallest subnormal and one (E4M3 "FN").
+    assert oracle.e4m3_decode(np.array([0x7E]))[0] == 448.0
+    assert oracle.e4m3_decode(np.array([0x08]))[0] == 2.0 ** -6
+    assert oracle.e4m3_decode(np.array([0x01]))[0] == 2.0 ** -9
+    assert oracle.e4m3_decode(np.array([0x38]))[0] == 1.0
+    assert oracle.e4m3_decode(np.array([0xB8]))[0] == -1.0
+
+
+def test_e4m3_widening_to_bf16_is_exact():
+    # "Sparse MLA decode" page: widening E4M3 to BF16 loses nothing.
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes)
+    finite = ~np.isnan(vals)
+    bf = torch.from_numpy(vals[finite]).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(bf, vals[finite])
+
+
+# --- (2) single key, (3) equal scores --------------------------------------
+
+@pytest.mark.parametrize("q_scale,kv_scale", [(1.0, 1.0), (0.5, 2.0)])
+def test_single_key_returns_v(q_scale, kv_scale):
+    inp = decode_inputs(1, 3, 1, [1], seed=11)
+    out, lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=1,
+                                  num_heads=3, causal=False, softmax_scale=0.3,
+                                  q_scale=q_scale, kv_scale=kv_scale)
+    k = _widen(inp.kv[int(inp.page_table[0, 0]), 0]) * kv_scale
+    for h in range(3):
+        q = _widen(inp.q[0, 0, h]) * q_scale
+        assert np.array_equal(out[h], k[:LATENT_DIM].numpy())
+        assert lse[h] == pytest.approx(0.3 * float(q @ k), abs=1e-12)
+
+
+def test_equal_scores_give_mean_of_v_and_log_n():
+    # Zero latent query: every score comes from the rope dims.  Give every key
+    # the same rope part, so every score is equal while V varies.
+    inp = decode_inputs(1, 2, 1, [77], seed=12)
+    inp.q[..., :LATENT_DIM] = 0
+    inp.kv[..., LATENT_DIM:] = inp.kv[0, 0, LATENT_DIM:]
+    out, lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=1,
+                                  num_heads=2, causal=False, softmax_scale=SOFTMAX_SCALE)
+    keys = _widen(_gather_keys(inp, 0))
+    mean_v = keys[:, :LATENT_DIM].mean(dim=0).numpy()
+    for h in range(2):
+        s = SOFTMAX_SCALE * float(_widen(inp.q[0, 0, h]) @ keys[0])
+        np.testing.assert_allclose(out[h], mean_v, rtol=0, atol=1e-13)
+        assert lse[h] == pytest.approx(s + math.log(77), abs=1e-12)
+
+
+# --- (7) brute force and the two-key closed form ---------------------------
+
+def _sdpa_reference(inp, causal, scale, q_scale=1.0, kv_scale=1.0):
+    """Attention through torch's float64 scaled_dot_product_attention."""
+    outs, lses = [], []
+    B, q_len, H = inp.batch, inp.q_len, inp.num_heads
+    for b in range(B):
+        keys = _widen(_gather_keys(inp, b)) * kv_scale          # [L, 576]
+        L = keys.shape[0]
+        q = _widen(inp.q[b]).reshape(q_len * H, HEAD_DIM) * q_scale
+        mask = torch.ones((q_len * H, L), dtype=torch.bool)
+        if causal:
+            for qi in range(q_len):
+                mask[qi * H:(qi + 1) * H, L - q_len + qi + 1:] = False
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q[None, None], keys[None, None], keys[None, None, :, :LATENT_DIM],
+            attn_mask=mask[None, None], scale=scale)[0, 0]
+        logits = (q @ keys.T) * scale
+        logits = logits.masked_fill(~mask, -math.inf)
+        outs.append(o)
+        lses.append(torch.logsumexp(logits, dim=-1))
+    return torch.cat(outs).numpy(), torch.cat(lses).numpy()
+
+
+@pytest.mark.parametrize("B,H,q_len,lens,causal", [
+    (1, 4, 1, [64], False),
+    (2, 3, 1, [33, 7], False),
+    (2, 2, 4, [40, 9], True),
+    (1, 1, 8, [61], True),
+])
+def test_bruteforce_matches_torch_attention(B, H, q_len, lens, causal):
+    inp = decode_inputs(B, H, q_len, lens, seed=13, extra_pages=3)
+    out, lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=q_len,
+                                  num_heads=H, causal=causal, softmax_scale=0.11,
+                                  q_scale=1.5, kv_scale=0.75)
+    ref_o, ref_lse = _sdpa_reference(inp, causal, 0.11, q_scale=1.5, kv_scale=0.75)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+
+
+def test_two_key_closed_form():
+    inp = decode_inputs(1, 1, 1, [2], seed=14)
+    out, lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=1,
+                                  num_heads=1, causal=False, softmax_scale=0.25)
+    q = _widen(inp.q[0, 0, 0]).numpy()
+    page = int(inp.page_table[0, 0])
+    k0 = _widen(inp.kv[page, 0]).numpy()
+    k1 = _widen(inp.kv[page, 1]).numpy()
+    s0, s1 = 0.25 * float(q @ k0), 0.25 * float(q @ k1)
+    e0, e1 = math.exp(s0), math.exp(s1)
+    expect = (e0 * k0[:LATENT_DIM] + e1 * k1[:LATENT_DIM]) / (e0 + e1)
+    np.testing.assert_allclose(out[0], expect, rtol=1e-13, atol=1e-15)
+    assert lse[0] == pytest.approx(math.log(e0 + e1), abs=1e-13)
+
+
+# --- (4) split invariance, (5) causal reduction, (6) permutation -----------
+
+@pytest.mark.parametrize("bounds", [[0, 100], [0, 1, 100], [0, 32, 64, 96, 100], [0, 3, 50, 51, 99, 100]])
+def test_split_partials_merge_to_unsplit(bounds):
+    inp = decode_inputs(1, 3, 2, [100], seed=15)
+    kw = dict(q_len=2, num_heads=3, causal=True, softmax_scale=0.2)
+    full_o, full_lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, **kw)
+    parts_o, parts_ml = [], []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        o, m, l = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, tok_begin=a,
+                                     tok_end=b, partial=True, **kw)
+        parts_o.append(o)
+        parts_ml.append(np.stack([m, l], axis=-1))
+    po = np.stack(parts_o, axis=1)
+    pml = np.stack(parts_ml, axis=1)
+    o, lse = oracle.merge(po, pml)
+    np.testing.assert_allclose(o, full_o, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse, full_lse, rtol=0, atol=1e-12)
+
+
+def test_causal_row_equals_truncated_noncausal():
+    L, q_len, H = 70, 8, 2
+    inp = decode_inputs(1, H, q_len, [L], seed=16)
+    oc, lc = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=q_len,
+                                num_heads=H, causal=True, softmax_scale=0.3)
+    for qi in range(q_len):
+        n = L - q_len + qi + 1
+        on, ln = oracle.decode_rows(inp.q, inp.kv, inp.page_table, torch.tensor([n], dtype=torch.int32),
+                                    q_len=q_len, num_heads=H, causal=False, softmax_scale=0.3)
+        sl = slice(qi * H, (qi + 1) * H)
+        np.testing.assert_array_equal(oc[sl], on[sl])
+        np.testing.assert_array_equal(lc[sl], ln[sl])
+
+
+def test_page_permutation_invariance():
+    inp = decode_inputs(2, 2, 1, [90, 45], seed=17, extra_pages=2)
+    kw = dict(q_len=1, num_heads=2, causal=False, softmax_scale=0.3)
+    o1, l1 = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, **kw)
+    P = inp.num_pages
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(5))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P)
+    kv2 = inp.kv[perm]                        # new page i holds old page perm[i]
+    pt = inp.page_table.clone()
+    valid = pt >= 0
+    pt[valid] = inv[pt[valid].long()].to(torch.int32)
+    o2, l2 = oracle.decode_rows(inp.q, kv2, pt, inp.kv_lens, **kw)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_scale_placement():
+    # q_scale and kv_scale multiply the logits; kv_scale also scales V.
+    inp = decode_inputs(1, 2, 1, [50], seed=18)
+    kw = dict(q_len=1, num_heads=2, causal=False)
+    o1, l1 = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, softmax_scale=0.3,
+                                q_scale=2.0, kv_scale=0.5, **kw)
+    o2, l2 = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, softmax_scale=0.3,
+                                **kw)
+    np.testing.assert_allclose(o1, 0.5 * o2, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+# --- merge pins ------------------------------------------------------------
+
+def test_merge_single_slot_and_empty_slots():
+    o, ml = merge_partials(rows=5, num_splits=6, seed=3, empty_frac=0.0)
+    # Only slot 2 is kept in each row: the merge must return O_2 / l_2.
+    ml_one = ml.copy()
+    o_one = o.copy()
+    keep = 2
+    for s in range(6):
+        if s != keep:
+            ml_one[:, s, 0] = -np.inf
+            ml_one[:, s, 1] = 0.0
+            o_one[:, s, :] = 0.0
+    out, lse = oracle.merge(o_one, ml_one)
+    np.testing.assert_allclose(out, o[:, keep, :].astype(np.float64) / ml[:, keep, 1:2], rtol=1e-15)
+    expect_lse = math.log(2.0) * ml[:, keep, 0].astype(np.float64) + np.log(ml[:, keep, 1].astype(np.float64))
+    np.testing.assert_allclose(lse, expect_lse, rtol=0, atol=1e-12)
+
+
+def test_merge_all_empty_row():
+    o, ml = merge_partials(rows=3, num_splits=4, seed=4, all_empty_rows=[1])
+    out, lse = oracle.merge(o, ml)
+    assert np.all(out[1] == 0.0) and lse[1] == -np.inf
+    assert np.all(np.isfinite(out[[0, 2]]))
+
+
+def test_merge_equals_pairwise_combination():
+    # Merging three slots at once equals merging two, then the third: the
+    # closed form is associative.  Written through the partial convention
+    # (m, l, O) -> (m, l, O) of two merged slots, with no reference to the
+    # oracle's own code.
+    o, ml = merge_partials(rows=4, num_splits=3, seed=5, empty_frac=0.0)
+    out3, lse3 = oracle.merge(o, ml)
+    m0, l0 = ml[:, 0, 0].astype(np.float64), ml[:, 0, 1].astype(np.float64)
+    m1, l1 = ml[:, 1, 0].astype(np.float64), ml[:, 1, 1].astype(np.float64)
+    mm = np.maximum(m0, m1)
+    a0, a1 = np.exp2(m0 - mm), np.exp2(m1 - mm)
+    o01 = a0[:, None] * o[:, 0] + a1[:, None] * o[:, 1]
+    l01 = a0 * l0 + a1 * l1
+    o2 = np.stack([o01, o[:, 2].astype(np.float64)], axis=1)
+    ml2 = np.stack([np.stack([mm, l01], -1), ml[:, 2].astype(np.float64)], axis=1)
+    out2, lse2 = oracle.merge(o2, ml2)
+    np.testing.assert_allclose(out3, out2, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(lse3, lse2, rtol=0, atol=1e-12)
