@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark: paged FP8 MLA split-KV decode on one GB300 (or N replicas).
+
+One step = one full decode call (split-KV kernel + merge) over one batch of
+synthetic, seeded inputs: H = 12 heads, q = 1, B = 16 requests of 1,048,576
+KV tokens each (latent 512 + rope 64 E4M3, page size 32, random page
+permutation), the long-context workload of TensorRT-LLM issue #20510.  The
+KV cache (9.66 GB) is far larger than L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 MLA split-KV decode us/call; KV-read HBM GB/s as fraction of GB300 peak"
+UNIT = "us/call"
+DEFAULT_WORKLOAD = "long_h12_q1_l1m_b16"
+# Published time for this exact workload (H12 q1 B16 1M, issue #20510 "Repro 1",
+# kernel before #19338, on an unspecified Blackwell SM10x GPU): context only.
+PUBLISHED_US = {"long_h12_q1_l1m_b16": 1095.5}
+KERNEL_SOURCES = ["split_kv_mla_paged_gb300/csrc/mla_decode.cu",
+                  "split_kv_mla_paged_gb300/csrc/sm103_ptx.cuh"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per split-KV launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "split_kv_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    entry = d.get(workload)
+    if not entry or entry.get("kernel_sha") != kernel_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(inp, w, rows_per_sample: int, softmax_scale: float):
+    """Time the oracle on the first `rows_per_sample` rows; return (seconds, rows, threads)."""
+    import numpy as np
+    import torch
+    import oracle
+    H, q_len = inp.num_heads, inp.q_len
+    per_req = H * q_len
+    n_req = max(1, -(-rows_per_sample // per_req))
+    rows = np.arange(min(rows_per_sample, inp.rows), dtype=np.int64)
+    # Host copies of only the sampled requests' pages (prepared outside the timing).
+    batches = []
+    for b in range(n_req):
+        L = int(inp.kv_lens[b])
+        n_pages = (L + 31) // 32
+        pages = inp.page_table[b, :n_pages].to(torch.int64).to(inp.kv.device)
+        kv_b = inp.kv[pages].cpu().numpy()
+        q_b = inp.q[b:b + 1].cpu().numpy()
+        table = np.arange(n_pages, dtype=np.int32)[None, :]
+        sel = rows[(rows // per_req) == b] - b * per_req
+        batches.append((q_b, kv_b, table, np.array([L], dtype=np.int32), sel))
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    done = 0
+    for q_b, kv_b, table, lens, sel in batches:
+        oracle.decode_rows(q_b, kv_b, table, lens, q_len=q_len, num_heads=H, causal=w["causal"],
+                           softmax_scale=softmax_scale, rows=sel)
+        done += len(sel)
+    return time.perf_counter() - t0, done, threads
+
+
+def run_reference(args, w, world, rank):
+    """The oracle, as it stands, on the host cores: each step a bounded sample."""
+    import torch
+    from synth import SOFTMAX_SCALE, workload_inputs
+    if world > 1 and rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if dev == "cpu":
+        # Only the sampled request is needed on the host.
+        from synth import decode_inputs
+        inp = decode_inputs(1, w["num_heads"], w["q_len"], w["kv_lens"][:1], w["seed"])
+    else:
+        inp = workload_inputs(args.workload, device=dev)
+    rows_total = w["batch"] * w["num_heads"] * w["q_len"]
+    sample_rows = args.ref_rows
+    times = []
+    for k in range(args.warmup + args.steps):
+        t, done, threads = cpu_oracle_sample(inp, w, sample_rows, SOFTMAX_SCALE)
+        if k >= args.warmup:
+            times.append(t / done * rows_total * 1e6)
+    value = statistics.mean(times)
+    sample = (f"{sample_rows} of {rows_total} rows per step (request 0, all heads), "
+              f"KV length {w['kv_lens'][0]}; time scaled by rows")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,0.5^2) cast to E4M3)",
+        "config": {"workload": args.workload, "batch": w["batch"], "num_heads": w["num_heads"],
+                   "q_len": w["q_len"], "kv_len": w["kv_lens"][0], "causal": w["causal"],
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--plan", choices=["gb300", "pages"], default="gb300")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-rows", type=int, default=24,
+                    help="rows of the oracle CPU baseline sample (0 disables it)")
+    ap.add_argument("--ref-rows", type=int, default=12)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from synth import SOFTMAX_SCALE, WORKLOADS, workload_inputs
+    w = WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+        run_reference(args, w, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import numpy as np
+    import torch
+    import split_kv_mla_paged_gb300 as mla
+    from split_kv_mla_paged_gb300 import build as mla_build
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(mla_build.LIB_PATH):
+        mla_build.build()
+    if world > 1:
+        dist.barrier()
+    mla.load_library()
+
+    inp = workload_inputs(args.workload, device=dev)
+    B, H, q_len = inp.batch, inp.num_heads, inp.q_len
+    lens = inp.kv_lens.tolist()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    if args.plan == "pages" and w["target"] is not None:
+        plan = mla.mla_decode_plan(lens, H, q_len, target_ctas=w["target"])
+    else:
+        plan = mla.mla_decode_plan(lens, H, q_len, sm_count=sm_count)
+    ws_bytes = mla.mla_decode_workspace_size(B, q_len, H, plan.max_splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    mla.mla_decode_workspace_init(ws, ws_bytes)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+    splits_d = torch.from_numpy(plan.splits).to(dev)
+    chunks_d = torch.from_numpy(plan.chunks).to(dev)
+    out = torch.empty((B, q_len, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
+    args_common = (inp.q, inp.kv, inp.num_pages, inp.page_table, inp.max_pages, lens_d, splits_d,
+                   chunks_d, plan.max_splits, plan.kv_split, B, q_len, H, w["causal"], 1.0, 1.0,
+                   SOFTMAX_SCALE, ws, ws_bytes, out, lse, None)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        mla.mla_decode(*args_common, stream)
+    torch.cuda.synchronize(dev)
+    mla.mla_decode_status(ws, stream)
+
+    # ---- timed region: K steps, events around each phase ----
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        mla.mla_decode_splitkv(*args_common, stream)
+        ev[k][1].record(stream)
+        mla.mla_decode_merge(*args_common, stream)
+        ev[k][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    split_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    merge_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    us_per_call = total_ms * 1e3 / K
+    if world > 1:
+        t = torch.tensor([us_per_call], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us_per_call = float(t.item())
+    mla.mla_decode_status(ws, stream)
+
+    # ---- end to end through the public API with host buffers ----
+    q_h = inp.q.cpu().pin_memory()
+    pt_h = inp.page_table.cpu().pin_memory()
+    meta_h = torch.tensor(np.stack([np.asarray(lens, np.int32), plan.splits, plan.chunks]),
+                          dtype=torch.int32).pin_memory()
+    meta_d = torch.empty_like(meta_h, device=dev)
+    q_d = torch.empty_like(inp.q)
+    pt_d = torch.empty_like(inp.page_table)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_args = list(args_common)
+    e2e_args[0], e2e_args[3] = q_d, pt_d
+    e2e_args[5], e2e_args[6], e2e_args[7] = meta_d[0], meta_d[1], meta_d[2]
+    h2d = q_h.numel() + pt_h.numel() * 4 + meta_h.numel() * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    def e2e_step():
+        p = mla.mla_decode_plan(lens, H, q_len, sm_count=sm_count) if args.plan == "gb300" else plan
+        del p
+        q_d.copy_(q_h, non_blocking=True)
+        pt_d.copy_(pt_h, non_blocking=True)
+        meta_d.copy_(meta_h, non_blocking=True)
+        mla.mla_decode(*e2e_args, stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_us = (time.perf_counter() - t0) * 1e6 / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_us], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_us = float(t.item())
+
+    # ---- roofline of the dominant kernel (split-KV) ----
+    kv_bytes = inp.kv_bytes()
+    split_avg_s = statistics.mean(split_ms) / 1e3
+    achieved = kv_bytes / split_avg_s / 1e9
+    peaks = measured_peaks()
+    traffic = recorded_traffic(args.workload)
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_rows > 0:
+        t, done, threads = cpu_oracle_sample(inp, w, args.cpu_rows, SOFTMAX_SCALE)
+        cpu = {"value": t / done * inp.rows * 1e6, "unit": UNIT, "cores": threads,
+               "kind": "oracle",
+               "sample": f"{done} of {inp.rows} rows (requests 0-1, all heads, full KV length), "
+                         f"time scaled by rows"}
+
+    if rank == 0:
+        pub = PUBLISHED_US.get(args.workload)
+        line = {
+            "metric": METRIC, "value": us_per_call, "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": us_per_call / 1e3,
+            "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": (us_per_call / pub) if pub else None,
+            "dtype": "e4m3", "data": "synthetic (seeded N(0,0.5^2) cast to E4M3, random pages)",
+            "config": {"workload": args.workload, "batch": B, "num_heads": H, "q_len": q_len,
+                       "kv_len": lens[0], "causal": w["causal"], "plan": args.plan,
+                       "splits": plan.splits.tolist()[:4] + (["..."] if B > 4 else []),
+                       "kv_split": plan.kv_split, "kv_bytes": kv_bytes,
+                       "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single"},
+            "kv_gbs": kv_bytes / (us_per_call * 1e-6) / 1e9,
+            "aggregate_kv_gbs": world * kv_bytes / (us_per_call * 1e-6) / 1e9,
+            "split_kernel_us": statistics.mean(split_ms) * 1e3,
+            "merge_kernel_us": statistics.mean(merge_ms) * 1e3,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": traffic, "peak_source": peaks["source"],
+                         "kernel": "mla_split_kv_kernel"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * mla_decode.h — C ABI of libmla_decode.so: paged FP8 multi-head latent
+ * attention (MLA) decode with split-KV partials and an online-softmax merge,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The problem (TensorRT-LLM issue #20510, "CuTe DSL FP8 MLA decode
+ * regression", sections "Setup" and "Repro 1/2"): each query row (head h of
+ * query token qi of request b) attends over the request's paged KV cache.
+ * A KV row is 576 E4M3 values: 512 latent + 64 rope.  K is the whole row, V is
+ * its first 512 values.  Pages hold 32 tokens.  Q is E4M3; the output is BF16
+ * with an optional fp32 log-sum-exp ("softmax stats").  The KV range of each
+ * request is split across CTAs (split_kv); each split writes (max, sum, O)
+ * partials that a merge kernel combines (TensorRT-LLM PR #20380, "split the
+ * KV partials of a row across thread groups in fmhaReductionKernel",
+ * "Description").
+ *
+ * Definition computed (all scales multiply the dequantised values):
+ *   q   = q_scale * Q[b, qi, h, 0:576],  k_j = kv_scale * KV(token j),
+ *   v_j = k_j[0:512],  s_j = softmax_scale * (q . k_j),
+ *   visible keys j < n with n = L_b (or L_b - q_len + qi + 1 when causal:
+ *   the MTP-verify block, query token i sees keys [0, L - q_len + i]),
+ *   O = sum_j softmax(s)_j v_j  (BF16, round to nearest even),
+ *   LSE = ln sum_j exp(s_j)     (natural log, fp32).
+ *
+ * Conventions for every function:
+ *   - Return value is an mla_status_t.  Nothing throws, exits or aborts.
+ *     On a non-OK return, mla_last_error() gives a message (thread-local).
+ *   - Device pointers are plain CUDA device addresses; host pointers are
+ *     marked "host".  The caller owns every buffer (including the workspace)
+ *     and keeps it alive until the stream has passed the call.
+ *   - The library never allocates device memory.  mla_decode and mla_merge
+ *     enqueue work on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and return without synchronising, so they can be captured in a CUDA
+ *     graph.
+ *   - Conditions only the device can see (a page id outside [0, num_pages),
+ *     inconsistent kv_lens/splits/chunks, a wait that ran out) are written to
+ *     a status word at the head of the workspace; mla_decode_status() reads
+ *     it.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,
+  MLA_ERR_UNSUPPORTED = 2,
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3,
+  MLA_ERR_CUDA = 4,
+  MLA_ERR_TIMEOUT = 5
+} mla_status_t;
+
+#define MLA_HEAD_DIM 576
+#define MLA_LATENT_DIM 512
+#define MLA_ROPE_DIM 64
+#define MLA_PAGE_SIZE 32
+#define MLA_TILE_TOKENS 128 /* split chunks are multiples of this */
+#define MLA_MAX_SPLITS 128  /* per-request split cap (issue #20510, "Repro 2") */
+#define MLA_MAX_ROWS 1024   /* num_heads * q_len */
+
+/*
+ * Split planner (host only; issue #20510, "Repro 2": per-request plan
+ * `block_split_kvs` with the split cap raised to 128, and the follow-up
+ * comment on skewed batches and the minimum tiles per split).
+ *
+ * kv_lens      host int32[batch], each >= q_len >= 1.
+ * num_heads    heads per request (H); num_heads * q_len <= MLA_MAX_ROWS.
+ * sm_count     SMs of the target GPU (used when target_ctas <= 0).
+ * target_ctas  > 0: reproduce the pages' planner: t = max(1, target/B')
+ *              splits per request, chunk = roundup128(ceil(L/t)), where B'
+ *              is batch times the number of row groups a request needs.
+ *              <= 0: GB300 planner: one common chunk for the whole batch,
+ *              chosen to balance whole waves of one CTA per SM.
+ * Outputs (host): splits_out[batch] (1..MLA_MAX_SPLITS), chunk_out[batch]
+ *              (tokens per split, a multiple of 128, splits*chunk >= L),
+ *              *kv_split_out (merge thread groups: 1, 2, 4, 8 or 16) and
+ *              *workspace_bytes_out for mla_decode with max(splits).
+ */
+MLA_API int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t num_heads, int32_t q_len,
+                    int32_t sm_count, int32_t target_ctas, int32_t* splits_out,
+                    int32_t* chunk_out, int32_t* kv_split_out, size_t* workspace_bytes_out);
+
+/* Workspace bytes mla_decode needs: a 256-byte status header, then per
+ * (row, split) an fp32 pair (m, l) and an fp32 O[512]. */
+MLA_API size_t mla_decode_workspace_size(int32_t batch, int32_t q_len, int32_t num_heads,
+                                 int32_t max_splits);
+
+/*
+ * Decode: split-KV kernel, then (if any request has more than one split) the
+ * merge.  Row r = (b*q_len + qi)*num_heads + h.
+ *
+ * q_fp8          E4M3 [batch, q_len, num_heads, 576], contiguous, 16-byte aligned.
+ * kv_pages_fp8   E4M3 [num_pages, 32, 576], contiguous, 16-byte aligned.
+ * page_table     int32 [batch, max_pages_per_req]; entry i of request b is the
+ *                page holding tokens [32i, 32i+32).  Only entries below
+ *                ceil(kv_lens[b]/32) are read.
+ * kv_lens, splits, chunks   int32 [batch] on the device, as planned by
+ *                mla_decode_plan (splits[b] <= max_splits).
+ * kv_split       merge thread groups (1, 2, 4, 8, 16).
+ * causal         nonzero: MTP-verify mask inside the q_len block.
+ * workspace      device buffer of >= mla_decode_workspace_size(...) bytes,
+ *                256-byte aligned, its status header zeroed once by
+ *                mla_decode_workspace_init.
+ * out_bf16       BF16 [batch, q_len, num_heads, 512].
+ * lse_f32        fp32 [batch, q_len, num_heads] or NULL.
+ * out_f32_debug  fp32 [batch, q_len, num_heads, 512] or NULL: the output
+ *                before the BF16 store (for tests).
+ * Errors: MLA_ERR_INVALID_ARG (null or misaligned pointer, bad sizes),
+ * MLA_ERR_WORKSPACE_TOO_SMALL, MLA_ERR_CUDA (launch failure).
+ */
+MLA_API int mla_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+               const int32_t* page_table, int32_t max_pages_per_req, const int32_t* kv_lens,
+               const int32_t* splits, const int32_t* chunks, int32_t max_splits,
+               int32_t kv_split, int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
+               float q_scale, float kv_scale, float softmax_scale, void* workspace,
+               size_t workspace_bytes, void* out_bf16, float* lse_f32, float* out_f32_debug,
+               void* stream);
+
+/*
+ * The two phases of mla_decode, for callers that schedule them separately
+ * (to overlap other work, or to time the kernels one by one).  Same arguments
+ * and checks as mla_decode.  mla_decode_splitkv launches the split-KV kernel:
+ * requests with one split get their final output, the others get partials in
+ * the workspace.  mla_decode_merge then launches the merge of those partials
+ * (nothing when max_splits == 1).  mla_decode == splitkv followed by merge on
+ * the same stream.
+ */
+MLA_API int mla_decode_splitkv(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                               const int32_t* page_table, int32_t max_pages_per_req,
+                               const int32_t* kv_lens, const int32_t* splits,
+                               const int32_t* chunks, int32_t max_splits, int32_t kv_split,
+                               int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
+                               float q_scale, float kv_scale, float softmax_scale,
+                               void* workspace, size_t workspace_bytes, void* out_bf16,
+                               float* lse_f32, float* out_f32_debug, void* stream);
+MLA_API int mla_decode_merge(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                             const int32_t* page_table, int32_t max_pages_per_req,
+                             const int32_t* kv_lens, const int32_t* splits,
+                             const int32_t* chunks, int32_t max_splits, int32_t kv_split,
+                             int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
+                             float q_scale, float kv_scale, float softmax_scale,
+                             void* workspace, size_t workspace_bytes, void* out_bf16,
+                             float* lse_f32, float* out_f32_debug, void* stream);
+
+/* Zero the 256-byte status header of a new workspace (async on `stream`).
+ * Call once per workspace before its first mla_decode; after that the
+ * header only changes when the device reports a condition, and
+ * mla_decode_status clears it again after reading.  The partial area needs
+ * no initialisation. */
+MLA_API int mla_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Merge alone (PR #20380, "Description": KvSplit thread groups, a shared-memory
+ * combine rescaled by exp2(group max - max), empty groups skipped, padded loads
+ * with weight 0).
+ *
+ * partial_o   fp32 [rows, num_ctas_kv, 512]: un-normalised outputs.
+ * partial_ml  fp32 [rows, num_ctas_kv, 2]: (m in log2 units, l).  A slot with
+ *             l == 0 (conventionally m = -inf) is empty and is skipped.
+ * Result per row: M = max m_s, w_s = 2^(m_s - M),
+ *   O = sum w_s O_s / sum w_s l_s (BF16 and optionally fp32),
+ *   LSE = ln2 * (M + log2 sum w_s l_s).  A row with no non-empty slot gives
+ *   O = 0 and LSE = -inf.
+ */
+MLA_API int mla_merge(const float* partial_o, const float* partial_ml, int32_t rows, int32_t num_ctas_kv,
+              int32_t kv_split, void* out_bf16, float* lse_f32, float* out_f32_debug,
+              void* stream);
+
+/* Synchronously reads the status word at the head of `workspace` (MLA_OK,
+ * MLA_ERR_INVALID_ARG for a bad page id or inconsistent plan arrays,
+ * MLA_ERR_TIMEOUT for a wait that ran out) after `stream` has drained, and
+ * clears it. */
+MLA_API int mla_decode_status(void* workspace, void* stream);
+
+/* Message for the last non-OK status returned on this thread. */
+MLA_API const char* mla_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DECODE_H_ */

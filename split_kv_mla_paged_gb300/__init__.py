@@ -1,0 +1,263 @@
+"""Paged FP8 MLA split-KV decode for GB300 (sm_103a).
+
+A thin ctypes binding over libmla_decode.so (declared in include/mla_decode.h).
+The functions keep the C names and only marshal arguments: every step of the
+decode runs in the library's CUDA kernels.  PyTorch supplies device memory and
+streams.  There is no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+from . import build as _build
+
+__all__ = [
+    "MLA_OK", "MLA_ERR_INVALID_ARG", "MLA_ERR_UNSUPPORTED", "MLA_ERR_WORKSPACE_TOO_SMALL",
+    "MLA_ERR_CUDA", "MLA_ERR_TIMEOUT", "MlaError", "Plan", "load_library", "library_path",
+    "mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init", "mla_decode",
+    "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
+    "decode", "merge", "EXPORTED_SYMBOLS",
+]
+
+MLA_OK = 0
+MLA_ERR_INVALID_ARG = 1
+MLA_ERR_UNSUPPORTED = 2
+MLA_ERR_WORKSPACE_TOO_SMALL = 3
+MLA_ERR_CUDA = 4
+MLA_ERR_TIMEOUT = 5
+_STATUS_NAMES = {
+    0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
+    3: "MLA_ERR_WORKSPACE_TOO_SMALL", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT",
+}
+EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init",
+                    "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
+                    "mla_decode_status", "mla_last_error")
+
+HEAD_DIM = 576
+LATENT_DIM = 512
+PAGE_SIZE = 32
+TILE_TOKENS = 128
+MAX_SPLITS = 128
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libmla_decode.so (built by `build.build()`); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with split_kv_mla_paged_gb300.build.build() "
+                "(there is no fallback implementation)")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                 ctypes.c_size_t)
+        lib.mla_decode_plan.restype = ctypes.c_int
+        lib.mla_decode_plan.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
+        lib.mla_decode_workspace_size.restype = sz
+        lib.mla_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+        dec_args = [vp, vp, i64, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, f32,
+                    vp, sz, vp, vp, vp, vp]
+        for name in ("mla_decode", "mla_decode_splitkv", "mla_decode_merge"):
+            getattr(lib, name).restype = ctypes.c_int
+            getattr(lib, name).argtypes = dec_args
+        lib.mla_decode_workspace_init.restype = ctypes.c_int
+        lib.mla_decode_workspace_init.argtypes = [vp, sz, vp]
+        lib.mla_merge.restype = ctypes.c_int
+        lib.mla_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
+        lib.mla_decode_status.restype = ctypes.c_int
+        lib.mla_decode_status.argtypes = [vp, vp]
+        lib.mla_last_error.restype = ctypes.c_char_p
+        lib.mla_last_error.argtypes = []
+        _lib = lib
+        return lib
+
+
+def mla_last_error() -> str:
+    return load_library().mla_last_error().decode("utf-8", "replace")
+
+
+def _check(status: int) -> None:
+    if status != MLA_OK:
+        raise MlaError(status, mla_last_error())
+
+
+def _ptr(t) -> Optional[int]:
+    """Address of a torch tensor / numpy array, or None."""
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+@dataclasses.dataclass
+class Plan:
+    splits: np.ndarray   # int32 [B]
+    chunks: np.ndarray   # int32 [B]
+    kv_split: int
+    workspace_bytes: int
+
+    @property
+    def max_splits(self) -> int:
+        return int(self.splits.max())
+
+
+def mla_decode_plan(kv_lens: Sequence[int], num_heads: int, q_len: int, sm_count: int = 0,
+                    target_ctas: int = 0) -> Plan:
+    lib = load_library()
+    lens = np.ascontiguousarray(np.asarray(kv_lens, dtype=np.int32))
+    b = int(lens.shape[0])
+    splits = np.zeros(b, dtype=np.int32)
+    chunks = np.zeros(b, dtype=np.int32)
+    kvs = ctypes.c_int32(0)
+    ws = ctypes.c_size_t(0)
+    _check(lib.mla_decode_plan(lens.ctypes.data, b, int(num_heads), int(q_len), int(sm_count),
+                               int(target_ctas), splits.ctypes.data, chunks.ctypes.data,
+                               ctypes.addressof(kvs), ctypes.addressof(ws)))
+    return Plan(splits=splits, chunks=chunks, kv_split=int(kvs.value), workspace_bytes=int(ws.value))
+
+
+def mla_decode_workspace_size(batch: int, q_len: int, num_heads: int, max_splits: int) -> int:
+    return int(load_library().mla_decode_workspace_size(batch, q_len, num_heads, max_splits))
+
+
+def mla_decode(q_fp8, kv_pages_fp8, num_pages: int, page_table, max_pages_per_req: int,
+               kv_lens, splits, chunks, max_splits: int, kv_split: int, batch: int, q_len: int,
+               num_heads: int, causal: bool, q_scale: float, kv_scale: float,
+               softmax_scale: float, workspace, workspace_bytes: int, out_bf16, lse_f32=None,
+               out_f32_debug=None, stream=None) -> None:
+    """Enqueue one decode (split-KV kernel + merge) on `stream`; see mla_decode.h."""
+    _decode_call("mla_decode", q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req,
+                 kv_lens, splits, chunks, max_splits, kv_split, batch, q_len, num_heads, causal,
+                 q_scale, kv_scale, softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32,
+                 out_f32_debug, stream)
+
+
+def _decode_call(fn_name, q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req, kv_lens,
+                 splits, chunks, max_splits, kv_split, batch, q_len, num_heads, causal, q_scale,
+                 kv_scale, softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32,
+                 out_f32_debug, stream):
+    fn = getattr(load_library(), fn_name)
+    _check(fn(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages), _ptr(page_table),
+              int(max_pages_per_req), _ptr(kv_lens), _ptr(splits), _ptr(chunks), int(max_splits),
+              int(kv_split), int(batch), int(q_len), int(num_heads), 1 if causal else 0,
+              float(q_scale), float(kv_scale), float(softmax_scale), _ptr(workspace),
+              int(workspace_bytes), _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
+              _stream_handle(stream)))
+
+
+def mla_decode_splitkv(*args, **kw) -> None:
+    """Split-KV phase of mla_decode (same arguments)."""
+    _decode_call("mla_decode_splitkv", *args, **kw)
+
+
+def mla_decode_merge(*args, **kw) -> None:
+    """Merge phase of mla_decode (same arguments)."""
+    _decode_call("mla_decode_merge", *args, **kw)
+
+
+def mla_decode_workspace_init(workspace, workspace_bytes: int, stream=None) -> None:
+    _check(load_library().mla_decode_workspace_init(_ptr(workspace), int(workspace_bytes),
+                                                    _stream_handle(stream)))
+
+
+def mla_merge(partial_o, partial_ml, rows: int, num_ctas_kv: int, kv_split: int, out_bf16,
+              lse_f32=None, out_f32_debug=None, stream=None) -> None:
+    lib = load_library()
+    _check(lib.mla_merge(_ptr(partial_o), _ptr(partial_ml), int(rows), int(num_ctas_kv),
+                         int(kv_split), _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
+                         _stream_handle(stream)))
+
+
+def mla_decode_status(workspace, stream=None) -> int:
+    """Read and clear the device status word; raises MlaError on a non-OK status."""
+    lib = load_library()
+    st = lib.mla_decode_status(_ptr(workspace), _stream_handle(stream))
+    _check(st)
+    return st
+
+
+# ---------------------------------------------------------------------------
+# Convenience wrappers over torch tensors (allocation on the caller's side).
+# ---------------------------------------------------------------------------
+
+def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: int,
+           causal: bool, softmax_scale: float, q_scale: float = 1.0, kv_scale: float = 1.0,
+           plan: Optional[Plan] = None, sm_count: Optional[int] = None, target_ctas: int = 0,
+           kv_split: Optional[int] = None, want_f32: bool = False, stream=None,
+           check_status: bool = True):
+    """Plan, allocate outputs and a workspace with torch, and run mla_decode.
+
+    q_fp8 uint8 [B, q, H, 576] and kv_pages_fp8 uint8 [P, 32, 576] (E4M3 codes)
+    and page_table int32 [B, max_pages] are CUDA tensors; kv_lens is a host
+    sequence.  Returns (out_bf16, lse, out_f32 or None).
+    """
+    import torch
+    dev = q_fp8.device
+    lens = np.asarray(kv_lens.cpu() if hasattr(kv_lens, "cpu") else kv_lens, dtype=np.int32)
+    batch = int(lens.shape[0])
+    if plan is None:
+        if sm_count is None:
+            sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+        plan = mla_decode_plan(lens, num_heads, q_len, sm_count=sm_count, target_ctas=target_ctas)
+    ks = plan.kv_split if kv_split is None else int(kv_split)
+    lens_d = torch.from_numpy(lens).to(dev)
+    splits_d = torch.from_numpy(plan.splits).to(dev)
+    chunks_d = torch.from_numpy(plan.chunks).to(dev)
+    ws_bytes = mla_decode_workspace_size(batch, q_len, num_heads, plan.max_splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    mla_decode_workspace_init(ws, ws_bytes, stream)
+    out = torch.empty((batch, q_len, num_heads, LATENT_DIM), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((batch, q_len, num_heads), dtype=torch.float32, device=dev)
+    out_f32 = (torch.empty((batch, q_len, num_heads, LATENT_DIM), dtype=torch.float32, device=dev)
+               if want_f32 else None)
+    mla_decode(q_fp8, kv_pages_fp8, kv_pages_fp8.shape[0], page_table, page_table.shape[1],
+               lens_d, splits_d, chunks_d, plan.max_splits, ks, batch, q_len, num_heads, causal,
+               q_scale, kv_scale, softmax_scale, ws, ws_bytes, out, lse, out_f32, stream)
+    if check_status:
+        mla_decode_status(ws, stream)
+    return out, lse, out_f32
+
+
+def merge(partial_o, partial_ml, kv_split: int, want_f32: bool = True, stream=None):
+    """Run mla_merge on CUDA tensors partial_o [rows, S, 512], partial_ml [rows, S, 2]."""
+    import torch
+    rows, s = int(partial_o.shape[0]), int(partial_o.shape[1])
+    out = torch.empty((rows, LATENT_DIM), dtype=torch.bfloat16, device=partial_o.device)
+    lse = torch.empty((rows,), dtype=torch.float32, device=partial_o.device)
+    out_f32 = (torch.empty((rows, LATENT_DIM), dtype=torch.float32, device=partial_o.device)
+               if want_f32 else None)
+    mla_merge(partial_o, partial_ml, rows, s, kv_split, out, lse, out_f32, stream)
+    return out, lse, out_f32

@@ -1,0 +1,1137 @@
+// Paged FP8 MLA decode for GB300 (sm_103a): split-KV kernel (TMA + tcgen05 +
+// TMEM) and the online-softmax merge kernel, plus their C-ABI launchers.
+//
+// Problem statement: TensorRT-LLM issue #20510 "CuTe DSL FP8 MLA decode
+// regression" (sections "Setup", "Repro 1", "Repro 2", "Analysis"): E4M3 Q
+// and paged E4M3 KV, 512 latent + 64 rope per row, page size 32, K = the whole
+// row, V = its first 512 values, BF16 output and fp32 softmax stats, the KV
+// range split across CTAs with per-split partials merged afterwards.  The merge
+// follows TensorRT-LLM PR #20380 ("Description"): KvSplit thread groups over
+// a row's partials, a shared-memory combine rescaled by exp2(group max - max),
+// empty groups skipped, weight-0 padded loads.
+//
+// Split-KV kernel design (one CTA per (split, request, row group), one CTA per
+// SM):
+//  * The MMA is "swapped": tokens are the M = 128 dimension and the query rows
+//    of a request (heads x query tokens, padded to a multiple of 16, at most
+//    96) are N.  S^T[128 tok x NR] = K[128 x 576] Q^T and
+//    O^T[512 x NR] += V^T[512 x 128 tok] P^T, as four M = 128 MMAs over the
+//    latent dims.  With H*q = 12 this does 16 columns of work instead of
+//    padding 12 rows to 128, and S^T plus O^T fit TMEM (NS*NR + 4*NR <= 512).
+//  * One TMA-staged copy of each KV tile (4 pages x 576 B x 32 tokens, 128 B
+//    swizzle for the latent blocks, 64 B for the rope block) serves as the K
+//    operand (K-major) and as the V operand (MN-major over the same bytes), so
+//    each KV byte is read from HBM once.
+//  * Online softmax in log2 units with integer reference maxima: per row the
+//    reference k is ceil(running max) and p = 2^(t - k + 8) is computed as
+//    ex2(t - rint(t)) * 2^(rint(t) - k + 8).  Every rescale is then an exact
+//    power of two, so the E4M3-quantised P fed to the PV MMA, and every
+//    partial, is the same for any split plan up to exact scaling.
+//  * Warp roles: warp 0 issues TMA, warp 1 issues tcgen05.mma (and owns TMEM),
+//    warps 2-5 (one warpgroup, TMEM lane quadrant = warp % 4) run the softmax,
+//    the rare O correction and the epilogue.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "mla_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+
+constexpr int kThreads = 192;
+constexpr int kStages = 2;
+constexpr int kTileTokens = 128;
+constexpr uint32_t kTileBytes = kTileTokens * MLA_HEAD_DIM;  // 73728
+constexpr uint32_t kLatBlockBytes = kTileTokens * 128;       // 16384: one 128-dim block
+constexpr uint32_t kRopeOffset = 4 * kLatBlockBytes;         // 65536
+constexpr uint32_t kPageLatBytes = MLA_PAGE_SIZE * 128;      // 4096
+constexpr uint32_t kPageRopeBytes = MLA_PAGE_SIZE * 64;      // 2048
+constexpr uint32_t kPageBytes = MLA_PAGE_SIZE * MLA_HEAD_DIM;
+constexpr long long kWaitLimitCycles = 4000000000LL;  // about 2 s at 2 GHz
+constexpr uint32_t kSoftmaxBarrier = 1;
+
+struct DecodeParams {
+  const int32_t* page_table;
+  const int32_t* kv_lens;
+  const int32_t* splits;
+  const int32_t* chunks;
+  int64_t num_pages;
+  int32_t max_pages;
+  int32_t max_splits;
+  int32_t q_len;
+  int32_t num_heads;
+  int32_t causal;
+  int32_t rows_per_req;    // R = q_len * num_heads
+  int32_t rows_per_group;  // RG
+  float c_log2;            // softmax_scale * q_scale * kv_scale * log2(e)
+  float kv_scale;
+  int* status;
+  float* ws_ml;
+  float* ws_o;
+  __nv_bfloat16* out;
+  float* lse;
+  float* out_f32;
+};
+
+template <int NR>
+struct Cfg {
+  static_assert(NR % 16 == 0 && NR >= 16 && NR <= kMaxRowsPerCta, "NR");
+  static constexpr int NS = (2 * NR + 4 * NR <= 512) ? 2 : 1;  // S^T buffers in TMEM
+  static constexpr uint32_t kTmemUsed = NS * NR + 4 * NR;
+  static constexpr uint32_t kTmemCols =
+      kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+      : kTmemUsed <= 256 ? 256 : 512;
+  static constexpr uint32_t kOCol = NS * NR;
+  // Shared memory, offsets from a 1024-byte aligned base.
+  static constexpr uint32_t kKV = 0;
+  static constexpr uint32_t kQ = kStages * kTileBytes;
+  static constexpr uint32_t kQBytes = NR * MLA_HEAD_DIM;
+  static constexpr uint32_t kP = kQ + kQBytes;
+  static constexpr uint32_t kPBytes = NR * kTileTokens;  // one P^T buffer
+  static constexpr uint32_t kAux = kP + 2 * kPBytes;
+  // aux: 16 mbarriers, tmem slot, flags, reductions
+  static constexpr uint32_t kBars = kAux;              // 16 x 8 B
+  static constexpr uint32_t kTmemSlot = kAux + 128;     // 4 B
+  static constexpr uint32_t kFlags = kAux + 144;        // 2 x 4 B
+  static constexpr uint32_t kRedMax = kAux + 160;       // 4 x NR floats
+  static constexpr uint32_t kRedSum = kRedMax + 16 * NR;
+  static constexpr uint32_t kKref = kRedSum + 16 * NR;  // NR floats
+  static constexpr uint32_t kAlpha = kKref + 4 * NR;    // NR floats
+  static constexpr uint32_t kEnd = kAlpha + 4 * NR;
+  static constexpr uint32_t kSmemBytes = kEnd + 1024;   // + alignment slack
+};
+
+// Barrier indices inside the aux block.
+enum : int {
+  BAR_FULL0 = 0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_QFULL, BAR_SFULL0, BAR_SFULL1,
+  BAR_SFREE0, BAR_SFREE1, BAR_PFULL0, BAR_PFULL1, BAR_PFREE0, BAR_PFREE1, BAR_ODONE,
+  BAR_FINAL, BAR_COUNT
+};
+
+__device__ __forceinline__ void report(int* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^i for an integer i in [-126, 127], exactly.
+__device__ __forceinline__ float pow2i(int i) { return __int_as_float((i + 127) << 23); }
+
+// 2^(t - k + 8) with exact power-of-two scaling (k integer-valued).
+__device__ __forceinline__ float softmax_weight(float t, float k) {
+  if (t == -INFINITY) return 0.0f;
+  const float a = rintf(t);
+  const float f = t - a;  // exact, |f| <= 0.5
+  const int sc = static_cast<int>(a) - static_cast<int>(k) + 8;
+  if (sc < -126) return 0.0f;
+  return ex2_approx(f) * pow2i(sc);
+}
+
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Warp reduce-scatter over N per-lane values (one per row): afterwards lane
+// `l` holds the warp-wide reduction of rows [base, base + final_n) in v[0..).
+// Halving steps exchange half of the values with the partner lane; once N is
+// odd the remaining lane bits are reduced in full.
+template <int N, int OFF>
+struct ReduceScatter {
+  static constexpr int kFinal = (OFF == 0) ? N
+                                : (N % 2 == 0) ? ReduceScatter<N / 2, OFF / 2>::kFinal
+                                               : ReduceScatter<N, OFF / 2>::kFinal;
+  template <bool MAX>
+  static __device__ __forceinline__ void run(float* v, int lane, int& base, bool& writer) {
+    if constexpr (OFF == 0) {
+      return;
+    } else if constexpr (N % 2 == 0) {
+      constexpr int H = N / 2;
+      const bool up = (lane & OFF) != 0;
+#pragma unroll
+      for (int k = 0; k < H; ++k) {
+        const float send = up ? v[k] : v[k + H];
+        const float keep = up ? v[k + H] : v[k];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, OFF);
+        v[k] = MAX ? fmaxf(keep, recv) : keep + recv;
+      }
+      if (up) base += H;
+      ReduceScatter<H, OFF / 2>::template run<MAX>(v, lane, base, writer);
+    } else {
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        const float recv = __shfl_xor_sync(0xffffffffu, v[k], OFF);
+        v[k] = MAX ? fmaxf(v[k], recv) : v[k] + recv;
+      }
+      if (lane & OFF) writer = false;
+      ReduceScatter<N, OFF / 2>::template run<MAX>(v, lane, base, writer);
+    }
+  }
+};
+template <int N>
+struct ReduceScatter<N, 0> {
+  static constexpr int kFinal = N;
+  template <bool MAX>
+  static __device__ __forceinline__ void run(float*, int, int&, bool&) {}
+};
+
+template <int NR, bool MAX>
+__device__ __forceinline__ void warp_reduce_rows(float* v, int lane, float* dst) {
+  int base = 0;
+  bool writer = true;
+  ReduceScatter<NR, 16>::template run<MAX>(v, lane, base, writer);
+  constexpr int F = ReduceScatter<NR, 16>::kFinal;
+  if (writer) {
+#pragma unroll
+    for (int k = 0; k < F; ++k) dst[base + k] = v[k];
+  }
+}
+
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_split_kv_kernel(const __grid_constant__ CUtensorMap tm_kv_lat,
+                        const __grid_constant__ CUtensorMap tm_kv_rope,
+                        const __grid_constant__ CUtensorMap tm_q_lat,
+                        const __grid_constant__ CUtensorMap tm_q_rope, const DecodeParams p) {
+  using C = Cfg<NR>;
+  const int split = blockIdx.x;
+  const int b = blockIdx.y;
+  const int grp = blockIdx.z;
+
+  // ---- plan checks (uniform over the CTA) -------------------------------
+  const int L = p.kv_lens[b];
+  const int nsplit = p.splits[b];
+  const int chunk = p.chunks[b];
+  if (split >= nsplit) return;  // empty split slot of a shorter request
+  {
+    const bool bad = L < 1 || (p.causal && L < p.q_len) || nsplit > p.max_splits ||
+                     chunk < kTileTokens || (chunk % kTileTokens) != 0 ||
+                     static_cast<int64_t>(nsplit) * chunk < L ||
+                     static_cast<int64_t>(nsplit - 1) * chunk >= L ||
+                     static_cast<int64_t>(L) > static_cast<int64_t>(p.max_pages) * MLA_PAGE_SIZE;
+    if (bad) {
+      if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
+      return;
+    }
+  }
+  const int tok_begin = split * chunk;
+  const int tok_end = min(L, tok_begin + chunk);
+  const int n_tiles = (tok_end - tok_begin + kTileTokens - 1) / kTileTokens;
+  const int row0 = grp * p.rows_per_group;                       // first row of this group
+  const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(base);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBars + 8u * i; };
+  volatile int* flags = reinterpret_cast<volatile int*>(base + C::kFlags);
+  volatile int* abort_flag = flags + 2;
+  float* red_max = reinterpret_cast<float*>(base + C::kRedMax);
+  float* red_sum = reinterpret_cast<float*>(base + C::kRedSum);
+  float* kref = reinterpret_cast<float*>(base + C::kKref);
+  float* alpha_s = reinterpret_cast<float*>(base + C::kAlpha);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(BAR_FULL0), 1);
+    mbar_init(bar(BAR_FULL1), 1);
+    mbar_init(bar(BAR_EMPTY0), 1);
+    mbar_init(bar(BAR_EMPTY1), 1);
+    mbar_init(bar(BAR_QFULL), 1);
+    mbar_init(bar(BAR_SFULL0), 1);
+    mbar_init(bar(BAR_SFULL1), 1);
+    mbar_init(bar(BAR_SFREE0), 128);
+    mbar_init(bar(BAR_SFREE1), 128);
+    mbar_init(bar(BAR_PFULL0), 128);
+    mbar_init(bar(BAR_PFULL1), 128);
+    mbar_init(bar(BAR_PFREE0), 1);
+    mbar_init(bar(BAR_PFREE1), 1);
+    mbar_init(bar(BAR_ODONE), 1);
+    mbar_init(bar(BAR_FINAL), 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + C::kTmemSlot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + C::kTmemSlot);
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_kv_lat);
+      tma_prefetch_desc(&tm_kv_rope);
+      tma_prefetch_desc(&tm_q_lat);
+      tma_prefetch_desc(&tm_q_rope);
+      const int qrow = b * p.rows_per_req + row0;
+      mbar_arrive_expect_tx(bar(BAR_QFULL), C::kQBytes);
+#pragma unroll
+      for (int d = 0; d < 4; ++d)
+        tma_load_2d(sbase + C::kQ + d * NR * 128, &tm_q_lat, d * 128, qrow, bar(BAR_QFULL));
+      tma_load_2d(sbase + C::kQ + 4 * NR * 128, &tm_q_rope, MLA_LATENT_DIM, qrow, bar(BAR_QFULL));
+    }
+    const uint64_t pol = l2_policy_evict_first();
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+    const int page0 = tok_begin / MLA_PAGE_SIZE;
+    const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
+    int window = 0;
+    int issued = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      if ((i & 7) == 0) {
+        const int pi = page0 + i * 4 + lane;
+        int pg = 0;
+        if (pi < page_end) {
+          pg = pt[pi];
+          if (pg < 0 || pg >= p.num_pages) {
+            report(p.status, MLA_ERR_INVALID_ARG);
+            pg = 0;
+          }
+        }
+        window = pg;
+      }
+      const int st = i & 1;
+      bool ok = true;
+      if (i >= kStages) ok = mbar_wait(bar(BAR_EMPTY0 + st), ((i >> 1) - 1) & 1, kWaitLimitCycles);
+      ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+      if (!ok) {
+        if (lane == 0) {
+          report(p.status, MLA_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      int pages[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) pages[q] = __shfl_sync(0xffffffffu, window, (i & 7) * 4 + q);
+      if (lane == 0) {
+        const int tp0 = page0 + i * 4;
+        int nvalid = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) nvalid += (tp0 + q < page_end) ? 1 : 0;
+        const uint32_t fb = bar(BAR_FULL0 + st);
+        mbar_arrive_expect_tx(fb, nvalid * kPageBytes);
+        const uint32_t kv = sbase + C::kKV + st * kTileBytes;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (tp0 + q < page_end) {
+            const int row = pages[q] * MLA_PAGE_SIZE;
+#pragma unroll
+            for (int d = 0; d < 4; ++d)
+              tma_load_2d_hint(kv + d * kLatBlockBytes + q * kPageLatBytes, &tm_kv_lat, d * 128,
+                               row, fb, pol);
+            tma_load_2d_hint(kv + kRopeOffset + q * kPageRopeBytes, &tm_kv_rope, MLA_LATENT_DIM,
+                             row, fb, pol);
+          }
+        }
+      }
+      __syncwarp();
+      issued = i + 1;
+    }
+    // Before the CTA can exit, the copies this warp issued must have landed
+    // (they have, unless a wait elsewhere ran out).  The full barrier of a
+    // stage is at most one phase behind the producer, so these waits are exact.
+    if (lane == 0) {
+      for (int k = max(0, issued - kStages); k < issued; ++k)
+        mbar_wait(bar(BAR_FULL0 + (k & 1)), (k >> 1) & 1, kWaitLimitCycles);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    constexpr uint32_t kIdQK = idesc_e4m3(128, NR, 0, 0);
+    constexpr uint32_t kIdPV = idesc_e4m3(128, NR, 1, 1);
+    bool ok = mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
+    auto fail = [&]() {
+      if (lane == 0) {
+        report(p.status, MLA_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    };
+    auto issue_pv = [&](int j) -> bool {
+      const int pb = j & 1;
+      bool w = mbar_wait(bar(BAR_PFULL0 + pb), (j >> 1) & 1, kWaitLimitCycles);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) return false;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t kv = sbase + C::kKV + (j & 1) * kTileBytes;
+        const uint32_t pbuf = sbase + C::kP + pb * C::kPBytes;
+#pragma unroll
+        for (int d = 0; d < 4; ++d) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t a = smem_desc(kv + d * kLatBlockBytes + ks * 4096, 16384, 1024,
+                                         kLayoutSW128);
+            const uint64_t bd = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
+            umma_f8(tmem + C::kOCol + d * NR, a, bd, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(bar(BAR_EMPTY0 + (j & 1)));
+        umma_commit(bar(BAR_PFREE0 + pb));
+        umma_commit(bar(BAR_ODONE));
+      }
+      __syncwarp();
+      return true;
+    };
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) fail();
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const int st = i & 1;
+      bool w = mbar_wait(bar(BAR_FULL0 + st), (i >> 1) & 1, kWaitLimitCycles);
+      const int sb = (C::NS == 2) ? (i & 1) : 0;
+      const int use = (C::NS == 2) ? (i >> 1) : i;
+      if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1, kWaitLimitCycles);
+      w = __all_sync(0xffffffffu, w && !*abort_flag);
+      if (!w) {
+        fail();
+        ok = false;
+        break;
+      }
+      const int tile_tok0 = tok_begin + i * kTileTokens;
+      const int valid = tok_end - tile_tok0;  // tokens of this tile inside the split
+      const uint32_t kv = sbase + C::kKV + st * kTileBytes;
+      if (valid < kTileTokens) {
+        // Rows past the split's end: pages that were not loaded, or the tail
+        // of a request's last page.  Zero them so V holds no stale or NaN
+        // bytes (0 * NaN would poison the PV sum).
+        const int nrow = kTileTokens - valid;
+        uint8_t* kvp = base + C::kKV + st * kTileBytes;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int idx = lane; idx < nrow * 36; idx += 32) {
+          const int r = valid + idx / 36;
+          const int c = idx % 36;
+          uint4* dst;
+          if (c < 32)
+            dst = reinterpret_cast<uint4*>(kvp + (c / 8) * kLatBlockBytes + r * 128 + (c % 8) * 16);
+          else
+            dst = reinterpret_cast<uint4*>(kvp + kRopeOffset + r * 64 + (c - 32) * 16);
+          *dst = z;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 18; ++kk) {
+          uint64_t a, bd;
+          if (kk < 16) {
+            const int d = kk >> 2, sub = kk & 3;
+            a = smem_desc(kv + d * kLatBlockBytes + sub * 32, 16, 1024, kLayoutSW128);
+            bd = smem_desc(sbase + C::kQ + d * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
+          } else {
+            const int sub = kk - 16;
+            a = smem_desc(kv + kRopeOffset + sub * 32, 16, 512, kLayoutSW64);
+            bd = smem_desc(sbase + C::kQ + 4 * NR * 128 + sub * 32, 16, 512, kLayoutSW64);
+          }
+          umma_f8(tmem + sb * NR, a, bd, kIdQK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(BAR_SFULL0 + sb));
+      }
+      __syncwarp();
+      if (i > 0) {
+        if (!issue_pv(i - 1)) {
+          fail();
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (ok && n_tiles > 0) {
+      if (!issue_pv(n_tiles - 1)) fail();
+    }
+    // One commit after everything this warp issued: the epilogue reads O^T
+    // after it, and TMEM is released only after it.
+    if (lane == 0) umma_commit(bar(BAR_FINAL));
+    __syncwarp();
+    mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
+  } else {
+    // ================= softmax warpgroup (warps 2-5) =================
+    // Every warp of the group passes the same sequence of named barriers
+    // whether or not a wait ran out (a failed wait only turns `ok` off and
+    // skips the work), so a timeout can never leave the group split across
+    // barriers.
+    const int quad = warp & 3;
+    const int tok_lane = quad * 32 + lane;  // TMEM lane == token index within the tile
+    const int sid = threadIdx.x - 64;       // 0..127, owner of row `sid` when < NR
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    float k_row = -INFINITY;  // owner state: reference max (integer, log2 units)
+    float l_row = 0.0f;       // owner state: sum of weights relative to k_row - 8
+    const float c = p.c_log2;
+    // Smallest visibility limit over this group's rows (MTP verify: the first
+    // query token of the block sees the fewest keys).
+    const int qi_first = row0 / p.num_heads;
+    const int lim_min = p.causal ? min(tok_end, L - p.q_len + qi_first + 1) : tok_end;
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int sb = (C::NS == 2) ? (i & 1) : 0;
+      const int use = (C::NS == 2) ? (i >> 1) : i;
+      if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, kWaitLimitCycles);
+      ok = __all_sync(0xffffffffu, ok);
+      float t[NR];
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[NR];
+#pragma unroll
+        for (int cc = 0; cc < NR / 16; ++cc)
+          tmem_ld16(tmem + lane_addr + sb * NR + cc * 16,
+                    *reinterpret_cast<uint32_t(*)[16]>(&r[cc * 16]));
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < NR; ++k) t[k] = __uint_as_float(r[k]);
+        tc_fence_before();
+        mbar_arrive(bar(BAR_SFREE0 + sb));
+      } else {
+#pragma unroll
+        for (int k = 0; k < NR; ++k) t[k] = 0.0f;
+      }
+      const int tile_tok0 = tok_begin + i * kTileTokens;
+      const int j = tile_tok0 + tok_lane;
+      // Scale and mask: rows past rows_here, tokens past the split, and (MTP
+      // verify) tokens after the row's query position are -inf.
+      if (tile_tok0 + kTileTokens <= lim_min) {
+#pragma unroll
+        for (int k = 0; k < NR; ++k) t[k] = (k < rows_here) ? t[k] * c : -INFINITY;
+      } else {
+        int qi = qi_first;
+        int h = row0 - qi_first * p.num_heads;
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+          const int lim = p.causal ? min(tok_end, L - p.q_len + qi + 1) : tok_end;
+          t[k] = (k < rows_here && j < lim) ? t[k] * c : -INFINITY;
+          if (++h == p.num_heads) {
+            h = 0;
+            ++qi;
+          }
+        }
+      }
+      {
+        float tm[NR];
+#pragma unroll
+        for (int k = 0; k < NR; ++k) tm[k] = t[k];
+        warp_reduce_rows<NR, true>(tm, lane, red_max + quad * NR);
+      }
+      named_bar_sync(kSoftmaxBarrier, 128);  // B1: tile maxima (and last tile's sums) ready
+      if (sid == 0) flags[(i + 1) & 1] = 0;
+      if (sid < NR) {
+        if (i > 0)
+          l_row += (red_sum[sid] + red_sum[NR + sid]) + (red_sum[2 * NR + sid] + red_sum[3 * NR + sid]);
+        const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
+                               fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
+        float k_new = k_row;
+        if (mt > k_row) k_new = ceilf(mt);
+        float alpha = 1.0f;
+        if (k_new != k_row && k_row != -INFINITY) {
+          const int e = static_cast<int>(k_row - k_new);
+          alpha = (e < -126) ? 0.0f : pow2i(e);
+          flags[i & 1] = 1;
+        }
+        l_row *= alpha;
+        k_row = k_new;
+        kref[sid] = k_new;
+        alpha_s[sid] = alpha;
+      }
+      named_bar_sync(kSoftmaxBarrier, 128);  // B2: references ready
+      const bool corr = flags[i & 1] != 0;
+      if (ok && corr && i > 0) {
+        // Rescale the O^T columns of rows whose reference moved (rare).
+        // o_done is at most one phase behind here: s_full(i) implies PV(i-2)
+        // completed, and PV(i) is not issued before this tile's p_full.
+        ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, kWaitLimitCycles);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int d = 0; d < 4; ++d) {
+#pragma unroll
+            for (int cc = 0; cc < NR / 16; ++cc) {
+              uint32_t r[16];
+              const uint32_t addr = tmem + lane_addr + C::kOCol + d * NR + cc * 16;
+              tmem_ld16(addr, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[cc * 16 + k]);
+              tmem_st16(addr, r);
+            }
+          }
+          tmem_st_wait();
+        }
+      }
+      // Weights 2^(t - k + 8), exact power-of-two scaling.
+#pragma unroll
+      for (int k = 0; k < NR; ++k) t[k] = softmax_weight(t[k], kref[k]);
+      // P^T (E4M3) into shared memory, MN-major: [NR/16][128 tokens][16 rows].
+      const int pb = i & 1;
+      if (ok && i >= 2) {
+        ok = mbar_wait(bar(BAR_PFREE0 + pb), ((i >> 1) - 1) & 1, kWaitLimitCycles);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        uint8_t* pbuf = base + C::kP + pb * C::kPBytes;
+#pragma unroll
+        for (int g = 0; g < NR / 16; ++g) {
+          uint4 v;
+          v.x = pack_e4m3x4(t[g * 16 + 0], t[g * 16 + 1], t[g * 16 + 2], t[g * 16 + 3]);
+          v.y = pack_e4m3x4(t[g * 16 + 4], t[g * 16 + 5], t[g * 16 + 6], t[g * 16 + 7]);
+          v.z = pack_e4m3x4(t[g * 16 + 8], t[g * 16 + 9], t[g * 16 + 10], t[g * 16 + 11]);
+          v.w = pack_e4m3x4(t[g * 16 + 12], t[g * 16 + 13], t[g * 16 + 14], t[g * 16 + 15]);
+          *reinterpret_cast<uint4*>(pbuf + g * 2048 + tok_lane * 16) = v;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(BAR_PFULL0 + pb));
+      }
+      // Row sums of the unquantised weights, folded in at the next B1.
+      warp_reduce_rows<NR, false>(t, lane, red_sum + quad * NR);
+    }
+    if (!ok && lane == 0) {
+      report(p.status, MLA_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // ---- epilogue ----
+    named_bar_sync(kSoftmaxBarrier, 128);
+    const bool single = (nsplit == 1);
+    float* scale_s = alpha_s;
+    if (sid < NR) {
+      if (n_tiles > 0)
+        l_row += (red_sum[sid] + red_sum[NR + sid]) + (red_sum[2 * NR + sid] + red_sum[3 * NR + sid]);
+      const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
+      const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + sid;
+      float sc = 0.0f;
+      if (sid < rows_here) {
+        if (single) {
+          const float ls = (l_row > 0.0f) ? 0.6931471805599453f * (m_s + log2f(l_row)) : -INFINITY;
+          if (p.lse) p.lse[grow] = ls;
+          sc = (l_row > 0.0f) ? p.kv_scale / l_row : 0.0f;
+        } else {
+          float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
+          ml[0] = m_s;
+          ml[1] = l_row;
+          sc = p.kv_scale;
+        }
+      }
+      scale_s[sid] = sc;
+    }
+    named_bar_sync(kSoftmaxBarrier, 128);
+    // The MMA warp commits BAR_FINAL once, after its last MMA.
+    bool fin = mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
+    fin = __all_sync(0xffffffffu, fin);
+    if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
+    if (ok && fin && n_tiles > 0) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int d = 0; d < 4; ++d) {
+        const int dim = d * 128 + tok_lane;
+#pragma unroll
+        for (int cc = 0; cc < NR / 16; ++cc) {
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_addr + C::kOCol + d * NR + cc * 16, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int row = cc * 16 + k;
+            if (row < rows_here) {
+              const float v = __uint_as_float(r[k]) * scale_s[row];
+              const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
+              if (single) {
+                p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
+                if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = v;
+              } else {
+                p.ws_o[(grow * p.max_splits + split) * MLA_LATENT_DIM + dim] = v;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Merge: one CTA per (128-dim quarter, row); G groups of 32 lanes, each lane
+// owning 4 consecutive dims.  Group g folds partials g, g+G, g+2G, ... with an
+// online softmax (4 loads in flight per step; slots past the end re-read the
+// step's first slot with weight 0), then group 0 combines the G group states
+// through shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float exp2_exact_int(float x) {
+  // 2^x; exact when x is an integer (the split kernel's reference maxima).
+  if (x == -INFINITY) return 0.0f;
+  const float a = rintf(x);
+  const int ia = static_cast<int>(a);
+  if (ia < -126) return 0.0f;
+  return ex2_approx(x - a) * pow2i(ia > 127 ? 127 : ia);
+}
+
+struct MergeParams {
+  const float* po;
+  const float* pml;
+  int32_t rows;
+  int32_t stride_s;      // slots per row in memory
+  int32_t uniform_s;     // slots per row when splits == nullptr
+  const int32_t* splits; // per-request slot counts (decode path) or nullptr
+  int32_t rows_per_req;
+  __nv_bfloat16* out;
+  float* lse;
+  float* out_f32;
+};
+
+template <int G>
+__global__ void __launch_bounds__(32 * G) mla_merge_kernel(const MergeParams p) {
+  constexpr int U = 4;
+  __shared__ float sm_m[G];
+  __shared__ float sm_l[G];
+  __shared__ float4 sm_o[G][32];
+  const int row = blockIdx.y;
+  const int quarter = blockIdx.x;
+  const int g = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int ns = p.uniform_s;
+  if (p.splits) {
+    ns = min(p.splits[row / p.rows_per_req], p.stride_s);
+    if (ns <= 1) return;  // the split kernel wrote this row directly
+  }
+  const int dim = quarter * 128 + lane * 4;
+  const float* pml = p.pml + static_cast<int64_t>(row) * p.stride_s * 2;
+  const float* po = p.po + static_cast<int64_t>(row) * p.stride_s * MLA_LATENT_DIM + dim;
+  float m = -INFINITY, l = 0.0f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = g; s0 < ns; s0 += G * U) {
+    float mu[U], lu[U];
+    float4 ou[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int s = s0 + u * G;
+      const bool in = s < ns;
+      const int slot = in ? s : s0;  // weight-0 padded load of a valid slot
+      const float2 ml = *reinterpret_cast<const float2*>(pml + slot * 2);
+      ou[u] = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(slot) * MLA_LATENT_DIM);
+      mu[u] = (in && ml.y > 0.0f) ? ml.x : -INFINITY;
+      lu[u] = ml.y;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (mu[u] == -INFINITY) continue;  // empty slot or padding: weight 0
+      const float m_new = fmaxf(m, mu[u]);
+      const float a = exp2_exact_int(m - m_new);
+      const float w = exp2_exact_int(mu[u] - m_new);
+      l = l * a + lu[u] * w;
+      o.x = o.x * a + ou[u].x * w;
+      o.y = o.y * a + ou[u].y * w;
+      o.z = o.z * a + ou[u].z * w;
+      o.w = o.w * a + ou[u].w * w;
+      m = m_new;
+    }
+  }
+  if (G > 1) {
+    if (lane == 0) {
+      sm_m[g] = m;
+      sm_l[g] = l;
+    }
+    sm_o[g][lane] = o;
+    __syncthreads();
+    if (g != 0) return;
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < G; ++k)
+      if (sm_l[k] > 0.0f) M = fmaxf(M, sm_m[k]);
+    l = 0.0f;
+    o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        if (!(sm_l[k] > 0.0f)) continue;  // empty group
+        const float w = exp2_exact_int(sm_m[k] - M);
+        const float4 v = sm_o[k][lane];
+        l += sm_l[k] * w;
+        o.x += v.x * w;
+        o.y += v.y * w;
+        o.z += v.z * w;
+        o.w += v.w * w;
+      }
+    }
+    m = M;
+  }
+  const bool empty = !(l > 0.0f);
+  const float inv = empty ? 0.0f : 1.0f / l;
+  const float4 r = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+  const int64_t off = static_cast<int64_t>(row) * MLA_LATENT_DIM + dim;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(r.x, r.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(r.z, r.w);
+  uint2 packed;
+  packed.x = *reinterpret_cast<uint32_t*>(&lo);
+  packed.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p.out + off) = packed;
+  if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + off) = r;
+  if (p.lse && quarter == 0 && lane == 0)
+    p.lse[row] = empty ? -INFINITY : 0.6931471805599453f * (m + log2f(l));
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D uint8 view [rows, 576] with a (box_x, box_y) box.
+static bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t box_x,
+                     uint32_t box_y, CUtensorMapSwizzle sw) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {MLA_HEAD_DIM, rows};
+  cuuint64_t strides[1] = {MLA_HEAD_DIM};
+  cuuint32_t box[2] = {box_x, box_y};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NR>
+static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages, int batch,
+                                int groups, const DecodeParams& prm, cudaStream_t stream) {
+  using C = Cfg<NR>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_kernel<NR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  CUtensorMap kv_lat, kv_rope, q_lat, q_rope;
+  const uint64_t kv_rows = static_cast<uint64_t>(num_pages) * MLA_PAGE_SIZE;
+  const uint64_t q_rows = static_cast<uint64_t>(batch) * prm.rows_per_req;
+  if (!make_map(&kv_lat, kv, kv_rows, 128, MLA_PAGE_SIZE, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&kv_rope, kv, kv_rows, 64, MLA_PAGE_SIZE, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&q_lat, q, q_rows, 128, NR, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&q_rope, q, q_rows, 64, NR, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  dim3 grid(prm.max_splits, batch, groups);
+  mla_split_kv_kernel<NR><<<grid, kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
+                                                                     q_rope, prm);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_merge(const MergeParams& mp, int kv_split, cudaStream_t stream) {
+  dim3 grid(4, mp.rows);
+  switch (kv_split) {
+    case 1: mla_merge_kernel<1><<<grid, 32, 0, stream>>>(mp); break;
+    case 2: mla_merge_kernel<2><<<grid, 64, 0, stream>>>(mp); break;
+    case 4: mla_merge_kernel<4><<<grid, 128, 0, stream>>>(mp); break;
+    case 8: mla_merge_kernel<8><<<grid, 256, 0, stream>>>(mp); break;
+    case 16: mla_merge_kernel<16><<<grid, 512, 0, stream>>>(mp); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+static bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+static int cuda_fail(const char* what, cudaError_t e) {
+  set_error(std::string(what) + ": " + cudaGetErrorString(e));
+  return MLA_ERR_CUDA;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+namespace mla {
+
+// Validated launch state shared by mla_decode, mla_decode_splitkv and
+// mla_decode_merge.
+struct DecodeLaunch {
+  DecodeParams prm;
+  MergeParams mp;
+  RowGroups rg;
+  int batch;
+  int kv_split;
+  int max_splits;
+};
+
+static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                          const int32_t* page_table, int32_t max_pages_per_req,
+                          const int32_t* kv_lens, const int32_t* splits, const int32_t* chunks,
+                          int32_t max_splits, int32_t kv_split, int32_t batch, int32_t q_len,
+                          int32_t num_heads, int32_t causal, float q_scale, float kv_scale,
+                          float softmax_scale, void* workspace, size_t workspace_bytes,
+                          void* out_bf16, float* lse_f32, float* out_f32_debug,
+                          const char* who, DecodeLaunch* dl) {
+  const std::string w(who);
+  if (!q_fp8 || !kv_pages_fp8 || !page_table || !kv_lens || !splits || !chunks || !workspace ||
+      !out_bf16) {
+    set_error(w + ": null pointer argument");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (batch < 1 || q_len < 1 || num_heads < 1 || max_pages_per_req < 1 || num_pages < 1) {
+    set_error(w + ": batch, q_len, num_heads, max_pages_per_req and num_pages must be >= 1");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(num_heads) * q_len > MLA_MAX_ROWS) {
+    set_error(w + ": num_heads * q_len exceeds MLA_MAX_ROWS");
+    return MLA_ERR_UNSUPPORTED;
+  }
+  if (batch > 65535) {
+    set_error(w + ": batch exceeds 65535");
+    return MLA_ERR_UNSUPPORTED;
+  }
+  if (num_pages * MLA_PAGE_SIZE > INT32_MAX) {
+    set_error(w + ": page pool too large for 32-bit TMA row coordinates");
+    return MLA_ERR_UNSUPPORTED;
+  }
+  if (max_splits < 1 || max_splits > MLA_MAX_SPLITS) {
+    set_error(w + ": max_splits must be in [1, MLA_MAX_SPLITS]");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (kv_split != 1 && kv_split != 2 && kv_split != 4 && kv_split != 8 && kv_split != 16) {
+    set_error(w + ": kv_split must be 1, 2, 4, 8 or 16");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!aligned(q_fp8, 16) || !aligned(kv_pages_fp8, 16) || !aligned(workspace, 256) ||
+      !aligned(out_bf16, 8) || (out_f32_debug && !aligned(out_f32_debug, 16))) {
+    set_error(w + ": q/kv need 16-byte, workspace 256-byte, outputs 8/16-byte alignment");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!(std::isfinite(q_scale) && std::isfinite(kv_scale) && std::isfinite(softmax_scale))) {
+    set_error(w + ": scales must be finite");
+    return MLA_ERR_INVALID_ARG;
+  }
+  const int64_t rows_total = static_cast<int64_t>(batch) * q_len * num_heads;
+  const size_t need = ws_total(rows_total, max_splits);
+  if (workspace_bytes < need) {
+    set_error(w + ": workspace of " + std::to_string(workspace_bytes) + " bytes is below the " +
+              std::to_string(need) + " required");
+    return MLA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  dl->rg = row_groups(num_heads * q_len);
+  dl->batch = batch;
+  dl->kv_split = kv_split;
+  dl->max_splits = max_splits;
+  DecodeParams& prm = dl->prm;
+  prm.page_table = page_table;
+  prm.kv_lens = kv_lens;
+  prm.splits = splits;
+  prm.chunks = chunks;
+  prm.num_pages = num_pages;
+  prm.max_pages = max_pages_per_req;
+  prm.max_splits = max_splits;
+  prm.q_len = q_len;
+  prm.num_heads = num_heads;
+  prm.causal = causal ? 1 : 0;
+  prm.rows_per_req = num_heads * q_len;
+  prm.rows_per_group = dl->rg.rows;
+  prm.c_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * kv_scale *
+                                  1.4426950408889634);
+  prm.kv_scale = kv_scale;
+  prm.status = reinterpret_cast<int*>(ws);
+  prm.ws_ml = reinterpret_cast<float*>(ws + ws_ml_offset());
+  prm.ws_o = reinterpret_cast<float*>(ws + ws_o_offset(rows_total, max_splits));
+  prm.out = reinterpret_cast<__nv_bfloat16*>(out_bf16);
+  prm.lse = lse_f32;
+  prm.out_f32 = out_f32_debug;
+  MergeParams& mp = dl->mp;
+  mp.po = prm.ws_o;
+  mp.pml = prm.ws_ml;
+  mp.rows = static_cast<int32_t>(rows_total);
+  mp.stride_s = max_splits;
+  mp.uniform_s = max_splits;
+  mp.splits = splits;
+  mp.rows_per_req = num_heads * q_len;
+  mp.out = prm.out;
+  mp.lse = lse_f32;
+  mp.out_f32 = out_f32_debug;
+  return MLA_OK;
+}
+
+static int launch_decode_split(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                               const DecodeLaunch& dl, cudaStream_t st) {
+  cudaError_t e;
+  const int b = dl.batch, g = dl.rg.groups;
+  switch (dl.rg.nr) {
+    case 16: e = launch_split<16>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
+    case 32: e = launch_split<32>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
+    case 48: e = launch_split<48>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
+    case 64: e = launch_split<64>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
+    case 80: e = launch_split<80>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
+    case 96: e = launch_split<96>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
+    default:
+      set_error("mla_decode: internal row grouping error");
+      return MLA_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return cuda_fail("mla_decode: split-KV launch", e);
+  return MLA_OK;
+}
+
+static int launch_decode_merge(const DecodeLaunch& dl, cudaStream_t st) {
+  if (dl.max_splits <= 1) return MLA_OK;  // every request was written directly
+  cudaError_t e = launch_merge(dl.mp, dl.kv_split, st);
+  if (e != cudaSuccess) return cuda_fail("mla_decode: merge launch", e);
+  return MLA_OK;
+}
+
+}  // namespace mla
+
+#define MLA_DECODE_ARGS                                                                     \
+  q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req, kv_lens, splits, chunks,   \
+      max_splits, kv_split, batch, q_len, num_heads, causal, q_scale, kv_scale, softmax_scale, \
+      workspace, workspace_bytes, out_bf16, lse_f32, out_f32_debug
+
+extern "C" int mla_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                          const int32_t* page_table, int32_t max_pages_per_req,
+                          const int32_t* kv_lens, const int32_t* splits, const int32_t* chunks,
+                          int32_t max_splits, int32_t kv_split, int32_t batch, int32_t q_len,
+                          int32_t num_heads, int32_t causal, float q_scale, float kv_scale,
+                          float softmax_scale, void* workspace, size_t workspace_bytes,
+                          void* out_bf16, float* lse_f32, float* out_f32_debug, void* stream) {
+  DecodeLaunch dl;
+  int rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode", &dl);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
+  if (rc != MLA_OK) return rc;
+  return launch_decode_merge(dl, st);
+}
+
+extern "C" int mla_decode_splitkv(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                                  const int32_t* page_table, int32_t max_pages_per_req,
+                                  const int32_t* kv_lens, const int32_t* splits,
+                                  const int32_t* chunks, int32_t max_splits, int32_t kv_split,
+                                  int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
+                                  float q_scale, float kv_scale, float softmax_scale,
+                                  void* workspace, size_t workspace_bytes, void* out_bf16,
+                                  float* lse_f32, float* out_f32_debug, void* stream) {
+  DecodeLaunch dl;
+  int rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode_splitkv", &dl);
+  if (rc != MLA_OK) return rc;
+  return launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mla_decode_merge(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                                const int32_t* page_table, int32_t max_pages_per_req,
+                                const int32_t* kv_lens, const int32_t* splits,
+                                const int32_t* chunks, int32_t max_splits, int32_t kv_split,
+                                int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
+                                float q_scale, float kv_scale, float softmax_scale,
+                                void* workspace, size_t workspace_bytes, void* out_bf16,
+                                float* lse_f32, float* out_f32_debug, void* stream) {
+  DecodeLaunch dl;
+  int rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode_merge", &dl);
+  if (rc != MLA_OK) return rc;
+  return launch_decode_merge(dl, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mla_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < kStatusBytes) {
+    set_error("mla_decode_workspace_init: null or too small workspace");
+    return MLA_ERR_INVALID_ARG;
+  }
+  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("mla_decode_workspace_init", e);
+  return MLA_OK;
+}
+
+extern "C" int mla_merge(const float* partial_o, const float* partial_ml, int32_t rows,
+                         int32_t num_ctas_kv, int32_t kv_split, void* out_bf16, float* lse_f32,
+                         float* out_f32_debug, void* stream) {
+  if (!partial_o || !partial_ml || !out_bf16) {
+    set_error("mla_merge: null pointer argument");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (rows < 1 || rows > 65535 || num_ctas_kv < 1) {
+    set_error("mla_merge: rows must be in [1, 65535] and num_ctas_kv >= 1");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (kv_split != 1 && kv_split != 2 && kv_split != 4 && kv_split != 8 && kv_split != 16) {
+    set_error("mla_merge: kv_split must be 1, 2, 4, 8 or 16");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!aligned(partial_o, 16) || !aligned(partial_ml, 8) || !aligned(out_bf16, 8) ||
+      (out_f32_debug && !aligned(out_f32_debug, 16))) {
+    set_error("mla_merge: partial_o/out_f32 need 16-byte, partial_ml/out 8-byte alignment");
+    return MLA_ERR_INVALID_ARG;
+  }
+  MergeParams mp;
+  mp.po = partial_o;
+  mp.pml = partial_ml;
+  mp.rows = rows;
+  mp.stride_s = num_ctas_kv;
+  mp.uniform_s = num_ctas_kv;
+  mp.splits = nullptr;
+  mp.rows_per_req = 1;
+  mp.out = reinterpret_cast<__nv_bfloat16*>(out_bf16);
+  mp.lse = lse_f32;
+  mp.out_f32 = out_f32_debug;
+  cudaError_t e = launch_merge(mp, kv_split, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("mla_merge: launch", e);
+  return MLA_OK;
+}
+
+extern "C" int mla_decode_status(void* workspace, void* stream) {
+  if (!workspace) {
+    set_error("mla_decode_status: null workspace");
+    return MLA_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail("mla_decode_status: stream", e);
+  int v = 0;
+  e = cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail("mla_decode_status: read", e);
+  e = cudaMemset(workspace, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail("mla_decode_status: clear", e);
+  if (v == MLA_ERR_TIMEOUT) {
+    set_error("mla_decode: a device wait ran out (timeout)");
+    return MLA_ERR_TIMEOUT;
+  }
+  if (v != 0) {
+    set_error("mla_decode: device detected a bad page id or inconsistent plan arrays");
+    return MLA_ERR_INVALID_ARG;
+  }
+  return MLA_OK;
+}

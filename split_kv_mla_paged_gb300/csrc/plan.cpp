@@ -1,0 +1,138 @@
+// Host split planner and workspace sizing for paged MLA decode.
+//
+// Two planners:
+//  * target_ctas > 0 reproduces the per-request plan printed in TensorRT-LLM
+//    issue #20510 ("Repro 2": H12 q8 splits 94/49/25/12/6 at 128K and
+//    100/50/25/12/6 at 1M for B = 1..16, split cap raised to 128):
+//    t = max(1, target / B) splits per request, chunk = roundup128(ceil(L / t)),
+//    splits = ceil(L / chunk).
+//  * target_ctas <= 0 is the GB300 planner.  One CTA of the split kernel fills
+//    an SM (its shared memory holds two 72 KB KV stages), so it balances whole
+//    waves of sm_count CTAs: one chunk for the whole batch (the skewed-batch
+//    finding in the same issue's follow-up: a common split size plus early
+//    exit of empty split slots beats one wave per request), a minimum of one
+//    128-token tile per split (the short-KV finding there), and an estimate of
+//    each CTA's fixed cost (prologue plus the partial it writes and the merge
+//    reads) to trade waves against splits.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <string>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+static thread_local std::string g_last_error;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// CTAs the split kernel launches with a common chunk (empty slots excluded).
+static int64_t ctas_for_chunk(const int32_t* lens, int batch, int64_t chunk, int groups) {
+  int64_t n = 0;
+  for (int b = 0; b < batch; ++b) n += ceil_div(lens[b], chunk);
+  return n * groups;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" const char* mla_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" size_t mla_decode_workspace_size(int32_t batch, int32_t q_len, int32_t num_heads,
+                                            int32_t max_splits) {
+  if (batch < 1 || q_len < 1 || num_heads < 1 || max_splits < 1) return 0;
+  const int64_t rows = static_cast<int64_t>(batch) * q_len * num_heads;
+  return ws_total(rows, max_splits);
+}
+
+extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t num_heads,
+                               int32_t q_len, int32_t sm_count, int32_t target_ctas,
+                               int32_t* splits_out, int32_t* chunk_out, int32_t* kv_split_out,
+                               size_t* workspace_bytes_out) {
+  if (!kv_lens || !splits_out || !chunk_out || !kv_split_out || !workspace_bytes_out) {
+    set_error("mla_decode_plan: null pointer argument");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (batch < 1 || num_heads < 1 || q_len < 1) {
+    set_error("mla_decode_plan: batch, num_heads and q_len must be >= 1");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(num_heads) * q_len > MLA_MAX_ROWS) {
+    set_error("mla_decode_plan: num_heads * q_len exceeds MLA_MAX_ROWS");
+    return MLA_ERR_UNSUPPORTED;
+  }
+  int64_t lmax = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (kv_lens[b] < q_len || kv_lens[b] < 1) {
+      set_error("mla_decode_plan: kv_lens[" + std::to_string(b) + "] = " +
+                std::to_string(kv_lens[b]) + " is below q_len (" + std::to_string(q_len) + ")");
+      return MLA_ERR_INVALID_ARG;
+    }
+    if (kv_lens[b] > INT32_MAX - MLA_TILE_TOKENS) {
+      set_error("mla_decode_plan: kv length too large");
+      return MLA_ERR_INVALID_ARG;
+    }
+    lmax = std::max<int64_t>(lmax, kv_lens[b]);
+  }
+  const RowGroups rg = row_groups(num_heads * q_len);
+  const int64_t T = MLA_TILE_TOKENS;
+
+  if (target_ctas > 0) {
+    const int64_t t = std::max<int64_t>(1, target_ctas / (static_cast<int64_t>(batch) * rg.groups));
+    for (int b = 0; b < batch; ++b) {
+      int64_t chunk = round_up(ceil_div(kv_lens[b], t), T);
+      if (ceil_div(kv_lens[b], chunk) > MLA_MAX_SPLITS)
+        chunk = round_up(ceil_div(kv_lens[b], MLA_MAX_SPLITS), T);
+      chunk_out[b] = static_cast<int32_t>(chunk);
+      splits_out[b] = static_cast<int32_t>(ceil_div(kv_lens[b], chunk));
+    }
+  } else {
+    if (sm_count < 1) {
+      set_error("mla_decode_plan: sm_count must be >= 1 when target_ctas <= 0");
+      return MLA_ERR_INVALID_ARG;
+    }
+    // Fixed cost of one CTA in token-equivalents of KV streaming: ~2.5 us of
+    // prologue/epilogue at ~76 tokens/us per SM, plus writing and re-reading
+    // its partials (rows x 2 KB each way) at 576 B per token.
+    const int64_t c0 = 200 + static_cast<int64_t>(rg.rows) * 2 * 2048 / MLA_HEAD_DIM;
+    const int64_t cmin = std::max<int64_t>(T, round_up(ceil_div(lmax, MLA_MAX_SPLITS), T));
+    const int64_t cmax = std::max<int64_t>(cmin, round_up(lmax, T));
+    int64_t best_chunk = cmax;
+    double best_cost = -1.0;
+    for (int w = 1; w <= 16; ++w) {
+      const int64_t slots = static_cast<int64_t>(w) * sm_count;
+      if (ctas_for_chunk(kv_lens, batch, cmax, rg.groups) > slots) continue;
+      int64_t lo = cmin / T, hi = cmax / T;  // smallest chunk/T that fits `slots`
+      while (lo < hi) {
+        const int64_t mid = (lo + hi) / 2;
+        if (ctas_for_chunk(kv_lens, batch, mid * T, rg.groups) <= slots)
+          hi = mid;
+        else
+          lo = mid + 1;
+      }
+      const int64_t chunk = lo * T;
+      const int64_t n = ctas_for_chunk(kv_lens, batch, chunk, rg.groups);
+      const double cost = static_cast<double>(ceil_div(n, sm_count)) * static_cast<double>(chunk + c0);
+      if (best_cost < 0.0 || cost < best_cost) {
+        best_cost = cost;
+        best_chunk = chunk;
+      }
+    }
+    for (int b = 0; b < batch; ++b) {
+      chunk_out[b] = static_cast<int32_t>(best_chunk);
+      splits_out[b] = static_cast<int32_t>(ceil_div(kv_lens[b], best_chunk));
+    }
+  }
+  int32_t max_splits = 1;
+  for (int b = 0; b < batch; ++b) max_splits = std::max(max_splits, splits_out[b]);
+  int32_t g = 16;
+  while (g > max_splits) g >>= 1;
+  *kv_split_out = g;
+  *workspace_bytes_out = mla_decode_workspace_size(batch, q_len, num_heads, max_splits);
+  return MLA_OK;
+}

@@ -14,4 +14,5 @@ from .mla_inputs import (  # noqa: F401
     decode_inputs,
     merge_partials,
     ragged_lens,
+    workload_inputs,
 )

@@ -1,0 +1,87 @@
+"""The C-ABI library loads and exports what include/mla_decode.h declares.
+
+No compute call here: host-side argument checks return before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import split_kv_mla_paged_gb300 as mla
+from split_kv_mla_paged_gb300 import build as mla_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "mla_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mla_build.build()
+    return mla.load_library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_exported_set():
+    assert _declared() == sorted(mla.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(mla.library_path())
+    for name in _declared():
+        assert hasattr(raw, name), name
+
+
+def test_workspace_size_layout(lib):
+    rows, s = 12 * 8 * 3, 7
+    ml = rows * s * 8
+    ml_aligned = (ml + 255) // 256 * 256
+    assert mla.mla_decode_workspace_size(3, 8, 12, s) == 256 + ml_aligned + rows * s * 2048
+    assert mla.mla_decode_workspace_size(0, 8, 12, s) == 0
+
+
+def test_decode_rejects_null_pointers_without_gpu(lib):
+    st = lib.mla_decode(None, None, 1, None, 1, None, None, None, 1, 1, 1, 1, 12, 0, 1.0, 1.0,
+                        0.1, None, 0, None, None, None, None)
+    assert st == mla.MLA_ERR_INVALID_ARG
+    assert "null" in mla.mla_last_error()
+
+
+def test_decode_rejects_small_workspace_without_gpu(lib):
+    fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced on this path
+    st = lib.mla_decode(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 1.0, 1.0,
+                        0.1, fake, 16, fake, None, None, None)
+    assert st == mla.MLA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_decode_rejects_bad_kv_split_and_rows(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    st = lib.mla_decode(fake, fake, 4, fake, 4, fake, fake, fake, 2, 3, 1, 1, 12, 0, 1.0, 1.0,
+                        0.1, fake, 1 << 30, fake, None, None, None)
+    assert st == mla.MLA_ERR_INVALID_ARG
+    st = lib.mla_decode(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 8, 256, 0, 1.0, 1.0,
+                        0.1, fake, 1 << 30, fake, None, None, None)
+    assert st == mla.MLA_ERR_UNSUPPORTED
+
+
+def test_decode_rejects_misaligned_inputs(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    st = lib.mla_decode(odd, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 1.0, 1.0,
+                        0.1, fake, 1 << 30, fake, None, None, None)
+    assert st == mla.MLA_ERR_INVALID_ARG
+
+
+def test_merge_rejects_bad_arguments(lib):
+    assert lib.mla_merge(None, None, 4, 4, 1, None, None, None, None) == mla.MLA_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.mla_merge(fake, fake, 4, 4, 5, fake, None, None, None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_merge(fake, fake, 0, 4, 4, fake, None, None, None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_status_rejects_null(lib):
+    assert lib.mla_decode_status(None, None) == mla.MLA_ERR_INVALID_ARG

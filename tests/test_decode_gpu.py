@@ -1,0 +1,208 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import split_kv_mla_paged_gb300 as mla
+from split_kv_mla_paged_gb300 import build as mla_build
+from synth import SOFTMAX_SCALE, WORKLOADS, decode_inputs, merge_partials, workload_inputs
+from mla_testutil import PLAN_ABS, assert_parity, oracle_rows, peaked_tolerance, run_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mla_build.build()
+    mla.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+def _full_check(inp, causal, scale, o_tol=None, **kw):
+    out, lse, out_f32 = run_decode(inp, causal, scale, **kw)
+    ref_o, ref_l = oracle.decode_rows(inp.q, inp.kv.cpu(), inp.page_table.cpu(), inp.kv_lens,
+                                      q_len=inp.q_len, num_heads=inp.num_heads, causal=causal,
+                                      softmax_scale=scale, q_scale=kw.get("q_scale", 1.0),
+                                      kv_scale=kw.get("kv_scale", 1.0))
+    assert_parity(out, lse, ref_o, ref_l, o_tol=o_tol)
+    # The fp32 pre-store output rounds to the BF16 output exactly.
+    assert torch.equal(out_f32.to(torch.bfloat16), out)
+    return out, lse, out_f32
+
+
+def test_tiny_config_pages_plan():
+    w = WORKLOADS["tiny_b1_h12_q1_l4096"]
+    inp = workload_inputs("tiny_b1_h12_q1_l4096")
+    plan = mla.mla_decode_plan(inp.kv_lens.tolist(), 12, 1, target_ctas=w["target"])
+    assert plan.splits.tolist() == [4]
+    _full_check(inp, False, SOFTMAX_SCALE, plan=plan)
+
+
+def test_tiny_config_gb300_plan():
+    inp = workload_inputs("tiny_b1_h12_q1_l4096")
+    _full_check(inp, False, SOFTMAX_SCALE)
+
+
+@pytest.mark.parametrize("B,H,q_len,lens,causal", [
+    (1, 12, 1, [1], False),
+    (1, 12, 1, [31], False),
+    (1, 12, 1, [129], False),
+    (2, 12, 1, [1000, 77], False),
+    (1, 12, 8, [8], True),
+    (2, 12, 8, [300, 1029], True),
+    (1, 1, 1, [5000], False),
+    (1, 3, 2, [513], True),
+    (1, 20, 1, [333], False),       # 20 rows -> 32 columns
+    (1, 10, 4, [700], True),        # 40 rows -> 48
+    (1, 16, 4, [2000], True),       # 64 rows
+    (1, 16, 5, [900], True),        # 80 rows
+    (2, 12, 8, [4096, 2500], True), # 96 rows
+    (1, 16, 8, [1500], True),       # 128 rows -> two groups of 64
+    (1, 96, 8, [600], True),        # 768 rows -> eight groups of 96
+])
+def test_parity_shapes(B, H, q_len, lens, causal):
+    inp = decode_inputs(B, H, q_len, lens, seed=100 + B * H + q_len, extra_pages=2)
+    _full_check(inp, causal, SOFTMAX_SCALE)
+
+
+@pytest.mark.parametrize("target", [1, 3, 7, 50])
+def test_parity_pages_planner_targets(target):
+    inp = decode_inputs(2, 12, 8, [3000, 1111], seed=7, extra_pages=1)
+    plan = mla.mla_decode_plan(inp.kv_lens.tolist(), 12, 8, target_ctas=target)
+    _full_check(inp, True, SOFTMAX_SCALE, plan=plan)
+
+
+def test_parity_scales_and_peaked_softmax():
+    inp = decode_inputs(1, 12, 2, [3333], seed=8)
+    _full_check(inp, True, 0.11, q_scale=1.5, kv_scale=0.75)
+    # Large logits: many reference moves and strongly peaked rows, checked
+    # against the bound the E4M3 weights allow (see peaked_tolerance).
+    _full_check(inp, False, 1.0, o_tol=peaked_tolerance(inp))
+
+
+def test_split_plans_agree_in_fp32():
+    inp = decode_inputs(2, 12, 8, [5000, 2345], seed=9, extra_pages=1)
+    lens = inp.kv_lens.tolist()
+    plans = [mla.mla_decode_plan(lens, 12, 8, target_ctas=t) for t in (1, 2, 6, 20, 100)]
+    plans.append(mla.mla_decode_plan(lens, 12, 8, sm_count=152))
+    base = None
+    for plan in plans:
+        for ks in (1, 2, 4, 8, 16):
+            if ks > plan.max_splits and ks != 1:
+                continue
+            _, lse, o32 = run_decode(inp, True, SOFTMAX_SCALE, plan=plan, kv_split=ks)
+            if base is None:
+                base = (o32.clone(), lse.clone())
+                continue
+            d = (o32 - base[0]).abs().max().item()
+            dl = (lse - base[1]).abs().max().item()
+            assert d <= PLAN_ABS, f"plan {plan.splits.tolist()} kv_split {ks}: {d:.3e}"
+            assert dl <= PLAN_ABS, f"plan {plan.splits.tolist()} kv_split {ks}: lse {dl:.3e}"
+
+
+def test_deterministic_run_to_run():
+    inp = decode_inputs(1, 12, 1, [9000], seed=10)
+    a = run_decode(inp, False, SOFTMAX_SCALE)
+    b = run_decode(inp, False, SOFTMAX_SCALE)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_page_permutation_changes_nothing():
+    inp = decode_inputs(1, 12, 1, [2500], seed=11, extra_pages=3)
+    a = run_decode(inp, False, SOFTMAX_SCALE)
+    P = inp.num_pages
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(3))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P)
+    inp.kv = inp.kv[perm]
+    pt = inp.page_table.clone()
+    m = pt >= 0
+    pt[m] = inv[pt[m].long()].to(torch.int32)
+    inp.page_table = pt
+    b = run_decode(inp, False, SOFTMAX_SCALE)
+    assert torch.equal(a[2], b[2]) and torch.equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------- merge alone
+
+@pytest.mark.parametrize("rows,S", [(12, 6), (96, 25), (192, 128), (7, 1), (40, 33)])
+@pytest.mark.parametrize("kv_split", [1, 2, 4, 8, 16])
+def test_merge_against_oracle(rows, S, kv_split):
+    o, ml = merge_partials(rows, S, seed=rows * 131 + S, all_empty_rows=[rows // 2])
+    ref_o, ref_l = oracle.merge(o, ml)
+    out, lse, out_f32 = mla.merge(torch.from_numpy(o).cuda(), torch.from_numpy(ml).cuda(), kv_split)
+    torch.cuda.synchronize()
+    f = out_f32.cpu().numpy().astype(np.float64)
+    scale = np.max(np.abs(ref_o))
+    assert np.max(np.abs(f - ref_o)) <= 2e-6 * scale
+    l = lse.cpu().numpy()
+    e = rows // 2
+    assert l[e] == -np.inf and np.all(f[e] == 0.0)
+    keep = np.arange(rows) != e
+    assert np.max(np.abs(l[keep] - ref_l[keep])) <= 1e-5
+    assert torch.equal(out_f32.to(torch.bfloat16), out)
+
+
+def test_merge_kv_split_invariance():
+    o, ml = merge_partials(24, 100, seed=5)
+    res = [mla.merge(torch.from_numpy(o).cuda(), torch.from_numpy(ml).cuda(), g)
+           for g in (1, 2, 4, 8, 16)]
+    for _, lse, f in res[1:]:
+        assert (f - res[0][2]).abs().max().item() <= PLAN_ABS * res[0][2].abs().max().item()
+        assert (lse - res[0][1]).abs().max().item() <= PLAN_ABS
+
+
+# ---------------------------------------------------------------- device status
+
+def test_bad_page_id_is_reported():
+    inp = decode_inputs(1, 12, 1, [200], seed=12)
+    inp.page_table[0, 2] = inp.num_pages + 5
+    with pytest.raises(mla.MlaError) as e:
+        run_decode(inp, False, SOFTMAX_SCALE)
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG
+
+
+def test_inconsistent_plan_is_reported():
+    inp = decode_inputs(1, 12, 1, [1000], seed=13)
+    plan = mla.mla_decode_plan(inp.kv_lens.tolist(), 12, 1, target_ctas=4)
+    plan.chunks[:] = 100  # not a multiple of the 128-token tile
+    with pytest.raises(mla.MlaError) as e:
+        run_decode(inp, False, SOFTMAX_SCALE, plan=plan)
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def _sample_rows(inp, n, seed):
+    g = np.random.default_rng(seed)
+    return np.sort(g.choice(inp.rows, size=min(n, inp.rows), replace=False))
+
+
+@pytest.mark.parametrize("name,nrows", [
+    ("h12_q1_l128k_b16", 8),
+    ("mtp_h12_q8_l128k_b4", 10),
+    ("ragged_h12_q1_b16", 16),
+    ("packed_h96_q8_l128k_b1", 12),
+    ("long_h12_q1_l1m_b16", 6),
+])
+def test_full_size_sampled_rows(name, nrows):
+    w = WORKLOADS[name]
+    inp = workload_inputs(name, device="cuda")
+    out, lse, o32 = run_decode(inp, w["causal"], SOFTMAX_SCALE)
+    rows = _sample_rows(inp, nrows, seed=len(name))
+    ref_o, ref_l = oracle_rows(inp, rows, w["causal"], SOFTMAX_SCALE)
+    flat_o = out.reshape(-1, 512)[torch.from_numpy(rows).cuda()]
+    flat_l = lse.reshape(-1)[torch.from_numpy(rows).cuda()]
+    assert_parity(flat_o, flat_l, ref_o, ref_l, what=name)
+    assert torch.isfinite(o32).all() and torch.isfinite(lse).all()
+    # Properties over every row at full size: a second split plan agrees in fp32.
+    if w["target"] is not None:
+        plan = mla.mla_decode_plan(inp.kv_lens.tolist(), w["num_heads"], w["q_len"],
+                                   target_ctas=w["target"])
+        _, lse2, o32b = run_decode(inp, w["causal"], SOFTMAX_SCALE, plan=plan)
+        assert (o32b - o32).abs().max().item() <= PLAN_ABS
+        assert (lse2 - lse).abs().max().item() <= PLAN_ABS
+    del inp
+    torch.cuda.empty_cache()

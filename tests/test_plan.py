@@ -1,0 +1,101 @@
+"""Host planner: the pages' printed plans, and invariants of the GB300 planner."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import split_kv_mla_paged_gb300 as mla
+from split_kv_mla_paged_gb300 import build as mla_build
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "p4_split_plans.json")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mla_build.build()
+    mla.load_library()
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _golden()["repro2_q8_target100"],
+                         ids=lambda c: f"B{c['batch']}_L{c['kv_len']}")
+def test_repro2_plans_reproduced(case):
+    p = mla.mla_decode_plan([case["kv_len"]] * case["batch"], num_heads=12, q_len=8,
+                            target_ctas=100)
+    assert p.splits.tolist() == [case["splits"]] * case["batch"]
+    assert np.all(p.chunks % 128 == 0)
+    assert np.all(p.splits.astype(np.int64) * p.chunks >= case["kv_len"])
+    assert np.all((p.splits.astype(np.int64) - 1) * p.chunks < case["kv_len"])
+
+
+@pytest.mark.parametrize("case", _golden()["repro1_q1_uniform"], ids=lambda c: f"B{c['batch']}")
+@pytest.mark.parametrize("kv_len", [131072, 1048576])
+def test_repro1_uniform_splits(case, kv_len):
+    b, split = case["batch"], case["split"]
+    p = mla.mla_decode_plan([kv_len] * b, num_heads=12, q_len=1, target_ctas=b * split)
+    assert p.splits.tolist() == [split] * b
+
+
+def test_tiny_plan():
+    t = _golden()["tiny"]
+    p = mla.mla_decode_plan([t["kv_len"]], num_heads=12, q_len=t["q_len"], target_ctas=t["target"])
+    assert p.splits.tolist() == [t["splits"]] and p.chunks.tolist() == [1024]
+
+
+@pytest.mark.parametrize("lens,H,q", [
+    ([1048576] * 16, 12, 1), ([1048576] * 16, 12, 8), ([131072] * 4, 12, 8), ([4096], 12, 1),
+    ([131072], 12, 8), ([1048576], 96, 8), ([1024, 131072, 5000, 77777, 1048576], 12, 1),
+    ([8] * 3, 12, 8), ([1], 1, 1),
+])
+@pytest.mark.parametrize("sm_count", [152, 148, 7])
+def test_gb300_planner_invariants(lens, H, q, sm_count):
+    p = mla.mla_decode_plan(lens, num_heads=H, q_len=q, sm_count=sm_count)
+    L = np.asarray(lens, dtype=np.int64)
+    assert np.all(p.chunks % 128 == 0) and np.all(p.chunks >= 128)
+    assert np.all(p.splits >= 1) and np.all(p.splits <= mla.MAX_SPLITS)
+    assert np.all(p.splits * p.chunks.astype(np.int64) >= L)
+    assert np.all((p.splits - 1) * p.chunks.astype(np.int64) < L)
+    assert p.kv_split in (1, 2, 4, 8, 16) and p.kv_split <= max(1, p.max_splits)
+    assert p.workspace_bytes == mla.mla_decode_workspace_size(len(lens), q, H, p.max_splits)
+
+
+def test_gb300_planner_fills_one_wave_for_uniform_long_batch():
+    p = mla.mla_decode_plan([1048576] * 16, num_heads=12, q_len=1, sm_count=152)
+    ctas = int(p.splits.sum())
+    # Whole waves of 152 CTAs, at least 90% busy.
+    waves = -(-ctas // 152)
+    assert ctas >= 0.9 * waves * 152
+
+
+def test_skewed_batch_gets_common_chunk():
+    lens = [1048576] + [2048] * 7
+    p = mla.mla_decode_plan(lens, num_heads=12, q_len=1, sm_count=152)
+    assert len(set(p.chunks.tolist())) == 1
+    assert p.splits[0] > 8 * p.splits[1]
+
+
+@pytest.mark.parametrize("bad", [
+    dict(kv_lens=[4, 10], q_len=8),       # kv_len below q_len
+    dict(kv_lens=[0], q_len=1),           # empty request
+    dict(kv_lens=[100], q_len=0),
+])
+def test_plan_rejects_bad_arguments(bad):
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_plan(bad["kv_lens"], num_heads=12, q_len=bad["q_len"], sm_count=152)
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG
+
+
+def test_plan_rejects_too_many_rows():
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_plan([4096], num_heads=256, q_len=8, sm_count=152)
+    assert e.value.status == mla.MLA_ERR_UNSUPPORTED
+
+
+def test_plan_needs_sm_count_without_target():
+    with pytest.raises(mla.MlaError):
+        mla.mla_decode_plan([4096], num_heads=12, q_len=1, sm_count=0, target_ctas=0)
