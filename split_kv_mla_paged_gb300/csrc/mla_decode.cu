@@ -32,6 +32,7 @@
 //    the rare O correction and the epilogue.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -95,8 +96,14 @@ struct Cfg {
   static constexpr uint32_t kQ = kStages * kTileBytes;
   static constexpr uint32_t kQBytes = NR * MLA_HEAD_DIM;
   static constexpr uint32_t kP = kQ + kQBytes;
-  static constexpr uint32_t kPBytes = NR * kTileTokens;  // one P^T buffer
-  static constexpr uint32_t kAux = kP + 2 * kPBytes;
+  // One P^T buffer holds the E4M3 high part and the E4M3 residual ("lo").
+  static constexpr uint32_t kPHalf = NR * kTileTokens;
+  static constexpr uint32_t kPBytes = 2 * kPHalf;
+  static constexpr uint32_t kAuxBytes = 160 + 40 * NR;
+  // Double-buffer P when shared memory allows (NR <= 64), else one buffer.
+  static constexpr int NPB =
+      (kP + 2 * kPBytes + kAuxBytes + 1024 <= 232448u) ? 2 : 1;
+  static constexpr uint32_t kAux = kP + NPB * kPBytes;
   // aux: 16 mbarriers, tmem slot, flags, reductions
   static constexpr uint32_t kBars = kAux;              // 16 x 8 B
   static constexpr uint32_t kTmemSlot = kAux + 128;     // 4 B
@@ -106,7 +113,9 @@ struct Cfg {
   static constexpr uint32_t kKref = kRedSum + 16 * NR;  // NR floats
   static constexpr uint32_t kAlpha = kKref + 4 * NR;    // NR floats
   static constexpr uint32_t kEnd = kAlpha + 4 * NR;
+  static_assert(kEnd - kAux <= kAuxBytes, "aux layout");
   static constexpr uint32_t kSmemBytes = kEnd + 1024;   // + alignment slack
+  static_assert(kSmemBytes <= 232448u, "shared memory");
 };
 
 // Barrier indices inside the aux block.
@@ -144,6 +153,23 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Two E4M3 codes (low byte = element 0) back to floats (exact).
+__device__ __forceinline__ float2 unpack_e4m3x2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+// P as a two-term E4M3 sum: hi = e4m3(p), lo = e4m3(p - hi).  p - hi is exact
+// in fp32, and hi + lo carries p to ~2^-8 relative (E4M3 keeps 3 mantissa bits).
+__device__ __forceinline__ void split_e4m3x4(const float* p, uint32_t& hi, uint32_t& lo) {
+  hi = pack_e4m3x4(p[0], p[1], p[2], p[3]);
+  const float2 h01 = unpack_e4m3x2(static_cast<uint16_t>(hi & 0xFFFFu));
+  const float2 h23 = unpack_e4m3x2(static_cast<uint16_t>(hi >> 16));
+  lo = pack_e4m3x4(p[0] - h01.x, p[1] - h01.y, p[2] - h23.x, p[3] - h23.y);
 }
 
 // Warp reduce-scatter over N per-lane values (one per row): afterwards lane
@@ -370,8 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     auto issue_pv = [&](int j) -> bool {
-      const int pb = j & 1;
-      bool w = mbar_wait(bar(BAR_PFULL0 + pb), (j >> 1) & 1, kWaitLimitCycles);
+      const int pb = (C::NPB == 2) ? (j & 1) : 0;
+      const int use = (C::NPB == 2) ? (j >> 1) : j;
+      bool w = mbar_wait(bar(BAR_PFULL0 + pb), use & 1, kWaitLimitCycles);
       w = __all_sync(0xffffffffu, w);
       if (!w) return false;
       if (lane == 0) {
@@ -384,8 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t a = smem_desc(kv + d * kLatBlockBytes + ks * 4096, 16384, 1024,
                                          kLayoutSW128);
-            const uint64_t bd = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
-            umma_f8(tmem + C::kOCol + d * NR, a, bd, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+            const uint64_t bhi = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
+            const uint64_t blo = smem_desc(pbuf + C::kPHalf + ks * 512, 128, 2048, kLayoutNone);
+            umma_f8(tmem + C::kOCol + d * NR, a, bhi, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+            umma_f8(tmem + C::kOCol + d * NR, a, blo, kIdPV, 1u);
           }
         }
         umma_commit(bar(BAR_EMPTY0 + (j & 1)));
@@ -584,21 +613,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < NR; ++k) t[k] = softmax_weight(t[k], kref[k]);
       // P^T (E4M3) into shared memory, MN-major: [NR/16][128 tokens][16 rows].
-      const int pb = i & 1;
-      if (ok && i >= 2) {
-        ok = mbar_wait(bar(BAR_PFREE0 + pb), ((i >> 1) - 1) & 1, kWaitLimitCycles);
+      const int pb = (C::NPB == 2) ? (i & 1) : 0;
+      const int puse = (C::NPB == 2) ? (i >> 1) : i;
+      if (ok && puse >= 1) {
+        // With one P buffer this waits for PV(i-1); the barrier is then at
+        // most one phase behind (s_full(i) implies PV(i-2) completed).
+        ok = mbar_wait(bar(BAR_PFREE0 + pb), (puse - 1) & 1, kWaitLimitCycles);
         ok = __all_sync(0xffffffffu, ok);
       }
       if (ok) {
         uint8_t* pbuf = base + C::kP + pb * C::kPBytes;
 #pragma unroll
         for (int g = 0; g < NR / 16; ++g) {
-          uint4 v;
-          v.x = pack_e4m3x4(t[g * 16 + 0], t[g * 16 + 1], t[g * 16 + 2], t[g * 16 + 3]);
-          v.y = pack_e4m3x4(t[g * 16 + 4], t[g * 16 + 5], t[g * 16 + 6], t[g * 16 + 7]);
-          v.z = pack_e4m3x4(t[g * 16 + 8], t[g * 16 + 9], t[g * 16 + 10], t[g * 16 + 11]);
-          v.w = pack_e4m3x4(t[g * 16 + 12], t[g * 16 + 13], t[g * 16 + 14], t[g * 16 + 15]);
-          *reinterpret_cast<uint4*>(pbuf + g * 2048 + tok_lane * 16) = v;
+          uint4 vh, vl;
+          split_e4m3x4(&t[g * 16 + 0], vh.x, vl.x);
+          split_e4m3x4(&t[g * 16 + 4], vh.y, vl.y);
+          split_e4m3x4(&t[g * 16 + 8], vh.z, vl.z);
+          split_e4m3x4(&t[g * 16 + 12], vh.w, vl.w);
+          *reinterpret_cast<uint4*>(pbuf + g * 2048 + tok_lane * 16) = vh;
+          *reinterpret_cast<uint4*>(pbuf + C::kPHalf + g * 2048 + tok_lane * 16) = vl;
         }
         fence_proxy_async_smem();
         tc_fence_before();

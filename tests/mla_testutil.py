@@ -69,16 +69,3 @@ def assert_parity(out_bf16, lse, out_ref, lse_ref, what="", o_tol=None):
     assert lerr <= LSE_ABS, f"{what}: max |LSE err| {lerr:.3e} > {LSE_ABS}"
     return worst, lerr
 
-
-def peaked_tolerance(inp):
-    """Bound for strongly peaked rows, derived from the arithmetic.
-
-    The PV product uses E4M3 weights: each weight carries a relative rounding
-    error of at most 2^-4, while the normaliser is the unrounded sum, so
-    |O_gpu - O| <= 2^-4 * max_j |v_j|, plus the BF16 store (2^-8 relative) and
-    the absolute 2e-3 term.
-    """
-    from oracle import e4m3_decode
-    vmax = float(np.nanmax(np.abs(e4m3_decode(np.arange(256, dtype=np.uint8))[
-        np.unique(inp.kv[..., :512].cpu().numpy())])))
-    return 2.0 ** -4 * vmax * (1 + 2.0 ** -8) + O_ABS

@@ -7,7 +7,7 @@ import oracle
 import split_kv_mla_paged_gb300 as mla
 from split_kv_mla_paged_gb300 import build as mla_build
 from synth import SOFTMAX_SCALE, WORKLOADS, decode_inputs, merge_partials, workload_inputs
-from mla_testutil import PLAN_ABS, assert_parity, oracle_rows, peaked_tolerance, run_decode
+from mla_testutil import PLAN_ABS, assert_parity, oracle_rows, run_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -77,9 +77,8 @@ def test_parity_pages_planner_targets(target):
 def test_parity_scales_and_peaked_softmax():
     inp = decode_inputs(1, 12, 2, [3333], seed=8)
     _full_check(inp, True, 0.11, q_scale=1.5, kv_scale=0.75)
-    # Large logits: many reference moves and strongly peaked rows, checked
-    # against the bound the E4M3 weights allow (see peaked_tolerance).
-    _full_check(inp, False, 1.0, o_tol=peaked_tolerance(inp))
+    # Large logits: many reference moves and strongly peaked rows.
+    _full_check(inp, False, 1.0)
 
 
 def test_split_plans_agree_in_fp32():
