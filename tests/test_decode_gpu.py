@@ -139,8 +139,11 @@ def test_merge_against_oracle(rows, S, kv_split):
     l = lse.cpu().numpy()
     e = rows // 2
     assert l[e] == -np.inf and np.all(f[e] == 0.0)
-    keep = np.arange(rows) != e
-    assert np.max(np.abs(l[keep] - ref_l[keep])) <= 1e-5
+    # Rows whose slots all came out empty (the forced one, or by chance) give
+    # -inf on both sides; the others agree to fp32 rounding.
+    empty = ref_l == -np.inf
+    assert np.array_equal(l == -np.inf, empty)
+    assert np.max(np.abs(l[~empty] - ref_l[~empty])) <= 1e-5
     assert torch.equal(out_f32.to(torch.bfloat16), out)
 
 
