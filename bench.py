@@ -125,6 +125,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank value over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -132,8 +143,10 @@ def dist_env():
     return world, rank, local
 
 
-def cpu_oracle_sample(inp, w, rows_per_sample: int, softmax_scale: float):
-    """Time the oracle on the first `rows_per_sample` rows; return (seconds, rows, threads)."""
+def cpu_oracle_sample(inp, w, rows_per_sample: int, softmax_scale: float, tokens: int = 0):
+    """Time the oracle on the first `rows_per_sample` rows, each over its first
+    `tokens` keys (0 = the full KV length).  Returns (seconds, row-tokens done,
+    threads); the work per (row, key) is uniform, so time scales by row-tokens."""
     import numpy as np
     import torch
     import oracle
@@ -145,27 +158,34 @@ def cpu_oracle_sample(inp, w, rows_per_sample: int, softmax_scale: float):
     batches = []
     for b in range(n_req):
         L = int(inp.kv_lens[b])
-        n_pages = (L + 31) // 32
+        n_tok = L if tokens <= 0 else min(L, tokens)
+        n_pages = (n_tok + 31) // 32
         pages = inp.page_table[b, :n_pages].to(torch.int64).to(inp.kv.device)
         kv_b = inp.kv[pages].cpu().numpy()
         q_b = inp.q[b:b + 1].cpu().numpy()
         table = np.arange(n_pages, dtype=np.int32)[None, :]
         sel = rows[(rows // per_req) == b] - b * per_req
-        batches.append((q_b, kv_b, table, np.array([L], dtype=np.int32), sel))
+        # Causal rows see up to L - q_len + qi + 1 keys; the sample keeps the
+        # first n_tok of them (all visible when n_tok <= L - q_len + 1).
+        batches.append((q_b, kv_b, table, np.array([L], dtype=np.int32), sel, n_tok))
     threads = oracle.max_threads()
     t0 = time.perf_counter()
     done = 0
-    for q_b, kv_b, table, lens, sel in batches:
+    for q_b, kv_b, table, lens, sel, n_tok in batches:
         oracle.decode_rows(q_b, kv_b, table, lens, q_len=q_len, num_heads=H, causal=w["causal"],
-                           softmax_scale=softmax_scale, rows=sel)
-        done += len(sel)
+                           softmax_scale=softmax_scale, rows=sel, tok_begin=0,
+                           tok_end=n_tok if n_tok < int(lens[0]) else -1)
+        done += len(sel) * n_tok
     return time.perf_counter() - t0, done, threads
 
 
 def run_reference(args, w, world, rank):
-    """The oracle, as it stands, on the host cores: each step a bounded sample."""
+    """The oracle, as it stands, on the host cores: each step a bounded sample
+    (one row per host thread, over a prefix of the KV range sized so that the
+    whole run takes about --ref-budget-s seconds), scaled by row-tokens."""
     import torch
     from synth import SOFTMAX_SCALE, workload_inputs
+    import oracle
     if world > 1 and rank != 0:
         return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -175,16 +195,22 @@ def run_reference(args, w, world, rank):
         inp = decode_inputs(1, w["num_heads"], w["q_len"], w["kv_lens"][:1], w["seed"])
     else:
         inp = workload_inputs(args.workload, device=dev)
-    rows_total = w["batch"] * w["num_heads"] * w["q_len"]
-    sample_rows = args.ref_rows
+    total_row_tokens = sum(int(L) for L in w["kv_lens"]) * w["num_heads"] * w["q_len"]
+    threads = oracle.max_threads()
+    rows = min(threads, w["num_heads"] * w["q_len"])
+    L0 = int(w["kv_lens"][0])
+    cal_tokens = min(L0, 16384)
+    t_cal, _, _ = cpu_oracle_sample(inp, w, rows, SOFTMAX_SCALE, tokens=cal_tokens)
+    per_step = args.ref_budget_s / (args.steps + args.warmup)
+    tokens = int(max(1024, min(L0, cal_tokens * per_step / max(t_cal, 1e-6))))
     times = []
     for k in range(args.warmup + args.steps):
-        t, done, threads = cpu_oracle_sample(inp, w, sample_rows, SOFTMAX_SCALE)
+        t, done, threads = cpu_oracle_sample(inp, w, rows, SOFTMAX_SCALE, tokens=tokens)
         if k >= args.warmup:
-            times.append(t / done * rows_total * 1e6)
+            times.append(t / done * total_row_tokens * 1e6)
     value = statistics.mean(times)
-    sample = (f"{sample_rows} of {rows_total} rows per step (request 0, all heads), "
-              f"KV length {w['kv_lens'][0]}; time scaled by rows")
+    sample = (f"{rows} rows of request 0 over their first {tokens} of {L0} keys per step; "
+              f"time scaled by row-keys to the whole call")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
@@ -211,7 +237,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-rows", type=int, default=24,
                     help="rows of the oracle CPU baseline sample (0 disables it)")
-    ap.add_argument("--ref-rows", type=int, default=12)
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="wall-clock budget of the whole --impl reference run")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -298,11 +325,7 @@ def main():
     total_ms = start.elapsed_time(end)
     split_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     merge_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
-    us_per_call = total_ms * 1e3 / K
-    if world > 1:
-        t = torch.tensor([us_per_call], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        us_per_call = float(t.item())
+    us_per_call = max_over_ranks(total_ms * 1e3 / K, dev)
     mla.mla_decode_status(ws, stream)
 
     # ---- end to end through the public API with host buffers ----
@@ -338,11 +361,7 @@ def main():
     for _ in range(args.e2e_steps):
         e2e_step()
     torch.cuda.synchronize(dev)
-    e2e_us = (time.perf_counter() - t0) * 1e6 / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_us], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_us = float(t.item())
+    e2e_us = max_over_ranks((time.perf_counter() - t0) * 1e6 / args.e2e_steps, dev)
 
     # ---- roofline of the dominant kernel (split-KV) ----
     kv_bytes = inp.kv_bytes()
@@ -354,10 +373,11 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and args.cpu_rows > 0:
         t, done, threads = cpu_oracle_sample(inp, w, args.cpu_rows, SOFTMAX_SCALE)
-        cpu = {"value": t / done * inp.rows * 1e6, "unit": UNIT, "cores": threads,
+        total = sum(lens) * H * q_len
+        cpu = {"value": t / done * total * 1e6, "unit": UNIT, "cores": threads,
                "kind": "oracle",
-               "sample": f"{done} of {inp.rows} rows (requests 0-1, all heads, full KV length), "
-                         f"time scaled by rows"}
+               "sample": f"first {args.cpu_rows} of {inp.rows} rows over their full KV length "
+                         f"({t:.1f} s); time scaled by row-keys to the whole call"}
 
     if rank == 0:
         pub = PUBLISHED_US.get(args.workload)

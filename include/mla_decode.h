@@ -184,6 +184,14 @@ MLA_API int mla_merge(const float* partial_o, const float* partial_ml, int32_t r
  * clears it. */
 MLA_API int mla_decode_status(void* workspace, void* stream);
 
+/* Test hook.  Sets the limit, in SM clock cycles, of the split-KV kernel's
+ * pipeline waits for launches made after the call (0 restores the default of
+ * about 2 s).  A tiny limit makes those waits run out: the kernel then records
+ * MLA_ERR_TIMEOUT in the status word, lets its own copies and MMAs finish
+ * (those drains keep the long limit), frees TMEM and exits, leaving the
+ * context usable.  Not for production use. */
+MLA_API void mla_debug_set_wait_limit(long long cycles);
+
 /* Message for the last non-OK status returned on this thread. */
 MLA_API const char* mla_last_error(void);
 

@@ -37,7 +37,7 @@ _STATUS_NAMES = {
 }
 EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init",
                     "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
-                    "mla_decode_status", "mla_last_error")
+                    "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
@@ -89,6 +89,8 @@ def load_library() -> ctypes.CDLL:
         lib.mla_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
         lib.mla_decode_status.restype = ctypes.c_int
         lib.mla_decode_status.argtypes = [vp, vp]
+        lib.mla_debug_set_wait_limit.restype = None
+        lib.mla_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
         lib.mla_last_error.restype = ctypes.c_char_p
         lib.mla_last_error.argtypes = []
         _lib = lib
@@ -199,6 +201,11 @@ def mla_merge(partial_o, partial_ml, rows: int, num_ctas_kv: int, kv_split: int,
     _check(lib.mla_merge(_ptr(partial_o), _ptr(partial_ml), int(rows), int(num_ctas_kv),
                          int(kv_split), _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
                          _stream_handle(stream)))
+
+
+def mla_debug_set_wait_limit(cycles: int) -> None:
+    """Test hook: limit of the kernel's pipeline waits (0 = default)."""
+    load_library().mla_debug_set_wait_limit(int(cycles))
 
 
 def mla_decode_status(workspace, stream=None) -> int:

@@ -39,6 +39,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -74,6 +75,7 @@ struct DecodeParams {
   int32_t rows_per_group;  // RG
   float c_log2;            // softmax_scale * q_scale * kv_scale * log2(e)
   float kv_scale;
+  long long wait_cycles;   // limit of the pipeline waits (drains always use the long limit)
   int* status;
   float* ws_ml;
   float* ws_o;
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int st = i & 1;
       bool ok = true;
-      if (i >= kStages) ok = mbar_wait(bar(BAR_EMPTY0 + st), ((i >> 1) - 1) & 1, kWaitLimitCycles);
+      if (i >= kStages) ok = mbar_wait(bar(BAR_EMPTY0 + st), ((i >> 1) - 1) & 1, p.wait_cycles);
       ok = __all_sync(0xffffffffu, ok && !*abort_flag);
       if (!ok) {
         if (lane == 0) {
@@ -382,13 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int k = max(0, issued - kStages); k < issued; ++k)
         mbar_wait(bar(BAR_FULL0 + (k & 1)), (k >> 1) & 1, kWaitLimitCycles);
+      mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ================= MMA issuer =================
     constexpr uint32_t kIdQK = idesc_e4m3(128, NR, 0, 0);
     constexpr uint32_t kIdPV = idesc_e4m3(128, NR, 1, 1);
-    bool ok = mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
+    bool ok = mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles);
     auto fail = [&]() {
       if (lane == 0) {
         report(p.status, MLA_ERR_TIMEOUT);
@@ -398,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_pv = [&](int j) -> bool {
       const int pb = (C::NPB == 2) ? (j & 1) : 0;
       const int use = (C::NPB == 2) ? (j >> 1) : j;
-      bool w = mbar_wait(bar(BAR_PFULL0 + pb), use & 1, kWaitLimitCycles);
+      bool w = mbar_wait(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles);
       w = __all_sync(0xffffffffu, w);
       if (!w) return false;
       if (lane == 0) {
@@ -428,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) fail();
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int st = i & 1;
-      bool w = mbar_wait(bar(BAR_FULL0 + st), (i >> 1) & 1, kWaitLimitCycles);
+      bool w = mbar_wait(bar(BAR_FULL0 + st), (i >> 1) & 1, p.wait_cycles);
       const int sb = (C::NS == 2) ? (i & 1) : 0;
       const int use = (C::NS == 2) ? (i >> 1) : i;
-      if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1, kWaitLimitCycles);
+      if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles);
       w = __all_sync(0xffffffffu, w && !*abort_flag);
       if (!w) {
         fail();
@@ -517,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < n_tiles; ++i) {
       const int sb = (C::NS == 2) ? (i & 1) : 0;
       const int use = (C::NS == 2) ? (i >> 1) : i;
-      if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, kWaitLimitCycles);
+      if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
       ok = __all_sync(0xffffffffu, ok);
       float t[NR];
       if (ok) {
@@ -588,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Rescale the O^T columns of rows whose reference moved (rare).
         // o_done is at most one phase behind here: s_full(i) implies PV(i-2)
         // completed, and PV(i) is not issued before this tile's p_full.
-        ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, kWaitLimitCycles);
+        ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, p.wait_cycles);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
           tc_fence_after();
@@ -618,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && puse >= 1) {
         // With one P buffer this waits for PV(i-1); the barrier is then at
         // most one phase behind (s_full(i) implies PV(i-2) completed).
-        ok = mbar_wait(bar(BAR_PFREE0 + pb), (puse - 1) & 1, kWaitLimitCycles);
+        ok = mbar_wait(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles);
         ok = __all_sync(0xffffffffu, ok);
       }
       if (ok) {
@@ -670,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     named_bar_sync(kSoftmaxBarrier, 128);
     // The MMA warp commits BAR_FINAL once, after its last MMA.
-    bool fin = mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
+    bool fin = mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
     fin = __all_sync(0xffffffffu, fin);
     if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
     if (ok && fin && n_tiles > 0) {
@@ -899,6 +902,9 @@ static cudaError_t launch_merge(const MergeParams& mp, int kv_split, cudaStream_
   return cudaGetLastError();
 }
 
+// Test hook: limit of the pipeline waits for later launches (0 = default).
+static std::atomic<long long> g_wait_cycles{0};
+
 static bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
@@ -1000,6 +1006,10 @@ static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
   prm.c_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * kv_scale *
                                   1.4426950408889634);
   prm.kv_scale = kv_scale;
+  {
+    const long long w = g_wait_cycles.load();
+    prm.wait_cycles = w > 0 ? w : kWaitLimitCycles;
+  }
   prm.status = reinterpret_cast<int*>(ws);
   prm.ws_ml = reinterpret_cast<float*>(ws + ws_ml_offset());
   prm.ws_o = reinterpret_cast<float*>(ws + ws_o_offset(rows_total, max_splits));
@@ -1096,6 +1106,10 @@ extern "C" int mla_decode_merge(const void* q_fp8, const void* kv_pages_fp8, int
   int rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode_merge", &dl);
   if (rc != MLA_OK) return rc;
   return launch_decode_merge(dl, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" void mla_debug_set_wait_limit(long long cycles) {
+  g_wait_cycles.store(cycles > 0 ? cycles : 0);
 }
 
 extern "C" int mla_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {

@@ -175,6 +175,25 @@ def test_inconsistent_plan_is_reported():
     assert e.value.status == mla.MLA_ERR_INVALID_ARG
 
 
+def test_wait_timeout_is_reported_and_context_survives():
+    # A tiny wait limit makes the pipeline waits run out; the kernel must
+    # record MLA_ERR_TIMEOUT, drain its own work and exit, and the next call
+    # must run normally.
+    inp = decode_inputs(1, 12, 8, [60000], seed=14)
+    mla.mla_debug_set_wait_limit(64)
+    try:
+        with pytest.raises(mla.MlaError) as e:
+            run_decode(inp, True, SOFTMAX_SCALE)
+        assert e.value.status == mla.MLA_ERR_TIMEOUT
+    finally:
+        mla.mla_debug_set_wait_limit(0)
+    out, lse, _ = run_decode(inp, True, SOFTMAX_SCALE)
+    rows = np.array([0, 17, 50, 95])
+    ref_o, ref_l = oracle_rows(inp, rows, True, SOFTMAX_SCALE)
+    assert_parity(out.reshape(-1, 512)[torch.from_numpy(rows).cuda()],
+                  lse.reshape(-1)[torch.from_numpy(rows).cuda()], ref_o, ref_l)
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 def _sample_rows(inp, n, seed):
