@@ -184,6 +184,36 @@ MLA_API int mla_merge(const float* partial_o, const float* partial_ml, int32_t r
  * clears it. */
 MLA_API int mla_decode_status(void* workspace, void* stream);
 
+/*
+ * Decode without a workspace argument, for callers that cannot allocate
+ * device memory (a host runtime that owns every allocation and forbids side
+ * allocations, or a latency-critical path that cannot afford cudaMalloc's
+ * implicit synchronisation).  The pages have no counterpart to this call.
+ *
+ * Same arguments and results as mla_decode, minus workspace/workspace_bytes.
+ * The scratch (status word and split partials) is a fixed, file-scope device
+ * array of MLA_STATIC_WS_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.  A call whose scratch
+ * (mla_decode_workspace_size) would exceed it returns
+ * MLA_ERR_WORKSPACE_TOO_SMALL.  The call allocates nothing.
+ *
+ * The first call on a device resolves the array's device address on that
+ * device (the current device), so make that first call before any stream
+ * capture.  All calls share the one array: calls that overlap on the GPU (on
+ * different streams, or from different threads) race on it and must be
+ * serialised by the caller.  Each call resets the status word; the device
+ * status of these calls is not readable through mla_decode_status.
+ */
+#define MLA_STATIC_WS_BYTES (16u * 1024u * 1024u)
+MLA_API int mla_decode_static_ws(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                                 const int32_t* page_table, int32_t max_pages_per_req,
+                                 const int32_t* kv_lens, const int32_t* splits,
+                                 const int32_t* chunks, int32_t max_splits, int32_t kv_split,
+                                 int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
+                                 float q_scale, float kv_scale, float softmax_scale,
+                                 void* out_bf16, float* lse_f32, float* out_f32_debug,
+                                 void* stream);
+
 /* Test hook.  Sets the limit, in SM clock cycles, of the split-KV kernel's
  * pipeline waits for launches made after the call (0 restores the default of
  * about 2 s).  A tiny limit makes those waits run out: the kernel then records

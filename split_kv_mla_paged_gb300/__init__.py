@@ -22,7 +22,7 @@ __all__ = [
     "MLA_ERR_CUDA", "MLA_ERR_TIMEOUT", "MlaError", "Plan", "load_library", "library_path",
     "mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init", "mla_decode",
     "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
-    "decode", "merge", "EXPORTED_SYMBOLS",
+    "mla_decode_static_ws", "decode", "merge", "EXPORTED_SYMBOLS",
 ]
 
 MLA_OK = 0
@@ -37,7 +37,8 @@ _STATUS_NAMES = {
 }
 EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init",
                     "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
-                    "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit")
+                    "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit",
+                    "mla_decode_static_ws")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
@@ -89,6 +90,9 @@ def load_library() -> ctypes.CDLL:
         lib.mla_merge.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp]
         lib.mla_decode_status.restype = ctypes.c_int
         lib.mla_decode_status.argtypes = [vp, vp]
+        lib.mla_decode_static_ws.restype = ctypes.c_int
+        lib.mla_decode_static_ws.argtypes = [vp, vp, i64, vp, i32, vp, vp, vp, i32, i32, i32, i32,
+                                             i32, i32, f32, f32, f32, vp, vp, vp, vp]
         lib.mla_debug_set_wait_limit.restype = None
         lib.mla_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
         lib.mla_last_error.restype = ctypes.c_char_p
@@ -201,6 +205,30 @@ def mla_merge(partial_o, partial_ml, rows: int, num_ctas_kv: int, kv_split: int,
     _check(lib.mla_merge(_ptr(partial_o), _ptr(partial_ml), int(rows), int(num_ctas_kv),
                          int(kv_split), _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
                          _stream_handle(stream)))
+
+
+def mla_decode_static_ws(q_fp8, kv_pages_fp8, num_pages: int, page_table,
+                         max_pages_per_req: int, kv_lens, splits, chunks, max_splits: int,
+                         kv_split: int, batch: int, q_len: int, num_heads: int, causal: bool,
+                         q_scale: float, kv_scale: float, softmax_scale: float, out_bf16,
+                         lse_f32=None, out_f32_debug=None, stream=None) -> None:
+    """mla_decode for callers that cannot allocate device memory.
+
+    The scratch lives in a fixed array inside the library
+    (MLA_STATIC_WS_BYTES = 16 MiB per GPU), so no workspace is passed.  The
+    first call on a device resolves that array's address and should come
+    before any stream capture; calls that overlap on the GPU race on the array.
+    """
+    lib = load_library()
+    _check(lib.mla_decode_static_ws(
+        _ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages), _ptr(page_table), int(max_pages_per_req),
+        _ptr(kv_lens), _ptr(splits), _ptr(chunks), int(max_splits), int(kv_split), int(batch),
+        int(q_len), int(num_heads), 1 if causal else 0, float(q_scale), float(kv_scale),
+        float(softmax_scale), _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
+        _stream_handle(stream)))
+
+
+STATIC_WS_BYTES = 16 * 1024 * 1024
 
 
 def mla_debug_set_wait_limit(cycles: int) -> None:

@@ -1108,6 +1108,84 @@ extern "C" int mla_decode_merge(const void* q_fp8, const void* kv_pages_fp8, int
   return launch_decode_merge(dl, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace mla {
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot call cudaMalloc: code running inside a host runtime that
+// owns every device allocation through its own planner and forbids side
+// allocations, or a latency-critical path where cudaMalloc's implicit
+// device-wide synchronisation is not acceptable.  For them this entry point
+// takes its scratch (the status word and the split partials) from a fixed
+// array that lives in the library image.  Every GPU that loads the library
+// holds the array until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_static_ws[MLA_STATIC_WS_BYTES];
+
+// Device address of g_static_ws on each device (host code cannot use the
+// symbol itself as a device pointer), resolved once per device.
+static std::mutex g_static_ws_mu;
+static void* g_static_ws_ptr[64] = {nullptr};
+
+static int static_ws_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("mla_decode_static_ws: cudaGetDevice", e);
+  if (dev < 0 || dev >= 64) {
+    set_error("mla_decode_static_ws: device ordinal above 63");
+    return MLA_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_static_ws_mu);
+  if (!g_static_ws_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_ws);
+    if (e != cudaSuccess || !ptr)
+      return cuda_fail("mla_decode_static_ws: cudaGetSymbolAddress", e);
+    g_static_ws_ptr[dev] = ptr;
+  }
+  *out = g_static_ws_ptr[dev];
+  return MLA_OK;
+}
+
+}  // namespace mla
+
+extern "C" int mla_decode_static_ws(const void* q_fp8, const void* kv_pages_fp8,
+                                    int64_t num_pages, const int32_t* page_table,
+                                    int32_t max_pages_per_req, const int32_t* kv_lens,
+                                    const int32_t* splits, const int32_t* chunks,
+                                    int32_t max_splits, int32_t kv_split, int32_t batch,
+                                    int32_t q_len, int32_t num_heads, int32_t causal,
+                                    float q_scale, float kv_scale, float softmax_scale,
+                                    void* out_bf16, float* lse_f32, float* out_f32_debug,
+                                    void* stream) {
+  if (batch >= 1 && q_len >= 1 && num_heads >= 1 && max_splits >= 1) {
+    const size_t need = ws_total(static_cast<int64_t>(batch) * q_len * num_heads, max_splits);
+    if (need > MLA_STATIC_WS_BYTES) {
+      set_error("mla_decode_static_ws: this call needs " + std::to_string(need) +
+                " bytes of scratch, above the fixed MLA_STATIC_WS_BYTES (" +
+                std::to_string(static_cast<size_t>(MLA_STATIC_WS_BYTES)) +
+                "); use mla_decode with a caller-owned workspace");
+      return MLA_ERR_WORKSPACE_TOO_SMALL;
+    }
+  }
+  void* workspace = nullptr;
+  int rc = static_ws_address(&workspace);
+  if (rc != MLA_OK) return rc;
+  const size_t workspace_bytes = MLA_STATIC_WS_BYTES;
+  DecodeLaunch dl;
+  rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode_static_ws", &dl);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the status word must start
+  // at zero (the partials are always written before they are read).
+  cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int), st);
+  if (e != cudaSuccess) return cuda_fail("mla_decode_static_ws: status reset", e);
+  rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
+  if (rc != MLA_OK) return rc;
+  return launch_decode_merge(dl, st);
+}
+
 extern "C" void mla_debug_set_wait_limit(long long cycles) {
   g_wait_cycles.store(cycles > 0 ? cycles : 0);
 }
