@@ -49,7 +49,6 @@
 namespace mla {
 
 constexpr int kThreads = 192;
-constexpr int kStages = 2;
 constexpr int kTileTokens = 128;
 constexpr uint32_t kTileBytes = kTileTokens * MLA_HEAD_DIM;  // 73728
 constexpr uint32_t kLatBlockBytes = kTileTokens * 128;       // 16384: one 128-dim block
@@ -94,23 +93,28 @@ struct Cfg {
       : kTmemUsed <= 256 ? 256 : 512;
   static constexpr uint32_t kOCol = NS * NR;
   // Shared memory, offsets from a 1024-byte aligned base.
-  static constexpr uint32_t kKV = 0;
-  static constexpr uint32_t kQ = kStages * kTileBytes;
+  static constexpr uint32_t kPHalf = NR * kTileTokens;  // one E4M3 term of P^T
+  static constexpr uint32_t kPBytes = 2 * kPHalf;       // hi + lo
+  static constexpr uint32_t kAuxBytes = 224 + 40 * NR;
   static constexpr uint32_t kQBytes = NR * MLA_HEAD_DIM;
+  // Three KV stages fit when P^T can live in the rope block of its own stage
+  // (QK has consumed that block before P is written): NR = 16.  Otherwise two
+  // stages and separate P^T buffers (two when they fit, else one).
+  static constexpr bool kPInStage =
+      kPBytes <= kTileTokens * 64 &&
+      3 * kTileBytes + kQBytes + kAuxBytes + 1024 <= 232448u;
+  static constexpr int NST = kPInStage ? 3 : 2;
+  static constexpr uint32_t kKV = 0;
+  static constexpr uint32_t kQ = NST * kTileBytes;
   static constexpr uint32_t kP = kQ + kQBytes;
-  // One P^T buffer holds the E4M3 high part and the E4M3 residual ("lo").
-  static constexpr uint32_t kPHalf = NR * kTileTokens;
-  static constexpr uint32_t kPBytes = 2 * kPHalf;
-  static constexpr uint32_t kAuxBytes = 160 + 40 * NR;
-  // Double-buffer P when shared memory allows (NR <= 64), else one buffer.
-  static constexpr int NPB =
-      (kP + 2 * kPBytes + kAuxBytes + 1024 <= 232448u) ? 2 : 1;
+  static constexpr int NPB = kPInStage ? 0
+                             : (kP + 2 * kPBytes + kAuxBytes + 1024 <= 232448u) ? 2 : 1;
   static constexpr uint32_t kAux = kP + NPB * kPBytes;
-  // aux: 16 mbarriers, tmem slot, flags, reductions
-  static constexpr uint32_t kBars = kAux;              // 16 x 8 B
-  static constexpr uint32_t kTmemSlot = kAux + 128;     // 4 B
-  static constexpr uint32_t kFlags = kAux + 144;        // 2 x 4 B
-  static constexpr uint32_t kRedMax = kAux + 160;       // 4 x NR floats
+  // aux: mbarriers, tmem slot, flags, reductions
+  static constexpr uint32_t kBars = kAux;               // 24 x 8 B
+  static constexpr uint32_t kTmemSlot = kAux + 192;     // 4 B
+  static constexpr uint32_t kFlags = kAux + 208;        // 3 x 4 B
+  static constexpr uint32_t kRedMax = kAux + 224;       // 4 x NR floats
   static constexpr uint32_t kRedSum = kRedMax + 16 * NR;
   static constexpr uint32_t kKref = kRedSum + 16 * NR;  // NR floats
   static constexpr uint32_t kAlpha = kKref + 4 * NR;    // NR floats
@@ -122,10 +126,10 @@ struct Cfg {
 
 // Barrier indices inside the aux block.
 enum : int {
-  BAR_FULL0 = 0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_QFULL, BAR_SFULL0, BAR_SFULL1,
-  BAR_SFREE0, BAR_SFREE1, BAR_PFULL0, BAR_PFULL1, BAR_PFREE0, BAR_PFREE1, BAR_ODONE,
-  BAR_FINAL, BAR_COUNT
+  BAR_FULL0 = 0, BAR_EMPTY0 = 3, BAR_QFULL = 6, BAR_SFULL0, BAR_SFULL1, BAR_SFREE0, BAR_SFREE1,
+  BAR_PFULL0, BAR_PFULL1, BAR_PFREE0, BAR_PFREE1, BAR_ODONE, BAR_FINAL, BAR_COUNT
 };
+static_assert(BAR_COUNT <= 24, "barrier slots");
 
 __device__ __forceinline__ void report(int* status, int code) {
   atomicCAS(status, 0, code);
@@ -278,10 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(BAR_FULL0), 1);
-    mbar_init(bar(BAR_FULL1), 1);
-    mbar_init(bar(BAR_EMPTY0), 1);
-    mbar_init(bar(BAR_EMPTY1), 1);
+    for (int k = 0; k < C::NST; ++k) {
+      mbar_init(bar(BAR_FULL0 + k), 1);
+      mbar_init(bar(BAR_EMPTY0 + k), 1);
+    }
     mbar_init(bar(BAR_QFULL), 1);
     mbar_init(bar(BAR_SFULL0), 1);
     mbar_init(bar(BAR_SFULL1), 1);
@@ -325,24 +329,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
     const int page0 = tok_begin / MLA_PAGE_SIZE;
     const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
-    int window = 0;
-    int issued = 0;
-    for (int i = 0; i < n_tiles; ++i) {
-      if ((i & 7) == 0) {
-        const int pi = page0 + i * 4 + lane;
-        int pg = 0;
-        if (pi < page_end) {
-          pg = pt[pi];
-          if (pg < 0 || pg >= p.num_pages) {
-            report(p.status, MLA_ERR_INVALID_ARG);
-            pg = 0;
-          }
+    // Page ids of 8 tiles (32 pages) per window, one per lane; the next
+    // window is fetched a window ahead so its latency is hidden.
+    auto load_window = [&](int w) -> int {
+      const int pi = page0 + w * 32 + lane;
+      int pg = 0;
+      if (pi < page_end) {
+        pg = pt[pi];
+        if (pg < 0 || pg >= p.num_pages) {
+          report(p.status, MLA_ERR_INVALID_ARG);
+          pg = 0;
         }
-        window = pg;
       }
-      const int st = i & 1;
+      return pg;
+    };
+    int window = load_window(0);
+    int window_next = load_window(1);
+    int issued = 0;
+    int st = 0, round = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      if (i > 0 && (i & 7) == 0) {
+        window = window_next;
+        window_next = load_window((i >> 3) + 1);
+      }
       bool ok = true;
-      if (i >= kStages) ok = mbar_wait(bar(BAR_EMPTY0 + st), ((i >> 1) - 1) & 1, p.wait_cycles);
+      if (round > 0) ok = mbar_wait(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles);
       ok = __all_sync(0xffffffffu, ok && !*abort_flag);
       if (!ok) {
         if (lane == 0) {
@@ -377,13 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       issued = i + 1;
+      if (++st == C::NST) {
+        st = 0;
+        ++round;
+      }
     }
     // Before the CTA can exit, the copies this warp issued must have landed
     // (they have, unless a wait elsewhere ran out).  The full barrier of a
     // stage is at most one phase behind the producer, so these waits are exact.
     if (lane == 0) {
-      for (int k = max(0, issued - kStages); k < issued; ++k)
-        mbar_wait(bar(BAR_FULL0 + (k & 1)), (k >> 1) & 1, kWaitLimitCycles);
+      for (int k = max(0, issued - C::NST); k < issued; ++k)
+        mbar_wait(bar(BAR_FULL0 + k % C::NST), (k / C::NST) & 1, kWaitLimitCycles);
       mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
     }
     __syncwarp();
@@ -398,16 +413,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
     };
-    auto issue_pv = [&](int j) -> bool {
-      const int pb = (C::NPB == 2) ? (j & 1) : 0;
-      const int use = (C::NPB == 2) ? (j >> 1) : j;
+    // PV of tile j, whose KV sits in stage jst.  p_full has two barriers
+    // (tiles alternate), so the softmax cannot run two phases ahead.
+    auto issue_pv = [&](int j, int jst) -> bool {
+      const int pb = (C::NPB == 1) ? 0 : (j & 1);
+      const int use = (C::NPB == 1) ? j : (j >> 1);
       bool w = mbar_wait(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles);
       w = __all_sync(0xffffffffu, w);
       if (!w) return false;
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t kv = sbase + C::kKV + (j & 1) * kTileBytes;
-        const uint32_t pbuf = sbase + C::kP + pb * C::kPBytes;
+        const uint32_t kv = sbase + C::kKV + jst * kTileBytes;
+        const uint32_t pbuf = C::kPInStage ? kv + kRopeOffset : sbase + C::kP + pb * C::kPBytes;
 #pragma unroll
         for (int d = 0; d < 4; ++d) {
 #pragma unroll
@@ -420,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_f8(tmem + C::kOCol + d * NR, a, blo, kIdPV, 1u);
           }
         }
-        umma_commit(bar(BAR_EMPTY0 + (j & 1)));
-        umma_commit(bar(BAR_PFREE0 + pb));
+        umma_commit(bar(BAR_EMPTY0 + jst));
+        if (!C::kPInStage) umma_commit(bar(BAR_PFREE0 + pb));
         umma_commit(bar(BAR_ODONE));
       }
       __syncwarp();
@@ -429,9 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) fail();
+    int st = 0, round = 0, prev_st = 0;
     for (int i = 0; ok && i < n_tiles; ++i) {
-      const int st = i & 1;
-      bool w = mbar_wait(bar(BAR_FULL0 + st), (i >> 1) & 1, p.wait_cycles);
+      bool w = mbar_wait(bar(BAR_FULL0 + st), round & 1, p.wait_cycles);
       const int sb = (C::NS == 2) ? (i & 1) : 0;
       const int use = (C::NS == 2) ? (i >> 1) : i;
       if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles);
@@ -484,15 +501,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (i > 0) {
-        if (!issue_pv(i - 1)) {
+        if (!issue_pv(i - 1, prev_st)) {
           fail();
           ok = false;
           break;
         }
       }
+      prev_st = st;
+      if (++st == C::NST) {
+        st = 0;
+        ++round;
+      }
     }
     if (ok && n_tiles > 0) {
-      if (!issue_pv(n_tiles - 1)) fail();
+      if (!issue_pv(n_tiles - 1, prev_st)) fail();
     }
     // One commit after everything this warp issued: the epilogue reads O^T
     // after it, and TMEM is released only after it.
@@ -616,16 +638,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < NR; ++k) t[k] = softmax_weight(t[k], kref[k]);
       // P^T (E4M3) into shared memory, MN-major: [NR/16][128 tokens][16 rows].
-      const int pb = (C::NPB == 2) ? (i & 1) : 0;
-      const int puse = (C::NPB == 2) ? (i >> 1) : i;
-      if (ok && puse >= 1) {
+      const int pb = (C::NPB == 1) ? 0 : (i & 1);
+      const int puse = (C::NPB == 1) ? i : (i >> 1);
+      if (ok && !C::kPInStage && puse >= 1) {
         // With one P buffer this waits for PV(i-1); the barrier is then at
         // most one phase behind (s_full(i) implies PV(i-2) completed).
         ok = mbar_wait(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles);
         ok = __all_sync(0xffffffffu, ok);
       }
       if (ok) {
-        uint8_t* pbuf = base + C::kP + pb * C::kPBytes;
+        // P^T of tile i goes to the rope block of its KV stage (consumed by
+        // QK(i), which s_full(i) reports complete) or to a P buffer.
+        uint8_t* pbuf = C::kPInStage
+                            ? base + C::kKV + (i % C::NST) * kTileBytes + kRopeOffset
+                            : base + C::kP + pb * C::kPBytes;
 #pragma unroll
         for (int g = 0; g < NR / 16; ++g) {
           uint4 vh, vl;
