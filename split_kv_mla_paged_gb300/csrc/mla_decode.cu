@@ -86,8 +86,14 @@ struct DecodeParams {
 template <int NR>
 struct Cfg {
   static_assert(NR % 16 == 0 && NR >= 16 && NR <= kMaxRowsPerCta, "NR");
-  static constexpr int NS = (2 * NR + 4 * NR <= 512) ? 2 : 1;  // S^T buffers in TMEM
-  static constexpr uint32_t kTmemUsed = NS * NR + 4 * NR;
+  // P^T = hi + lo.  With NR <= 48 both terms go through one PV MMA with
+  // N = 2*NR (O^T holds the hi and lo products side by side and the epilogue
+  // adds them), so V is read from shared memory once per tile; above that
+  // TMEM is too small and PV runs twice over V.
+  static constexpr bool kStack = NR <= 48;
+  static constexpr int OW = kStack ? 2 * NR : NR;  // O^T columns per latent block
+  static constexpr int NS = (2 * NR + 4 * OW <= 512) ? 2 : 1;  // S^T buffers in TMEM
+  static constexpr uint32_t kTmemUsed = NS * NR + 4 * OW;
   static constexpr uint32_t kTmemCols =
       kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
       : kTmemUsed <= 256 ? 256 : 512;
@@ -362,29 +368,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         break;
       }
-      int pages[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) pages[q] = __shfl_sync(0xffffffffu, window, (i & 7) * 4 + q);
+      // Lane q (< 4) takes the id of the tile's page q.
+      const int my_page = __shfl_sync(0xffffffffu, window, (i & 7) * 4 + (lane & 3));
+      const int tp0 = page0 + i * 4;
+      const uint32_t fb = bar(BAR_FULL0 + st);
       if (lane == 0) {
-        const int tp0 = page0 + i * 4;
         int nvalid = 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q) nvalid += (tp0 + q < page_end) ? 1 : 0;
-        const uint32_t fb = bar(BAR_FULL0 + st);
         mbar_arrive_expect_tx(fb, nvalid * kPageBytes);
+      }
+      __syncwarp();
+      // Lanes 0-3 issue one page each (5 boxes: 4 latent blocks + rope).
+      if (lane < 4 && tp0 + lane < page_end) {
         const uint32_t kv = sbase + C::kKV + st * kTileBytes;
+        const int row = my_page * MLA_PAGE_SIZE;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (tp0 + q < page_end) {
-            const int row = pages[q] * MLA_PAGE_SIZE;
-#pragma unroll
-            for (int d = 0; d < 4; ++d)
-              tma_load_2d_hint(kv + d * kLatBlockBytes + q * kPageLatBytes, &tm_kv_lat, d * 128,
-                               row, fb, pol);
-            tma_load_2d_hint(kv + kRopeOffset + q * kPageRopeBytes, &tm_kv_rope, MLA_LATENT_DIM,
-                             row, fb, pol);
-          }
-        }
+        for (int d = 0; d < 4; ++d)
+          tma_load_2d_hint(kv + d * kLatBlockBytes + lane * kPageLatBytes, &tm_kv_lat, d * 128,
+                           row, fb, pol);
+        tma_load_2d_hint(kv + kRopeOffset + lane * kPageRopeBytes, &tm_kv_rope, MLA_LATENT_DIM,
+                         row, fb, pol);
       }
       __syncwarp();
       issued = i + 1;
@@ -405,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ================= MMA issuer =================
     constexpr uint32_t kIdQK = idesc_e4m3(128, NR, 0, 0);
-    constexpr uint32_t kIdPV = idesc_e4m3(128, NR, 1, 1);
+    constexpr uint32_t kIdPV = idesc_e4m3(128, C::OW, 1, 1);
     bool ok = mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles);
     auto fail = [&]() {
       if (lane == 0) {
@@ -413,108 +417,125 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
     };
-    // PV of tile j, whose KV sits in stage jst.  p_full has two barriers
-    // (tiles alternate), so the softmax cannot run two phases ahead.
-    auto issue_pv = [&](int j, int jst) -> bool {
-      const int pb = (C::NPB == 1) ? 0 : (j & 1);
-      const int use = (C::NPB == 1) ? j : (j >> 1);
-      bool w = mbar_wait(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles);
-      w = __all_sync(0xffffffffu, w);
-      if (!w) return false;
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t kv = sbase + C::kKV + jst * kTileBytes;
-        const uint32_t pbuf = C::kPInStage ? kv + kRopeOffset : sbase + C::kP + pb * C::kPBytes;
+    // PV of tile j (KV in stage jst, P^T in buffer pb); lane 0 issues.
+    auto issue_pv = [&](int j, int jst, int pb) {
+      tc_fence_after();
+      const uint32_t kv = sbase + C::kKV + jst * kTileBytes;
+      const uint32_t pbuf = C::kPInStage ? kv + kRopeOffset : sbase + C::kP + pb * C::kPBytes;
 #pragma unroll
-        for (int d = 0; d < 4; ++d) {
+      for (int d = 0; d < 4; ++d) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t a = smem_desc(kv + d * kLatBlockBytes + ks * 4096, 16384, 1024,
-                                         kLayoutSW128);
-            const uint64_t bhi = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = smem_desc(kv + d * kLatBlockBytes + ks * 4096, 16384, 1024,
+                                       kLayoutSW128);
+          const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+          // B = P^T, MN-major: 16-row groups 2048 B apart (hi groups, then lo
+          // groups), 8-token groups 128 B apart.
+          const uint64_t bhi = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
+          if constexpr (C::kStack) {
+            umma_f8(tmem + C::kOCol + d * C::OW, a, bhi, kIdPV, acc);
+          } else {
             const uint64_t blo = smem_desc(pbuf + C::kPHalf + ks * 512, 128, 2048, kLayoutNone);
-            umma_f8(tmem + C::kOCol + d * NR, a, bhi, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
-            umma_f8(tmem + C::kOCol + d * NR, a, blo, kIdPV, 1u);
+            umma_f8(tmem + C::kOCol + d * C::OW, a, bhi, kIdPV, acc);
+            umma_f8(tmem + C::kOCol + d * C::OW, a, blo, kIdPV, 1u);
           }
         }
-        umma_commit(bar(BAR_EMPTY0 + jst));
-        if (!C::kPInStage) umma_commit(bar(BAR_PFREE0 + pb));
-        umma_commit(bar(BAR_ODONE));
       }
-      __syncwarp();
-      return true;
+      umma_commit(bar(BAR_EMPTY0 + jst));
+      if (!C::kPInStage) umma_commit(bar(BAR_PFREE0 + pb));
+      umma_commit(bar(BAR_ODONE));
+    };
+    // QK of tile i (KV in stage ist) into S buffer sb; lane 0 issues.
+    auto issue_qk = [&](int ist, int sb) {
+      tc_fence_after();
+      const uint32_t kv = sbase + C::kKV + ist * kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < 18; ++kk) {
+        uint64_t a, bd;
+        if (kk < 16) {
+          const int d = kk >> 2, sub = kk & 3;
+          a = smem_desc(kv + d * kLatBlockBytes + sub * 32, 16, 1024, kLayoutSW128);
+          bd = smem_desc(sbase + C::kQ + d * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
+        } else {
+          const int sub = kk - 16;
+          a = smem_desc(kv + kRopeOffset + sub * 32, 16, 512, kLayoutSW64);
+          bd = smem_desc(sbase + C::kQ + 4 * NR * 128 + sub * 32, 16, 512, kLayoutSW64);
+        }
+        umma_f8(tmem + sb * NR, a, bd, kIdQK, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(bar(BAR_SFULL0 + sb));
     };
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) fail();
-    int st = 0, round = 0, prev_st = 0;
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      bool w = mbar_wait(bar(BAR_FULL0 + st), round & 1, p.wait_cycles);
-      const int sb = (C::NS == 2) ? (i & 1) : 0;
-      const int use = (C::NS == 2) ? (i >> 1) : i;
-      if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles);
-      w = __all_sync(0xffffffffu, w && !*abort_flag);
-      if (!w) {
-        fail();
-        ok = false;
-        break;
-      }
-      const int tile_tok0 = tok_begin + i * kTileTokens;
-      const int valid = tok_end - tile_tok0;  // tokens of this tile inside the split
-      const uint32_t kv = sbase + C::kKV + st * kTileBytes;
-      if (valid < kTileTokens) {
-        // Rows past the split's end: pages that were not loaded, or the tail
-        // of a request's last page.  Zero them so V holds no stale or NaN
-        // bytes (0 * NaN would poison the PV sum).
-        const int nrow = kTileTokens - valid;
-        uint8_t* kvp = base + C::kKV + st * kTileBytes;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int idx = lane; idx < nrow * 36; idx += 32) {
-          const int r = valid + idx / 36;
-          const int c = idx % 36;
-          uint4* dst;
-          if (c < 32)
-            dst = reinterpret_cast<uint4*>(kvp + (c / 8) * kLatBlockBytes + r * 128 + (c % 8) * 16);
-          else
-            dst = reinterpret_cast<uint4*>(kvp + kRopeOffset + r * 64 + (c - 32) * 16);
-          *dst = z;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
+    // Issue loop.  PV(pv) goes out as soon as its P^T is ready and QK(qk) as
+    // soon as its tile has landed and its S^T buffer is free, in whichever
+    // order they become ready; QK runs at most one tile ahead of PV
+    // (qk <= pv + 1), which keeps each p_full barrier at most one phase ahead
+    // of this warp.  PV is preferred: it releases a KV stage.
+    int qk = 0, pv = 0;
+    int qk_st = 0, qk_round = 0, pv_st = 0;
+    long long t_last = clock64();
+    while (ok && pv < n_tiles) {
+      int action = 0;
       if (lane == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 18; ++kk) {
-          uint64_t a, bd;
-          if (kk < 16) {
-            const int d = kk >> 2, sub = kk & 3;
-            a = smem_desc(kv + d * kLatBlockBytes + sub * 32, 16, 1024, kLayoutSW128);
-            bd = smem_desc(sbase + C::kQ + d * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
-          } else {
-            const int sub = kk - 16;
-            a = smem_desc(kv + kRopeOffset + sub * 32, 16, 512, kLayoutSW64);
-            bd = smem_desc(sbase + C::kQ + 4 * NR * 128 + sub * 32, 16, 512, kLayoutSW64);
-          }
-          umma_f8(tmem + sb * NR, a, bd, kIdQK, kk > 0 ? 1u : 0u);
+        if (pv < qk) {
+          const int pb = (C::NPB == 1) ? 0 : (pv & 1);
+          const int use = (C::NPB == 1) ? pv : (pv >> 1);
+          if (mbar_test_wait(bar(BAR_PFULL0 + pb), use & 1)) action = 1;
         }
-        umma_commit(bar(BAR_SFULL0 + sb));
+        if (action == 0 && qk < n_tiles && qk <= pv + 1) {
+          const int sb = (C::NS == 2) ? (qk & 1) : 0;
+          const int use = (C::NS == 2) ? (qk >> 1) : qk;
+          if (mbar_test_wait(bar(BAR_FULL0 + qk_st), qk_round & 1) &&
+              (use < 1 || mbar_test_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1)))
+            action = 2;
+        }
       }
-      __syncwarp();
-      if (i > 0) {
-        if (!issue_pv(i - 1, prev_st)) {
+      action = __shfl_sync(0xffffffffu, action, 0);
+      if (action == 1) {
+        if (lane == 0) issue_pv(pv, pv_st, (C::NPB == 1) ? 0 : (pv & 1));
+        __syncwarp();
+        ++pv;
+        if (++pv_st == C::NST) pv_st = 0;
+        t_last = clock64();
+      } else if (action == 2) {
+        const int tile_tok0 = tok_begin + qk * kTileTokens;
+        const int valid = tok_end - tile_tok0;  // tokens of this tile inside the split
+        if (valid < kTileTokens) {
+          // Rows past the split's end: pages that were not loaded, or the tail
+          // of a request's last page.  Zero them so V holds no stale or NaN
+          // bytes (0 * NaN would poison the PV sum).
+          const int nrow = kTileTokens - valid;
+          uint8_t* kvp = base + C::kKV + qk_st * kTileBytes;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          for (int idx = lane; idx < nrow * 36; idx += 32) {
+            const int r = valid + idx / 36;
+            const int c = idx % 36;
+            uint4* dst;
+            if (c < 32)
+              dst = reinterpret_cast<uint4*>(kvp + (c / 8) * kLatBlockBytes + r * 128 + (c % 8) * 16);
+            else
+              dst = reinterpret_cast<uint4*>(kvp + kRopeOffset + r * 64 + (c - 32) * 16);
+            *dst = z;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) issue_qk(qk_st, (C::NS == 2) ? (qk & 1) : 0);
+        __syncwarp();
+        ++qk;
+        if (++qk_st == C::NST) {
+          qk_st = 0;
+          ++qk_round;
+        }
+        t_last = clock64();
+      } else {
+        const bool late = (clock64() - t_last > p.wait_cycles) || *abort_flag;
+        if (__any_sync(0xffffffffu, late)) {
           fail();
           ok = false;
-          break;
         }
       }
-      prev_st = st;
-      if (++st == C::NST) {
-        st = 0;
-        ++round;
-      }
-    }
-    if (ok && n_tiles > 0) {
-      if (!issue_pv(n_tiles - 1, prev_st)) fail();
     }
     // One commit after everything this warp issued: the epilogue reads O^T
     // after it, and TMEM is released only after it.
@@ -620,14 +641,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int d = 0; d < 4; ++d) {
 #pragma unroll
-            for (int cc = 0; cc < NR / 16; ++cc) {
+            for (int cc = 0; cc < C::OW / 16; ++cc) {
               uint32_t r[16];
-              const uint32_t addr = tmem + lane_addr + C::kOCol + d * NR + cc * 16;
+              const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + cc * 16;
+              const int row0c = (cc * 16) % NR;  // hi and lo columns share a row's scale
               tmem_ld16(addr, r);
               tmem_ld_wait();
 #pragma unroll
               for (int k = 0; k < 16; ++k)
-                r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[cc * 16 + k]);
+                r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[row0c + k]);
               tmem_st16(addr, r);
             }
           }
@@ -710,8 +732,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < NR / 16; ++cc) {
           uint32_t r[16];
-          tmem_ld16(tmem + lane_addr + C::kOCol + d * NR + cc * 16, r);
-          tmem_ld_wait();
+          tmem_ld16(tmem + lane_addr + C::kOCol + d * C::OW + cc * 16, r);
+          if constexpr (C::kStack) {
+            uint32_t r2[16];
+            tmem_ld16(tmem + lane_addr + C::kOCol + d * C::OW + NR + cc * 16, r2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              r[k] = __float_as_uint(__uint_as_float(r[k]) + __uint_as_float(r2[k]));
+          } else {
+            tmem_ld_wait();
+          }
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             const int row = cc * 16 + k;
