@@ -31,6 +31,7 @@ DEFAULT_WORKLOAD = "long_h12_q1_l1m_b16"
 # Published time for this exact workload (H12 q1 B16 1M, issue #20510 "Repro 1",
 # kernel before #19338, on an unspecified Blackwell SM10x GPU): context only.
 PUBLISHED_US = {"long_h12_q1_l1m_b16": 1095.5}
+L2_ROTATE_BYTES = 2 * 126 * 1024 * 1024  # rotate inputs below 2x the 126 MB L2
 KERNEL_SOURCES = ["split_kv_mla_paged_gb300/csrc/mla_decode.cu",
                   "split_kv_mla_paged_gb300/csrc/sm103_ptx.cuh"]
 
@@ -282,51 +283,74 @@ def main():
     else:
         plan = mla.mla_decode_plan(lens, H, q_len, sm_count=sm_count)
     ws_bytes = mla.mla_decode_workspace_size(B, q_len, H, plan.max_splits)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    mla.mla_decode_workspace_init(ws, ws_bytes)
     lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
     splits_d = torch.from_numpy(plan.splits).to(dev)
     chunks_d = torch.from_numpy(plan.chunks).to(dev)
-    out = torch.empty((B, q_len, H, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
-    args_common = (inp.q, inp.kv, inp.num_pages, inp.page_table, inp.max_pages, lens_d, splits_d,
-                   chunks_d, plan.max_splits, plan.kv_split, B, q_len, H, w["causal"], 1.0, 1.0,
-                   SOFTMAX_SCALE, ws, ws_bytes, out, lse, None)
-    stream = torch.cuda.current_stream(dev)
+    # Inputs larger than L2 need no flush.  Smaller ones rotate over enough
+    # distinct seeded pools (with their own workspaces and outputs) that
+    # consecutive steps never find their KV in L2.
+    kv_bytes = inp.kv_bytes()
+    n_pools = 1 if kv_bytes >= L2_ROTATE_BYTES else min(64, -(-L2_ROTATE_BYTES // kv_bytes))
+    pools = [inp] + [workload_inputs(args.workload, device=dev, seed_offset=k)
+                     for k in range(1, n_pools)]
+    calls = []
+    for pool in pools:
+        ws_k = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        mla.mla_decode_workspace_init(ws_k, ws_bytes)
+        out_k = torch.empty((B, q_len, H, 512), dtype=torch.bfloat16, device=dev)
+        lse_k = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
+        calls.append((pool.q, pool.kv, pool.num_pages, pool.page_table, pool.max_pages, lens_d,
+                      splits_d, chunks_d, plan.max_splits, plan.kv_split, B, q_len, H,
+                      w["causal"], 1.0, 1.0, SOFTMAX_SCALE, ws_k, ws_bytes, out_k, lse_k, None))
+    args_common = calls[0]
+    ws, out, lse = args_common[17], args_common[19], args_common[20]
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
 
-    for _ in range(args.warmup):
-        mla.mla_decode(*args_common, stream)
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            mla.mla_decode(*calls[k % n_pools], stream)
     torch.cuda.synchronize(dev)
     mla.mla_decode_status(ws, stream)
 
-    # ---- timed region: K steps, events around each phase ----
+    # ---- timed region: K steps replayed from a CUDA graph ----
+    # One graph holds the K decode calls (split-KV kernel + merge); two more
+    # hold the same K calls of each phase alone, for per-kernel durations.
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    graphs = {}
+    for name, fn in (("full", mla.mla_decode), ("split", mla.mla_decode_splitkv),
+                     ("merge", mla.mla_decode_merge)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(K):
+                fn(*calls[k % n_pools], None)
+        graphs[name] = g
+    for g in graphs.values():  # one untimed replay each
+        g.replay()
+    torch.cuda.synchronize(dev)
+    ev = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for n in graphs}
     sampler = ClockSampler(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for k in range(K):
-        ev[k][0].record(stream)
-        mla.mla_decode_splitkv(*args_common, stream)
-        ev[k][1].record(stream)
-        mla.mla_decode_merge(*args_common, stream)
-        ev[k][2].record(stream)
-    end.record(stream)
+    with torch.cuda.stream(stream):
+        for n in ("full", "split", "merge"):
+            ev[n][0].record(stream)
+            graphs[n].replay()
+            ev[n][1].record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     if world > 1:
         dist.barrier()
-    total_ms = start.elapsed_time(end)
-    split_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    merge_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    total_ms = ev["full"][0].elapsed_time(ev["full"][1])
+    split_us = ev["split"][0].elapsed_time(ev["split"][1]) * 1e3 / K
+    merge_us = ev["merge"][0].elapsed_time(ev["merge"][1]) * 1e3 / K
     us_per_call = max_over_ranks(total_ms * 1e3 / K, dev)
     mla.mla_decode_status(ws, stream)
+    del graphs
 
     # ---- end to end through the public API with host buffers ----
     q_h = inp.q.cpu().pin_memory()
@@ -354,18 +378,18 @@ def main():
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize(dev)
     e2e_us = max_over_ranks((time.perf_counter() - t0) * 1e6 / args.e2e_steps, dev)
 
     # ---- roofline of the dominant kernel (split-KV) ----
-    kv_bytes = inp.kv_bytes()
-    split_avg_s = statistics.mean(split_ms) / 1e3
+    split_avg_s = split_us * 1e-6
     achieved = kv_bytes / split_avg_s / 1e9
     peaks = measured_peaks()
     traffic = recorded_traffic(args.workload)
@@ -391,12 +415,14 @@ def main():
                        "kv_len": lens[0], "causal": w["causal"], "plan": args.plan,
                        "splits": plan.splits.tolist()[:4] + (["..."] if B > 4 else []),
                        "kv_split": plan.kv_split, "kv_bytes": kv_bytes,
-                       "l2": "inputs larger than L2 (no flush)",
+                       "l2": ("inputs larger than L2 (no flush)" if n_pools == 1 else
+                              f"{n_pools} rotating input pools ({n_pools * kv_bytes} B > 2x L2)"),
+                       "timing": "CUDA graph of K calls, CUDA events",
                        "parallelism": f"replicas x{world}" if world > 1 else "single"},
             "kv_gbs": kv_bytes / (us_per_call * 1e-6) / 1e9,
             "aggregate_kv_gbs": world * kv_bytes / (us_per_call * 1e-6) / 1e9,
-            "split_kernel_us": statistics.mean(split_ms) * 1e3,
-            "merge_kernel_us": statistics.mean(merge_ms) * 1e3,
+            "split_kernel_us": split_us,
+            "merge_kernel_us": merge_us,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "traffic": traffic, "peak_source": peaks["source"],

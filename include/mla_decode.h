@@ -78,9 +78,10 @@ typedef enum {
  * kv_lens      host int32[batch], each >= q_len >= 1.
  * num_heads    heads per request (H); num_heads * q_len <= MLA_MAX_ROWS.
  * sm_count     SMs of the target GPU (used when target_ctas <= 0).
- * target_ctas  > 0: reproduce the pages' planner: t = max(1, target/B')
- *              splits per request, chunk = roundup128(ceil(L/t)), where B'
- *              is batch times the number of row groups a request needs.
+ * target_ctas  > 0: reproduce the pages' planner: t = max(1, target/B)
+ *              splits per request, chunk = roundup128(ceil(L/t)).  (A request
+ *              with more than 48 rows runs each split as several row-group
+ *              CTAs on top of that.)
  *              <= 0: GB300 planner: one common chunk for the whole batch,
  *              chosen to balance whole waves of one CTA per SM.
  * Outputs (host): splits_out[batch] (1..MLA_MAX_SPLITS), chunk_out[batch]

@@ -58,6 +58,7 @@ constexpr uint32_t kPageRopeBytes = MLA_PAGE_SIZE * 64;      // 2048
 constexpr uint32_t kPageBytes = MLA_PAGE_SIZE * MLA_HEAD_DIM;
 constexpr long long kWaitLimitCycles = 4000000000LL;  // about 2 s at 2 GHz
 constexpr uint32_t kSoftmaxBarrier = 1;
+constexpr uint32_t kVoteBarrier = 2;
 
 struct DecodeParams {
   const int32_t* page_table;
@@ -101,7 +102,7 @@ struct Cfg {
   // Shared memory, offsets from a 1024-byte aligned base.
   static constexpr uint32_t kPHalf = NR * kTileTokens;  // one E4M3 term of P^T
   static constexpr uint32_t kPBytes = 2 * kPHalf;       // hi + lo
-  static constexpr uint32_t kAuxBytes = 224 + 40 * NR;
+  static constexpr uint32_t kAuxBytes = 160 + 52 * NR;
   static constexpr uint32_t kQBytes = NR * MLA_HEAD_DIM;
   // Three KV stages fit when P^T can live in the rope block of its own stage
   // (QK has consumed that block before P is written): NR = 16.  Otherwise two
@@ -117,15 +118,18 @@ struct Cfg {
                              : (kP + 2 * kPBytes + kAuxBytes + 1024 <= 232448u) ? 2 : 1;
   static constexpr uint32_t kAux = kP + NPB * kPBytes;
   // aux: mbarriers, tmem slot, flags, reductions
-  static constexpr uint32_t kBars = kAux;               // 24 x 8 B
-  static constexpr uint32_t kTmemSlot = kAux + 192;     // 4 B
-  static constexpr uint32_t kFlags = kAux + 208;        // 3 x 4 B
-  static constexpr uint32_t kRedMax = kAux + 224;       // 4 x NR floats
-  static constexpr uint32_t kRedSum = kRedMax + 16 * NR;
-  static constexpr uint32_t kKref = kRedSum + 16 * NR;  // NR floats
-  static constexpr uint32_t kAlpha = kKref + 4 * NR;    // NR floats
-  static constexpr uint32_t kEnd = kAlpha + 4 * NR;
+  static constexpr uint32_t kBars = kAux;               // 17 x 8 B
+  static constexpr uint32_t kTmemSlot = kAux + 136;     // 4 B
+  static constexpr uint32_t kFlags = kAux + 144;        // 3 x 4 B
+  static constexpr uint32_t kRedMax = kAux + 160;       // 4 x NR floats
+  // Row owner r reads red_max[.][r] before writing alpha[r]: alpha reuses
+  // red_max's first row.
+  static constexpr uint32_t kAlpha = kRedMax;           // NR floats
+  static constexpr uint32_t kRedSum = kRedMax + 16 * NR;  // 2 x 4 x NR floats
+  static constexpr uint32_t kKref = kRedSum + 32 * NR;  // NR floats
+  static constexpr uint32_t kEnd = kKref + 4 * NR;
   static_assert(kEnd - kAux <= kAuxBytes, "aux layout");
+  static_assert(NR != 16 || NST == 3, "16-row CTAs must keep three KV stages");
   static constexpr uint32_t kSmemBytes = kEnd + 1024;   // + alignment slack
   static_assert(kSmemBytes <= 232448u, "shared memory");
 };
@@ -135,7 +139,7 @@ enum : int {
   BAR_FULL0 = 0, BAR_EMPTY0 = 3, BAR_QFULL = 6, BAR_SFULL0, BAR_SFULL1, BAR_SFREE0, BAR_SFREE1,
   BAR_PFULL0, BAR_PFULL1, BAR_PFREE0, BAR_PFREE1, BAR_ODONE, BAR_FINAL, BAR_COUNT
 };
-static_assert(BAR_COUNT <= 24, "barrier slots");
+static_assert(BAR_COUNT <= 17, "barrier slots");
 
 __device__ __forceinline__ void report(int* status, int code) {
   atomicCAS(status, 0, code);
@@ -158,6 +162,18 @@ __device__ __forceinline__ float softmax_weight(float t, float k) {
   const int sc = static_cast<int>(a) - static_cast<int>(k) + 8;
   if (sc < -126) return 0.0f;
   return ex2_approx(f) * pow2i(sc);
+}
+
+// Named barrier over `nthreads` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred q, p;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, %3, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
@@ -246,9 +262,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tm_q_lat,
                         const __grid_constant__ CUtensorMap tm_q_rope, const DecodeParams p) {
   using C = Cfg<NR>;
-  const int split = blockIdx.x;
+  // Row groups of one (request, split) are adjacent in the grid so that the
+  // CTAs that read the same KV tiles run at the same time (L2 serves the
+  // repeats).
+  const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
+  const int split = blockIdx.x / ngroups;
+  const int grp = blockIdx.x - split * ngroups;
   const int b = blockIdx.y;
-  const int grp = blockIdx.z;
 
   // ---- plan checks (uniform over the CTA) -------------------------------
   const int L = p.kv_lens[b];
@@ -552,7 +572,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tok_lane = quad * 32 + lane;  // TMEM lane == token index within the tile
     const int sid = threadIdx.x - 64;       // 0..127, owner of row `sid` when < NR
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    float k_row = -INFINITY;  // owner state: reference max (integer, log2 units)
+    float k_row = -INFINITY;  // owner state: reference (integer, log2 units)
+    float kreg[NR];           // every thread's copy of all rows' references
+#pragma unroll
+    for (int k = 0; k < NR; ++k) kreg[k] = -INFINITY;
     float l_row = 0.0f;       // owner state: sum of weights relative to k_row - 8
     const float c = p.c_log2;
     // Smallest visibility limit over this group's rows (MTP verify: the first
@@ -602,63 +625,82 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      {
-        float tm[NR];
+      // Reference check.  A row's reference k only has to bound its scores:
+      // with p = 2^(t - k + 8), E4M3 holds p up to 448 = 2^8.8, so any k with
+      // t <= k + 0.75 works.  One vote finds whether some score of the tile
+      // exceeds its row's reference; only then (always on the first tile)
+      // are the tile maxima reduced and references raised to ceil(max).
+      bool over = false;
 #pragma unroll
-        for (int k = 0; k < NR; ++k) tm[k] = t[k];
-        warp_reduce_rows<NR, true>(tm, lane, red_max + quad * NR);
+      for (int k = 0; k < NR; ++k) over |= t[k] > kreg[k] + 0.75f;
+      const bool any_over = bar_sync_or(kVoteBarrier, 128, over);
+      // Owners fold the previous tile's row sums (relative to its reference).
+      if (sid < NR && i > 0) {
+        const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
+        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
       }
-      named_bar_sync(kSoftmaxBarrier, 128);  // B1: tile maxima (and last tile's sums) ready
-      if (sid == 0) flags[(i + 1) & 1] = 0;
-      if (sid < NR) {
-        if (i > 0)
-          l_row += (red_sum[sid] + red_sum[NR + sid]) + (red_sum[2 * NR + sid] + red_sum[3 * NR + sid]);
-        const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
-                               fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
-        float k_new = k_row;
-        if (mt > k_row) k_new = ceilf(mt);
-        float alpha = 1.0f;
-        if (k_new != k_row && k_row != -INFINITY) {
-          const int e = static_cast<int>(k_row - k_new);
-          alpha = (e < -126) ? 0.0f : pow2i(e);
-          flags[i & 1] = 1;
+      if (any_over) {
+        {
+          float tm[NR];
+#pragma unroll
+          for (int k = 0; k < NR; ++k) tm[k] = t[k];
+          warp_reduce_rows<NR, true>(tm, lane, red_max + quad * NR);
         }
-        l_row *= alpha;
-        k_row = k_new;
-        kref[sid] = k_new;
-        alpha_s[sid] = alpha;
-      }
-      named_bar_sync(kSoftmaxBarrier, 128);  // B2: references ready
-      const bool corr = flags[i & 1] != 0;
-      if (ok && corr && i > 0) {
-        // Rescale the O^T columns of rows whose reference moved (rare).
-        // o_done is at most one phase behind here: s_full(i) implies PV(i-2)
-        // completed, and PV(i) is not issued before this tile's p_full.
-        ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, p.wait_cycles);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int d = 0; d < 4; ++d) {
-#pragma unroll
-            for (int cc = 0; cc < C::OW / 16; ++cc) {
-              uint32_t r[16];
-              const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + cc * 16;
-              const int row0c = (cc * 16) % NR;  // hi and lo columns share a row's scale
-              tmem_ld16(addr, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int k = 0; k < 16; ++k)
-                r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[row0c + k]);
-              tmem_st16(addr, r);
-            }
+        // The correction flag: cleared before B1 (every read of its last
+        // value happened before this tile's vote), set by owners after B1,
+        // read by all after B2.
+        if (sid == 0) flags[0] = 0;
+        named_bar_sync(kSoftmaxBarrier, 128);  // B1: tile maxima ready
+        if (sid < NR) {
+          const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
+                                 fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
+          float k_new = k_row;
+          if (mt > k_row + 0.75f) k_new = ceilf(mt);
+          float alpha = 1.0f;
+          if (k_new != k_row && k_row != -INFINITY) {
+            const int e = static_cast<int>(k_row - k_new);
+            alpha = (e < -126) ? 0.0f : pow2i(e);
+            flags[0] = 1;
           }
-          tmem_st_wait();
+          l_row *= alpha;
+          k_row = k_new;
+          kref[sid] = k_new;
+          alpha_s[sid] = alpha;
+        }
+        named_bar_sync(kSoftmaxBarrier, 128);  // B2: references ready
+#pragma unroll
+        for (int k = 0; k < NR; ++k) kreg[k] = kref[k];
+        const bool corr = flags[0] != 0;
+        if (ok && corr && i > 0) {
+          // Rescale the O^T columns of rows whose reference moved (rare).
+          // o_done is at most one phase behind here: s_full(i) implies PV(i-2)
+          // completed, and PV(i) is not issued before this tile's p_full.
+          ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, p.wait_cycles);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int d = 0; d < 4; ++d) {
+#pragma unroll
+              for (int cc = 0; cc < C::OW / 16; ++cc) {
+                uint32_t r[16];
+                const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + cc * 16;
+                const int row0c = (cc * 16) % NR;  // hi and lo columns share a row's scale
+                tmem_ld16(addr, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                  r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[row0c + k]);
+                tmem_st16(addr, r);
+              }
+            }
+            tmem_st_wait();
+          }
         }
       }
       // Weights 2^(t - k + 8), exact power-of-two scaling.
 #pragma unroll
-      for (int k = 0; k < NR; ++k) t[k] = softmax_weight(t[k], kref[k]);
+      for (int k = 0; k < NR; ++k) t[k] = softmax_weight(t[k], kreg[k]);
       // P^T (E4M3) into shared memory, MN-major: [NR/16][128 tokens][16 rows].
       const int pb = (C::NPB == 1) ? 0 : (i & 1);
       const int puse = (C::NPB == 1) ? i : (i >> 1);
@@ -688,8 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(BAR_PFULL0 + pb));
       }
-      // Row sums of the unquantised weights, folded in at the next B1.
-      warp_reduce_rows<NR, false>(t, lane, red_sum + quad * NR);
+      // Row sums of the unquantised weights, folded in by the owners after
+      // the next tile's vote (double-buffered by tile parity).
+      warp_reduce_rows<NR, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR);
     }
     if (!ok && lane == 0) {
       report(p.status, MLA_ERR_TIMEOUT);
@@ -700,8 +743,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool single = (nsplit == 1);
     float* scale_s = alpha_s;
     if (sid < NR) {
-      if (n_tiles > 0)
-        l_row += (red_sum[sid] + red_sum[NR + sid]) + (red_sum[2 * NR + sid] + red_sum[3 * NR + sid]);
+      if (n_tiles > 0) {
+        const float* rs = red_sum + ((n_tiles - 1) & 1) * 4 * NR;
+        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+      }
       const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
       const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + sid;
       float sc = 0.0f;
@@ -940,7 +985,7 @@ static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages
       !make_map(&q_lat, q, q_rows, 128, NR, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&q_rope, q, q_rows, 64, NR, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  dim3 grid(prm.max_splits, batch, groups);
+  dim3 grid(prm.max_splits * groups, batch);
   mla_split_kv_kernel<NR><<<grid, kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
                                                                      q_rope, prm);
   return cudaGetLastError();
@@ -1095,9 +1140,6 @@ static int launch_decode_split(const void* q_fp8, const void* kv_pages_fp8, int6
     case 16: e = launch_split<16>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
     case 32: e = launch_split<32>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
     case 48: e = launch_split<48>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
-    case 64: e = launch_split<64>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
-    case 80: e = launch_split<80>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
-    case 96: e = launch_split<96>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
     default:
       set_error("mla_decode: internal row grouping error");
       return MLA_ERR_UNSUPPORTED;

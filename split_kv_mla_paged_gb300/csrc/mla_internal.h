@@ -8,10 +8,12 @@
 
 namespace mla {
 
-// Rows (heads x query tokens) one CTA of the split-KV kernel handles.  TMEM
-// holds S^T (NR columns) and O^T (4 x NR columns) in 512 columns, so NR <= 96
-// with 16-row granularity (the MMA N step).
-constexpr int kMaxRowsPerCta = 96;
+// Rows (heads x query tokens) one CTA of the split-KV kernel handles, in
+// multiples of 16 (the MMA N step).  At most 48: TMEM then holds two S^T
+// buffers (2 x NR columns) and O^T for both E4M3 terms of P
+// (4 blocks x 2 x NR columns) in 512 columns, and shared memory holds two
+// P^T buffers next to two KV stages.  More rows use more CTAs (row groups).
+constexpr int kMaxRowsPerCta = 48;
 
 struct RowGroups {
   int groups;   // CTAs per (request, split) along the row dimension

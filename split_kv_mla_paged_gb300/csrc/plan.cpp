@@ -83,7 +83,9 @@ extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t nu
   const int64_t T = MLA_TILE_TOKENS;
 
   if (target_ctas > 0) {
-    const int64_t t = std::max<int64_t>(1, target_ctas / (static_cast<int64_t>(batch) * rg.groups));
+    // The pages' formula counts splits per request; row groups (CTAs that
+    // share a split's KV range) come on top of the target.
+    const int64_t t = std::max<int64_t>(1, target_ctas / static_cast<int64_t>(batch));
     for (int b = 0; b < batch; ++b) {
       int64_t chunk = round_up(ceil_div(kv_lens[b], t), T);
       if (ceil_div(kv_lens[b], chunk) > MLA_MAX_SPLITS)

@@ -184,7 +184,10 @@ _add("ragged_h12_q1_b16", batch=16, num_heads=12, q_len=1, kv_lens=ragged_lens(4
 
 
 def workload_inputs(name: str, device: str | torch.device = "cpu",
-                    kv_lens_override: Optional[Sequence[int]] = None) -> DecodeInputs:
+                    kv_lens_override: Optional[Sequence[int]] = None,
+                    seed_offset: int = 0) -> DecodeInputs:
+    """Inputs of a named workload; seed_offset draws further distinct pools."""
     w = WORKLOADS[name]
     lens = list(kv_lens_override) if kv_lens_override is not None else w["kv_lens"]
-    return decode_inputs(w["batch"], w["num_heads"], w["q_len"], lens, w["seed"], device=device)
+    return decode_inputs(w["batch"], w["num_heads"], w["q_len"], lens,
+                         w["seed"] + 1000 * seed_offset, device=device)
