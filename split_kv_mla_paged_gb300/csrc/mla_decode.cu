@@ -154,11 +154,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // 2^i for an integer i in [-126, 127], exactly.
 __device__ __forceinline__ float pow2i(int i) { return __int_as_float((i + 127) << 23); }
 
-// 2^(t - k + 8) with exact power-of-two scaling (k integer-valued).
+// 2^(t - k + 8) with exact power-of-two scaling (k integer-valued): split
+// t = r + f with r = rint(t), then 2^f * 2^(r - k + 8), the second factor
+// built from its exponent bits.  For |t| < 2^21 the rounding uses the
+// 1.5 * 2^23 addition trick (FMA-pipe adds instead of rint and float-to-int
+// conversions, which share the slow special-function pipe with ex2).
 __device__ __forceinline__ float softmax_weight(float t, float k) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  if (fabsf(t) < 2097152.0f) {
+    const float tr = t + kMagic;
+    const float r = tr - kMagic;          // rint(t)
+    const float f = t - r;                // exact, |f| <= 0.5
+    const float ef = (r - k) + 8.0f;      // integer-valued and exact (|r|, |k| < 2^22)
+    int e = __float_as_int(ef + kMagic) - 0x4B400000 + 127;
+    e = max(e, 0);                        // below 2^-126 the weight is flushed to 0
+    return ex2_approx(f) * __int_as_float(e << 23);
+  }
   if (t == -INFINITY) return 0.0f;
   const float a = rintf(t);
-  const float f = t - a;  // exact, |f| <= 0.5
+  const float f = t - a;
   const int sc = static_cast<int>(a) - static_cast<int>(k) + 8;
   if (sc < -126) return 0.0f;
   return ex2_approx(f) * pow2i(sc);
