@@ -48,7 +48,6 @@
 
 namespace mla {
 
-constexpr int kThreads = 192;
 constexpr int kTileTokens = 128;
 constexpr uint32_t kTileBytes = kTileTokens * MLA_HEAD_DIM;  // 73728
 constexpr uint32_t kLatBlockBytes = kTileTokens * 128;       // 16384: one 128-dim block
@@ -87,14 +86,18 @@ struct DecodeParams {
 template <int NR>
 struct Cfg {
   static_assert(NR % 16 == 0 && NR >= 16 && NR <= kMaxRowsPerCta, "NR");
-  // P^T = hi + lo.  With NR <= 48 both terms go through one PV MMA with
-  // N = 2*NR (O^T holds the hi and lo products side by side and the epilogue
-  // adds them), so V is read from shared memory once per tile; above that
-  // TMEM is too small and PV runs twice over V.
-  static constexpr bool kStack = NR <= 48;
-  static constexpr int OW = kStack ? 2 * NR : NR;  // O^T columns per latent block
-  static constexpr int NS = (2 * NR + 4 * OW <= 512) ? 2 : 1;  // S^T buffers in TMEM
+  // P^T = hi + lo.  Both terms go through one PV MMA with N = 2*NR (O^T
+  // holds the hi and lo products side by side and the epilogue adds them), so
+  // V is read from shared memory once per tile.
+  static constexpr int OW = 2 * NR;  // O^T columns per latent block
+  static constexpr int NS = 2;       // S^T buffers in TMEM
   static constexpr uint32_t kTmemUsed = NS * NR + 4 * OW;
+  static_assert(kTmemUsed <= 512, "TMEM");
+  // Softmax warpgroups: two (each owning half the rows) from 32 rows up.
+  static constexpr int SWG = NR >= 32 ? 2 : 1;
+  static constexpr int NRH = NR / SWG;
+  static_assert(NRH % 8 == 0, "rows per softmax warpgroup");
+  static constexpr int kThreads = 64 + 128 * SWG;
   static constexpr uint32_t kTmemCols =
       kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
       : kTmemUsed <= 256 ? 256 : 512;
@@ -116,6 +119,7 @@ struct Cfg {
   static constexpr uint32_t kP = kQ + kQBytes;
   static constexpr int NPB = kPInStage ? 0
                              : (kP + 2 * kPBytes + kAuxBytes + 1024 <= 232448u) ? 2 : 1;
+  static_assert(NPB != 1, "P^T needs two buffers or a slot in each KV stage");
   static constexpr uint32_t kAux = kP + NPB * kPBytes;
   // aux: mbarriers, tmem slot, flags, reductions
   static constexpr uint32_t kBars = kAux;               // 17 x 8 B
@@ -270,7 +274,7 @@ __device__ __forceinline__ void warp_reduce_rows(float* v, int lane, float* dst)
 }
 
 template <int NR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     mla_split_kv_kernel(const __grid_constant__ CUtensorMap tm_kv_lat,
                         const __grid_constant__ CUtensorMap tm_kv_rope,
                         const __grid_constant__ CUtensorMap tm_q_lat,
@@ -329,10 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(BAR_QFULL), 1);
     mbar_init(bar(BAR_SFULL0), 1);
     mbar_init(bar(BAR_SFULL1), 1);
-    mbar_init(bar(BAR_SFREE0), 128);
-    mbar_init(bar(BAR_SFREE1), 128);
-    mbar_init(bar(BAR_PFULL0), 128);
-    mbar_init(bar(BAR_PFULL1), 128);
+    mbar_init(bar(BAR_SFREE0), 128 * C::SWG);
+    mbar_init(bar(BAR_SFREE1), 128 * C::SWG);
+    mbar_init(bar(BAR_PFULL0), 128 * C::SWG);
+    mbar_init(bar(BAR_PFULL1), 128 * C::SWG);
     mbar_init(bar(BAR_PFREE0), 1);
     mbar_init(bar(BAR_PFREE1), 1);
     mbar_init(bar(BAR_ODONE), 1);
@@ -465,14 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
           // B = P^T, MN-major: 16-row groups 2048 B apart (hi groups, then lo
           // groups), 8-token groups 128 B apart.
-          const uint64_t bhi = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
-          if constexpr (C::kStack) {
-            umma_f8(tmem + C::kOCol + d * C::OW, a, bhi, kIdPV, acc);
-          } else {
-            const uint64_t blo = smem_desc(pbuf + C::kPHalf + ks * 512, 128, 2048, kLayoutNone);
-            umma_f8(tmem + C::kOCol + d * C::OW, a, bhi, kIdPV, acc);
-            umma_f8(tmem + C::kOCol + d * C::OW, a, blo, kIdPV, 1u);
-          }
+          const uint64_t bd = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
+          umma_f8(tmem + C::kOCol + d * C::OW, a, bd, kIdPV, acc);
         }
       }
       umma_commit(bar(BAR_EMPTY0 + jst));
@@ -577,47 +575,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
   } else {
-    // ================= softmax warpgroup (warps 2-5) =================
-    // Every warp of the group passes the same sequence of named barriers
-    // whether or not a wait ran out (a failed wait only turns `ok` off and
-    // skips the work), so a timeout can never leave the group split across
-    // barriers.
+    // ================= softmax warpgroups (warps 2 .. 2 + 4*SWG) =================
+    // SWG warpgroups share each tile: warpgroup g owns rows [g*NRH, (g+1)*NRH)
+    // of every token (two warps per SM sub-partition when SWG = 2, so one
+    // warp's latency hides behind the other's).  TMEM lane quadrant = warp % 4.
+    // Every warp passes the same sequence of named barriers whether or not a
+    // wait ran out (a failed wait only turns `ok` off and skips the work), so a
+    // timeout can never leave the group split across barriers.
+    constexpr int NRH = C::NRH;
+    constexpr int NT = 128 * C::SWG;
     const int quad = warp & 3;
+    const int rbase = ((warp - 2) >> 2) * NRH;  // first row of this warpgroup
     const int tok_lane = quad * 32 + lane;  // TMEM lane == token index within the tile
-    const int sid = threadIdx.x - 64;       // 0..127, owner of row `sid` when < NR
+    const int sid = threadIdx.x - 64;       // 0..NT-1, owner of row `sid` when < NR
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     float k_row = -INFINITY;  // owner state: reference (integer, log2 units)
-    float kreg[NR];           // every thread's copy of all rows' references
-#pragma unroll
-    for (int k = 0; k < NR; ++k) kreg[k] = -INFINITY;
     float l_row = 0.0f;       // owner state: sum of weights relative to k_row - 8
+    float kreg[NRH];          // this thread's copy of its rows' references
+#pragma unroll
+    for (int k = 0; k < NRH; ++k) kreg[k] = -INFINITY;
     const float c = p.c_log2;
     // Smallest visibility limit over this group's rows (MTP verify: the first
     // query token of the block sees the fewest keys).
     const int qi_first = row0 / p.num_heads;
     const int lim_min = p.causal ? min(tok_end, L - p.q_len + qi_first + 1) : tok_end;
+    const int my_row0 = row0 + rbase;  // first request row of this warpgroup
+    const int my_rows = max(0, min(NRH, rows_here - rbase));
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
-      const int sb = (C::NS == 2) ? (i & 1) : 0;
-      const int use = (C::NS == 2) ? (i >> 1) : i;
+      const int sb = i & 1;
+      const int use = i >> 1;
       if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
       ok = __all_sync(0xffffffffu, ok);
-      float t[NR];
+      float t[NRH];
       if (ok) {
         tc_fence_after();
-        uint32_t r[NR];
+        uint32_t r[NRH];
 #pragma unroll
-        for (int cc = 0; cc < NR / 16; ++cc)
-          tmem_ld16(tmem + lane_addr + sb * NR + cc * 16,
-                    *reinterpret_cast<uint32_t(*)[16]>(&r[cc * 16]));
+        for (int cc = 0; cc < NRH / 8; ++cc)
+          tmem_ld8(tmem + lane_addr + sb * NR + rbase + cc * 8,
+                   *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
         tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < NR; ++k) t[k] = __uint_as_float(r[k]);
+        for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
         tc_fence_before();
         mbar_arrive(bar(BAR_SFREE0 + sb));
       } else {
 #pragma unroll
-        for (int k = 0; k < NR; ++k) t[k] = 0.0f;
+        for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
       }
       const int tile_tok0 = tok_begin + i * kTileTokens;
       const int j = tile_tok0 + tok_lane;
@@ -625,14 +630,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // verify) tokens after the row's query position are -inf.
       if (tile_tok0 + kTileTokens <= lim_min) {
 #pragma unroll
-        for (int k = 0; k < NR; ++k) t[k] = (k < rows_here) ? t[k] * c : -INFINITY;
+        for (int k = 0; k < NRH; ++k) t[k] = (k < my_rows) ? t[k] * c : -INFINITY;
       } else {
-        int qi = qi_first;
-        int h = row0 - qi_first * p.num_heads;
+        int qi = my_row0 / p.num_heads;
+        int h = my_row0 - qi * p.num_heads;
 #pragma unroll
-        for (int k = 0; k < NR; ++k) {
+        for (int k = 0; k < NRH; ++k) {
           const int lim = p.causal ? min(tok_end, L - p.q_len + qi + 1) : tok_end;
-          t[k] = (k < rows_here && j < lim) ? t[k] * c : -INFINITY;
+          t[k] = (k < my_rows && j < lim) ? t[k] * c : -INFINITY;
           if (++h == p.num_heads) {
             h = 0;
             ++qi;
@@ -646,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // are the tile maxima reduced and references raised to ceil(max).
       bool over = false;
 #pragma unroll
-      for (int k = 0; k < NR; ++k) over |= t[k] > kreg[k] + 0.75f;
-      const bool any_over = bar_sync_or(kVoteBarrier, 128, over);
+      for (int k = 0; k < NRH; ++k) over |= t[k] > kreg[k] + 0.75f;
+      const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
       // Owners fold the previous tile's row sums (relative to its reference).
       if (sid < NR && i > 0) {
         const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
@@ -655,16 +660,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (any_over) {
         {
-          float tm[NR];
+          float tm[NRH];
 #pragma unroll
-          for (int k = 0; k < NR; ++k) tm[k] = t[k];
-          warp_reduce_rows<NR, true>(tm, lane, red_max + quad * NR);
+          for (int k = 0; k < NRH; ++k) tm[k] = t[k];
+          warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
         }
         // The correction flag: cleared before B1 (every read of its last
         // value happened before this tile's vote), set by owners after B1,
         // read by all after B2.
         if (sid == 0) flags[0] = 0;
-        named_bar_sync(kSoftmaxBarrier, 128);  // B1: tile maxima ready
+        named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
         if (sid < NR) {
           const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
                                  fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
@@ -681,14 +686,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           kref[sid] = k_new;
           alpha_s[sid] = alpha;
         }
-        named_bar_sync(kSoftmaxBarrier, 128);  // B2: references ready
+        named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
 #pragma unroll
-        for (int k = 0; k < NR; ++k) kreg[k] = kref[k];
+        for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
         const bool corr = flags[0] != 0;
         if (ok && corr && i > 0) {
-          // Rescale the O^T columns of rows whose reference moved (rare).
-          // o_done is at most one phase behind here: s_full(i) implies PV(i-2)
-          // completed, and PV(i) is not issued before this tile's p_full.
+          // Rescale the O^T columns (hi and lo) of rows whose reference moved
+          // (rare).  o_done is at most one phase behind here: s_full(i)
+          // implies PV(i-2) completed, and PV(i) is not issued before this
+          // tile's p_full.
           ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, p.wait_cycles);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
@@ -696,16 +702,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int d = 0; d < 4; ++d) {
 #pragma unroll
-              for (int cc = 0; cc < C::OW / 16; ++cc) {
-                uint32_t r[16];
-                const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + cc * 16;
-                const int row0c = (cc * 16) % NR;  // hi and lo columns share a row's scale
-                tmem_ld16(addr, r);
-                tmem_ld_wait();
+              for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                  r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[row0c + k]);
-                tmem_st16(addr, r);
+                for (int cc = 0; cc < NRH / 8; ++cc) {
+                  uint32_t r[8];
+                  const uint32_t addr =
+                      tmem + lane_addr + C::kOCol + d * C::OW + half * NR + rbase + cc * 8;
+                  tmem_ld8(addr, r);
+                  tmem_ld_wait();
+#pragma unroll
+                  for (int k = 0; k < 8; ++k)
+                    r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[rbase + cc * 8 + k]);
+                  tmem_st8(addr, r);
+                }
               }
             }
             tmem_st_wait();
@@ -714,13 +723,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Weights 2^(t - k + 8), exact power-of-two scaling.
 #pragma unroll
-      for (int k = 0; k < NR; ++k) t[k] = softmax_weight(t[k], kreg[k]);
-      // P^T (E4M3) into shared memory, MN-major: [NR/16][128 tokens][16 rows].
-      const int pb = (C::NPB == 1) ? 0 : (i & 1);
-      const int puse = (C::NPB == 1) ? i : (i >> 1);
+      for (int k = 0; k < NRH; ++k) t[k] = softmax_weight(t[k], kreg[k]);
+      // P^T as two E4M3 terms into shared memory, MN-major:
+      // [term][NR/16 row groups][128 tokens][16 rows]; this thread writes its
+      // token's bytes for rows rbase .. rbase + NRH, 8 rows per store.
+      const int pb = i & 1;
+      const int puse = i >> 1;
       if (ok && !C::kPInStage && puse >= 1) {
-        // With one P buffer this waits for PV(i-1); the barrier is then at
-        // most one phase behind (s_full(i) implies PV(i-2) completed).
         ok = mbar_wait(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles);
         ok = __all_sync(0xffffffffu, ok);
       }
@@ -731,14 +740,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ? base + C::kKV + (i % C::NST) * kTileBytes + kRopeOffset
                             : base + C::kP + pb * C::kPBytes;
 #pragma unroll
-        for (int g = 0; g < NR / 16; ++g) {
-          uint4 vh, vl;
-          split_e4m3x4(&t[g * 16 + 0], vh.x, vl.x);
-          split_e4m3x4(&t[g * 16 + 4], vh.y, vl.y);
-          split_e4m3x4(&t[g * 16 + 8], vh.z, vl.z);
-          split_e4m3x4(&t[g * 16 + 12], vh.w, vl.w);
-          *reinterpret_cast<uint4*>(pbuf + g * 2048 + tok_lane * 16) = vh;
-          *reinterpret_cast<uint4*>(pbuf + C::kPHalf + g * 2048 + tok_lane * 16) = vl;
+        for (int g = 0; g < NRH / 8; ++g) {
+          const int row = rbase + g * 8;
+          uint2 vh, vl;
+          split_e4m3x4(&t[g * 8 + 0], vh.x, vl.x);
+          split_e4m3x4(&t[g * 8 + 4], vh.y, vl.y);
+          const uint32_t off = (row >> 4) * 2048 + tok_lane * 16 + (row & 15);
+          *reinterpret_cast<uint2*>(pbuf + off) = vh;
+          *reinterpret_cast<uint2*>(pbuf + C::kPHalf + off) = vl;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -746,14 +755,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Row sums of the unquantised weights, folded in by the owners after
       // the next tile's vote (double-buffered by tile parity).
-      warp_reduce_rows<NR, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR);
+      warp_reduce_rows<NRH, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR + rbase);
     }
     if (!ok && lane == 0) {
       report(p.status, MLA_ERR_TIMEOUT);
       *abort_flag = 1;
     }
     // ---- epilogue ----
-    named_bar_sync(kSoftmaxBarrier, 128);
+    named_bar_sync(kSoftmaxBarrier, NT);
     const bool single = (nsplit == 1);
     float* scale_s = alpha_s;
     if (sid < NR) {
@@ -778,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       scale_s[sid] = sc;
     }
-    named_bar_sync(kSoftmaxBarrier, 128);
+    named_bar_sync(kSoftmaxBarrier, NT);
     // The MMA warp commits BAR_FINAL once, after its last MMA.
     bool fin = mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
     fin = __all_sync(0xffffffffu, fin);
@@ -789,24 +798,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int d = 0; d < 4; ++d) {
         const int dim = d * 128 + tok_lane;
 #pragma unroll
-        for (int cc = 0; cc < NR / 16; ++cc) {
-          uint32_t r[16];
-          tmem_ld16(tmem + lane_addr + C::kOCol + d * C::OW + cc * 16, r);
-          if constexpr (C::kStack) {
-            uint32_t r2[16];
-            tmem_ld16(tmem + lane_addr + C::kOCol + d * C::OW + NR + cc * 16, r2);
-            tmem_ld_wait();
+        for (int cc = 0; cc < NRH / 8; ++cc) {
+          uint32_t r[8], r2[8];
+          const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + rbase + cc * 8;
+          tmem_ld8(addr, r);
+          tmem_ld8(addr + NR, r2);  // the lo term's product
+          tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-              r[k] = __float_as_uint(__uint_as_float(r[k]) + __uint_as_float(r2[k]));
-          } else {
-            tmem_ld_wait();
-          }
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int row = cc * 16 + k;
+          for (int k = 0; k < 8; ++k) {
+            const int row = rbase + cc * 8 + k;
             if (row < rows_here) {
-              const float v = __uint_as_float(r[k]) * scale_s[row];
+              const float v = (__uint_as_float(r[k]) + __uint_as_float(r2[k])) * scale_s[row];
               const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
               if (single) {
                 p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
@@ -1000,7 +1002,7 @@ static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages
       !make_map(&q_rope, q, q_rows, 64, NR, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   dim3 grid(prm.max_splits * groups, batch);
-  mla_split_kv_kernel<NR><<<grid, kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
+  mla_split_kv_kernel<NR><<<grid, C::kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
                                                                      q_rope, prm);
   return cudaGetLastError();
 }
