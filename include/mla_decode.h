@@ -179,6 +179,32 @@ MLA_API int mla_merge(const float* partial_o, const float* partial_ml, int32_t r
               int32_t kv_split, void* out_bf16, float* lse_f32, float* out_f32_debug,
               void* stream);
 
+/*
+ * FP8 paged KV append: quantize n_tokens new latent rows and scatter them into
+ * the paged cache that mla_decode reads (TensorRT-LLM PR #17273, "Fuse the DSv4
+ * MLA prologue": a latent row is quantized to FP8 and scattered into the paged
+ * cache; the model-specific RMSNorm and RoPE before it are not part of this
+ * library).
+ *
+ * rows_bf16     BF16 [n_tokens, 576] (512 latent + 64 rope), 16-byte aligned.
+ * req_idx       int32 [n_tokens]: request of each row (0 <= b < batch).
+ * positions     int32 [n_tokens]: token index of each row within its request;
+ *               it lands in slot pos % 32 of page page_table[b][pos / 32].
+ * page_table    int32 [batch, max_pages_per_req].
+ * kv_pages_fp8  E4M3 [num_pages, 32, 576], 8-byte aligned; written in place.
+ * kv_scale      the stored code is e4m3(x / kv_scale): IEEE fp32 division,
+ *               nearest E4M3 value with ties to even, magnitudes beyond 448
+ *               saturate to 448, NaN stays NaN.
+ * status        device int32 or NULL: set to MLA_ERR_INVALID_ARG if some row
+ *               had an out-of-range request, position or page id (that row is
+ *               skipped); never cleared by the call.
+ * Rows with the same (request, position) race; the caller keeps them unique.
+ */
+MLA_API int mla_kv_append(const void* rows_bf16, int64_t n_tokens, const int32_t* req_idx,
+                          const int32_t* positions, const int32_t* page_table,
+                          int32_t max_pages_per_req, int32_t batch, void* kv_pages_fp8,
+                          int64_t num_pages, float kv_scale, int32_t* status, void* stream);
+
 /* Synchronously reads the status word at the head of `workspace` (MLA_OK,
  * MLA_ERR_INVALID_ARG for a bad page id or inconsistent plan arrays,
  * MLA_ERR_TIMEOUT for a wait that ran out) after `stream` has drained, and

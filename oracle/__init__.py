@@ -62,6 +62,10 @@ def _load():
             lib.mla_oracle_decode_rows.argtypes = [
                 p, p, i64, p, i32, p, i32, i32, i32, i32, f64, f64, f64, p, i64, i64, i64, i32,
                 p, p, p, p, i32]
+            lib.mla_oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.mla_oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.mla_oracle_kv_append.restype = ctypes.c_int
+            lib.mla_oracle_kv_append.argtypes = [p, i64, p, p, p, i32, i32, p, i64, ctypes.c_float]
             lib.mla_oracle_merge.restype = None
             lib.mla_oracle_merge.argtypes = [p, p, i64, i32, p, p]
             _lib = lib
@@ -144,3 +148,33 @@ def merge(partial_o, partial_ml):
     lse = np.zeros((rows,), dtype=np.float64)
     lib.mla_oracle_merge(ml.ctypes.data, o.ctypes.data, rows, S, out.ctypes.data, lse.ctypes.data)
     return out, lse
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """Nearest E4M3 codes (ties to even, saturating at 448) of float32 values."""
+    lib = _load()
+    v = _np(values, np.float32)
+    out = np.array([lib.mla_oracle_e4m3_encode(float(x)) for x in v.reshape(-1)], dtype=np.uint8)
+    return out.reshape(v.shape)
+
+
+def kv_append(rows_bf16, req, pos, page_table, kv, kv_scale: float):
+    """Quantize bf16 rows [n, 576] (given as uint16/int16 bit patterns or a torch
+    bfloat16 tensor) into a copy of the uint8 pool kv [P, 32, 576]; returns the
+    new pool and the status (0, or -1 if some row had an invalid target)."""
+    lib = _load()
+    try:
+        import torch
+        if isinstance(rows_bf16, torch.Tensor) and rows_bf16.dtype == torch.bfloat16:
+            rows_bf16 = rows_bf16.view(torch.int16)
+    except ImportError:  # pragma: no cover
+        pass
+    r = _np(rows_bf16, np.int16).view(np.uint16)
+    rq = _np(req, np.int32)
+    ps = _np(pos, np.int32)
+    pt = _np(page_table, np.int32)
+    pool = _np(kv, np.uint8).copy()
+    st = lib.mla_oracle_kv_append(r.ctypes.data, int(r.shape[0]), rq.ctypes.data, ps.ctypes.data,
+                                  pt.ctypes.data, int(pt.shape[1]), int(pt.shape[0]),
+                                  pool.ctypes.data, int(pool.shape[0]), float(kv_scale))
+    return pool, int(st)

@@ -36,6 +36,15 @@
  *   LSE = ln 2 * (M + log2 sum_s w_s l_s); empty partials contribute nothing.
  *
  * Two passes over stored scores per row; no online rescaling, no blocking.
+ *
+ * KV append (the step that fills the paged cache; TensorRT-LLM PR #17273,
+ * "Fuse the DSv4 MLA prologue": a latent row is quantized to FP8 and scattered
+ * into the paged cache): each new 576-value row x of request b at token
+ * position j is stored as code = e4m3(x / kv_scale) in slot j % 32 of page
+ * page_table[b][j / 32].  The division is IEEE fp32 (the precision the
+ * quantised code is decided in on the device); e4m3() is the nearest E4M3
+ * value, ties to the even code, magnitudes beyond 448 saturate to 448, NaN
+ * stays NaN.
  */
 #include <math.h>
 #include <stdint.h>
@@ -227,4 +236,50 @@ void mla_oracle_merge(const double* ml, const double* o, int64_t rows, int32_t S
     for (int d = 0; d < ORC_LATENT_DIM; ++d) dst[d] /= den;
     lse[r] = log(2.0) * (M + log2(den));
   }
+}
+
+/* Nearest E4M3 code to v (ties to even), saturating at +-448; NaN -> 0x7F. */
+uint8_t mla_oracle_e4m3_encode(float v) {
+  double lut[256];
+  build_lut(lut);
+  if (v != v) return 0x7F;
+  double x = (double)v;
+  int neg = signbit(v) ? 1 : 0;
+  double a = neg ? -x : x;
+  if (a >= 448.0) return (uint8_t)(neg ? 0xFE : 0x7E);
+  /* Positive codes 0x00..0x7E are increasing in value. */
+  int best = 0;
+  for (int c = 0; c <= 0x7E; ++c) {
+    double d = fabs(lut[c] - a), db = fabs(lut[best] - a);
+    if (d < db || (d == db && (c & 1) == 0 && (best & 1) == 1)) best = c;
+  }
+  return (uint8_t)(neg ? (best | 0x80) : best);
+}
+
+/* Append: rows[n][576] are bf16 bit patterns (widened exactly to float). */
+int mla_oracle_kv_append(const uint16_t* rows_bf16, int64_t n, const int32_t* req,
+                         const int32_t* pos, const int32_t* page_table, int32_t max_pages,
+                         int32_t batch, uint8_t* kv, int64_t num_pages, float kv_scale) {
+  int status = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t b = req[i], j = pos[i];
+    if (b < 0 || b >= batch || j < 0 || j / ORC_PAGE >= max_pages) {
+      status = -1;
+      continue;
+    }
+    int64_t page = page_table[(int64_t)b * max_pages + j / ORC_PAGE];
+    if (page < 0 || page >= num_pages) {
+      status = -1;
+      continue;
+    }
+    uint8_t* dst = kv + (page * ORC_PAGE + j % ORC_PAGE) * ORC_HEAD_DIM;
+    for (int d = 0; d < ORC_HEAD_DIM; ++d) {
+      uint32_t bits = (uint32_t)rows_bf16[i * ORC_HEAD_DIM + d] << 16;
+      float x;
+      memcpy(&x, &bits, sizeof(x));
+      volatile float q = x / kv_scale; /* IEEE fp32 division */
+      dst[d] = mla_oracle_e4m3_encode(q);
+    }
+  }
+  return status;
 }

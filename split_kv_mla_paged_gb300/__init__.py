@@ -22,7 +22,7 @@ __all__ = [
     "MLA_ERR_CUDA", "MLA_ERR_TIMEOUT", "MlaError", "Plan", "load_library", "library_path",
     "mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init", "mla_decode",
     "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
-    "mla_decode_static_ws", "decode", "merge", "EXPORTED_SYMBOLS",
+    "mla_decode_static_ws", "mla_kv_append", "decode", "merge", "EXPORTED_SYMBOLS",
 ]
 
 MLA_OK = 0
@@ -38,7 +38,7 @@ _STATUS_NAMES = {
 EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init",
                     "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
                     "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit",
-                    "mla_decode_static_ws")
+                    "mla_decode_static_ws", "mla_kv_append")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
@@ -93,6 +93,8 @@ def load_library() -> ctypes.CDLL:
         lib.mla_decode_static_ws.restype = ctypes.c_int
         lib.mla_decode_static_ws.argtypes = [vp, vp, i64, vp, i32, vp, vp, vp, i32, i32, i32, i32,
                                              i32, i32, f32, f32, f32, vp, vp, vp, vp]
+        lib.mla_kv_append.restype = ctypes.c_int
+        lib.mla_kv_append.argtypes = [vp, i64, vp, vp, vp, i32, i32, vp, i64, f32, vp, vp]
         lib.mla_debug_set_wait_limit.restype = None
         lib.mla_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
         lib.mla_last_error.restype = ctypes.c_char_p
@@ -229,6 +231,16 @@ def mla_decode_static_ws(q_fp8, kv_pages_fp8, num_pages: int, page_table,
 
 
 STATIC_WS_BYTES = 16 * 1024 * 1024
+
+
+def mla_kv_append(rows_bf16, n_tokens: int, req_idx, positions, page_table,
+                  max_pages_per_req: int, batch: int, kv_pages_fp8, num_pages: int,
+                  kv_scale: float, status=None, stream=None) -> None:
+    """Quantize BF16 latent rows to E4M3 and scatter them into the paged cache."""
+    _check(load_library().mla_kv_append(
+        _ptr(rows_bf16), int(n_tokens), _ptr(req_idx), _ptr(positions), _ptr(page_table),
+        int(max_pages_per_req), int(batch), _ptr(kv_pages_fp8), int(num_pages), float(kv_scale),
+        _ptr(status), _stream_handle(stream)))
 
 
 def mla_debug_set_wait_limit(cycles: int) -> None:

@@ -9,7 +9,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB_NAME = "libmla_decode.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = [os.path.join(CSRC, "mla_decode.cu"), os.path.join(CSRC, "plan.cpp")]
+SOURCES = [os.path.join(CSRC, "mla_decode.cu"), os.path.join(CSRC, "kv_append.cu"),
+           os.path.join(CSRC, "plan.cpp")]
 DEPENDS = SOURCES + [
     os.path.join(CSRC, "mla_internal.h"),
     os.path.join(CSRC, "sm103_ptx.cuh"),

@@ -254,3 +254,55 @@ def test_merge_equals_pairwise_combination():
     out2, lse2 = oracle.merge(o2, ml2)
     np.testing.assert_allclose(out3, out2, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(lse3, lse2, rtol=0, atol=1e-12)
+
+
+# --- KV append: E4M3 encoder ----------------------------------------------
+
+def test_e4m3_encode_roundtrips_every_finite_code():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    enc = oracle.e4m3_encode(vals)
+    # -0.0 encodes to 0x80, +0.0 to 0x00: every code comes back.
+    assert np.array_equal(enc, codes)
+
+
+def test_e4m3_encode_matches_torch_cast_in_range():
+    g = torch.Generator().manual_seed(21)
+    x = (torch.randn(20000, generator=g) * torch.exp2(torch.randint(-12, 9, (20000,), generator=g)))
+    x = x.clamp(-440, 440).to(torch.float32)
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x.numpy()), ref)
+
+
+def test_e4m3_encode_ties_go_to_even_and_saturate():
+    # 1.0 + 1/16 lies halfway between 1.0 (0x38) and 1.125 (0x39): even code wins.
+    assert oracle.e4m3_encode(np.array([1.0625], np.float32))[0] == 0x38
+    # 1.125 + 1/16 lies between 0x39 and 0x3A: 0x3A is even.
+    assert oracle.e4m3_encode(np.array([1.1875], np.float32))[0] == 0x3A
+    # Halfway between the two smallest subnormals 2^-9 and 2^-8: 0x02 is even.
+    assert oracle.e4m3_encode(np.array([1.5 * 2.0 ** -9], np.float32))[0] == 0x02
+    assert oracle.e4m3_encode(np.array([1000.0, -1e30], np.float32)).tolist() == [0x7E, 0xFE]
+    assert oracle.e4m3_encode(np.array([np.nan], np.float32))[0] == 0x7F
+
+
+def test_kv_append_scatters_through_page_table():
+    pool = np.full((5, 32, 576), 0x7F, dtype=np.uint8)
+    table = np.array([[3, 1], [0, 4]], dtype=np.int32)
+    g = torch.Generator().manual_seed(22)
+    rows = (torch.randn(3, 576, generator=g)).to(torch.bfloat16)
+    req = np.array([0, 0, 1], np.int32)
+    pos = np.array([0, 33, 40], np.int32)
+    new, st = oracle.kv_append(rows, req, pos, table, pool, kv_scale=0.5)
+    assert st == 0
+    want = (rows.float() / 0.5).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(new[3, 0], want[0])
+    assert np.array_equal(new[1, 1], want[1])
+    assert np.array_equal(new[4, 8], want[2])
+    touched = {(3, 0), (1, 1), (4, 8)}
+    for pg in range(5):
+        for sl in range(32):
+            if (pg, sl) not in touched:
+                assert np.all(new[pg, sl] == 0x7F)
+    _, st = oracle.kv_append(rows[:1], np.array([2], np.int32), np.array([0], np.int32), table,
+                             pool, kv_scale=1.0)
+    assert st == -1
