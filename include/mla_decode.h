@@ -86,7 +86,8 @@ typedef enum {
  *              chosen to balance whole waves of one CTA per SM.
  * Outputs (host): splits_out[batch] (1..MLA_MAX_SPLITS), chunk_out[batch]
  *              (tokens per split, a multiple of 128, splits*chunk >= L),
- *              *kv_split_out (merge thread groups: 1, 2, 4, 8 or 16) and
+ *              *kv_split_out (merge thread groups: 1, 2, 4, 8 or 16, about
+ *              four partials per group) and
  *              *workspace_bytes_out for mla_decode with max(splits).
  */
 MLA_API int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t num_heads, int32_t q_len,

@@ -62,6 +62,10 @@ def _load():
             lib.mla_oracle_decode_rows.argtypes = [
                 p, p, i64, p, i32, p, i32, i32, i32, i32, f64, f64, f64, p, i64, i64, i64, i32,
                 p, p, p, p, i32]
+            lib.mla_oracle_decode_rows_ex.restype = ctypes.c_int
+            lib.mla_oracle_decode_rows_ex.argtypes = [
+                p, p, i64, p, i32, p, i32, i32, i32, i32, f64, f64, f64, p, f64, p, i64, i64,
+                i64, i32, p, p, p, p, i32]
             lib.mla_oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.mla_oracle_e4m3_encode.argtypes = [ctypes.c_float]
             lib.mla_oracle_kv_append.restype = ctypes.c_int
@@ -98,12 +102,13 @@ def e4m3_decode(codes) -> np.ndarray:
 def decode_rows(q, kv, page_table, kv_lens, *, q_len: int, num_heads: int, causal: bool,
                 softmax_scale: float, q_scale: float = 1.0, kv_scale: float = 1.0,
                 rows=None, tok_begin: int = -1, tok_end: int = -1, partial: bool = False,
-                n_threads: int = 0):
+                n_threads: int = 0, sinks=None, output_scale: float = 1.0):
     """Run the fp64 oracle on the given rows.
 
     q: uint8 [B, q_len, H, 576]; kv: uint8 [P, 32, 576]; page_table int32
     [B, max_pages]; kv_lens int32 [B].  rows: flat row ids (b*q_len+qi)*H+h,
-    default all.  Returns (O [n, 512], LSE [n]) or, with partial=True,
+    default all.  sinks: optional per-head sink logits [H] (natural-log units);
+    output_scale multiplies O.  Returns (O [n, 512], LSE [n]) or, with partial=True,
     (O_unnormalised [n, 512], m_log2 [n], l [n]).
     """
     lib = _load()
@@ -121,10 +126,12 @@ def decode_rows(q, kv, page_table, kv_lens, *, q_len: int, num_heads: int, causa
     m = np.zeros((n,), dtype=np.float64)
     l = np.zeros((n,), dtype=np.float64)
     num_pages = int(kva.shape[0])
-    st = lib.mla_oracle_decode_rows(
+    sk = None if sinks is None else _np(sinks, np.float64)
+    st = lib.mla_oracle_decode_rows_ex(
         qa.ctypes.data, kva.ctypes.data, num_pages, pt.ctypes.data, int(pt.shape[1]),
         lens.ctypes.data, batch, int(q_len), int(num_heads), int(bool(causal)), float(q_scale),
-        float(kv_scale), float(softmax_scale), ra.ctypes.data, n, int(tok_begin), int(tok_end),
+        float(kv_scale), float(softmax_scale), None if sk is None else sk.ctypes.data,
+        float(output_scale), ra.ctypes.data, n, int(tok_begin), int(tok_end),
         1 if partial else 0, out.ctypes.data, lse.ctypes.data, m.ctypes.data, l.ctypes.data,
         int(n_threads))
     if st != 0:

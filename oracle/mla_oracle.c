@@ -112,6 +112,15 @@ static const uint8_t* key_row(const uint8_t* kv, const int32_t* page_table, int3
  *         l_out[i] = l.
  * Returns 0, or -1 on an out-of-range page id, -2 on allocation failure.
  */
+int mla_oracle_decode_rows_ex(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
+                              const int32_t* page_table, int32_t max_pages,
+                              const int32_t* kv_lens, int32_t batch, int32_t q_len,
+                              int32_t num_heads, int32_t causal, double q_scale,
+                              double kv_scale, double softmax_scale, const double* sinks,
+                              double output_scale, const int64_t* rows, int64_t n_rows,
+                              int64_t tok_begin, int64_t tok_end, int32_t mode, double* out,
+                              double* lse, double* m_out, double* l_out, int32_t n_threads);
+
 int mla_oracle_decode_rows(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
                            const int32_t* page_table, int32_t max_pages,
                            const int32_t* kv_lens, int32_t batch, int32_t q_len,
@@ -120,6 +129,27 @@ int mla_oracle_decode_rows(const uint8_t* q, const uint8_t* kv, int64_t num_page
                            int64_t n_rows, int64_t tok_begin, int64_t tok_end, int32_t mode,
                            double* out, double* lse, double* m_out, double* l_out,
                            int32_t n_threads) {
+  return mla_oracle_decode_rows_ex(q, kv, num_pages, page_table, max_pages, kv_lens, batch,
+                                   q_len, num_heads, causal, q_scale, kv_scale, softmax_scale,
+                                   NULL, 1.0, rows, n_rows, tok_begin, tok_end, mode, out, lse,
+                                   m_out, l_out, n_threads);
+}
+
+/*
+ * Same, with per-head attention sinks and an output scale.  A sink is a
+ * virtual key of logit sinks[h] (natural-log units, compared with the scaled
+ * scores s_j) and zero value: Z gains exp(sink - M), O shrinks accordingly,
+ * LSE = ln(sum_j exp(s_j) + exp(sink)).  output_scale multiplies O only.
+ * Sinks and output_scale apply to mode 0 (final outputs) only.
+ */
+int mla_oracle_decode_rows_ex(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
+                              const int32_t* page_table, int32_t max_pages,
+                              const int32_t* kv_lens, int32_t batch, int32_t q_len,
+                              int32_t num_heads, int32_t causal, double q_scale,
+                              double kv_scale, double softmax_scale, const double* sinks,
+                              double output_scale, const int64_t* rows, int64_t n_rows,
+                              int64_t tok_begin, int64_t tok_end, int32_t mode, double* out,
+                              double* lse, double* m_out, double* l_out, int32_t n_threads) {
   double lut[256];
   int status = 0;
   build_lut(lut);
@@ -139,13 +169,13 @@ int mla_oracle_decode_rows(const uint8_t* q, const uint8_t* kv, int64_t num_page
     double qd[ORC_HEAD_DIM];
     double* o = out + i * ORC_LATENT_DIM;
     int64_t lo, hi;
-    (void)h;
     for (int d = 0; d < ORC_HEAD_DIM; ++d) qd[d] = q_scale * lut[q[r * ORC_HEAD_DIM + d]];
     row_range(kv_lens[b], q_len, qi, causal, tok_begin, tok_end, &lo, &hi);
     for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] = 0.0;
+    const double sink = (sinks && mode == 0) ? sinks[h] : -INFINITY;
     if (hi <= lo) {
       if (mode == 0) {
-        lse[i] = -INFINITY;
+        lse[i] = sink;
       } else {
         m_out[i] = -INFINITY;
         l_out[i] = 0.0;
@@ -172,11 +202,12 @@ int mla_oracle_decode_rows(const uint8_t* q, const uint8_t* kv, int64_t num_page
       for (int d = 0; d < ORC_HEAD_DIM; ++d) dot += qd[d] * (kv_scale * lut[k[d]]);
       s[j - lo] = softmax_scale * dot;
     }
-    double M = -INFINITY;
+    double M = sink;
     for (int64_t j = lo; j < hi; ++j)
       if (s[j - lo] > M) M = s[j - lo];
-    /* Pass 2: weights and the weighted sum of values. */
-    double Z = 0.0;
+    /* Pass 2: weights and the weighted sum of values (the sink adds weight
+       and no value). */
+    double Z = (sink == -INFINITY) ? 0.0 : exp(sink - M);
     for (int64_t j = lo; j < hi; ++j) {
       double w = exp(s[j - lo] - M);
       const uint8_t* k;
@@ -192,7 +223,7 @@ int mla_oracle_decode_rows(const uint8_t* q, const uint8_t* kv, int64_t num_page
       status = -1;
     }
     if (mode == 0) {
-      for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] /= Z;
+      for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] = output_scale * (o[d] / Z);
       lse[i] = M + log(Z);
     } else {
       m_out[i] = M * (1.0 / log(2.0));

@@ -823,6 +823,8 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  // This CTA's partials are written: the merge may start once every CTA is here.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -860,6 +862,8 @@ __global__ void __launch_bounds__(32 * G) mla_merge_kernel(const MergeParams p) 
   __shared__ float sm_m[G];
   __shared__ float sm_l[G];
   __shared__ float4 sm_o[G][32];
+  // Partials are written by the preceding (programmatically dependent) grid.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = blockIdx.y;
   const int quarter = blockIdx.x;
   const int g = threadIdx.x >> 5;
@@ -1002,16 +1006,36 @@ static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages
   return cudaGetLastError();
 }
 
+// The merge is launched as a programmatic dependent of whatever precedes it
+// on the stream (the split-KV kernel in mla_decode): its CTAs may be scheduled
+// while the split kernel drains and wait in griddepcontrol.wait until the
+// partials are visible.  Launched after anything else, the wait returns at once.
+template <int G>
+static cudaError_t launch_merge_g(const MergeParams& mp, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(4, mp.rows);
+  cfg.blockDim = dim3(32 * G);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_merge_kernel<G>, mp);
+}
+
 static cudaError_t launch_merge(const MergeParams& mp, int kv_split, cudaStream_t stream) {
-  dim3 grid(4, mp.rows);
+  cudaError_t e;
   switch (kv_split) {
-    case 1: mla_merge_kernel<1><<<grid, 32, 0, stream>>>(mp); break;
-    case 2: mla_merge_kernel<2><<<grid, 64, 0, stream>>>(mp); break;
-    case 4: mla_merge_kernel<4><<<grid, 128, 0, stream>>>(mp); break;
-    case 8: mla_merge_kernel<8><<<grid, 256, 0, stream>>>(mp); break;
-    case 16: mla_merge_kernel<16><<<grid, 512, 0, stream>>>(mp); break;
+    case 1: e = launch_merge_g<1>(mp, stream); break;
+    case 2: e = launch_merge_g<2>(mp, stream); break;
+    case 4: e = launch_merge_g<4>(mp, stream); break;
+    case 8: e = launch_merge_g<8>(mp, stream); break;
+    case 16: e = launch_merge_g<16>(mp, stream); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -132,8 +132,10 @@ extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t nu
   }
   int32_t max_splits = 1;
   for (int b = 0; b < batch; ++b) max_splits = std::max(max_splits, splits_out[b]);
+  // Merge thread groups: about four partials per group (each group keeps four
+  // loads in flight), at most 16 groups.
   int32_t g = 16;
-  while (g > max_splits) g >>= 1;
+  while (g > 1 && g * 4 > max_splits) g >>= 1;
   *kv_split_out = g;
   *workspace_bytes_out = mla_decode_workspace_size(batch, q_len, num_heads, max_splits);
   return MLA_OK;

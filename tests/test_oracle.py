@@ -306,3 +306,42 @@ def test_kv_append_scatters_through_page_table():
     _, st = oracle.kv_append(rows[:1], np.array([2], np.int32), np.array([0], np.int32), table,
                              pool, kv_scale=1.0)
     assert st == -1
+
+
+# --- sinks and output scale --------------------------------------------------
+
+def test_sink_at_minus_infinity_changes_nothing_and_output_scale_is_linear():
+    inp = decode_inputs(1, 3, 2, [90], seed=23)
+    kw = dict(q_len=2, num_heads=3, causal=True, softmax_scale=0.2)
+    o1, l1 = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, **kw)
+    o2, l2 = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens,
+                                sinks=np.full(3, -np.inf), output_scale=2.5, **kw)
+    np.testing.assert_array_equal(l1, l2)
+    np.testing.assert_allclose(o2, 2.5 * o1, rtol=1e-15, atol=0)
+
+
+def test_sink_single_key_closed_form():
+    inp = decode_inputs(1, 2, 1, [1], seed=24)
+    sinks = np.array([0.3, -1.7])
+    o, l = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=1, num_heads=2,
+                              causal=False, softmax_scale=0.25, sinks=sinks)
+    k = _widen(inp.kv[int(inp.page_table[0, 0]), 0]).numpy()
+    for h in range(2):
+        s0 = 0.25 * float(_widen(inp.q[0, 0, h]).numpy() @ k)
+        w = math.exp(s0) / (math.exp(s0) + math.exp(sinks[h]))
+        np.testing.assert_allclose(o[h], w * k[:LATENT_DIM], rtol=1e-13, atol=1e-15)
+        assert l[h] == pytest.approx(math.log(math.exp(s0) + math.exp(sinks[h])), abs=1e-13)
+
+
+def test_sink_equal_scores_mean_shrinks():
+    inp = decode_inputs(1, 1, 1, [40], seed=25)
+    inp.q[..., :LATENT_DIM] = 0
+    inp.kv[..., LATENT_DIM:] = inp.kv[0, 0, LATENT_DIM:]
+    keys = _widen(_gather_keys(inp, 0))
+    s = SOFTMAX_SCALE * float(_widen(inp.q[0, 0, 0]) @ keys[0])
+    sink = s + math.log(10.0)  # the sink weighs as much as 10 keys
+    o, l = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=1, num_heads=1,
+                              causal=False, softmax_scale=SOFTMAX_SCALE, sinks=np.array([sink]))
+    np.testing.assert_allclose(o[0], keys[:, :LATENT_DIM].mean(0).numpy() * 40 / 50, rtol=1e-12,
+                               atol=1e-15)
+    assert l[0] == pytest.approx(s + math.log(50.0), abs=1e-12)
