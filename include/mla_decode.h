@@ -131,6 +131,39 @@ MLA_API int mla_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_
                void* stream);
 
 /*
+ * Options of mla_decode_ex (issue #20510, "Repro 1/2" run() arguments and the
+ * follow-up's device-side scales; PR #20380, "Description": sinks are handled
+ * in the merge).
+ *
+ * q_scale_dev, kv_scale_dev, softmax_scale_dev  device fp32 pointers or NULL.
+ *     When set, element 0 is read by the kernels instead of the host value, so
+ *     a captured CUDA graph picks up new scales on replay without a host read.
+ * output_scale  multiplies O (BF16 and fp32 outputs), not the LSE.  1 = off.
+ * sinks  NULL or device fp32 [num_heads]: per-head attention-sink logit in the
+ *     units of the scaled scores (natural log).  A sink acts as one more key
+ *     with that logit and a zero value: it joins the softmax denominator, so
+ *     O shrinks and LSE = ln(sum_j exp(s_j) + exp(sink)).
+ */
+typedef struct {
+  const float* q_scale_dev;
+  const float* kv_scale_dev;
+  const float* softmax_scale_dev;
+  float output_scale;
+  const float* sinks;
+} mla_decode_options_t;
+
+/* mla_decode with options (NULL options = mla_decode).  Same arguments,
+ * checks and results otherwise. */
+MLA_API int mla_decode_ex(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                          const int32_t* page_table, int32_t max_pages_per_req,
+                          const int32_t* kv_lens, const int32_t* splits, const int32_t* chunks,
+                          int32_t max_splits, int32_t kv_split, int32_t batch, int32_t q_len,
+                          int32_t num_heads, int32_t causal, float q_scale, float kv_scale,
+                          float softmax_scale, void* workspace, size_t workspace_bytes,
+                          void* out_bf16, float* lse_f32, float* out_f32_debug,
+                          const mla_decode_options_t* options, void* stream);
+
+/*
  * The two phases of mla_decode, for callers that schedule them separately
  * (to overlap other work, or to time the kernels one by one).  Same arguments
  * and checks as mla_decode.  mla_decode_splitkv launches the split-KV kernel:

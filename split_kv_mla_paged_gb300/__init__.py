@@ -22,7 +22,8 @@ __all__ = [
     "MLA_ERR_CUDA", "MLA_ERR_TIMEOUT", "MlaError", "Plan", "load_library", "library_path",
     "mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init", "mla_decode",
     "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
-    "mla_decode_static_ws", "mla_kv_append", "decode", "merge", "EXPORTED_SYMBOLS",
+    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "DecodeOptions", "decode", "merge",
+    "EXPORTED_SYMBOLS",
 ]
 
 MLA_OK = 0
@@ -38,13 +39,20 @@ _STATUS_NAMES = {
 EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init",
                     "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
                     "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit",
-                    "mla_decode_static_ws", "mla_kv_append")
+                    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
 PAGE_SIZE = 32
 TILE_TOKENS = 128
 MAX_SPLITS = 128
+
+
+class DecodeOptions(ctypes.Structure):
+    """mla_decode_options_t (include/mla_decode.h)."""
+    _fields_ = [("q_scale_dev", ctypes.c_void_p), ("kv_scale_dev", ctypes.c_void_p),
+                ("softmax_scale_dev", ctypes.c_void_p), ("output_scale", ctypes.c_float),
+                ("sinks", ctypes.c_void_p)]
 
 
 class MlaError(RuntimeError):
@@ -84,6 +92,8 @@ def load_library() -> ctypes.CDLL:
         for name in ("mla_decode", "mla_decode_splitkv", "mla_decode_merge"):
             getattr(lib, name).restype = ctypes.c_int
             getattr(lib, name).argtypes = dec_args
+        lib.mla_decode_ex.restype = ctypes.c_int
+        lib.mla_decode_ex.argtypes = dec_args[:-1] + [ctypes.POINTER(DecodeOptions), vp]
         lib.mla_decode_workspace_init.restype = ctypes.c_int
         lib.mla_decode_workspace_init.argtypes = [vp, sz, vp]
         lib.mla_merge.restype = ctypes.c_int
@@ -186,6 +196,25 @@ def _decode_call(fn_name, q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_
               _stream_handle(stream)))
 
 
+def mla_decode_ex(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req, kv_lens, splits,
+                  chunks, max_splits, kv_split, batch, q_len, num_heads, causal, q_scale,
+                  kv_scale, softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32=None,
+                  out_f32_debug=None, *, q_scale_dev=None, kv_scale_dev=None,
+                  softmax_scale_dev=None, output_scale: float = 1.0, sinks=None,
+                  stream=None) -> None:
+    """mla_decode with device-side scales, an output scale and attention sinks."""
+    opts = DecodeOptions(_ptr(q_scale_dev), _ptr(kv_scale_dev), _ptr(softmax_scale_dev),
+                         float(output_scale), _ptr(sinks))
+    lib = load_library()
+    _check(lib.mla_decode_ex(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages), _ptr(page_table),
+                             int(max_pages_per_req), _ptr(kv_lens), _ptr(splits), _ptr(chunks),
+                             int(max_splits), int(kv_split), int(batch), int(q_len),
+                             int(num_heads), 1 if causal else 0, float(q_scale), float(kv_scale),
+                             float(softmax_scale), _ptr(workspace), int(workspace_bytes),
+                             _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
+                             ctypes.byref(opts), _stream_handle(stream)))
+
+
 def mla_decode_splitkv(*args, **kw) -> None:
     """Split-KV phase of mla_decode (same arguments)."""
     _decode_call("mla_decode_splitkv", *args, **kw)
@@ -264,7 +293,8 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
            causal: bool, softmax_scale: float, q_scale: float = 1.0, kv_scale: float = 1.0,
            plan: Optional[Plan] = None, sm_count: Optional[int] = None, target_ctas: int = 0,
            kv_split: Optional[int] = None, want_f32: bool = False, stream=None,
-           check_status: bool = True):
+           check_status: bool = True, sinks=None, output_scale: float = 1.0,
+           device_scales: bool = False):
     """Plan, allocate outputs and a workspace with torch, and run mla_decode.
 
     q_fp8 uint8 [B, q, H, 576] and kv_pages_fp8 uint8 [P, 32, 576] (E4M3 codes)
@@ -290,9 +320,25 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
     lse = torch.empty((batch, q_len, num_heads), dtype=torch.float32, device=dev)
     out_f32 = (torch.empty((batch, q_len, num_heads, LATENT_DIM), dtype=torch.float32, device=dev)
                if want_f32 else None)
-    mla_decode(q_fp8, kv_pages_fp8, kv_pages_fp8.shape[0], page_table, page_table.shape[1],
-               lens_d, splits_d, chunks_d, plan.max_splits, ks, batch, q_len, num_heads, causal,
-               q_scale, kv_scale, softmax_scale, ws, ws_bytes, out, lse, out_f32, stream)
+    common = (q_fp8, kv_pages_fp8, kv_pages_fp8.shape[0], page_table, page_table.shape[1],
+              lens_d, splits_d, chunks_d, plan.max_splits, ks, batch, q_len, num_heads, causal)
+    if sinks is None and output_scale == 1.0 and not device_scales:
+        mla_decode(*common, q_scale, kv_scale, softmax_scale, ws, ws_bytes, out, lse, out_f32,
+                   stream)
+    else:
+        dev_s = None
+        if device_scales:
+            dev_s = torch.tensor([q_scale, kv_scale, softmax_scale], dtype=torch.float32,
+                                 device=dev)
+        sk = None if sinks is None else torch.as_tensor(sinks, dtype=torch.float32).to(dev)
+        # With device scales the host values are placeholders the kernel must
+        # ignore (deliberately wrong, so a kernel that used them would fail).
+        host = (99.0,) * 3 if device_scales else (q_scale, kv_scale, softmax_scale)
+        mla_decode_ex(*common, *host, ws, ws_bytes, out, lse, out_f32,
+                      q_scale_dev=None if dev_s is None else dev_s[0:1],
+                      kv_scale_dev=None if dev_s is None else dev_s[1:2],
+                      softmax_scale_dev=None if dev_s is None else dev_s[2:3],
+                      output_scale=output_scale, sinks=sk, stream=stream)
     if check_status:
         mla_decode_status(ws, stream)
     return out, lse, out_f32

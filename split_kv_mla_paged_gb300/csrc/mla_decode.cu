@@ -74,6 +74,15 @@ struct DecodeParams {
   int32_t rows_per_group;  // RG
   float c_log2;            // softmax_scale * q_scale * kv_scale * log2(e)
   float kv_scale;
+  // Optional device-side scales (element 0 is read by the kernel, so a graph
+  // replay picks up new values); NULL means the host value above.
+  const float* q_scale_dev;
+  const float* kv_scale_dev;
+  const float* sm_scale_dev;
+  float q_scale_h;
+  float sm_scale_h;
+  float output_scale;      // multiplies O (not the LSE)
+  const float* sinks;      // optional per-head sink logits (natural-log units)
   long long wait_cycles;   // limit of the pipeline waits (drains always use the long limit)
   int* status;
   float* ws_ml;
@@ -302,6 +311,13 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
   const int tok_begin = split * chunk;
   const int tok_end = min(L, tok_begin + chunk);
   const int n_tiles = (tok_end - tok_begin + kTileTokens - 1) / kTileTokens;
+  float c_log2 = p.c_log2, kv_scale = p.kv_scale;
+  if (p.q_scale_dev || p.kv_scale_dev || p.sm_scale_dev) {
+    const float qs = p.q_scale_dev ? *p.q_scale_dev : p.q_scale_h;
+    kv_scale = p.kv_scale_dev ? *p.kv_scale_dev : p.kv_scale;
+    const float ss = p.sm_scale_dev ? *p.sm_scale_dev : p.sm_scale_h;
+    c_log2 = ss * qs * kv_scale * 1.4426950408889634f;
+  }
   const int row0 = grp * p.rows_per_group;                       // first row of this group
   const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
 
@@ -589,7 +605,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     float kreg[NRH];          // this thread's copy of its rows' references
 #pragma unroll
     for (int k = 0; k < NRH; ++k) kreg[k] = -INFINITY;
-    const float c = p.c_log2;
+    const float c = c_log2;
     // Smallest visibility limit over this group's rows (MTP verify: the first
     // query token of the block sees the fewest keys).
     const int qi_first = row0 / p.num_heads;
@@ -770,14 +786,21 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       float sc = 0.0f;
       if (sid < rows_here) {
         if (single) {
-          const float ls = (l_row > 0.0f) ? 0.6931471805599453f * (m_s + log2f(l_row)) : -INFINITY;
+          // A sink is one more (zero-valued) key: it joins the denominator.
+          const float sink2 = p.sinks
+                                  ? p.sinks[(row0 + sid) % p.num_heads] * 1.4426950408889634f
+                                  : -INFINITY;
+          const float mm = fmaxf(l_row > 0.0f ? m_s : -INFINITY, sink2);
+          const float a = (l_row > 0.0f) ? exp2f(m_s - mm) : 0.0f;
+          const float den = l_row * a + (sink2 == -INFINITY ? 0.0f : exp2f(sink2 - mm));
+          const float ls = (den > 0.0f) ? 0.6931471805599453f * (mm + log2f(den)) : -INFINITY;
           if (p.lse) p.lse[grow] = ls;
-          sc = (l_row > 0.0f) ? p.kv_scale / l_row : 0.0f;
+          sc = (den > 0.0f) ? kv_scale * p.output_scale * a / den : 0.0f;
         } else {
           float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
           ml[0] = m_s;
           ml[1] = l_row;
-          sc = p.kv_scale;
+          sc = kv_scale;
         }
       }
       scale_s[sid] = sc;
@@ -851,6 +874,9 @@ struct MergeParams {
   int32_t uniform_s;     // slots per row when splits == nullptr
   const int32_t* splits; // per-request slot counts (decode path) or nullptr
   int32_t rows_per_req;
+  int32_t num_heads;       // row r belongs to head r % num_heads (for sinks)
+  float output_scale;
+  const float* sinks;      // optional per-head sink logits (natural-log units)
   __nv_bfloat16* out;
   float* lse;
   float* out_f32;
@@ -934,8 +960,14 @@ __global__ void __launch_bounds__(32 * G) mla_merge_kernel(const MergeParams p) 
     }
     m = M;
   }
-  const bool empty = !(l > 0.0f);
-  const float inv = empty ? 0.0f : 1.0f / l;
+  if (!(l > 0.0f)) m = -INFINITY;
+  // A sink is one more (zero-valued) key: it joins the denominator.
+  const float sink2 = p.sinks ? p.sinks[row % p.num_heads] * 1.4426950408889634f : -INFINITY;
+  const float mm = fmaxf(m, sink2);
+  const float a = (m == -INFINITY) ? 0.0f : exp2_exact_int(m - mm);
+  const float den = l * a + (sink2 == -INFINITY ? 0.0f : exp2f(sink2 - mm));
+  const bool empty = !(den > 0.0f);
+  const float inv = empty ? 0.0f : p.output_scale * a / den;
   const float4 r = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
   const int64_t off = static_cast<int64_t>(row) * MLA_LATENT_DIM + dim;
   __nv_bfloat162 lo = __floats2bfloat162_rn(r.x, r.y);
@@ -946,7 +978,7 @@ __global__ void __launch_bounds__(32 * G) mla_merge_kernel(const MergeParams p) 
   *reinterpret_cast<uint2*>(p.out + off) = packed;
   if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + off) = r;
   if (p.lse && quarter == 0 && lane == 0)
-    p.lse[row] = empty ? -INFINITY : 0.6931471805599453f * (m + log2f(l));
+    p.lse[row] = empty ? -INFINITY : 0.6931471805599453f * (mm + log2f(den));
 }
 
 // ---------------------------------------------------------------------------
@@ -1143,6 +1175,13 @@ static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
   prm.c_log2 = static_cast<float>(static_cast<double>(softmax_scale) * q_scale * kv_scale *
                                   1.4426950408889634);
   prm.kv_scale = kv_scale;
+  prm.q_scale_dev = nullptr;
+  prm.kv_scale_dev = nullptr;
+  prm.sm_scale_dev = nullptr;
+  prm.q_scale_h = q_scale;
+  prm.sm_scale_h = softmax_scale;
+  prm.output_scale = 1.0f;
+  prm.sinks = nullptr;
   {
     const long long w = g_wait_cycles.load();
     prm.wait_cycles = w > 0 ? w : kWaitLimitCycles;
@@ -1161,6 +1200,9 @@ static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
   mp.uniform_s = max_splits;
   mp.splits = splits;
   mp.rows_per_req = num_heads * q_len;
+  mp.num_heads = num_heads;
+  mp.output_scale = 1.0f;
+  mp.sinks = nullptr;
   mp.out = prm.out;
   mp.lse = lse_f32;
   mp.out_f32 = out_f32_debug;
@@ -1207,6 +1249,36 @@ extern "C" int mla_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
   DecodeLaunch dl;
   int rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode", &dl);
   if (rc != MLA_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
+  if (rc != MLA_OK) return rc;
+  return launch_decode_merge(dl, st);
+}
+
+extern "C" int mla_decode_ex(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                             const int32_t* page_table, int32_t max_pages_per_req,
+                             const int32_t* kv_lens, const int32_t* splits, const int32_t* chunks,
+                             int32_t max_splits, int32_t kv_split, int32_t batch, int32_t q_len,
+                             int32_t num_heads, int32_t causal, float q_scale, float kv_scale,
+                             float softmax_scale, void* workspace, size_t workspace_bytes,
+                             void* out_bf16, float* lse_f32, float* out_f32_debug,
+                             const mla_decode_options_t* options, void* stream) {
+  DecodeLaunch dl;
+  int rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode_ex", &dl);
+  if (rc != MLA_OK) return rc;
+  if (options) {
+    if (!std::isfinite(options->output_scale)) {
+      set_error("mla_decode_ex: output_scale must be finite");
+      return MLA_ERR_INVALID_ARG;
+    }
+    dl.prm.q_scale_dev = options->q_scale_dev;
+    dl.prm.kv_scale_dev = options->kv_scale_dev;
+    dl.prm.sm_scale_dev = options->softmax_scale_dev;
+    dl.prm.output_scale = options->output_scale;
+    dl.prm.sinks = options->sinks;
+    dl.mp.output_scale = options->output_scale;
+    dl.mp.sinks = options->sinks;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
   if (rc != MLA_OK) return rc;
@@ -1363,6 +1435,9 @@ extern "C" int mla_merge(const float* partial_o, const float* partial_ml, int32_
   mp.uniform_s = num_ctas_kv;
   mp.splits = nullptr;
   mp.rows_per_req = 1;
+  mp.num_heads = 1;
+  mp.output_scale = 1.0f;
+  mp.sinks = nullptr;
   mp.out = reinterpret_cast<__nv_bfloat16*>(out_bf16);
   mp.lse = lse_f32;
   mp.out_f32 = out_f32_debug;
