@@ -169,21 +169,45 @@ __device__ __forceinline__ float pow2i(int i) { return __int_as_float((i + 127) 
 
 // 2^(t - k + 8) with exact power-of-two scaling (k integer-valued): split
 // t = r + f with r = rint(t), then 2^f * 2^(r - k + 8), the second factor
-// built from its exponent bits.  Branch-free: the rounding uses the
-// 1.5 * 2^23 addition trick (exact for |t| <= 2^21, so t is clamped there;
-// t far below k comes out as 0 through the exponent clamp, -inf by a select).
-// Scores of magnitude above 2^21 in log2 units are outside the supported range.
+// built from its exponent bits.  The rounding uses the 1.5 * 2^23 addition
+// trick (FMA-pipe adds instead of rint and float-to-int conversions), exact
+// for |t| < 2^21.  Two forms with the same values there, chosen per kernel
+// configuration by measurement: kBranchFree clamps t to +-2^21 and flushes
+// t far below k to 0 through the exponent clamp (-inf by a select), which
+// keeps the many independent weights of a 24-row thread in flight; the other
+// form takes an exact fallback branch for |t| >= 2^21 or -inf, which is
+// faster for the 16-row kernel.  Scores above 2^21 in log2 units are outside
+// the branch-free form's range.
+template <bool kBranchFree>
 __device__ __forceinline__ float softmax_weight(float t, float k) {
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-  const float tc = fminf(fmaxf(t, -2097152.0f), 2097152.0f);
-  const float tr = tc + kMagic;
-  const float r = tr - kMagic;            // rint(tc)
-  const float f = tc - r;                 // exact, |f| <= 0.5
-  const float ef = fmaxf((r - k) + 8.0f, -200.0f);  // integer-valued; exact
-  int e = __float_as_int(ef + kMagic) - 0x4B400000 + 127;
-  e = max(e, 0);                          // below 2^-126 the weight is flushed to 0
-  const float w = ex2_approx(f) * __int_as_float(e << 23);
-  return t == -INFINITY ? 0.0f : w;       // masked (the row's k may still be -inf)
+  if constexpr (kBranchFree) {
+    const float tc = fminf(fmaxf(t, -2097152.0f), 2097152.0f);
+    const float tr = tc + kMagic;
+    const float r = tr - kMagic;            // rint(tc)
+    const float f = tc - r;                 // exact, |f| <= 0.5
+    const float ef = fmaxf((r - k) + 8.0f, -200.0f);  // integer-valued; exact
+    int e = __float_as_int(ef + kMagic) - 0x4B400000 + 127;
+    e = max(e, 0);                          // below 2^-126 the weight is flushed to 0
+    const float w = ex2_approx(f) * __int_as_float(e << 23);
+    return t == -INFINITY ? 0.0f : w;       // masked (the row's k may still be -inf)
+  } else {
+    if (fabsf(t) < 2097152.0f) {
+      const float tr = t + kMagic;
+      const float r = tr - kMagic;          // rint(t)
+      const float f = t - r;                // exact, |f| <= 0.5
+      const float ef = (r - k) + 8.0f;      // integer-valued and exact
+      int e = __float_as_int(ef + kMagic) - 0x4B400000 + 127;
+      e = max(e, 0);
+      return ex2_approx(f) * __int_as_float(e << 23);
+    }
+    if (t == -INFINITY) return 0.0f;
+    const float a = rintf(t);
+    const float f = t - a;
+    const int sc = static_cast<int>(a) - static_cast<int>(k) + 8;
+    if (sc < -126) return 0.0f;
+    return ex2_approx(f) * pow2i(sc);
+  }
 }
 
 // Named barrier over `nthreads` threads that also ORs a predicate across them.
@@ -734,7 +758,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       }
       // Weights 2^(t - k + 8), exact power-of-two scaling.
 #pragma unroll
-      for (int k = 0; k < NRH; ++k) t[k] = softmax_weight(t[k], kreg[k]);
+      for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], kreg[k]);
       // P^T as two E4M3 terms into shared memory, MN-major:
       // [term][NR/16 row groups][128 tokens][16 rows]; this thread writes its
       // token's bytes for rows rbase .. rbase + NRH, 8 rows per store.
