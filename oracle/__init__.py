@@ -64,8 +64,8 @@ def _load():
                 p, p, p, p, i32]
             lib.mla_oracle_decode_rows_ex.restype = ctypes.c_int
             lib.mla_oracle_decode_rows_ex.argtypes = [
-                p, p, i64, p, i32, p, i32, i32, i32, i32, f64, f64, f64, p, f64, p, i64, i64,
-                i64, i32, p, p, p, p, i32]
+                p, p, i32, i64, p, i32, p, i32, i32, i32, i32, f64, f64, f64, p, f64, p, i64,
+                i64, i64, i32, p, p, p, p, i32]
             lib.mla_oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.mla_oracle_e4m3_encode.argtypes = [ctypes.c_float]
             lib.mla_oracle_kv_append.restype = ctypes.c_int
@@ -105,15 +105,29 @@ def decode_rows(q, kv, page_table, kv_lens, *, q_len: int, num_heads: int, causa
                 n_threads: int = 0, sinks=None, output_scale: float = 1.0):
     """Run the fp64 oracle on the given rows.
 
-    q: uint8 [B, q_len, H, 576]; kv: uint8 [P, 32, 576]; page_table int32
+    q: uint8 [B, q_len, H, 576]; kv: uint8 [P, 32, 576] (E4M3 codes), or both
+    torch bfloat16 tensors (the BF16-KV variant); page_table int32
     [B, max_pages]; kv_lens int32 [B].  rows: flat row ids (b*q_len+qi)*H+h,
     default all.  sinks: optional per-head sink logits [H] (natural-log units);
     output_scale multiplies O.  Returns (O [n, 512], LSE [n]) or, with partial=True,
     (O_unnormalised [n, 512], m_log2 [n], l [n]).
     """
     lib = _load()
-    qa = _np(q, np.uint8)
-    kva = _np(kv, np.uint8)
+    dtype = 0
+    try:
+        import torch
+        if isinstance(q, torch.Tensor) and q.dtype in (torch.bfloat16, torch.int16):
+            dtype = 1
+            q = q.view(torch.int16)
+            kv = kv.view(torch.int16)
+    except ImportError:  # pragma: no cover
+        pass
+    if dtype == 0:
+        qa = _np(q, np.uint8)
+        kva = _np(kv, np.uint8)
+    else:
+        qa = _np(q, np.int16)
+        kva = _np(kv, np.int16)
     pt = _np(page_table, np.int32)
     lens = _np(kv_lens, np.int32)
     batch = int(lens.shape[0])
@@ -128,7 +142,7 @@ def decode_rows(q, kv, page_table, kv_lens, *, q_len: int, num_heads: int, causa
     num_pages = int(kva.shape[0])
     sk = None if sinks is None else _np(sinks, np.float64)
     st = lib.mla_oracle_decode_rows_ex(
-        qa.ctypes.data, kva.ctypes.data, num_pages, pt.ctypes.data, int(pt.shape[1]),
+        qa.ctypes.data, kva.ctypes.data, dtype, num_pages, pt.ctypes.data, int(pt.shape[1]),
         lens.ctypes.data, batch, int(q_len), int(num_heads), int(bool(causal)), float(q_scale),
         float(kv_scale), float(softmax_scale), None if sk is None else sk.ctypes.data,
         float(output_scale), ra.ctypes.data, n, int(tok_begin), int(tok_end),

@@ -97,10 +97,20 @@ static void row_range(int32_t L, int32_t q_len, int32_t qi, int32_t causal,
   *hi = b;
 }
 
-static const uint8_t* key_row(const uint8_t* kv, const int32_t* page_table, int32_t max_pages,
-                              int32_t b, int64_t j) {
+/* Value d of the 576-value row at element index `row` of an array of
+ * element type dtype: 0 = E4M3 codes (uint8), 1 = BF16 bit patterns (uint16,
+ * widened exactly: the 16 bits are the top half of an IEEE float). */
+static double elem(const void* base, int dtype, int64_t row, int d, const double lut[256]) {
+  if (dtype == 0) return lut[((const uint8_t*)base)[row * ORC_HEAD_DIM + d]];
+  uint32_t bits = (uint32_t)((const uint16_t*)base)[row * ORC_HEAD_DIM + d] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof(f));
+  return (double)f;
+}
+
+static int64_t key_index(const int32_t* page_table, int32_t max_pages, int32_t b, int64_t j) {
   int64_t page = page_table[(int64_t)b * max_pages + j / ORC_PAGE];
-  return kv + ((page * ORC_PAGE) + (j % ORC_PAGE)) * ORC_HEAD_DIM;
+  return page * ORC_PAGE + (j % ORC_PAGE);
 }
 
 /*
@@ -112,7 +122,7 @@ static const uint8_t* key_row(const uint8_t* kv, const int32_t* page_table, int3
  *         l_out[i] = l.
  * Returns 0, or -1 on an out-of-range page id, -2 on allocation failure.
  */
-int mla_oracle_decode_rows_ex(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
+int mla_oracle_decode_rows_ex(const void* q, const void* kv, int32_t dtype, int64_t num_pages,
                               const int32_t* page_table, int32_t max_pages,
                               const int32_t* kv_lens, int32_t batch, int32_t q_len,
                               int32_t num_heads, int32_t causal, double q_scale,
@@ -129,20 +139,22 @@ int mla_oracle_decode_rows(const uint8_t* q, const uint8_t* kv, int64_t num_page
                            int64_t n_rows, int64_t tok_begin, int64_t tok_end, int32_t mode,
                            double* out, double* lse, double* m_out, double* l_out,
                            int32_t n_threads) {
-  return mla_oracle_decode_rows_ex(q, kv, num_pages, page_table, max_pages, kv_lens, batch,
+  return mla_oracle_decode_rows_ex(q, kv, 0, num_pages, page_table, max_pages, kv_lens, batch,
                                    q_len, num_heads, causal, q_scale, kv_scale, softmax_scale,
                                    NULL, 1.0, rows, n_rows, tok_begin, tok_end, mode, out, lse,
                                    m_out, l_out, n_threads);
 }
 
 /*
- * Same, with per-head attention sinks and an output scale.  A sink is a
+ * Same, with per-head attention sinks, an output scale, and the element type
+ * of Q and KV (dtype 0: E4M3 codes; 1: BF16, the pages' BF16-KV kernel,
+ * issue #20510 "Repro 2" comparison, same geometry).  A sink is a
  * virtual key of logit sinks[h] (natural-log units, compared with the scaled
  * scores s_j) and zero value: Z gains exp(sink - M), O shrinks accordingly,
  * LSE = ln(sum_j exp(s_j) + exp(sink)).  output_scale multiplies O only.
  * Sinks and output_scale apply to mode 0 (final outputs) only.
  */
-int mla_oracle_decode_rows_ex(const uint8_t* q, const uint8_t* kv, int64_t num_pages,
+int mla_oracle_decode_rows_ex(const void* q, const void* kv, int32_t dtype, int64_t num_pages,
                               const int32_t* page_table, int32_t max_pages,
                               const int32_t* kv_lens, int32_t batch, int32_t q_len,
                               int32_t num_heads, int32_t causal, double q_scale,
@@ -169,7 +181,7 @@ int mla_oracle_decode_rows_ex(const uint8_t* q, const uint8_t* kv, int64_t num_p
     double qd[ORC_HEAD_DIM];
     double* o = out + i * ORC_LATENT_DIM;
     int64_t lo, hi;
-    for (int d = 0; d < ORC_HEAD_DIM; ++d) qd[d] = q_scale * lut[q[r * ORC_HEAD_DIM + d]];
+    for (int d = 0; d < ORC_HEAD_DIM; ++d) qd[d] = q_scale * elem(q, dtype, r, d, lut);
     row_range(kv_lens[b], q_len, qi, causal, tok_begin, tok_end, &lo, &hi);
     for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] = 0.0;
     const double sink = (sinks && mode == 0) ? sinks[h] : -INFINITY;
@@ -197,9 +209,9 @@ int mla_oracle_decode_rows_ex(const uint8_t* q, const uint8_t* kv, int64_t num_p
         s[j - lo] = 0.0;
         continue;
       }
-      const uint8_t* k = key_row(kv, page_table, max_pages, b, j);
+      const int64_t kr = key_index(page_table, max_pages, b, j);
       double dot = 0.0;
-      for (int d = 0; d < ORC_HEAD_DIM; ++d) dot += qd[d] * (kv_scale * lut[k[d]]);
+      for (int d = 0; d < ORC_HEAD_DIM; ++d) dot += qd[d] * (kv_scale * elem(kv, dtype, kr, d, lut));
       s[j - lo] = softmax_scale * dot;
     }
     double M = sink;
@@ -210,12 +222,11 @@ int mla_oracle_decode_rows_ex(const uint8_t* q, const uint8_t* kv, int64_t num_p
     double Z = (sink == -INFINITY) ? 0.0 : exp(sink - M);
     for (int64_t j = lo; j < hi; ++j) {
       double w = exp(s[j - lo] - M);
-      const uint8_t* k;
       int64_t page = page_table[(int64_t)b * max_pages + j / ORC_PAGE];
       Z += w;
       if (page < 0 || page >= num_pages) continue;
-      k = key_row(kv, page_table, max_pages, b, j);
-      for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] += w * (kv_scale * lut[k[d]]);
+      const int64_t kr = key_index(page_table, max_pages, b, j);
+      for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] += w * (kv_scale * elem(kv, dtype, kr, d, lut));
     }
     free(s);
     if (bad) {

@@ -59,7 +59,7 @@ class DecodeInputs:
         return self.batch * self.q_len * self.num_heads
 
     def kv_bytes(self) -> int:
-        return int(self.kv_lens.to(torch.int64).sum().item()) * HEAD_DIM
+        return int(self.kv_lens.to(torch.int64).sum().item()) * HEAD_DIM * self.kv.element_size()
 
 
 def _fill_e4m3(out_u8: torch.Tensor, gen: torch.Generator, std: float) -> None:
@@ -79,13 +79,28 @@ def _generator(device: torch.device, seed: int) -> torch.Generator:
     return g
 
 
+def _fill_bf16(out: torch.Tensor, gen: torch.Generator, std: float) -> None:
+    """Fill a flat bfloat16 tensor with N(0, std^2) draws (round to nearest even)."""
+    flat = out.view(-1)
+    n = flat.numel()
+    for start in range(0, n, _CHUNK_ELEMS):
+        cnt = min(_CHUNK_ELEMS, n - start)
+        vals = torch.randn(cnt, generator=gen, device=flat.device, dtype=torch.float32)
+        vals.mul_(std)
+        flat[start:start + cnt].copy_(vals.to(torch.bfloat16))
+
+
+BF16_NAN = float("nan")
+
+
 def decode_inputs(batch: int, num_heads: int, q_len: int, kv_lens: Sequence[int],
                   seed: int, device: str | torch.device = "cpu", std: float = 0.5,
-                  extra_pages: int = 0) -> DecodeInputs:
+                  extra_pages: int = 0, dtype: str = "e4m3") -> DecodeInputs:
     """Draw one seeded decode batch.
 
     kv_lens: per-request KV lengths (len == batch).  extra_pages adds unused,
-    NaN-filled pages to the pool (shuffled in with the used ones).
+    NaN-filled pages to the pool (shuffled in with the used ones).  dtype
+    "e4m3" gives uint8 E4M3 codes; "bf16" gives bfloat16 Q and KV.
     """
     device = torch.device(device)
     lens = [int(x) for x in kv_lens]
@@ -97,10 +112,20 @@ def decode_inputs(batch: int, num_heads: int, q_len: int, kv_lens: Sequence[int]
     max_pages = max(1, max(pages_per_req))
 
     g = _generator(device, seed)
-    q = torch.empty((batch, q_len, num_heads, HEAD_DIM), dtype=torch.uint8, device=device)
-    _fill_e4m3(q, g, std)
-    kv = torch.empty((total_pages, PAGE_SIZE, HEAD_DIM), dtype=torch.uint8, device=device)
-    _fill_e4m3(kv, g, std)
+    if dtype == "e4m3":
+        q = torch.empty((batch, q_len, num_heads, HEAD_DIM), dtype=torch.uint8, device=device)
+        _fill_e4m3(q, g, std)
+        kv = torch.empty((total_pages, PAGE_SIZE, HEAD_DIM), dtype=torch.uint8, device=device)
+        _fill_e4m3(kv, g, std)
+        poison = E4M3_NAN_CODE
+    elif dtype == "bf16":
+        q = torch.empty((batch, q_len, num_heads, HEAD_DIM), dtype=torch.bfloat16, device=device)
+        _fill_bf16(q, g, std)
+        kv = torch.empty((total_pages, PAGE_SIZE, HEAD_DIM), dtype=torch.bfloat16, device=device)
+        _fill_bf16(kv, g, std)
+        poison = BF16_NAN
+    else:
+        raise ValueError(f"unknown dtype {dtype}")
 
     # Page permutation is drawn on the host so that it does not depend on the device.
     gh = _generator(torch.device("cpu"), seed * 7919 + 17)
@@ -112,12 +137,12 @@ def decode_inputs(batch: int, num_heads: int, q_len: int, kv_lens: Sequence[int]
         off += n
     # Unused pool pages and the tail slots past each request's length are poison.
     if extra_pages:
-        kv[perm[used:].to(torch.int64).to(device)] = E4M3_NAN_CODE
+        kv[perm[used:].to(torch.int64).to(device)] = poison
     for b, n in enumerate(lens):
         tail = n % PAGE_SIZE
         if n > 0 and tail:
             last = int(table[b, pages_per_req[b] - 1])
-            kv[last, tail:, :] = E4M3_NAN_CODE
+            kv[last, tail:, :] = poison
     return DecodeInputs(q=q, kv=kv, page_table=table.to(device),
                         kv_lens=torch.tensor(lens, dtype=torch.int32),
                         batch=batch, q_len=q_len, num_heads=num_heads, seed=seed)
@@ -181,6 +206,12 @@ for _b in (1, 4):
              kv_lens=[_l] * _b, causal=True, target=None, seed=4)
 _add("ragged_h12_q1_b16", batch=16, num_heads=12, q_len=1, kv_lens=ragged_lens(4),
      causal=False, target=None, seed=4)
+# BF16 KV cache (the pages' BF16 kernel is quoted at H12 q8 B1 1M).
+for _q in (1, 8):
+    _add(f"bf16_h12_q{_q}_l1m_b1", batch=1, num_heads=12, q_len=_q, kv_lens=[1048576],
+         causal=(_q > 1), target=None, seed=5, dtype="bf16")
+_add("bf16_h12_q1_l1m_b16", batch=16, num_heads=12, q_len=1, kv_lens=[1048576] * 16,
+     causal=False, target=None, seed=5, dtype="bf16")
 
 
 def workload_inputs(name: str, device: str | torch.device = "cpu",
@@ -190,4 +221,5 @@ def workload_inputs(name: str, device: str | torch.device = "cpu",
     w = WORKLOADS[name]
     lens = list(kv_lens_override) if kv_lens_override is not None else w["kv_lens"]
     return decode_inputs(w["batch"], w["num_heads"], w["q_len"], lens,
-                         w["seed"] + 1000 * seed_offset, device=device)
+                         w["seed"] + 1000 * seed_offset, device=device,
+                         dtype=w.get("dtype", "e4m3"))

@@ -345,3 +345,28 @@ def test_sink_equal_scores_mean_shrinks():
     np.testing.assert_allclose(o[0], keys[:, :LATENT_DIM].mean(0).numpy() * 40 / 50, rtol=1e-12,
                                atol=1e-15)
     assert l[0] == pytest.approx(s + math.log(50.0), abs=1e-12)
+
+
+# --- BF16 KV variant -----------------------------------------------------------
+
+@pytest.mark.parametrize("B,H,q_len,lens,causal", [(1, 4, 1, [64], False), (2, 2, 4, [40, 9], True)])
+def test_bf16_oracle_matches_torch_attention(B, H, q_len, lens, causal):
+    inp = decode_inputs(B, H, q_len, lens, seed=26, extra_pages=2, dtype="bf16")
+    out, lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=q_len,
+                                  num_heads=H, causal=causal, softmax_scale=0.11)
+    outs, lses = [], []
+    for b in range(B):
+        L = int(inp.kv_lens[b])
+        keys = torch.stack([inp.kv[int(inp.page_table[b, j // PAGE_SIZE]), j % PAGE_SIZE]
+                            for j in range(L)]).to(torch.float64)
+        q = inp.q[b].reshape(q_len * H, HEAD_DIM).to(torch.float64)
+        mask = torch.ones((q_len * H, L), dtype=torch.bool)
+        if causal:
+            for qi in range(q_len):
+                mask[qi * H:(qi + 1) * H, L - q_len + qi + 1:] = False
+        outs.append(torch.nn.functional.scaled_dot_product_attention(
+            q[None, None], keys[None, None], keys[None, None, :, :LATENT_DIM],
+            attn_mask=mask[None, None], scale=0.11)[0, 0])
+        lses.append(torch.logsumexp(((q @ keys.T) * 0.11).masked_fill(~mask, -math.inf), -1))
+    np.testing.assert_allclose(out, torch.cat(outs).numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.cat(lses).numpy(), rtol=1e-12, atol=1e-12)
