@@ -14,6 +14,7 @@ SOURCES = [os.path.join(CSRC, "mla_decode.cu"), os.path.join(CSRC, "kv_append.cu
 DEPENDS = SOURCES + [
     os.path.join(CSRC, "mla_internal.h"),
     os.path.join(CSRC, "sm103_ptx.cuh"),
+    os.path.join(CSRC, "mla_device.cuh"),
     os.path.join(os.path.dirname(HERE), "include", "mla_decode.h"),
 ]
 NVCC_FLAGS = [
