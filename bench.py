@@ -33,6 +33,8 @@ DEFAULT_WORKLOAD = "long_h12_q1_l1m_b16"
 PUBLISHED_US = {"long_h12_q1_l1m_b16": 1095.5}
 L2_ROTATE_BYTES = 2 * 126 * 1024 * 1024  # rotate inputs below 2x the 126 MB L2
 KERNEL_SOURCES = ["split_kv_mla_paged_gb300/csrc/mla_decode.cu",
+                  "split_kv_mla_paged_gb300/csrc/mla_decode_bf16.cu",
+                  "split_kv_mla_paged_gb300/csrc/mla_device.cuh",
                   "split_kv_mla_paged_gb300/csrc/sm103_ptx.cuh"]
 
 
@@ -306,10 +308,25 @@ def main():
     ws, out, lse = args_common[17], args_common[19], args_common[20]
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize(dev)
+    is_bf16 = inp.q.dtype == torch.bfloat16
+
+    def decode_call(*a):
+        # a = one call's arguments followed by the stream
+        if is_bf16:  # BF16 Q and KV: no q/kv scales
+            mla.mla_decode_bf16(*a[:14], *a[16:])
+        else:
+            mla.mla_decode(*a)
+
+    # The BF16 entry point has no separate phases: its "split" graph is the
+    # whole call (an upper bound on the split kernel's time), and its merge is
+    # the shared merge kernel, launched on the same workspace and plan.
+    phases = (("full", decode_call),
+              ("split", decode_call if is_bf16 else mla.mla_decode_splitkv),
+              ("merge", mla.mla_decode_merge))
 
     with torch.cuda.stream(stream):
         for k in range(args.warmup):
-            mla.mla_decode(*calls[k % n_pools], stream)
+            decode_call(*calls[k % n_pools], stream)
     torch.cuda.synchronize(dev)
     mla.mla_decode_status(ws, stream)
 
@@ -318,8 +335,7 @@ def main():
     # hold the same K calls of each phase alone, for per-kernel durations.
     K = args.steps
     graphs = {}
-    for name, fn in (("full", mla.mla_decode), ("split", mla.mla_decode_splitkv),
-                     ("merge", mla.mla_decode_merge)):
+    for name, fn in phases:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for k in range(K):
@@ -365,7 +381,7 @@ def main():
     e2e_args = list(args_common)
     e2e_args[0], e2e_args[3] = q_d, pt_d
     e2e_args[5], e2e_args[6], e2e_args[7] = meta_d[0], meta_d[1], meta_d[2]
-    h2d = q_h.numel() + pt_h.numel() * 4 + meta_h.numel() * 4
+    h2d = q_h.numel() * q_h.element_size() + pt_h.numel() * 4 + meta_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
     def e2e_step():
@@ -374,7 +390,7 @@ def main():
         q_d.copy_(q_h, non_blocking=True)
         pt_d.copy_(pt_h, non_blocking=True)
         meta_d.copy_(meta_h, non_blocking=True)
-        mla.mla_decode(*e2e_args, stream)
+        decode_call(*e2e_args, stream)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
@@ -410,7 +426,9 @@ def main():
             "steps": K, "warmup": args.warmup, "ms_per_step": us_per_call / 1e3,
             "higher_is_better": False, "scaling": "weak",
             "vs_baseline": (us_per_call / pub) if pub else None,
-            "dtype": "e4m3", "data": "synthetic (seeded N(0,0.5^2) cast to E4M3, random pages)",
+            "dtype": "bf16" if is_bf16 else "e4m3",
+            "data": ("synthetic (seeded N(0,0.5^2) cast to "
+                     f"{'BF16' if is_bf16 else 'E4M3'}, random pages)"),
             "config": {"workload": args.workload, "batch": B, "num_heads": H, "q_len": q_len,
                        "kv_len": lens[0], "causal": w["causal"], "plan": args.plan,
                        "splits": plan.splits.tolist()[:4] + (["..."] if B > 4 else []),
@@ -426,7 +444,8 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "traffic": traffic, "peak_source": peaks["source"],
-                         "kernel": "mla_split_kv_kernel"},
+                         "kernel": ("mla_split_kv_bf16_kernel (timed with its merge)"
+                                    if is_bf16 else "mla_split_kv_kernel")},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

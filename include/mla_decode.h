@@ -189,6 +189,25 @@ MLA_API int mla_decode_merge(const void* q_fp8, const void* kv_pages_fp8, int64_
                              void* workspace, size_t workspace_bytes, void* out_bf16,
                              float* lse_f32, float* out_f32_debug, void* stream);
 
+/*
+ * BF16-KV decode: the same method and split plan with a BF16 cache (issue
+ * #20510, "Repro 2": the BF16 kernel mla_decode_fp16.py, 512 latent + 64 rope,
+ * page size 32, BF16 output).  Q and KV are BF16, so there are no q/kv scales;
+ * everything else (plan, workspace, status, row order, outputs, merge, error
+ * codes) is as for mla_decode.
+ *
+ * q_bf16          BF16 [batch, q_len, num_heads, 576], contiguous, 16-byte aligned.
+ * kv_pages_bf16   BF16 [num_pages, 32, 576], contiguous, 16-byte aligned.
+ * The workspace size is mla_decode_workspace_size(...) for the same plan.
+ */
+MLA_API int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t num_pages,
+                            const int32_t* page_table, int32_t max_pages_per_req,
+                            const int32_t* kv_lens, const int32_t* splits, const int32_t* chunks,
+                            int32_t max_splits, int32_t kv_split, int32_t batch, int32_t q_len,
+                            int32_t num_heads, int32_t causal, float softmax_scale,
+                            void* workspace, size_t workspace_bytes, void* out_bf16,
+                            float* lse_f32, float* out_f32_debug, void* stream);
+
 /* Zero the 256-byte status header of a new workspace (async on `stream`).
  * Call once per workspace before its first mla_decode; after that the
  * header only changes when the device reports a condition, and

@@ -22,7 +22,8 @@ __all__ = [
     "MLA_ERR_CUDA", "MLA_ERR_TIMEOUT", "MlaError", "Plan", "load_library", "library_path",
     "mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init", "mla_decode",
     "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
-    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "DecodeOptions", "decode", "merge",
+    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16", "DecodeOptions",
+    "decode", "merge",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -39,7 +40,7 @@ _STATUS_NAMES = {
 EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init",
                     "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
                     "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit",
-                    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex")
+                    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
@@ -94,6 +95,8 @@ def load_library() -> ctypes.CDLL:
             getattr(lib, name).argtypes = dec_args
         lib.mla_decode_ex.restype = ctypes.c_int
         lib.mla_decode_ex.argtypes = dec_args[:-1] + [ctypes.POINTER(DecodeOptions), vp]
+        lib.mla_decode_bf16.restype = ctypes.c_int
+        lib.mla_decode_bf16.argtypes = dec_args[:14] + [f32] + dec_args[17:]
         lib.mla_decode_workspace_init.restype = ctypes.c_int
         lib.mla_decode_workspace_init.argtypes = [vp, sz, vp]
         lib.mla_merge.restype = ctypes.c_int
@@ -215,6 +218,22 @@ def mla_decode_ex(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req,
                              ctypes.byref(opts), _stream_handle(stream)))
 
 
+def mla_decode_bf16(q_bf16, kv_pages_bf16, num_pages: int, page_table, max_pages_per_req: int,
+                    kv_lens, splits, chunks, max_splits: int, kv_split: int, batch: int,
+                    q_len: int, num_heads: int, causal: bool, softmax_scale: float, workspace,
+                    workspace_bytes: int, out_bf16, lse_f32=None, out_f32_debug=None,
+                    stream=None) -> None:
+    """Enqueue one BF16-KV decode (split-KV kernel + merge) on `stream`."""
+    lib = load_library()
+    _check(lib.mla_decode_bf16(_ptr(q_bf16), _ptr(kv_pages_bf16), int(num_pages),
+                               _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),
+                               _ptr(splits), _ptr(chunks), int(max_splits), int(kv_split),
+                               int(batch), int(q_len), int(num_heads), 1 if causal else 0,
+                               float(softmax_scale), _ptr(workspace), int(workspace_bytes),
+                               _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
+                               _stream_handle(stream)))
+
+
 def mla_decode_splitkv(*args, **kw) -> None:
     """Split-KV phase of mla_decode (same arguments)."""
     _decode_call("mla_decode_splitkv", *args, **kw)
@@ -299,7 +318,9 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
 
     q_fp8 uint8 [B, q, H, 576] and kv_pages_fp8 uint8 [P, 32, 576] (E4M3 codes)
     and page_table int32 [B, max_pages] are CUDA tensors; kv_lens is a host
-    sequence.  Returns (out_bf16, lse, out_f32 or None).
+    sequence.  With torch.bfloat16 q and kv this runs mla_decode_bf16 (no
+    scales, sinks or output scale there).  Returns (out_bf16, lse, out_f32 or
+    None).
     """
     import torch
     dev = q_fp8.device
@@ -322,7 +343,13 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
                if want_f32 else None)
     common = (q_fp8, kv_pages_fp8, kv_pages_fp8.shape[0], page_table, page_table.shape[1],
               lens_d, splits_d, chunks_d, plan.max_splits, ks, batch, q_len, num_heads, causal)
-    if sinks is None and output_scale == 1.0 and not device_scales:
+    if q_fp8.dtype == torch.bfloat16:
+        if (kv_pages_fp8.dtype != torch.bfloat16 or sinks is not None or output_scale != 1.0
+                or device_scales or q_scale != 1.0 or kv_scale != 1.0):
+            raise ValueError("BF16 decode takes BF16 q and kv and no scales, sinks or "
+                             "output scale")
+        mla_decode_bf16(*common, softmax_scale, ws, ws_bytes, out, lse, out_f32, stream)
+    elif sinks is None and output_scale == 1.0 and not device_scales:
         mla_decode(*common, q_scale, kv_scale, softmax_scale, ws, ws_bytes, out, lse, out_f32,
                    stream)
     else:

@@ -9,8 +9,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB_NAME = "libmla_decode.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = [os.path.join(CSRC, "mla_decode.cu"), os.path.join(CSRC, "kv_append.cu"),
-           os.path.join(CSRC, "plan.cpp")]
+SOURCES = [os.path.join(CSRC, "mla_decode.cu"), os.path.join(CSRC, "mla_decode_bf16.cu"),
+           os.path.join(CSRC, "kv_append.cu"), os.path.join(CSRC, "plan.cpp")]
+OBJ_DIR = os.path.join(HERE, "_build")
 DEPENDS = SOURCES + [
     os.path.join(CSRC, "mla_internal.h"),
     os.path.join(CSRC, "sm103_ptx.cuh"),
@@ -20,7 +21,7 @@ DEPENDS = SOURCES + [
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-shared", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+    "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
 ]
 
 
@@ -40,12 +41,28 @@ def build(force: bool = False, verbose: bool = False) -> str:
     """Compile the C-ABI library if it is missing or stale; return its path."""
     if not force and not needs_build():
         return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *NVCC_FLAGS, *SOURCES, "-o", tmp]
+    # One nvcc per translation unit, all at once, then one link.
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    tag = f"{os.getpid()}"
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(OBJ_DIR, os.path.basename(src) + f".{tag}.o")
+        cmd = [_nvcc(), *NVCC_FLAGS, "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        objs.append(obj)
+        procs.append((src, subprocess.Popen(cmd)))
+    failed = [src for src, pr in procs if pr.wait() != 0]
+    if failed:
+        raise RuntimeError(f"nvcc failed for {failed}")
+    tmp = LIB_PATH + f".tmp{tag}"
+    cmd = [_nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", *objs, "-o", tmp]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB_PATH)
+    for obj in objs:
+        os.remove(obj)
     return LIB_PATH
 
 

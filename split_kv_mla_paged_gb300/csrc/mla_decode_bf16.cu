@@ -1,0 +1,718 @@
+// Paged BF16-KV MLA decode for GB300 (sm_103a): the same split-KV method as
+// the FP8 kernel with a BF16 cache (issue #20510 "CuTe DSL FP8 MLA decode
+// regression", Repro 2 text: the BF16 kernel mla_decode_fp16.py, same
+// geometry: 512 latent + 64 rope, page size 32, BF16 output).
+//
+// Differences from the FP8 kernel (mla_decode.cu):
+//  * A token row is 1152 bytes, so a KV tile is 64 tokens (73,728 B, the same
+//    stage size as 128 FP8 tokens) in nine 64-element blocks (8 latent + 1
+//    rope), each [64 tokens][128 B] with the 128-byte swizzle.
+//  * QK is tcgen05.mma kind::f16 with M = 64 tokens: D row 16q + i lands in
+//    TMEM lane 32q + i, so each softmax warp (quadrant q) owns 16 tokens in
+//    its lanes 0-15.  K = 16 elements per instruction, 36 per tile.
+//  * P is BF16 (8 mantissa bits, so one term is enough: |err| <= 2^-9 of a
+//    weight), written MN-major into the rope block of its own stage, which QK
+//    has consumed.  PV is M = 128 latent dims (two 64-element swizzle atoms),
+//    N = rows, K = 16 tokens, 16 instructions per tile.
+//  * Q is BF16 too (kind::f16 takes A and B of one type); there are no q/kv
+//    scales.  Partials have the FP8 kernel's layout, so the merge is shared.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <string>
+
+#include "mla_device.cuh"
+
+namespace mla {
+
+constexpr int kTokB = 64;                                   // tokens per tile
+constexpr uint32_t kRowBytesB = MLA_HEAD_DIM * 2;           // 1152
+constexpr uint32_t kTileBytesB = kTokB * kRowBytesB;        // 73728
+constexpr uint32_t kBlkBytesB = kTokB * 128;                // 8192: one 64-element block
+constexpr uint32_t kRopeOffB = 8 * kBlkBytesB;              // block 8 = rope
+constexpr uint32_t kPageBlkBytesB = MLA_PAGE_SIZE * 128;    // 4096: one page of one block
+constexpr uint32_t kPageBytesB = MLA_PAGE_SIZE * kRowBytesB;
+
+// Instruction descriptor for kind::f16 with BF16 A and B, fp32 D.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32_t a_mn,
+                                                  uint32_t b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // a in the low half
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int NR>
+struct CfgB {
+  static_assert(NR % 16 == 0 && NR >= 16 && NR <= kMaxRowsPerCta, "NR");
+  static constexpr int NS = 2;  // S^T buffers
+  static constexpr uint32_t kTmemUsed = NS * NR + 4 * NR;
+  static constexpr uint32_t kTmemCols =
+      kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+      : kTmemUsed <= 256 ? 256 : 512;
+  static constexpr uint32_t kOCol = NS * NR;
+  static constexpr int SWG = NR >= 32 ? 2 : 1;
+  static constexpr int NRH = NR / SWG;
+  static_assert(NRH % 8 == 0, "rows per softmax warpgroup");
+  static constexpr int kThreads = 64 + 128 * SWG;
+  static constexpr uint32_t kPBytes = NR * kTokB * 2;  // BF16 P^T, in the rope block
+  static_assert(kPBytes <= kBlkBytesB, "P^T must fit the rope block");
+  static constexpr int NST = 2;
+  static constexpr uint32_t kQBytes = NR * kRowBytesB;
+  static constexpr uint32_t kAuxBytes = 160 + 52 * NR;
+  static constexpr uint32_t kKV = 0;
+  static constexpr uint32_t kQ = NST * kTileBytesB;
+  static constexpr uint32_t kAux = kQ + kQBytes;
+  static constexpr uint32_t kBars = kAux;
+  static constexpr uint32_t kTmemSlot = kAux + 136;
+  static constexpr uint32_t kFlags = kAux + 144;
+  static constexpr uint32_t kRedMax = kAux + 160;
+  static constexpr uint32_t kAlpha = kRedMax;
+  static constexpr uint32_t kRedSum = kRedMax + 16 * NR;
+  static constexpr uint32_t kKref = kRedSum + 32 * NR;
+  static constexpr uint32_t kEnd = kKref + 4 * NR;
+  static_assert(kEnd - kAux <= kAuxBytes, "aux layout");
+  static constexpr uint32_t kSmemBytes = kEnd + 1024;
+  static_assert(kSmemBytes <= 232448u, "shared memory");
+};
+
+template <int NR>
+__global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
+    mla_split_kv_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
+                             const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+  using C = CfgB<NR>;
+  const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
+  const int split = blockIdx.x / ngroups;
+  const int grp = blockIdx.x - split * ngroups;
+  const int b = blockIdx.y;
+
+  const int L = p.kv_lens[b];
+  const int nsplit = p.splits[b];
+  const int chunk = p.chunks[b];
+  if (split >= nsplit) return;
+  {
+    const bool bad = L < 1 || (p.causal && L < p.q_len) || nsplit > p.max_splits ||
+                     chunk < MLA_TILE_TOKENS || (chunk % MLA_TILE_TOKENS) != 0 ||
+                     static_cast<int64_t>(nsplit) * chunk < L ||
+                     static_cast<int64_t>(nsplit - 1) * chunk >= L ||
+                     static_cast<int64_t>(L) > static_cast<int64_t>(p.max_pages) * MLA_PAGE_SIZE;
+    if (bad) {
+      if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
+      return;
+    }
+  }
+  const int tok_begin = split * chunk;
+  const int tok_end = min(L, tok_begin + chunk);
+  const int n_tiles = (tok_end - tok_begin + kTokB - 1) / kTokB;
+  const float c_log2 = p.c_log2;
+  const int row0 = grp * p.rows_per_group;
+  const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(base);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBars + 8u * i; };
+  volatile int* flags = reinterpret_cast<volatile int*>(base + C::kFlags);
+  volatile int* abort_flag = flags + 2;
+  float* red_max = reinterpret_cast<float*>(base + C::kRedMax);
+  float* red_sum = reinterpret_cast<float*>(base + C::kRedSum);
+  float* kref = reinterpret_cast<float*>(base + C::kKref);
+  float* alpha_s = reinterpret_cast<float*>(base + C::kAlpha);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < C::NST; ++k) {
+      mbar_init(bar(BAR_FULL0 + k), 1);
+      mbar_init(bar(BAR_EMPTY0 + k), 1);
+    }
+    mbar_init(bar(BAR_QFULL), 1);
+    mbar_init(bar(BAR_SFULL0), 1);
+    mbar_init(bar(BAR_SFULL1), 1);
+    mbar_init(bar(BAR_SFREE0), 128 * C::SWG);
+    mbar_init(bar(BAR_SFREE1), 128 * C::SWG);
+    mbar_init(bar(BAR_PFULL0), 128 * C::SWG);
+    mbar_init(bar(BAR_PFULL1), 128 * C::SWG);
+    mbar_init(bar(BAR_ODONE), 1);
+    mbar_init(bar(BAR_FINAL), 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + C::kTmemSlot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + C::kTmemSlot);
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_kv);
+      tma_prefetch_desc(&tm_q);
+      const int qrow = b * p.rows_per_req + row0;
+      mbar_arrive_expect_tx(bar(BAR_QFULL), C::kQBytes);
+#pragma unroll
+      for (int d = 0; d < 9; ++d)
+        tma_load_2d(sbase + C::kQ + d * NR * 128, &tm_q, d * 64, qrow, bar(BAR_QFULL));
+    }
+    const uint64_t pol = l2_policy_evict_first();
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+    const int page0 = tok_begin / MLA_PAGE_SIZE;
+    const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
+    // Page ids of 16 tiles (32 pages) per window, one per lane, fetched a
+    // window ahead.
+    auto load_window = [&](int w) -> int {
+      const int pi = page0 + w * 32 + lane;
+      int pg = 0;
+      if (pi < page_end) {
+        pg = pt[pi];
+        if (pg < 0 || pg >= p.num_pages) {
+          report(p.status, MLA_ERR_INVALID_ARG);
+          pg = 0;
+        }
+      }
+      return pg;
+    };
+    int window = load_window(0);
+    int window_next = load_window(1);
+    int issued = 0;
+    int st = 0, round = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      if (i > 0 && (i & 15) == 0) {
+        window = window_next;
+        window_next = load_window((i >> 4) + 1);
+      }
+      bool ok = true;
+      if (round > 0) ok = mbar_wait(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles);
+      ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+      if (!ok) {
+        if (lane == 0) {
+          report(p.status, MLA_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      // Lane q (< 2) takes the id of the tile's page q.
+      const int my_page = __shfl_sync(0xffffffffu, window, (i & 15) * 2 + (lane & 1));
+      const int tp0 = page0 + i * 2;
+      const uint32_t fb = bar(BAR_FULL0 + st);
+      if (lane == 0) {
+        const int nvalid = (tp0 < page_end ? 1 : 0) + (tp0 + 1 < page_end ? 1 : 0);
+        mbar_arrive_expect_tx(fb, nvalid * kPageBytesB);
+      }
+      __syncwarp();
+      if (lane < 2 && tp0 + lane < page_end) {
+        const uint32_t kv = sbase + C::kKV + st * kTileBytesB;
+        const int row = my_page * MLA_PAGE_SIZE;
+#pragma unroll
+        for (int d = 0; d < 9; ++d)
+          tma_load_2d_hint(kv + d * kBlkBytesB + lane * kPageBlkBytesB, &tm_kv, d * 64, row, fb,
+                           pol);
+      }
+      __syncwarp();
+      issued = i + 1;
+      if (++st == C::NST) {
+        st = 0;
+        ++round;
+      }
+    }
+    if (lane == 0) {
+      for (int k = max(0, issued - C::NST); k < issued; ++k)
+        mbar_wait(bar(BAR_FULL0 + k % C::NST), (k / C::NST) & 1, kWaitLimitCycles);
+      mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    constexpr uint32_t kIdQK = idesc_bf16(64, NR, 0, 0);
+    constexpr uint32_t kIdPV = idesc_bf16(128, NR, 1, 1);
+    bool ok = mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles);
+    auto fail = [&]() {
+      if (lane == 0) {
+        report(p.status, MLA_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    };
+    // PV of tile j (KV in stage jst; P^T in its rope block).
+    auto issue_pv = [&](int j, int jst) {
+      tc_fence_after();
+      const uint32_t kv = sbase + C::kKV + jst * kTileBytesB;
+      const uint32_t pbuf = kv + kRopeOffB;
+#pragma unroll
+      for (int d = 0; d < 4; ++d) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          // A = V^T, MN-major: 64-element atoms 8 KB apart (latent blocks 2d,
+          // 2d + 1), 8-token groups 1 KB apart; 16 tokens per instruction.
+          const uint64_t a = smem_desc(kv + 2 * d * kBlkBytesB + ks * 2048, kBlkBytesB, 1024,
+                                       kLayoutSW128);
+          // B = P^T, MN-major, no swizzle: 8-row groups 1 KB apart, 8-token
+          // groups 128 B apart.
+          const uint64_t bd = smem_desc(pbuf + ks * 256, 128, 1024, kLayoutNone);
+          umma_bf16(tmem + C::kOCol + d * NR, a, bd, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(bar(BAR_EMPTY0 + jst));
+      umma_commit(bar(BAR_ODONE));
+    };
+    // QK of a tile (KV in stage ist) into S buffer sb.
+    auto issue_qk = [&](int ist, int sb) {
+      tc_fence_after();
+      const uint32_t kv = sbase + C::kKV + ist * kTileBytesB;
+#pragma unroll
+      for (int kk = 0; kk < 36; ++kk) {
+        const int d = kk >> 2, sub = kk & 3;
+        const uint64_t a = smem_desc(kv + d * kBlkBytesB + sub * 32, 16, 1024, kLayoutSW128);
+        const uint64_t bd =
+            smem_desc(sbase + C::kQ + d * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
+        umma_bf16(tmem + sb * NR, a, bd, kIdQK, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(bar(BAR_SFULL0 + sb));
+    };
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) fail();
+    // Issue loop: PV(pv) as soon as its P^T is ready, QK(qk) as soon as its
+    // tile has landed and its S^T buffer is free; QK at most one tile ahead.
+    int qk = 0, pv = 0;
+    int qk_st = 0, qk_round = 0, pv_st = 0;
+    long long t_last = clock64();
+    while (ok && pv < n_tiles) {
+      int action = 0;
+      if (lane == 0) {
+        if (pv < qk && mbar_test_wait(bar(BAR_PFULL0 + (pv & 1)), (pv >> 1) & 1)) action = 1;
+        if (action == 0 && qk < n_tiles && qk <= pv + 1) {
+          const int use = qk >> 1;
+          if (mbar_test_wait(bar(BAR_FULL0 + qk_st), qk_round & 1) &&
+              (use < 1 || mbar_test_wait(bar(BAR_SFREE0 + (qk & 1)), (use - 1) & 1)))
+            action = 2;
+        }
+      }
+      action = __shfl_sync(0xffffffffu, action, 0);
+      if (action == 1) {
+        if (lane == 0) issue_pv(pv, pv_st);
+        __syncwarp();
+        ++pv;
+        if (++pv_st == C::NST) pv_st = 0;
+        t_last = clock64();
+      } else if (action == 2) {
+        const int tile_tok0 = tok_begin + qk * kTokB;
+        const int valid = tok_end - tile_tok0;
+        if (valid < kTokB) {
+          // Rows past the split's end (unloaded pages or a last page's tail):
+          // zero them so V holds no stale or NaN values.
+          const int nrow = kTokB - valid;
+          uint8_t* kvp = base + C::kKV + qk_st * kTileBytesB;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          for (int idx = lane; idx < nrow * 72; idx += 32) {
+            const int r = valid + idx / 72;
+            const int c = idx % 72;
+            *reinterpret_cast<uint4*>(kvp + (c / 8) * kBlkBytesB + r * 128 + (c % 8) * 16) = z;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) issue_qk(qk_st, qk & 1);
+        __syncwarp();
+        ++qk;
+        if (++qk_st == C::NST) {
+          qk_st = 0;
+          ++qk_round;
+        }
+        t_last = clock64();
+      } else {
+        const bool late = (clock64() - t_last > p.wait_cycles) || *abort_flag;
+        if (__any_sync(0xffffffffu, late)) {
+          fail();
+          ok = false;
+        }
+      }
+    }
+    if (lane == 0) umma_commit(bar(BAR_FINAL));
+    __syncwarp();
+    mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
+  } else {
+    // ================= softmax warpgroups =================
+    // As in the FP8 kernel, with the M = 64 S^T layout: warp quadrant q
+    // holds tokens 16q .. 16q + 15 in its lanes 0-15; lanes 16-31 carry no
+    // token (their scores are -inf and their weights 0).
+    constexpr int NRH = C::NRH;
+    constexpr int NT = 128 * C::SWG;
+    const int quad = warp & 3;
+    const int rbase = ((warp - 2) >> 2) * NRH;
+    const bool has_tok = lane < 16;
+    const int tok = quad * 16 + lane;       // token index within the tile (when has_tok)
+    const int dim_lane = quad * 32 + lane;  // TMEM lane for O^T (M = 128 layout)
+    const int sid = threadIdx.x - 64;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    float k_row = -INFINITY;
+    float l_row = 0.0f;
+    float kreg[NRH];
+#pragma unroll
+    for (int k = 0; k < NRH; ++k) kreg[k] = -INFINITY;
+    const float c = c_log2;
+    const int qi_first = row0 / p.num_heads;
+    const int lim_min = p.causal ? min(tok_end, L - p.q_len + qi_first + 1) : tok_end;
+    const int my_row0 = row0 + rbase;
+    const int my_rows = max(0, min(NRH, rows_here - rbase));
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int sb = i & 1;
+      const int use = i >> 1;
+      if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
+      ok = __all_sync(0xffffffffu, ok);
+      float t[NRH];
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[NRH];
+#pragma unroll
+        for (int cc = 0; cc < NRH / 8; ++cc)
+          tmem_ld8(tmem + lane_addr + sb * NR + rbase + cc * 8,
+                   *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
+        tc_fence_before();
+        mbar_arrive(bar(BAR_SFREE0 + sb));
+      } else {
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
+      }
+      const int tile_tok0 = tok_begin + i * kTokB;
+      const int j = tile_tok0 + tok;
+      if (tile_tok0 + kTokB <= lim_min) {
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) t[k] = (has_tok && k < my_rows) ? t[k] * c : -INFINITY;
+      } else {
+        int qi = my_row0 / p.num_heads;
+        int h = my_row0 - qi * p.num_heads;
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) {
+          const int lim = p.causal ? min(tok_end, L - p.q_len + qi + 1) : tok_end;
+          t[k] = (has_tok && k < my_rows && j < lim) ? t[k] * c : -INFINITY;
+          if (++h == p.num_heads) {
+            h = 0;
+            ++qi;
+          }
+        }
+      }
+      bool over = false;
+#pragma unroll
+      for (int k = 0; k < NRH; ++k) over |= t[k] > kreg[k] + 0.75f;
+      const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
+      if (sid < NR && i > 0) {
+        const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
+        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+      }
+      if (any_over) {
+        {
+          float tm[NRH];
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) tm[k] = t[k];
+          warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
+        }
+        if (sid == 0) flags[0] = 0;
+        named_bar_sync(kSoftmaxBarrier, NT);
+        if (sid < NR) {
+          const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
+                                 fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
+          float k_new = k_row;
+          if (mt > k_row + 0.75f) k_new = ceilf(mt);
+          float alpha = 1.0f;
+          if (k_new != k_row && k_row != -INFINITY) {
+            const int e = static_cast<int>(k_row - k_new);
+            alpha = (e < -126) ? 0.0f : pow2i(e);
+            flags[0] = 1;
+          }
+          l_row *= alpha;
+          k_row = k_new;
+          kref[sid] = k_new;
+          alpha_s[sid] = alpha;
+        }
+        named_bar_sync(kSoftmaxBarrier, NT);
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
+        const bool corr = flags[0] != 0;
+        if (ok && corr && i > 0) {
+          ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, p.wait_cycles);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int d = 0; d < 4; ++d) {
+#pragma unroll
+              for (int cc = 0; cc < NRH / 8; ++cc) {
+                uint32_t r[8];
+                const uint32_t addr = tmem + lane_addr + C::kOCol + d * NR + rbase + cc * 8;
+                tmem_ld8(addr, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[rbase + cc * 8 + k]);
+                tmem_st8(addr, r);
+              }
+            }
+            tmem_st_wait();
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], kreg[k]);
+      if (ok) {
+        // P^T (BF16) into the rope block of this tile's stage, MN-major:
+        // [NR/8 row groups][64 tokens][8 rows].
+        uint8_t* pbuf = base + C::kKV + (i % C::NST) * kTileBytesB + kRopeOffB;
+        if (has_tok) {
+#pragma unroll
+          for (int g = 0; g < NRH / 8; ++g) {
+            uint4 v;
+            v.x = pack_bf16x2(t[g * 8 + 0], t[g * 8 + 1]);
+            v.y = pack_bf16x2(t[g * 8 + 2], t[g * 8 + 3]);
+            v.z = pack_bf16x2(t[g * 8 + 4], t[g * 8 + 5]);
+            v.w = pack_bf16x2(t[g * 8 + 6], t[g * 8 + 7]);
+            *reinterpret_cast<uint4*>(pbuf + ((rbase >> 3) + g) * 1024 + tok * 16) = v;
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(BAR_PFULL0 + (i & 1)));
+      }
+      warp_reduce_rows<NRH, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR + rbase);
+    }
+    if (!ok && lane == 0) {
+      report(p.status, MLA_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // ---- epilogue (as in the FP8 kernel; O^T has NR columns per block) ----
+    named_bar_sync(kSoftmaxBarrier, NT);
+    const bool single = (nsplit == 1);
+    float* scale_s = alpha_s;
+    if (sid < NR) {
+      if (n_tiles > 0) {
+        const float* rs = red_sum + ((n_tiles - 1) & 1) * 4 * NR;
+        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+      }
+      const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
+      const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + sid;
+      float sc = 0.0f;
+      if (sid < rows_here) {
+        if (single) {
+          const float ls = (l_row > 0.0f) ? 0.6931471805599453f * (m_s + log2f(l_row)) : -INFINITY;
+          if (p.lse) p.lse[grow] = ls;
+          sc = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
+        } else {
+          float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
+          ml[0] = m_s;
+          ml[1] = l_row;
+          sc = 1.0f;
+        }
+      }
+      scale_s[sid] = sc;
+    }
+    named_bar_sync(kSoftmaxBarrier, NT);
+    bool fin = mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
+    fin = __all_sync(0xffffffffu, fin);
+    if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
+    if (ok && fin && n_tiles > 0) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int d = 0; d < 4; ++d) {
+        const int dim = d * 128 + dim_lane;
+#pragma unroll
+        for (int cc = 0; cc < NRH / 8; ++cc) {
+          uint32_t r[8];
+          tmem_ld8(tmem + lane_addr + C::kOCol + d * NR + rbase + cc * 8, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int row = rbase + cc * 8 + k;
+            if (row < rows_here) {
+              const float v = __uint_as_float(r[k]) * scale_s[row];
+              const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
+              if (single) {
+                p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
+                if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = v;
+              } else {
+                p.ws_o[(grow * p.max_splits + split) * MLA_LATENT_DIM + dim] = v;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 2-D BF16 view [rows, 576] with a (64, box_y) box, 128-byte swizzle.
+static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t box_y) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {MLA_HEAD_DIM, rows};
+  cuuint64_t strides[1] = {kRowBytesB};
+  cuuint32_t box[2] = {64, box_y};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NR>
+static cudaError_t launch_split_bf16(const void* q, const void* kv, int64_t num_pages, int batch,
+                                     int groups, const DecodeParams& prm, cudaStream_t stream) {
+  using C = CfgB<NR>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_bf16_kernel<NR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  CUtensorMap tm_kv, tm_q;
+  if (!make_map_bf16(&tm_kv, kv, static_cast<uint64_t>(num_pages) * MLA_PAGE_SIZE,
+                     MLA_PAGE_SIZE) ||
+      !make_map_bf16(&tm_q, q, static_cast<uint64_t>(batch) * prm.rows_per_req, NR))
+    return cudaErrorInvalidValue;
+  dim3 grid(prm.max_splits * groups, batch);
+  mla_split_kv_bf16_kernel<NR><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_q, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t num_pages,
+                               const int32_t* page_table, int32_t max_pages_per_req,
+                               const int32_t* kv_lens, const int32_t* splits,
+                               const int32_t* chunks, int32_t max_splits, int32_t kv_split,
+                               int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
+                               float softmax_scale, void* workspace, size_t workspace_bytes,
+                               void* out_bf16, float* lse_f32, float* out_f32_debug,
+                               void* stream) {
+  if (!q_bf16 || !kv_pages_bf16 || !page_table || !kv_lens || !splits || !chunks || !workspace ||
+      !out_bf16) {
+    set_error("mla_decode_bf16: null pointer argument");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (batch < 1 || q_len < 1 || num_heads < 1 || max_pages_per_req < 1 || num_pages < 1) {
+    set_error("mla_decode_bf16: batch, q_len, num_heads, max_pages_per_req and num_pages must be >= 1");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(num_heads) * q_len > MLA_MAX_ROWS || batch > 65535) {
+    set_error("mla_decode_bf16: num_heads * q_len above MLA_MAX_ROWS or batch above 65535");
+    return MLA_ERR_UNSUPPORTED;
+  }
+  if (num_pages * MLA_PAGE_SIZE > INT32_MAX) {
+    set_error("mla_decode_bf16: page pool too large for 32-bit TMA row coordinates");
+    return MLA_ERR_UNSUPPORTED;
+  }
+  if (max_splits < 1 || max_splits > MLA_MAX_SPLITS ||
+      (kv_split != 1 && kv_split != 2 && kv_split != 4 && kv_split != 8 && kv_split != 16)) {
+    set_error("mla_decode_bf16: max_splits in [1, MLA_MAX_SPLITS], kv_split in {1,2,4,8,16}");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!aligned(q_bf16, 16) || !aligned(kv_pages_bf16, 16) || !aligned(workspace, 256) ||
+      !aligned(out_bf16, 8) || (out_f32_debug && !aligned(out_f32_debug, 16))) {
+    set_error("mla_decode_bf16: q/kv need 16-byte, workspace 256-byte, outputs 8/16-byte alignment");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(softmax_scale)) {
+    set_error("mla_decode_bf16: softmax_scale must be finite");
+    return MLA_ERR_INVALID_ARG;
+  }
+  const int64_t rows_total = static_cast<int64_t>(batch) * q_len * num_heads;
+  const size_t need = ws_total(rows_total, max_splits);
+  if (workspace_bytes < need) {
+    set_error("mla_decode_bf16: workspace of " + std::to_string(workspace_bytes) +
+              " bytes is below the " + std::to_string(need) + " required");
+    return MLA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  const RowGroups rg = row_groups(num_heads * q_len);
+  DecodeParams prm = {};
+  prm.page_table = page_table;
+  prm.kv_lens = kv_lens;
+  prm.splits = splits;
+  prm.chunks = chunks;
+  prm.num_pages = num_pages;
+  prm.max_pages = max_pages_per_req;
+  prm.max_splits = max_splits;
+  prm.q_len = q_len;
+  prm.num_heads = num_heads;
+  prm.causal = causal ? 1 : 0;
+  prm.rows_per_req = num_heads * q_len;
+  prm.rows_per_group = rg.rows;
+  prm.c_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+  prm.kv_scale = 1.0f;
+  prm.output_scale = 1.0f;
+  {
+    const long long w = g_wait_cycles.load();
+    prm.wait_cycles = w > 0 ? w : kWaitLimitCycles;
+  }
+  prm.status = reinterpret_cast<int*>(ws);
+  prm.ws_ml = reinterpret_cast<float*>(ws + ws_ml_offset());
+  prm.ws_o = reinterpret_cast<float*>(ws + ws_o_offset(rows_total, max_splits));
+  prm.out = reinterpret_cast<__nv_bfloat16*>(out_bf16);
+  prm.lse = lse_f32;
+  prm.out_f32 = out_f32_debug;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (rg.nr) {
+    case 16: e = launch_split_bf16<16>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
+    case 32: e = launch_split_bf16<32>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
+    case 48: e = launch_split_bf16<48>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
+    default:
+      set_error("mla_decode_bf16: internal row grouping error");
+      return MLA_ERR_UNSUPPORTED;
+  }
+  if (e != cudaSuccess) return cuda_fail("mla_decode_bf16: split-KV launch", e);
+  if (max_splits > 1) {
+    MergeParams mp = {};
+    mp.po = prm.ws_o;
+    mp.pml = prm.ws_ml;
+    mp.rows = static_cast<int32_t>(rows_total);
+    mp.stride_s = max_splits;
+    mp.uniform_s = max_splits;
+    mp.splits = splits;
+    mp.rows_per_req = num_heads * q_len;
+    mp.num_heads = num_heads;
+    mp.output_scale = 1.0f;
+    mp.sinks = nullptr;
+    mp.out = prm.out;
+    mp.lse = lse_f32;
+    mp.out_f32 = out_f32_debug;
+    e = launch_merge(mp, kv_split, st);
+    if (e != cudaSuccess) return cuda_fail("mla_decode_bf16: merge launch", e);
+  }
+  return MLA_OK;
+}
