@@ -66,6 +66,10 @@ def _load():
             lib.mla_oracle_decode_rows_ex.argtypes = [
                 p, p, i32, i64, p, i32, p, i32, i32, i32, i32, f64, f64, f64, p, f64, p, i64,
                 i64, i64, i32, p, p, p, p, i32]
+            lib.mla_oracle_decode_rows_v2.restype = ctypes.c_int
+            lib.mla_oracle_decode_rows_v2.argtypes = [
+                p, p, i32, i64, p, i32, p, i32, i32, i32, i32, f64, f64, f64, p, f64, p, p, p,
+                i32, p, i64, i64, i64, i32, p, p, p, p, i32]
             lib.mla_oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.mla_oracle_e4m3_encode.argtypes = [ctypes.c_float]
             lib.mla_oracle_kv_append.restype = ctypes.c_int
@@ -102,15 +106,19 @@ def e4m3_decode(codes) -> np.ndarray:
 def decode_rows(q, kv, page_table, kv_lens, *, q_len: int, num_heads: int, causal: bool,
                 softmax_scale: float, q_scale: float = 1.0, kv_scale: float = 1.0,
                 rows=None, tok_begin: int = -1, tok_end: int = -1, partial: bool = False,
-                n_threads: int = 0, sinks=None, output_scale: float = 1.0):
+                n_threads: int = 0, sinks=None, output_scale: float = 1.0, query_lens=None,
+                kv_bounds=None, block_idx=None):
     """Run the fp64 oracle on the given rows.
 
     q: uint8 [B, q_len, H, 576]; kv: uint8 [P, 32, 576] (E4M3 codes), or both
     torch bfloat16 tensors (the BF16-KV variant); page_table int32
     [B, max_pages]; kv_lens int32 [B].  rows: flat row ids (b*q_len+qi)*H+h,
     default all.  sinks: optional per-head sink logits [H] (natural-log units);
-    output_scale multiplies O.  Returns (O [n, 512], LSE [n]) or, with partial=True,
-    (O_unnormalised [n, 512], m_log2 [n], l [n]).
+    output_scale multiplies O.  query_lens int32 [B] (per-request query tokens in
+    the padded q_len slots), kv_bounds int32 [B, 2] (key window [lo, hi)) and
+    block_idx int32 [B, topk] (selected logical pages, negative = unused)
+    restrict the visible keys; see mla_oracle.c.  Returns (O [n, 512], LSE [n])
+    or, with partial=True, (O_unnormalised [n, 512], m_log2 [n], l [n]).
     """
     lib = _load()
     dtype = 0
@@ -141,11 +149,16 @@ def decode_rows(q, kv, page_table, kv_lens, *, q_len: int, num_heads: int, causa
     l = np.zeros((n,), dtype=np.float64)
     num_pages = int(kva.shape[0])
     sk = None if sinks is None else _np(sinks, np.float64)
-    st = lib.mla_oracle_decode_rows_ex(
+    ql = None if query_lens is None else _np(query_lens, np.int32)
+    kb = None if kv_bounds is None else _np(kv_bounds, np.int32).reshape(batch, 2)
+    bi = None if block_idx is None else _np(block_idx, np.int32).reshape(batch, -1)
+    st = lib.mla_oracle_decode_rows_v2(
         qa.ctypes.data, kva.ctypes.data, dtype, num_pages, pt.ctypes.data, int(pt.shape[1]),
         lens.ctypes.data, batch, int(q_len), int(num_heads), int(bool(causal)), float(q_scale),
         float(kv_scale), float(softmax_scale), None if sk is None else sk.ctypes.data,
-        float(output_scale), ra.ctypes.data, n, int(tok_begin), int(tok_end),
+        float(output_scale), None if ql is None else ql.ctypes.data,
+        None if kb is None else kb.ctypes.data, None if bi is None else bi.ctypes.data,
+        0 if bi is None else int(bi.shape[1]), ra.ctypes.data, n, int(tok_begin), int(tok_end),
         1 if partial else 0, out.ctypes.data, lse.ctypes.data, m.ctypes.data, l.ctypes.data,
         int(n_threads))
     if st != 0:

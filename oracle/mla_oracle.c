@@ -122,6 +122,16 @@ static int64_t key_index(const int32_t* page_table, int32_t max_pages, int32_t b
  *         l_out[i] = l.
  * Returns 0, or -1 on an out-of-range page id, -2 on allocation failure.
  */
+int mla_oracle_decode_rows_v2(const void* q, const void* kv, int32_t dtype, int64_t num_pages,
+                              const int32_t* page_table, int32_t max_pages,
+                              const int32_t* kv_lens, int32_t batch, int32_t q_len,
+                              int32_t num_heads, int32_t causal, double q_scale,
+                              double kv_scale, double softmax_scale, const double* sinks,
+                              double output_scale, const int32_t* query_lens,
+                              const int32_t* kv_bounds, const int32_t* block_idx, int32_t topk,
+                              const int64_t* rows, int64_t n_rows, int64_t tok_begin,
+                              int64_t tok_end, int32_t mode, double* out, double* lse,
+                              double* m_out, double* l_out, int32_t n_threads);
 int mla_oracle_decode_rows_ex(const void* q, const void* kv, int32_t dtype, int64_t num_pages,
                               const int32_t* page_table, int32_t max_pages,
                               const int32_t* kv_lens, int32_t batch, int32_t q_len,
@@ -162,6 +172,43 @@ int mla_oracle_decode_rows_ex(const void* q, const void* kv, int32_t dtype, int6
                               double output_scale, const int64_t* rows, int64_t n_rows,
                               int64_t tok_begin, int64_t tok_end, int32_t mode, double* out,
                               double* lse, double* m_out, double* l_out, int32_t n_threads) {
+  return mla_oracle_decode_rows_v2(q, kv, dtype, num_pages, page_table, max_pages, kv_lens, batch,
+                                   q_len, num_heads, causal, q_scale, kv_scale, softmax_scale,
+                                   sinks, output_scale, NULL, NULL, NULL, 0, rows, n_rows,
+                                   tok_begin, tok_end, mode, out, lse, m_out, l_out, n_threads);
+}
+
+/*
+ * The general form: mla_oracle_decode_rows_ex plus three restrictions of the
+ * visible keys: the run() arguments is_var_q/query_lens and kv_bounds (issue
+ * #20510, "Repro 1", arguments added after #19338), and the sparse decode over
+ * selected pages (TensorRT-LLM PR #17441 "m3 decode perf": the sparse decode
+ * kernel after the block selector, with E4M3 q widened inside the kernel).
+ * The pages name these arguments without defining them; the readings are:
+ *
+ *   query_lens (int32 [B] or NULL): request b has q_b = query_lens[b] query
+ *     tokens, 1 <= q_b <= q_len, in slots qi < q_b of the padded
+ *     [B][q_len][H] row layout.  They are the last q_b positions of the
+ *     request, so under causal query qi sees keys j <= L_b - q_b + qi.  Rows
+ *     with qi >= q_b see no key (O = 0, LSE = -inf, or the sink).
+ *   kv_bounds (int32 [B][2] or NULL): keys restricted to lo <= j < hi with
+ *     (lo, hi) = kv_bounds[b] (a window of the request's keys).
+ *   block_idx (int32 [B][topk] or NULL): keys restricted to the request's
+ *     logical pages listed in block_idx[b] (page p holds keys [32p, 32p+32));
+ *     negative entries are unused slots.  A page listed twice counts once.
+ *
+ * All restrictions intersect the causal range and [0, L_b).
+ */
+int mla_oracle_decode_rows_v2(const void* q, const void* kv, int32_t dtype, int64_t num_pages,
+                              const int32_t* page_table, int32_t max_pages,
+                              const int32_t* kv_lens, int32_t batch, int32_t q_len,
+                              int32_t num_heads, int32_t causal, double q_scale,
+                              double kv_scale, double softmax_scale, const double* sinks,
+                              double output_scale, const int32_t* query_lens,
+                              const int32_t* kv_bounds, const int32_t* block_idx, int32_t topk,
+                              const int64_t* rows, int64_t n_rows, int64_t tok_begin,
+                              int64_t tok_end, int32_t mode, double* out, double* lse,
+                              double* m_out, double* l_out, int32_t n_threads) {
   double lut[256];
   int status = 0;
   build_lut(lut);
@@ -182,10 +229,34 @@ int mla_oracle_decode_rows_ex(const void* q, const void* kv, int32_t dtype, int6
     double* o = out + i * ORC_LATENT_DIM;
     int64_t lo, hi;
     for (int d = 0; d < ORC_HEAD_DIM; ++d) qd[d] = q_scale * elem(q, dtype, r, d, lut);
-    row_range(kv_lens[b], q_len, qi, causal, tok_begin, tok_end, &lo, &hi);
+    const int32_t qb = query_lens ? query_lens[b] : q_len;
+    row_range(kv_lens[b], qb, qi, causal, tok_begin, tok_end, &lo, &hi);
+    if (qi >= qb) hi = lo;  /* a padding slot of a shorter query block */
+    if (kv_bounds) {
+      if (lo < kv_bounds[2 * b]) lo = kv_bounds[2 * b];
+      if (hi > kv_bounds[2 * b + 1]) hi = kv_bounds[2 * b + 1];
+      if (hi < lo) hi = lo;
+    }
     for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] = 0.0;
     const double sink = (sinks && mode == 0) ? sinks[h] : -INFINITY;
-    if (hi <= lo) {
+    /* Selected pages of this request (all pages when there is no selection). */
+    unsigned char* sel = NULL;
+    if (block_idx && hi > lo) {
+      sel = (unsigned char*)calloc((size_t)max_pages, 1);
+      if (!sel) {
+#pragma omp atomic write
+        status = -2;
+        continue;
+      }
+      for (int32_t t = 0; t < topk; ++t) {
+        int32_t pg = block_idx[(int64_t)b * topk + t];
+        if (pg >= 0 && pg < max_pages) sel[pg] = 1;
+      }
+    }
+    int64_t n_vis = 0;
+    for (int64_t j = lo; j < hi; ++j) n_vis += (!sel || sel[j / ORC_PAGE]) ? 1 : 0;
+    if (n_vis == 0) {
+      free(sel);
       if (mode == 0) {
         lse[i] = sink;
       } else {
@@ -196,13 +267,18 @@ int mla_oracle_decode_rows_ex(const void* q, const void* kv, int32_t dtype, int6
     }
     double* s = (double*)malloc(sizeof(double) * (size_t)(hi - lo));
     if (!s) {
+      free(sel);
 #pragma omp atomic write
       status = -2;
       continue;
     }
     int bad = 0;
-    /* Pass 1: scores. */
+    /* Pass 1: scores (keys outside the selection are not visible: -inf). */
     for (int64_t j = lo; j < hi; ++j) {
+      if (sel && !sel[j / ORC_PAGE]) {
+        s[j - lo] = -INFINITY;
+        continue;
+      }
       int64_t page = page_table[(int64_t)b * max_pages + j / ORC_PAGE];
       if (page < 0 || page >= num_pages) {
         bad = 1;
@@ -221,6 +297,7 @@ int mla_oracle_decode_rows_ex(const void* q, const void* kv, int32_t dtype, int6
        and no value). */
     double Z = (sink == -INFINITY) ? 0.0 : exp(sink - M);
     for (int64_t j = lo; j < hi; ++j) {
+      if (sel && !sel[j / ORC_PAGE]) continue;
       double w = exp(s[j - lo] - M);
       int64_t page = page_table[(int64_t)b * max_pages + j / ORC_PAGE];
       Z += w;
@@ -229,6 +306,7 @@ int mla_oracle_decode_rows_ex(const void* q, const void* kv, int32_t dtype, int6
       for (int d = 0; d < ORC_LATENT_DIM; ++d) o[d] += w * (kv_scale * elem(kv, dtype, kr, d, lut));
     }
     free(s);
+    free(sel);
     if (bad) {
 #pragma omp atomic write
       status = -1;

@@ -12,7 +12,10 @@ from .mla_inputs import (  # noqa: F401
     DecodeInputs,
     WORKLOADS,
     decode_inputs,
+    kv_windows,
     merge_partials,
+    page_selection,
+    query_lens_ragged,
     ragged_lens,
     workload_inputs,
 )

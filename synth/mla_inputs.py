@@ -154,6 +154,54 @@ def ragged_lens(seed: int = 4, n: int = 16, lo: int = 1024, hi: int = 131072) ->
     return [int(x) for x in rng.integers(lo, hi, size=n, endpoint=True)]
 
 
+def query_lens_ragged(batch: int, q_len: int, seed: int) -> List[int]:
+    """Per-request query-token counts, uniform in [1, q_len], seeded."""
+    rng = np.random.default_rng(seed)
+    return [int(x) for x in rng.integers(1, q_len, size=batch, endpoint=True)]
+
+
+def kv_windows(kv_lens: Sequence[int], seed: int, full_every: int = 4) -> np.ndarray:
+    """Key windows [lo, hi) per request, int32 [B, 2], seeded.
+
+    lo is uniform in [0, L - 1] and hi uniform in [lo + 1, L]; every
+    full_every-th request keeps its whole range and every other one ends at L
+    (a sliding window), so whole, trailing and inner windows all occur.
+    """
+    rng = np.random.default_rng(seed)
+    out = np.zeros((len(kv_lens), 2), dtype=np.int32)
+    for b, L in enumerate(kv_lens):
+        L = int(L)
+        if full_every and b % full_every == 0:
+            out[b] = (0, L)
+            continue
+        lo = int(rng.integers(0, L))
+        hi = L if b % 2 == 1 else int(rng.integers(lo + 1, L, endpoint=True))
+        out[b] = (lo, hi)
+    return out
+
+
+def page_selection(kv_lens: Sequence[int], topk: int, seed: int,
+                   keep_last: bool = True) -> np.ndarray:
+    """Selected logical pages per request, int32 [B, topk], seeded.
+
+    Each request gets min(topk, pages) distinct pages in ascending order
+    (with keep_last, always including its last, possibly partial, page, as a
+    local window does); unused slots at the end are -1.
+    """
+    rng = np.random.default_rng(seed)
+    out = np.full((len(kv_lens), topk), -1, dtype=np.int32)
+    for b, L in enumerate(kv_lens):
+        n_pages = (int(L) + PAGE_SIZE - 1) // PAGE_SIZE
+        k = min(topk, n_pages)
+        if keep_last:
+            rest = rng.choice(n_pages - 1, size=k - 1, replace=False) if k > 1 else []
+            pages = np.sort(np.concatenate([np.asarray(rest, dtype=np.int64), [n_pages - 1]]))
+        else:
+            pages = np.sort(rng.choice(n_pages, size=k, replace=False))
+        out[b, :k] = pages
+    return out
+
+
 def merge_partials(rows: int, num_splits: int, seed: int, empty_frac: float = 0.1,
                    all_empty_rows: Sequence[int] = ()):
     """Synthetic split partials for the merge alone.

@@ -12,7 +12,8 @@ import pytest
 import torch
 
 import oracle
-from synth import HEAD_DIM, LATENT_DIM, PAGE_SIZE, SOFTMAX_SCALE, decode_inputs, merge_partials
+from synth import (HEAD_DIM, LATENT_DIM, PAGE_SIZE, SOFTMAX_SCALE, decode_inputs, kv_windows,
+                   merge_partials, page_selection, query_lens_ragged)
 
 
 def _gather_keys(inp, b):
@@ -370,3 +371,161 @@ def test_bf16_oracle_matches_torch_attention(B, H, q_len, lens, causal):
         lses.append(torch.logsumexp(((q @ keys.T) * 0.11).masked_fill(~mask, -math.inf), -1))
     np.testing.assert_allclose(out, torch.cat(outs).numpy(), rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(lse, torch.cat(lses).numpy(), rtol=1e-12, atol=1e-12)
+
+
+# --- Restricted key sets: ragged q, key windows, page selection ----------------
+#
+# Readings of the run() arguments is_var_q/query_lens and kv_bounds (issue
+# #20510, "Repro 1") and of the sparse decode over selected pages (PR #17441):
+# query_lens[b] real query tokens in the first slots of the padded q_len block
+# (the request's last positions), a key window [lo, hi), and a set of logical
+# pages.  Pinned against torch's float64 attention with the visibility mask
+# written from those definitions, and against the unrestricted oracle on
+# caches rebuilt to hold only the visible keys.
+
+def _visible(L, q_b, qi, causal, window, pages):
+    """Boolean [L] visibility of keys for query slot qi (test-side definition)."""
+    j = torch.arange(L)
+    vis = torch.full((L,), qi < q_b, dtype=torch.bool)
+    if causal:
+        vis &= j <= L - q_b + qi
+    if window is not None:
+        vis &= (j >= int(window[0])) & (j < int(window[1]))
+    if pages is not None:
+        sel = torch.zeros(((L + PAGE_SIZE - 1) // PAGE_SIZE,), dtype=torch.bool)
+        for p in pages:
+            if p >= 0:
+                sel[int(p)] = True
+        vis &= sel[j // PAGE_SIZE]
+    return vis
+
+
+def _restricted_reference(inp, causal, scale, qlens=None, windows=None, sel=None):
+    outs, lses = [], []
+    B, q_len, H = inp.batch, inp.q_len, inp.num_heads
+    for b in range(B):
+        keys = _widen(_gather_keys(inp, b))
+        L = keys.shape[0]
+        q = _widen(inp.q[b]).reshape(q_len * H, HEAD_DIM)
+        q_b = q_len if qlens is None else int(qlens[b])
+        for qi in range(q_len):
+            vis = _visible(L, q_b, qi, causal, None if windows is None else windows[b],
+                           None if sel is None else sel[b])
+            for h in range(H):
+                if not bool(vis.any()):
+                    outs.append(torch.zeros(LATENT_DIM, dtype=torch.float64))
+                    lses.append(torch.tensor(-math.inf, dtype=torch.float64))
+                    continue
+                qr = q[qi * H + h]
+                o = torch.nn.functional.scaled_dot_product_attention(
+                    qr[None, None, None], keys[None, None], keys[None, None, :, :LATENT_DIM],
+                    attn_mask=vis[None, None, None], scale=scale)[0, 0, 0]
+                logits = ((keys @ qr) * scale).masked_fill(~vis, -math.inf)
+                outs.append(o)
+                lses.append(torch.logsumexp(logits, dim=0))
+    return torch.stack(outs).numpy(), torch.stack(lses).numpy()
+
+
+@pytest.mark.parametrize("kind", ["query_lens", "window", "pages", "all"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_restricted_keys_match_torch_attention(kind, causal):
+    lens = [77, 130, 41]
+    inp = decode_inputs(3, 2, 4, lens, seed=31, extra_pages=2)
+    ql = query_lens_ragged(3, 4, seed=5) if kind in ("query_lens", "all") else None
+    win = kv_windows(lens, seed=6, full_every=0) if kind in ("window", "all") else None
+    sel = page_selection(lens, 3, seed=7, keep_last=False) if kind in ("pages", "all") else None
+    out, lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=4,
+                                  num_heads=2, causal=causal, softmax_scale=0.2,
+                                  query_lens=ql, kv_bounds=win, block_idx=sel)
+    ref_o, ref_l = _restricted_reference(inp, causal, 0.2, ql, win, sel)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-12, atol=1e-12)
+    fin = np.isfinite(ref_l)
+    assert np.array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(lse[fin], ref_l[fin], rtol=1e-12, atol=1e-12)
+
+
+def test_query_lens_padding_rows_are_empty_and_sinks_fill_them():
+    inp = decode_inputs(2, 3, 4, [50, 60], seed=32)
+    ql = [2, 4]
+    sinks = np.array([0.5, -1.0, 2.0])
+    out, lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=4,
+                                  num_heads=3, causal=True, softmax_scale=0.2, query_lens=ql,
+                                  sinks=sinks)
+    rows = np.arange(2 * 4 * 3)
+    qi = (rows // 3) % 4
+    b = rows // 12
+    pad = qi >= np.array(ql)[b]
+    assert pad.sum() == 2 * 3
+    # A row that sees no key is the sink alone: O = 0, LSE = the sink logit.
+    assert np.all(out[pad] == 0.0)
+    np.testing.assert_array_equal(lse[pad], sinks[rows[pad] % 3])
+
+
+def _repaged(inp, b, tokens):
+    """A one-request cache holding the given token positions of request b, in
+    order, packed from position 0 (pages filled in order)."""
+    keys = _gather_keys(inp, b)[tokens]
+    n = keys.shape[0]
+    n_pages = (n + PAGE_SIZE - 1) // PAGE_SIZE
+    pool = torch.zeros((n_pages, PAGE_SIZE, HEAD_DIM), dtype=torch.uint8)
+    pool.view(-1, HEAD_DIM)[:n] = keys
+    table = torch.arange(n_pages, dtype=torch.int32)[None, :]
+    return pool, table, n
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_trailing_window_equals_cache_of_the_window(causal):
+    # A window [lo, L) equals attention over a cache that holds only those keys
+    # (the causal limit moves with the end of the cache).
+    inp = decode_inputs(1, 2, 3, [150], seed=33)
+    lo = 37
+    out, lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=3,
+                                  num_heads=2, causal=causal, softmax_scale=0.2,
+                                  kv_bounds=[[lo, 150]])
+    pool, table, n = _repaged(inp, 0, torch.arange(lo, 150))
+    ref_o, ref_l = oracle.decode_rows(inp.q, pool, table, [n], q_len=3, num_heads=2,
+                                      causal=causal, softmax_scale=0.2)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(lse, ref_l, rtol=1e-13, atol=1e-13)
+
+
+def test_page_selection_equals_gathered_cache():
+    # Selected pages (ascending, last page partial) equal attention over a cache
+    # made of those pages alone.
+    lens = [300]
+    inp = decode_inputs(1, 3, 1, lens, seed=34)
+    sel = np.array([[1, 4, 5, 9]], dtype=np.int32)  # page 9 holds tokens 288..299
+    out, lse = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=1,
+                                  num_heads=3, causal=False, softmax_scale=0.2, block_idx=sel)
+    toks = torch.cat([torch.arange(p * PAGE_SIZE, min((p + 1) * PAGE_SIZE, 300))
+                      for p in sel[0]])
+    pool, table, n = _repaged(inp, 0, toks)
+    ref_o, ref_l = oracle.decode_rows(inp.q, pool, table, [n], q_len=1, num_heads=3,
+                                      causal=False, softmax_scale=0.2)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(lse, ref_l, rtol=1e-13, atol=1e-13)
+    # Unused (-1) slots and a repeated page change nothing.
+    sel2 = np.array([[1, 4, 4, 5, 9, -1, -1]], dtype=np.int32)
+    out2, lse2 = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=1,
+                                    num_heads=3, causal=False, softmax_scale=0.2, block_idx=sel2)
+    np.testing.assert_array_equal(out2, out)
+    np.testing.assert_array_equal(lse2, lse)
+
+
+def test_window_split_partials_merge_to_the_window():
+    # Split invariance holds on a restricted key set too: partials over two
+    # halves of the token range merge to the whole.
+    inp = decode_inputs(1, 2, 1, [260], seed=35)
+    win = [[50, 230]]
+    o_all, l_all = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=1,
+                                      num_heads=2, causal=False, softmax_scale=0.2,
+                                      kv_bounds=win)
+    parts = [oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens, q_len=1,
+                                num_heads=2, causal=False, softmax_scale=0.2, kv_bounds=win,
+                                tok_begin=a, tok_end=e, partial=True)
+             for a, e in ((0, 128), (128, 260))]
+    po = np.stack([p[0] for p in parts], axis=1)
+    pml = np.stack([np.stack([p[1], p[2]], axis=-1) for p in parts], axis=1)
+    o, l = oracle.merge(po, pml)
+    np.testing.assert_allclose(o, o_all, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l, l_all, rtol=1e-12, atol=1e-12)
