@@ -143,6 +143,19 @@ MLA_API int mla_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_
  *     units of the scaled scores (natural log).  A sink acts as one more key
  *     with that logit and a zero value: it joins the softmax denominator, so
  *     O shrinks and LSE = ln(sum_j exp(s_j) + exp(sink)).
+ * query_lens  NULL or device int32 [batch] (issue #20510, "Repro 1": the
+ *     run() arguments is_var_q / query_lens; the pages do not define them, so
+ *     this is the plain reading): request b has query_lens[b] query tokens,
+ *     1 <= query_lens[b] <= q_len, in slots qi < query_lens[b] of the padded
+ *     [batch, q_len, num_heads] row layout.  They are the request's last
+ *     positions, so under causal slot qi sees keys j <= L - query_lens[b] + qi.
+ *     Rows of the other slots see no key: O = 0, LSE = -inf (or the sink).
+ *     Out-of-range values are reported as MLA_ERR_INVALID_ARG by the device.
+ * kv_bounds  NULL or device int32 [batch][2] (issue #20510, "Repro 1": the
+ *     run() argument kv_bounds; plain reading): keys restricted to
+ *     lo <= j < hi for (lo, hi) = kv_bounds[b], intersected with [0, L) and
+ *     the causal range.  Whole 128-token tiles below lo are skipped.
+ * Zero-initialise the structure: fields added later default to off.
  */
 typedef struct {
   const float* q_scale_dev;
@@ -150,6 +163,8 @@ typedef struct {
   const float* softmax_scale_dev;
   float output_scale;
   const float* sinks;
+  const int32_t* query_lens;
+  const int32_t* kv_bounds;
 } mla_decode_options_t;
 
 /* mla_decode with options (NULL options = mla_decode).  Same arguments,
@@ -162,6 +177,38 @@ MLA_API int mla_decode_ex(const void* q_fp8, const void* kv_pages_fp8, int64_t n
                           float softmax_scale, void* workspace, size_t workspace_bytes,
                           void* out_bf16, float* lse_f32, float* out_f32_debug,
                           const mla_decode_options_t* options, void* stream);
+
+/*
+ * Sparse decode over selected pages (TensorRT-LLM PR #17441 "m3 decode perf":
+ * the sparse MLA decode after the top-k block selector, which reads E4M3 q and
+ * the paged FP8 cache directly).  Keys are restricted to the logical pages
+ * listed per request:
+ *
+ * block_idx  device int32 [batch][topk]: logical page indices of request b
+ *            (page p holds keys [32p, 32p + 32)), strictly increasing over
+ *            the non-negative entries; negative entries are unused slots.
+ *            Pages at or past ceil(L/32) hold no key and are skipped.  Order
+ *            violations seen inside a split are reported as
+ *            MLA_ERR_INVALID_ARG by the device.
+ * topk       entries per request, >= 1.
+ * kv_lens    the requests' true lengths L (the causal limit and the last
+ *            page's tail come from them).
+ * splits, chunks, max_splits, kv_split  the plan of mla_decode_plan for the
+ *            compact lengths 32 * topk of every request: split s covers
+ *            selection entries [s * chunk / 32, (s + 1) * chunk / 32).
+ * options    as for mla_decode_ex (query_lens and kv_bounds also apply), or
+ *            NULL.
+ * Everything else is as for mla_decode.
+ */
+MLA_API int mla_decode_sparse(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                              const int32_t* page_table, int32_t max_pages_per_req,
+                              const int32_t* kv_lens, const int32_t* block_idx, int32_t topk,
+                              const int32_t* splits, const int32_t* chunks, int32_t max_splits,
+                              int32_t kv_split, int32_t batch, int32_t q_len, int32_t num_heads,
+                              int32_t causal, float q_scale, float kv_scale, float softmax_scale,
+                              void* workspace, size_t workspace_bytes, void* out_bf16,
+                              float* lse_f32, float* out_f32_debug,
+                              const mla_decode_options_t* options, void* stream);
 
 /*
  * The two phases of mla_decode, for callers that schedule them separately

@@ -22,8 +22,8 @@ __all__ = [
     "MLA_ERR_CUDA", "MLA_ERR_TIMEOUT", "MlaError", "Plan", "load_library", "library_path",
     "mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init", "mla_decode",
     "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
-    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16", "DecodeOptions",
-    "decode", "merge",
+    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16",
+    "mla_decode_sparse", "DecodeOptions", "decode", "merge",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -40,7 +40,8 @@ _STATUS_NAMES = {
 EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init",
                     "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
                     "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit",
-                    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16")
+                    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16",
+                    "mla_decode_sparse")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
@@ -53,7 +54,8 @@ class DecodeOptions(ctypes.Structure):
     """mla_decode_options_t (include/mla_decode.h)."""
     _fields_ = [("q_scale_dev", ctypes.c_void_p), ("kv_scale_dev", ctypes.c_void_p),
                 ("softmax_scale_dev", ctypes.c_void_p), ("output_scale", ctypes.c_float),
-                ("sinks", ctypes.c_void_p)]
+                ("sinks", ctypes.c_void_p), ("query_lens", ctypes.c_void_p),
+                ("kv_bounds", ctypes.c_void_p)]
 
 
 class MlaError(RuntimeError):
@@ -95,6 +97,9 @@ def load_library() -> ctypes.CDLL:
             getattr(lib, name).argtypes = dec_args
         lib.mla_decode_ex.restype = ctypes.c_int
         lib.mla_decode_ex.argtypes = dec_args[:-1] + [ctypes.POINTER(DecodeOptions), vp]
+        lib.mla_decode_sparse.restype = ctypes.c_int
+        lib.mla_decode_sparse.argtypes = (dec_args[:6] + [vp, i32] + dec_args[6:-1]
+                                          + [ctypes.POINTER(DecodeOptions), vp])
         lib.mla_decode_bf16.restype = ctypes.c_int
         lib.mla_decode_bf16.argtypes = dec_args[:14] + [f32] + dec_args[17:]
         lib.mla_decode_workspace_init.restype = ctypes.c_int
@@ -204,10 +209,11 @@ def mla_decode_ex(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req,
                   kv_scale, softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32=None,
                   out_f32_debug=None, *, q_scale_dev=None, kv_scale_dev=None,
                   softmax_scale_dev=None, output_scale: float = 1.0, sinks=None,
-                  stream=None) -> None:
-    """mla_decode with device-side scales, an output scale and attention sinks."""
+                  query_lens=None, kv_bounds=None, stream=None) -> None:
+    """mla_decode with device-side scales, an output scale, attention sinks,
+    ragged query counts and key windows."""
     opts = DecodeOptions(_ptr(q_scale_dev), _ptr(kv_scale_dev), _ptr(softmax_scale_dev),
-                         float(output_scale), _ptr(sinks))
+                         float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds))
     lib = load_library()
     _check(lib.mla_decode_ex(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages), _ptr(page_table),
                              int(max_pages_per_req), _ptr(kv_lens), _ptr(splits), _ptr(chunks),
@@ -232,6 +238,29 @@ def mla_decode_bf16(q_bf16, kv_pages_bf16, num_pages: int, page_table, max_pages
                                float(softmax_scale), _ptr(workspace), int(workspace_bytes),
                                _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
                                _stream_handle(stream)))
+
+
+def mla_decode_sparse(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req, kv_lens,
+                      block_idx, topk, splits, chunks, max_splits, kv_split, batch, q_len,
+                      num_heads, causal, q_scale, kv_scale, softmax_scale, workspace,
+                      workspace_bytes, out_bf16, lse_f32=None, out_f32_debug=None, *,
+                      q_scale_dev=None, kv_scale_dev=None, softmax_scale_dev=None,
+                      output_scale: float = 1.0, sinks=None, query_lens=None, kv_bounds=None,
+                      stream=None) -> None:
+    """Sparse decode over the selected pages block_idx [batch, topk] (plan with
+    the compact lengths 32 * topk)."""
+    opts = DecodeOptions(_ptr(q_scale_dev), _ptr(kv_scale_dev), _ptr(softmax_scale_dev),
+                         float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds))
+    lib = load_library()
+    _check(lib.mla_decode_sparse(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages),
+                                 _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),
+                                 _ptr(block_idx), int(topk), _ptr(splits), _ptr(chunks),
+                                 int(max_splits), int(kv_split), int(batch), int(q_len),
+                                 int(num_heads), 1 if causal else 0, float(q_scale),
+                                 float(kv_scale), float(softmax_scale), _ptr(workspace),
+                                 int(workspace_bytes), _ptr(out_bf16), _ptr(lse_f32),
+                                 _ptr(out_f32_debug), ctypes.byref(opts),
+                                 _stream_handle(stream)))
 
 
 def mla_decode_splitkv(*args, **kw) -> None:
@@ -313,23 +342,28 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
            plan: Optional[Plan] = None, sm_count: Optional[int] = None, target_ctas: int = 0,
            kv_split: Optional[int] = None, want_f32: bool = False, stream=None,
            check_status: bool = True, sinks=None, output_scale: float = 1.0,
-           device_scales: bool = False):
+           device_scales: bool = False, query_lens=None, kv_bounds=None, block_idx=None):
     """Plan, allocate outputs and a workspace with torch, and run mla_decode.
 
     q_fp8 uint8 [B, q, H, 576] and kv_pages_fp8 uint8 [P, 32, 576] (E4M3 codes)
     and page_table int32 [B, max_pages] are CUDA tensors; kv_lens is a host
     sequence.  With torch.bfloat16 q and kv this runs mla_decode_bf16 (no
-    scales, sinks or output scale there).  Returns (out_bf16, lse, out_f32 or
-    None).
+    scales, sinks or output scale there).  query_lens [B], kv_bounds [B, 2]
+    and block_idx [B, topk] (selected pages: mla_decode_sparse, planned on the
+    compact lengths) restrict the visible keys.  Returns (out_bf16, lse,
+    out_f32 or None).
     """
     import torch
     dev = q_fp8.device
     lens = np.asarray(kv_lens.cpu() if hasattr(kv_lens, "cpu") else kv_lens, dtype=np.int32)
     batch = int(lens.shape[0])
+    topk = 0 if block_idx is None else int(block_idx.shape[1])
     if plan is None:
         if sm_count is None:
             sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-        plan = mla_decode_plan(lens, num_heads, q_len, sm_count=sm_count, target_ctas=target_ctas)
+        plan_lens = lens if block_idx is None else np.full_like(lens, PAGE_SIZE * topk)
+        plan = mla_decode_plan(plan_lens, num_heads, q_len, sm_count=sm_count,
+                               target_ctas=target_ctas)
     ks = plan.kv_split if kv_split is None else int(kv_split)
     lens_d = torch.from_numpy(lens).to(dev)
     splits_d = torch.from_numpy(plan.splits).to(dev)
@@ -343,13 +377,14 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
                if want_f32 else None)
     common = (q_fp8, kv_pages_fp8, kv_pages_fp8.shape[0], page_table, page_table.shape[1],
               lens_d, splits_d, chunks_d, plan.max_splits, ks, batch, q_len, num_heads, causal)
+    restricted = query_lens is not None or kv_bounds is not None or block_idx is not None
     if q_fp8.dtype == torch.bfloat16:
         if (kv_pages_fp8.dtype != torch.bfloat16 or sinks is not None or output_scale != 1.0
-                or device_scales or q_scale != 1.0 or kv_scale != 1.0):
-            raise ValueError("BF16 decode takes BF16 q and kv and no scales, sinks or "
-                             "output scale")
+                or device_scales or q_scale != 1.0 or kv_scale != 1.0 or restricted):
+            raise ValueError("BF16 decode takes BF16 q and kv and no scales, sinks, output "
+                             "scale or key restrictions")
         mla_decode_bf16(*common, softmax_scale, ws, ws_bytes, out, lse, out_f32, stream)
-    elif sinks is None and output_scale == 1.0 and not device_scales:
+    elif sinks is None and output_scale == 1.0 and not device_scales and not restricted:
         mla_decode(*common, q_scale, kv_scale, softmax_scale, ws, ws_bytes, out, lse, out_f32,
                    stream)
     else:
@@ -361,11 +396,20 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
         # With device scales the host values are placeholders the kernel must
         # ignore (deliberately wrong, so a kernel that used them would fail).
         host = (99.0,) * 3 if device_scales else (q_scale, kv_scale, softmax_scale)
-        mla_decode_ex(*common, *host, ws, ws_bytes, out, lse, out_f32,
-                      q_scale_dev=None if dev_s is None else dev_s[0:1],
-                      kv_scale_dev=None if dev_s is None else dev_s[1:2],
-                      softmax_scale_dev=None if dev_s is None else dev_s[2:3],
-                      output_scale=output_scale, sinks=sk, stream=stream)
+
+        def _dev_i32(x):
+            return None if x is None else torch.as_tensor(x, dtype=torch.int32).to(dev).contiguous()
+        ql_d, kb_d, bi_d = _dev_i32(query_lens), _dev_i32(kv_bounds), _dev_i32(block_idx)
+        extra = dict(q_scale_dev=None if dev_s is None else dev_s[0:1],
+                     kv_scale_dev=None if dev_s is None else dev_s[1:2],
+                     softmax_scale_dev=None if dev_s is None else dev_s[2:3],
+                     output_scale=output_scale, sinks=sk, query_lens=ql_d, kv_bounds=kb_d,
+                     stream=stream)
+        if bi_d is None:
+            mla_decode_ex(*common, *host, ws, ws_bytes, out, lse, out_f32, **extra)
+        else:
+            mla_decode_sparse(*common[:6], bi_d, topk, *common[6:], *host, ws, ws_bytes, out,
+                              lse, out_f32, **extra)
     if check_status:
         mla_decode_status(ws, stream)
     return out, lse, out_f32

@@ -78,7 +78,7 @@ struct Cfg {
   // Shared memory, offsets from a 1024-byte aligned base.
   static constexpr uint32_t kPHalf = NR * kTileTokens;  // one E4M3 term of P^T
   static constexpr uint32_t kPBytes = 2 * kPHalf;       // hi + lo
-  static constexpr uint32_t kAuxBytes = 160 + 52 * NR;
+  static constexpr uint32_t kAuxBytes = 176 + 52 * NR;
   static constexpr uint32_t kQBytes = NR * MLA_HEAD_DIM;
   // Three KV stages fit when P^T can live in the rope block of its own stage
   // (QK has consumed that block before P is written): NR = 16.  Otherwise two
@@ -98,7 +98,8 @@ struct Cfg {
   static constexpr uint32_t kBars = kAux;               // 17 x 8 B
   static constexpr uint32_t kTmemSlot = kAux + 136;     // 4 B
   static constexpr uint32_t kFlags = kAux + 144;        // 3 x 4 B
-  static constexpr uint32_t kRedMax = kAux + 160;       // 4 x NR floats
+  static constexpr uint32_t kStageInfo = kAux + 160;    // NST x 4 B: rows loaded per page
+  static constexpr uint32_t kRedMax = kAux + 176;       // 4 x NR floats
   // Row owner r reads red_max[.][r] before writing alpha[r]: alpha reuses
   // red_max's first row.
   static constexpr uint32_t kAlpha = kRedMax;           // NR floats
@@ -112,7 +113,11 @@ struct Cfg {
 };
 
 
-template <int NR>
+// kGather: the variant for restricted key sets (key windows, selected pages):
+// tiles may have pages that are not loaded, and every score is masked by its
+// key position.  The plain variant (kGather = false) covers full key ranges,
+// with or without ragged query counts.
+template <int NR, bool kGather>
 __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     mla_split_kv_kernel(const __grid_constant__ CUtensorMap tm_kv_lat,
                         const __grid_constant__ CUtensorMap tm_kv_rope,
@@ -132,11 +137,17 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
   const int nsplit = p.splits[b];
   const int chunk = p.chunks[b];
   if (split >= nsplit) return;  // empty split slot of a shorter request
+  // With selected pages the split plan covers the compact range of the
+  // selection (32 * topk tokens); otherwise the key positions [0, L).
+  const bool sparse = kGather && p.block_idx != nullptr;
+  const int Lspace = sparse ? p.topk * MLA_PAGE_SIZE : L;
+  const int q_b = p.query_lens ? p.query_lens[b] : p.q_len;  // this request's query tokens
   {
-    const bool bad = L < 1 || (p.causal && L < p.q_len) || nsplit > p.max_splits ||
-                     chunk < kTileTokens || (chunk % kTileTokens) != 0 ||
-                     static_cast<int64_t>(nsplit) * chunk < L ||
-                     static_cast<int64_t>(nsplit - 1) * chunk >= L ||
+    const bool bad = L < 1 || q_b < 1 || q_b > p.q_len || (p.causal && L < q_b) ||
+                     nsplit > p.max_splits || chunk < kTileTokens ||
+                     (chunk % kTileTokens) != 0 ||
+                     static_cast<int64_t>(nsplit) * chunk < Lspace ||
+                     static_cast<int64_t>(nsplit - 1) * chunk >= Lspace ||
                      static_cast<int64_t>(L) > static_cast<int64_t>(p.max_pages) * MLA_PAGE_SIZE;
     if (bad) {
       if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
@@ -144,8 +155,23 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     }
   }
   const int tok_begin = split * chunk;
-  const int tok_end = min(L, tok_begin + chunk);
-  const int n_tiles = (tok_end - tok_begin + kTileTokens - 1) / kTileTokens;
+  int tok_end = min(Lspace, tok_begin + chunk);
+  // Key window in positions ([0, L) without one).
+  int win_lo = 0, win_hi = L;
+  if (kGather && p.kv_bounds) {
+    win_lo = max(0, p.kv_bounds[2 * b]);
+    win_hi = min(L, p.kv_bounds[2 * b + 1]);
+  }
+  // First tile of the split: whole tiles below a dense window are skipped
+  // (tiles stay aligned to the split start, so pages stay whole).
+  int t0 = tok_begin;
+  if (kGather && !sparse) {
+    tok_end = min(tok_end, win_hi);
+    if (win_lo >= tok_end)
+      t0 = tok_end;  // nothing of the window in this split
+    else if (win_lo > tok_begin)
+      t0 = tok_begin + (win_lo - tok_begin) / kTileTokens * kTileTokens;
+  }
   float c_log2 = p.c_log2, kv_scale = p.kv_scale;
   if (p.q_scale_dev || p.kv_scale_dev || p.sm_scale_dev) {
     const float qs = p.q_scale_dev ? *p.q_scale_dev : p.q_scale_h;
@@ -155,6 +181,11 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
   }
   const int row0 = grp * p.rows_per_group;                       // first row of this group
   const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
+  // Rows of real query tokens (the others are padding slots of a shorter
+  // query block: no key is visible to them).
+  const int rows_valid = max(0, min(rows_here, q_b * p.num_heads - row0));
+  const int n_tiles =
+      (rows_valid > 0 && tok_end > t0) ? (tok_end - t0 + kTileTokens - 1) / kTileTokens : 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -217,30 +248,64 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     }
     const uint64_t pol = l2_policy_evict_first();
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-    const int page0 = tok_begin / MLA_PAGE_SIZE;
+    const int page0 = t0 / MLA_PAGE_SIZE;
     const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
     // Page ids of 8 tiles (32 pages) per window, one per lane; the next
-    // window is fetched a window ahead so its latency is hidden.
-    auto load_window = [&](int w) -> int {
+    // window is fetched a window ahead so its latency is hidden.  kGather
+    // also keeps, per page, the number of its rows to load (0: not loaded):
+    // compact page cp maps to logical page lp (cp itself, or the selection's
+    // entry), which is loaded when it holds keys inside the window and before
+    // the end of the split (dense) or of the request (selection).
+    int last_lp = -1;  // selection: the entry before this window (order check)
+    auto load_window = [&](int w, int& nv_out) -> int {
       const int pi = page0 + w * 32 + lane;
       int pg = 0;
-      if (pi < page_end) {
-        pg = pt[pi];
-        if (pg < 0 || pg >= p.num_pages) {
-          report(p.status, MLA_ERR_INVALID_ARG);
-          pg = 0;
+      nv_out = 0;
+      if constexpr (!kGather) {
+        if (pi < page_end) {
+          pg = pt[pi];
+          if (pg < 0 || pg >= p.num_pages) {
+            report(p.status, MLA_ERR_INVALID_ARG);
+            pg = 0;
+          }
+        }
+      } else {
+        int lp = -1;
+        if (pi < page_end) {
+          lp = pi;
+          if (sparse) lp = (pi < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + pi] : -1;
+        }
+        if (sparse) {
+          // Selected pages must be listed in increasing order, each once.
+          int prev = __shfl_up_sync(0xffffffffu, lp, 1);
+          if (lane == 0) prev = last_lp;
+          if (lp >= 0 && prev >= 0 && lp <= prev) report(p.status, MLA_ERR_INVALID_ARG);
+          last_lp = __shfl_sync(0xffffffffu, lp, 31);
+        }
+        const int64_t end_pos = sparse ? win_hi : tok_end;
+        const int64_t first = static_cast<int64_t>(lp) * MLA_PAGE_SIZE;
+        if (lp >= 0 && first < end_pos && first + MLA_PAGE_SIZE > win_lo) {
+          pg = pt[lp];
+          if (pg < 0 || pg >= p.num_pages) {
+            report(p.status, MLA_ERR_INVALID_ARG);
+            pg = 0;
+          }
+          nv_out = static_cast<int>(end_pos - first < MLA_PAGE_SIZE ? end_pos - first : MLA_PAGE_SIZE);
         }
       }
       return pg;
     };
-    int window = load_window(0);
-    int window_next = load_window(1);
+    int window_nv, window_next_nv;
+    int window = load_window(0, window_nv);
+    int window_next = load_window(1, window_next_nv);
+    volatile uint32_t* stage_info = reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo);
     int issued = 0;
     int st = 0, round = 0;
     for (int i = 0; i < n_tiles; ++i) {
       if (i > 0 && (i & 7) == 0) {
         window = window_next;
-        window_next = load_window((i >> 3) + 1);
+        window_nv = window_next_nv;
+        window_next = load_window((i >> 3) + 1, window_next_nv);
       }
       bool ok = true;
       if (round > 0) ok = mbar_wait(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles);
@@ -253,18 +318,33 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         break;
       }
       // Lane q (< 4) takes the id of the tile's page q.
-      const int my_page = __shfl_sync(0xffffffffu, window, (i & 7) * 4 + (lane & 3));
+      const int src = (i & 7) * 4 + (lane & 3);
+      const int my_page = __shfl_sync(0xffffffffu, window, src);
       const int tp0 = page0 + i * 4;
+      bool my_load;
+      uint32_t info = 0;
+      if constexpr (kGather) {
+        // Rows to load of pages 0-3, one byte each, for the MMA warp (which
+        // zeroes the rest); published by the arrive below.
+        const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
+        my_load = my_nv > 0;
+        const int n1 = __shfl_sync(0xffffffffu, my_nv, 1);
+        const int n2 = __shfl_sync(0xffffffffu, my_nv, 2);
+        const int n3 = __shfl_sync(0xffffffffu, my_nv, 3);
+        info = static_cast<uint32_t>(my_nv) | (static_cast<uint32_t>(n1) << 8) |
+               (static_cast<uint32_t>(n2) << 16) | (static_cast<uint32_t>(n3) << 24);
+      } else {
+        my_load = tp0 + (lane & 3) < page_end;
+      }
+      const int nload = __popc(__ballot_sync(0xffffffffu, lane < 4 && my_load));
       const uint32_t fb = bar(BAR_FULL0 + st);
       if (lane == 0) {
-        int nvalid = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) nvalid += (tp0 + q < page_end) ? 1 : 0;
-        mbar_arrive_expect_tx(fb, nvalid * kPageBytes);
+        if constexpr (kGather) stage_info[st] = info;
+        mbar_arrive_expect_tx(fb, nload * kPageBytes);
       }
       __syncwarp();
       // Lanes 0-3 issue one page each (5 boxes: 4 latent blocks + rope).
-      if (lane < 4 && tp0 + lane < page_end) {
+      if (lane < 4 && my_load) {
         const uint32_t kv = sbase + C::kKV + st * kTileBytes;
         const int row = my_page * MLA_PAGE_SIZE;
 #pragma unroll
@@ -377,17 +457,15 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         if (++pv_st == C::NST) pv_st = 0;
         t_last = clock64();
       } else if (action == 2) {
-        const int tile_tok0 = tok_begin + qk * kTileTokens;
-        const int valid = tok_end - tile_tok0;  // tokens of this tile inside the split
-        if (valid < kTileTokens) {
-          // Rows past the split's end: pages that were not loaded, or the tail
-          // of a request's last page.  Zero them so V holds no stale or NaN
-          // bytes (0 * NaN would poison the PV sum).
-          const int nrow = kTileTokens - valid;
-          uint8_t* kvp = base + C::kKV + qk_st * kTileBytes;
-          const uint4 z = make_uint4(0, 0, 0, 0);
+        // Rows that hold no loaded key: pages that were not loaded (past the
+        // split's end, outside a window or an unused selection slot) and the
+        // tail of a request's last page.  Zero them so V holds no stale or NaN
+        // bytes (0 * NaN would poison the PV sum).
+        uint8_t* kvp = base + C::kKV + qk_st * kTileBytes;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        auto zero_rows = [&](int r0, int nrow) {
           for (int idx = lane; idx < nrow * 36; idx += 32) {
-            const int r = valid + idx / 36;
+            const int r = r0 + idx / 36;
             const int c = idx % 36;
             uint4* dst;
             if (c < 32)
@@ -396,8 +474,30 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
               dst = reinterpret_cast<uint4*>(kvp + kRopeOffset + r * 64 + (c - 32) * 16);
             *dst = z;
           }
-          fence_proxy_async_smem();
-          __syncwarp();
+        };
+        if constexpr (kGather) {
+          // Rows loaded per page, as the producer published them with the
+          // stage's full barrier (which lane 0 has just observed).
+          uint32_t info = 0;
+          if (lane == 0) info = *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * qk_st);
+          info = __shfl_sync(0xffffffffu, info, 0);
+          if (info != 0x20202020u) {
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+              const int nv = static_cast<int>((info >> (8 * q)) & 0xFFu);
+              if (nv < MLA_PAGE_SIZE) zero_rows(q * MLA_PAGE_SIZE + nv, MLA_PAGE_SIZE - nv);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        } else {
+          const int tile_tok0 = t0 + qk * kTileTokens;
+          const int valid = tok_end - tile_tok0;  // tokens of this tile inside the split
+          if (valid < kTileTokens) {
+            zero_rows(valid, kTileTokens - valid);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
         }
         if (lane == 0) issue_qk(qk_st, (C::NS == 2) ? (qk & 1) : 0);
         __syncwarp();
@@ -444,9 +544,20 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     // Smallest visibility limit over this group's rows (MTP verify: the first
     // query token of the block sees the fewest keys).
     const int qi_first = row0 / p.num_heads;
-    const int lim_min = p.causal ? min(tok_end, L - p.q_len + qi_first + 1) : tok_end;
+    const int lim_min = p.causal ? min(tok_end, L - q_b + qi_first + 1) : tok_end;
     const int my_row0 = row0 + rbase;  // first request row of this warpgroup
-    const int my_rows = max(0, min(NRH, rows_here - rbase));
+    const int my_rows = max(0, min(NRH, rows_valid - rbase));
+    // Selection: logical page ids of 8 tiles' compact pages, one per lane
+    // (this warp's token page is page `quad` of its tile).
+    auto sel_window = [&](int w) -> int {
+      const int cp = t0 / MLA_PAGE_SIZE + w * 32 + lane;
+      return (cp < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + cp] : -1;
+    };
+    int sel_cur = -1, sel_next = -1;
+    if (sparse) {
+      sel_cur = sel_window(0);
+      sel_next = sel_window(1);
+    }
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
       const int sb = i & 1;
@@ -470,11 +581,36 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
       }
-      const int tile_tok0 = tok_begin + i * kTileTokens;
+      const int tile_tok0 = t0 + i * kTileTokens;
       const int j = tile_tok0 + tok_lane;
-      // Scale and mask: rows past rows_here, tokens past the split, and (MTP
-      // verify) tokens after the row's query position are -inf.
-      if (tile_tok0 + kTileTokens <= lim_min) {
+      // Scale and mask: rows past the real query rows, tokens past the split,
+      // and (MTP verify) tokens after the row's query position are -inf.
+      if constexpr (kGather) {
+        // Restricted key sets: the token's key position decides.
+        int64_t pos = j;
+        bool tok_ok = j < tok_end;
+        if (sparse) {
+          if (i > 0 && (i & 7) == 0) {
+            sel_cur = sel_next;
+            sel_next = sel_window((i >> 3) + 1);
+          }
+          const int lp = __shfl_sync(0xffffffffu, sel_cur, (i & 7) * 4 + quad);
+          pos = static_cast<int64_t>(lp) * MLA_PAGE_SIZE + lane;
+          tok_ok = tok_ok && lp >= 0;
+        }
+        tok_ok = tok_ok && pos >= win_lo && pos < win_hi;
+        int qi = my_row0 / p.num_heads;
+        int h = my_row0 - qi * p.num_heads;
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) {
+          const bool vis = tok_ok && k < my_rows && (!p.causal || pos < L - q_b + qi + 1);
+          t[k] = vis ? t[k] * c : -INFINITY;
+          if (++h == p.num_heads) {
+            h = 0;
+            ++qi;
+          }
+        }
+      } else if (tile_tok0 + kTileTokens <= lim_min) {
 #pragma unroll
         for (int k = 0; k < NRH; ++k) t[k] = (k < my_rows) ? t[k] * c : -INFINITY;
       } else {
@@ -482,7 +618,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         int h = my_row0 - qi * p.num_heads;
 #pragma unroll
         for (int k = 0; k < NRH; ++k) {
-          const int lim = p.causal ? min(tok_end, L - p.q_len + qi + 1) : tok_end;
+          const int lim = p.causal ? min(tok_end, L - q_b + qi + 1) : tok_end;
           t[k] = (k < my_rows && j < lim) ? t[k] * c : -INFINITY;
           if (++h == p.num_heads) {
             h = 0;
@@ -673,6 +809,19 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           }
         }
       }
+    } else if (ok && fin && n_tiles == 0 && single) {
+      // No key of this split is visible to any row here (padding query slots,
+      // an empty window or selection): O = 0.  Partials need only (-inf, 0),
+      // written above; the merge gives such slots weight 0 without reading O.
+#pragma unroll 1
+      for (int d = 0; d < 4; ++d) {
+        const int dim = d * 128 + tok_lane;
+        for (int row = rbase; row < min(rows_here, rbase + NRH); ++row) {
+          const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
+          p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(0.0f);
+          if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = 0.0f;
+        }
+      }
     }
   }
   tc_fence_before();
@@ -816,13 +965,13 @@ static bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t bo
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NR>
+template <int NR, bool kGather>
 static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages, int batch,
                                 int groups, const DecodeParams& prm, cudaStream_t stream) {
   using C = Cfg<NR>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_kernel<NR>,
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_kernel<NR, kGather>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
@@ -837,7 +986,7 @@ static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages
       !make_map(&q_rope, q, q_rows, 64, NR, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   dim3 grid(prm.max_splits * groups, batch);
-  mla_split_kv_kernel<NR><<<grid, C::kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
+  mla_split_kv_kernel<NR, kGather><<<grid, C::kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
                                                                      q_rope, prm);
   return cudaGetLastError();
 }
@@ -985,6 +1134,10 @@ static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
   prm.sm_scale_h = softmax_scale;
   prm.output_scale = 1.0f;
   prm.sinks = nullptr;
+  prm.query_lens = nullptr;
+  prm.kv_bounds = nullptr;
+  prm.block_idx = nullptr;
+  prm.topk = 0;
   {
     const long long w = g_wait_cycles.load();
     prm.wait_cycles = w > 0 ? w : kWaitLimitCycles;
@@ -1016,10 +1169,21 @@ static int launch_decode_split(const void* q_fp8, const void* kv_pages_fp8, int6
                                const DecodeLaunch& dl, cudaStream_t st) {
   cudaError_t e;
   const int b = dl.batch, g = dl.rg.groups;
+  // Key windows and page selections take the masked-position variant.
+  const bool gather = dl.prm.kv_bounds != nullptr || dl.prm.block_idx != nullptr;
   switch (dl.rg.nr) {
-    case 16: e = launch_split<16>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
-    case 32: e = launch_split<32>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
-    case 48: e = launch_split<48>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st); break;
+    case 16:
+      e = gather ? launch_split<16, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st)
+                 : launch_split<16, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st);
+      break;
+    case 32:
+      e = gather ? launch_split<32, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st)
+                 : launch_split<32, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st);
+      break;
+    case 48:
+      e = gather ? launch_split<48, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st)
+                 : launch_split<48, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st);
+      break;
     default:
       set_error("mla_decode: internal row grouping error");
       return MLA_ERR_UNSUPPORTED;
@@ -1079,6 +1243,52 @@ extern "C" int mla_decode_ex(const void* q_fp8, const void* kv_pages_fp8, int64_
     dl.prm.sm_scale_dev = options->softmax_scale_dev;
     dl.prm.output_scale = options->output_scale;
     dl.prm.sinks = options->sinks;
+    dl.prm.query_lens = options->query_lens;
+    dl.prm.kv_bounds = options->kv_bounds;
+    dl.mp.output_scale = options->output_scale;
+    dl.mp.sinks = options->sinks;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
+  if (rc != MLA_OK) return rc;
+  return launch_decode_merge(dl, st);
+}
+
+extern "C" int mla_decode_sparse(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                                 const int32_t* page_table, int32_t max_pages_per_req,
+                                 const int32_t* kv_lens, const int32_t* block_idx, int32_t topk,
+                                 const int32_t* splits, const int32_t* chunks, int32_t max_splits,
+                                 int32_t kv_split, int32_t batch, int32_t q_len,
+                                 int32_t num_heads, int32_t causal, float q_scale,
+                                 float kv_scale, float softmax_scale, void* workspace,
+                                 size_t workspace_bytes, void* out_bf16, float* lse_f32,
+                                 float* out_f32_debug, const mla_decode_options_t* options,
+                                 void* stream) {
+  if (!block_idx) {
+    set_error("mla_decode_sparse: null block_idx");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (topk < 1 || static_cast<int64_t>(topk) * MLA_PAGE_SIZE > INT32_MAX / 2) {
+    set_error("mla_decode_sparse: topk must be >= 1 and 32 * topk must fit in int32");
+    return MLA_ERR_INVALID_ARG;
+  }
+  DecodeLaunch dl;
+  int rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode_sparse", &dl);
+  if (rc != MLA_OK) return rc;
+  dl.prm.block_idx = block_idx;
+  dl.prm.topk = topk;
+  if (options) {
+    if (!std::isfinite(options->output_scale)) {
+      set_error("mla_decode_sparse: output_scale must be finite");
+      return MLA_ERR_INVALID_ARG;
+    }
+    dl.prm.q_scale_dev = options->q_scale_dev;
+    dl.prm.kv_scale_dev = options->kv_scale_dev;
+    dl.prm.sm_scale_dev = options->softmax_scale_dev;
+    dl.prm.output_scale = options->output_scale;
+    dl.prm.sinks = options->sinks;
+    dl.prm.query_lens = options->query_lens;
+    dl.prm.kv_bounds = options->kv_bounds;
     dl.mp.output_scale = options->output_scale;
     dl.mp.sinks = options->sinks;
   }

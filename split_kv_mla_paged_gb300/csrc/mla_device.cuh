@@ -43,6 +43,14 @@ struct DecodeParams {
   float sm_scale_h;
   float output_scale;      // multiplies O (not the LSE)
   const float* sinks;      // optional per-head sink logits (natural-log units)
+  // Restrictions of the visible keys (NULL = none): per-request query-token
+  // counts in the padded q_len slots, key windows [lo, hi) (int32 [B][2]) and
+  // selected logical pages (int32 [B][topk], ascending, negative = unused; the
+  // split plan then covers the compact range of 32 * topk tokens).
+  const int32_t* query_lens;
+  const int32_t* kv_bounds;
+  const int32_t* block_idx;
+  int32_t topk;
   long long wait_cycles;   // limit of the pipeline waits (drains always use the long limit)
   int* status;
   float* ws_ml;
