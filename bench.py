@@ -32,15 +32,21 @@ DEFAULT_WORKLOAD = "long_h12_q1_l1m_b16"
 # kernel before #19338, on an unspecified Blackwell SM10x GPU): context only.
 PUBLISHED_US = {"long_h12_q1_l1m_b16": 1095.5}
 L2_ROTATE_BYTES = 2 * 126 * 1024 * 1024  # rotate inputs below 2x the 126 MB L2
-KERNEL_SOURCES = ["split_kv_mla_paged_gb300/csrc/mla_decode.cu",
-                  "split_kv_mla_paged_gb300/csrc/mla_decode_bf16.cu",
-                  "split_kv_mla_paged_gb300/csrc/mla_device.cuh",
-                  "split_kv_mla_paged_gb300/csrc/sm103_ptx.cuh"]
+# Sources of the split-KV kernel a workload runs (recorded ncu traffic is
+# valid only for the source it was taken on).
+_COMMON_SOURCES = ["split_kv_mla_paged_gb300/csrc/mla_device.cuh",
+                   "split_kv_mla_paged_gb300/csrc/mla_internal.h",
+                   "split_kv_mla_paged_gb300/csrc/sm103_ptx.cuh"]
+KERNEL_SOURCES = {
+    "e4m3": ["split_kv_mla_paged_gb300/csrc/mla_decode.cu"] + _COMMON_SOURCES,
+    "bf16": ["split_kv_mla_paged_gb300/csrc/mla_decode_bf16.cu",
+             "split_kv_mla_paged_gb300/csrc/mla_decode.cu"] + _COMMON_SOURCES,
+}
 
 
-def kernel_hash() -> str:
+def kernel_hash(dtype: str = "e4m3") -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[dtype]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -64,7 +70,9 @@ def recorded_traffic(workload: str):
     with open(path) as f:
         d = json.load(f)
     entry = d.get(workload)
-    if not entry or entry.get("kernel_sha") != kernel_hash():
+    from synth import WORKLOADS
+    dtype = WORKLOADS.get(workload, {}).get("dtype", "e4m3")
+    if not entry or entry.get("kernel_sha") != kernel_hash(dtype):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -146,10 +154,23 @@ def dist_env():
     return world, rank, local
 
 
-def cpu_oracle_sample(inp, w, rows_per_sample: int, softmax_scale: float, tokens: int = 0):
+def selected_keys(sel_row, L: int, n_tok: int) -> int:
+    """Keys of the selected pages (one request's block_idx row) below n_tok."""
+    n = 0
+    for p in sel_row:
+        p = int(p)
+        if p >= 0:
+            n += max(0, min(32, min(L, n_tok) - 32 * p))
+    return n
+
+
+def cpu_oracle_sample(inp, w, rows_per_sample: int, softmax_scale: float, tokens: int = 0,
+                      selection=None):
     """Time the oracle on the first `rows_per_sample` rows, each over its first
-    `tokens` keys (0 = the full KV length).  Returns (seconds, row-tokens done,
-    threads); the work per (row, key) is uniform, so time scales by row-tokens."""
+    `tokens` keys (0 = the full KV length; with a page selection `selection`
+    [B, topk], only the selected keys among them).  Returns (seconds, row-keys
+    done, threads); the work per (row, key) is uniform, so time scales by
+    row-keys."""
     import numpy as np
     import torch
     import oracle
@@ -174,11 +195,13 @@ def cpu_oracle_sample(inp, w, rows_per_sample: int, softmax_scale: float, tokens
     threads = oracle.max_threads()
     t0 = time.perf_counter()
     done = 0
-    for q_b, kv_b, table, lens, sel, n_tok in batches:
+    for b, (q_b, kv_b, table, lens, rsel, n_tok) in enumerate(batches):
+        blk = None if selection is None else selection[b:b + 1]
         oracle.decode_rows(q_b, kv_b, table, lens, q_len=q_len, num_heads=H, causal=w["causal"],
-                           softmax_scale=softmax_scale, rows=sel, tok_begin=0,
-                           tok_end=n_tok if n_tok < int(lens[0]) else -1)
-        done += len(sel) * n_tok
+                           softmax_scale=softmax_scale, rows=rsel, tok_begin=0,
+                           tok_end=n_tok if n_tok < int(lens[0]) else -1, block_idx=blk)
+        keys = n_tok if selection is None else selected_keys(selection[b], int(lens[0]), n_tok)
+        done += len(rsel) * keys
     return time.perf_counter() - t0, done, threads
 
 
@@ -198,27 +221,39 @@ def run_reference(args, w, world, rank):
         inp = decode_inputs(1, w["num_heads"], w["q_len"], w["kv_lens"][:1], w["seed"])
     else:
         inp = workload_inputs(args.workload, device=dev)
-    total_row_tokens = sum(int(L) for L in w["kv_lens"]) * w["num_heads"] * w["q_len"]
+    sel = None
+    if w.get("topk"):
+        from synth import page_selection
+        sel = page_selection(w["kv_lens"], w["topk"], seed=w["seed"] + 100)
+        total_row_tokens = (sum(selected_keys(sel[b], int(L), int(L))
+                                for b, L in enumerate(w["kv_lens"]))
+                            * w["num_heads"] * w["q_len"])
+    else:
+        total_row_tokens = sum(int(L) for L in w["kv_lens"]) * w["num_heads"] * w["q_len"]
     threads = oracle.max_threads()
     rows = min(threads, w["num_heads"] * w["q_len"])
     L0 = int(w["kv_lens"][0])
     cal_tokens = min(L0, 16384)
-    t_cal, _, _ = cpu_oracle_sample(inp, w, rows, SOFTMAX_SCALE, tokens=cal_tokens)
+    t_cal, _, _ = cpu_oracle_sample(inp, w, rows, SOFTMAX_SCALE, tokens=cal_tokens,
+                                    selection=sel)
     per_step = args.ref_budget_s / (args.steps + args.warmup)
     tokens = int(max(1024, min(L0, cal_tokens * per_step / max(t_cal, 1e-6))))
     times = []
     for k in range(args.warmup + args.steps):
-        t, done, threads = cpu_oracle_sample(inp, w, rows, SOFTMAX_SCALE, tokens=tokens)
+        t, done, threads = cpu_oracle_sample(inp, w, rows, SOFTMAX_SCALE, tokens=tokens,
+                                             selection=sel)
         if k >= args.warmup:
             times.append(t / done * total_row_tokens * 1e6)
     value = statistics.mean(times)
-    sample = (f"{rows} rows of request 0 over their first {tokens} of {L0} keys per step; "
+    sample = (f"{rows} rows of request 0 over their first {tokens} of {L0} keys per step"
+              f"{' (selected pages only)' if sel is not None else ''}; "
               f"time scaled by row-keys to the whole call")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,0.5^2) cast to E4M3)",
+        "data": ("synthetic (seeded N(0,0.5^2) cast to "
+                 f"{'BF16' if w.get('dtype') == 'bf16' else 'E4M3'})"),
         "config": {"workload": args.workload, "batch": w["batch"], "num_heads": w["num_heads"],
                    "q_len": w["q_len"], "kv_len": w["kv_lens"][0], "causal": w["causal"],
                    "parallelism": "replicas" if world > 1 else "single"},
@@ -279,11 +314,15 @@ def main():
     inp = workload_inputs(args.workload, device=dev)
     B, H, q_len = inp.batch, inp.num_heads, inp.q_len
     lens = inp.kv_lens.tolist()
+    topk = w.get("topk")
+    is_sparse = topk is not None
+    # A sparse decode is planned over the compact range of its selection.
+    plan_lens = [32 * topk] * B if is_sparse else lens
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     if args.plan == "pages" and w["target"] is not None:
-        plan = mla.mla_decode_plan(lens, H, q_len, target_ctas=w["target"])
+        plan = mla.mla_decode_plan(plan_lens, H, q_len, target_ctas=w["target"])
     else:
-        plan = mla.mla_decode_plan(lens, H, q_len, sm_count=sm_count)
+        plan = mla.mla_decode_plan(plan_lens, H, q_len, sm_count=sm_count)
     ws_bytes = mla.mla_decode_workspace_size(B, q_len, H, plan.max_splits)
     lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
     splits_d = torch.from_numpy(plan.splits).to(dev)
@@ -291,19 +330,33 @@ def main():
     # Inputs larger than L2 need no flush.  Smaller ones rotate over enough
     # distinct seeded pools (with their own workspaces and outputs) that
     # consecutive steps never find their KV in L2.
-    kv_bytes = inp.kv_bytes()
-    n_pools = 1 if kv_bytes >= L2_ROTATE_BYTES else min(64, -(-L2_ROTATE_BYTES // kv_bytes))
-    pools = [inp] + [workload_inputs(args.workload, device=dev, seed_offset=k)
-                     for k in range(1, n_pools)]
+    sels = []
+    if is_sparse:
+        # One KV pool; the steps rotate over distinct page selections of it, so
+        # consecutive steps read different pages (L2 is cold for each).
+        from synth import page_selection
+        sel0 = page_selection(lens, topk, seed=w["seed"] + 100)
+        kv_bytes = sum(selected_keys(sel0[b], L, L) for b, L in enumerate(lens)) * 576
+        n_pools = 1 if kv_bytes >= L2_ROTATE_BYTES else min(64, -(-L2_ROTATE_BYTES // kv_bytes))
+        sels = [torch.from_numpy(sel0).to(dev)] + [
+            torch.from_numpy(page_selection(lens, topk, seed=w["seed"] + 100 + k)).to(dev)
+            for k in range(1, n_pools)]
+        pools = [inp] * n_pools
+    else:
+        kv_bytes = inp.kv_bytes()
+        n_pools = 1 if kv_bytes >= L2_ROTATE_BYTES else min(64, -(-L2_ROTATE_BYTES // kv_bytes))
+        pools = [inp] + [workload_inputs(args.workload, device=dev, seed_offset=k)
+                         for k in range(1, n_pools)]
     calls = []
-    for pool in pools:
+    for k, pool in enumerate(pools):
         ws_k = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         mla.mla_decode_workspace_init(ws_k, ws_bytes)
         out_k = torch.empty((B, q_len, H, 512), dtype=torch.bfloat16, device=dev)
         lse_k = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
         calls.append((pool.q, pool.kv, pool.num_pages, pool.page_table, pool.max_pages, lens_d,
                       splits_d, chunks_d, plan.max_splits, plan.kv_split, B, q_len, H,
-                      w["causal"], 1.0, 1.0, SOFTMAX_SCALE, ws_k, ws_bytes, out_k, lse_k, None))
+                      w["causal"], 1.0, 1.0, SOFTMAX_SCALE, ws_k, ws_bytes, out_k, lse_k, None)
+                     + ((sels[k],) if is_sparse else ()))
     args_common = calls[0]
     ws, out, lse = args_common[17], args_common[19], args_common[20]
     stream = torch.cuda.Stream(dev)
@@ -311,18 +364,28 @@ def main():
     is_bf16 = inp.q.dtype == torch.bfloat16
 
     def decode_call(*a):
-        # a = one call's arguments followed by the stream
-        if is_bf16:  # BF16 Q and KV: no q/kv scales
-            mla.mla_decode_bf16(*a[:14], *a[16:])
+        # a = one call's 22 arguments (+ the page selection), then the stream
+        c, s = a[:-1], a[-1]
+        if is_sparse:
+            mla.mla_decode_sparse(*c[:6], c[22], topk, *c[6:22], stream=s)
+        elif is_bf16:  # BF16 Q and KV: no q/kv scales
+            mla.mla_decode_bf16(*c[:14], *c[16:22], s)
         else:
-            mla.mla_decode(*a)
+            mla.mla_decode(*c[:22], s)
 
-    # The BF16 entry point has no separate phases: its "split" graph is the
-    # whole call (an upper bound on the split kernel's time), and its merge is
-    # the shared merge kernel, launched on the same workspace and plan.
-    phases = (("full", decode_call),
-              ("split", decode_call if is_bf16 else mla.mla_decode_splitkv),
-              ("merge", mla.mla_decode_merge))
+    def split_call(*a):
+        if is_bf16 or is_sparse:
+            decode_call(*a)
+        else:
+            mla.mla_decode_splitkv(*a[:22], a[-1])
+
+    def merge_call(*a):
+        mla.mla_decode_merge(*a[:22], a[-1])
+
+    # The BF16 and sparse entry points have no separate phases: their "split"
+    # graph is the whole call (an upper bound on the split kernel's time), and
+    # the merge is the shared merge kernel on the same workspace and plan.
+    phases = (("full", decode_call), ("split", split_call), ("merge", merge_call))
 
     with torch.cuda.stream(stream):
         for k in range(args.warmup):
@@ -382,14 +445,22 @@ def main():
     e2e_args[0], e2e_args[3] = q_d, pt_d
     e2e_args[5], e2e_args[6], e2e_args[7] = meta_d[0], meta_d[1], meta_d[2]
     h2d = q_h.numel() * q_h.element_size() + pt_h.numel() * 4 + meta_h.numel() * 4
+    if is_sparse:
+        sel_h = sels[0].cpu().pin_memory()
+        sel_d = torch.empty_like(sels[0])
+        e2e_args[22] = sel_d
+        h2d += sel_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
     def e2e_step():
-        p = mla.mla_decode_plan(lens, H, q_len, sm_count=sm_count) if args.plan == "gb300" else plan
+        p = (mla.mla_decode_plan(plan_lens, H, q_len, sm_count=sm_count)
+             if args.plan == "gb300" else plan)
         del p
         q_d.copy_(q_h, non_blocking=True)
         pt_d.copy_(pt_h, non_blocking=True)
         meta_d.copy_(meta_h, non_blocking=True)
+        if is_sparse:
+            sel_d.copy_(sel_h, non_blocking=True)
         decode_call(*e2e_args, stream)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
@@ -412,8 +483,10 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_rows > 0:
-        t, done, threads = cpu_oracle_sample(inp, w, args.cpu_rows, SOFTMAX_SCALE)
-        total = sum(lens) * H * q_len
+        sel_np = sels[0].cpu().numpy() if is_sparse else None
+        t, done, threads = cpu_oracle_sample(inp, w, args.cpu_rows, SOFTMAX_SCALE,
+                                             selection=sel_np)
+        total = kv_bytes // (576 * inp.kv.element_size()) * H * q_len  # row-keys
         cpu = {"value": t / done * total * 1e6, "unit": UNIT, "cores": threads,
                "kind": "oracle",
                "sample": f"first {args.cpu_rows} of {inp.rows} rows over their full KV length "

@@ -260,6 +260,12 @@ for _q in (1, 8):
          causal=(_q > 1), target=None, seed=5, dtype="bf16")
 _add("bf16_h12_q1_l1m_b16", batch=16, num_heads=12, q_len=1, kv_lens=[1048576] * 16,
      causal=False, target=None, seed=5, dtype="bf16")
+# Sparse decode over selected pages: 256 pages (8192 keys) of each 1M-key
+# request, picked by a seeded stand-in for the block selector (the last page
+# always included).
+for _q in (1, 8):
+    _add(f"sparse_h12_q{_q}_l1m_b16_top256", batch=16, num_heads=12, q_len=_q,
+         kv_lens=[1048576] * 16, causal=(_q > 1), target=None, seed=6, topk=256)
 
 
 def workload_inputs(name: str, device: str | torch.device = "cpu",
