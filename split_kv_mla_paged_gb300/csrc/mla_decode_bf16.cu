@@ -53,6 +53,31 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// tcgen05.mma kind::f16 with the A operand in TMEM (lane = row, two 16-bit
+// elements per 32-bit column, element 2c in the low half; K = 16 elements =
+// 8 columns per instruction).
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32"
+      " [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // a in the low half
   return *reinterpret_cast<uint32_t*>(&v);
@@ -572,6 +597,503 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Row groups of at most 16 rows (H12 q1, the common BF16 case): Q lives in
+// TMEM as the A operand of a non-swapped QK, which frees the shared memory
+// for three KV stages.
+//  * TMEM: Q [128 lanes x 288 columns] (lane l holds row l % 16: eight copies
+//    of the 16 rows, two BF16 values per column, element 2c in the low half),
+//    S [128 x 64 tokens] x 2 buffers, O^T [128 dims x 16 rows] x 4 blocks.
+//  * QK: S = Q K^T, M = 128 (the row copies), N = 64 tokens, K = 16 per
+//    instruction, B = the K tile (K-major, 128-byte swizzle), 36 per tile.
+//  * Softmax: thread (lane l of warp w) takes row l % 16 and the eight tokens
+//    8 (2w + l / 16) .. +7, so all 128 threads work on distinct scores.
+//  * P^T goes K-major (a row's 64 tokens = one 128-byte swizzled line) into
+//    the consumed rope block; PV is the swapped O^T += V^T P^T as before.
+// ---------------------------------------------------------------------------
+namespace q16 {
+constexpr int NR = 16;
+constexpr int NST = 3;
+constexpr int kThreads = 64 + 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kQCol = 0;      // 288 columns
+constexpr uint32_t kSCol = 288;    // 2 x 64 columns
+constexpr uint32_t kOCol = 416;    // 4 x 16 columns
+constexpr uint32_t kQStage = (NST - 1) * kTileBytesB;  // Q staged by TMA in the last stage
+constexpr uint32_t kAux = NST * kTileBytesB;
+constexpr uint32_t kBars = kAux;               // 17 x 8 B
+constexpr uint32_t kTmemSlot = kAux + 136;
+constexpr uint32_t kFlags = kAux + 144;
+constexpr uint32_t kRedMax = kAux + 160;       // 4 warps x 16 rows
+constexpr uint32_t kRedSum = kRedMax + 256;    // 2 x 4 x 16
+constexpr uint32_t kKref = kRedSum + 512;      // 16
+constexpr uint32_t kAlpha = kKref + 64;        // 16
+constexpr uint32_t kEnd = kAlpha + 64;
+constexpr uint32_t kSmemBytes = kEnd + 1024;
+static_assert(kSmemBytes <= 232448u, "shared memory");
+constexpr int BAR_QTMEM = BAR_PFREE0;  // Q copied into TMEM (128 arrivals)
+}  // namespace q16
+
+__global__ void __launch_bounds__(q16::kThreads, 1)
+    mla_split_kv_bf16_q16_kernel(const __grid_constant__ CUtensorMap tm_kv,
+                                 const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+  using namespace q16;
+  const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
+  const int split = blockIdx.x / ngroups;
+  const int grp = blockIdx.x - split * ngroups;
+  const int b = blockIdx.y;
+
+  const int L = p.kv_lens[b];
+  const int nsplit = p.splits[b];
+  const int chunk = p.chunks[b];
+  if (split >= nsplit) return;
+  {
+    const bool bad = L < 1 || (p.causal && L < p.q_len) || nsplit > p.max_splits ||
+                     chunk < MLA_TILE_TOKENS || (chunk % MLA_TILE_TOKENS) != 0 ||
+                     static_cast<int64_t>(nsplit) * chunk < L ||
+                     static_cast<int64_t>(nsplit - 1) * chunk >= L ||
+                     static_cast<int64_t>(L) > static_cast<int64_t>(p.max_pages) * MLA_PAGE_SIZE;
+    if (bad) {
+      if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
+      return;
+    }
+  }
+  const int tok_begin = split * chunk;
+  const int tok_end = min(L, tok_begin + chunk);
+  const int n_tiles = (tok_end - tok_begin + kTokB - 1) / kTokB;
+  const float c_log2 = p.c_log2;
+  const int row0 = grp * p.rows_per_group;
+  const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(base);
+  auto bar = [&](int i) -> uint32_t { return sbase + kBars + 8u * i; };
+  volatile int* flags = reinterpret_cast<volatile int*>(base + kFlags);
+  volatile int* abort_flag = flags + 2;
+  float* red_max = reinterpret_cast<float*>(base + kRedMax);
+  float* red_sum = reinterpret_cast<float*>(base + kRedSum);
+  float* kref = reinterpret_cast<float*>(base + kKref);
+  float* alpha_s = reinterpret_cast<float*>(base + kAlpha);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < NST; ++k) {
+      mbar_init(bar(BAR_FULL0 + k), 1);
+      mbar_init(bar(BAR_EMPTY0 + k), 1);
+    }
+    mbar_init(bar(BAR_QFULL), 1);
+    mbar_init(bar(BAR_QTMEM), 128);
+    mbar_init(bar(BAR_SFULL0), 1);
+    mbar_init(bar(BAR_SFULL1), 1);
+    mbar_init(bar(BAR_SFREE0), 128);
+    mbar_init(bar(BAR_SFREE1), 128);
+    mbar_init(bar(BAR_PFULL0), 128);
+    mbar_init(bar(BAR_PFULL1), 128);
+    mbar_init(bar(BAR_ODONE), 1);
+    mbar_init(bar(BAR_FINAL), 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + kTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + kTmemSlot);
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_kv);
+      tma_prefetch_desc(&tm_q);
+      const int qrow = b * p.rows_per_req + row0;
+      mbar_arrive_expect_tx(bar(BAR_QFULL), NR * kRowBytesB);
+#pragma unroll
+      for (int d = 0; d < 9; ++d)
+        tma_load_2d(sbase + kQStage + d * NR * 128, &tm_q, d * 64, qrow, bar(BAR_QFULL));
+    }
+    const uint64_t pol = l2_policy_evict_first();
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+    const int page0 = tok_begin / MLA_PAGE_SIZE;
+    const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
+    auto load_window = [&](int w) -> int {
+      const int pi = page0 + w * 32 + lane;
+      int pg = 0;
+      if (pi < page_end) {
+        pg = pt[pi];
+        if (pg < 0 || pg >= p.num_pages) {
+          report(p.status, MLA_ERR_INVALID_ARG);
+          pg = 0;
+        }
+      }
+      return pg;
+    };
+    int window = load_window(0);
+    int window_next = load_window(1);
+    int issued = 0;
+    int st = 0, round = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      if (i > 0 && (i & 15) == 0) {
+        window = window_next;
+        window_next = load_window((i >> 4) + 1);
+      }
+      bool ok = true;
+      if (round > 0) {
+        ok = mbar_wait(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles);
+      } else if (st == NST - 1) {
+        // The last stage holds the staged Q until it has been copied to TMEM.
+        ok = mbar_wait(bar(BAR_QTMEM), 0, p.wait_cycles);
+      }
+      ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+      if (!ok) {
+        if (lane == 0) {
+          report(p.status, MLA_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      const int my_page = __shfl_sync(0xffffffffu, window, (i & 15) * 2 + (lane & 1));
+      const int tp0 = page0 + i * 2;
+      const uint32_t fb = bar(BAR_FULL0 + st);
+      if (lane == 0) {
+        const int nvalid = (tp0 < page_end ? 1 : 0) + (tp0 + 1 < page_end ? 1 : 0);
+        mbar_arrive_expect_tx(fb, nvalid * kPageBytesB);
+      }
+      __syncwarp();
+      if (lane < 2 && tp0 + lane < page_end) {
+        const uint32_t kv = sbase + st * kTileBytesB;
+        const int row = my_page * MLA_PAGE_SIZE;
+#pragma unroll
+        for (int d = 0; d < 9; ++d)
+          tma_load_2d_hint(kv + d * kBlkBytesB + lane * kPageBlkBytesB, &tm_kv, d * 64, row, fb,
+                           pol);
+      }
+      __syncwarp();
+      issued = i + 1;
+      if (++st == NST) {
+        st = 0;
+        ++round;
+      }
+    }
+    if (lane == 0) {
+      for (int k = max(0, issued - NST); k < issued; ++k)
+        mbar_wait(bar(BAR_FULL0 + k % NST), (k / NST) & 1, kWaitLimitCycles);
+      mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    constexpr uint32_t kIdQK = idesc_bf16(128, 64, 0, 0);
+    constexpr uint32_t kIdPV = idesc_bf16(128, NR, 1, 0);
+    bool ok = mbar_wait(bar(BAR_QTMEM), 0, p.wait_cycles);
+    auto fail = [&]() {
+      if (lane == 0) {
+        report(p.status, MLA_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    };
+    auto issue_pv = [&](int j, int jst) {
+      tc_fence_after();
+      const uint32_t kv = sbase + jst * kTileBytesB;
+      const uint32_t pbuf = kv + kRopeOffB;
+#pragma unroll
+      for (int d = 0; d < 4; ++d) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = smem_desc(kv + 2 * d * kBlkBytesB + ks * 2048, kBlkBytesB, 1024,
+                                       kLayoutSW128);
+          // B = P^T, K-major: a row's 64 tokens in one swizzled 128-byte line,
+          // 16 tokens (32 B) per instruction, 8-row groups 1 KB apart.
+          const uint64_t bd = smem_desc(pbuf + ks * 32, 16, 1024, kLayoutSW128);
+          umma_bf16(tmem + kOCol + d * NR, a, bd, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(bar(BAR_EMPTY0 + jst));
+      umma_commit(bar(BAR_ODONE));
+    };
+    auto issue_qk = [&](int ist, int sb) {
+      tc_fence_after();
+      const uint32_t kv = sbase + ist * kTileBytesB;
+#pragma unroll
+      for (int kk = 0; kk < 36; ++kk) {
+        const int d = kk >> 2, sub = kk & 3;
+        const uint64_t bd = smem_desc(kv + d * kBlkBytesB + sub * 32, 16, 1024, kLayoutSW128);
+        umma_bf16_ta(tmem + kSCol + sb * 64, tmem + kQCol + kk * 8, bd, kIdQK, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(bar(BAR_SFULL0 + sb));
+    };
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) fail();
+    tc_fence_after();
+    int qk = 0, pv = 0;
+    int qk_st = 0, qk_round = 0, pv_st = 0;
+    long long t_last = clock64();
+    while (ok && pv < n_tiles) {
+      int action = 0;
+      if (lane == 0) {
+        if (pv < qk && mbar_test_wait(bar(BAR_PFULL0 + (pv & 1)), (pv >> 1) & 1)) action = 1;
+        if (action == 0 && qk < n_tiles && qk <= pv + 1) {
+          const int use = qk >> 1;
+          if (mbar_test_wait(bar(BAR_FULL0 + qk_st), qk_round & 1) &&
+              (use < 1 || mbar_test_wait(bar(BAR_SFREE0 + (qk & 1)), (use - 1) & 1)))
+            action = 2;
+        }
+      }
+      action = __shfl_sync(0xffffffffu, action, 0);
+      if (action == 1) {
+        if (lane == 0) issue_pv(pv, pv_st);
+        __syncwarp();
+        ++pv;
+        if (++pv_st == NST) pv_st = 0;
+        t_last = clock64();
+      } else if (action == 2) {
+        const int tile_tok0 = tok_begin + qk * kTokB;
+        const int valid = tok_end - tile_tok0;
+        if (valid < kTokB) {
+          const int nrow = kTokB - valid;
+          uint8_t* kvp = base + qk_st * kTileBytesB;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          for (int idx = lane; idx < nrow * 72; idx += 32) {
+            const int r = valid + idx / 72;
+            const int c = idx % 72;
+            *reinterpret_cast<uint4*>(kvp + (c / 8) * kBlkBytesB + r * 128 + (c % 8) * 16) = z;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) issue_qk(qk_st, qk & 1);
+        __syncwarp();
+        ++qk;
+        if (++qk_st == NST) {
+          qk_st = 0;
+          ++qk_round;
+        }
+        t_last = clock64();
+      } else {
+        const bool late = (clock64() - t_last > p.wait_cycles) || *abort_flag;
+        if (__any_sync(0xffffffffu, late)) {
+          fail();
+          ok = false;
+        }
+      }
+    }
+    if (lane == 0) umma_commit(bar(BAR_FINAL));
+    __syncwarp();
+    mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
+  } else {
+    // ================= softmax warpgroup =================
+    const int w = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int lidx = w * 32 + lane;         // TMEM lane
+    const int row = lidx & 15;              // query row of this thread
+    const int slot = lidx >> 4;             // tokens 8*slot .. 8*slot + 7 of a tile
+    const bool hi = lane >= 16;
+    const int sid = threadIdx.x - 64;       // 0..127; owner of row sid when < 16
+    const uint32_t lane_addr = static_cast<uint32_t>(w * 32) << 16;
+    bool ok = true;
+    // ---- Q: staged rows -> TMEM (lane l gets row l % 16) ----
+    ok = mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      const uint8_t* qs = base + kQStage;
+#pragma unroll 1
+      for (int d = 0; d < 9; ++d) {
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              qs + d * NR * 128 + row * 128 + ((j ^ (row & 7)) * 16));
+          r[4 * j + 0] = v.x;
+          r[4 * j + 1] = v.y;
+          r[4 * j + 2] = v.z;
+          r[4 * j + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_addr + kQCol + d * 32, r);
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    mbar_arrive(bar(BAR_QTMEM));
+
+    float k_row = -INFINITY;  // owner state
+    float l_row = 0.0f;
+    float kreg = -INFINITY;   // this thread's row reference
+    const float c = c_log2;
+    const int qi = (row0 + row) / p.num_heads;
+    const bool row_ok = row < rows_here;
+    const int lim = p.causal ? min(tok_end, L - p.q_len + qi + 1) : tok_end;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int sb = i & 1;
+      const int use = i >> 1;
+      if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
+      ok = __all_sync(0xffffffffu, ok);
+      float t[8];
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_addr + kSCol + sb * 64 + w * 16, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = __uint_as_float(hi ? r[8 + k] : r[k]);
+        tc_fence_before();
+        mbar_arrive(bar(BAR_SFREE0 + sb));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = 0.0f;
+      }
+      const int j0 = tok_begin + i * kTokB + slot * 8;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t[k] = (row_ok && j0 + k < lim) ? t[k] * c : -INFINITY;
+      bool over = false;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) over |= t[k] > kreg + 0.75f;
+      const bool any_over = bar_sync_or(kVoteBarrier, 128, over);
+      if (sid < NR && i > 0) {
+        const float* rs = red_sum + ((i - 1) & 1) * 64;
+        l_row += (rs[sid] + rs[16 + sid]) + (rs[32 + sid] + rs[48 + sid]);
+      }
+      if (any_over) {
+        float m = t[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) m = fmaxf(m, t[k]);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if (!hi) red_max[w * 16 + row] = m;
+        if (sid == 0) flags[0] = 0;
+        named_bar_sync(kSoftmaxBarrier, 128);
+        if (sid < NR) {
+          const float mt = fmaxf(fmaxf(red_max[sid], red_max[16 + sid]),
+                                 fmaxf(red_max[32 + sid], red_max[48 + sid]));
+          float k_new = k_row;
+          if (mt > k_row + 0.75f) k_new = ceilf(mt);
+          float alpha = 1.0f;
+          if (k_new != k_row && k_row != -INFINITY) {
+            const int e = static_cast<int>(k_row - k_new);
+            alpha = (e < -126) ? 0.0f : pow2i(e);
+            flags[0] = 1;
+          }
+          l_row *= alpha;
+          k_row = k_new;
+          kref[sid] = k_new;
+          alpha_s[sid] = alpha;
+        }
+        named_bar_sync(kSoftmaxBarrier, 128);
+        kreg = kref[row];
+        const bool corr = flags[0] != 0;
+        if (ok && corr && i > 0) {
+          ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, p.wait_cycles);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int d = 0; d < 4; ++d) {
+              uint32_t r[16];
+              const uint32_t addr = tmem + lane_addr + kOCol + d * NR;
+              tmem_ld16(addr, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[k]);
+              tmem_st16(addr, r);
+            }
+            tmem_st_wait();
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t[k] = softmax_weight<false>(t[k], kreg);
+      if (ok) {
+        // P^T row `row`, tokens 8*slot..+7: one 16-byte chunk of the row's
+        // swizzled 128-byte line in the rope block of this tile's stage.
+        uint8_t* pbuf = base + (i % NST) * kTileBytesB + kRopeOffB;
+        uint4 v;
+        v.x = pack_bf16x2(t[0], t[1]);
+        v.y = pack_bf16x2(t[2], t[3]);
+        v.z = pack_bf16x2(t[4], t[5]);
+        v.w = pack_bf16x2(t[6], t[7]);
+        *reinterpret_cast<uint4*>(pbuf + (row >> 3) * 1024 + (row & 7) * 128 +
+                                  ((slot ^ (row & 7)) * 16)) = v;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(BAR_PFULL0 + (i & 1)));
+      }
+      float sum = ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+      if (!hi) red_sum[(i & 1) * 64 + w * 16 + row] = sum;
+    }
+    if (!ok && lane == 0) {
+      report(p.status, MLA_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // ---- epilogue ----
+    named_bar_sync(kSoftmaxBarrier, 128);
+    const bool single = (nsplit == 1);
+    float* scale_s = alpha_s;
+    if (sid < NR) {
+      if (n_tiles > 0) {
+        const float* rs = red_sum + ((n_tiles - 1) & 1) * 64;
+        l_row += (rs[sid] + rs[16 + sid]) + (rs[32 + sid] + rs[48 + sid]);
+      }
+      const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
+      const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + sid;
+      float sc = 0.0f;
+      if (sid < rows_here) {
+        if (single) {
+          const float ls = (l_row > 0.0f) ? 0.6931471805599453f * (m_s + log2f(l_row)) : -INFINITY;
+          if (p.lse) p.lse[grow] = ls;
+          sc = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
+        } else {
+          float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
+          ml[0] = m_s;
+          ml[1] = l_row;
+          sc = 1.0f;
+        }
+      }
+      scale_s[sid] = sc;
+    }
+    named_bar_sync(kSoftmaxBarrier, 128);
+    bool fin = mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
+    fin = __all_sync(0xffffffffu, fin);
+    if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
+    if (ok && fin && n_tiles > 0) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int d = 0; d < 4; ++d) {
+        const int dim = d * 128 + lidx;
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_addr + kOCol + d * NR, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          if (k < rows_here) {
+            const float v = __uint_as_float(r[k]) * scale_s[k];
+            const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + k;
+            if (single) {
+              p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
+              if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = v;
+            } else {
+              p.ws_o[(grow * p.max_splits + split) * MLA_LATENT_DIM + dim] = v;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2-D BF16 view [rows, 576] with a (64, box_y) box, 128-byte swizzle.
 static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t box_y) {
   auto enc = encode_fn();
@@ -604,6 +1126,28 @@ static cudaError_t launch_split_bf16(const void* q, const void* kv, int64_t num_
     return cudaErrorInvalidValue;
   dim3 grid(prm.max_splits * groups, batch);
   mla_split_kv_bf16_kernel<NR><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_q, prm);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_split_bf16_q16(const void* q, const void* kv, int64_t num_pages,
+                                         int batch, int groups, const DecodeParams& prm,
+                                         cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_bf16_q16_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(q16::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  CUtensorMap tm_kv, tm_q;
+  if (!make_map_bf16(&tm_kv, kv, static_cast<uint64_t>(num_pages) * MLA_PAGE_SIZE,
+                     MLA_PAGE_SIZE) ||
+      !make_map_bf16(&tm_q, q, static_cast<uint64_t>(batch) * prm.rows_per_req, q16::NR))
+    return cudaErrorInvalidValue;
+  dim3 grid(prm.max_splits * groups, batch);
+  mla_split_kv_bf16_q16_kernel<<<grid, q16::kThreads, q16::kSmemBytes, stream>>>(tm_kv, tm_q,
+                                                                                prm);
   return cudaGetLastError();
 }
 
@@ -688,7 +1232,9 @@ extern "C" int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, in
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (rg.nr) {
-    case 16: e = launch_split_bf16<16>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
+    case 16:
+      e = launch_split_bf16_q16(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st);
+      break;
     case 32: e = launch_split_bf16<32>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
     case 48: e = launch_split_bf16<48>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
     default:
