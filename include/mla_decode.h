@@ -67,7 +67,8 @@ typedef enum {
 #define MLA_ROPE_DIM 64
 #define MLA_PAGE_SIZE 32
 #define MLA_TILE_TOKENS 128 /* split chunks are multiples of this */
-#define MLA_MAX_SPLITS 128  /* per-request split cap (issue #20510, "Repro 2") */
+#define MLA_MAX_SPLITS 256  /* per-request split cap of the GB300 planner and the kernels */
+#define MLA_PAGES_SPLIT_CAP 128 /* the pages' planner cap (issue #20510, "Repro 2") */
 #define MLA_MAX_ROWS 1024   /* num_heads * q_len */
 
 /*
@@ -84,7 +85,9 @@ typedef enum {
  *              CTAs on top of that.)
  *              <= 0: GB300 planner: one common chunk for the whole batch,
  *              chosen to balance whole waves of one CTA per SM.
- * Outputs (host): splits_out[batch] (1..MLA_MAX_SPLITS), chunk_out[batch]
+ * Outputs (host): splits_out[batch] (1..MLA_PAGES_SPLIT_CAP with a target,
+ *              1..MLA_MAX_SPLITS for the GB300 planner: a single long request
+ *              can then fill every SM), chunk_out[batch]
  *              (tokens per split, a multiple of 128, splits*chunk >= L),
  *              *kv_split_out (merge thread groups: 1, 2, 4, 8 or 16, about
  *              four partials per group) and

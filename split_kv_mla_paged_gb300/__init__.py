@@ -47,7 +47,8 @@ HEAD_DIM = 576
 LATENT_DIM = 512
 PAGE_SIZE = 32
 TILE_TOKENS = 128
-MAX_SPLITS = 128
+MAX_SPLITS = 256
+PAGES_SPLIT_CAP = 128
 
 
 class DecodeOptions(ctypes.Structure):

@@ -7,8 +7,10 @@
 //    t = max(1, target / B) splits per request, chunk = roundup128(ceil(L / t)),
 //    splits = ceil(L / chunk).
 //  * target_ctas <= 0 is the GB300 planner.  One CTA of the split kernel fills
-//    an SM (its shared memory holds two 72 KB KV stages), so it balances whole
-//    waves of sm_count CTAs: one chunk for the whole batch (the skewed-batch
+//    an SM (its shared memory holds two or three 72 KB KV stages), so it
+//    balances whole waves of sm_count CTAs, with up to MLA_MAX_SPLITS splits
+//    per request (a single long request fills every SM): one chunk for the
+//    whole batch (the skewed-batch
 //    finding in the same issue's follow-up: a common split size plus early
 //    exit of empty split slots beats one wave per request), a minimum of one
 //    128-token tile per split (the short-KV finding there), and an estimate of
@@ -88,8 +90,8 @@ extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t nu
     const int64_t t = std::max<int64_t>(1, target_ctas / static_cast<int64_t>(batch));
     for (int b = 0; b < batch; ++b) {
       int64_t chunk = round_up(ceil_div(kv_lens[b], t), T);
-      if (ceil_div(kv_lens[b], chunk) > MLA_MAX_SPLITS)
-        chunk = round_up(ceil_div(kv_lens[b], MLA_MAX_SPLITS), T);
+      if (ceil_div(kv_lens[b], chunk) > MLA_PAGES_SPLIT_CAP)
+        chunk = round_up(ceil_div(kv_lens[b], MLA_PAGES_SPLIT_CAP), T);
       chunk_out[b] = static_cast<int32_t>(chunk);
       splits_out[b] = static_cast<int32_t>(ceil_div(kv_lens[b], chunk));
     }
