@@ -273,7 +273,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--plan", choices=["gb300", "pages"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--cpu-rows", type=int, default=24,
+    ap.add_argument("--replays", type=int, default=10,
+                    help="further replays of the K-call graph for p10/median/p90")
+    ap.add_argument("--cpu-rows", type=int, default=192,
                     help="rows of the oracle CPU baseline sample (0 disables it)")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="wall-clock budget of the whole --impl reference run")
@@ -429,7 +431,40 @@ def main():
     merge_us = ev["merge"][0].elapsed_time(ev["merge"][1]) * 1e3 / K
     us_per_call = max_over_ranks(total_ms * 1e3 / K, dev)
     mla.mla_decode_status(ws, stream)
-    del graphs
+
+    # ---- spread over further replays, and the graph-launch floor ----
+    # p10 / median / p90 of the per-call time over further replays of the
+    # K-call graph (reported beside `value`, which is the bracketed run above).
+    rep_us = []
+    with torch.cuda.stream(stream):
+        for _ in range(max(0, args.replays)):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graphs["full"].replay()
+            e1.record(stream)
+            e1.synchronize()
+            rep_us.append(e0.elapsed_time(e1) * 1e3 / K)
+    # Trivial-kernel floor: K one-element kernels through the same graph path.
+    tiny = torch.zeros(1, device=dev)
+    with torch.cuda.stream(stream):
+        tiny.add_(1.0)
+    torch.cuda.synchronize(dev)
+    g_floor = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_floor, stream=stream):
+        for _ in range(K):
+            tiny.add_(1.0)
+    with torch.cuda.stream(stream):
+        g_floor.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g_floor.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    floor_us = e0.elapsed_time(e1) * 1e3 / K
+    mla.mla_decode_status(ws, stream)
+    del graphs, g_floor
 
     # ---- end to end through the public API with host buffers ----
     q_h = inp.q.cpu().pin_memory()
@@ -522,7 +557,11 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * K,
+            "gpu_launches": K * (2 if plan.max_splits > 1 else 1),
+            "replays": ({"n": len(rep_us), "p10_us": float(np.percentile(rep_us, 10)),
+                         "median_us": float(np.median(rep_us)),
+                         "p90_us": float(np.percentile(rep_us, 90))} if rep_us else None),
+            "floor_us_per_call": floor_us,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
