@@ -833,58 +833,50 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) fail();
     tc_fence_after();
-    int qk = 0, pv = 0;
-    int qk_st = 0, qk_round = 0, pv_st = 0;
-    long long t_last = clock64();
-    while (ok && pv < n_tiles) {
-      int action = 0;
-      if (lane == 0) {
-        if (pv < qk && mbar_test_wait(bar(BAR_PFULL0 + (pv & 1)), (pv >> 1) & 1)) action = 1;
-        if (action == 0 && qk < n_tiles && qk <= pv + 1) {
-          const int use = qk >> 1;
-          if (mbar_test_wait(bar(BAR_FULL0 + qk_st), qk_round & 1) &&
-              (use < 1 || mbar_test_wait(bar(BAR_SFREE0 + (qk & 1)), (use - 1) & 1)))
-            action = 2;
+    // Fixed issue order QK(i+1), PV(i): with 52 MMAs per 64-token tile this
+    // kernel is bound by MMA issue, so the next tile has landed by the time
+    // QK(i+1) is due and P(i) is ready when QK(i+1) has gone out (the softmax
+    // of a tile is shorter than a QK); direct waits on one barrier at a time
+    // keep the issue warp busy.
+    auto qk_step = [&](int j) -> bool {
+      const int st = j % NST;
+      bool w = mbar_wait(bar(BAR_FULL0 + st), (j / NST) & 1, p.wait_cycles);
+      const int use = j >> 1;
+      if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + (j & 1)), (use - 1) & 1, p.wait_cycles);
+      w = __all_sync(0xffffffffu, w && !*abort_flag);
+      if (!w) return false;
+      const int valid = tok_end - (tok_begin + j * kTokB);
+      if (valid < kTokB) {
+        // Rows past the split's end: zero them so V holds no stale or NaN values.
+        const int nrow = kTokB - valid;
+        uint8_t* kvp = base + st * kTileBytesB;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int idx = lane; idx < nrow * 72; idx += 32) {
+          const int r = valid + idx / 72;
+          const int c = idx % 72;
+          *reinterpret_cast<uint4*>(kvp + (c / 8) * kBlkBytesB + r * 128 + (c % 8) * 16) = z;
         }
-      }
-      action = __shfl_sync(0xffffffffu, action, 0);
-      if (action == 1) {
-        if (lane == 0) issue_pv(pv, pv_st);
+        fence_proxy_async_smem();
         __syncwarp();
-        ++pv;
-        if (++pv_st == NST) pv_st = 0;
-        t_last = clock64();
-      } else if (action == 2) {
-        const int tile_tok0 = tok_begin + qk * kTokB;
-        const int valid = tok_end - tile_tok0;
-        if (valid < kTokB) {
-          const int nrow = kTokB - valid;
-          uint8_t* kvp = base + qk_st * kTileBytesB;
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          for (int idx = lane; idx < nrow * 72; idx += 32) {
-            const int r = valid + idx / 72;
-            const int c = idx % 72;
-            *reinterpret_cast<uint4*>(kvp + (c / 8) * kBlkBytesB + r * 128 + (c % 8) * 16) = z;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        if (lane == 0) issue_qk(qk_st, qk & 1);
-        __syncwarp();
-        ++qk;
-        if (++qk_st == NST) {
-          qk_st = 0;
-          ++qk_round;
-        }
-        t_last = clock64();
-      } else {
-        const bool late = (clock64() - t_last > p.wait_cycles) || *abort_flag;
-        if (__any_sync(0xffffffffu, late)) {
-          fail();
-          ok = false;
-        }
       }
+      if (lane == 0) issue_qk(st, j & 1);
+      __syncwarp();
+      return true;
+    };
+    if (ok && n_tiles > 0) ok = qk_step(0);
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      if (i + 1 < n_tiles) ok = qk_step(i + 1);
+      if (!ok) break;
+      bool w = mbar_wait(bar(BAR_PFULL0 + (i & 1)), (i >> 1) & 1, p.wait_cycles);
+      w = __all_sync(0xffffffffu, w && !*abort_flag);
+      if (!w) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) issue_pv(i, i % NST);
+      __syncwarp();
     }
+    if (!ok) fail();
     if (lane == 0) umma_commit(bar(BAR_FINAL));
     __syncwarp();
     mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);

@@ -101,6 +101,20 @@ def test_split_plans_agree_in_fp32():
             assert dl <= PLAN_ABS, f"plan {plan.splits.tolist()} kv_split {ks}: lse {dl:.3e}"
 
 
+def test_maximum_rows_per_request():
+    # H * q = 1024 = MLA_MAX_ROWS: 22 row groups (21 of 48 and one of 16).
+    inp = decode_inputs(2, 128, 8, [700, 300], seed=21, extra_pages=1)
+    _full_check(inp, True, SOFTMAX_SCALE)
+
+
+def test_maximum_splits_per_request():
+    # 256 splits (MLA_MAX_SPLITS) of one 128-token tile each, merged by 16 groups.
+    inp = decode_inputs(1, 12, 1, [32768], seed=22)
+    plan = mla.mla_decode_plan([32768], 12, 1, sm_count=256)
+    assert plan.max_splits == mla.MAX_SPLITS == 256 and plan.kv_split == 16
+    _full_check(inp, False, SOFTMAX_SCALE, plan=plan)
+
+
 def test_deterministic_run_to_run():
     inp = decode_inputs(1, 12, 1, [9000], seed=10)
     a = run_decode(inp, False, SOFTMAX_SCALE)
