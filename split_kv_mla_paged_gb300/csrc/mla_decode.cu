@@ -124,13 +124,16 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tm_q_lat,
                         const __grid_constant__ CUtensorMap tm_q_rope, const DecodeParams p) {
   using C = Cfg<NR>;
-  // Row groups of one (request, split) are adjacent in the grid so that the
-  // CTAs that read the same KV tiles run at the same time (L2 serves the
-  // repeats).
+  // Grid (request, split x row group), dispatched split-major: every
+  // request's first splits go out before anyone's later ones, so the empty
+  // slots of short requests (split >= splits[b], exiting at once) do not hold
+  // back real work in a skewed batch; the row groups of one split are
+  // `batch` CTAs apart and run in the same wave, so L2 serves their repeated
+  // reads of the same KV tiles.
   const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
-  const int split = blockIdx.x / ngroups;
-  const int grp = blockIdx.x - split * ngroups;
-  const int b = blockIdx.y;
+  const int split = blockIdx.y / ngroups;
+  const int grp = blockIdx.y - split * ngroups;
+  const int b = blockIdx.x;
 
   // ---- plan checks (uniform over the CTA) -------------------------------
   const int L = p.kv_lens[b];
@@ -843,8 +846,8 @@ __global__ void __launch_bounds__(32 * G) mla_merge_kernel(const MergeParams p) 
   __shared__ float4 sm_o[G][32];
   // Partials are written by the preceding (programmatically dependent) grid.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int row = blockIdx.y;
-  const int quarter = blockIdx.x;
+  const int row = blockIdx.x;
+  const int quarter = blockIdx.y;
   const int g = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int ns = p.uniform_s;
@@ -985,7 +988,7 @@ static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages
       !make_map(&q_lat, q, q_rows, 128, NR, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&q_rope, q, q_rows, 64, NR, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  dim3 grid(prm.max_splits * groups, batch);
+  dim3 grid(batch, prm.max_splits * groups);
   mla_split_kv_kernel<NR, kGather><<<grid, C::kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
                                                                      q_rope, prm);
   return cudaGetLastError();
@@ -998,7 +1001,7 @@ static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages
 template <int G>
 static cudaError_t launch_merge_g(const MergeParams& mp, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(4, mp.rows);
+  cfg.gridDim = dim3(mp.rows, 4);  // rows on x: no 65535 limit
   cfg.blockDim = dim3(32 * G);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -123,9 +123,9 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
                              const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
   using C = CfgB<NR>;
   const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
-  const int split = blockIdx.x / ngroups;
-  const int grp = blockIdx.x - split * ngroups;
-  const int b = blockIdx.y;
+  const int split = blockIdx.y / ngroups;
+  const int grp = blockIdx.y - split * ngroups;
+  const int b = blockIdx.x;
 
   const int L = p.kv_lens[b];
   const int nsplit = p.splits[b];
@@ -639,9 +639,9 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
                                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
   using namespace q16;
   const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
-  const int split = blockIdx.x / ngroups;
-  const int grp = blockIdx.x - split * ngroups;
-  const int b = blockIdx.y;
+  const int split = blockIdx.y / ngroups;
+  const int grp = blockIdx.y - split * ngroups;
+  const int b = blockIdx.x;
 
   const int L = p.kv_lens[b];
   const int nsplit = p.splits[b];
@@ -1116,7 +1116,7 @@ static cudaError_t launch_split_bf16(const void* q, const void* kv, int64_t num_
                      MLA_PAGE_SIZE) ||
       !make_map_bf16(&tm_q, q, static_cast<uint64_t>(batch) * prm.rows_per_req, NR))
     return cudaErrorInvalidValue;
-  dim3 grid(prm.max_splits * groups, batch);
+  dim3 grid(batch, prm.max_splits * groups);
   mla_split_kv_bf16_kernel<NR><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_q, prm);
   return cudaGetLastError();
 }
@@ -1137,7 +1137,7 @@ static cudaError_t launch_split_bf16_q16(const void* q, const void* kv, int64_t 
                      MLA_PAGE_SIZE) ||
       !make_map_bf16(&tm_q, q, static_cast<uint64_t>(batch) * prm.rows_per_req, q16::NR))
     return cudaErrorInvalidValue;
-  dim3 grid(prm.max_splits * groups, batch);
+  dim3 grid(batch, prm.max_splits * groups);
   mla_split_kv_bf16_q16_kernel<<<grid, q16::kThreads, q16::kSmemBytes, stream>>>(tm_kv, tm_q,
                                                                                 prm);
   return cudaGetLastError();

@@ -254,6 +254,11 @@ for _b in (1, 4):
              kv_lens=[_l] * _b, causal=True, target=None, seed=4)
 _add("ragged_h12_q1_b16", batch=16, num_heads=12, q_len=1, kv_lens=ragged_lens(4),
      causal=False, target=None, seed=4)
+# Skewed batch (issue #20510 follow-up: "one 1M request plus short ones";
+# the count and lengths of the short ones are not given: seven of 4K here).
+for _q in (1, 8):
+    _add(f"skewed_h12_q{_q}_1m_plus_7x4k", batch=8, num_heads=12, q_len=_q,
+         kv_lens=[1048576] + [4096] * 7, causal=(_q > 1), target=None, seed=7)
 # BF16 KV cache (the pages' BF16 kernel is quoted at H12 q8 B1 1M).
 for _q in (1, 8):
     _add(f"bf16_h12_q{_q}_l1m_b1", batch=1, num_heads=12, q_len=_q, kv_lens=[1048576],

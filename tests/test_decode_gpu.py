@@ -221,6 +221,7 @@ def _sample_rows(inp, n, seed):
     ("ragged_h12_q1_b16", 16),
     ("packed_h96_q8_l128k_b1", 12),
     ("long_h12_q1_l1m_b16", 6),
+    ("skewed_h12_q8_1m_plus_7x4k", 8),
 ])
 def test_full_size_sampled_rows(name, nrows):
     w = WORKLOADS[name]
