@@ -85,3 +85,51 @@ def test_merge_rejects_bad_arguments(lib):
 
 def test_status_rejects_null(lib):
     assert lib.mla_decode_status(None, None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_bf16_decode_host_checks(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    st = lib.mla_decode_bf16(None, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 0.1,
+                             fake, 1 << 30, fake, None, None, None)
+    assert st == mla.MLA_ERR_INVALID_ARG and "null" in mla.mla_last_error()
+    st = lib.mla_decode_bf16(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 8, 256, 0, 0.1,
+                             fake, 1 << 30, fake, None, None, None)
+    assert st == mla.MLA_ERR_UNSUPPORTED
+    st = lib.mla_decode_bf16(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0,
+                             float("nan"), fake, 1 << 30, fake, None, None, None)
+    assert st == mla.MLA_ERR_INVALID_ARG
+    st = lib.mla_decode_bf16(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 0.1,
+                             fake, 16, fake, None, None, None)
+    assert st == mla.MLA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_sparse_decode_host_checks(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake, fake, 4, fake, 4, fake]
+    tail = [fake, fake, 2, 2, 1, 1, 12, 0, 1.0, 1.0, 0.1, fake, 1 << 30, fake, None, None, None,
+            None]
+    assert lib.mla_decode_sparse(*args, None, 8, *tail) == mla.MLA_ERR_INVALID_ARG
+    assert "block_idx" in mla.mla_last_error()
+    assert lib.mla_decode_sparse(*args, fake, 0, *tail) == mla.MLA_ERR_INVALID_ARG
+    assert "topk" in mla.mla_last_error()
+    small = list(tail)
+    small[12] = 16  # workspace bytes
+    assert lib.mla_decode_sparse(*args, fake, 8, *small) == mla.MLA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_decode_ex_rejects_nonfinite_output_scale(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    opts = mla.DecodeOptions(None, None, None, float("inf"), None, None, None)
+    st = lib.mla_decode_ex(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 1.0, 1.0,
+                           0.1, fake, 1 << 30, fake, None, None, ctypes.byref(opts), None)
+    assert st == mla.MLA_ERR_INVALID_ARG and "output_scale" in mla.mla_last_error()
+
+
+def test_kv_append_host_checks(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    # Zero tokens is a no-op that touches nothing.
+    assert lib.mla_kv_append(None, 0, None, None, None, 1, 1, None, 1, 1.0, None, None) == mla.MLA_OK
+    assert lib.mla_kv_append(None, 4, fake, fake, fake, 1, 1, fake, 1, 1.0, None,
+                             None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_kv_append(fake, 4, fake, fake, fake, 1, 1, fake, 1, 0.0, None,
+                             None) == mla.MLA_ERR_INVALID_ARG
