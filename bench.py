@@ -365,18 +365,27 @@ def main():
     torch.cuda.synchronize(dev)
     is_bf16 = inp.q.dtype == torch.bfloat16
 
-    def decode_call(*a):
+    # A plan with empty split slots (a skewed or ragged batch) launches the FP8
+    # kernel over its CTA item list: exactly the CTAs that have work.
+    use_items = (not is_bf16) and bool(np.any(plan.splits < plan.max_splits))
+    items_h = mla.mla_decode_plan_items(plan.splits, H, q_len) if use_items else None
+    items_d = torch.from_numpy(items_h).to(dev) if use_items else None
+
+    def decode_call(*a, items=None):
         # a = one call's 22 arguments (+ the page selection), then the stream
         c, s = a[:-1], a[-1]
+        it = items_d if items is None else items
         if is_sparse:
-            mla.mla_decode_sparse(*c[:6], c[22], topk, *c[6:22], stream=s)
+            mla.mla_decode_sparse(*c[:6], c[22], topk, *c[6:22], cta_items=it, stream=s)
         elif is_bf16:  # BF16 Q and KV: no q/kv scales
             mla.mla_decode_bf16(*c[:14], *c[16:22], s)
+        elif use_items:
+            mla.mla_decode_ex(*c[:22], cta_items=it, stream=s)
         else:
             mla.mla_decode(*c[:22], s)
 
     def split_call(*a):
-        if is_bf16 or is_sparse:
+        if is_bf16 or is_sparse or use_items:
             decode_call(*a)
         else:
             mla.mla_decode_splitkv(*a[:22], a[-1])
@@ -384,9 +393,10 @@ def main():
     def merge_call(*a):
         mla.mla_decode_merge(*a[:22], a[-1])
 
-    # The BF16 and sparse entry points have no separate phases: their "split"
-    # graph is the whole call (an upper bound on the split kernel's time), and
-    # the merge is the shared merge kernel on the same workspace and plan.
+    # The BF16, sparse and item-list calls have no separate phases: their
+    # "split" graph is the whole call (an upper bound on the split kernel's
+    # time), and the merge is the shared merge kernel on the same workspace
+    # and plan.
     phases = (("full", decode_call), ("split", split_call), ("merge", merge_call))
 
     with torch.cuda.stream(stream):
@@ -485,6 +495,10 @@ def main():
         sel_d = torch.empty_like(sels[0])
         e2e_args[22] = sel_d
         h2d += sel_h.numel() * 4
+    if use_items:
+        it_h = torch.from_numpy(items_h).pin_memory()
+        it_d = torch.empty_like(items_d)
+        h2d += it_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
     def e2e_step():
@@ -496,7 +510,10 @@ def main():
         meta_d.copy_(meta_h, non_blocking=True)
         if is_sparse:
             sel_d.copy_(sel_h, non_blocking=True)
-        decode_call(*e2e_args, stream)
+        if use_items:
+            mla.mla_decode_plan_items(plan.splits, H, q_len)  # host cost of the item list
+            it_d.copy_(it_h, non_blocking=True)
+        decode_call(*e2e_args, stream, items=it_d if use_items else None)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
@@ -541,6 +558,7 @@ def main():
                        "kv_len": lens[0], "causal": w["causal"], "plan": args.plan,
                        "splits": plan.splits.tolist()[:4] + (["..."] if B > 4 else []),
                        "kv_split": plan.kv_split, "kv_bytes": kv_bytes,
+                       "cta_items": use_items,
                        "l2": ("inputs larger than L2 (no flush)" if n_pools == 1 else
                               f"{n_pools} rotating input pools ({n_pools * kv_bytes} B > 2x L2)"),
                        "timing": "CUDA graph of K calls, CUDA events",

@@ -97,6 +97,28 @@ MLA_API int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t num_h
                     int32_t sm_count, int32_t target_ctas, int32_t* splits_out,
                     int32_t* chunk_out, int32_t* kv_split_out, size_t* workspace_bytes_out);
 
+/*
+ * CTA item list of a plan (host only): one entry per (request, split, row
+ * group) that has work, packed as (b << MLA_ITEM_B_SHIFT) |
+ * (split << MLA_ITEM_S_SHIFT) | row_group, in split-major order (every
+ * request's split s before anyone's split s + 1).  Passed to the decode
+ * through mla_decode_options_t.cta_items (a device copy) and num_ctas, it
+ * replaces the batch x max_splits grid, whose empty slots (split >= splits[b])
+ * a skewed batch has many of, by exactly the CTAs that have work (issue
+ * #20510 follow-up: skewed batches, skip_empty_splits).
+ *
+ * splits      host int32[batch], as planned by mla_decode_plan.
+ * items_out   host int32[capacity] or NULL (then only *n_items_out is set).
+ * Errors: MLA_ERR_INVALID_ARG (null, batch > MLA_ITEM_MAX_BATCH, a split
+ * count out of range, capacity too small), MLA_ERR_UNSUPPORTED (rows).
+ */
+#define MLA_ITEM_B_SHIFT 14
+#define MLA_ITEM_S_SHIFT 5
+#define MLA_ITEM_MAX_BATCH 65535
+MLA_API int mla_decode_plan_items(const int32_t* splits, int32_t batch, int32_t num_heads,
+                                  int32_t q_len, int32_t* items_out, int32_t capacity,
+                                  int32_t* n_items_out);
+
 /* Workspace bytes mla_decode needs: a 256-byte status header, then per
  * (row, split) an fp32 pair (m, l) and an fp32 O[512]. */
 MLA_API size_t mla_decode_workspace_size(int32_t batch, int32_t q_len, int32_t num_heads,
@@ -158,6 +180,9 @@ MLA_API int mla_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_
  *     run() argument kv_bounds; plain reading): keys restricted to
  *     lo <= j < hi for (lo, hi) = kv_bounds[b], intersected with [0, L) and
  *     the causal range.  Whole 128-token tiles below lo are skipped.
+ * cta_items, num_ctas  NULL / 0, or the device copy of the item list of
+ *     mla_decode_plan_items for this call's splits and its length: the
+ *     split-KV kernel then launches exactly num_ctas CTAs.
  * Zero-initialise the structure: fields added later default to off.
  */
 typedef struct {
@@ -168,6 +193,8 @@ typedef struct {
   const float* sinks;
   const int32_t* query_lens;
   const int32_t* kv_bounds;
+  const int32_t* cta_items;
+  int32_t num_ctas;
 } mla_decode_options_t;
 
 /* mla_decode with options (NULL options = mla_decode).  Same arguments,

@@ -23,7 +23,7 @@ __all__ = [
     "mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init", "mla_decode",
     "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
     "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16",
-    "mla_decode_sparse", "DecodeOptions", "decode", "merge",
+    "mla_decode_sparse", "mla_decode_plan_items", "DecodeOptions", "decode", "merge",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_
                     "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
                     "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit",
                     "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16",
-                    "mla_decode_sparse")
+                    "mla_decode_sparse", "mla_decode_plan_items")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
@@ -56,7 +56,8 @@ class DecodeOptions(ctypes.Structure):
     _fields_ = [("q_scale_dev", ctypes.c_void_p), ("kv_scale_dev", ctypes.c_void_p),
                 ("softmax_scale_dev", ctypes.c_void_p), ("output_scale", ctypes.c_float),
                 ("sinks", ctypes.c_void_p), ("query_lens", ctypes.c_void_p),
-                ("kv_bounds", ctypes.c_void_p)]
+                ("kv_bounds", ctypes.c_void_p), ("cta_items", ctypes.c_void_p),
+                ("num_ctas", ctypes.c_int32)]
 
 
 class MlaError(RuntimeError):
@@ -89,6 +90,8 @@ def load_library() -> ctypes.CDLL:
                                  ctypes.c_size_t)
         lib.mla_decode_plan.restype = ctypes.c_int
         lib.mla_decode_plan.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
+        lib.mla_decode_plan_items.restype = ctypes.c_int
+        lib.mla_decode_plan_items.argtypes = [vp, i32, i32, i32, vp, i32, vp]
         lib.mla_decode_workspace_size.restype = sz
         lib.mla_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         dec_args = [vp, vp, i64, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, f32,
@@ -176,6 +179,19 @@ def mla_decode_plan(kv_lens: Sequence[int], num_heads: int, q_len: int, sm_count
     return Plan(splits=splits, chunks=chunks, kv_split=int(kvs.value), workspace_bytes=int(ws.value))
 
 
+def mla_decode_plan_items(splits, num_heads: int, q_len: int) -> np.ndarray:
+    """CTA item list of a plan (one int32 per CTA that has work, split-major)."""
+    lib = load_library()
+    sp = np.ascontiguousarray(np.asarray(splits, dtype=np.int32))
+    n = ctypes.c_int32(0)
+    _check(lib.mla_decode_plan_items(sp.ctypes.data, int(sp.shape[0]), int(num_heads), int(q_len),
+                                     None, 0, ctypes.addressof(n)))
+    items = np.zeros(int(n.value), dtype=np.int32)
+    _check(lib.mla_decode_plan_items(sp.ctypes.data, int(sp.shape[0]), int(num_heads), int(q_len),
+                                     items.ctypes.data, int(items.shape[0]), ctypes.addressof(n)))
+    return items
+
+
 def mla_decode_workspace_size(batch: int, q_len: int, num_heads: int, max_splits: int) -> int:
     return int(load_library().mla_decode_workspace_size(batch, q_len, num_heads, max_splits))
 
@@ -210,11 +226,13 @@ def mla_decode_ex(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req,
                   kv_scale, softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32=None,
                   out_f32_debug=None, *, q_scale_dev=None, kv_scale_dev=None,
                   softmax_scale_dev=None, output_scale: float = 1.0, sinks=None,
-                  query_lens=None, kv_bounds=None, stream=None) -> None:
+                  query_lens=None, kv_bounds=None, cta_items=None, stream=None) -> None:
     """mla_decode with device-side scales, an output scale, attention sinks,
-    ragged query counts and key windows."""
+    ragged query counts, key windows and a CTA item list (a device int32
+    tensor from mla_decode_plan_items)."""
     opts = DecodeOptions(_ptr(q_scale_dev), _ptr(kv_scale_dev), _ptr(softmax_scale_dev),
-                         float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds))
+                         float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds),
+                         _ptr(cta_items), 0 if cta_items is None else int(cta_items.numel()))
     lib = load_library()
     _check(lib.mla_decode_ex(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages), _ptr(page_table),
                              int(max_pages_per_req), _ptr(kv_lens), _ptr(splits), _ptr(chunks),
@@ -247,11 +265,12 @@ def mla_decode_sparse(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_
                       workspace_bytes, out_bf16, lse_f32=None, out_f32_debug=None, *,
                       q_scale_dev=None, kv_scale_dev=None, softmax_scale_dev=None,
                       output_scale: float = 1.0, sinks=None, query_lens=None, kv_bounds=None,
-                      stream=None) -> None:
+                      cta_items=None, stream=None) -> None:
     """Sparse decode over the selected pages block_idx [batch, topk] (plan with
     the compact lengths 32 * topk)."""
     opts = DecodeOptions(_ptr(q_scale_dev), _ptr(kv_scale_dev), _ptr(softmax_scale_dev),
-                         float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds))
+                         float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds),
+                         _ptr(cta_items), 0 if cta_items is None else int(cta_items.numel()))
     lib = load_library()
     _check(lib.mla_decode_sparse(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages),
                                  _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),
@@ -343,7 +362,8 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
            plan: Optional[Plan] = None, sm_count: Optional[int] = None, target_ctas: int = 0,
            kv_split: Optional[int] = None, want_f32: bool = False, stream=None,
            check_status: bool = True, sinks=None, output_scale: float = 1.0,
-           device_scales: bool = False, query_lens=None, kv_bounds=None, block_idx=None):
+           device_scales: bool = False, query_lens=None, kv_bounds=None, block_idx=None,
+           use_items: Optional[bool] = None):
     """Plan, allocate outputs and a workspace with torch, and run mla_decode.
 
     q_fp8 uint8 [B, q, H, 576] and kv_pages_fp8 uint8 [P, 32, 576] (E4M3 codes)
@@ -351,8 +371,9 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
     sequence.  With torch.bfloat16 q and kv this runs mla_decode_bf16 (no
     scales, sinks or output scale there).  query_lens [B], kv_bounds [B, 2]
     and block_idx [B, topk] (selected pages: mla_decode_sparse, planned on the
-    compact lengths) restrict the visible keys.  Returns (out_bf16, lse,
-    out_f32 or None).
+    compact lengths) restrict the visible keys.  use_items (default: when the
+    plan has empty split slots) launches the FP8 kernel over the plan's CTA
+    item list.  Returns (out_bf16, lse, out_f32 or None).
     """
     import torch
     dev = q_fp8.device
@@ -379,13 +400,19 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
     common = (q_fp8, kv_pages_fp8, kv_pages_fp8.shape[0], page_table, page_table.shape[1],
               lens_d, splits_d, chunks_d, plan.max_splits, ks, batch, q_len, num_heads, causal)
     restricted = query_lens is not None or kv_bounds is not None or block_idx is not None
+    if use_items is None:
+        use_items = bool(np.any(plan.splits < plan.max_splits))
+    items_d = None
+    if use_items and q_fp8.dtype != torch.bfloat16:
+        items_d = torch.from_numpy(mla_decode_plan_items(plan.splits, num_heads, q_len)).to(dev)
     if q_fp8.dtype == torch.bfloat16:
         if (kv_pages_fp8.dtype != torch.bfloat16 or sinks is not None or output_scale != 1.0
                 or device_scales or q_scale != 1.0 or kv_scale != 1.0 or restricted):
             raise ValueError("BF16 decode takes BF16 q and kv and no scales, sinks, output "
                              "scale or key restrictions")
         mla_decode_bf16(*common, softmax_scale, ws, ws_bytes, out, lse, out_f32, stream)
-    elif sinks is None and output_scale == 1.0 and not device_scales and not restricted:
+    elif (sinks is None and output_scale == 1.0 and not device_scales and not restricted
+          and items_d is None):
         mla_decode(*common, q_scale, kv_scale, softmax_scale, ws, ws_bytes, out, lse, out_f32,
                    stream)
     else:
@@ -405,7 +432,7 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
                      kv_scale_dev=None if dev_s is None else dev_s[1:2],
                      softmax_scale_dev=None if dev_s is None else dev_s[2:3],
                      output_scale=output_scale, sinks=sk, query_lens=ql_d, kv_bounds=kb_d,
-                     stream=stream)
+                     cta_items=items_d, stream=stream)
         if bi_d is None:
             mla_decode_ex(*common, *host, ws, ws_bytes, out, lse, out_f32, **extra)
         else:

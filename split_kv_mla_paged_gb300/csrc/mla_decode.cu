@@ -117,7 +117,7 @@ struct Cfg {
 // tiles may have pages that are not loaded, and every score is masked by its
 // key position.  The plain variant (kGather = false) covers full key ranges,
 // with or without ragged query counts.
-template <int NR, bool kGather>
+template <int NR, bool kGather, bool kItems>
 __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     mla_split_kv_kernel(const __grid_constant__ CUtensorMap tm_kv_lat,
                         const __grid_constant__ CUtensorMap tm_kv_rope,
@@ -131,9 +131,22 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
   // `batch` CTAs apart and run in the same wave, so L2 serves their repeated
   // reads of the same KV tiles.
   const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
-  const int split = blockIdx.y / ngroups;
-  const int grp = blockIdx.y - split * ngroups;
-  const int b = blockIdx.x;
+  int split, grp, b;
+  if constexpr (kItems) {
+    // Item list: exactly the CTAs that have work.
+    const int it = p.cta_items[blockIdx.x];
+    b = it >> MLA_ITEM_B_SHIFT;
+    split = (it >> MLA_ITEM_S_SHIFT) & ((1 << (MLA_ITEM_B_SHIFT - MLA_ITEM_S_SHIFT)) - 1);
+    grp = it & ((1 << MLA_ITEM_S_SHIFT) - 1);
+    if (it < 0 || b >= p.batch || grp >= ngroups) {
+      if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
+      return;
+    }
+  } else {
+    split = blockIdx.y / ngroups;
+    grp = blockIdx.y - split * ngroups;
+    b = blockIdx.x;
+  }
 
   // ---- plan checks (uniform over the CTA) -------------------------------
   const int L = p.kv_lens[b];
@@ -968,13 +981,14 @@ static bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t bo
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NR, bool kGather>
-static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages, int batch,
-                                int groups, const DecodeParams& prm, cudaStream_t stream) {
+template <int NR, bool kGather, bool kItems>
+static cudaError_t launch_split_t(const void* q, const void* kv, int64_t num_pages, int batch,
+                                int groups, int num_ctas, const DecodeParams& prm,
+                                cudaStream_t stream) {
   using C = Cfg<NR>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_kernel<NR, kGather>,
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_kernel<NR, kGather, kItems>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
@@ -988,10 +1002,23 @@ static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages
       !make_map(&q_lat, q, q_rows, 128, NR, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&q_rope, q, q_rows, 64, NR, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  dim3 grid(batch, prm.max_splits * groups);
-  mla_split_kv_kernel<NR, kGather><<<grid, C::kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
+  const dim3 grid = kItems ? dim3(num_ctas) : dim3(batch, prm.max_splits * groups);
+  mla_split_kv_kernel<NR, kGather, kItems><<<grid, C::kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
                                                                      q_rope, prm);
   return cudaGetLastError();
+}
+
+template <int NR, bool kGather>
+static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages, int batch,
+                                int groups, int num_ctas, const DecodeParams& prm,
+                                cudaStream_t stream) {
+  // The item-list mapping is its own instantiation, so the grid variant's
+  // code is exactly what it is without it.
+  return prm.cta_items
+             ? launch_split_t<NR, kGather, true>(q, kv, num_pages, batch, groups, num_ctas, prm,
+                                                 stream)
+             : launch_split_t<NR, kGather, false>(q, kv, num_pages, batch, groups, num_ctas, prm,
+                                                  stream);
 }
 
 // The merge is launched as a programmatic dependent of whatever precedes it
@@ -1053,6 +1080,7 @@ struct DecodeLaunch {
   int batch;
   int kv_split;
   int max_splits;
+  int num_ctas;  // length of prm.cta_items (0 without an item list)
 };
 
 static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
@@ -1141,6 +1169,9 @@ static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
   prm.kv_bounds = nullptr;
   prm.block_idx = nullptr;
   prm.topk = 0;
+  prm.cta_items = nullptr;
+  prm.batch = batch;
+  dl->num_ctas = 0;
   {
     const long long w = g_wait_cycles.load();
     prm.wait_cycles = w > 0 ? w : kWaitLimitCycles;
@@ -1168,6 +1199,35 @@ static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
   return MLA_OK;
 }
 
+// Options of mla_decode_ex / mla_decode_sparse (NULL = none).
+static int apply_options(const mla_decode_options_t* o, const char* who, DecodeLaunch* dl) {
+  if (!o) return MLA_OK;
+  const std::string w(who);
+  if (!std::isfinite(o->output_scale)) {
+    set_error(w + ": output_scale must be finite");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (o->cta_items) {
+    const int64_t cap = static_cast<int64_t>(dl->batch) * dl->max_splits * dl->rg.groups;
+    if (o->num_ctas < 1 || o->num_ctas > cap) {
+      set_error(w + ": num_ctas must be in [1, batch * max_splits * row groups]");
+      return MLA_ERR_INVALID_ARG;
+    }
+  }
+  dl->prm.q_scale_dev = o->q_scale_dev;
+  dl->prm.kv_scale_dev = o->kv_scale_dev;
+  dl->prm.sm_scale_dev = o->softmax_scale_dev;
+  dl->prm.output_scale = o->output_scale;
+  dl->prm.sinks = o->sinks;
+  dl->prm.query_lens = o->query_lens;
+  dl->prm.kv_bounds = o->kv_bounds;
+  dl->prm.cta_items = o->cta_items;
+  dl->num_ctas = o->cta_items ? o->num_ctas : 0;
+  dl->mp.output_scale = o->output_scale;
+  dl->mp.sinks = o->sinks;
+  return MLA_OK;
+}
+
 static int launch_decode_split(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
                                const DecodeLaunch& dl, cudaStream_t st) {
   cudaError_t e;
@@ -1176,16 +1236,16 @@ static int launch_decode_split(const void* q_fp8, const void* kv_pages_fp8, int6
   const bool gather = dl.prm.kv_bounds != nullptr || dl.prm.block_idx != nullptr;
   switch (dl.rg.nr) {
     case 16:
-      e = gather ? launch_split<16, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st)
-                 : launch_split<16, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st);
+      e = gather ? launch_split<16, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.num_ctas, dl.prm, st)
+                 : launch_split<16, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.num_ctas, dl.prm, st);
       break;
     case 32:
-      e = gather ? launch_split<32, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st)
-                 : launch_split<32, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st);
+      e = gather ? launch_split<32, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.num_ctas, dl.prm, st)
+                 : launch_split<32, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.num_ctas, dl.prm, st);
       break;
     case 48:
-      e = gather ? launch_split<48, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st)
-                 : launch_split<48, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.prm, st);
+      e = gather ? launch_split<48, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.num_ctas, dl.prm, st)
+                 : launch_split<48, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.num_ctas, dl.prm, st);
       break;
     default:
       set_error("mla_decode: internal row grouping error");
@@ -1236,21 +1296,8 @@ extern "C" int mla_decode_ex(const void* q_fp8, const void* kv_pages_fp8, int64_
   DecodeLaunch dl;
   int rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode_ex", &dl);
   if (rc != MLA_OK) return rc;
-  if (options) {
-    if (!std::isfinite(options->output_scale)) {
-      set_error("mla_decode_ex: output_scale must be finite");
-      return MLA_ERR_INVALID_ARG;
-    }
-    dl.prm.q_scale_dev = options->q_scale_dev;
-    dl.prm.kv_scale_dev = options->kv_scale_dev;
-    dl.prm.sm_scale_dev = options->softmax_scale_dev;
-    dl.prm.output_scale = options->output_scale;
-    dl.prm.sinks = options->sinks;
-    dl.prm.query_lens = options->query_lens;
-    dl.prm.kv_bounds = options->kv_bounds;
-    dl.mp.output_scale = options->output_scale;
-    dl.mp.sinks = options->sinks;
-  }
+  rc = apply_options(options, "mla_decode_ex", &dl);
+  if (rc != MLA_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
   if (rc != MLA_OK) return rc;
@@ -1280,21 +1327,8 @@ extern "C" int mla_decode_sparse(const void* q_fp8, const void* kv_pages_fp8, in
   if (rc != MLA_OK) return rc;
   dl.prm.block_idx = block_idx;
   dl.prm.topk = topk;
-  if (options) {
-    if (!std::isfinite(options->output_scale)) {
-      set_error("mla_decode_sparse: output_scale must be finite");
-      return MLA_ERR_INVALID_ARG;
-    }
-    dl.prm.q_scale_dev = options->q_scale_dev;
-    dl.prm.kv_scale_dev = options->kv_scale_dev;
-    dl.prm.sm_scale_dev = options->softmax_scale_dev;
-    dl.prm.output_scale = options->output_scale;
-    dl.prm.sinks = options->sinks;
-    dl.prm.query_lens = options->query_lens;
-    dl.prm.kv_bounds = options->kv_bounds;
-    dl.mp.output_scale = options->output_scale;
-    dl.mp.sinks = options->sinks;
-  }
+  rc = apply_options(options, "mla_decode_sparse", &dl);
+  if (rc != MLA_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
   if (rc != MLA_OK) return rc;

@@ -51,6 +51,10 @@ struct DecodeParams {
   const int32_t* kv_bounds;
   const int32_t* block_idx;
   int32_t topk;
+  // Optional CTA item list (mla_decode_plan_items): CTA i works on item
+  // cta_items[i] of a 1-D grid; NULL = the (batch, splits x groups) grid.
+  const int32_t* cta_items;
+  int32_t batch;
   long long wait_cycles;   // limit of the pipeline waits (drains always use the long limit)
   int* status;
   float* ws_ml;

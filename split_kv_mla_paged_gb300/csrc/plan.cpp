@@ -142,3 +142,47 @@ extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t nu
   *workspace_bytes_out = mla_decode_workspace_size(batch, q_len, num_heads, max_splits);
   return MLA_OK;
 }
+
+extern "C" int mla_decode_plan_items(const int32_t* splits, int32_t batch, int32_t num_heads,
+                                     int32_t q_len, int32_t* items_out, int32_t capacity,
+                                     int32_t* n_items_out) {
+  if (!splits || !n_items_out) {
+    set_error("mla_decode_plan_items: null pointer argument");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (batch < 1 || num_heads < 1 || q_len < 1 || batch > MLA_ITEM_MAX_BATCH) {
+    set_error("mla_decode_plan_items: batch in [1, MLA_ITEM_MAX_BATCH], num_heads, q_len >= 1");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (static_cast<int64_t>(num_heads) * q_len > MLA_MAX_ROWS) {
+    set_error("mla_decode_plan_items: num_heads * q_len exceeds MLA_MAX_ROWS");
+    return MLA_ERR_UNSUPPORTED;
+  }
+  const RowGroups rg = row_groups(num_heads * q_len);
+  int32_t max_splits = 0;
+  int64_t total = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (splits[b] < 1 || splits[b] > MLA_MAX_SPLITS) {
+      set_error("mla_decode_plan_items: splits[" + std::to_string(b) + "] out of range");
+      return MLA_ERR_INVALID_ARG;
+    }
+    max_splits = std::max(max_splits, splits[b]);
+    total += static_cast<int64_t>(splits[b]) * rg.groups;
+  }
+  *n_items_out = static_cast<int32_t>(total);
+  if (!items_out) return MLA_OK;  // size query
+  if (capacity < total) {
+    set_error("mla_decode_plan_items: capacity " + std::to_string(capacity) + " below the " +
+              std::to_string(total) + " items");
+    return MLA_ERR_INVALID_ARG;
+  }
+  // Split-major: every request's split s before anyone's split s + 1; the row
+  // groups of one split are adjacent.
+  int64_t k = 0;
+  for (int32_t s = 0; s < max_splits; ++s)
+    for (int b = 0; b < batch; ++b)
+      if (s < splits[b])
+        for (int g = 0; g < rg.groups; ++g)
+          items_out[k++] = (b << MLA_ITEM_B_SHIFT) | (s << MLA_ITEM_S_SHIFT) | g;
+  return MLA_OK;
+}

@@ -242,3 +242,47 @@ def test_full_size_sampled_rows(name, nrows):
         assert (lse2 - lse).abs().max().item() <= PLAN_ABS
     del inp
     torch.cuda.empty_cache()
+
+
+def test_item_list_matches_the_grid_launch():
+    # A skewed batch: the item list launches only the CTAs with work; the
+    # results are the same numbers as the full grid's.
+    lens = [9000, 300, 129, 2000, 4100]
+    inp = decode_inputs(5, 12, 8, lens, seed=23, extra_pages=1)
+    for target in (0, 40):
+        plan = (mla.mla_decode_plan(lens, 12, 8, target_ctas=target) if target
+                else mla.mla_decode_plan(lens, 12, 8, sm_count=152))
+        assert np.any(plan.splits < plan.max_splits)
+        dev = torch.device("cuda")
+        kw = dict(num_heads=12, q_len=8, causal=True, softmax_scale=SOFTMAX_SCALE, plan=plan,
+                  want_f32=True)
+        out_i, lse_i, o32_i = mla.decode(inp.q.to(dev), inp.kv.to(dev), inp.page_table.to(dev),
+                                         inp.kv_lens, use_items=True, **kw)
+        out_g, lse_g, o32_g = mla.decode(inp.q.to(dev), inp.kv.to(dev), inp.page_table.to(dev),
+                                         inp.kv_lens, use_items=False, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(o32_i, o32_g) and torch.equal(lse_i, lse_g)
+        ref_o, ref_l = oracle.decode_rows(inp.q, inp.kv.cpu(), inp.page_table.cpu(), inp.kv_lens,
+                                          q_len=8, num_heads=12, causal=True,
+                                          softmax_scale=SOFTMAX_SCALE)
+        assert_parity(out_i, lse_i, ref_o, ref_l)
+
+
+def test_bad_item_is_reported():
+    inp = decode_inputs(2, 12, 1, [3000, 300], seed=24)
+    dev = torch.device("cuda")
+    plan = mla.mla_decode_plan([3000, 300], 12, 1, target_ctas=6)
+    items = torch.from_numpy(mla.mla_decode_plan_items(plan.splits, 12, 1)).to(dev)
+    items[1] = (7 << 14)  # request 7 of a batch of 2
+    ws_bytes = mla.mla_decode_workspace_size(2, 1, 12, plan.max_splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    mla.mla_decode_workspace_init(ws, ws_bytes)
+    out = torch.empty((2, 1, 12, 512), dtype=torch.bfloat16, device=dev)
+    lens = torch.tensor([3000, 300], dtype=torch.int32, device=dev)
+    mla.mla_decode_ex(inp.q.to(dev), inp.kv.to(dev), inp.num_pages, inp.page_table.to(dev),
+                      inp.max_pages, lens, torch.from_numpy(plan.splits).to(dev),
+                      torch.from_numpy(plan.chunks).to(dev), plan.max_splits, plan.kv_split, 2, 1,
+                      12, False, 1.0, 1.0, SOFTMAX_SCALE, ws, ws_bytes, out, cta_items=items)
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_status(ws)
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG

@@ -99,3 +99,29 @@ def test_plan_rejects_too_many_rows():
 def test_plan_needs_sm_count_without_target():
     with pytest.raises(mla.MlaError):
         mla.mla_decode_plan([4096], num_heads=12, q_len=1, sm_count=0, target_ctas=0)
+
+
+def test_plan_items_are_the_ctas_with_work_in_split_major_order():
+    splits = np.array([3, 1, 2], dtype=np.int32)
+    for H, q, groups in ((12, 1, 1), (12, 8, 2), (96, 8, 16)):
+        items = mla.mla_decode_plan_items(splits, H, q)
+        assert items.shape[0] == int(splits.sum()) * groups
+        b = items >> 14
+        s = (items >> 5) & 511
+        g = items & 31
+        # every (request, split < splits[b], group) exactly once
+        got = sorted(zip(b.tolist(), s.tolist(), g.tolist()))
+        want = sorted((bb, ss, gg) for bb in range(3) for ss in range(int(splits[bb]))
+                      for gg in range(groups))
+        assert got == want
+        # split-major, row groups adjacent
+        assert np.all(np.diff(s) >= 0)
+        key = s * 1000 + b
+        assert np.all(np.diff(key) >= 0)
+
+
+def test_plan_items_rejects_bad_splits():
+    with pytest.raises(mla.MlaError):
+        mla.mla_decode_plan_items([2, 0], 12, 1)
+    with pytest.raises(mla.MlaError):
+        mla.mla_decode_plan_items([2, mla.MAX_SPLITS + 1], 12, 1)

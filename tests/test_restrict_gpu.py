@@ -199,3 +199,11 @@ def test_sparse_full_size_sampled_rows():
     assert torch.isfinite(o32).all()
     del inp
     torch.cuda.empty_cache()
+
+
+def test_sparse_with_item_list():
+    lens = [6000, 200, 3000]
+    inp = decode_inputs(3, 12, 1, lens, seed=470)
+    sel = page_selection(lens, 24, seed=471, keep_last=False)
+    plan = mla.mla_decode_plan([PAGE_SIZE * 24] * 3, 12, 1, target_ctas=30)
+    _check(inp, False, dict(block_idx=sel), run_kw=dict(block_idx=sel, use_items=True), plan=plan)
