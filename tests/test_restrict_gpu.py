@@ -207,3 +207,40 @@ def test_sparse_with_item_list():
     sel = page_selection(lens, 24, seed=471, keep_last=False)
     plan = mla.mla_decode_plan([PAGE_SIZE * 24] * 3, 12, 1, target_ctas=30)
     _check(inp, False, dict(block_idx=sel), run_kw=dict(block_idx=sel, use_items=True), plan=plan)
+
+
+def test_graph_replay_picks_up_new_selection():
+    # The selection is a device input: a captured sparse decode reads the new
+    # pages on every replay (the block selector runs before it each step).
+    lens = [7000, 4000]
+    inp = decode_inputs(2, 12, 1, lens, seed=480)
+    dev = torch.device("cuda")
+    topk = 20
+    plan = mla.mla_decode_plan([PAGE_SIZE * topk] * 2, 12, 1, sm_count=152)
+    sel_d = torch.from_numpy(page_selection(lens, topk, seed=481)).to(dev)
+    q, kv, pt = inp.q.to(dev), inp.kv.to(dev), inp.page_table.to(dev)
+    lens_d = inp.kv_lens.to(dev)
+    ws_bytes = plan.workspace_bytes
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    mla.mla_decode_workspace_init(ws, ws_bytes)
+    out = torch.empty((2, 1, 12, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((2, 1, 12), dtype=torch.float32, device=dev)
+    args = (q, kv, inp.num_pages, pt, inp.max_pages, lens_d, sel_d, topk,
+            torch.from_numpy(plan.splits).to(dev), torch.from_numpy(plan.chunks).to(dev),
+            plan.max_splits, plan.kv_split, 2, 1, 12, False, 1.0, 1.0, SOFTMAX_SCALE, ws,
+            ws_bytes, out, lse, None)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        mla.mla_decode_sparse(*args, stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        mla.mla_decode_sparse(*args)
+    for s in (481, 482, 483):
+        sel = page_selection(lens, topk, seed=s)
+        sel_d.copy_(torch.from_numpy(sel))
+        g.replay()
+        torch.cuda.synchronize()
+        ref_o, ref_l = _oracle(inp, False, block_idx=sel)
+        assert_parity(out, lse, ref_o, ref_l, what=f"selection {s}")
+    mla.mla_decode_status(ws, stream)
