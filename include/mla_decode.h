@@ -285,6 +285,18 @@ MLA_API int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64
                             void* workspace, size_t workspace_bytes, void* out_bf16,
                             float* lse_f32, float* out_f32_debug, void* stream);
 
+/* mla_decode_bf16 with options (NULL options = mla_decode_bf16): output_scale,
+ * sinks, query_lens and softmax_scale_dev as for mla_decode_ex.  q_scale_dev,
+ * kv_scale_dev, kv_bounds and cta_items are FP8-only: MLA_ERR_UNSUPPORTED. */
+MLA_API int mla_decode_bf16_ex(const void* q_bf16, const void* kv_pages_bf16, int64_t num_pages,
+                               const int32_t* page_table, int32_t max_pages_per_req,
+                               const int32_t* kv_lens, const int32_t* splits,
+                               const int32_t* chunks, int32_t max_splits, int32_t kv_split,
+                               int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
+                               float softmax_scale, void* workspace, size_t workspace_bytes,
+                               void* out_bf16, float* lse_f32, float* out_f32_debug,
+                               const mla_decode_options_t* options, void* stream);
+
 /* Zero the 256-byte status header of a new workspace (async on `stream`).
  * Call once per workspace before its first mla_decode; after that the
  * header only changes when the device reports a condition, and

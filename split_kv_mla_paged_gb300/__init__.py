@@ -23,7 +23,8 @@ __all__ = [
     "mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init", "mla_decode",
     "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
     "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16",
-    "mla_decode_sparse", "mla_decode_plan_items", "DecodeOptions", "decode", "merge",
+    "mla_decode_sparse", "mla_decode_plan_items", "mla_decode_bf16_ex", "DecodeOptions",
+    "decode", "merge",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -41,7 +42,7 @@ EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_
                     "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
                     "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit",
                     "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16",
-                    "mla_decode_sparse", "mla_decode_plan_items")
+                    "mla_decode_sparse", "mla_decode_plan_items", "mla_decode_bf16_ex")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
@@ -106,6 +107,9 @@ def load_library() -> ctypes.CDLL:
                                           + [ctypes.POINTER(DecodeOptions), vp])
         lib.mla_decode_bf16.restype = ctypes.c_int
         lib.mla_decode_bf16.argtypes = dec_args[:14] + [f32] + dec_args[17:]
+        lib.mla_decode_bf16_ex.restype = ctypes.c_int
+        lib.mla_decode_bf16_ex.argtypes = (dec_args[:14] + [f32] + dec_args[17:-1]
+                                           + [ctypes.POINTER(DecodeOptions), vp])
         lib.mla_decode_workspace_init.restype = ctypes.c_int
         lib.mla_decode_workspace_init.argtypes = [vp, sz, vp]
         lib.mla_merge.restype = ctypes.c_int
@@ -259,6 +263,25 @@ def mla_decode_bf16(q_bf16, kv_pages_bf16, num_pages: int, page_table, max_pages
                                _stream_handle(stream)))
 
 
+def mla_decode_bf16_ex(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_per_req, kv_lens,
+                       splits, chunks, max_splits, kv_split, batch, q_len, num_heads, causal,
+                       softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32=None,
+                       out_f32_debug=None, *, softmax_scale_dev=None, output_scale: float = 1.0,
+                       sinks=None, query_lens=None, stream=None) -> None:
+    """mla_decode_bf16 with a device softmax scale, output scale, sinks and
+    ragged query counts."""
+    opts = DecodeOptions(None, None, _ptr(softmax_scale_dev), float(output_scale), _ptr(sinks),
+                         _ptr(query_lens), None, None, 0)
+    lib = load_library()
+    _check(lib.mla_decode_bf16_ex(_ptr(q_bf16), _ptr(kv_pages_bf16), int(num_pages),
+                                  _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),
+                                  _ptr(splits), _ptr(chunks), int(max_splits), int(kv_split),
+                                  int(batch), int(q_len), int(num_heads), 1 if causal else 0,
+                                  float(softmax_scale), _ptr(workspace), int(workspace_bytes),
+                                  _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
+                                  ctypes.byref(opts), _stream_handle(stream)))
+
+
 def mla_decode_sparse(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req, kv_lens,
                       block_idx, topk, splits, chunks, max_splits, kv_split, batch, q_len,
                       num_heads, causal, q_scale, kv_scale, softmax_scale, workspace,
@@ -406,11 +429,22 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
     if use_items and q_fp8.dtype != torch.bfloat16:
         items_d = torch.from_numpy(mla_decode_plan_items(plan.splits, num_heads, q_len)).to(dev)
     if q_fp8.dtype == torch.bfloat16:
-        if (kv_pages_fp8.dtype != torch.bfloat16 or sinks is not None or output_scale != 1.0
-                or device_scales or q_scale != 1.0 or kv_scale != 1.0 or restricted):
-            raise ValueError("BF16 decode takes BF16 q and kv and no scales, sinks, output "
-                             "scale or key restrictions")
-        mla_decode_bf16(*common, softmax_scale, ws, ws_bytes, out, lse, out_f32, stream)
+        if (kv_pages_fp8.dtype != torch.bfloat16 or q_scale != 1.0 or kv_scale != 1.0
+                or kv_bounds is not None or block_idx is not None):
+            raise ValueError("BF16 decode takes BF16 q and kv, no q/kv scales and no key "
+                             "windows or page selections")
+        if sinks is None and output_scale == 1.0 and not device_scales and query_lens is None:
+            mla_decode_bf16(*common, softmax_scale, ws, ws_bytes, out, lse, out_f32, stream)
+        else:
+            sm_d = (torch.tensor([softmax_scale], dtype=torch.float32, device=dev)
+                    if device_scales else None)
+            sk = None if sinks is None else torch.as_tensor(sinks, dtype=torch.float32).to(dev)
+            ql = (None if query_lens is None
+                  else torch.as_tensor(query_lens, dtype=torch.int32).to(dev).contiguous())
+            # With a device scale the host value is a placeholder the kernel must ignore.
+            mla_decode_bf16_ex(*common, 99.0 if device_scales else softmax_scale, ws, ws_bytes,
+                               out, lse, out_f32, softmax_scale_dev=sm_d,
+                               output_scale=output_scale, sinks=sk, query_lens=ql, stream=stream)
     elif (sinks is None and output_scale == 1.0 and not device_scales and not restricted
           and items_d is None):
         mla_decode(*common, q_scale, kv_scale, softmax_scale, ws, ws_bytes, out, lse, out_f32,

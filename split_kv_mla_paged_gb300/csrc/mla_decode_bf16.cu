@@ -131,8 +131,10 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
   const int nsplit = p.splits[b];
   const int chunk = p.chunks[b];
   if (split >= nsplit) return;
+  const int q_b = p.query_lens ? p.query_lens[b] : p.q_len;  // this request's query tokens
   {
-    const bool bad = L < 1 || (p.causal && L < p.q_len) || nsplit > p.max_splits ||
+    const bool bad = L < 1 || q_b < 1 || q_b > p.q_len || (p.causal && L < q_b) ||
+                     nsplit > p.max_splits ||
                      chunk < MLA_TILE_TOKENS || (chunk % MLA_TILE_TOKENS) != 0 ||
                      static_cast<int64_t>(nsplit) * chunk < L ||
                      static_cast<int64_t>(nsplit - 1) * chunk >= L ||
@@ -144,10 +146,15 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
   }
   const int tok_begin = split * chunk;
   const int tok_end = min(L, tok_begin + chunk);
-  const int n_tiles = (tok_end - tok_begin + kTokB - 1) / kTokB;
-  const float c_log2 = p.c_log2;
+  const float c_log2 =
+      p.sm_scale_dev ? *p.sm_scale_dev * 1.4426950408889634f : p.c_log2;
   const int row0 = grp * p.rows_per_group;
   const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
+  // Rows of real query tokens (the others are padding slots of a shorter
+  // query block: no key is visible to them).
+  const int rows_valid = max(0, min(rows_here, q_b * p.num_heads - row0));
+  const int n_tiles =
+      rows_valid > 0 ? (tok_end - tok_begin + kTokB - 1) / kTokB : 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -399,9 +406,9 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
     for (int k = 0; k < NRH; ++k) kreg[k] = -INFINITY;
     const float c = c_log2;
     const int qi_first = row0 / p.num_heads;
-    const int lim_min = p.causal ? min(tok_end, L - p.q_len + qi_first + 1) : tok_end;
+    const int lim_min = p.causal ? min(tok_end, L - q_b + qi_first + 1) : tok_end;
     const int my_row0 = row0 + rbase;
-    const int my_rows = max(0, min(NRH, rows_here - rbase));
+    const int my_rows = max(0, min(NRH, rows_valid - rbase));
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
       const int sb = i & 1;
@@ -435,7 +442,7 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
         int h = my_row0 - qi * p.num_heads;
 #pragma unroll
         for (int k = 0; k < NRH; ++k) {
-          const int lim = p.causal ? min(tok_end, L - p.q_len + qi + 1) : tok_end;
+          const int lim = p.causal ? min(tok_end, L - q_b + qi + 1) : tok_end;
           t[k] = (has_tok && k < my_rows && j < lim) ? t[k] * c : -INFINITY;
           if (++h == p.num_heads) {
             h = 0;
@@ -544,9 +551,16 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
       float sc = 0.0f;
       if (sid < rows_here) {
         if (single) {
-          const float ls = (l_row > 0.0f) ? 0.6931471805599453f * (m_s + log2f(l_row)) : -INFINITY;
-          if (p.lse) p.lse[grow] = ls;
-          sc = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
+          // A sink is one more (zero-valued) key: it joins the denominator.
+          const float sink2 = p.sinks
+                                  ? p.sinks[(row0 + sid) % p.num_heads] * 1.4426950408889634f
+                                  : -INFINITY;
+          const float mm = fmaxf(l_row > 0.0f ? m_s : -INFINITY, sink2);
+          const float a = (l_row > 0.0f) ? exp2f(m_s - mm) : 0.0f;
+          const float den = l_row * a + (sink2 == -INFINITY ? 0.0f : exp2f(sink2 - mm));
+          if (p.lse)
+            p.lse[grow] = (den > 0.0f) ? 0.6931471805599453f * (mm + log2f(den)) : -INFINITY;
+          sc = (den > 0.0f) ? p.output_scale * a / den : 0.0f;
         } else {
           float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
           ml[0] = m_s;
@@ -584,6 +598,16 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
               }
             }
           }
+        }
+      }
+    } else if (ok && fin && n_tiles == 0 && single) {
+      // Only padding query slots here: O = 0 (partials need only (-inf, 0)).
+      for (int d = 0; d < 4; ++d) {
+        const int dim = d * 128 + dim_lane;
+        for (int row = rbase; row < min(rows_here, rbase + NRH); ++row) {
+          const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
+          p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(0.0f);
+          if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = 0.0f;
         }
       }
     }
@@ -647,8 +671,10 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
   const int nsplit = p.splits[b];
   const int chunk = p.chunks[b];
   if (split >= nsplit) return;
+  const int q_b = p.query_lens ? p.query_lens[b] : p.q_len;  // this request's query tokens
   {
-    const bool bad = L < 1 || (p.causal && L < p.q_len) || nsplit > p.max_splits ||
+    const bool bad = L < 1 || q_b < 1 || q_b > p.q_len || (p.causal && L < q_b) ||
+                     nsplit > p.max_splits ||
                      chunk < MLA_TILE_TOKENS || (chunk % MLA_TILE_TOKENS) != 0 ||
                      static_cast<int64_t>(nsplit) * chunk < L ||
                      static_cast<int64_t>(nsplit - 1) * chunk >= L ||
@@ -660,10 +686,15 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
   }
   const int tok_begin = split * chunk;
   const int tok_end = min(L, tok_begin + chunk);
-  const int n_tiles = (tok_end - tok_begin + kTokB - 1) / kTokB;
-  const float c_log2 = p.c_log2;
+  const float c_log2 =
+      p.sm_scale_dev ? *p.sm_scale_dev * 1.4426950408889634f : p.c_log2;
   const int row0 = grp * p.rows_per_group;
   const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
+  // Rows of real query tokens (the others are padding slots of a shorter
+  // query block: no key is visible to them).
+  const int rows_valid = max(0, min(rows_here, q_b * p.num_heads - row0));
+  const int n_tiles =
+      rows_valid > 0 ? (tok_end - tok_begin + kTokB - 1) / kTokB : 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -919,8 +950,8 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
     float kreg = -INFINITY;   // this thread's row reference
     const float c = c_log2;
     const int qi = (row0 + row) / p.num_heads;
-    const bool row_ok = row < rows_here;
-    const int lim = p.causal ? min(tok_end, L - p.q_len + qi + 1) : tok_end;
+    const bool row_ok = row < rows_valid;
+    const int lim = p.causal ? min(tok_end, L - q_b + qi + 1) : tok_end;
     for (int i = 0; i < n_tiles; ++i) {
       const int sb = i & 1;
       const int use = i >> 1;
@@ -1037,9 +1068,16 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
       float sc = 0.0f;
       if (sid < rows_here) {
         if (single) {
-          const float ls = (l_row > 0.0f) ? 0.6931471805599453f * (m_s + log2f(l_row)) : -INFINITY;
-          if (p.lse) p.lse[grow] = ls;
-          sc = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
+          // A sink is one more (zero-valued) key: it joins the denominator.
+          const float sink2 = p.sinks
+                                  ? p.sinks[(row0 + sid) % p.num_heads] * 1.4426950408889634f
+                                  : -INFINITY;
+          const float mm = fmaxf(l_row > 0.0f ? m_s : -INFINITY, sink2);
+          const float a = (l_row > 0.0f) ? exp2f(m_s - mm) : 0.0f;
+          const float den = l_row * a + (sink2 == -INFINITY ? 0.0f : exp2f(sink2 - mm));
+          if (p.lse)
+            p.lse[grow] = (den > 0.0f) ? 0.6931471805599453f * (mm + log2f(den)) : -INFINITY;
+          sc = (den > 0.0f) ? p.output_scale * a / den : 0.0f;
         } else {
           float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
           ml[0] = m_s;
@@ -1073,6 +1111,16 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
               p.ws_o[(grow * p.max_splits + split) * MLA_LATENT_DIM + dim] = v;
             }
           }
+        }
+      }
+    } else if (ok && fin && n_tiles == 0 && single) {
+      // Only padding query slots here: O = 0 (partials need only (-inf, 0)).
+      for (int d = 0; d < 4; ++d) {
+        const int dim = d * 128 + lidx;
+        for (int k = 0; k < rows_here; ++k) {
+          const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + k;
+          p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(0.0f);
+          if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = 0.0f;
         }
       }
     }
@@ -1147,49 +1195,50 @@ static cudaError_t launch_split_bf16_q16(const void* q, const void* kv, int64_t 
 
 using namespace mla;
 
-extern "C" int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t num_pages,
-                               const int32_t* page_table, int32_t max_pages_per_req,
-                               const int32_t* kv_lens, const int32_t* splits,
-                               const int32_t* chunks, int32_t max_splits, int32_t kv_split,
-                               int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
-                               float softmax_scale, void* workspace, size_t workspace_bytes,
-                               void* out_bf16, float* lse_f32, float* out_f32_debug,
-                               void* stream) {
+static int decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t num_pages,
+                       const int32_t* page_table, int32_t max_pages_per_req,
+                       const int32_t* kv_lens, const int32_t* splits, const int32_t* chunks,
+                       int32_t max_splits, int32_t kv_split, int32_t batch, int32_t q_len,
+                       int32_t num_heads, int32_t causal, float softmax_scale, void* workspace,
+                       size_t workspace_bytes, void* out_bf16, float* lse_f32,
+                       float* out_f32_debug, const mla_decode_options_t* options,
+                       void* stream) {
+  const std::string who = options ? "mla_decode_bf16_ex" : "mla_decode_bf16";
   if (!q_bf16 || !kv_pages_bf16 || !page_table || !kv_lens || !splits || !chunks || !workspace ||
       !out_bf16) {
-    set_error("mla_decode_bf16: null pointer argument");
+    set_error(who + ": null pointer argument");
     return MLA_ERR_INVALID_ARG;
   }
   if (batch < 1 || q_len < 1 || num_heads < 1 || max_pages_per_req < 1 || num_pages < 1) {
-    set_error("mla_decode_bf16: batch, q_len, num_heads, max_pages_per_req and num_pages must be >= 1");
+    set_error(who + ": batch, q_len, num_heads, max_pages_per_req and num_pages must be >= 1");
     return MLA_ERR_INVALID_ARG;
   }
   if (static_cast<int64_t>(num_heads) * q_len > MLA_MAX_ROWS || batch > 65535) {
-    set_error("mla_decode_bf16: num_heads * q_len above MLA_MAX_ROWS or batch above 65535");
+    set_error(who + ": num_heads * q_len above MLA_MAX_ROWS or batch above 65535");
     return MLA_ERR_UNSUPPORTED;
   }
   if (num_pages * MLA_PAGE_SIZE > INT32_MAX) {
-    set_error("mla_decode_bf16: page pool too large for 32-bit TMA row coordinates");
+    set_error(who + ": page pool too large for 32-bit TMA row coordinates");
     return MLA_ERR_UNSUPPORTED;
   }
   if (max_splits < 1 || max_splits > MLA_MAX_SPLITS ||
       (kv_split != 1 && kv_split != 2 && kv_split != 4 && kv_split != 8 && kv_split != 16)) {
-    set_error("mla_decode_bf16: max_splits in [1, MLA_MAX_SPLITS], kv_split in {1,2,4,8,16}");
+    set_error(who + ": max_splits in [1, MLA_MAX_SPLITS], kv_split in {1,2,4,8,16}");
     return MLA_ERR_INVALID_ARG;
   }
   if (!aligned(q_bf16, 16) || !aligned(kv_pages_bf16, 16) || !aligned(workspace, 256) ||
       !aligned(out_bf16, 8) || (out_f32_debug && !aligned(out_f32_debug, 16))) {
-    set_error("mla_decode_bf16: q/kv need 16-byte, workspace 256-byte, outputs 8/16-byte alignment");
+    set_error(who + ": q/kv need 16-byte, workspace 256-byte, outputs 8/16-byte alignment");
     return MLA_ERR_INVALID_ARG;
   }
   if (!std::isfinite(softmax_scale)) {
-    set_error("mla_decode_bf16: softmax_scale must be finite");
+    set_error(who + ": softmax_scale must be finite");
     return MLA_ERR_INVALID_ARG;
   }
   const int64_t rows_total = static_cast<int64_t>(batch) * q_len * num_heads;
   const size_t need = ws_total(rows_total, max_splits);
   if (workspace_bytes < need) {
-    set_error("mla_decode_bf16: workspace of " + std::to_string(workspace_bytes) +
+    set_error(who + ": workspace of " + std::to_string(workspace_bytes) +
               " bytes is below the " + std::to_string(need) + " required");
     return MLA_ERR_WORKSPACE_TOO_SMALL;
   }
@@ -1221,6 +1270,21 @@ extern "C" int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, in
   prm.out = reinterpret_cast<__nv_bfloat16*>(out_bf16);
   prm.lse = lse_f32;
   prm.out_f32 = out_f32_debug;
+  if (options) {
+    if (!std::isfinite(options->output_scale)) {
+      set_error("mla_decode_bf16_ex: output_scale must be finite");
+      return MLA_ERR_INVALID_ARG;
+    }
+    if (options->q_scale_dev || options->kv_scale_dev || options->kv_bounds ||
+        options->cta_items) {
+      set_error("mla_decode_bf16_ex: q/kv scales, key windows and item lists are FP8-only");
+      return MLA_ERR_UNSUPPORTED;
+    }
+    prm.sm_scale_dev = options->softmax_scale_dev;
+    prm.output_scale = options->output_scale;
+    prm.sinks = options->sinks;
+    prm.query_lens = options->query_lens;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (rg.nr) {
@@ -1230,7 +1294,7 @@ extern "C" int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, in
     case 32: e = launch_split_bf16<32>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
     case 48: e = launch_split_bf16<48>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
     default:
-      set_error("mla_decode_bf16: internal row grouping error");
+      set_error(who + ": internal row grouping error");
       return MLA_ERR_UNSUPPORTED;
   }
   if (e != cudaSuccess) return cuda_fail("mla_decode_bf16: split-KV launch", e);
@@ -1244,8 +1308,8 @@ extern "C" int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, in
     mp.splits = splits;
     mp.rows_per_req = num_heads * q_len;
     mp.num_heads = num_heads;
-    mp.output_scale = 1.0f;
-    mp.sinks = nullptr;
+    mp.output_scale = prm.output_scale;
+    mp.sinks = prm.sinks;
     mp.out = prm.out;
     mp.lse = lse_f32;
     mp.out_f32 = out_f32_debug;
@@ -1253,4 +1317,33 @@ extern "C" int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, in
     if (e != cudaSuccess) return cuda_fail("mla_decode_bf16: merge launch", e);
   }
   return MLA_OK;
+}
+
+extern "C" int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t num_pages,
+                               const int32_t* page_table, int32_t max_pages_per_req,
+                               const int32_t* kv_lens, const int32_t* splits,
+                               const int32_t* chunks, int32_t max_splits, int32_t kv_split,
+                               int32_t batch, int32_t q_len, int32_t num_heads, int32_t causal,
+                               float softmax_scale, void* workspace, size_t workspace_bytes,
+                               void* out_bf16, float* lse_f32, float* out_f32_debug,
+                               void* stream) {
+  return decode_bf16(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_per_req, kv_lens,
+                     splits, chunks, max_splits, kv_split, batch, q_len, num_heads, causal,
+                     softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32, out_f32_debug,
+                     nullptr, stream);
+}
+
+extern "C" int mla_decode_bf16_ex(const void* q_bf16, const void* kv_pages_bf16,
+                                  int64_t num_pages, const int32_t* page_table,
+                                  int32_t max_pages_per_req, const int32_t* kv_lens,
+                                  const int32_t* splits, const int32_t* chunks,
+                                  int32_t max_splits, int32_t kv_split, int32_t batch,
+                                  int32_t q_len, int32_t num_heads, int32_t causal,
+                                  float softmax_scale, void* workspace, size_t workspace_bytes,
+                                  void* out_bf16, float* lse_f32, float* out_f32_debug,
+                                  const mla_decode_options_t* options, void* stream) {
+  return decode_bf16(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_per_req, kv_lens,
+                     splits, chunks, max_splits, kv_split, batch, q_len, num_heads, causal,
+                     softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32, out_f32_debug,
+                     options, stream);
 }

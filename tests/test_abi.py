@@ -133,3 +133,11 @@ def test_kv_append_host_checks(lib):
                              None) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_kv_append(fake, 4, fake, fake, fake, 1, 1, fake, 1, 0.0, None,
                              None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_bf16_ex_rejects_fp8_only_options(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    opts = mla.DecodeOptions(None, None, None, 1.0, None, None, fake, None, 0)
+    st = lib.mla_decode_bf16_ex(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 0.1,
+                                fake, 1 << 30, fake, None, None, ctypes.byref(opts), None)
+    assert st == mla.MLA_ERR_UNSUPPORTED and "FP8-only" in mla.mla_last_error()

@@ -105,3 +105,31 @@ def test_bf16_full_size_sampled_rows(name, nrows):
     assert torch.isfinite(o32).all() and torch.isfinite(lse).all()
     del inp
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B,H,q_len,lens,causal", [
+    (2, 12, 1, [3000, 700], False),     # 16-row groups: Q in TMEM
+    (2, 12, 4, [2000, 900], True),      # one 48-row group
+    (2, 12, 8, [1500, 4100], True),     # two 48-row groups
+])
+def test_bf16_options_parity(B, H, q_len, lens, causal):
+    from synth import query_lens_ragged
+    inp = decode_inputs(B, H, q_len, lens, seed=320 + q_len, extra_pages=1, dtype="bf16")
+    sinks = np.linspace(-2.0, 3.0, H)
+    ql = np.asarray(query_lens_ragged(B, q_len, seed=q_len), np.int32) if q_len > 1 else None
+    dev = torch.device("cuda")
+    for target in (0, 1, 9):
+        plan = (mla.mla_decode_plan(lens, H, q_len, target_ctas=target) if target else None)
+        for device_scales in (False, True):
+            out, lse, o32 = mla.decode(inp.q.to(dev), inp.kv.to(dev), inp.page_table.to(dev),
+                                       inp.kv_lens, num_heads=H, q_len=q_len, causal=causal,
+                                       softmax_scale=0.13, plan=plan, want_f32=True,
+                                       sinks=sinks, output_scale=1.7, query_lens=ql,
+                                       device_scales=device_scales)
+            torch.cuda.synchronize()
+            ref_o, ref_l = oracle.decode_rows(inp.q, inp.kv.cpu(), inp.page_table.cpu(),
+                                              inp.kv_lens, q_len=q_len, num_heads=H,
+                                              causal=causal, softmax_scale=0.13, sinks=sinks,
+                                              output_scale=1.7, query_lens=ql)
+            assert_parity(out, lse, ref_o, ref_l, what=f"target {target} dev {device_scales}")
+            assert torch.equal(o32.to(torch.bfloat16), out)
