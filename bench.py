@@ -45,10 +45,14 @@ KERNEL_SOURCES = {
 
 
 def kernel_hash(dtype: str = "e4m3") -> str:
+    """Hash of the kernel sources' code (comments and blank lines excluded)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[dtype]:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -10,14 +10,16 @@
 // a row's partials, a shared-memory combine rescaled by exp2(group max - max),
 // empty groups skipped, weight-0 padded loads.
 //
-// Split-KV kernel design (one CTA per (split, request, row group), one CTA per
+// Split-KV kernel design (one CTA per (request, split, row group), one CTA per
 // SM):
-//  * The MMA is "swapped": tokens are the M = 128 dimension and the query rows
-//    of a request (heads x query tokens, padded to a multiple of 16, at most
-//    96) are N.  S^T[128 tok x NR] = K[128 x 576] Q^T and
-//    O^T[512 x NR] += V^T[512 x 128 tok] P^T, as four M = 128 MMAs over the
-//    latent dims.  With H*q = 12 this does 16 columns of work instead of
-//    padding 12 rows to 128, and S^T plus O^T fit TMEM (NS*NR + 4*NR <= 512).
+//  * The MMA is "swapped": tokens are the M = 128 dimension and a row group of
+//    the request's query rows (heads x query tokens, at most 48 per CTA,
+//    padded to a multiple of 16: NR = 16, 32 or 48) is N.
+//    S^T[128 tok x NR] = K[128 x 576] Q^T and
+//    O^T[512 x 2NR] += V^T[512 x 128 tok] [P_hi | P_lo]^T, as four M = 128
+//    MMAs over the latent dims.  With H*q = 12 this does 16 columns of work
+//    instead of padding 12 rows to 128, and S^T plus O^T fit TMEM
+//    (2*NR + 4*2NR <= 512).
 //  * One TMA-staged copy of each KV tile (4 pages x 576 B x 32 tokens, 128 B
 //    swizzle for the latent blocks, 64 B for the rope block) serves as the K
 //    operand (K-major) and as the V operand (MN-major over the same bytes), so
@@ -28,8 +30,8 @@
 //    power of two, so the E4M3-quantised P fed to the PV MMA, and every
 //    partial, is the same for any split plan up to exact scaling.
 //  * Warp roles: warp 0 issues TMA, warp 1 issues tcgen05.mma (and owns TMEM),
-//    warps 2-5 (one warpgroup, TMEM lane quadrant = warp % 4) run the softmax,
-//    the rare O correction and the epilogue.
+//    warps 2-5 (and 6-9 for 32 and 48 rows; TMEM lane quadrant = warp % 4)
+//    run the softmax, the rare O correction and the epilogue.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

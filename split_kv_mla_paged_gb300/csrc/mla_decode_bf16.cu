@@ -16,6 +16,9 @@
 //    N = rows, K = 16 tokens, 16 instructions per tile.
 //  * Q is BF16 too (kind::f16 takes A and B of one type); there are no q/kv
 //    scales.  Partials have the FP8 kernel's layout, so the merge is shared.
+//  * Row groups of at most 16 rows run a variant with Q in TMEM (see
+//    mla_split_kv_bf16_q16_kernel below); the description above is the
+//    kernel for 32 and 48 rows.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
