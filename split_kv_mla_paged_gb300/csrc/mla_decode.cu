@@ -988,13 +988,11 @@ static cudaError_t launch_split_t(const void* q, const void* kv, int64_t num_pag
                                 int groups, int num_ctas, const DecodeParams& prm,
                                 cudaStream_t stream) {
   using C = Cfg<NR>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_kernel<NR, kGather, kItems>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::kSmemBytes));
+  static std::atomic<uint64_t> attr_done{0};
+  {
+    const cudaError_t e =
+        ensure_smem_attr(mla_split_kv_kernel<NR, kGather, kItems>, static_cast<int>(C::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   CUtensorMap kv_lat, kv_rope, q_lat, q_rope;
   const uint64_t kv_rows = static_cast<uint64_t>(num_pages) * MLA_PAGE_SIZE;

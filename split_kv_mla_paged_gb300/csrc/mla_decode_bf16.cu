@@ -1154,13 +1154,11 @@ template <int NR>
 static cudaError_t launch_split_bf16(const void* q, const void* kv, int64_t num_pages, int batch,
                                      int groups, const DecodeParams& prm, cudaStream_t stream) {
   using C = CfgB<NR>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_bf16_kernel<NR>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::kSmemBytes));
+  static std::atomic<uint64_t> attr_done{0};
+  {
+    const cudaError_t e =
+        ensure_smem_attr(mla_split_kv_bf16_kernel<NR>, static_cast<int>(C::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   CUtensorMap tm_kv, tm_q;
   if (!make_map_bf16(&tm_kv, kv, static_cast<uint64_t>(num_pages) * MLA_PAGE_SIZE,
@@ -1175,13 +1173,11 @@ static cudaError_t launch_split_bf16(const void* q, const void* kv, int64_t num_
 static cudaError_t launch_split_bf16_q16(const void* q, const void* kv, int64_t num_pages,
                                          int batch, int groups, const DecodeParams& prm,
                                          cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mla_split_kv_bf16_q16_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(q16::kSmemBytes));
+  static std::atomic<uint64_t> attr_done{0};
+  {
+    const cudaError_t e =
+        ensure_smem_attr(mla_split_kv_bf16_q16_kernel, static_cast<int>(q16::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   CUtensorMap tm_kv, tm_q;
   if (!make_map_bf16(&tm_kv, kv, static_cast<uint64_t>(num_pages) * MLA_PAGE_SIZE,

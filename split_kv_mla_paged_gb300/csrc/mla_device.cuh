@@ -253,6 +253,20 @@ struct MergeParams {
   float* out_f32;
 };
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` once per device
+// (the attribute is per device; `done` holds one bit per device id < 64).
+template <typename Kernel>
+inline cudaError_t ensure_smem_attr(Kernel fn, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 // Launches the merge as a programmatic dependent of the preceding grid.
 cudaError_t launch_merge(const MergeParams& mp, int kv_split, cudaStream_t stream);
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
