@@ -268,6 +268,76 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def merge_sweep(args):
+    """The merge alone on seeded partials: rows = B*q*H in {12 .. 192}, splits
+    {6 .. 128}, KvSplit {1 .. 16} (10 % empty slots), CUDA graphs of K calls
+    per point, rotating over partial sets larger than 2x L2 in total.  Prints
+    one JSON line: the per-point times, the partial bytes read per call and the
+    graph floor of a one-element kernel."""
+    import numpy as np
+    import torch
+    import split_kv_mla_paged_gb300 as mla
+    from split_kv_mla_paged_gb300 import build as mla_build
+    from synth import merge_partials
+    mla_build.build()
+    mla.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    K = max(10, min(args.steps, 200))
+    tiny = torch.zeros(1, device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(K):
+            tiny.add_(1.0)
+
+    def time_graph(graph):
+        with torch.cuda.stream(stream):
+            graph.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / K
+
+    floor = time_graph(g)
+    points = []
+    for rows in (12, 96, 192):
+        for S in (6, 25, 128):
+            for ks in (1, 4, 16):
+                if ks > S:
+                    continue
+                o, ml = merge_partials(rows, S, seed=rows * 1000 + S)
+                part_bytes = o.nbytes + ml.nbytes
+                n_sets = max(1, min(16, -(-L2_ROTATE_BYTES // part_bytes)))
+                sets = []
+                for k in range(n_sets):
+                    o_d = torch.from_numpy(np.roll(o, k, axis=0)).to(dev)
+                    ml_d = torch.from_numpy(np.roll(ml, k, axis=0)).to(dev)
+                    out = torch.empty((rows, 512), dtype=torch.bfloat16, device=dev)
+                    lse = torch.empty((rows,), dtype=torch.float32, device=dev)
+                    sets.append((o_d, ml_d, out, lse))
+                with torch.cuda.stream(stream):
+                    mla.mla_merge(*sets[0][:2], rows, S, ks, sets[0][2], sets[0][3], None, stream)
+                torch.cuda.synchronize(dev)
+                gm = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gm, stream=stream):
+                    for k in range(K):
+                        o_d, ml_d, out, lse = sets[k % n_sets]
+                        mla.mla_merge(o_d, ml_d, rows, S, ks, out, lse, None)
+                us = time_graph(gm)
+                points.append({"rows": rows, "splits": S, "kv_split": ks, "us": us,
+                               "partial_bytes": part_bytes,
+                               "gbs": part_bytes / (us * 1e-6) / 1e9})
+                del gm, sets
+    line = {"metric": "MLA merge us/call (merge-only sweep)", "unit": "us/call", "n_gpus": 1,
+            "steps": K, "higher_is_better": False, "dtype": "f32", "data": "synthetic partials",
+            "floor_us_per_call": floor, "points": points}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -277,6 +347,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--plan", choices=["gb300", "pages"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--merge-sweep", action="store_true",
+                    help="time the merge alone over the merge-only sweep (rows x splits x KvSplit)")
     ap.add_argument("--replays", type=int, default=10,
                     help="further replays of the K-call graph for p10/median/p90")
     ap.add_argument("--cpu-rows", type=int, default=192,
@@ -290,6 +362,9 @@ def main():
     from synth import SOFTMAX_SCALE, WORKLOADS, workload_inputs
     w = WORKLOADS[args.workload]
     world, rank, local = dist_env()
+    if args.merge_sweep:
+        merge_sweep(args)
+        return
 
     if args.impl == "reference":
         if world > 1:
