@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import os
 import statistics
@@ -268,6 +269,70 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def kv_append_bench(args):
+    """The FP8 paged KV append (quantise BF16 latent rows, scatter through the
+    page table): 16 requests x 8 new tokens (an MTP decode step) and 16 x 65,536
+    (a prefill chunk), positions in random pages of a larger pool, with a
+    power-of-two kv_scale (1.0) and a calibrated-looking one (0.37).
+    Algorithmic bytes per row: 1152 read + 576 written + 8 of indices.  Prints
+    one JSON line with every case against the measured copy bandwidth."""
+    import numpy as np
+    import torch
+    import split_kv_mla_paged_gb300 as mla
+    from split_kv_mla_paged_gb300 import build as mla_build
+    mla_build.build()
+    mla.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    peaks = measured_peaks()
+    K = max(10, min(args.steps, 100))
+    cases = []
+    for (name, per_req), kv_scale in itertools.product(
+            (("mtp_step_b16_q8", 8), ("prefill_b16_64k", 65536)), (1.0, 0.37)):
+        B = 16
+        n = B * per_req
+        pages_per_req = (per_req + 31) // 32 + 1
+        n_pages = B * pages_per_req * 2
+        g = torch.Generator(device="cpu").manual_seed(7)
+        table = torch.randperm(n_pages, generator=g)[:B * pages_per_req].reshape(
+            B, pages_per_req).to(torch.int32)
+        start = torch.randint(0, 32, (B,), generator=g)
+        req = torch.arange(B, dtype=torch.int32).repeat_interleave(per_req)
+        pos = (start.repeat_interleave(per_req) + torch.arange(per_req).repeat(B)).to(torch.int32)
+        rows = (torch.randn(n, 576, generator=g) * 0.5).to(torch.bfloat16)
+        kv = torch.zeros((n_pages, 32, 576), dtype=torch.uint8, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        args_d = (rows.to(dev), n, req.to(dev), pos.to(dev), table.to(dev), pages_per_req, B,
+                  kv, n_pages, kv_scale, st)
+        with torch.cuda.stream(stream):
+            mla.mla_kv_append(*args_d, stream=stream)
+        torch.cuda.synchronize(dev)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for _ in range(K):
+                mla.mla_kv_append(*args_d)
+        with torch.cuda.stream(stream):
+            gr.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / K
+        assert int(st.item()) == 0
+        nbytes = n * (1152 + 576 + 8)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        cases.append({"case": name, "kv_scale": kv_scale, "rows": n, "us": us, "bytes": nbytes, "gbs": gbs,
+                      "frac": gbs / peaks["hbm_gbs"]})
+        del gr
+    line = {"metric": "FP8 paged KV append us/call", "unit": "us/call", "n_gpus": 1, "steps": K,
+            "higher_is_better": False, "dtype": "bf16->e4m3", "data": "synthetic",
+            "peak_gbs": peaks["hbm_gbs"], "cases": cases}
+    print(json.dumps(line), flush=True)
+
+
 def merge_sweep(args):
     """The merge alone on seeded partials: rows = B*q*H in {12 .. 192}, splits
     {6 .. 128}, KvSplit {1 .. 16} (10 % empty slots), CUDA graphs of K calls
@@ -347,6 +412,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--plan", choices=["gb300", "pages"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--kv-append", action="store_true",
+                    help="time the FP8 paged KV append (decode-sized and prefill-sized batches)")
     ap.add_argument("--merge-sweep", action="store_true",
                     help="time the merge alone over the merge-only sweep (rows x splits x KvSplit)")
     ap.add_argument("--replays", type=int, default=10,
@@ -364,6 +431,9 @@ def main():
     world, rank, local = dist_env()
     if args.merge_sweep:
         merge_sweep(args)
+        return
+    if args.kv_append:
+        kv_append_bench(args)
         return
 
     if args.impl == "reference":

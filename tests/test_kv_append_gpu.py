@@ -33,7 +33,7 @@ def _append(rows, req, pos, table, pool, kv_scale):
     return kv_d.cpu().numpy(), int(st.item())
 
 
-@pytest.mark.parametrize("kv_scale", [1.0, 0.37, 4.0])
+@pytest.mark.parametrize("kv_scale", [1.0, 0.37, 4.0, 0.125, -2.0, 3.0e-5])
 def test_append_bytes_match_oracle(kv_scale):
     g = torch.Generator().manual_seed(41)
     n_pages, batch = 40, 3
@@ -45,6 +45,31 @@ def test_append_bytes_match_oracle(kv_scale):
     # Values spanning E4M3's range: normals, subnormals, saturating ones.
     mag = torch.exp2(torch.randint(-14, 10, (req.size, 576), generator=g).float())
     rows = (torch.randn(req.size, 576, generator=g) * mag).to(torch.bfloat16)
+    got, st = _append(rows, req, pos, table, pool, kv_scale)
+    want, st_o = oracle.kv_append(rows, req, pos, table, pool, kv_scale)
+    assert st == 0 and st_o == 0
+    assert np.array_equal(got, want)
+
+
+# Scales for each way the kernel forms x / kv_scale: powers of two (a
+# multiplication), positive scales in [2^-32, 2^32] (reciprocal and one
+# correction) and the rest (the IEEE division).
+ALL_MODE_SCALES = [1.0, 4.0, -2.0, 2.0 ** -20,
+                   0.37, 3.0e-5, 1.0 / 448.0, 0.1, 1.5 * 2.0 ** -32, 1.3 * 2.0 ** 31,
+                   -0.37, 1.0e-12, 1.0e12]
+
+
+@pytest.mark.parametrize("kv_scale", ALL_MODE_SCALES)
+def test_append_every_bf16_pattern(kv_scale):
+    # All 65,536 BF16 bit patterns (zeros, subnormals, +-inf, NaN included):
+    # the codes equal the oracle's (IEEE fp32 quotient, then E4M3).
+    bits = np.zeros(114 * 576, dtype=np.uint16)
+    bits[:65536] = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    rows = torch.from_numpy(bits.view(np.int16).reshape(114, 576)).view(torch.bfloat16)
+    pool = np.full((4, 32, 576), 0x55, dtype=np.uint8)
+    table = np.array([[2, 0, 3, 1]], dtype=np.int32)
+    req = np.zeros(114, np.int32)
+    pos = np.arange(114, dtype=np.int32)
     got, st = _append(rows, req, pos, table, pool, kv_scale)
     want, st_o = oracle.kv_append(rows, req, pos, table, pool, kv_scale)
     assert st == 0 and st_o == 0
