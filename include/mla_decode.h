@@ -81,7 +81,7 @@ typedef enum {
  * sm_count     SMs of the target GPU (used when target_ctas <= 0).
  * target_ctas  > 0: reproduce the pages' planner: t = max(1, target/B)
  *              splits per request, chunk = roundup128(ceil(L/t)).  (A request
- *              with more than 48 rows runs each split as several row-group
+ *              with more than 96 rows runs each split as several row-group
  *              CTAs on top of that.)
  *              <= 0: GB300 planner: one common chunk for the whole batch,
  *              chosen to balance whole waves of one CTA per SM.

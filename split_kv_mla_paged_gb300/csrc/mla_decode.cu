@@ -13,13 +13,15 @@
 // Split-KV kernel design (one CTA per (request, split, row group), one CTA per
 // SM):
 //  * The MMA is "swapped": tokens are the M = 128 dimension and a row group of
-//    the request's query rows (heads x query tokens, at most 48 per CTA,
-//    padded to a multiple of 16: NR = 16, 32 or 48) is N.
-//    S^T[128 tok x NR] = K[128 x 576] Q^T and
+//    the request's query rows (heads x query tokens, padded: NR = 16, 32, 48
+//    or 96 per CTA) is N.  S^T[128 tok x NR] = K[128 x 576] Q^T and
 //    O^T[512 x 2NR] += V^T[512 x 128 tok] [P_hi | P_lo]^T, as four M = 128
 //    MMAs over the latent dims.  With H*q = 12 this does 16 columns of work
 //    instead of padding 12 rows to 128, and S^T plus O^T fit TMEM
-//    (2*NR + 4*2NR <= 512).
+//    (2*NR + 4*2NR <= 512).  The 96-row configuration (H12 q8 in one CTA, so
+//    each KV tile is read from shared memory once for all 96 rows) keeps one
+//    S^T buffer and accumulates P_hi and P_lo into the same O^T with two MMAs
+//    (96 + 4*96 columns), with one P^T buffer and per-thread row sums.
 //  * One TMA-staged copy of each KV tile (4 pages x 576 B x 32 tokens, 128 B
 //    swizzle for the latent blocks, 64 B for the rope block) serves as the K
 //    operand (K-major) and as the V operand (MN-major over the same bytes), so
@@ -30,8 +32,8 @@
 //    power of two, so the E4M3-quantised P fed to the PV MMA, and every
 //    partial, is the same for any split plan up to exact scaling.
 //  * Warp roles: warp 0 issues TMA, warp 1 issues tcgen05.mma (and owns TMEM),
-//    warps 2-5 (and 6-9 for 32 and 48 rows; TMEM lane quadrant = warp % 4)
-//    run the softmax, the rare O correction and the epilogue.
+//    warps 2-5 (and 6-9 from 32 rows up; TMEM lane quadrant = warp % 4) run
+//    the softmax, the rare O correction and the epilogue.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -60,12 +62,17 @@ constexpr uint32_t kPageBytes = MLA_PAGE_SIZE * MLA_HEAD_DIM;
 
 template <int NR>
 struct Cfg {
-  static_assert(NR % 16 == 0 && NR >= 16 && NR <= kMaxRowsPerCta, "NR");
-  // P^T = hi + lo.  Both terms go through one PV MMA with N = 2*NR (O^T
-  // holds the hi and lo products side by side and the epilogue adds them), so
-  // V is read from shared memory once per tile.
-  static constexpr int OW = 2 * NR;  // O^T columns per latent block
-  static constexpr int NS = 2;       // S^T buffers in TMEM
+  static_assert(NR == 16 || NR == 32 || NR == 48 || NR == kMaxRowsPerCtaFp8, "NR");
+  // kWide: the 96-row configuration.  TMEM holds one S^T buffer and O^T for
+  // 96 rows; the two E4M3 terms of P^T go through two PV MMAs into the same
+  // O^T, and each softmax thread keeps its own row sums across tiles (so the
+  // shared-memory reduction buffers fit next to two KV stages, Q and P^T).
+  static constexpr bool kWide = NR > kMaxRowsPerCta;
+  // P^T = hi + lo.  Up to 48 rows both terms go through one PV MMA with
+  // N = 2*NR (O^T holds the hi and lo products side by side and the epilogue
+  // adds them), so V is read from shared memory once per tile.
+  static constexpr int OW = kWide ? NR : 2 * NR;  // O^T columns per latent block
+  static constexpr int NS = kWide ? 1 : 2;        // S^T buffers in TMEM
   static constexpr uint32_t kTmemUsed = NS * NR + 4 * OW;
   static_assert(kTmemUsed <= 512, "TMEM");
   // Softmax warpgroups: two (each owning half the rows) from 32 rows up.
@@ -80,7 +87,10 @@ struct Cfg {
   // Shared memory, offsets from a 1024-byte aligned base.
   static constexpr uint32_t kPHalf = NR * kTileTokens;  // one E4M3 term of P^T
   static constexpr uint32_t kPBytes = 2 * kPHalf;       // hi + lo
-  static constexpr uint32_t kAuxBytes = 176 + 52 * NR;
+  // Reductions: tile maxima 16 NR B, row sums 32 NR B (double-buffered by
+  // tile parity; 16 NR B, one buffer, with per-thread sums), references 4 NR B.
+  static constexpr uint32_t kRedSumBytes = kWide ? 16 * NR : 32 * NR;
+  static constexpr uint32_t kAuxBytes = 176 + 20 * NR + kRedSumBytes;
   static constexpr uint32_t kQBytes = NR * MLA_HEAD_DIM;
   // Three KV stages fit when P^T can live in the rope block of its own stage
   // (QK has consumed that block before P is written): NR = 16.  Otherwise two
@@ -94,7 +104,7 @@ struct Cfg {
   static constexpr uint32_t kP = kQ + kQBytes;
   static constexpr int NPB = kPInStage ? 0
                              : (kP + 2 * kPBytes + kAuxBytes + 1024 <= 232448u) ? 2 : 1;
-  static_assert(NPB != 1, "P^T needs two buffers or a slot in each KV stage");
+  static_assert(NPB != 1 || kWide, "P^T needs two buffers or a slot in each KV stage");
   static constexpr uint32_t kAux = kP + NPB * kPBytes;
   // aux: mbarriers, tmem slot, flags, reductions
   static constexpr uint32_t kBars = kAux;               // 17 x 8 B
@@ -105,8 +115,8 @@ struct Cfg {
   // Row owner r reads red_max[.][r] before writing alpha[r]: alpha reuses
   // red_max's first row.
   static constexpr uint32_t kAlpha = kRedMax;           // NR floats
-  static constexpr uint32_t kRedSum = kRedMax + 16 * NR;  // 2 x 4 x NR floats
-  static constexpr uint32_t kKref = kRedSum + 32 * NR;  // NR floats
+  static constexpr uint32_t kRedSum = kRedMax + 16 * NR;  // (2 x) 4 x NR floats
+  static constexpr uint32_t kKref = kRedSum + kRedSumBytes;  // NR floats
   static constexpr uint32_t kEnd = kKref + 4 * NR;
   static_assert(kEnd - kAux <= kAuxBytes, "aux layout");
   static_assert(NR != 16 || NST == 3, "16-row CTAs must keep three KV stages");
@@ -239,6 +249,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;
+    for (int r = 0; r < NR; ++r) kref[r] = -INFINITY;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -415,6 +426,11 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           // groups), 8-token groups 128 B apart.
           const uint64_t bd = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
           umma_f8(tmem + C::kOCol + d * C::OW, a, bd, kIdPV, acc);
+          if constexpr (C::kWide) {
+            // The lo term: a second MMA into the same O^T columns.
+            const uint64_t bl = smem_desc(pbuf + C::kPHalf + ks * 512, 128, 2048, kLayoutNone);
+            umma_f8(tmem + C::kOCol + d * C::OW, a, bl, kIdPV, 1u);
+          }
         }
       }
       umma_commit(bar(BAR_EMPTY0 + jst));
@@ -555,9 +571,22 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     float k_row = -INFINITY;  // owner state: reference (integer, log2 units)
     float l_row = 0.0f;       // owner state: sum of weights relative to k_row - 8
-    float kreg[NRH];          // this thread's copy of its rows' references
+    // This thread's copy of its rows' references; kWide reads them from
+    // shared memory instead (owners write kref only between B1 and B2, when
+    // every thread has passed the tile's vote and none has reached its
+    // weights), which keeps the 32-row thread within its registers.
+    float kreg[C::kWide ? 1 : NRH];
+    auto ref = [&](int k) -> float {
+      if constexpr (C::kWide) return kref[rbase + k];
+      else return kreg[k];
+    };
+    // kWide: this thread's sums of its token's weights per row, relative to
+    // the row's current reference (reduced once, after the last tile).
+    float lsum[C::kWide ? NRH : 1];
 #pragma unroll
-    for (int k = 0; k < NRH; ++k) kreg[k] = -INFINITY;
+    for (int k = 0; k < (C::kWide ? NRH : 1); ++k) lsum[k] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < (C::kWide ? 1 : NRH); ++k) kreg[k] = -INFINITY;
     const float c = c_log2;
     // Smallest visibility limit over this group's rows (MTP verify: the first
     // query token of the block sees the fewest keys).
@@ -578,8 +607,8 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     }
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
-      const int sb = i & 1;
-      const int use = i >> 1;
+      const int sb = (C::NS == 2) ? (i & 1) : 0;
+      const int use = (C::NS == 2) ? (i >> 1) : i;
       if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
       ok = __all_sync(0xffffffffu, ok);
       float t[NRH];
@@ -651,10 +680,10 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       // are the tile maxima reduced and references raised to ceil(max).
       bool over = false;
 #pragma unroll
-      for (int k = 0; k < NRH; ++k) over |= t[k] > kreg[k] + 0.75f;
+      for (int k = 0; k < NRH; ++k) over |= t[k] > ref(k) + 0.75f;
       const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
       // Owners fold the previous tile's row sums (relative to its reference).
-      if (sid < NR && i > 0) {
+      if (!C::kWide && sid < NR && i > 0) {
         const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
         l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
       }
@@ -687,8 +716,15 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           alpha_s[sid] = alpha;
         }
         named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
+        if constexpr (!C::kWide) {
 #pragma unroll
-        for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
+          for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
+        } else {
+          // Per-thread sums follow their rows' references (alpha = 1 where
+          // the reference did not move).
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) lsum[k] *= alpha_s[rbase + k];
+        }
         const bool corr = flags[0] != 0;
         if (ok && corr && i > 0) {
           // Rescale the O^T columns (hi and lo) of rows whose reference moved
@@ -702,7 +738,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
 #pragma unroll 1
             for (int d = 0; d < 4; ++d) {
 #pragma unroll
-              for (int half = 0; half < 2; ++half) {
+              for (int half = 0; half < (C::kWide ? 1 : 2); ++half) {
 #pragma unroll
                 for (int cc = 0; cc < NRH / 8; ++cc) {
                   uint32_t r[8];
@@ -723,12 +759,14 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       }
       // Weights 2^(t - k + 8), exact power-of-two scaling.
 #pragma unroll
-      for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], kreg[k]);
+      for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], ref(k));
       // P^T as two E4M3 terms into shared memory, MN-major:
       // [term][NR/16 row groups][128 tokens][16 rows]; this thread writes its
       // token's bytes for rows rbase .. rbase + NRH, 8 rows per store.
-      const int pb = i & 1;
-      const int puse = i >> 1;
+      // P barriers (and buffers) alternate by tile parity unless there is a
+      // single P^T buffer; the MMA warp uses the same rule.
+      const int pb = (C::NPB == 1) ? 0 : (i & 1);
+      const int puse = (C::NPB == 1) ? i : (i >> 1);
       if (ok && !C::kPInStage && puse >= 1) {
         ok = mbar_wait(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles);
         ok = __all_sync(0xffffffffu, ok);
@@ -753,21 +791,32 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(BAR_PFULL0 + pb));
       }
-      // Row sums of the unquantised weights, folded in by the owners after
-      // the next tile's vote (double-buffered by tile parity).
-      warp_reduce_rows<NRH, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR + rbase);
+      // Row sums of the unquantised weights: per thread across tiles (kWide),
+      // or reduced per tile and folded in by the owners after the next tile's
+      // vote (double-buffered by tile parity).
+      if constexpr (C::kWide) {
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) lsum[k] += t[k];
+      } else {
+        warp_reduce_rows<NRH, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR + rbase);
+      }
     }
     if (!ok && lane == 0) {
       report(p.status, MLA_ERR_TIMEOUT);
       *abort_flag = 1;
     }
     // ---- epilogue ----
+    if constexpr (C::kWide) {
+      // The per-thread sums, reduced over the 32 tokens of each warp; the
+      // owners add the four lane quadrants below.
+      warp_reduce_rows<NRH, false>(lsum, lane, red_sum + quad * NR + rbase);
+    }
     named_bar_sync(kSoftmaxBarrier, NT);
     const bool single = (nsplit == 1);
     float* scale_s = alpha_s;
     if (sid < NR) {
       if (n_tiles > 0) {
-        const float* rs = red_sum + ((n_tiles - 1) & 1) * 4 * NR;
+        const float* rs = red_sum + (C::kWide ? 0 : ((n_tiles - 1) & 1) * 4 * NR);
         l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
       }
       const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
@@ -809,13 +858,15 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           uint32_t r[8], r2[8];
           const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + rbase + cc * 8;
           tmem_ld8(addr, r);
-          tmem_ld8(addr + NR, r2);  // the lo term's product
+          if constexpr (!C::kWide) tmem_ld8(addr + NR, r2);  // the lo term's product
           tmem_ld_wait();
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const int row = rbase + cc * 8 + k;
             if (row < rows_here) {
-              const float v = (__uint_as_float(r[k]) + __uint_as_float(r2[k])) * scale_s[row];
+              const float o = C::kWide ? __uint_as_float(r[k])
+                                       : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
+              const float v = o * scale_s[row];
               const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
               if (single) {
                 p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
@@ -1138,7 +1189,7 @@ static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
     return MLA_ERR_WORKSPACE_TOO_SMALL;
   }
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  dl->rg = row_groups(num_heads * q_len);
+  dl->rg = row_groups_fp8(num_heads * q_len);
   dl->batch = batch;
   dl->kv_split = kv_split;
   dl->max_splits = max_splits;
@@ -1246,6 +1297,12 @@ static int launch_decode_split(const void* q_fp8, const void* kv_pages_fp8, int6
     case 48:
       e = gather ? launch_split<48, true>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.num_ctas, dl.prm, st)
                  : launch_split<48, false>(q_fp8, kv_pages_fp8, num_pages, b, g, dl.num_ctas, dl.prm, st);
+      break;
+    case kMaxRowsPerCtaFp8:
+      e = gather ? launch_split<kMaxRowsPerCtaFp8, true>(q_fp8, kv_pages_fp8, num_pages, b, g,
+                                                         dl.num_ctas, dl.prm, st)
+                 : launch_split<kMaxRowsPerCtaFp8, false>(q_fp8, kv_pages_fp8, num_pages, b, g,
+                                                          dl.num_ctas, dl.prm, st);
       break;
     default:
       set_error("mla_decode: internal row grouping error");

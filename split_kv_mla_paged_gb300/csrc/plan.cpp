@@ -81,7 +81,7 @@ extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t nu
     }
     lmax = std::max<int64_t>(lmax, kv_lens[b]);
   }
-  const RowGroups rg = row_groups(num_heads * q_len);
+  const RowGroups rg = row_groups_fp8(num_heads * q_len);
   const int64_t T = MLA_TILE_TOKENS;
 
   if (target_ctas > 0) {
@@ -158,7 +158,7 @@ extern "C" int mla_decode_plan_items(const int32_t* splits, int32_t batch, int32
     set_error("mla_decode_plan_items: num_heads * q_len exceeds MLA_MAX_ROWS");
     return MLA_ERR_UNSUPPORTED;
   }
-  const RowGroups rg = row_groups(num_heads * q_len);
+  const RowGroups rg = row_groups_fp8(num_heads * q_len);
   int32_t max_splits = 0;
   int64_t total = 0;
   for (int b = 0; b < batch; ++b) {

@@ -102,7 +102,7 @@ def test_split_plans_agree_in_fp32():
 
 
 def test_maximum_rows_per_request():
-    # H * q = 1024 = MLA_MAX_ROWS: 22 row groups (21 of 48 and one of 16).
+    # H * q = 1024 = MLA_MAX_ROWS: 11 row groups of at most 94 rows (96-row CTAs).
     inp = decode_inputs(2, 128, 8, [700, 300], seed=21, extra_pages=1)
     _full_check(inp, True, SOFTMAX_SCALE)
 

@@ -103,7 +103,7 @@ def test_plan_needs_sm_count_without_target():
 
 def test_plan_items_are_the_ctas_with_work_in_split_major_order():
     splits = np.array([3, 1, 2], dtype=np.int32)
-    for H, q, groups in ((12, 1, 1), (12, 8, 2), (96, 8, 16)):
+    for H, q, groups in ((12, 1, 1), (12, 4, 1), (12, 8, 1), (16, 8, 2), (96, 8, 8)):
         items = mla.mla_decode_plan_items(splits, H, q)
         assert items.shape[0] == int(splits.sum()) * groups
         b = items >> 14

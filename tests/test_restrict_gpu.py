@@ -71,14 +71,16 @@ def test_query_lens_parity(B, H, q_len, lens, causal):
         _check(inp, causal, dict(query_lens=np.asarray(ql, np.int32)), plan=plan)
 
 
-def test_query_lens_whole_padding_group_and_sinks():
-    # q_b = 1 of 8 with H = 12: the second 48-row group of the request is all
-    # padding (no tile runs there); sinks give those rows LSE = sink.
-    inp = decode_inputs(2, 12, 8, [3000, 700], seed=410)
+@pytest.mark.parametrize("H", [12, 16])
+def test_query_lens_whole_padding_group_and_sinks(H):
+    # q_b = 1 of 8: with H = 12 the 96-row group holds 12 real rows; with
+    # H = 16 (128 rows, two groups of 64) the second group of the request is
+    # all padding (no tile runs there).  Sinks give padding rows LSE = sink.
+    inp = decode_inputs(2, H, 8, [3000, 700], seed=410)
     ql = np.array([1, 8], np.int32)
-    sinks = np.linspace(-1.0, 2.0, 12)
+    sinks = np.linspace(-1.0, 2.0, H)
     for target in (2, 30):
-        plan = mla.mla_decode_plan([3000, 700], 12, 8, target_ctas=target)
+        plan = mla.mla_decode_plan([3000, 700], H, 8, target_ctas=target)
         out, lse, _ = _run(inp, True, plan=plan, query_lens=ql, sinks=sinks)
         ref_o, ref_l = _oracle(inp, True, query_lens=ql, sinks=sinks)
         assert_parity(out, lse, ref_o, ref_l)
