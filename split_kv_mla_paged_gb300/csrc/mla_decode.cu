@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], ref(k));
       // P^T as two E4M3 terms into shared memory, MN-major:
       // [term][NR/16 row groups][128 tokens][16 rows]; this thread writes its
-      // token's bytes for rows rbase .. rbase + NRH, 8 rows per store.
+      // token's bytes for rows rbase .. rbase + NRH, 16 (or 8) rows per store.
       // P barriers (and buffers) alternate by tile parity unless there is a
       // single P^T buffer; the MMA warp uses the same rule.
       const int pb = (C::NPB == 1) ? 0 : (i & 1);
@@ -777,15 +777,32 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         uint8_t* pbuf = C::kPInStage
                             ? base + C::kKV + (i % C::NST) * kTileBytes + kRopeOffset
                             : base + C::kP + pb * C::kPBytes;
+        if constexpr (NRH % 16 == 0) {
+          // Whole 16-row groups: one 16-byte store per term and group, the
+          // warp's 32 tokens covering 512 contiguous bytes (no bank conflict).
 #pragma unroll
-        for (int g = 0; g < NRH / 8; ++g) {
-          const int row = rbase + g * 8;
-          uint2 vh, vl;
-          split_e4m3x4(&t[g * 8 + 0], vh.x, vl.x);
-          split_e4m3x4(&t[g * 8 + 4], vh.y, vl.y);
-          const uint32_t off = (row >> 4) * 2048 + tok_lane * 16 + (row & 15);
-          *reinterpret_cast<uint2*>(pbuf + off) = vh;
-          *reinterpret_cast<uint2*>(pbuf + C::kPHalf + off) = vl;
+          for (int g = 0; g < NRH / 16; ++g) {
+            const int row = rbase + g * 16;
+            uint4 vh, vl;
+            split_e4m3x4(&t[g * 16 + 0], vh.x, vl.x);
+            split_e4m3x4(&t[g * 16 + 4], vh.y, vl.y);
+            split_e4m3x4(&t[g * 16 + 8], vh.z, vl.z);
+            split_e4m3x4(&t[g * 16 + 12], vh.w, vl.w);
+            const uint32_t off = (row >> 4) * 2048 + tok_lane * 16;
+            *reinterpret_cast<uint4*>(pbuf + off) = vh;
+            *reinterpret_cast<uint4*>(pbuf + C::kPHalf + off) = vl;
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < NRH / 8; ++g) {
+            const int row = rbase + g * 8;
+            uint2 vh, vl;
+            split_e4m3x4(&t[g * 8 + 0], vh.x, vl.x);
+            split_e4m3x4(&t[g * 8 + 4], vh.y, vl.y);
+            const uint32_t off = (row >> 4) * 2048 + tok_lane * 16 + (row & 15);
+            *reinterpret_cast<uint2*>(pbuf + off) = vh;
+            *reinterpret_cast<uint2*>(pbuf + C::kPHalf + off) = vl;
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
