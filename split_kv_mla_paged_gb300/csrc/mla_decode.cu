@@ -921,9 +921,10 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
 }
 
 
-template <int G>
-__global__ void __launch_bounds__(32 * G) mla_merge_kernel(const MergeParams p) {
-  constexpr int U = 4;
+// The merge of one (row, quarter of the latent dims): G thread groups over
+// the row's partials, U loads in flight per group.
+template <int G, int U>
+__device__ __forceinline__ void merge_body(const MergeParams& p) {
   __shared__ float sm_m[G];
   __shared__ float sm_l[G];
   __shared__ float4 sm_o[G][32];
@@ -1020,6 +1021,18 @@ __global__ void __launch_bounds__(32 * G) mla_merge_kernel(const MergeParams p) 
     p.lse[row] = empty ? -INFINITY : 0.6931471805599453f * (mm + log2f(den));
 }
 
+template <int G>
+__global__ void __launch_bounds__(32 * G) mla_merge_kernel(const MergeParams p) {
+  merge_body<G, 4>(p);
+}
+
+// Grids of more than two 512-thread CTAs per SM: three per SM (at most 40
+// registers, two loads in flight per group instead of four), so that the
+// grid fits one wave.
+__global__ void __launch_bounds__(512, 3) mla_merge_many_kernel(const MergeParams p) {
+  merge_body<16, 2>(p);
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -1093,7 +1106,7 @@ static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages
 // on the stream (the split-KV kernel in mla_decode): its CTAs may be scheduled
 // while the split kernel drains and wait in griddepcontrol.wait until the
 // partials are visible.  Launched after anything else, the wait returns at once.
-template <int G>
+template <int G, bool kMany = false>
 static cudaError_t launch_merge_g(const MergeParams& mp, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(mp.rows, 4);  // rows on x: no 65535 limit
@@ -1105,7 +1118,12 @@ static cudaError_t launch_merge_g(const MergeParams& mp, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_merge_kernel<G>, mp);
+  if constexpr (kMany) {
+    static_assert(G == 16, "the many-row merge has 16 groups");
+    return cudaLaunchKernelEx(&cfg, mla_merge_many_kernel, mp);
+  } else {
+    return cudaLaunchKernelEx(&cfg, mla_merge_kernel<G>, mp);
+  }
 }
 
 cudaError_t launch_merge(const MergeParams& mp, int kv_split, cudaStream_t stream) {
@@ -1115,7 +1133,16 @@ cudaError_t launch_merge(const MergeParams& mp, int kv_split, cudaStream_t strea
     case 2: e = launch_merge_g<2>(mp, stream); break;
     case 4: e = launch_merge_g<4>(mp, stream); break;
     case 8: e = launch_merge_g<8>(mp, stream); break;
-    case 16: e = launch_merge_g<16>(mp, stream); break;
+    case 16: {
+      int dev = 0, sms = 0;
+      e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      e = (static_cast<int64_t>(mp.rows) * 4 > 2 * static_cast<int64_t>(sms))
+              ? launch_merge_g<16, true>(mp, stream)
+              : launch_merge_g<16, false>(mp, stream);
+      break;
+    }
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
