@@ -79,7 +79,13 @@ struct Cfg {
   static constexpr int SWG = NR >= 32 ? 2 : 1;
   static constexpr int NRH = NR / SWG;
   static_assert(NRH % 8 == 0, "rows per softmax warpgroup");
-  static constexpr int kThreads = 64 + 128 * SWG;
+  // Warp 0 TMA, warp 1 QK issuer (and TMEM owner), warp 2 PV issuer, then
+  // the softmax warpgroups.  The 96-row CTA issues both from warp 1 (one S^T
+  // and one P^T buffer leave a second issuer nothing to overlap: measured
+  // 441 -> 475 us on MTP q8 B16 128K with two).
+  static constexpr int kMmaWarps = kWide ? 1 : 2;
+  static constexpr int kSoftmaxWarp0 = 1 + kMmaWarps;
+  static constexpr int kThreads = 32 * kSoftmaxWarp0 + 128 * SWG;
   static constexpr uint32_t kTmemCols =
       kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
       : kTmemUsed <= 256 ? 256 : 512;
@@ -106,6 +112,11 @@ struct Cfg {
                              : (kP + 2 * kPBytes + kAuxBytes + 1024 <= 232448u) ? 2 : 1;
   static_assert(NPB != 1 || kWide, "P^T needs two buffers or a slot in each KV stage");
   static constexpr uint32_t kAux = kP + NPB * kPBytes;
+  // PV completions alternate between two barriers by tile parity; the second
+  // takes a slot this configuration does not use (the second P^T-free
+  // barrier when P^T lives in the stages, else the third stage's full one).
+  static constexpr int kBarOdone1 = kPInStage ? BAR_PFREE1 : BAR_FULL0 + 2;
+  static_assert(kPInStage || NST == 2, "the third stage's barrier must be free");
   // aux: mbarriers, tmem slot, flags, reductions
   static constexpr uint32_t kBars = kAux;               // 17 x 8 B
   static constexpr uint32_t kTmemSlot = kAux + 136;     // 4 B
@@ -245,7 +256,8 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     mbar_init(bar(BAR_PFREE0), 1);
     mbar_init(bar(BAR_PFREE1), 1);
     mbar_init(bar(BAR_ODONE), 1);
-    mbar_init(bar(BAR_FINAL), 1);
+    mbar_init(bar(C::kBarOdone1), 1);
+    mbar_init(bar(BAR_FINAL), C::kMmaWarps);  // one commit from each MMA warp
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;
@@ -399,11 +411,14 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ================= MMA issuer =================
+  } else if (warp == 1 || (!C::kWide && warp == 2)) {
+    // ================= MMA issuers: warp 1 QK, warp 2 PV =================
+    // Two issuing warps keep the tensor pipe fed with QK(i + 1) while PV(i)
+    // goes out: one warp issuing both left ~30 % of the pipe's rate unused
+    // at these N (measured with a probe of the issue rate).
     constexpr uint32_t kIdQK = idesc_e4m3(128, NR, 0, 0);
     constexpr uint32_t kIdPV = idesc_e4m3(128, C::OW, 1, 1);
-    bool ok = mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles);
+    bool ok = (warp == 1) ? mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles) : true;
     auto fail = [&]() {
       if (lane == 0) {
         report(p.status, MLA_ERR_TIMEOUT);
@@ -435,7 +450,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       }
       umma_commit(bar(BAR_EMPTY0 + jst));
       if (!C::kPInStage) umma_commit(bar(BAR_PFREE0 + pb));
-      umma_commit(bar(BAR_ODONE));
+      umma_commit(bar((j & 1) ? C::kBarOdone1 : BAR_ODONE));
     };
     // QK of tile i (KV in stage ist) into S buffer sb; lane 0 issues.
     auto issue_qk = [&](int ist, int sb) {
@@ -459,43 +474,120 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     };
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) fail();
-    // Issue loop.  PV(pv) goes out as soon as its P^T is ready and QK(qk) as
-    // soon as its tile has landed and its S^T buffer is free, in whichever
-    // order they become ready; QK runs at most one tile ahead of PV
-    // (qk <= pv + 1), which keeps each p_full barrier at most one phase ahead
-    // of this warp.  PV is preferred: it releases a KV stage.
-    int qk = 0, pv = 0;
-    int qk_st = 0, qk_round = 0, pv_st = 0;
-    long long t_last = clock64();
-    while (ok && pv < n_tiles) {
-      int action = 0;
-      if (lane == 0) {
-        if (pv < qk) {
-          const int pb = (C::NPB == 1) ? 0 : (pv & 1);
-          const int use = (C::NPB == 1) ? pv : (pv >> 1);
-          if (mbar_test_wait(bar(BAR_PFULL0 + pb), use & 1)) action = 1;
+    if constexpr (C::kWide) {
+      // One issuing warp.  PV(pv) goes out as soon as its P^T is ready and QK(qk) as
+      // soon as its tile has landed and its S^T buffer is free, in whichever
+      // order they become ready; QK runs at most one tile ahead of PV
+      // (qk <= pv + 1), which keeps each p_full barrier at most one phase ahead
+      // of this warp.  PV is preferred: it releases a KV stage.
+      int qk = 0, pv = 0;
+      int qk_st = 0, qk_round = 0, pv_st = 0;
+      long long t_last = clock64();
+      while (ok && pv < n_tiles) {
+        int action = 0;
+        if (lane == 0) {
+          if (pv < qk) {
+            const int pb = (C::NPB == 1) ? 0 : (pv & 1);
+            const int use = (C::NPB == 1) ? pv : (pv >> 1);
+            if (mbar_test_wait(bar(BAR_PFULL0 + pb), use & 1)) action = 1;
+          }
+          if (action == 0 && qk < n_tiles && qk <= pv + 1) {
+            const int sb = (C::NS == 2) ? (qk & 1) : 0;
+            const int use = (C::NS == 2) ? (qk >> 1) : qk;
+            if (mbar_test_wait(bar(BAR_FULL0 + qk_st), qk_round & 1) &&
+                (use < 1 || mbar_test_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1)))
+              action = 2;
+          }
         }
-        if (action == 0 && qk < n_tiles && qk <= pv + 1) {
-          const int sb = (C::NS == 2) ? (qk & 1) : 0;
-          const int use = (C::NS == 2) ? (qk >> 1) : qk;
-          if (mbar_test_wait(bar(BAR_FULL0 + qk_st), qk_round & 1) &&
-              (use < 1 || mbar_test_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1)))
-            action = 2;
+        action = __shfl_sync(0xffffffffu, action, 0);
+        if (action == 1) {
+          if (lane == 0) issue_pv(pv, pv_st, (C::NPB == 1) ? 0 : (pv & 1));
+          __syncwarp();
+          ++pv;
+          if (++pv_st == C::NST) pv_st = 0;
+          t_last = clock64();
+        } else if (action == 2) {
+          // Rows that hold no loaded key: pages that were not loaded (past the
+          // split's end, outside a window or an unused selection slot) and the
+          // tail of a request's last page.  Zero them so V holds no stale or NaN
+          // bytes (0 * NaN would poison the PV sum).
+          uint8_t* kvp = base + C::kKV + qk_st * kTileBytes;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          auto zero_rows = [&](int r0, int nrow) {
+            for (int idx = lane; idx < nrow * 36; idx += 32) {
+              const int r = r0 + idx / 36;
+              const int c = idx % 36;
+              uint4* dst;
+              if (c < 32)
+                dst = reinterpret_cast<uint4*>(kvp + (c / 8) * kLatBlockBytes + r * 128 + (c % 8) * 16);
+              else
+                dst = reinterpret_cast<uint4*>(kvp + kRopeOffset + r * 64 + (c - 32) * 16);
+              *dst = z;
+            }
+          };
+          if constexpr (kGather) {
+            // Rows loaded per page, as the producer published them with the
+            // stage's full barrier (which lane 0 has just observed).
+            uint32_t info = 0;
+            if (lane == 0) info = *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * qk_st);
+            info = __shfl_sync(0xffffffffu, info, 0);
+            if (info != 0x20202020u) {
+  #pragma unroll 1
+              for (int q = 0; q < 4; ++q) {
+                const int nv = static_cast<int>((info >> (8 * q)) & 0xFFu);
+                if (nv < MLA_PAGE_SIZE) zero_rows(q * MLA_PAGE_SIZE + nv, MLA_PAGE_SIZE - nv);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+          } else {
+            const int tile_tok0 = t0 + qk * kTileTokens;
+            const int valid = tok_end - tile_tok0;  // tokens of this tile inside the split
+            if (valid < kTileTokens) {
+              zero_rows(valid, kTileTokens - valid);
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+          }
+          if (lane == 0) issue_qk(qk_st, (C::NS == 2) ? (qk & 1) : 0);
+          __syncwarp();
+          ++qk;
+          if (++qk_st == C::NST) {
+            qk_st = 0;
+            ++qk_round;
+          }
+          t_last = clock64();
+        } else {
+          const bool late = (clock64() - t_last > p.wait_cycles) || *abort_flag;
+          if (__any_sync(0xffffffffu, late)) {
+            fail();
+            ok = false;
+          }
         }
       }
-      action = __shfl_sync(0xffffffffu, action, 0);
-      if (action == 1) {
-        if (lane == 0) issue_pv(pv, pv_st, (C::NPB == 1) ? 0 : (pv & 1));
-        __syncwarp();
-        ++pv;
-        if (++pv_st == C::NST) pv_st = 0;
-        t_last = clock64();
-      } else if (action == 2) {
+    } else if (warp == 1) {
+      // QK(j) once its tile has landed, its S^T buffer is free and PV(j - 2)
+      // has completed (so the softmax's wait for PV(j - 1) stays within one
+      // phase of its barrier; QK(j) still overlaps PV(j - 1)).
+      int st = 0, round = 0;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int sb = (C::NS == 2) ? (j & 1) : 0;
+        const int use = (C::NS == 2) ? (j >> 1) : j;
+        bool w = mbar_wait(bar(BAR_FULL0 + st), round & 1, p.wait_cycles);
+        if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles);
+        if (w && j >= 2)
+          w = mbar_wait(bar(((j - 2) & 1) ? C::kBarOdone1 : BAR_ODONE), ((j - 2) >> 1) & 1,
+                        p.wait_cycles);
+        w = __all_sync(0xffffffffu, w && !*abort_flag);
+        if (!w) {
+          ok = false;
+          break;
+        }
         // Rows that hold no loaded key: pages that were not loaded (past the
         // split's end, outside a window or an unused selection slot) and the
         // tail of a request's last page.  Zero them so V holds no stale or NaN
         // bytes (0 * NaN would poison the PV sum).
-        uint8_t* kvp = base + C::kKV + qk_st * kTileBytes;
+        uint8_t* kvp = base + C::kKV + st * kTileBytes;
         const uint4 z = make_uint4(0, 0, 0, 0);
         auto zero_rows = [&](int r0, int nrow) {
           for (int idx = lane; idx < nrow * 36; idx += 32) {
@@ -511,10 +603,8 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         };
         if constexpr (kGather) {
           // Rows loaded per page, as the producer published them with the
-          // stage's full barrier (which lane 0 has just observed).
-          uint32_t info = 0;
-          if (lane == 0) info = *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * qk_st);
-          info = __shfl_sync(0xffffffffu, info, 0);
+          // stage's full barrier (observed above).
+          const uint32_t info = *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st);
           if (info != 0x20202020u) {
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
@@ -525,30 +615,38 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
             __syncwarp();
           }
         } else {
-          const int tile_tok0 = t0 + qk * kTileTokens;
-          const int valid = tok_end - tile_tok0;  // tokens of this tile inside the split
+          const int valid = tok_end - (t0 + j * kTileTokens);  // tokens of this tile inside the split
           if (valid < kTileTokens) {
             zero_rows(valid, kTileTokens - valid);
             fence_proxy_async_smem();
             __syncwarp();
           }
         }
-        if (lane == 0) issue_qk(qk_st, (C::NS == 2) ? (qk & 1) : 0);
+        if (lane == 0) issue_qk(st, sb);
         __syncwarp();
-        ++qk;
-        if (++qk_st == C::NST) {
-          qk_st = 0;
-          ++qk_round;
-        }
-        t_last = clock64();
-      } else {
-        const bool late = (clock64() - t_last > p.wait_cycles) || *abort_flag;
-        if (__any_sync(0xffffffffu, late)) {
-          fail();
-          ok = false;
+        if (++st == C::NST) {
+          st = 0;
+          ++round;
         }
       }
+    } else {
+      // PV(i) as soon as its P^T is ready.
+      int st = 0;
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int pb = (C::NPB == 1) ? 0 : (i & 1);
+        const int use = (C::NPB == 1) ? i : (i >> 1);
+        bool w = mbar_wait(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles);
+        w = __all_sync(0xffffffffu, w && !*abort_flag);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) issue_pv(i, st, pb);
+        __syncwarp();
+        if (++st == C::NST) st = 0;
+      }
     }
+    if (!ok) fail();
     // One commit after everything this warp issued: the epilogue reads O^T
     // after it, and TMEM is released only after it.
     if (lane == 0) umma_commit(bar(BAR_FINAL));
@@ -565,17 +663,19 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     constexpr int NRH = C::NRH;
     constexpr int NT = 128 * C::SWG;
     const int quad = warp & 3;
-    const int rbase = ((warp - 2) >> 2) * NRH;  // first row of this warpgroup
+    const int rbase = ((warp - C::kSoftmaxWarp0) >> 2) * NRH;  // first row of this warpgroup
     const int tok_lane = quad * 32 + lane;  // TMEM lane == token index within the tile
-    const int sid = threadIdx.x - 64;       // 0..NT-1, owner of row `sid` when < NR
+    const int sid = threadIdx.x - 32 * C::kSoftmaxWarp0;  // 0..NT-1, owner of row `sid` when < NR
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     float k_row = -INFINITY;  // owner state: reference (integer, log2 units)
     float l_row = 0.0f;       // owner state: sum of weights relative to k_row - 8
     // This thread's copy of its rows' references; kWide reads them from
     // shared memory instead (owners write kref only between B1 and B2, when
     // every thread has passed the tile's vote and none has reached its
-    // weights), which keeps the 32-row thread within its registers.
+    // weights), which keeps the 48-row thread within its registers.
     float kreg[C::kWide ? 1 : NRH];
+#pragma unroll
+    for (int k = 0; k < (C::kWide ? 1 : NRH); ++k) kreg[k] = -INFINITY;
     auto ref = [&](int k) -> float {
       if constexpr (C::kWide) return kref[rbase + k];
       else return kreg[k];
@@ -585,8 +685,6 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     float lsum[C::kWide ? NRH : 1];
 #pragma unroll
     for (int k = 0; k < (C::kWide ? NRH : 1); ++k) lsum[k] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < (C::kWide ? 1 : NRH); ++k) kreg[k] = -INFINITY;
     const float c = c_log2;
     // Smallest visibility limit over this group's rows (MTP verify: the first
     // query token of the block sees the fewest keys).
@@ -728,10 +826,12 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         const bool corr = flags[0] != 0;
         if (ok && corr && i > 0) {
           // Rescale the O^T columns (hi and lo) of rows whose reference moved
-          // (rare).  o_done is at most one phase behind here: s_full(i)
-          // implies PV(i-2) completed, and PV(i) is not issued before this
-          // tile's p_full.
-          ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, p.wait_cycles);
+          // (rare), once PV(i-1) is done.  PV completions alternate between
+          // two barriers, and the one of PV(i-1)'s parity is within one phase
+          // of the awaited one: s_full(i) implies PV(i-2) completed (QK(i)
+          // waits for it) and PV(i+1) needs a later tile's P^T.
+          ok = mbar_wait(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE), ((i - 1) >> 1) & 1,
+                         p.wait_cycles);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
             tc_fence_after();

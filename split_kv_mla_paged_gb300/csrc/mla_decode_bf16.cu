@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
 namespace q16 {
 constexpr int NR = 16;
 constexpr int NST = 3;
-constexpr int kThreads = 64 + 128;
+constexpr int kThreads = 96 + 128;  // TMA, QK issuer, PV issuer, softmax warpgroup
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kQCol = 0;      // 288 columns
 constexpr uint32_t kSCol = 288;    // 2 x 64 columns
@@ -659,6 +659,11 @@ constexpr uint32_t kEnd = kAlpha + 64;
 constexpr uint32_t kSmemBytes = kEnd + 1024;
 static_assert(kSmemBytes <= 232448u, "shared memory");
 constexpr int BAR_QTMEM = BAR_PFREE0;  // Q copied into TMEM (128 arrivals)
+// PV(i) completion, alternating by tile parity (this kernel has no P^T
+// buffer barriers): with QK and PV issued by different warps, a waiter is
+// then never more than one phase away from the phase it waits for.
+constexpr int BAR_ODONE_0 = BAR_ODONE;
+constexpr int BAR_ODONE_1 = BAR_PFREE1;
 }  // namespace q16
 
 __global__ void __launch_bounds__(q16::kThreads, 1)
@@ -727,8 +732,9 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
     mbar_init(bar(BAR_SFREE1), 128);
     mbar_init(bar(BAR_PFULL0), 128);
     mbar_init(bar(BAR_PFULL1), 128);
-    mbar_init(bar(BAR_ODONE), 1);
-    mbar_init(bar(BAR_FINAL), 1);
+    mbar_init(bar(BAR_ODONE_0), 1);
+    mbar_init(bar(BAR_ODONE_1), 1);
+    mbar_init(bar(BAR_FINAL), 2);  // one commit from each MMA warp
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;
@@ -823,11 +829,13 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
       mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ================= MMA issuer =================
+  } else if (warp == 1 || warp == 2) {
+    // ================= MMA issuers: warp 1 QK, warp 2 PV =================
+    // Two issuing warps keep the tensor pipe fed with QK(i + 1) while PV(i)
+    // goes out (one warp issuing both left ~30 % of the pipe's rate unused).
     constexpr uint32_t kIdQK = idesc_bf16(128, 64, 0, 0);
     constexpr uint32_t kIdPV = idesc_bf16(128, NR, 1, 0);
-    bool ok = mbar_wait(bar(BAR_QTMEM), 0, p.wait_cycles);
+    bool ok = (warp == 1) ? mbar_wait(bar(BAR_QTMEM), 0, p.wait_cycles) : true;
     auto fail = [&]() {
       if (lane == 0) {
         report(p.status, MLA_ERR_TIMEOUT);
@@ -851,7 +859,7 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
         }
       }
       umma_commit(bar(BAR_EMPTY0 + jst));
-      umma_commit(bar(BAR_ODONE));
+      umma_commit(bar((j & 1) ? BAR_ODONE_1 : BAR_ODONE_0));
     };
     auto issue_qk = [&](int ist, int sb) {
       tc_fence_after();
@@ -867,11 +875,7 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) fail();
     tc_fence_after();
-    // Fixed issue order QK(i+1), PV(i): with 52 MMAs per 64-token tile this
-    // kernel is bound by MMA issue, so the next tile has landed by the time
-    // QK(i+1) is due and P(i) is ready when QK(i+1) has gone out (the softmax
-    // of a tile is shorter than a QK); direct waits on one barrier at a time
-    // keep the issue warp busy.
+    // Each warp waits on one barrier at a time, in tile order.
     auto qk_step = [&](int j) -> bool {
       const int st = j % NST;
       bool w = mbar_wait(bar(BAR_FULL0 + st), (j / NST) & 1, p.wait_cycles);
@@ -897,18 +901,33 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
       __syncwarp();
       return true;
     };
-    if (ok && n_tiles > 0) ok = qk_step(0);
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      if (i + 1 < n_tiles) ok = qk_step(i + 1);
-      if (!ok) break;
-      bool w = mbar_wait(bar(BAR_PFULL0 + (i & 1)), (i >> 1) & 1, p.wait_cycles);
-      w = __all_sync(0xffffffffu, w && !*abort_flag);
-      if (!w) {
-        ok = false;
-        break;
+    if (warp == 1) {
+      // QK(j) once its tile has landed, its S^T buffer is free and PV(j - 2)
+      // has completed (which keeps the softmax's wait for PV(j - 1) within
+      // one phase of its barrier; QK(j) still overlaps PV(j - 1)).
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j >= 2) {
+          bool w = mbar_wait(bar(((j - 2) & 1) ? BAR_ODONE_1 : BAR_ODONE_0), ((j - 2) >> 1) & 1,
+                             p.wait_cycles);
+          w = __all_sync(0xffffffffu, w && !*abort_flag);
+          if (!w) {
+            ok = false;
+            break;
+          }
+        }
+        ok = qk_step(j);
       }
-      if (lane == 0) issue_pv(i, i % NST);
-      __syncwarp();
+    } else {
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        bool w = mbar_wait(bar(BAR_PFULL0 + (i & 1)), (i >> 1) & 1, p.wait_cycles);
+        w = __all_sync(0xffffffffu, w && !*abort_flag);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) issue_pv(i, i % NST);
+        __syncwarp();
+      }
     }
     if (!ok) fail();
     if (lane == 0) umma_commit(bar(BAR_FINAL));
@@ -921,7 +940,7 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
     const int row = lidx & 15;              // query row of this thread
     const int slot = lidx >> 4;             // tokens 8*slot .. 8*slot + 7 of a tile
     const bool hi = lane >= 16;
-    const int sid = threadIdx.x - 64;       // 0..127; owner of row sid when < 16
+    const int sid = threadIdx.x - 96;       // 0..127; owner of row sid when < 16
     const uint32_t lane_addr = static_cast<uint32_t>(w * 32) << 16;
     bool ok = true;
     // ---- Q: staged rows -> TMEM (lane l gets row l % 16) ----
@@ -1013,7 +1032,11 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
         kreg = kref[row];
         const bool corr = flags[0] != 0;
         if (ok && corr && i > 0) {
-          ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, p.wait_cycles);
+          // PV(i - 1) done.  PV(i - 2) completed before QK(i) was issued and
+          // PV(i + 1) needs this tile's P^T, so the barrier of PV(i - 1)'s
+          // parity is within one phase of the awaited one.
+          ok = mbar_wait(bar(((i - 1) & 1) ? BAR_ODONE_1 : BAR_ODONE_0), ((i - 1) >> 1) & 1,
+                         p.wait_cycles);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
             tc_fence_after();
