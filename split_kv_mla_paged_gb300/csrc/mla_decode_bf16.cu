@@ -86,6 +86,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// PV(i) completion of the 32/48-row kernel alternates between BAR_ODONE and
+// this slot (P^T lives in the KV stages, so the P^T-free barriers are unused).
+constexpr int kBarOdone1B = BAR_PFREE1;
+
 template <int NR>
 struct CfgB {
   static_assert(NR % 16 == 0 && NR >= 16 && NR <= kMaxRowsPerCta, "NR");
@@ -98,7 +102,9 @@ struct CfgB {
   static constexpr int SWG = NR >= 32 ? 2 : 1;
   static constexpr int NRH = NR / SWG;
   static_assert(NRH % 8 == 0, "rows per softmax warpgroup");
-  static constexpr int kThreads = 64 + 128 * SWG;
+  // Warp 0 TMA, warp 1 QK issuer (and TMEM owner), warp 2 PV issuer, then
+  // the softmax warpgroups.
+  static constexpr int kThreads = 96 + 128 * SWG;
   static constexpr uint32_t kPBytes = NR * kTokB * 2;  // BF16 P^T, in the rope block
   static_assert(kPBytes <= kBlkBytesB, "P^T must fit the rope block");
   static constexpr int NST = 2;
@@ -187,7 +193,8 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
     mbar_init(bar(BAR_PFULL0), 128 * C::SWG);
     mbar_init(bar(BAR_PFULL1), 128 * C::SWG);
     mbar_init(bar(BAR_ODONE), 1);
-    mbar_init(bar(BAR_FINAL), 1);
+    mbar_init(bar(kBarOdone1B), 1);
+    mbar_init(bar(BAR_FINAL), 2);  // one commit from each MMA warp
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;
@@ -280,11 +287,11 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
       mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ================= MMA issuer =================
+  } else if (warp == 1 || warp == 2) {
+    // ================= MMA issuers: warp 1 QK, warp 2 PV =================
     constexpr uint32_t kIdQK = idesc_bf16(64, NR, 0, 0);
     constexpr uint32_t kIdPV = idesc_bf16(128, NR, 1, 1);
-    bool ok = mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles);
+    bool ok = (warp == 1) ? mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles) : true;
     auto fail = [&]() {
       if (lane == 0) {
         report(p.status, MLA_ERR_TIMEOUT);
@@ -311,7 +318,7 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
         }
       }
       umma_commit(bar(BAR_EMPTY0 + jst));
-      umma_commit(bar(BAR_ODONE));
+      umma_commit(bar((j & 1) ? kBarOdone1B : BAR_ODONE));
     };
     // QK of a tile (KV in stage ist) into S buffer sb.
     auto issue_qk = [&](int ist, int sb) {
@@ -329,37 +336,29 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
     };
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) fail();
-    // Issue loop: PV(pv) as soon as its P^T is ready, QK(qk) as soon as its
-    // tile has landed and its S^T buffer is free; QK at most one tile ahead.
-    int qk = 0, pv = 0;
-    int qk_st = 0, qk_round = 0, pv_st = 0;
-    long long t_last = clock64();
-    while (ok && pv < n_tiles) {
-      int action = 0;
-      if (lane == 0) {
-        if (pv < qk && mbar_test_wait(bar(BAR_PFULL0 + (pv & 1)), (pv >> 1) & 1)) action = 1;
-        if (action == 0 && qk < n_tiles && qk <= pv + 1) {
-          const int use = qk >> 1;
-          if (mbar_test_wait(bar(BAR_FULL0 + qk_st), qk_round & 1) &&
-              (use < 1 || mbar_test_wait(bar(BAR_SFREE0 + (qk & 1)), (use - 1) & 1)))
-            action = 2;
+    if (warp == 1) {
+      // QK(j) once its tile has landed, its S^T buffer is free and PV(j - 2)
+      // has completed (two stages: the tile's stage was freed by PV(j - 2)
+      // anyway; the wait keeps the softmax's PV(j - 1) wait exact).
+      int st = 0, round = 0;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int use = j >> 1;
+        bool w = mbar_wait(bar(BAR_FULL0 + st), round & 1, p.wait_cycles);
+        if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + (j & 1)), (use - 1) & 1, p.wait_cycles);
+        if (w && j >= 2)
+          w = mbar_wait(bar(((j - 2) & 1) ? kBarOdone1B : BAR_ODONE), ((j - 2) >> 1) & 1,
+                        p.wait_cycles);
+        w = __all_sync(0xffffffffu, w && !*abort_flag);
+        if (!w) {
+          ok = false;
+          break;
         }
-      }
-      action = __shfl_sync(0xffffffffu, action, 0);
-      if (action == 1) {
-        if (lane == 0) issue_pv(pv, pv_st);
-        __syncwarp();
-        ++pv;
-        if (++pv_st == C::NST) pv_st = 0;
-        t_last = clock64();
-      } else if (action == 2) {
-        const int tile_tok0 = tok_begin + qk * kTokB;
-        const int valid = tok_end - tile_tok0;
+        const int valid = tok_end - (tok_begin + j * kTokB);
         if (valid < kTokB) {
           // Rows past the split's end (unloaded pages or a last page's tail):
           // zero them so V holds no stale or NaN values.
           const int nrow = kTokB - valid;
-          uint8_t* kvp = base + C::kKV + qk_st * kTileBytesB;
+          uint8_t* kvp = base + C::kKV + st * kTileBytesB;
           const uint4 z = make_uint4(0, 0, 0, 0);
           for (int idx = lane; idx < nrow * 72; idx += 32) {
             const int r = valid + idx / 72;
@@ -369,22 +368,29 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (lane == 0) issue_qk(qk_st, qk & 1);
+        if (lane == 0) issue_qk(st, j & 1);
         __syncwarp();
-        ++qk;
-        if (++qk_st == C::NST) {
-          qk_st = 0;
-          ++qk_round;
-        }
-        t_last = clock64();
-      } else {
-        const bool late = (clock64() - t_last > p.wait_cycles) || *abort_flag;
-        if (__any_sync(0xffffffffu, late)) {
-          fail();
-          ok = false;
+        if (++st == C::NST) {
+          st = 0;
+          ++round;
         }
       }
+    } else {
+      // PV(i) as soon as its P^T is ready.
+      int st = 0;
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        bool w = mbar_wait(bar(BAR_PFULL0 + (i & 1)), (i >> 1) & 1, p.wait_cycles);
+        w = __all_sync(0xffffffffu, w && !*abort_flag);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) issue_pv(i, st);
+        __syncwarp();
+        if (++st == C::NST) st = 0;
+      }
     }
+    if (!ok) fail();
     if (lane == 0) umma_commit(bar(BAR_FINAL));
     __syncwarp();
     mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
@@ -396,11 +402,11 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
     constexpr int NRH = C::NRH;
     constexpr int NT = 128 * C::SWG;
     const int quad = warp & 3;
-    const int rbase = ((warp - 2) >> 2) * NRH;
+    const int rbase = ((warp - 3) >> 2) * NRH;
     const bool has_tok = lane < 16;
     const int tok = quad * 16 + lane;       // token index within the tile (when has_tok)
     const int dim_lane = quad * 32 + lane;  // TMEM lane for O^T (M = 128 layout)
-    const int sid = threadIdx.x - 64;
+    const int sid = threadIdx.x - 96;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     float k_row = -INFINITY;
     float l_row = 0.0f;
@@ -491,7 +497,10 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
         for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
         const bool corr = flags[0] != 0;
         if (ok && corr && i > 0) {
-          ok = mbar_wait(bar(BAR_ODONE), (i - 1) & 1, p.wait_cycles);
+          // PV(i - 1) done; PV completions alternate between two barriers
+          // and the one of PV(i - 1)'s parity is within one phase of it.
+          ok = mbar_wait(bar(((i - 1) & 1) ? kBarOdone1B : BAR_ODONE), ((i - 1) >> 1) & 1,
+                         p.wait_cycles);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
             tc_fence_after();
