@@ -31,9 +31,10 @@
 //    ex2(t - rint(t)) * 2^(rint(t) - k + 8).  Every rescale is then an exact
 //    power of two, so the E4M3-quantised P fed to the PV MMA, and every
 //    partial, is the same for any split plan up to exact scaling.
-//  * Warp roles: warp 0 issues TMA, warp 1 issues tcgen05.mma (and owns TMEM),
-//    warps 2-5 (and 6-9 from 32 rows up; TMEM lane quadrant = warp % 4) run
-//    the softmax, the rare O correction and the epilogue.
+//  * Warp roles: warp 0 issues TMA, warp 1 issues the QK tcgen05.mma (and
+//    owns TMEM), warp 2 the PV ones (the 96-row CTA issues both from warp 1),
+//    and the next four warps (eight from 32 rows up; TMEM lane quadrant =
+//    warp % 4) run the softmax, the rare O correction and the epilogue.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       bool my_load;
       uint32_t info = 0;
       if constexpr (kGather) {
-        // Rows to load of pages 0-3, one byte each, for the MMA warp (which
+        // Rows to load of pages 0-3, one byte each, for the QK warp (which
         // zeroes the rest); published by the arrive below.
         const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
         my_load = my_nv > 0;
@@ -653,7 +654,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     __syncwarp();
     mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
   } else {
-    // ================= softmax warpgroups (warps 2 .. 2 + 4*SWG) =================
+    // ===== softmax warpgroups (warps kSoftmaxWarp0 .. kSoftmaxWarp0 + 4*SWG - 1) =====
     // SWG warpgroups share each tile: warpgroup g owns rows [g*NRH, (g+1)*NRH)
     // of every token (two warps per SM sub-partition when SWG = 2, so one
     // warp's latency hides behind the other's).  TMEM lane quadrant = warp % 4.
@@ -864,7 +865,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       // [term][NR/16 row groups][128 tokens][16 rows]; this thread writes its
       // token's bytes for rows rbase .. rbase + NRH, 16 (or 8) rows per store.
       // P barriers (and buffers) alternate by tile parity unless there is a
-      // single P^T buffer; the MMA warp uses the same rule.
+      // single P^T buffer; the PV issuer uses the same rule.
       const int pb = (C::NPB == 1) ? 0 : (i & 1);
       const int puse = (C::NPB == 1) ? i : (i >> 1);
       if (ok && !C::kPInStage && puse >= 1) {
@@ -961,7 +962,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       scale_s[sid] = sc;
     }
     named_bar_sync(kSoftmaxBarrier, NT);
-    // The MMA warp commits BAR_FINAL once, after its last MMA.
+    // Each MMA warp commits BAR_FINAL once, after its last MMA.
     bool fin = mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
     fin = __all_sync(0xffffffffu, fin);
     if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);

@@ -19,6 +19,8 @@
 //  * Row groups of at most 16 rows run a variant with Q in TMEM (see
 //    mla_split_kv_bf16_q16_kernel below); the description above is the
 //    kernel for 32 and 48 rows.
+//  * As in the FP8 kernel, warp 1 issues QK and warp 2 PV, and PV
+//    completions alternate between two barriers by tile parity.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
