@@ -60,6 +60,7 @@ def test_tiny_config_gb300_plan():
     (1, 16, 5, [900], True),        # 80 rows
     (2, 12, 8, [4096, 2500], True), # 96 rows
     (1, 16, 8, [1500], True),       # 128 rows -> two groups of 64
+    (2, 25, 4, [1200, 700], True),  # 100 rows -> two groups of 50 in 96-row CTAs
     (1, 96, 8, [600], True),        # 768 rows -> eight groups of 96
 ])
 def test_parity_shapes(B, H, q_len, lens, causal):
@@ -113,6 +114,16 @@ def test_maximum_splits_per_request():
     plan = mla.mla_decode_plan([32768], 12, 1, sm_count=256)
     assert plan.max_splits == mla.MAX_SPLITS == 256 and plan.kv_split == 16
     _full_check(inp, False, SOFTMAX_SCALE, plan=plan)
+
+
+def test_many_row_merge_fits_one_wave():
+    # 96 rows over ~96 splits: 16 merge groups and rows x 4 CTAs above two per
+    # SM, the case the one-wave merge kernel serves.
+    inp = decode_inputs(1, 12, 8, [12288], seed=24)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = mla.mla_decode_plan([12288], 12, 8, sm_count=sms)
+    assert plan.kv_split == 16 and 96 * 4 > 2 * sms
+    _full_check(inp, True, SOFTMAX_SCALE, plan=plan)
 
 
 def test_deterministic_run_to_run():
