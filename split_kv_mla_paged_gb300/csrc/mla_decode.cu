@@ -137,6 +137,48 @@ struct Cfg {
 };
 
 
+// Rows of a staged tile that hold no loaded key: pages that were not loaded
+// (past the split's end, outside a window or an unused selection slot) and
+// the tail of a request's last page.  The warp zeroes them (all 576 bytes of
+// a row: four 128-byte latent blocks and the 64-byte rope block) so V holds
+// no stale or NaN bytes (0 * NaN would poison the PV sum).  kGather: `info`
+// holds the rows loaded per page, one byte each; otherwise the first `valid`
+// rows of the tile are keys of the split.
+template <bool kGather>
+__device__ __forceinline__ void zero_unloaded_rows(uint8_t* kvp, int lane, uint32_t info,
+                                                   int valid) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  auto zero_rows = [&](int r0, int nrow) {
+    for (int idx = lane; idx < nrow * 36; idx += 32) {
+      const int r = r0 + idx / 36;
+      const int c = idx % 36;
+      uint4* dst;
+      if (c < 32)
+        dst = reinterpret_cast<uint4*>(kvp + (c / 8) * kLatBlockBytes + r * 128 + (c % 8) * 16);
+      else
+        dst = reinterpret_cast<uint4*>(kvp + kRopeOffset + r * 64 + (c - 32) * 16);
+      *dst = z;
+    }
+  };
+  if constexpr (kGather) {
+    if (info != 0x20202020u) {
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const int nv = static_cast<int>((info >> (8 * q)) & 0xFFu);
+        if (nv < MLA_PAGE_SIZE) zero_rows(q * MLA_PAGE_SIZE + nv, MLA_PAGE_SIZE - nv);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+  } else {
+    if (valid < kTileTokens) {
+      zero_rows(valid, kTileTokens - valid);
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+  }
+}
+
 // kGather: the variant for restricted key sets (key windows, selected pages):
 // tiles may have pages that are not loaded, and every score is masked by its
 // key position.  The plain variant (kGather = false) covers full key ranges,
@@ -508,48 +550,15 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           if (++pv_st == C::NST) pv_st = 0;
           t_last = clock64();
         } else if (action == 2) {
-          // Rows that hold no loaded key: pages that were not loaded (past the
-          // split's end, outside a window or an unused selection slot) and the
-          // tail of a request's last page.  Zero them so V holds no stale or NaN
-          // bytes (0 * NaN would poison the PV sum).
-          uint8_t* kvp = base + C::kKV + qk_st * kTileBytes;
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          auto zero_rows = [&](int r0, int nrow) {
-            for (int idx = lane; idx < nrow * 36; idx += 32) {
-              const int r = r0 + idx / 36;
-              const int c = idx % 36;
-              uint4* dst;
-              if (c < 32)
-                dst = reinterpret_cast<uint4*>(kvp + (c / 8) * kLatBlockBytes + r * 128 + (c % 8) * 16);
-              else
-                dst = reinterpret_cast<uint4*>(kvp + kRopeOffset + r * 64 + (c - 32) * 16);
-              *dst = z;
-            }
-          };
+          // Rows loaded per page, as the producer published them with the
+          // stage's full barrier (which lane 0 has just observed).
+          uint32_t info = 0;
           if constexpr (kGather) {
-            // Rows loaded per page, as the producer published them with the
-            // stage's full barrier (which lane 0 has just observed).
-            uint32_t info = 0;
             if (lane == 0) info = *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * qk_st);
             info = __shfl_sync(0xffffffffu, info, 0);
-            if (info != 0x20202020u) {
-  #pragma unroll 1
-              for (int q = 0; q < 4; ++q) {
-                const int nv = static_cast<int>((info >> (8 * q)) & 0xFFu);
-                if (nv < MLA_PAGE_SIZE) zero_rows(q * MLA_PAGE_SIZE + nv, MLA_PAGE_SIZE - nv);
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-            }
-          } else {
-            const int tile_tok0 = t0 + qk * kTileTokens;
-            const int valid = tok_end - tile_tok0;  // tokens of this tile inside the split
-            if (valid < kTileTokens) {
-              zero_rows(valid, kTileTokens - valid);
-              fence_proxy_async_smem();
-              __syncwarp();
-            }
           }
+          zero_unloaded_rows<kGather>(base + C::kKV + qk_st * kTileBytes, lane, info,
+                                      tok_end - (t0 + qk * kTileTokens));
           if (lane == 0) issue_qk(qk_st, (C::NS == 2) ? (qk & 1) : 0);
           __syncwarp();
           ++qk;
@@ -584,45 +593,12 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           ok = false;
           break;
         }
-        // Rows that hold no loaded key: pages that were not loaded (past the
-        // split's end, outside a window or an unused selection slot) and the
-        // tail of a request's last page.  Zero them so V holds no stale or NaN
-        // bytes (0 * NaN would poison the PV sum).
-        uint8_t* kvp = base + C::kKV + st * kTileBytes;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        auto zero_rows = [&](int r0, int nrow) {
-          for (int idx = lane; idx < nrow * 36; idx += 32) {
-            const int r = r0 + idx / 36;
-            const int c = idx % 36;
-            uint4* dst;
-            if (c < 32)
-              dst = reinterpret_cast<uint4*>(kvp + (c / 8) * kLatBlockBytes + r * 128 + (c % 8) * 16);
-            else
-              dst = reinterpret_cast<uint4*>(kvp + kRopeOffset + r * 64 + (c - 32) * 16);
-            *dst = z;
-          }
-        };
-        if constexpr (kGather) {
-          // Rows loaded per page, as the producer published them with the
-          // stage's full barrier (observed above).
-          const uint32_t info = *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st);
-          if (info != 0x20202020u) {
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-              const int nv = static_cast<int>((info >> (8 * q)) & 0xFFu);
-              if (nv < MLA_PAGE_SIZE) zero_rows(q * MLA_PAGE_SIZE + nv, MLA_PAGE_SIZE - nv);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-        } else {
-          const int valid = tok_end - (t0 + j * kTileTokens);  // tokens of this tile inside the split
-          if (valid < kTileTokens) {
-            zero_rows(valid, kTileTokens - valid);
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-        }
+        // Rows loaded per page, as the producer published them with the
+        // stage's full barrier (observed above).
+        const uint32_t info =
+            kGather ? *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st) : 0u;
+        zero_unloaded_rows<kGather>(base + C::kKV + st * kTileBytes, lane, info,
+                                    tok_end - (t0 + j * kTileTokens));
         if (lane == 0) issue_qk(st, sb);
         __syncwarp();
         if (++st == C::NST) {

@@ -120,6 +120,15 @@ def test_plan_items_are_the_ctas_with_work_in_split_major_order():
         assert np.all(np.diff(key) >= 0)
 
 
+def test_fp8_row_groups_over_all_row_counts():
+    # Up to 48 rows run in one CTA; above that, groups of at most 96 rows.
+    for rows in list(range(1, 200)) + [255, 256, 287, 288, 289, 767, 768, 769, 1000, 1024]:
+        items = mla.mla_decode_plan_items(np.array([1], np.int32), rows, 1)
+        want = 1 if rows <= 48 else -(-rows // 96)
+        assert items.shape[0] == want, rows
+        assert sorted((items & 31).tolist()) == list(range(want))
+
+
 def test_plan_items_rejects_bad_splits():
     with pytest.raises(mla.MlaError):
         mla.mla_decode_plan_items([2, 0], 12, 1)
