@@ -3,7 +3,6 @@ maximum over ranks and rank 0 alone prints."""
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
