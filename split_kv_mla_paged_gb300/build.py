@@ -10,7 +10,8 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_NAME = "libmla_decode.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = [os.path.join(CSRC, "mla_decode.cu"), os.path.join(CSRC, "mla_decode_bf16.cu"),
-           os.path.join(CSRC, "kv_append.cu"), os.path.join(CSRC, "plan.cpp")]
+           os.path.join(CSRC, "mla_merge.cu"), os.path.join(CSRC, "kv_append.cu"),
+           os.path.join(CSRC, "plan.cpp")]
 OBJ_DIR = os.path.join(HERE, "_build")
 DEPENDS = SOURCES + [
     os.path.join(CSRC, "mla_internal.h"),
