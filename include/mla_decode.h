@@ -351,7 +351,7 @@ MLA_API int mla_kv_append(const void* rows_bf16, int64_t n_tokens, const int32_t
  * MLA_ERR_INVALID_ARG for a bad page id or inconsistent plan arrays,
  * MLA_ERR_TIMEOUT for a wait that ran out) after `stream` has drained, and
  * clears it. */
-MLA_API int mla_decode_status(void* workspace, void* stream);
+MLA_API int mla_decode_status(const void* workspace, void* stream);
 
 /*
  * Decode without a workspace argument, for callers that cannot allocate
@@ -366,12 +366,16 @@ MLA_API int mla_decode_status(void* workspace, void* stream);
  * (mla_decode_workspace_size) would exceed it returns
  * MLA_ERR_WORKSPACE_TOO_SMALL.  The call allocates nothing.
  *
- * The first call on a device resolves the array's device address on that
- * device (the current device), so make that first call before any stream
- * capture.  All calls share the one array: calls that overlap on the GPU (on
- * different streams, or from different threads) race on it and must be
- * serialised by the caller.  Each call resets the status word; the device
- * status of these calls is not readable through mla_decode_status.
+ * The first call on a device (and the first after the device's context has
+ * been replaced, e.g. by cudaDeviceReset) resolves the array's device address
+ * on that device (the current device) and zeroes its status header with a
+ * synchronous cudaMemset, so make that first call before any stream capture.
+ * All calls share the one array: calls that overlap on the GPU (on different
+ * streams, or from different threads) race on it and must be serialised by
+ * the caller.  Conditions the device detects (a bad page id, inconsistent
+ * plan arrays, a wait that ran out) go to the array's status word, which
+ * stays set across calls until mla_decode_static_ws_status reads and clears
+ * it; the output of such a call is not valid.
  */
 #define MLA_STATIC_WS_BYTES (16u * 1024u * 1024u)
 MLA_API int mla_decode_static_ws(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
@@ -382,6 +386,14 @@ MLA_API int mla_decode_static_ws(const void* q_fp8, const void* kv_pages_fp8, in
                                  float q_scale, float kv_scale, float softmax_scale,
                                  void* out_bf16, float* lse_f32, float* out_f32_debug,
                                  void* stream);
+
+/* Status of mla_decode_static_ws calls (no counterpart on the pages): waits
+ * for `stream` to drain, then reads and clears the status word of the fixed
+ * scratch array on the current device, like mla_decode_status does for a
+ * caller-owned workspace.  Returns MLA_OK, MLA_ERR_INVALID_ARG (bad page id or
+ * inconsistent plan arrays in some call since the last read) or
+ * MLA_ERR_TIMEOUT.  Allocates nothing. */
+MLA_API int mla_decode_static_ws_status(void* stream);
 
 /* Test hook.  Sets the limit, in SM clock cycles, of the split-KV kernel's
  * pipeline waits for launches made after the call (0 restores the default of

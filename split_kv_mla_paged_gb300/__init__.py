@@ -22,8 +22,9 @@ __all__ = [
     "MLA_ERR_CUDA", "MLA_ERR_TIMEOUT", "MlaError", "Plan", "load_library", "library_path",
     "mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init", "mla_decode",
     "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
-    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16",
-    "mla_decode_sparse", "mla_decode_plan_items", "mla_decode_bf16_ex", "DecodeOptions",
+    "mla_decode_static_ws", "mla_decode_static_ws_status", "mla_kv_append", "mla_decode_ex",
+    "mla_decode_bf16", "mla_decode_sparse", "mla_decode_plan_items", "mla_decode_bf16_ex",
+    "DecodeOptions",
     "decode", "merge",
     "EXPORTED_SYMBOLS",
 ]
@@ -41,8 +42,9 @@ _STATUS_NAMES = {
 EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_workspace_init",
                     "mla_decode", "mla_decode_splitkv", "mla_decode_merge", "mla_merge",
                     "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit",
-                    "mla_decode_static_ws", "mla_kv_append", "mla_decode_ex", "mla_decode_bf16",
-                    "mla_decode_sparse", "mla_decode_plan_items", "mla_decode_bf16_ex")
+                    "mla_decode_static_ws", "mla_decode_static_ws_status", "mla_kv_append",
+                    "mla_decode_ex", "mla_decode_bf16", "mla_decode_sparse",
+                    "mla_decode_plan_items", "mla_decode_bf16_ex")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
@@ -119,6 +121,8 @@ def load_library() -> ctypes.CDLL:
         lib.mla_decode_static_ws.restype = ctypes.c_int
         lib.mla_decode_static_ws.argtypes = [vp, vp, i64, vp, i32, vp, vp, vp, i32, i32, i32, i32,
                                              i32, i32, f32, f32, f32, vp, vp, vp, vp]
+        lib.mla_decode_static_ws_status.restype = ctypes.c_int
+        lib.mla_decode_static_ws_status.argtypes = [vp]
         lib.mla_kv_append.restype = ctypes.c_int
         lib.mla_kv_append.argtypes = [vp, i64, vp, vp, vp, i32, i32, vp, i64, f32, vp, vp]
         lib.mla_debug_set_wait_limit.restype = None
@@ -340,6 +344,7 @@ def mla_decode_static_ws(q_fp8, kv_pages_fp8, num_pages: int, page_table,
     (MLA_STATIC_WS_BYTES = 16 MiB per GPU), so no workspace is passed.  The
     first call on a device resolves that array's address and should come
     before any stream capture; calls that overlap on the GPU race on the array.
+    Device-detected conditions are read with mla_decode_static_ws_status().
     """
     lib = load_library()
     _check(lib.mla_decode_static_ws(
@@ -351,6 +356,14 @@ def mla_decode_static_ws(q_fp8, kv_pages_fp8, num_pages: int, page_table,
 
 
 STATIC_WS_BYTES = 16 * 1024 * 1024
+
+
+def mla_decode_static_ws_status(stream=None) -> int:
+    """Read and clear the status word of mla_decode_static_ws's fixed scratch
+    array (after `stream` drains); raises MlaError on a non-OK status."""
+    st = load_library().mla_decode_static_ws_status(_stream_handle(stream))
+    _check(st)
+    return st
 
 
 def mla_kv_append(rows_bf16, n_tokens: int, req_idx, positions, page_table,

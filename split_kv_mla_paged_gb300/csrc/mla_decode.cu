@@ -1398,25 +1398,67 @@ namespace mla {
 static __device__ __align__(256) uint8_t g_static_ws[MLA_STATIC_WS_BYTES];
 
 // Device address of g_static_ws on each device (host code cannot use the
-// symbol itself as a device pointer), resolved once per device.
+// symbol itself as a device pointer), resolved at set-up: once per device and
+// CUDA context.  The context id is kept with the address so that, after a
+// cudaDeviceReset (which unloads the library's module and may reload it
+// elsewhere), the next call resolves the address again instead of using a
+// stale one.
 static std::mutex g_static_ws_mu;
 static void* g_static_ws_ptr[64] = {nullptr};
+static unsigned long long g_static_ws_ctx[64] = {0};
 
-static int static_ws_address(void** out) {
+typedef CUresult (*PfnCtxGetCurrent)(CUcontext*);
+typedef CUresult (*PfnCtxGetId)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if it cannot be read).
+static unsigned long long current_ctx_id() {
+  static PfnCtxGetCurrent get_cur = nullptr;
+  static PfnCtxGetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PfnCtxGetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PfnCtxGetId>(f);
+  });
+  if (!get_cur || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+static int static_ws_address(void** out, const char* who) {
+  const std::string w(who);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail("mla_decode_static_ws: cudaGetDevice", e);
+  if (e != cudaSuccess) return cuda_fail((w + ": cudaGetDevice").c_str(), e);
   if (dev < 0 || dev >= 64) {
-    set_error("mla_decode_static_ws: device ordinal above 63");
+    set_error(w + ": device ordinal above 63");
     return MLA_ERR_UNSUPPORTED;
   }
   std::lock_guard<std::mutex> lock(g_static_ws_mu);
-  if (!g_static_ws_ptr[dev]) {
+  // Before the runtime's first use of the device no context is current yet
+  // (id 0); cudaGetSymbolAddress below makes the primary context current.
+  unsigned long long ctx = current_ctx_id();
+  const bool stale = g_static_ws_ptr[dev] && ctx != 0 && ctx != g_static_ws_ctx[dev];
+  if (!g_static_ws_ptr[dev] || stale) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_static_ws);
-    if (e != cudaSuccess || !ptr)
-      return cuda_fail("mla_decode_static_ws: cudaGetSymbolAddress", e);
+    if (e != cudaSuccess || !ptr) return cuda_fail((w + ": cudaGetSymbolAddress").c_str(), e);
+    if (ctx == 0) ctx = current_ctx_id();  // the call above made the context current
+    // The status header starts at zero on a fresh set-up (after that it is
+    // only set by the device and cleared by mla_decode_static_ws_status).
+    e = cudaMemset(ptr, 0, kStatusBytes);
+    if (e != cudaSuccess) return cuda_fail((w + ": status header reset").c_str(), e);
     g_static_ws_ptr[dev] = ptr;
+    g_static_ws_ctx[dev] = ctx;
   }
   *out = g_static_ws_ptr[dev];
   return MLA_OK;
@@ -1444,20 +1486,27 @@ extern "C" int mla_decode_static_ws(const void* q_fp8, const void* kv_pages_fp8,
     }
   }
   void* workspace = nullptr;
-  int rc = static_ws_address(&workspace);
+  int rc = static_ws_address(&workspace, "mla_decode_static_ws");
   if (rc != MLA_OK) return rc;
   const size_t workspace_bytes = MLA_STATIC_WS_BYTES;
   DecodeLaunch dl;
   rc = prepare_decode(MLA_DECODE_ARGS, "mla_decode_static_ws", &dl);
   if (rc != MLA_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents: the status word must start
-  // at zero (the partials are always written before they are read).
-  cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int), st);
-  if (e != cudaSuccess) return cuda_fail("mla_decode_static_ws: status reset", e);
+  // The array keeps the previous call's partials; every partial the merge
+  // reads is written by this call's split kernel first.  The status word is
+  // sticky: a condition any call reports stays until
+  // mla_decode_static_ws_status reads and clears it.
   rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
   if (rc != MLA_OK) return rc;
   return launch_decode_merge(dl, st);
+}
+
+extern "C" int mla_decode_static_ws_status(void* stream) {
+  void* workspace = nullptr;
+  int rc = static_ws_address(&workspace, "mla_decode_static_ws_status");
+  if (rc != MLA_OK) return rc;
+  return mla_decode_status(workspace, stream);
 }
 
 extern "C" void mla_debug_set_wait_limit(long long cycles) {
@@ -1482,8 +1531,9 @@ extern "C" int mla_merge(const float* partial_o, const float* partial_ml, int32_
     set_error("mla_merge: null pointer argument");
     return MLA_ERR_INVALID_ARG;
   }
-  if (rows < 1 || rows > 65535 || num_ctas_kv < 1) {
-    set_error("mla_merge: rows must be in [1, 65535] and num_ctas_kv >= 1");
+  // Rows run on grid x (up to 2^31 - 1 CTAs); offsets are 64-bit.
+  if (rows < 1 || num_ctas_kv < 1) {
+    set_error("mla_merge: rows and num_ctas_kv must be >= 1");
     return MLA_ERR_INVALID_ARG;
   }
   if (kv_split != 1 && kv_split != 2 && kv_split != 4 && kv_split != 8 && kv_split != 16) {
@@ -1514,7 +1564,7 @@ extern "C" int mla_merge(const float* partial_o, const float* partial_ml, int32_
   return MLA_OK;
 }
 
-extern "C" int mla_decode_status(void* workspace, void* stream) {
+extern "C" int mla_decode_status(const void* workspace, void* stream) {
   if (!workspace) {
     set_error("mla_decode_status: null workspace");
     return MLA_ERR_INVALID_ARG;
@@ -1525,7 +1575,7 @@ extern "C" int mla_decode_status(void* workspace, void* stream) {
   int v = 0;
   e = cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail("mla_decode_status: read", e);
-  e = cudaMemset(workspace, 0, sizeof(int));
+  e = cudaMemset(const_cast<void*>(workspace), 0, sizeof(int));
   if (e != cudaSuccess) return cuda_fail("mla_decode_status: clear", e);
   if (v == MLA_ERR_TIMEOUT) {
     set_error("mla_decode: a device wait ran out (timeout)");

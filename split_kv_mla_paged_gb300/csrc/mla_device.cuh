@@ -219,10 +219,7 @@ __device__ __forceinline__ void warp_reduce_rows(float* v, int lane, float* dst)
 }
 
 // ---------------------------------------------------------------------------
-// Merge (defined in mla_decode.cu).
-// ---------------------------------------------------------------------------
-// ---------------------------------------------------------------------------
-// Merge: one CTA per (128-dim quarter, row); G groups of 32 lanes, each lane
+// Merge (the kernels are defined in mla_merge.cu): one CTA per (128-dim quarter, row); G groups of 32 lanes, each lane
 // owning 4 consecutive dims.  Group g folds partials g, g+G, g+2G, ... with an
 // online softmax (4 loads in flight per step; slots past the end re-read the
 // step's first slot with weight 0), then group 0 combines the G group states

@@ -5,8 +5,10 @@ allocation, or a latency-critical path that cannot take cudaMalloc's implicit
 synchronisation) use this entry point: its scratch is a fixed array inside the
 library instead of a caller-provided workspace.  These tests check, through the
 C ABI, that it returns what mla_decode returns on two calls in a row (the
-second call sees the first call's leftovers in the shared array), and that a
-call needing more scratch than the array holds is refused with a clear error.
+second call sees the first call's leftovers in the shared array), that a call
+needing more scratch than the array holds is refused with a clear error, and
+that a condition the device detects (a bad page id) is reported by
+mla_decode_static_ws_status, which reads and clears the array's status word.
 
 This file is collected last on purpose; it passes alone in a fresh process
 and after the other tests.
@@ -62,6 +64,7 @@ def _run_both(inp, causal, target_ctas=0):
     mla.mla_decode_static_ws(*common, *got)
     torch.cuda.synchronize()
     mla.mla_decode_status(ws)
+    assert mla.mla_decode_static_ws_status() == mla.MLA_OK
     return ref, got, plan
 
 
@@ -101,3 +104,28 @@ def test_static_ws_refuses_oversized_scratch():
                                  True, 1.0, 1.0, SOFTMAX_SCALE, out)
     assert e.value.status == mla.MLA_ERR_WORKSPACE_TOO_SMALL
     assert "MLA_STATIC_WS_BYTES" in mla.mla_last_error()
+
+
+def test_static_ws_status_reports_a_bad_page_id():
+    # The split CTAs that meet a page id outside the pool stop early, so that
+    # call's output is not valid; the status word says so until it is read.
+    inp = decode_inputs(1, 12, 8, [6000], seed=33)
+    plan = mla.mla_decode_plan([6000], 12, 8, target_ctas=6)
+    assert plan.max_splits > 1
+    a = _device_args(inp, plan)
+    bad_pt = a["pt"].clone()
+    bad_pt[0, 40] = inp.num_pages + 9
+    out = _outputs(inp)
+    args = (a["q"], a["kv"], inp.num_pages, bad_pt, inp.max_pages, a["lens"], a["splits"],
+            a["chunks"], plan.max_splits, plan.kv_split, 1, 8, 12, True, 1.0, 1.0,
+            SOFTMAX_SCALE)
+    mla.mla_decode_static_ws(*args, *out)
+    # A second call with the same bad id: the word stays set (not reset per call).
+    mla.mla_decode_static_ws(*args, *out)
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode_static_ws_status()
+    assert e.value.status == mla.MLA_ERR_INVALID_ARG
+    # Read and cleared: the next good call reports OK and matches mla_decode.
+    assert mla.mla_decode_static_ws_status() == mla.MLA_OK
+    ref, got, _ = _run_both(inp, causal=True, target_ctas=6)
+    _assert_same(ref, got)
