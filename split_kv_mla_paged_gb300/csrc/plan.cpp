@@ -10,12 +10,14 @@
 //    an SM (its shared memory holds two or three 72 KB KV stages), so it
 //    balances whole waves of sm_count CTAs, with up to MLA_MAX_SPLITS splits
 //    per request (a single long request fills every SM): one chunk for the
-//    whole batch (the skewed-batch
-//    finding in the same issue's follow-up: a common split size plus early
-//    exit of empty split slots beats one wave per request), a minimum of one
-//    128-token tile per split (the short-KV finding there), and an estimate of
-//    each CTA's fixed cost (prologue plus the partial it writes and the merge
-//    reads) to trade waves against splits.
+//    whole batch (the skewed-batch finding in the same issue's follow-up: a
+//    common split size plus early exit of empty split slots beats one wave
+//    per request), a minimum of one 128-token tile per split (the short-KV
+//    finding there), at most two waves of CTAs (the 2 x SMs grid CTA budget
+//    of PR #20380, "Description"; only a batch whose requests alone exceed it
+//    gets one split each), and an estimate of each CTA's fixed cost (prologue
+//    plus the partial it writes and the merge reads) to choose between one
+//    and two waves.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -31,6 +33,9 @@ void set_error(const std::string& msg) { g_last_error = msg; }
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// The GB300 planner's CTA budget, in waves of sm_count CTAs.
+constexpr int kMaxWaves = 2;
 
 // CTAs the split kernel launches with a common chunk (empty slots excluded).
 static int64_t ctas_for_chunk(const int32_t* lens, int batch, int64_t chunk, int groups) {
@@ -108,7 +113,7 @@ extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t nu
     const int64_t cmax = std::max<int64_t>(cmin, round_up(lmax, T));
     int64_t best_chunk = cmax;
     double best_cost = -1.0;
-    for (int w = 1; w <= 16; ++w) {
+    for (int w = 1; w <= kMaxWaves; ++w) {
       const int64_t slots = static_cast<int64_t>(w) * sm_count;
       if (ctas_for_chunk(kv_lens, batch, cmax, rg.groups) > slots) continue;
       int64_t lo = cmin / T, hi = cmax / T;  // smallest chunk/T that fits `slots`

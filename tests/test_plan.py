@@ -62,6 +62,35 @@ def test_gb300_planner_invariants(lens, H, q, sm_count):
     assert np.all((p.splits - 1) * p.chunks.astype(np.int64) < L)
     assert p.kv_split in (1, 2, 4, 8, 16) and p.kv_split <= max(1, p.max_splits)
     assert p.workspace_bytes == mla.mla_decode_workspace_size(len(lens), q, H, p.max_splits)
+    # CTA budget: at most two waves (2 x SMs) of split-kernel CTAs, unless one
+    # split per request already exceeds it (then every request has one split).
+    ctas = int(p.splits.sum()) * _row_groups(H * q)
+    if len(lens) * _row_groups(H * q) <= 2 * sm_count:
+        assert ctas <= 2 * sm_count, (ctas, sm_count)
+    else:
+        assert np.all(p.splits == 1)
+
+
+def _row_groups(rows):
+    """CTAs per (request, split) of the FP8 split kernel: one CTA of up to 48
+    rows, else groups of at most 96 rows."""
+    return 1 if rows <= 48 else -(-rows // 96)
+
+
+def test_gb300_planner_stays_within_two_waves_on_every_workload():
+    from synth import WORKLOADS
+    for name, w in WORKLOADS.items():
+        lens = [32 * w["topk"]] * w["batch"] if w.get("topk") else w["kv_lens"]
+        p = mla.mla_decode_plan(lens, num_heads=w["num_heads"], q_len=w["q_len"], sm_count=152)
+        ctas = int(p.splits.sum()) * _row_groups(w["num_heads"] * w["q_len"])
+        assert ctas <= 2 * 152, (name, ctas)
+
+
+def test_gb300_planner_budget_with_many_requests():
+    # 64 requests x 8 row groups (H96 q8) exceed two waves with one split
+    # each: every request keeps one split.
+    p = mla.mla_decode_plan([100000] * 64, num_heads=96, q_len=8, sm_count=152)
+    assert np.all(p.splits == 1)
 
 
 def test_gb300_planner_fills_one_wave_for_uniform_long_batch():
