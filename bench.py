@@ -369,9 +369,12 @@ def merge_sweep(args):
 
     floor = time_graph(g)
     points = []
-    for rows in (12, 96, 192):
-        for S in (6, 25, 128):
-            for ks in (1, 4, 16):
+    # rows = B*q*H of the workloads (12 .. 192; 768 = H96 q8 B1), splits of
+    # the pages' and the GB300 planner's plans, every KvSplit.
+    for rows in (12, 96, 192, 768):
+        for S in (6, 12, 19, 25, 50, 100, 128, 152):
+            plan_ks = mla.mla_decode_plan([S * 128], 1, 1, sm_count=S).kv_split
+            for ks in (1, 2, 4, 8, 16):
                 if ks > S:
                     continue
                 o, ml = merge_partials(rows, S, seed=rows * 1000 + S)
@@ -394,6 +397,7 @@ def merge_sweep(args):
                         mla.mla_merge(o_d, ml_d, rows, S, ks, out, lse, None)
                 us = time_graph(gm)
                 points.append({"rows": rows, "splits": S, "kv_split": ks, "us": us,
+                               "planner_kv_split": plan_ks,
                                "partial_bytes": part_bytes,
                                "gbs": part_bytes / (us * 1e-6) / 1e9})
                 del gm, sets
