@@ -95,7 +95,7 @@ struct Cfg {
   // Reductions: tile maxima 16 NR B, row sums 32 NR B (double-buffered by
   // tile parity; 16 NR B, one buffer, with per-thread sums), references 4 NR B.
   static constexpr uint32_t kRedSumBytes = kWide ? 16 * NR : 32 * NR;
-  static constexpr uint32_t kAuxBytes = 176 + 20 * NR + kRedSumBytes;
+  static constexpr uint32_t kAuxBytes = 176 + 20 * NR + kRedSumBytes + (kWide ? 4 * NR : 0);
   static constexpr uint32_t kQBytes = NR * MLA_HEAD_DIM;
   // Three KV stages fit when P^T can live in the rope block of its own stage
   // (QK has consumed that block before P is written): NR = 16.  Otherwise two
@@ -127,7 +127,10 @@ struct Cfg {
   static constexpr uint32_t kAlpha = kRedMax;           // NR floats
   static constexpr uint32_t kRedSum = kRedMax + 16 * NR;  // (2 x) 4 x NR floats
   static constexpr uint32_t kKref = kRedSum + kRedSumBytes;  // NR floats
-  static constexpr uint32_t kEnd = kKref + 4 * NR;
+  // 96 rows: kref holds each row's vote threshold k + 0.75, and kKci its
+  // integer exponent offset for softmax_weight_kc (NR ints).
+  static constexpr uint32_t kKci = kKref + 4 * NR;
+  static constexpr uint32_t kEnd = kKci + (kWide ? 4 * NR : 0);
   static_assert(kEnd - kAux <= kAuxBytes, "aux layout");
   static_assert(NR != 16 || NST == 3, "16-row CTAs must keep three KV stages");
   static constexpr uint32_t kSmemBytes = kEnd + 1024;   // + alignment slack
@@ -303,6 +306,8 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     flags[1] = 0;
     flags[2] = 0;
     for (int r = 0; r < NR; ++r) kref[r] = -INFINITY;
+    if constexpr (C::kWide)
+      for (int r = 0; r < NR; ++r) reinterpret_cast<int*>(base + C::kKci)[r] = kKcNone;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -644,18 +649,15 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     float k_row = -INFINITY;  // owner state: reference (integer, log2 units)
     float l_row = 0.0f;       // owner state: sum of weights relative to k_row - 8
-    // This thread's copy of its rows' references; kWide reads them from
-    // shared memory instead (owners write kref only between B1 and B2, when
-    // every thread has passed the tile's vote and none has reached its
-    // weights), which keeps the 48-row thread within its registers.
+    // This thread's copy of its rows' references; the 96-row configuration
+    // reads its rows' thresholds and exponent offsets from shared memory
+    // instead (owners write them only between B1 and B2, when every thread
+    // has passed the tile's vote and none has reached its weights), which
+    // keeps the 48-row thread within its registers.
     float kreg[C::kWide ? 1 : NRH];
 #pragma unroll
     for (int k = 0; k < (C::kWide ? 1 : NRH); ++k) kreg[k] = -INFINITY;
-    auto ref = [&](int k) -> float {
-      if constexpr (C::kWide) return kref[rbase + k];
-      else return kreg[k];
-    };
-    // kWide: this thread's sums of its token's weights per row, relative to
+    // 96 rows: this thread's sums of its token's weights per row, relative to
     // the row's current reference (reduced once, after the last tile).
     float lsum[C::kWide ? NRH : 1];
 #pragma unroll
@@ -679,32 +681,12 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       sel_next = sel_window(1);
     }
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int sb = (C::NS == 2) ? (i & 1) : 0;
-      const int use = (C::NS == 2) ? (i >> 1) : i;
-      if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
-      ok = __all_sync(0xffffffffu, ok);
-      float t[NRH];
-      if (ok) {
-        tc_fence_after();
-        uint32_t r[NRH];
-#pragma unroll
-        for (int cc = 0; cc < NRH / 8; ++cc)
-          tmem_ld8(tmem + lane_addr + sb * NR + rbase + cc * 8,
-                   *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
-        tc_fence_before();
-        mbar_arrive(bar(BAR_SFREE0 + sb));
-      } else {
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
-      }
+    // Scale the scores of tile i by c and mask them (-inf): rows past the real
+    // query rows, tokens past the split, and (MTP verify) tokens after the
+    // row's query position; with restricted key sets the key position decides.
+    auto scale_mask = [&](float (&t)[NRH], int i) {
       const int tile_tok0 = t0 + i * kTileTokens;
       const int j = tile_tok0 + tok_lane;
-      // Scale and mask: rows past the real query rows, tokens past the split,
-      // and (MTP verify) tokens after the row's query position are -inf.
       if constexpr (kGather) {
         // Restricted key sets: the token's key position decides.
         int64_t pos = j;
@@ -746,79 +728,96 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           }
         }
       }
-      // Reference check.  A row's reference k only has to bound its scores:
-      // with p = 2^(t - k + 8), E4M3 holds p up to 448 = 2^8.8, so any k with
-      // t <= k + 0.75 works.  One vote finds whether some score of the tile
-      // exceeds its row's reference; only then (always on the first tile)
-      // are the tile maxima reduced and references raised to ceil(max).
-      bool over = false;
+    };
+    if constexpr (C::kWide) {
+      // 96 rows: each thread holds 48 rows of one token.  Per tile: load S^T
+      // and free it, scale and mask, vote on the rows' thresholds (k + 0.75,
+      // from shared memory), then weights from the rows' integer exponent
+      // offsets (softmax_weight_kc), the row sums of this thread, and P^T as
+      // hi and lo E4M3 terms through packed halves.
+      float* thr = kref;                                  // k + 0.75 per row
+      int* kci = reinterpret_cast<int*>(base + C::kKci);  // exponent offset per row
+      for (int i = 0; i < n_tiles; ++i) {
+        if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0), i & 1, p.wait_cycles);
+        ok = __all_sync(0xffffffffu, ok);
+        float t[NRH];
+        if (ok) {
+          tc_fence_after();
+          uint32_t r[NRH];
 #pragma unroll
-      for (int k = 0; k < NRH; ++k) over |= t[k] > ref(k) + 0.75f;
-      const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
-      // Owners fold the previous tile's row sums (relative to its reference).
-      if (!C::kWide && sid < NR && i > 0) {
-        const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
-        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
-      }
-      if (any_over) {
-        {
-          float tm[NRH];
+          for (int cc = 0; cc < NRH / 16; ++cc)
+            tmem_ld16(tmem + lane_addr + rbase + cc * 16,
+                      *reinterpret_cast<uint32_t(*)[16]>(&r[cc * 16]));
+          tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < NRH; ++k) tm[k] = t[k];
-          warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
-        }
-        // The correction flag: cleared before B1 (every read of its last
-        // value happened before this tile's vote), set by owners after B1,
-        // read by all after B2.
-        if (sid == 0) flags[0] = 0;
-        named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
-        if (sid < NR) {
-          const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
-                                 fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
-          float k_new = k_row;
-          if (mt > k_row + 0.75f) k_new = ceilf(mt);
-          float alpha = 1.0f;
-          if (k_new != k_row && k_row != -INFINITY) {
-            const int e = static_cast<int>(k_row - k_new);
-            alpha = (e < -126) ? 0.0f : pow2i(e);
-            flags[0] = 1;
-          }
-          l_row *= alpha;
-          k_row = k_new;
-          kref[sid] = k_new;
-          alpha_s[sid] = alpha;
-        }
-        named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
-        if constexpr (!C::kWide) {
-#pragma unroll
-          for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
+          for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
+          tc_fence_before();
+          mbar_arrive(bar(BAR_SFREE0));
         } else {
-          // Per-thread sums follow their rows' references (alpha = 1 where
-          // the reference did not move).
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
+        }
+        if (!kGather && my_rows == NRH && t0 + i * kTileTokens + kTileTokens <= lim_min) {
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) t[k] *= c;
+        } else {
+          scale_mask(t, i);
+        }
+        // Vote: does some score exceed its row's threshold?
+        bool over = false;
+#pragma unroll
+        for (int k4 = 0; k4 < NRH / 4; ++k4) {
+          const float4 th = *reinterpret_cast<const float4*>(thr + rbase + 4 * k4);
+          over |= (t[4 * k4] > th.x) | (t[4 * k4 + 1] > th.y) | (t[4 * k4 + 2] > th.z) |
+                  (t[4 * k4 + 3] > th.w);
+        }
+        const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
+        if (any_over) {
+          {
+            float tm[NRH];
+#pragma unroll
+            for (int k = 0; k < NRH; ++k) tm[k] = t[k];
+            warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
+          }
+          if (sid == 0) flags[0] = 0;
+          named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
+          if (sid < NR) {
+            const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
+                                   fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
+            float k_new = k_row;
+            if (mt > k_row + 0.75f) k_new = ceilf(mt);
+            float alpha = 1.0f;
+            if (k_new != k_row && k_row != -INFINITY) {
+              const int e = static_cast<int>(k_row - k_new);
+              alpha = (e < -126) ? 0.0f : pow2i(e);
+              flags[0] = 1;
+            }
+            k_row = k_new;
+            thr[sid] = k_new + 0.75f;
+            kci[sid] = (k_new == -INFINITY) ? kKcNone
+                                            : 135 - 0x4B400000 - static_cast<int>(k_new);
+            alpha_s[sid] = alpha;
+          }
+          named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
+          // This thread's sums follow their rows' references.
 #pragma unroll
           for (int k = 0; k < NRH; ++k) lsum[k] *= alpha_s[rbase + k];
-        }
-        const bool corr = flags[0] != 0;
-        if (ok && corr && i > 0) {
-          // Rescale the O^T columns (hi and lo) of rows whose reference moved
-          // (rare), once PV(i-1) is done.  PV completions alternate between
-          // two barriers, and the one of PV(i-1)'s parity is within one phase
-          // of the awaited one: s_full(i) implies PV(i-2) completed (QK(i)
-          // waits for it) and PV(i+1) needs a later tile's P^T.
-          ok = mbar_wait(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE), ((i - 1) >> 1) & 1,
-                         p.wait_cycles);
-          ok = __all_sync(0xffffffffu, ok);
-          if (ok) {
-            tc_fence_after();
+          const bool corr = flags[0] != 0;
+          if (ok && corr && i > 0) {
+            // Rescale the O^T columns of rows whose reference moved (rare),
+            // once PV(i - 1) is done (its completion barrier is within one
+            // phase of the awaited one, as in the other configurations).
+            ok = mbar_wait(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE), ((i - 1) >> 1) & 1,
+                           p.wait_cycles);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+              tc_fence_after();
 #pragma unroll 1
-            for (int d = 0; d < 4; ++d) {
-#pragma unroll
-              for (int half = 0; half < (C::kWide ? 1 : 2); ++half) {
+              for (int d = 0; d < 4; ++d) {
 #pragma unroll
                 for (int cc = 0; cc < NRH / 8; ++cc) {
                   uint32_t r[8];
-                  const uint32_t addr =
-                      tmem + lane_addr + C::kOCol + d * C::OW + half * NR + rbase + cc * 8;
+                  const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + rbase + cc * 8;
                   tmem_ld8(addr, r);
                   tmem_ld_wait();
 #pragma unroll
@@ -827,69 +826,206 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
                   tmem_st8(addr, r);
                 }
               }
+              tmem_st_wait();
             }
-            tmem_st_wait();
           }
         }
-      }
-      // Weights 2^(t - k + 8), exact power-of-two scaling.
+        // Weights 2^(t - k + 8) and this thread's row sums.
 #pragma unroll
-      for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], ref(k));
-      // P^T as two E4M3 terms into shared memory, MN-major:
-      // [term][NR/16 row groups][128 tokens][16 rows]; this thread writes its
-      // token's bytes for rows rbase .. rbase + NRH, 16 (or 8) rows per store.
-      // P barriers (and buffers) alternate by tile parity unless there is a
-      // single P^T buffer; the PV issuer uses the same rule.
-      const int pb = (C::NPB == 1) ? 0 : (i & 1);
-      const int puse = (C::NPB == 1) ? i : (i >> 1);
-      if (ok && !C::kPInStage && puse >= 1) {
-        ok = mbar_wait(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (ok) {
-        // P^T of tile i goes to the rope block of its KV stage (consumed by
-        // QK(i), which s_full(i) reports complete) or to a P buffer.
-        uint8_t* pbuf = C::kPInStage
-                            ? base + C::kKV + (i % C::NST) * kTileBytes + kRopeOffset
-                            : base + C::kP + pb * C::kPBytes;
-        if constexpr (NRH % 16 == 0) {
-          // Whole 16-row groups: one 16-byte store per term and group, the
-          // warp's 32 tokens covering 512 contiguous bytes (no bank conflict).
+        for (int k4 = 0; k4 < NRH / 4; ++k4) {
+          const int4 kc = *reinterpret_cast<const int4*>(kci + rbase + 4 * k4);
+          t[4 * k4] = softmax_weight_kc(t[4 * k4], kc.x);
+          t[4 * k4 + 1] = softmax_weight_kc(t[4 * k4 + 1], kc.y);
+          t[4 * k4 + 2] = softmax_weight_kc(t[4 * k4 + 2], kc.z);
+          t[4 * k4 + 3] = softmax_weight_kc(t[4 * k4 + 3], kc.w);
+        }
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) lsum[k] += t[k];
+        // P^T (one buffer): wait until PV(i - 1) has read it.
+        if (ok && i >= 1) {
+          ok = mbar_wait(bar(BAR_PFREE0), (i - 1) & 1, p.wait_cycles);
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+          // MN-major [term][NR/16 row groups][128 tokens][16 rows]: one
+          // 16-byte store per term and 16-row group.
+          uint8_t* pbuf = base + C::kP;
 #pragma unroll
           for (int g = 0; g < NRH / 16; ++g) {
-            const int row = rbase + g * 16;
-            uint4 vh, vl;
-            split_e4m3x4(&t[g * 16 + 0], vh.x, vl.x);
-            split_e4m3x4(&t[g * 16 + 4], vh.y, vl.y);
-            split_e4m3x4(&t[g * 16 + 8], vh.z, vl.z);
-            split_e4m3x4(&t[g * 16 + 12], vh.w, vl.w);
-            const uint32_t off = (row >> 4) * 2048 + tok_lane * 16;
+            uint32_t h[8], l[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+              split_e4m3x2_h(t[g * 16 + 2 * m], t[g * 16 + 2 * m + 1], h[m], l[m]);
+            const uint4 vh = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
+                                        h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+            const uint4 vl = make_uint4(l[0] | (l[1] << 16), l[2] | (l[3] << 16),
+                                        l[4] | (l[5] << 16), l[6] | (l[7] << 16));
+            const uint32_t off = ((rbase >> 4) + g) * 2048 + tok_lane * 16;
             *reinterpret_cast<uint4*>(pbuf + off) = vh;
             *reinterpret_cast<uint4*>(pbuf + C::kPHalf + off) = vl;
           }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(bar(BAR_PFULL0));
+        }
+      }
+    } else {
+      for (int i = 0; i < n_tiles; ++i) {
+        const int sb = (C::NS == 2) ? (i & 1) : 0;
+        const int use = (C::NS == 2) ? (i >> 1) : i;
+        if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
+        ok = __all_sync(0xffffffffu, ok);
+        float t[NRH];
+        if (ok) {
+          tc_fence_after();
+          uint32_t r[NRH];
+#pragma unroll
+          for (int cc = 0; cc < NRH / 8; ++cc)
+            tmem_ld8(tmem + lane_addr + sb * NR + rbase + cc * 8,
+                     *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
+          tc_fence_before();
+          mbar_arrive(bar(BAR_SFREE0 + sb));
         } else {
 #pragma unroll
-          for (int g = 0; g < NRH / 8; ++g) {
-            const int row = rbase + g * 8;
-            uint2 vh, vl;
-            split_e4m3x4(&t[g * 8 + 0], vh.x, vl.x);
-            split_e4m3x4(&t[g * 8 + 4], vh.y, vl.y);
-            const uint32_t off = (row >> 4) * 2048 + tok_lane * 16 + (row & 15);
-            *reinterpret_cast<uint2*>(pbuf + off) = vh;
-            *reinterpret_cast<uint2*>(pbuf + C::kPHalf + off) = vl;
+          for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
+        }
+        scale_mask(t, i);
+        // Reference check.  A row's reference k only has to bound its scores:
+        // with p = 2^(t - k + 8), E4M3 holds p up to 448 = 2^8.8, so any k with
+        // t <= k + 0.75 works.  One vote finds whether some score of the tile
+        // exceeds its row's reference; only then (always on the first tile)
+        // are the tile maxima reduced and references raised to ceil(max).
+        bool over = false;
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) over |= t[k] > kreg[k] + 0.75f;
+        const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
+        // Owners fold the previous tile's row sums (relative to its reference).
+        if (sid < NR && i > 0) {
+          const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
+          l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+        }
+        if (any_over) {
+          {
+            float tm[NRH];
+#pragma unroll
+            for (int k = 0; k < NRH; ++k) tm[k] = t[k];
+            warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
+          }
+          // The correction flag: cleared before B1 (every read of its last
+          // value happened before this tile's vote), set by owners after B1,
+          // read by all after B2.
+          if (sid == 0) flags[0] = 0;
+          named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
+          if (sid < NR) {
+            const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
+                                   fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
+            float k_new = k_row;
+            if (mt > k_row + 0.75f) k_new = ceilf(mt);
+            float alpha = 1.0f;
+            if (k_new != k_row && k_row != -INFINITY) {
+              const int e = static_cast<int>(k_row - k_new);
+              alpha = (e < -126) ? 0.0f : pow2i(e);
+              flags[0] = 1;
+            }
+            l_row *= alpha;
+            k_row = k_new;
+            kref[sid] = k_new;
+            alpha_s[sid] = alpha;
+          }
+          named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
+          const bool corr = flags[0] != 0;
+          if (ok && corr && i > 0) {
+            // Rescale the O^T columns (hi and lo) of rows whose reference moved
+            // (rare), once PV(i-1) is done.  PV completions alternate between
+            // two barriers, and the one of PV(i-1)'s parity is within one phase
+            // of the awaited one: s_full(i) implies PV(i-2) completed (QK(i)
+            // waits for it) and PV(i+1) needs a later tile's P^T.
+            ok = mbar_wait(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE), ((i - 1) >> 1) & 1,
+                           p.wait_cycles);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+              tc_fence_after();
+#pragma unroll 1
+              for (int d = 0; d < 4; ++d) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                  for (int cc = 0; cc < NRH / 8; ++cc) {
+                    uint32_t r[8];
+                    const uint32_t addr =
+                        tmem + lane_addr + C::kOCol + d * C::OW + half * NR + rbase + cc * 8;
+                    tmem_ld8(addr, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                      r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[rbase + cc * 8 + k]);
+                    tmem_st8(addr, r);
+                  }
+                }
+              }
+              tmem_st_wait();
+            }
           }
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar(BAR_PFULL0 + pb));
-      }
-      // Row sums of the unquantised weights: per thread across tiles (kWide),
-      // or reduced per tile and folded in by the owners after the next tile's
-      // vote (double-buffered by tile parity).
-      if constexpr (C::kWide) {
+        // Weights 2^(t - k + 8), exact power-of-two scaling.
 #pragma unroll
-        for (int k = 0; k < NRH; ++k) lsum[k] += t[k];
-      } else {
+        for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], kreg[k]);
+        // P^T as two E4M3 terms into shared memory, MN-major:
+        // [term][NR/16 row groups][128 tokens][16 rows]; this thread writes its
+        // token's bytes for rows rbase .. rbase + NRH, 16 (or 8) rows per store.
+        // P barriers (and buffers) alternate by tile parity; the PV issuer
+        // uses the same rule.
+        const int pb = i & 1;
+        const int puse = i >> 1;
+        if (ok && !C::kPInStage && puse >= 1) {
+          ok = mbar_wait(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles);
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+          // P^T of tile i goes to the rope block of its KV stage (consumed by
+          // QK(i), which s_full(i) reports complete) or to a P buffer.
+          uint8_t* pbuf = C::kPInStage
+                              ? base + C::kKV + (i % C::NST) * kTileBytes + kRopeOffset
+                              : base + C::kP + pb * C::kPBytes;
+          if constexpr (NRH % 16 == 0) {
+            // Whole 16-row groups: one 16-byte store per term and group, the
+            // warp's 32 tokens covering 512 contiguous bytes (no bank conflict).
+#pragma unroll
+            for (int g = 0; g < NRH / 16; ++g) {
+              const int row = rbase + g * 16;
+              uint4 vh, vl;
+              split_e4m3x4(&t[g * 16 + 0], vh.x, vl.x);
+              split_e4m3x4(&t[g * 16 + 4], vh.y, vl.y);
+              split_e4m3x4(&t[g * 16 + 8], vh.z, vl.z);
+              split_e4m3x4(&t[g * 16 + 12], vh.w, vl.w);
+              const uint32_t off = (row >> 4) * 2048 + tok_lane * 16;
+              *reinterpret_cast<uint4*>(pbuf + off) = vh;
+              *reinterpret_cast<uint4*>(pbuf + C::kPHalf + off) = vl;
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < NRH / 8; ++g) {
+              const int row = rbase + g * 8;
+              uint2 vh, vl;
+              split_e4m3x4(&t[g * 8 + 0], vh.x, vl.x);
+              split_e4m3x4(&t[g * 8 + 4], vh.y, vl.y);
+              const uint32_t off = (row >> 4) * 2048 + tok_lane * 16 + (row & 15);
+              *reinterpret_cast<uint2*>(pbuf + off) = vh;
+              *reinterpret_cast<uint2*>(pbuf + C::kPHalf + off) = vl;
+            }
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(bar(BAR_PFULL0 + pb));
+        }
+        // Row sums of the unquantised weights, reduced per tile and folded in
+        // by the owners after the next tile's vote (double-buffered by tile
+        // parity).
         warp_reduce_rows<NRH, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR + rbase);
       }
     }

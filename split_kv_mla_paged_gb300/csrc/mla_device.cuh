@@ -163,6 +163,43 @@ __device__ __forceinline__ void split_e4m3x4(const float* p, uint32_t& hi, uint3
   lo = pack_e4m3x4(p[0] - h01.x, p[1] - h01.y, p[2] - h23.x, p[3] - h23.y);
 }
 
+// Two weights as E4M3 hi and lo terms through packed halves: h = f16x2(w0, w1)
+// (round to nearest), hi = e4m3(h), lo = e4m3(h - hi).  h - hi is exact in
+// f16 (both are multiples of h's f16 quantum and |h - hi| <= half an E4M3
+// step), so hi + lo carries each weight to ~2^-8 relative like the fp32 form,
+// in five conversions and subtractions per pair instead of seven per value.
+// Byte / half 0 holds w0.
+__device__ __forceinline__ void split_e4m3x2_h(float w0, float w1, uint32_t& hi, uint32_t& lo) {
+  uint32_t h, hh, d;
+  uint16_t h8, l8;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(w1), "f"(w0));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(h));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(h8));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(hh));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(d));
+  hi = h8;
+  lo = l8;
+}
+
+// 2^(t - k + 8) for the 96-row softmax: the same value as softmax_weight (t
+// split as rint(t) + f, exact power-of-two scaling) from a per-row integer
+// kc = 135 - 0x4B400000 - k: the bits of t + 1.5 * 2^23 are 0x4B400000 +
+// rint(t), so bits + kc is the biased exponent rint(t) - k + 8 + 127, clamped
+// at 0 (weights below 2^-126 flush to 0).  A masked score (-inf) and a row
+// without a reference (kc = kKcNone) give an exponent below 0, i.e. 0.
+// Requires t <= k + 0.75 (the vote guarantees it), so the exponent stays
+// below 255.
+constexpr int kKcNone = -2130706432;  // -2^31 + 2^24: bits + kc < 0 for every t
+__device__ __forceinline__ float softmax_weight_kc(float t, int kc) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  const float tc = fmaxf(t, -2097152.0f);
+  const float tr = tc + kMagic;
+  const float r = tr - kMagic;  // rint(tc)
+  const float f = tc - r;       // exact, |f| <= 0.5
+  const int e = max(__float_as_int(tr) + kc, 0);
+  return ex2_approx(f) * __int_as_float(e << 23);
+}
+
 // Warp reduce-scatter over N per-lane values (one per row): afterwards lane
 // `l` holds the warp-wide reduction of rows [base, base + final_n) in v[0..).
 // Halving steps exchange half of the values with the partner lane; once N is
