@@ -119,6 +119,14 @@ MLA_API int mla_decode_plan_items(const int32_t* splits, int32_t batch, int32_t 
                                   int32_t q_len, int32_t* items_out, int32_t capacity,
                                   int32_t* n_items_out);
 
+/* The item list for the BF16 entry points (mla_decode_bf16_ex,
+ * mla_decode_bf16_sparse): the same list, with the BF16 kernels' row groups
+ * (at most 48 rows per CTA, where the FP8 kernels take up to 96).  Arguments
+ * and errors as for mla_decode_plan_items. */
+MLA_API int mla_decode_plan_items_bf16(const int32_t* splits, int32_t batch, int32_t num_heads,
+                                       int32_t q_len, int32_t* items_out, int32_t capacity,
+                                       int32_t* n_items_out);
+
 /* Workspace bytes mla_decode needs: a 256-byte status header, then per
  * (row, split) an fp32 pair (m, l) and an fp32 O[512]. */
 MLA_API size_t mla_decode_workspace_size(int32_t batch, int32_t q_len, int32_t num_heads,
@@ -286,8 +294,10 @@ MLA_API int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64
                             float* lse_f32, float* out_f32_debug, void* stream);
 
 /* mla_decode_bf16 with options (NULL options = mla_decode_bf16): output_scale,
- * sinks, query_lens and softmax_scale_dev as for mla_decode_ex.  q_scale_dev,
- * kv_scale_dev, kv_bounds and cta_items are FP8-only: MLA_ERR_UNSUPPORTED. */
+ * sinks, query_lens, kv_bounds and softmax_scale_dev as for mla_decode_ex;
+ * cta_items / num_ctas as for mla_decode_ex with a list built by
+ * mla_decode_plan_items_bf16.  q_scale_dev and kv_scale_dev are FP8-only
+ * (BF16 Q and KV carry no scale): MLA_ERR_UNSUPPORTED. */
 MLA_API int mla_decode_bf16_ex(const void* q_bf16, const void* kv_pages_bf16, int64_t num_pages,
                                const int32_t* page_table, int32_t max_pages_per_req,
                                const int32_t* kv_lens, const int32_t* splits,
@@ -296,6 +306,22 @@ MLA_API int mla_decode_bf16_ex(const void* q_bf16, const void* kv_pages_bf16, in
                                float softmax_scale, void* workspace, size_t workspace_bytes,
                                void* out_bf16, float* lse_f32, float* out_f32_debug,
                                const mla_decode_options_t* options, void* stream);
+
+/* Sparse decode over selected pages with a BF16 cache: mla_decode_sparse's
+ * selection (block_idx, topk, the plan over the compact lengths 32 * topk)
+ * with mla_decode_bf16's Q, KV and outputs (PR #17441 "m3 decode perf": the
+ * sparse MLA decode after the top-k block selector; here on the BF16 cache of
+ * issue #20510's mla_decode_fp16.py).  options as for mla_decode_bf16_ex. */
+MLA_API int mla_decode_bf16_sparse(const void* q_bf16, const void* kv_pages_bf16,
+                                   int64_t num_pages, const int32_t* page_table,
+                                   int32_t max_pages_per_req, const int32_t* kv_lens,
+                                   const int32_t* block_idx, int32_t topk, const int32_t* splits,
+                                   const int32_t* chunks, int32_t max_splits, int32_t kv_split,
+                                   int32_t batch, int32_t q_len, int32_t num_heads,
+                                   int32_t causal, float softmax_scale, void* workspace,
+                                   size_t workspace_bytes, void* out_bf16, float* lse_f32,
+                                   float* out_f32_debug, const mla_decode_options_t* options,
+                                   void* stream);
 
 /* Zero the 256-byte status header of a new workspace (async on `stream`).
  * Call once per workspace before its first mla_decode; after that the
@@ -402,6 +428,18 @@ MLA_API int mla_decode_static_ws_status(void* stream);
  * (those drains keep the long limit), frees TMEM and exits, leaving the
  * context usable.  Not for production use. */
 MLA_API void mla_debug_set_wait_limit(long long cycles);
+
+/* Test hook.  For launches made after the call, the pipeline wait of `role`
+ * at tile index `tile` of every split-KV CTA reads as expired without any
+ * stall: 0 the producer's wait for a free KV stage, 1 the QK issuer's wait
+ * for a landed tile, 2 the PV issuer's wait for P^T, 3 the softmax's wait
+ * for S^T, 4 its wait for a free P^T buffer (FP8 configurations of 32 rows
+ * or more), 5 its wait for the last MMAs before the epilogue (tile 0).  The
+ * kernel then does what a wait that ran out does: records MLA_ERR_TIMEOUT,
+ * stops the other roles, lets its own copies and MMAs finish, frees TMEM and
+ * exits (the call's output is not valid).  role < 0 turns it off.  Not for
+ * production use. */
+MLA_API void mla_debug_set_expire(int32_t role, int32_t tile);
 
 /* Message for the last non-OK status returned on this thread. */
 MLA_API const char* mla_last_error(void);

@@ -24,7 +24,7 @@ __all__ = [
     "mla_decode_splitkv", "mla_decode_merge", "mla_merge", "mla_decode_status", "mla_last_error",
     "mla_decode_static_ws", "mla_decode_static_ws_status", "mla_kv_append", "mla_decode_ex",
     "mla_decode_bf16", "mla_decode_sparse", "mla_decode_plan_items", "mla_decode_bf16_ex",
-    "DecodeOptions",
+    "mla_decode_bf16_sparse", "mla_decode_plan_items_bf16", "DecodeOptions",
     "decode", "merge",
     "EXPORTED_SYMBOLS",
 ]
@@ -44,7 +44,8 @@ EXPORTED_SYMBOLS = ("mla_decode_plan", "mla_decode_workspace_size", "mla_decode_
                     "mla_decode_status", "mla_last_error", "mla_debug_set_wait_limit",
                     "mla_decode_static_ws", "mla_decode_static_ws_status", "mla_kv_append",
                     "mla_decode_ex", "mla_decode_bf16", "mla_decode_sparse",
-                    "mla_decode_plan_items", "mla_decode_bf16_ex")
+                    "mla_decode_plan_items", "mla_decode_bf16_ex", "mla_decode_bf16_sparse",
+                    "mla_decode_plan_items_bf16", "mla_debug_set_expire")
 
 HEAD_DIM = 576
 LATENT_DIM = 512
@@ -93,8 +94,9 @@ def load_library() -> ctypes.CDLL:
                                  ctypes.c_size_t)
         lib.mla_decode_plan.restype = ctypes.c_int
         lib.mla_decode_plan.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
-        lib.mla_decode_plan_items.restype = ctypes.c_int
-        lib.mla_decode_plan_items.argtypes = [vp, i32, i32, i32, vp, i32, vp]
+        for name in ("mla_decode_plan_items", "mla_decode_plan_items_bf16"):
+            getattr(lib, name).restype = ctypes.c_int
+            getattr(lib, name).argtypes = [vp, i32, i32, i32, vp, i32, vp]
         lib.mla_decode_workspace_size.restype = sz
         lib.mla_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         dec_args = [vp, vp, i64, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, f32,
@@ -112,6 +114,10 @@ def load_library() -> ctypes.CDLL:
         lib.mla_decode_bf16_ex.restype = ctypes.c_int
         lib.mla_decode_bf16_ex.argtypes = (dec_args[:14] + [f32] + dec_args[17:-1]
                                            + [ctypes.POINTER(DecodeOptions), vp])
+        lib.mla_decode_bf16_sparse.restype = ctypes.c_int
+        lib.mla_decode_bf16_sparse.argtypes = (dec_args[:6] + [vp, i32] + dec_args[6:14] + [f32]
+                                               + dec_args[17:-1]
+                                               + [ctypes.POINTER(DecodeOptions), vp])
         lib.mla_decode_workspace_init.restype = ctypes.c_int
         lib.mla_decode_workspace_init.argtypes = [vp, sz, vp]
         lib.mla_merge.restype = ctypes.c_int
@@ -127,6 +133,8 @@ def load_library() -> ctypes.CDLL:
         lib.mla_kv_append.argtypes = [vp, i64, vp, vp, vp, i32, i32, vp, i64, f32, vp, vp]
         lib.mla_debug_set_wait_limit.restype = None
         lib.mla_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
+        lib.mla_debug_set_expire.restype = None
+        lib.mla_debug_set_expire.argtypes = [i32, i32]
         lib.mla_last_error.restype = ctypes.c_char_p
         lib.mla_last_error.argtypes = []
         _lib = lib
@@ -187,17 +195,24 @@ def mla_decode_plan(kv_lens: Sequence[int], num_heads: int, q_len: int, sm_count
     return Plan(splits=splits, chunks=chunks, kv_split=int(kvs.value), workspace_bytes=int(ws.value))
 
 
-def mla_decode_plan_items(splits, num_heads: int, q_len: int) -> np.ndarray:
-    """CTA item list of a plan (one int32 per CTA that has work, split-major)."""
+def mla_decode_plan_items(splits, num_heads: int, q_len: int, bf16: bool = False) -> np.ndarray:
+    """CTA item list of a plan (one int32 per CTA that has work, split-major);
+    bf16=True builds it with the BF16 kernels' row groups."""
     lib = load_library()
+    fn = lib.mla_decode_plan_items_bf16 if bf16 else lib.mla_decode_plan_items
     sp = np.ascontiguousarray(np.asarray(splits, dtype=np.int32))
     n = ctypes.c_int32(0)
-    _check(lib.mla_decode_plan_items(sp.ctypes.data, int(sp.shape[0]), int(num_heads), int(q_len),
-                                     None, 0, ctypes.addressof(n)))
+    _check(fn(sp.ctypes.data, int(sp.shape[0]), int(num_heads), int(q_len), None, 0,
+              ctypes.addressof(n)))
     items = np.zeros(int(n.value), dtype=np.int32)
-    _check(lib.mla_decode_plan_items(sp.ctypes.data, int(sp.shape[0]), int(num_heads), int(q_len),
-                                     items.ctypes.data, int(items.shape[0]), ctypes.addressof(n)))
+    _check(fn(sp.ctypes.data, int(sp.shape[0]), int(num_heads), int(q_len), items.ctypes.data,
+              int(items.shape[0]), ctypes.addressof(n)))
     return items
+
+
+def mla_decode_plan_items_bf16(splits, num_heads: int, q_len: int) -> np.ndarray:
+    """The CTA item list for the BF16 entry points."""
+    return mla_decode_plan_items(splits, num_heads, q_len, bf16=True)
 
 
 def mla_decode_workspace_size(batch: int, q_len: int, num_heads: int, max_splits: int) -> int:
@@ -271,11 +286,14 @@ def mla_decode_bf16_ex(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_p
                        splits, chunks, max_splits, kv_split, batch, q_len, num_heads, causal,
                        softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32=None,
                        out_f32_debug=None, *, softmax_scale_dev=None, output_scale: float = 1.0,
-                       sinks=None, query_lens=None, stream=None) -> None:
-    """mla_decode_bf16 with a device softmax scale, output scale, sinks and
-    ragged query counts."""
+                       sinks=None, query_lens=None, kv_bounds=None, cta_items=None,
+                       stream=None) -> None:
+    """mla_decode_bf16 with a device softmax scale, output scale, sinks,
+    ragged query counts, key windows and a CTA item list (a device int32
+    tensor from mla_decode_plan_items_bf16)."""
     opts = DecodeOptions(None, None, _ptr(softmax_scale_dev), float(output_scale), _ptr(sinks),
-                         _ptr(query_lens), None, None, 0)
+                         _ptr(query_lens), _ptr(kv_bounds), _ptr(cta_items),
+                         0 if cta_items is None else int(cta_items.numel()))
     lib = load_library()
     _check(lib.mla_decode_bf16_ex(_ptr(q_bf16), _ptr(kv_pages_bf16), int(num_pages),
                                   _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),
@@ -284,6 +302,28 @@ def mla_decode_bf16_ex(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_p
                                   float(softmax_scale), _ptr(workspace), int(workspace_bytes),
                                   _ptr(out_bf16), _ptr(lse_f32), _ptr(out_f32_debug),
                                   ctypes.byref(opts), _stream_handle(stream)))
+
+
+def mla_decode_bf16_sparse(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_per_req,
+                           kv_lens, block_idx, topk, splits, chunks, max_splits, kv_split, batch,
+                           q_len, num_heads, causal, softmax_scale, workspace, workspace_bytes,
+                           out_bf16, lse_f32=None, out_f32_debug=None, *, softmax_scale_dev=None,
+                           output_scale: float = 1.0, sinks=None, query_lens=None,
+                           kv_bounds=None, cta_items=None, stream=None) -> None:
+    """BF16 sparse decode over the selected pages block_idx [batch, topk]
+    (plan with the compact lengths 32 * topk)."""
+    opts = DecodeOptions(None, None, _ptr(softmax_scale_dev), float(output_scale), _ptr(sinks),
+                         _ptr(query_lens), _ptr(kv_bounds), _ptr(cta_items),
+                         0 if cta_items is None else int(cta_items.numel()))
+    lib = load_library()
+    _check(lib.mla_decode_bf16_sparse(_ptr(q_bf16), _ptr(kv_pages_bf16), int(num_pages),
+                                      _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),
+                                      _ptr(block_idx), int(topk), _ptr(splits), _ptr(chunks),
+                                      int(max_splits), int(kv_split), int(batch), int(q_len),
+                                      int(num_heads), 1 if causal else 0, float(softmax_scale),
+                                      _ptr(workspace), int(workspace_bytes), _ptr(out_bf16),
+                                      _ptr(lse_f32), _ptr(out_f32_debug), ctypes.byref(opts),
+                                      _stream_handle(stream)))
 
 
 def mla_decode_sparse(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req, kv_lens,
@@ -381,6 +421,12 @@ def mla_debug_set_wait_limit(cycles: int) -> None:
     load_library().mla_debug_set_wait_limit(int(cycles))
 
 
+def mla_debug_set_expire(role: int, tile: int = 0) -> None:
+    """Test hook: the pipeline wait `role` at tile `tile` of later launches
+    reads as expired (role < 0 = off); see mla_decode.h."""
+    load_library().mla_debug_set_expire(int(role), int(tile))
+
+
 def mla_decode_status(workspace, stream=None) -> int:
     """Read and clear the device status word; raises MlaError on a non-OK status."""
     lib = load_library()
@@ -405,11 +451,11 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
     q_fp8 uint8 [B, q, H, 576] and kv_pages_fp8 uint8 [P, 32, 576] (E4M3 codes)
     and page_table int32 [B, max_pages] are CUDA tensors; kv_lens is a host
     sequence.  With torch.bfloat16 q and kv this runs mla_decode_bf16 (no
-    scales, sinks or output scale there).  query_lens [B], kv_bounds [B, 2]
-    and block_idx [B, topk] (selected pages: mla_decode_sparse, planned on the
-    compact lengths) restrict the visible keys.  use_items (default: when the
-    plan has empty split slots) launches the FP8 kernel over the plan's CTA
-    item list.  Returns (out_bf16, lse, out_f32 or None).
+    q/kv scales there).  query_lens [B], kv_bounds [B, 2] and block_idx
+    [B, topk] (selected pages: mla_decode_sparse / mla_decode_bf16_sparse,
+    planned on the compact lengths) restrict the visible keys.  use_items
+    (default: when the plan has empty split slots) launches the split kernel
+    over the plan's CTA item list.  Returns (out_bf16, lse, out_f32 or None).
     """
     import torch
     dev = q_fp8.device
@@ -438,26 +484,35 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
     restricted = query_lens is not None or kv_bounds is not None or block_idx is not None
     if use_items is None:
         use_items = bool(np.any(plan.splits < plan.max_splits))
+    is_bf16 = q_fp8.dtype == torch.bfloat16
     items_d = None
-    if use_items and q_fp8.dtype != torch.bfloat16:
-        items_d = torch.from_numpy(mla_decode_plan_items(plan.splits, num_heads, q_len)).to(dev)
-    if q_fp8.dtype == torch.bfloat16:
-        if (kv_pages_fp8.dtype != torch.bfloat16 or q_scale != 1.0 or kv_scale != 1.0
-                or kv_bounds is not None or block_idx is not None):
-            raise ValueError("BF16 decode takes BF16 q and kv, no q/kv scales and no key "
-                             "windows or page selections")
-        if sinks is None and output_scale == 1.0 and not device_scales and query_lens is None:
+    if use_items:
+        items_d = torch.from_numpy(
+            mla_decode_plan_items(plan.splits, num_heads, q_len, bf16=is_bf16)).to(dev)
+
+    def _dev_i32(x):
+        return None if x is None else torch.as_tensor(x, dtype=torch.int32).to(dev).contiguous()
+    if is_bf16:
+        if kv_pages_fp8.dtype != torch.bfloat16 or q_scale != 1.0 or kv_scale != 1.0:
+            raise ValueError("BF16 decode takes BF16 q and kv and no q/kv scales")
+        if (sinks is None and output_scale == 1.0 and not device_scales and not restricted
+                and items_d is None):
             mla_decode_bf16(*common, softmax_scale, ws, ws_bytes, out, lse, out_f32, stream)
         else:
             sm_d = (torch.tensor([softmax_scale], dtype=torch.float32, device=dev)
                     if device_scales else None)
             sk = None if sinks is None else torch.as_tensor(sinks, dtype=torch.float32).to(dev)
-            ql = (None if query_lens is None
-                  else torch.as_tensor(query_lens, dtype=torch.int32).to(dev).contiguous())
+            extra = dict(softmax_scale_dev=sm_d, output_scale=output_scale, sinks=sk,
+                         query_lens=_dev_i32(query_lens), kv_bounds=_dev_i32(kv_bounds),
+                         cta_items=items_d, stream=stream)
             # With a device scale the host value is a placeholder the kernel must ignore.
-            mla_decode_bf16_ex(*common, 99.0 if device_scales else softmax_scale, ws, ws_bytes,
-                               out, lse, out_f32, softmax_scale_dev=sm_d,
-                               output_scale=output_scale, sinks=sk, query_lens=ql, stream=stream)
+            sm_h = 99.0 if device_scales else softmax_scale
+            bi_d = _dev_i32(block_idx)
+            if bi_d is None:
+                mla_decode_bf16_ex(*common, sm_h, ws, ws_bytes, out, lse, out_f32, **extra)
+            else:
+                mla_decode_bf16_sparse(*common[:6], bi_d, topk, *common[6:], sm_h, ws, ws_bytes,
+                                       out, lse, out_f32, **extra)
     elif (sinks is None and output_scale == 1.0 and not device_scales and not restricted
           and items_d is None):
         mla_decode(*common, q_scale, kv_scale, softmax_scale, ws, ws_bytes, out, lse, out_f32,
@@ -471,9 +526,6 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
         # With device scales the host values are placeholders the kernel must
         # ignore (deliberately wrong, so a kernel that used them would fail).
         host = (99.0,) * 3 if device_scales else (q_scale, kv_scale, softmax_scale)
-
-        def _dev_i32(x):
-            return None if x is None else torch.as_tensor(x, dtype=torch.int32).to(dev).contiguous()
         ql_d, kb_d, bi_d = _dev_i32(query_lens), _dev_i32(kv_bounds), _dev_i32(block_idx)
         extra = dict(q_scale_dev=None if dev_s is None else dev_s[0:1],
                      kv_scale_dev=None if dev_s is None else dev_s[1:2],

@@ -92,6 +92,165 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // this slot (P^T lives in the KV stages, so the P^T-free barriers are unused).
 constexpr int kBarOdone1B = BAR_PFREE1;
 
+// Rows of a staged 64-token tile (two pages) that hold no loaded key: pages
+// not loaded (past the split's end, outside a window, an unused selection
+// slot) and the tail of a request's last page.  The warp zeroes all 1152
+// bytes of such a row (nine 128-byte blocks) so V holds no stale or NaN
+// values.  kGather: `info` holds the rows loaded per page (byte q for page
+// q); otherwise the first `valid` rows of the tile are keys of the split.
+template <bool kGather>
+__device__ __forceinline__ void zero_unloaded_rows_bf16(uint8_t* kvp, int lane, uint32_t info,
+                                                        int valid) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  auto zero_rows = [&](int r0, int nrow) {
+    for (int idx = lane; idx < nrow * 72; idx += 32) {
+      const int r = r0 + idx / 72;
+      const int c = idx % 72;
+      *reinterpret_cast<uint4*>(kvp + (c / 8) * kBlkBytesB + r * 128 + (c % 8) * 16) = z;
+    }
+  };
+  bool any = false;
+  if constexpr (kGather) {
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      const int nv = static_cast<int>((info >> (8 * q)) & 0xFFu);
+      if (nv < MLA_PAGE_SIZE) {
+        zero_rows(q * MLA_PAGE_SIZE + nv, MLA_PAGE_SIZE - nv);
+        any = true;
+      }
+    }
+  } else if (valid < kTokB) {
+    zero_rows(valid, kTokB - valid);
+    any = true;
+  }
+  if (any) {
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+}
+
+// CTA coordinates of the split kernels: the (request, split x row group)
+// grid, split-major, or an entry of the CTA item list (kItems).  Returns
+// false (after reporting) for an item outside the batch or the row groups.
+template <bool kItems>
+__device__ __forceinline__ bool cta_coords(const DecodeParams& p, int ngroups, int& b, int& split,
+                                           int& grp) {
+  if constexpr (kItems) {
+    const int it = p.cta_items[blockIdx.x];
+    b = it >> MLA_ITEM_B_SHIFT;
+    split = (it >> MLA_ITEM_S_SHIFT) & ((1 << (MLA_ITEM_B_SHIFT - MLA_ITEM_S_SHIFT)) - 1);
+    grp = it & ((1 << MLA_ITEM_S_SHIFT) - 1);
+    if (it < 0 || b >= p.batch || grp >= ngroups) {
+      if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
+      return false;
+    }
+  } else {
+    split = blockIdx.y / ngroups;
+    grp = blockIdx.y - split * ngroups;
+    b = blockIdx.x;
+  }
+  return true;
+}
+
+// Key range of split `split` of request b for the BF16 kernels (64-token
+// tiles): the plan checks (reported as MLA_ERR_INVALID_ARG), the split's
+// token range in the planned space (positions, or the compact range of a
+// page selection), the key window, and the first tile (whole tiles below a
+// dense window are skipped; tiles stay aligned to the split start).
+struct SplitRange {
+  int L, nsplit, q_b, tok_begin, tok_end, t0, win_lo, win_hi;
+  bool sparse;
+};
+
+template <bool kGather>
+__device__ __forceinline__ bool split_range(const DecodeParams& p, int b, int split,
+                                            SplitRange& r) {
+  r.L = p.kv_lens[b];
+  r.nsplit = p.splits[b];
+  const int chunk = p.chunks[b];
+  r.sparse = kGather && p.block_idx != nullptr;
+  const int Lspace = r.sparse ? p.topk * MLA_PAGE_SIZE : r.L;
+  r.q_b = p.query_lens ? p.query_lens[b] : p.q_len;
+  const bool bad = r.L < 1 || r.q_b < 1 || r.q_b > p.q_len || (p.causal && r.L < r.q_b) ||
+                   r.nsplit > p.max_splits || chunk < MLA_TILE_TOKENS ||
+                   (chunk % MLA_TILE_TOKENS) != 0 ||
+                   static_cast<int64_t>(r.nsplit) * chunk < Lspace ||
+                   static_cast<int64_t>(r.nsplit - 1) * chunk >= Lspace ||
+                   static_cast<int64_t>(r.L) > static_cast<int64_t>(p.max_pages) * MLA_PAGE_SIZE;
+  if (bad) {
+    if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
+    return false;
+  }
+  r.tok_begin = split * chunk;
+  r.tok_end = min(Lspace, r.tok_begin + chunk);
+  r.win_lo = 0;
+  r.win_hi = r.L;
+  if (kGather && p.kv_bounds) {
+    r.win_lo = max(0, p.kv_bounds[2 * b]);
+    r.win_hi = min(r.L, p.kv_bounds[2 * b + 1]);
+  }
+  r.t0 = r.tok_begin;
+  if (kGather && !r.sparse) {
+    r.tok_end = min(r.tok_end, r.win_hi);
+    if (r.win_lo >= r.tok_end)
+      r.t0 = r.tok_end;
+    else if (r.win_lo > r.tok_begin)
+      r.t0 = r.tok_begin + (r.win_lo - r.tok_begin) / kTokB * kTokB;
+  }
+  return true;
+}
+
+// One lane's page of a producer window (32 pages = 16 tiles per window):
+// compact page pi = page0 + w * 32 + lane maps to logical page lp (pi
+// itself, or the selection's entry), loaded when it holds keys inside the
+// window and before the end of the split (dense) or of the request
+// (selection).  Returns the physical page (0 if none) and sets nv_out to the
+// page's rows to load (0: not loaded).  Out-of-pool page ids and selection
+// order violations are reported.
+template <bool kGather>
+__device__ __forceinline__ int bf16_window_page(const DecodeParams& p, const SplitRange& r,
+                                                const int32_t* pt, int b, int page0,
+                                                int page_end, int w, int lane, int& last_lp,
+                                                int& nv_out) {
+  const int pi = page0 + w * 32 + lane;
+  int pg = 0;
+  nv_out = 0;
+  if constexpr (!kGather) {
+    if (pi < page_end) {
+      pg = pt[pi];
+      if (pg < 0 || pg >= p.num_pages) {
+        report(p.status, MLA_ERR_INVALID_ARG);
+        pg = 0;
+      }
+      nv_out = MLA_PAGE_SIZE;
+    }
+  } else {
+    int lp = -1;
+    if (pi < page_end) {
+      lp = pi;
+      if (r.sparse) lp = (pi < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + pi] : -1;
+    }
+    if (r.sparse) {
+      int prev = __shfl_up_sync(0xffffffffu, lp, 1);
+      if (lane == 0) prev = last_lp;
+      if (lp >= 0 && prev >= 0 && lp <= prev) report(p.status, MLA_ERR_INVALID_ARG);
+      last_lp = __shfl_sync(0xffffffffu, lp, 31);
+    }
+    const int64_t end_pos = r.sparse ? r.win_hi : r.tok_end;
+    const int64_t first = static_cast<int64_t>(lp) * MLA_PAGE_SIZE;
+    if (lp >= 0 && first < end_pos && first + MLA_PAGE_SIZE > r.win_lo) {
+      pg = pt[lp];
+      if (pg < 0 || pg >= p.num_pages) {
+        report(p.status, MLA_ERR_INVALID_ARG);
+        pg = 0;
+      }
+      nv_out = static_cast<int>(end_pos - first < MLA_PAGE_SIZE ? end_pos - first
+                                                                 : MLA_PAGE_SIZE);
+    }
+  }
+  return pg;
+}
+
 template <int NR>
 struct CfgB {
   static_assert(NR % 16 == 0 && NR >= 16 && NR <= kMaxRowsPerCta, "NR");
@@ -111,14 +270,15 @@ struct CfgB {
   static_assert(kPBytes <= kBlkBytesB, "P^T must fit the rope block");
   static constexpr int NST = 2;
   static constexpr uint32_t kQBytes = NR * kRowBytesB;
-  static constexpr uint32_t kAuxBytes = 160 + 52 * NR;
+  static constexpr uint32_t kAuxBytes = 176 + 52 * NR;
   static constexpr uint32_t kKV = 0;
   static constexpr uint32_t kQ = NST * kTileBytesB;
   static constexpr uint32_t kAux = kQ + kQBytes;
   static constexpr uint32_t kBars = kAux;
   static constexpr uint32_t kTmemSlot = kAux + 136;
   static constexpr uint32_t kFlags = kAux + 144;
-  static constexpr uint32_t kRedMax = kAux + 160;
+  static constexpr uint32_t kStageInfo = kAux + 160;  // NST x 4 B: rows loaded per page
+  static constexpr uint32_t kRedMax = kAux + 176;
   static constexpr uint32_t kAlpha = kRedMax;
   static constexpr uint32_t kRedSum = kRedMax + 16 * NR;
   static constexpr uint32_t kKref = kRedSum + 32 * NR;
@@ -128,35 +288,22 @@ struct CfgB {
   static_assert(kSmemBytes <= 232448u, "shared memory");
 };
 
-template <int NR>
+// kGather: the variant for restricted key sets (key windows, selected pages),
+// where tiles may hold pages that are not loaded and every score is masked by
+// its key position; kItems: the CTA item list instead of the full grid.
+template <int NR, bool kGather, bool kItems>
 __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
     mla_split_kv_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
                              const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
   using C = CfgB<NR>;
   const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
-  const int split = blockIdx.y / ngroups;
-  const int grp = blockIdx.y - split * ngroups;
-  const int b = blockIdx.x;
-
-  const int L = p.kv_lens[b];
-  const int nsplit = p.splits[b];
-  const int chunk = p.chunks[b];
-  if (split >= nsplit) return;
-  const int q_b = p.query_lens ? p.query_lens[b] : p.q_len;  // this request's query tokens
-  {
-    const bool bad = L < 1 || q_b < 1 || q_b > p.q_len || (p.causal && L < q_b) ||
-                     nsplit > p.max_splits ||
-                     chunk < MLA_TILE_TOKENS || (chunk % MLA_TILE_TOKENS) != 0 ||
-                     static_cast<int64_t>(nsplit) * chunk < L ||
-                     static_cast<int64_t>(nsplit - 1) * chunk >= L ||
-                     static_cast<int64_t>(L) > static_cast<int64_t>(p.max_pages) * MLA_PAGE_SIZE;
-    if (bad) {
-      if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
-      return;
-    }
-  }
-  const int tok_begin = split * chunk;
-  const int tok_end = min(L, tok_begin + chunk);
+  int b, split, grp;
+  if (!cta_coords<kItems>(p, ngroups, b, split, grp)) return;
+  if (split >= p.splits[b]) return;  // empty split slot of a shorter request
+  SplitRange sr;
+  if (!split_range<kGather>(p, b, split, sr)) return;
+  const int L = sr.L, nsplit = sr.nsplit, q_b = sr.q_b, tok_end = sr.tok_end, t0 = sr.t0;
+  const bool sparse = sr.sparse;
   const float c_log2 =
       p.sm_scale_dev ? *p.sm_scale_dev * 1.4426950408889634f : p.c_log2;
   const int row0 = grp * p.rows_per_group;
@@ -165,7 +312,7 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
   // query block: no key is visible to them).
   const int rows_valid = max(0, min(rows_here, q_b * p.num_heads - row0));
   const int n_tiles =
-      rows_valid > 0 ? (tok_end - tok_begin + kTokB - 1) / kTokB : 0;
+      (rows_valid > 0 && tok_end > t0) ? (tok_end - t0 + kTokB - 1) / kTokB : 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -224,33 +371,29 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
     }
     const uint64_t pol = l2_policy_evict_first();
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-    const int page0 = tok_begin / MLA_PAGE_SIZE;
+    const int page0 = t0 / MLA_PAGE_SIZE;
     const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
     // Page ids of 16 tiles (32 pages) per window, one per lane, fetched a
-    // window ahead.
-    auto load_window = [&](int w) -> int {
-      const int pi = page0 + w * 32 + lane;
-      int pg = 0;
-      if (pi < page_end) {
-        pg = pt[pi];
-        if (pg < 0 || pg >= p.num_pages) {
-          report(p.status, MLA_ERR_INVALID_ARG);
-          pg = 0;
-        }
-      }
-      return pg;
-    };
-    int window = load_window(0);
-    int window_next = load_window(1);
+    // window ahead, with the rows of each page to load (0: not loaded).
+    int last_lp = -1;
+    int window_nv, window_next_nv;
+    int window = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, 0, lane, last_lp,
+                                           window_nv);
+    int window_next = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, 1, lane, last_lp,
+                                                window_next_nv);
+    volatile uint32_t* stage_info = reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo);
     int issued = 0;
     int st = 0, round = 0;
     for (int i = 0; i < n_tiles; ++i) {
       if (i > 0 && (i & 15) == 0) {
         window = window_next;
-        window_next = load_window((i >> 4) + 1);
+        window_nv = window_next_nv;
+        window_next = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, (i >> 4) + 1,
+                                                lane, last_lp, window_next_nv);
       }
-      bool ok = true;
-      if (round > 0) ok = mbar_wait(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles);
+      bool ok = !expired_here(p, WAIT_STAGE_FREE, i);
+      if (ok && round > 0)
+        ok = mbar_wait_abort(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles, abort_flag);
       ok = __all_sync(0xffffffffu, ok && !*abort_flag);
       if (!ok) {
         if (lane == 0) {
@@ -259,16 +402,23 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
         }
         break;
       }
-      // Lane q (< 2) takes the id of the tile's page q.
-      const int my_page = __shfl_sync(0xffffffffu, window, (i & 15) * 2 + (lane & 1));
-      const int tp0 = page0 + i * 2;
+      // Lane q (< 2) takes the id and the rows to load of the tile's page q;
+      // the rows per page go to the QK warp (which zeroes the rest) with the
+      // stage's full barrier.
+      const int src = (i & 15) * 2 + (lane & 1);
+      const int my_page = __shfl_sync(0xffffffffu, window, src);
+      const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
+      const int nv1 = __shfl_sync(0xffffffffu, my_nv, 1);
+      const bool my_load = my_nv > 0;
+      const int nload = __popc(__ballot_sync(0xffffffffu, lane < 2 && my_load));
       const uint32_t fb = bar(BAR_FULL0 + st);
       if (lane == 0) {
-        const int nvalid = (tp0 < page_end ? 1 : 0) + (tp0 + 1 < page_end ? 1 : 0);
-        mbar_arrive_expect_tx(fb, nvalid * kPageBytesB);
+        if constexpr (kGather)
+          stage_info[st] = static_cast<uint32_t>(my_nv) | (static_cast<uint32_t>(nv1) << 8);
+        mbar_arrive_expect_tx(fb, nload * kPageBytesB);
       }
       __syncwarp();
-      if (lane < 2 && tp0 + lane < page_end) {
+      if (lane < 2 && my_load) {
         const uint32_t kv = sbase + C::kKV + st * kTileBytesB;
         const int row = my_page * MLA_PAGE_SIZE;
 #pragma unroll
@@ -345,31 +495,25 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
       int st = 0, round = 0;
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int use = j >> 1;
-        bool w = mbar_wait(bar(BAR_FULL0 + st), round & 1, p.wait_cycles);
-        if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + (j & 1)), (use - 1) & 1, p.wait_cycles);
+        bool w = !expired_here(p, WAIT_TILE_FULL, j) &&
+                 mbar_wait_abort(bar(BAR_FULL0 + st), round & 1, p.wait_cycles, abort_flag);
+        if (w && use >= 1)
+          w = mbar_wait_abort(bar(BAR_SFREE0 + (j & 1)), (use - 1) & 1, p.wait_cycles,
+                              abort_flag);
         if (w && j >= 2)
-          w = mbar_wait(bar(((j - 2) & 1) ? kBarOdone1B : BAR_ODONE), ((j - 2) >> 1) & 1,
-                        p.wait_cycles);
+          w = mbar_wait_abort(bar(((j - 2) & 1) ? kBarOdone1B : BAR_ODONE), ((j - 2) >> 1) & 1,
+                              p.wait_cycles, abort_flag);
         w = __all_sync(0xffffffffu, w && !*abort_flag);
         if (!w) {
           ok = false;
           break;
         }
-        const int valid = tok_end - (tok_begin + j * kTokB);
-        if (valid < kTokB) {
-          // Rows past the split's end (unloaded pages or a last page's tail):
-          // zero them so V holds no stale or NaN values.
-          const int nrow = kTokB - valid;
-          uint8_t* kvp = base + C::kKV + st * kTileBytesB;
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          for (int idx = lane; idx < nrow * 72; idx += 32) {
-            const int r = valid + idx / 72;
-            const int c = idx % 72;
-            *reinterpret_cast<uint4*>(kvp + (c / 8) * kBlkBytesB + r * 128 + (c % 8) * 16) = z;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
+        // Rows loaded per page, as the producer published them with the
+        // stage's full barrier (observed above).
+        const uint32_t info =
+            kGather ? *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st) : 0u;
+        zero_unloaded_rows_bf16<kGather>(base + C::kKV + st * kTileBytesB, lane, info,
+                                         tok_end - (t0 + j * kTokB));
         if (lane == 0) issue_qk(st, j & 1);
         __syncwarp();
         if (++st == C::NST) {
@@ -381,7 +525,9 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
       // PV(i) as soon as its P^T is ready.
       int st = 0;
       for (int i = 0; ok && i < n_tiles; ++i) {
-        bool w = mbar_wait(bar(BAR_PFULL0 + (i & 1)), (i >> 1) & 1, p.wait_cycles);
+        bool w = !expired_here(p, WAIT_P_FULL, i) &&
+                 mbar_wait_abort(bar(BAR_PFULL0 + (i & 1)), (i >> 1) & 1, p.wait_cycles,
+                                 abort_flag);
         w = __all_sync(0xffffffffu, w && !*abort_flag);
         if (!w) {
           ok = false;
@@ -420,12 +566,26 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
     const int lim_min = p.causal ? min(tok_end, L - q_b + qi_first + 1) : tok_end;
     const int my_row0 = row0 + rbase;
     const int my_rows = max(0, min(NRH, rows_valid - rbase));
+    // Selection: logical page ids of 16 tiles' compact pages, one per lane
+    // (this thread's token lies in page quad / 2 of its tile).
+    auto sel_window = [&](int w) -> int {
+      const int cp = t0 / MLA_PAGE_SIZE + w * 32 + lane;
+      return (cp < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + cp] : -1;
+    };
+    int sel_cur = -1, sel_next = -1;
+    if (sparse) {
+      sel_cur = sel_window(0);
+      sel_next = sel_window(1);
+    }
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
       const int sb = i & 1;
       const int use = i >> 1;
-      if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
+      if (ok)
+        ok = !expired_here(p, WAIT_S_FULL, i) &&
+             mbar_wait_abort(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
+      if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
       float t[NRH];
       if (ok) {
         tc_fence_after();
@@ -443,9 +603,34 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
       }
-      const int tile_tok0 = tok_begin + i * kTokB;
+      const int tile_tok0 = t0 + i * kTokB;
       const int j = tile_tok0 + tok;
-      if (tile_tok0 + kTokB <= lim_min) {
+      if constexpr (kGather) {
+        // Restricted key sets: the token's key position decides.
+        int64_t pos = j;
+        bool tok_ok = has_tok && j < tok_end;
+        if (sparse) {
+          if (i > 0 && (i & 15) == 0) {
+            sel_cur = sel_next;
+            sel_next = sel_window((i >> 4) + 1);
+          }
+          const int lp = __shfl_sync(0xffffffffu, sel_cur, (i & 15) * 2 + (quad >> 1));
+          pos = static_cast<int64_t>(lp) * MLA_PAGE_SIZE + (quad & 1) * 16 + lane;
+          tok_ok = tok_ok && lp >= 0;
+        }
+        tok_ok = tok_ok && pos >= sr.win_lo && pos < sr.win_hi;
+        int qi = my_row0 / p.num_heads;
+        int h = my_row0 - qi * p.num_heads;
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) {
+          const bool vis = tok_ok && k < my_rows && (!p.causal || pos < L - q_b + qi + 1);
+          t[k] = vis ? t[k] * c : -INFINITY;
+          if (++h == p.num_heads) {
+            h = 0;
+            ++qi;
+          }
+        }
+      } else if (tile_tok0 + kTokB <= lim_min) {
 #pragma unroll
         for (int k = 0; k < NRH; ++k) t[k] = (has_tok && k < my_rows) ? t[k] * c : -INFINITY;
       } else {
@@ -501,8 +686,8 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
         if (ok && corr && i > 0) {
           // PV(i - 1) done; PV completions alternate between two barriers
           // and the one of PV(i - 1)'s parity is within one phase of it.
-          ok = mbar_wait(bar(((i - 1) & 1) ? kBarOdone1B : BAR_ODONE), ((i - 1) >> 1) & 1,
-                         p.wait_cycles);
+          ok = mbar_wait_abort(bar(((i - 1) & 1) ? kBarOdone1B : BAR_ODONE),
+                               ((i - 1) >> 1) & 1, p.wait_cycles, abort_flag);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
             tc_fence_after();
@@ -585,7 +770,7 @@ __global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
       scale_s[sid] = sc;
     }
     named_bar_sync(kSoftmaxBarrier, NT);
-    bool fin = mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
+    bool fin = !expired_here(p, WAIT_FINAL, 0) && mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
     fin = __all_sync(0xffffffffu, fin);
     if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
     if (ok && fin && n_tiles > 0) {
@@ -662,7 +847,8 @@ constexpr uint32_t kAux = NST * kTileBytesB;
 constexpr uint32_t kBars = kAux;               // 17 x 8 B
 constexpr uint32_t kTmemSlot = kAux + 136;
 constexpr uint32_t kFlags = kAux + 144;
-constexpr uint32_t kRedMax = kAux + 160;       // 4 warps x 16 rows
+constexpr uint32_t kStageInfo = kAux + 160;    // NST x 4 B: rows loaded per page
+constexpr uint32_t kRedMax = kAux + 176;       // 4 warps x 16 rows
 constexpr uint32_t kRedSum = kRedMax + 256;    // 2 x 4 x 16
 constexpr uint32_t kKref = kRedSum + 512;      // 16
 constexpr uint32_t kAlpha = kKref + 64;        // 16
@@ -677,34 +863,19 @@ constexpr int BAR_ODONE_0 = BAR_ODONE;
 constexpr int BAR_ODONE_1 = BAR_PFREE1;
 }  // namespace q16
 
+template <bool kGather, bool kItems>
 __global__ void __launch_bounds__(q16::kThreads, 1)
     mla_split_kv_bf16_q16_kernel(const __grid_constant__ CUtensorMap tm_kv,
                                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
   using namespace q16;
   const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
-  const int split = blockIdx.y / ngroups;
-  const int grp = blockIdx.y - split * ngroups;
-  const int b = blockIdx.x;
-
-  const int L = p.kv_lens[b];
-  const int nsplit = p.splits[b];
-  const int chunk = p.chunks[b];
-  if (split >= nsplit) return;
-  const int q_b = p.query_lens ? p.query_lens[b] : p.q_len;  // this request's query tokens
-  {
-    const bool bad = L < 1 || q_b < 1 || q_b > p.q_len || (p.causal && L < q_b) ||
-                     nsplit > p.max_splits ||
-                     chunk < MLA_TILE_TOKENS || (chunk % MLA_TILE_TOKENS) != 0 ||
-                     static_cast<int64_t>(nsplit) * chunk < L ||
-                     static_cast<int64_t>(nsplit - 1) * chunk >= L ||
-                     static_cast<int64_t>(L) > static_cast<int64_t>(p.max_pages) * MLA_PAGE_SIZE;
-    if (bad) {
-      if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
-      return;
-    }
-  }
-  const int tok_begin = split * chunk;
-  const int tok_end = min(L, tok_begin + chunk);
+  int b, split, grp;
+  if (!cta_coords<kItems>(p, ngroups, b, split, grp)) return;
+  if (split >= p.splits[b]) return;  // empty split slot of a shorter request
+  SplitRange sr;
+  if (!split_range<kGather>(p, b, split, sr)) return;
+  const int L = sr.L, nsplit = sr.nsplit, q_b = sr.q_b, tok_end = sr.tok_end, t0 = sr.t0;
+  const bool sparse = sr.sparse;
   const float c_log2 =
       p.sm_scale_dev ? *p.sm_scale_dev * 1.4426950408889634f : p.c_log2;
   const int row0 = grp * p.rows_per_group;
@@ -713,7 +884,7 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
   // query block: no key is visible to them).
   const int rows_valid = max(0, min(rows_here, q_b * p.num_heads - row0));
   const int n_tiles =
-      rows_valid > 0 ? (tok_end - tok_begin + kTokB - 1) / kTokB : 0;
+      (rows_valid > 0 && tok_end > t0) ? (tok_end - t0 + kTokB - 1) / kTokB : 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -773,35 +944,30 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
     }
     const uint64_t pol = l2_policy_evict_first();
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-    const int page0 = tok_begin / MLA_PAGE_SIZE;
+    const int page0 = t0 / MLA_PAGE_SIZE;
     const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
-    auto load_window = [&](int w) -> int {
-      const int pi = page0 + w * 32 + lane;
-      int pg = 0;
-      if (pi < page_end) {
-        pg = pt[pi];
-        if (pg < 0 || pg >= p.num_pages) {
-          report(p.status, MLA_ERR_INVALID_ARG);
-          pg = 0;
-        }
-      }
-      return pg;
-    };
-    int window = load_window(0);
-    int window_next = load_window(1);
+    int last_lp = -1;
+    int window_nv, window_next_nv;
+    int window = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, 0, lane, last_lp,
+                                           window_nv);
+    int window_next = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, 1, lane, last_lp,
+                                                window_next_nv);
+    volatile uint32_t* stage_info = reinterpret_cast<volatile uint32_t*>(base + kStageInfo);
     int issued = 0;
     int st = 0, round = 0;
     for (int i = 0; i < n_tiles; ++i) {
       if (i > 0 && (i & 15) == 0) {
         window = window_next;
-        window_next = load_window((i >> 4) + 1);
+        window_nv = window_next_nv;
+        window_next = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, (i >> 4) + 1,
+                                                lane, last_lp, window_next_nv);
       }
-      bool ok = true;
-      if (round > 0) {
-        ok = mbar_wait(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles);
-      } else if (st == NST - 1) {
+      bool ok = !expired_here(p, WAIT_STAGE_FREE, i);
+      if (ok && round > 0) {
+        ok = mbar_wait_abort(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles, abort_flag);
+      } else if (ok && st == NST - 1) {
         // The last stage holds the staged Q until it has been copied to TMEM.
-        ok = mbar_wait(bar(BAR_QTMEM), 0, p.wait_cycles);
+        ok = mbar_wait_abort(bar(BAR_QTMEM), 0, p.wait_cycles, abort_flag);
       }
       ok = __all_sync(0xffffffffu, ok && !*abort_flag);
       if (!ok) {
@@ -811,15 +977,20 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
         }
         break;
       }
-      const int my_page = __shfl_sync(0xffffffffu, window, (i & 15) * 2 + (lane & 1));
-      const int tp0 = page0 + i * 2;
+      const int src = (i & 15) * 2 + (lane & 1);
+      const int my_page = __shfl_sync(0xffffffffu, window, src);
+      const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
+      const int nv1 = __shfl_sync(0xffffffffu, my_nv, 1);
+      const bool my_load = my_nv > 0;
+      const int nload = __popc(__ballot_sync(0xffffffffu, lane < 2 && my_load));
       const uint32_t fb = bar(BAR_FULL0 + st);
       if (lane == 0) {
-        const int nvalid = (tp0 < page_end ? 1 : 0) + (tp0 + 1 < page_end ? 1 : 0);
-        mbar_arrive_expect_tx(fb, nvalid * kPageBytesB);
+        if constexpr (kGather)
+          stage_info[st] = static_cast<uint32_t>(my_nv) | (static_cast<uint32_t>(nv1) << 8);
+        mbar_arrive_expect_tx(fb, nload * kPageBytesB);
       }
       __syncwarp();
-      if (lane < 2 && tp0 + lane < page_end) {
+      if (lane < 2 && my_load) {
         const uint32_t kv = sbase + st * kTileBytesB;
         const int row = my_page * MLA_PAGE_SIZE;
 #pragma unroll
@@ -889,25 +1060,17 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
     // Each warp waits on one barrier at a time, in tile order.
     auto qk_step = [&](int j) -> bool {
       const int st = j % NST;
-      bool w = mbar_wait(bar(BAR_FULL0 + st), (j / NST) & 1, p.wait_cycles);
+      bool w = !expired_here(p, WAIT_TILE_FULL, j) &&
+               mbar_wait_abort(bar(BAR_FULL0 + st), (j / NST) & 1, p.wait_cycles, abort_flag);
       const int use = j >> 1;
-      if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + (j & 1)), (use - 1) & 1, p.wait_cycles);
+      if (w && use >= 1)
+        w = mbar_wait_abort(bar(BAR_SFREE0 + (j & 1)), (use - 1) & 1, p.wait_cycles, abort_flag);
       w = __all_sync(0xffffffffu, w && !*abort_flag);
       if (!w) return false;
-      const int valid = tok_end - (tok_begin + j * kTokB);
-      if (valid < kTokB) {
-        // Rows past the split's end: zero them so V holds no stale or NaN values.
-        const int nrow = kTokB - valid;
-        uint8_t* kvp = base + st * kTileBytesB;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int idx = lane; idx < nrow * 72; idx += 32) {
-          const int r = valid + idx / 72;
-          const int c = idx % 72;
-          *reinterpret_cast<uint4*>(kvp + (c / 8) * kBlkBytesB + r * 128 + (c % 8) * 16) = z;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
+      const uint32_t info =
+          kGather ? *reinterpret_cast<volatile uint32_t*>(base + kStageInfo + 4 * st) : 0u;
+      zero_unloaded_rows_bf16<kGather>(base + st * kTileBytesB, lane, info,
+                                       tok_end - (t0 + j * kTokB));
       if (lane == 0) issue_qk(st, j & 1);
       __syncwarp();
       return true;
@@ -918,8 +1081,8 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
       // one phase of its barrier; QK(j) still overlaps PV(j - 1)).
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j >= 2) {
-          bool w = mbar_wait(bar(((j - 2) & 1) ? BAR_ODONE_1 : BAR_ODONE_0), ((j - 2) >> 1) & 1,
-                             p.wait_cycles);
+          bool w = mbar_wait_abort(bar(((j - 2) & 1) ? BAR_ODONE_1 : BAR_ODONE_0),
+                                   ((j - 2) >> 1) & 1, p.wait_cycles, abort_flag);
           w = __all_sync(0xffffffffu, w && !*abort_flag);
           if (!w) {
             ok = false;
@@ -930,7 +1093,9 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
       }
     } else {
       for (int i = 0; ok && i < n_tiles; ++i) {
-        bool w = mbar_wait(bar(BAR_PFULL0 + (i & 1)), (i >> 1) & 1, p.wait_cycles);
+        bool w = !expired_here(p, WAIT_P_FULL, i) &&
+                 mbar_wait_abort(bar(BAR_PFULL0 + (i & 1)), (i >> 1) & 1, p.wait_cycles,
+                                 abort_flag);
         w = __all_sync(0xffffffffu, w && !*abort_flag);
         if (!w) {
           ok = false;
@@ -985,11 +1150,25 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
     const int qi = (row0 + row) / p.num_heads;
     const bool row_ok = row < rows_valid;
     const int lim = p.causal ? min(tok_end, L - q_b + qi + 1) : tok_end;
+    // Selection: logical page ids of 16 tiles' compact pages, one per lane
+    // (this thread's tokens lie in page slot / 4 of its tile).
+    auto sel_window = [&](int wn) -> int {
+      const int cp = t0 / MLA_PAGE_SIZE + wn * 32 + lane;
+      return (cp < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + cp] : -1;
+    };
+    int sel_cur = -1, sel_next = -1;
+    if (sparse) {
+      sel_cur = sel_window(0);
+      sel_next = sel_window(1);
+    }
     for (int i = 0; i < n_tiles; ++i) {
       const int sb = i & 1;
       const int use = i >> 1;
-      if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
+      if (ok)
+        ok = !expired_here(p, WAIT_S_FULL, i) &&
+             mbar_wait_abort(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
+      if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
       float t[8];
       if (ok) {
         tc_fence_after();
@@ -1004,9 +1183,31 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) t[k] = 0.0f;
       }
-      const int j0 = tok_begin + i * kTokB + slot * 8;
+      const int j0 = t0 + i * kTokB + slot * 8;
+      if constexpr (kGather) {
+        // Restricted key sets: the token's key position decides.
+        int64_t pos0 = j0;
+        bool page_ok = true;
+        if (sparse) {
+          if (i > 0 && (i & 15) == 0) {
+            sel_cur = sel_next;
+            sel_next = sel_window((i >> 4) + 1);
+          }
+          const int lp = __shfl_sync(0xffffffffu, sel_cur, (i & 15) * 2 + (slot >> 2));
+          pos0 = static_cast<int64_t>(lp) * MLA_PAGE_SIZE + (slot & 3) * 8;
+          page_ok = lp >= 0;
+        }
+        const int plim = p.causal ? min(sr.win_hi, L - q_b + qi + 1) : sr.win_hi;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) t[k] = (row_ok && j0 + k < lim) ? t[k] * c : -INFINITY;
+        for (int k = 0; k < 8; ++k) {
+          const bool vis = row_ok && page_ok && j0 + k < tok_end && pos0 + k >= sr.win_lo &&
+                           pos0 + k < plim;
+          t[k] = vis ? t[k] * c : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = (row_ok && j0 + k < lim) ? t[k] * c : -INFINITY;
+      }
       bool over = false;
 #pragma unroll
       for (int k = 0; k < 8; ++k) over |= t[k] > kreg + 0.75f;
@@ -1046,8 +1247,8 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
           // PV(i - 1) done.  PV(i - 2) completed before QK(i) was issued and
           // PV(i + 1) needs this tile's P^T, so the barrier of PV(i - 1)'s
           // parity is within one phase of the awaited one.
-          ok = mbar_wait(bar(((i - 1) & 1) ? BAR_ODONE_1 : BAR_ODONE_0), ((i - 1) >> 1) & 1,
-                         p.wait_cycles);
+          ok = mbar_wait_abort(bar(((i - 1) & 1) ? BAR_ODONE_1 : BAR_ODONE_0),
+                               ((i - 1) >> 1) & 1, p.wait_cycles, abort_flag);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
             tc_fence_after();
@@ -1125,7 +1326,7 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
       scale_s[sid] = sc;
     }
     named_bar_sync(kSoftmaxBarrier, 128);
-    bool fin = mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
+    bool fin = !expired_here(p, WAIT_FINAL, 0) && mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
     fin = __all_sync(0xffffffffu, fin);
     if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
     if (ok && fin && n_tiles > 0) {
@@ -1184,14 +1385,15 @@ static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NR>
-static cudaError_t launch_split_bf16(const void* q, const void* kv, int64_t num_pages, int batch,
-                                     int groups, const DecodeParams& prm, cudaStream_t stream) {
+template <int NR, bool kGather, bool kItems>
+static cudaError_t launch_split_bf16_t(const void* q, const void* kv, int64_t num_pages,
+                                       int batch, int groups, int num_ctas,
+                                       const DecodeParams& prm, cudaStream_t stream) {
   using C = CfgB<NR>;
   static std::atomic<uint64_t> attr_done{0};
   {
-    const cudaError_t e =
-        ensure_smem_attr(mla_split_kv_bf16_kernel<NR>, static_cast<int>(C::kSmemBytes), attr_done);
+    const cudaError_t e = ensure_smem_attr(mla_split_kv_bf16_kernel<NR, kGather, kItems>,
+                                           static_cast<int>(C::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tm_kv, tm_q;
@@ -1199,18 +1401,20 @@ static cudaError_t launch_split_bf16(const void* q, const void* kv, int64_t num_
                      MLA_PAGE_SIZE) ||
       !make_map_bf16(&tm_q, q, static_cast<uint64_t>(batch) * prm.rows_per_req, NR))
     return cudaErrorInvalidValue;
-  dim3 grid(batch, prm.max_splits * groups);
-  mla_split_kv_bf16_kernel<NR><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_q, prm);
+  const dim3 grid = kItems ? dim3(num_ctas) : dim3(batch, prm.max_splits * groups);
+  mla_split_kv_bf16_kernel<NR, kGather, kItems>
+      <<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_q, prm);
   return cudaGetLastError();
 }
 
-static cudaError_t launch_split_bf16_q16(const void* q, const void* kv, int64_t num_pages,
-                                         int batch, int groups, const DecodeParams& prm,
-                                         cudaStream_t stream) {
+template <bool kGather, bool kItems>
+static cudaError_t launch_split_bf16_q16_t(const void* q, const void* kv, int64_t num_pages,
+                                           int batch, int groups, int num_ctas,
+                                           const DecodeParams& prm, cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
   {
-    const cudaError_t e =
-        ensure_smem_attr(mla_split_kv_bf16_q16_kernel, static_cast<int>(q16::kSmemBytes), attr_done);
+    const cudaError_t e = ensure_smem_attr(mla_split_kv_bf16_q16_kernel<kGather, kItems>,
+                                           static_cast<int>(q16::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tm_kv, tm_q;
@@ -1218,10 +1422,42 @@ static cudaError_t launch_split_bf16_q16(const void* q, const void* kv, int64_t 
                      MLA_PAGE_SIZE) ||
       !make_map_bf16(&tm_q, q, static_cast<uint64_t>(batch) * prm.rows_per_req, q16::NR))
     return cudaErrorInvalidValue;
-  dim3 grid(batch, prm.max_splits * groups);
-  mla_split_kv_bf16_q16_kernel<<<grid, q16::kThreads, q16::kSmemBytes, stream>>>(tm_kv, tm_q,
-                                                                                prm);
+  const dim3 grid = kItems ? dim3(num_ctas) : dim3(batch, prm.max_splits * groups);
+  mla_split_kv_bf16_q16_kernel<kGather, kItems>
+      <<<grid, q16::kThreads, q16::kSmemBytes, stream>>>(tm_kv, tm_q, prm);
   return cudaGetLastError();
+}
+
+// Row-group configuration x (key windows or selections) x (item list): each
+// combination is its own kernel instantiation, so the plain grid variant's
+// code is what it is without the options.
+template <int NR>
+static cudaError_t launch_split_bf16(const void* q, const void* kv, int64_t num_pages, int batch,
+                                     int groups, int num_ctas, const DecodeParams& prm,
+                                     cudaStream_t stream) {
+  const bool gather = prm.kv_bounds != nullptr || prm.block_idx != nullptr;
+  const bool items = prm.cta_items != nullptr;
+  if constexpr (NR == q16::NR) {
+    if (gather)
+      return items ? launch_split_bf16_q16_t<true, true>(q, kv, num_pages, batch, groups,
+                                                          num_ctas, prm, stream)
+                   : launch_split_bf16_q16_t<true, false>(q, kv, num_pages, batch, groups,
+                                                           num_ctas, prm, stream);
+    return items ? launch_split_bf16_q16_t<false, true>(q, kv, num_pages, batch, groups,
+                                                         num_ctas, prm, stream)
+                 : launch_split_bf16_q16_t<false, false>(q, kv, num_pages, batch, groups,
+                                                          num_ctas, prm, stream);
+  } else {
+    if (gather)
+      return items ? launch_split_bf16_t<NR, true, true>(q, kv, num_pages, batch, groups,
+                                                          num_ctas, prm, stream)
+                   : launch_split_bf16_t<NR, true, false>(q, kv, num_pages, batch, groups,
+                                                           num_ctas, prm, stream);
+    return items ? launch_split_bf16_t<NR, false, true>(q, kv, num_pages, batch, groups,
+                                                         num_ctas, prm, stream)
+                 : launch_split_bf16_t<NR, false, false>(q, kv, num_pages, batch, groups,
+                                                          num_ctas, prm, stream);
+  }
 }
 
 }  // namespace mla
@@ -1230,13 +1466,14 @@ using namespace mla;
 
 static int decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t num_pages,
                        const int32_t* page_table, int32_t max_pages_per_req,
-                       const int32_t* kv_lens, const int32_t* splits, const int32_t* chunks,
+                       const int32_t* kv_lens, const int32_t* block_idx, int32_t topk,
+                       const int32_t* splits, const int32_t* chunks,
                        int32_t max_splits, int32_t kv_split, int32_t batch, int32_t q_len,
                        int32_t num_heads, int32_t causal, float softmax_scale, void* workspace,
                        size_t workspace_bytes, void* out_bf16, float* lse_f32,
                        float* out_f32_debug, const mla_decode_options_t* options,
-                       void* stream) {
-  const std::string who = options ? "mla_decode_bf16_ex" : "mla_decode_bf16";
+                       const char* who_c, void* stream) {
+  const std::string who(who_c);
   if (!q_bf16 || !kv_pages_bf16 || !page_table || !kv_lens || !splits || !chunks || !workspace ||
       !out_bf16) {
     set_error(who + ": null pointer argument");
@@ -1297,40 +1534,61 @@ static int decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t nu
     const long long w = g_wait_cycles.load();
     prm.wait_cycles = w > 0 ? w : kWaitLimitCycles;
   }
+  prm.debug_expire = g_debug_expire.load();
   prm.status = reinterpret_cast<int*>(ws);
   prm.ws_ml = reinterpret_cast<float*>(ws + ws_ml_offset());
   prm.ws_o = reinterpret_cast<float*>(ws + ws_o_offset(rows_total, max_splits));
   prm.out = reinterpret_cast<__nv_bfloat16*>(out_bf16);
   prm.lse = lse_f32;
   prm.out_f32 = out_f32_debug;
+  prm.block_idx = block_idx;
+  prm.topk = topk;
+  prm.batch = batch;
+  int num_ctas = 0;
   if (options) {
     if (!std::isfinite(options->output_scale)) {
-      set_error("mla_decode_bf16_ex: output_scale must be finite");
+      set_error(who + ": output_scale must be finite");
       return MLA_ERR_INVALID_ARG;
     }
-    if (options->q_scale_dev || options->kv_scale_dev || options->kv_bounds ||
-        options->cta_items) {
-      set_error("mla_decode_bf16_ex: q/kv scales, key windows and item lists are FP8-only");
+    if (options->q_scale_dev || options->kv_scale_dev) {
+      set_error(who + ": q/kv scales are FP8-only (BF16 Q and KV carry no scale)");
       return MLA_ERR_UNSUPPORTED;
+    }
+    if (options->cta_items) {
+      const int64_t cap = static_cast<int64_t>(batch) * max_splits * rg.groups;
+      if (options->num_ctas < 1 || options->num_ctas > cap) {
+        set_error(who + ": num_ctas must be in [1, batch * max_splits * row groups]");
+        return MLA_ERR_INVALID_ARG;
+      }
+      num_ctas = options->num_ctas;
     }
     prm.sm_scale_dev = options->softmax_scale_dev;
     prm.output_scale = options->output_scale;
     prm.sinks = options->sinks;
     prm.query_lens = options->query_lens;
+    prm.kv_bounds = options->kv_bounds;
+    prm.cta_items = options->cta_items;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (rg.nr) {
     case 16:
-      e = launch_split_bf16_q16(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st);
+      e = launch_split_bf16<16>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, num_ctas,
+                                prm, st);
       break;
-    case 32: e = launch_split_bf16<32>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
-    case 48: e = launch_split_bf16<48>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, prm, st); break;
+    case 32:
+      e = launch_split_bf16<32>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, num_ctas,
+                                prm, st);
+      break;
+    case 48:
+      e = launch_split_bf16<48>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, num_ctas,
+                                prm, st);
+      break;
     default:
       set_error(who + ": internal row grouping error");
       return MLA_ERR_UNSUPPORTED;
   }
-  if (e != cudaSuccess) return cuda_fail("mla_decode_bf16: split-KV launch", e);
+  if (e != cudaSuccess) return cuda_fail((who + ": split-KV launch").c_str(), e);
   if (max_splits > 1) {
     MergeParams mp = {};
     mp.po = prm.ws_o;
@@ -1347,7 +1605,7 @@ static int decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t nu
     mp.lse = lse_f32;
     mp.out_f32 = out_f32_debug;
     e = launch_merge(mp, kv_split, st);
-    if (e != cudaSuccess) return cuda_fail("mla_decode_bf16: merge launch", e);
+    if (e != cudaSuccess) return cuda_fail((who + ": merge launch").c_str(), e);
   }
   return MLA_OK;
 }
@@ -1361,9 +1619,9 @@ extern "C" int mla_decode_bf16(const void* q_bf16, const void* kv_pages_bf16, in
                                void* out_bf16, float* lse_f32, float* out_f32_debug,
                                void* stream) {
   return decode_bf16(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_per_req, kv_lens,
-                     splits, chunks, max_splits, kv_split, batch, q_len, num_heads, causal,
-                     softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32, out_f32_debug,
-                     nullptr, stream);
+                     nullptr, 0, splits, chunks, max_splits, kv_split, batch, q_len, num_heads,
+                     causal, softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32,
+                     out_f32_debug, nullptr, "mla_decode_bf16", stream);
 }
 
 extern "C" int mla_decode_bf16_ex(const void* q_bf16, const void* kv_pages_bf16,
@@ -1376,7 +1634,32 @@ extern "C" int mla_decode_bf16_ex(const void* q_bf16, const void* kv_pages_bf16,
                                   void* out_bf16, float* lse_f32, float* out_f32_debug,
                                   const mla_decode_options_t* options, void* stream) {
   return decode_bf16(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_per_req, kv_lens,
-                     splits, chunks, max_splits, kv_split, batch, q_len, num_heads, causal,
-                     softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32, out_f32_debug,
-                     options, stream);
+                     nullptr, 0, splits, chunks, max_splits, kv_split, batch, q_len, num_heads,
+                     causal, softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32,
+                     out_f32_debug, options, "mla_decode_bf16_ex", stream);
+}
+
+extern "C" int mla_decode_bf16_sparse(const void* q_bf16, const void* kv_pages_bf16,
+                                      int64_t num_pages, const int32_t* page_table,
+                                      int32_t max_pages_per_req, const int32_t* kv_lens,
+                                      const int32_t* block_idx, int32_t topk,
+                                      const int32_t* splits, const int32_t* chunks,
+                                      int32_t max_splits, int32_t kv_split, int32_t batch,
+                                      int32_t q_len, int32_t num_heads, int32_t causal,
+                                      float softmax_scale, void* workspace,
+                                      size_t workspace_bytes, void* out_bf16, float* lse_f32,
+                                      float* out_f32_debug, const mla_decode_options_t* options,
+                                      void* stream) {
+  if (!block_idx) {
+    set_error("mla_decode_bf16_sparse: null block_idx");
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (topk < 1 || static_cast<int64_t>(topk) * MLA_PAGE_SIZE > INT32_MAX / 2) {
+    set_error("mla_decode_bf16_sparse: topk must be >= 1 and 32 * topk must fit in int32");
+    return MLA_ERR_INVALID_ARG;
+  }
+  return decode_bf16(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_per_req, kv_lens,
+                     block_idx, topk, splits, chunks, max_splits, kv_split, batch, q_len,
+                     num_heads, causal, softmax_scale, workspace, workspace_bytes, out_bf16,
+                     lse_f32, out_f32_debug, options, "mla_decode_bf16_sparse", stream);
 }

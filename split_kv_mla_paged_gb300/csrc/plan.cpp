@@ -148,27 +148,30 @@ extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t nu
   return MLA_OK;
 }
 
-extern "C" int mla_decode_plan_items(const int32_t* splits, int32_t batch, int32_t num_heads,
-                                     int32_t q_len, int32_t* items_out, int32_t capacity,
-                                     int32_t* n_items_out) {
+// The item list of a plan for row groups `rg` (shared by the FP8 and BF16
+// builders, whose kernels group rows differently).
+static int plan_items(const char* who_c, const int32_t* splits, int32_t batch, int32_t num_heads,
+                      int32_t q_len, bool bf16, int32_t* items_out, int32_t capacity,
+                      int32_t* n_items_out) {
+  const std::string who(who_c);
   if (!splits || !n_items_out) {
-    set_error("mla_decode_plan_items: null pointer argument");
+    set_error(who + ": null pointer argument");
     return MLA_ERR_INVALID_ARG;
   }
   if (batch < 1 || num_heads < 1 || q_len < 1 || batch > MLA_ITEM_MAX_BATCH) {
-    set_error("mla_decode_plan_items: batch in [1, MLA_ITEM_MAX_BATCH], num_heads, q_len >= 1");
+    set_error(who + ": batch in [1, MLA_ITEM_MAX_BATCH], num_heads, q_len >= 1");
     return MLA_ERR_INVALID_ARG;
   }
   if (static_cast<int64_t>(num_heads) * q_len > MLA_MAX_ROWS) {
-    set_error("mla_decode_plan_items: num_heads * q_len exceeds MLA_MAX_ROWS");
+    set_error(who + ": num_heads * q_len exceeds MLA_MAX_ROWS");
     return MLA_ERR_UNSUPPORTED;
   }
-  const RowGroups rg = row_groups_fp8(num_heads * q_len);
+  const RowGroups rg = bf16 ? row_groups(num_heads * q_len) : row_groups_fp8(num_heads * q_len);
   int32_t max_splits = 0;
   int64_t total = 0;
   for (int b = 0; b < batch; ++b) {
     if (splits[b] < 1 || splits[b] > MLA_MAX_SPLITS) {
-      set_error("mla_decode_plan_items: splits[" + std::to_string(b) + "] out of range");
+      set_error(who + ": splits[" + std::to_string(b) + "] out of range");
       return MLA_ERR_INVALID_ARG;
     }
     max_splits = std::max(max_splits, splits[b]);
@@ -177,7 +180,7 @@ extern "C" int mla_decode_plan_items(const int32_t* splits, int32_t batch, int32
   *n_items_out = static_cast<int32_t>(total);
   if (!items_out) return MLA_OK;  // size query
   if (capacity < total) {
-    set_error("mla_decode_plan_items: capacity " + std::to_string(capacity) + " below the " +
+    set_error(who + ": capacity " + std::to_string(capacity) + " below the " +
               std::to_string(total) + " items");
     return MLA_ERR_INVALID_ARG;
   }
@@ -190,4 +193,18 @@ extern "C" int mla_decode_plan_items(const int32_t* splits, int32_t batch, int32
         for (int g = 0; g < rg.groups; ++g)
           items_out[k++] = (b << MLA_ITEM_B_SHIFT) | (s << MLA_ITEM_S_SHIFT) | g;
   return MLA_OK;
+}
+
+extern "C" int mla_decode_plan_items(const int32_t* splits, int32_t batch, int32_t num_heads,
+                                     int32_t q_len, int32_t* items_out, int32_t capacity,
+                                     int32_t* n_items_out) {
+  return plan_items("mla_decode_plan_items", splits, batch, num_heads, q_len, false, items_out,
+                    capacity, n_items_out);
+}
+
+extern "C" int mla_decode_plan_items_bf16(const int32_t* splits, int32_t batch, int32_t num_heads,
+                                          int32_t q_len, int32_t* items_out, int32_t capacity,
+                                          int32_t* n_items_out) {
+  return plan_items("mla_decode_plan_items_bf16", splits, batch, num_heads, q_len, true,
+                    items_out, capacity, n_items_out);
 }

@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import split_kv_mla_paged_gb300 as mla
@@ -137,7 +138,41 @@ def test_kv_append_host_checks(lib):
 
 def test_bf16_ex_rejects_fp8_only_options(lib):
     fake = ctypes.c_void_p(1 << 20)
-    opts = mla.DecodeOptions(None, None, None, 1.0, None, None, fake, None, 0)
+    opts = mla.DecodeOptions(fake, None, None, 1.0, None, None, None, None, 0)
     st = lib.mla_decode_bf16_ex(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 0.1,
                                 fake, 1 << 30, fake, None, None, ctypes.byref(opts), None)
     assert st == mla.MLA_ERR_UNSUPPORTED and "FP8-only" in mla.mla_last_error()
+
+
+def test_bf16_item_list_size_is_checked(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    opts = mla.DecodeOptions(None, None, None, 1.0, None, None, None, fake, 0)
+    st = lib.mla_decode_bf16_ex(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 0.1,
+                                fake, 1 << 30, fake, None, None, ctypes.byref(opts), None)
+    assert st == mla.MLA_ERR_INVALID_ARG and "num_ctas" in mla.mla_last_error()
+
+
+def test_bf16_sparse_host_checks(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake, fake, 4, fake, 4, fake]
+    tail = [fake, fake, 2, 2, 1, 1, 12, 0, 0.1, fake, 1 << 30, fake, None, None, None, None]
+    assert lib.mla_decode_bf16_sparse(*args, None, 8, *tail) == mla.MLA_ERR_INVALID_ARG
+    assert "block_idx" in mla.mla_last_error()
+    assert lib.mla_decode_bf16_sparse(*args, fake, 0, *tail) == mla.MLA_ERR_INVALID_ARG
+    assert "topk" in mla.mla_last_error()
+    small = list(tail)
+    small[10] = 16  # workspace bytes
+    assert lib.mla_decode_bf16_sparse(*args, fake, 8, *small) == mla.MLA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_bf16_item_lists_use_the_bf16_row_groups(lib):
+    splits = [3, 1, 2]
+    # Up to 48 rows both kernels run one CTA per split.
+    assert np.array_equal(mla.mla_decode_plan_items(splits, 12, 4),
+                          mla.mla_decode_plan_items_bf16(splits, 12, 4))
+    # 96 rows: one FP8 CTA per split, two BF16 CTAs (48 rows each).
+    fp8 = mla.mla_decode_plan_items(splits, 12, 8)
+    bf16 = mla.mla_decode_plan_items_bf16(splits, 12, 8)
+    assert len(fp8) == sum(splits) and len(bf16) == 2 * sum(splits)
+    groups = bf16 & ((1 << 5) - 1)
+    assert sorted(set(groups.tolist())) == [0, 1]
