@@ -394,8 +394,9 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         window_nv = window_next_nv;
         window_next = load_window((i >> 3) + 1, window_next_nv);
       }
-      bool ok = true;
-      if (round > 0) ok = mbar_wait(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles);
+      bool ok = !expired_here(p, WAIT_STAGE_FREE, i);
+      if (ok && round > 0)
+        ok = mbar_wait_abort(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles, abort_flag);
       ok = __all_sync(0xffffffffu, ok && !*abort_flag);
       if (!ok) {
         if (lane == 0) {
@@ -530,6 +531,12 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       int qk_st = 0, qk_round = 0, pv_st = 0;
       long long t_last = clock64();
       while (ok && pv < n_tiles) {
+        if ((pv < qk && expired_here(p, WAIT_P_FULL, pv)) ||
+            (qk < n_tiles && qk <= pv + 1 && expired_here(p, WAIT_TILE_FULL, qk))) {
+          fail();
+          ok = false;
+          break;
+        }
         int action = 0;
         if (lane == 0) {
           if (pv < qk) {
@@ -586,11 +593,13 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int sb = (C::NS == 2) ? (j & 1) : 0;
         const int use = (C::NS == 2) ? (j >> 1) : j;
-        bool w = mbar_wait(bar(BAR_FULL0 + st), round & 1, p.wait_cycles);
-        if (w && use >= 1) w = mbar_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles);
+        bool w = !expired_here(p, WAIT_TILE_FULL, j) &&
+                 mbar_wait_abort(bar(BAR_FULL0 + st), round & 1, p.wait_cycles, abort_flag);
+        if (w && use >= 1)
+          w = mbar_wait_abort(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles, abort_flag);
         if (w && j >= 2)
-          w = mbar_wait(bar(((j - 2) & 1) ? C::kBarOdone1 : BAR_ODONE), ((j - 2) >> 1) & 1,
-                        p.wait_cycles);
+          w = mbar_wait_abort(bar(((j - 2) & 1) ? C::kBarOdone1 : BAR_ODONE), ((j - 2) >> 1) & 1,
+                              p.wait_cycles, abort_flag);
         w = __all_sync(0xffffffffu, w && !*abort_flag);
         if (!w) {
           ok = false;
@@ -615,7 +624,8 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       for (int i = 0; ok && i < n_tiles; ++i) {
         const int pb = (C::NPB == 1) ? 0 : (i & 1);
         const int use = (C::NPB == 1) ? i : (i >> 1);
-        bool w = mbar_wait(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles);
+        bool w = !expired_here(p, WAIT_P_FULL, i) &&
+                 mbar_wait_abort(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles, abort_flag);
         w = __all_sync(0xffffffffu, w && !*abort_flag);
         if (!w) {
           ok = false;
@@ -738,8 +748,11 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       float* thr = kref;                                  // k + 0.75 per row
       int* kci = reinterpret_cast<int*>(base + C::kKci);  // exponent offset per row
       for (int i = 0; i < n_tiles; ++i) {
-        if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0), i & 1, p.wait_cycles);
+        if (ok)
+          ok = !expired_here(p, WAIT_S_FULL, i) &&
+               mbar_wait_abort(bar(BAR_SFULL0), i & 1, p.wait_cycles, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
         float t[NRH];
         if (ok) {
           tc_fence_after();
@@ -807,8 +820,8 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
             // Rescale the O^T columns of rows whose reference moved (rare),
             // once PV(i - 1) is done (its completion barrier is within one
             // phase of the awaited one, as in the other configurations).
-            ok = mbar_wait(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE), ((i - 1) >> 1) & 1,
-                           p.wait_cycles);
+            ok = mbar_wait_abort(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE),
+                                 ((i - 1) >> 1) & 1, p.wait_cycles, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
               tc_fence_after();
@@ -842,10 +855,11 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < NRH; ++k) lsum[k] += t[k];
         // P^T (one buffer): wait until PV(i - 1) has read it.
-        if (ok && i >= 1) {
-          ok = mbar_wait(bar(BAR_PFREE0), (i - 1) & 1, p.wait_cycles);
-          ok = __all_sync(0xffffffffu, ok);
-        }
+        if (ok && expired_here(p, WAIT_P_FREE, i)) ok = false;
+        if (ok && i >= 1)
+          ok = mbar_wait_abort(bar(BAR_PFREE0), (i - 1) & 1, p.wait_cycles, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) *abort_flag = 1;
         if (ok) {
           // MN-major [term][NR/16 row groups][128 tokens][16 rows]: one
           // 16-byte store per term and 16-row group.
@@ -873,8 +887,11 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       for (int i = 0; i < n_tiles; ++i) {
         const int sb = (C::NS == 2) ? (i & 1) : 0;
         const int use = (C::NS == 2) ? (i >> 1) : i;
-        if (ok) ok = !*abort_flag && mbar_wait(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles);
+        if (ok)
+          ok = !expired_here(p, WAIT_S_FULL, i) &&
+               mbar_wait_abort(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
         float t[NRH];
         if (ok) {
           tc_fence_after();
@@ -945,8 +962,8 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
             // two barriers, and the one of PV(i-1)'s parity is within one phase
             // of the awaited one: s_full(i) implies PV(i-2) completed (QK(i)
             // waits for it) and PV(i+1) needs a later tile's P^T.
-            ok = mbar_wait(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE), ((i - 1) >> 1) & 1,
-                           p.wait_cycles);
+            ok = mbar_wait_abort(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE),
+                                 ((i - 1) >> 1) & 1, p.wait_cycles, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
               tc_fence_after();
@@ -982,10 +999,11 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         // uses the same rule.
         const int pb = i & 1;
         const int puse = i >> 1;
-        if (ok && !C::kPInStage && puse >= 1) {
-          ok = mbar_wait(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles);
-          ok = __all_sync(0xffffffffu, ok);
-        }
+        if (ok && !C::kPInStage && expired_here(p, WAIT_P_FREE, i)) ok = false;
+        if (ok && !C::kPInStage && puse >= 1)
+          ok = mbar_wait_abort(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) *abort_flag = 1;
         if (ok) {
           // P^T of tile i goes to the rope block of its KV stage (consumed by
           // QK(i), which s_full(i) reports complete) or to a P buffer.
@@ -1073,7 +1091,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     }
     named_bar_sync(kSoftmaxBarrier, NT);
     // Each MMA warp commits BAR_FINAL once, after its last MMA.
-    bool fin = mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
+    bool fin = !expired_here(p, WAIT_FINAL, 0) && mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
     fin = __all_sync(0xffffffffu, fin);
     if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
     if (ok && fin && n_tiles > 0) {
@@ -1203,6 +1221,7 @@ static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages
 }
 
 std::atomic<long long> g_wait_cycles{0};
+std::atomic<int> g_debug_expire{-1};
 
 bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
@@ -1324,6 +1343,7 @@ static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
     const long long w = g_wait_cycles.load();
     prm.wait_cycles = w > 0 ? w : kWaitLimitCycles;
   }
+  prm.debug_expire = g_debug_expire.load();
   prm.status = reinterpret_cast<int*>(ws);
   prm.ws_ml = reinterpret_cast<float*>(ws + ws_ml_offset());
   prm.ws_o = reinterpret_cast<float*>(ws + ws_o_offset(rows_total, max_splits));
@@ -1647,6 +1667,12 @@ extern "C" int mla_decode_static_ws_status(void* stream) {
 
 extern "C" void mla_debug_set_wait_limit(long long cycles) {
   g_wait_cycles.store(cycles > 0 ? cycles : 0);
+}
+
+extern "C" void mla_debug_set_expire(int32_t role, int32_t tile) {
+  g_debug_expire.store((role < 0 || role > 255 || tile < 0 || tile >= (1 << 24))
+                           ? -1
+                           : (role << 24) | tile);
 }
 
 extern "C" int mla_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {

@@ -56,6 +56,9 @@ struct DecodeParams {
   const int32_t* cta_items;
   int32_t batch;
   long long wait_cycles;   // limit of the pipeline waits (drains always use the long limit)
+  // Test hook (mla_debug_set_expire): (role << 24) | tile makes that one
+  // pipeline wait read as expired; -1 = off.
+  int32_t debug_expire;
   int* status;
   float* ws_ml;
   float* ws_o;
@@ -73,6 +76,18 @@ static_assert(BAR_COUNT <= 17, "barrier slots");
 
 __device__ __forceinline__ void report(int* status, int code) {
   atomicCAS(status, 0, code);
+}
+
+// Pipeline wait roles of the test hook: the producer's wait for a free stage,
+// the QK issuer's wait for a landed tile, the PV issuer's wait for P^T, the
+// softmax's waits for S^T and for a free P^T buffer, and the softmax's wait
+// for the last MMAs before the epilogue (tile 0).
+enum : int {
+  WAIT_STAGE_FREE = 0, WAIT_TILE_FULL = 1, WAIT_P_FULL = 2, WAIT_S_FULL = 3, WAIT_P_FREE = 4,
+  WAIT_FINAL = 5
+};
+__device__ __forceinline__ bool expired_here(const DecodeParams& p, int role, int i) {
+  return p.debug_expire == ((role << 24) | i);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -309,5 +324,8 @@ bool aligned(const void* p, uintptr_t a);
 int cuda_fail(const char* what, cudaError_t e);
 // Test hook: limit of the pipeline waits for later launches (0 = default).
 extern std::atomic<long long> g_wait_cycles;
+// Test hook: the pipeline wait (role << 24) | tile that later launches treat
+// as expired (-1 = none).
+extern std::atomic<int> g_debug_expire;
 
 }  // namespace mla

@@ -69,6 +69,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// mbar_wait that also gives up (returns false) once *abort is set, for the
+// pipeline waits of a CTA in which another role has already failed.  The
+// first test is the same as mbar_wait's, so a phase that has completed costs
+// nothing extra.
+__device__ __forceinline__ bool mbar_wait_abort(uint32_t bar, uint32_t parity,
+                                                long long limit_cycles,
+                                                const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort || clock64() - t0 > limit_cycles) return false;
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
