@@ -89,8 +89,10 @@ typedef enum {
  *              1..MLA_MAX_SPLITS for the GB300 planner: a single long request
  *              can then fill every SM), chunk_out[batch]
  *              (tokens per split, a multiple of 128, splits*chunk >= L),
- *              *kv_split_out (merge thread groups: 1, 2, 4, 8 or 16, about
- *              four partials per group) and
+ *              *kv_split_out (merge thread groups: the largest of 16, 8, 4, 2,
+ *              1 with at least two partials per group and
+ *              batch * num_heads * q_len * groups <= 6 * sm_count, with
+ *              sm_count 152 when <= 0) and
  *              *workspace_bytes_out for mla_decode with max(splits).
  */
 MLA_API int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t num_heads, int32_t q_len,

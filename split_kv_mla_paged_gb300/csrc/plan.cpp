@@ -36,6 +36,9 @@ static int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // The GB300 planner's CTA budget, in waves of sm_count CTAs.
 constexpr int kMaxWaves = 2;
+// SMs assumed by the merge's KvSplit budget when the caller passes none (the
+// pages' planner mode): a GB300.
+constexpr int kDefaultSms = 152;
 
 // CTAs the split kernel launches with a common chunk (empty slots excluded).
 static int64_t ctas_for_chunk(const int32_t* lens, int batch, int64_t chunk, int groups) {
@@ -139,10 +142,20 @@ extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t nu
   }
   int32_t max_splits = 1;
   for (int b = 0; b < batch; ++b) max_splits = std::max(max_splits, splits_out[b]);
-  // Merge thread groups: about four partials per group (each group keeps four
-  // loads in flight), at most 16 groups.
+  // Merge thread groups (KvSplit): PR #20380 "Description" takes the largest
+  // power of two up to the cap that still gives every group whole work and
+  // keeps the grid within its CTA budget.  Here: the largest power of two up
+  // to 16 with at least two partials per group and rows x groups <= 6 x SMs
+  // (the merge runs rows x 4 CTAs of 32 threads per group, so this keeps it
+  // near a third of the GPU's thread slots; past that, more groups add
+  // threads but no parallel loads).  Fitted to the
+  // merge-only sweep on GB300 (rows 12-768, 6-152 splits, every KvSplit):
+  // within 5 % of the best KvSplit per point in total, against 14 % for
+  // "about four partials per group".
+  const int64_t rows = static_cast<int64_t>(batch) * num_heads * q_len;
+  const int64_t budget = 6 * static_cast<int64_t>(sm_count > 0 ? sm_count : kDefaultSms);
   int32_t g = 16;
-  while (g > 1 && g * 4 > max_splits) g >>= 1;
+  while (g > 1 && (g * 2 > max_splits || rows * g > budget)) g >>= 1;
   *kv_split_out = g;
   *workspace_bytes_out = mla_decode_workspace_size(batch, q_len, num_heads, max_splits);
   return MLA_OK;

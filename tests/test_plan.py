@@ -163,3 +163,17 @@ def test_plan_items_rejects_bad_splits():
         mla.mla_decode_plan_items([2, 0], 12, 1)
     with pytest.raises(mla.MlaError):
         mla.mla_decode_plan_items([2, mla.MAX_SPLITS + 1], 12, 1)
+
+
+@pytest.mark.parametrize("rows_hq,splits,expect", [
+    ((12, 1), 6, 2), ((12, 1), 12, 4), ((12, 1), 25, 8), ((12, 1), 128, 16),
+    ((12, 8), 25, 8), ((12, 8), 128, 8), ((12, 16), 50, 4), ((96, 8), 19, 1), ((12, 1), 1, 1),
+])
+def test_merge_kv_split_rule(rows_hq, splits, expect):
+    # KvSplit = the largest of 16/8/4/2/1 with >= 2 partials per group and
+    # rows x groups <= 6 x SMs (152 SMs: 912); one request planned by the
+    # pages' planner to exactly `splits` splits of one tile each.
+    H, q = rows_hq
+    p = mla.mla_decode_plan([splits * 128], num_heads=H, q_len=q, sm_count=152,
+                            target_ctas=splits)
+    assert p.max_splits == splits and p.kv_split == expect
