@@ -30,9 +30,9 @@
 //    power of two, so the E4M3-quantised P fed to the PV MMA, and every
 //    partial, is the same for any split plan up to exact scaling.
 //  * Warp roles: warp 0 issues TMA, warp 1 issues the QK tcgen05.mma (and
-//    owns TMEM), warp 2 the PV ones (the 96-row CTA issues both from warp 1),
-//    and the next four warps (eight from 32 rows up; TMEM lane quadrant =
-//    warp % 4) run the softmax, the rare O correction and the epilogue.
+//    owns TMEM), warp 2 the PV ones, and the next four warps (eight from 32
+//    rows up; TMEM lane quadrant = warp % 4) run the softmax, the rare O
+//    correction and the epilogue.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -79,10 +79,11 @@ struct Cfg {
   static constexpr int NRH = NR / SWG;
   static_assert(NRH % 8 == 0, "rows per softmax warpgroup");
   // Warp 0 TMA, warp 1 QK issuer (and TMEM owner), warp 2 PV issuer, then
-  // the softmax warpgroups.  The 96-row CTA issues both from warp 1 (one S^T
-  // and one P^T buffer leave a second issuer nothing to overlap: measured
-  // 441 -> 475 us on MTP q8 B16 128K with two).
-  static constexpr int kMmaWarps = kWide ? 1 : 2;
+  // the softmax warpgroups.  Each issuer blocks on its own barriers; for the
+  // 96-row CTA this measured 2 % faster on H96 q8 B1 1M (and 1 % slower on
+  // MTP q8 B16 128K) than one warp polling both, and the polling loop lost
+  // 4 % to any extra work in it.
+  static constexpr int kMmaWarps = 2;
   static constexpr int kSoftmaxWarp0 = 1 + kMmaWarps;
   static constexpr int kThreads = 32 * kSoftmaxWarp0 + 128 * SWG;
   static constexpr uint32_t kTmemCols =
@@ -458,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
     }
     __syncwarp();
-  } else if (warp == 1 || (!C::kWide && warp == 2)) {
+  } else if (warp == 1 || warp == 2) {
     // ================= MMA issuers: warp 1 QK, warp 2 PV =================
     // Two issuing warps keep the tensor pipe fed with QK(i + 1) while PV(i)
     // goes out: one warp issuing both left ~30 % of the pipe's rate unused
@@ -521,71 +522,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     };
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) fail();
-    if constexpr (C::kWide) {
-      // One issuing warp.  PV(pv) goes out as soon as its P^T is ready and QK(qk) as
-      // soon as its tile has landed and its S^T buffer is free, in whichever
-      // order they become ready; QK runs at most one tile ahead of PV
-      // (qk <= pv + 1), which keeps each p_full barrier at most one phase ahead
-      // of this warp.  PV is preferred: it releases a KV stage.
-      int qk = 0, pv = 0;
-      int qk_st = 0, qk_round = 0, pv_st = 0;
-      long long t_last = clock64();
-      while (ok && pv < n_tiles) {
-        if ((pv < qk && expired_here(p, WAIT_P_FULL, pv)) ||
-            (qk < n_tiles && qk <= pv + 1 && expired_here(p, WAIT_TILE_FULL, qk))) {
-          fail();
-          ok = false;
-          break;
-        }
-        int action = 0;
-        if (lane == 0) {
-          if (pv < qk) {
-            const int pb = (C::NPB == 1) ? 0 : (pv & 1);
-            const int use = (C::NPB == 1) ? pv : (pv >> 1);
-            if (mbar_test_wait(bar(BAR_PFULL0 + pb), use & 1)) action = 1;
-          }
-          if (action == 0 && qk < n_tiles && qk <= pv + 1) {
-            const int sb = (C::NS == 2) ? (qk & 1) : 0;
-            const int use = (C::NS == 2) ? (qk >> 1) : qk;
-            if (mbar_test_wait(bar(BAR_FULL0 + qk_st), qk_round & 1) &&
-                (use < 1 || mbar_test_wait(bar(BAR_SFREE0 + sb), (use - 1) & 1)))
-              action = 2;
-          }
-        }
-        action = __shfl_sync(0xffffffffu, action, 0);
-        if (action == 1) {
-          if (lane == 0) issue_pv(pv, pv_st, (C::NPB == 1) ? 0 : (pv & 1));
-          __syncwarp();
-          ++pv;
-          if (++pv_st == C::NST) pv_st = 0;
-          t_last = clock64();
-        } else if (action == 2) {
-          // Rows loaded per page, as the producer published them with the
-          // stage's full barrier (which lane 0 has just observed).
-          uint32_t info = 0;
-          if constexpr (kGather) {
-            if (lane == 0) info = *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * qk_st);
-            info = __shfl_sync(0xffffffffu, info, 0);
-          }
-          zero_unloaded_rows<kGather>(base + C::kKV + qk_st * kTileBytes, lane, info,
-                                      tok_end - (t0 + qk * kTileTokens));
-          if (lane == 0) issue_qk(qk_st, (C::NS == 2) ? (qk & 1) : 0);
-          __syncwarp();
-          ++qk;
-          if (++qk_st == C::NST) {
-            qk_st = 0;
-            ++qk_round;
-          }
-          t_last = clock64();
-        } else {
-          const bool late = (clock64() - t_last > p.wait_cycles) || *abort_flag;
-          if (__any_sync(0xffffffffu, late)) {
-            fail();
-            ok = false;
-          }
-        }
-      }
-    } else if (warp == 1) {
+    if (warp == 1) {
       // QK(j) once its tile has landed, its S^T buffer is free and PV(j - 2)
       // has completed (so the softmax's wait for PV(j - 1) stays within one
       // phase of its barrier; QK(j) still overlaps PV(j - 1)).
@@ -597,7 +534,10 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
                  mbar_wait_abort(bar(BAR_FULL0 + st), round & 1, p.wait_cycles, abort_flag);
         if (w && use >= 1)
           w = mbar_wait_abort(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles, abort_flag);
-        if (w && j >= 2)
+        // The 96-row CTA needs no PV(j - 2) wait: its softmax waited for PV(i - 2)
+        // (the P^T buffer) before writing P(i - 1), which keeps its wait for
+        // PV(i - 1) within one phase; the tile's stage implies PV(j - 2) anyway.
+        if (w && j >= 2 && !C::kWide)
           w = mbar_wait_abort(bar(((j - 2) & 1) ? C::kBarOdone1 : BAR_ODONE), ((j - 2) >> 1) & 1,
                               p.wait_cycles, abort_flag);
         w = __all_sync(0xffffffffu, w && !*abort_flag);
