@@ -415,6 +415,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--plan", choices=["gb300", "pages"], default="gb300")
+    ap.add_argument("--target", type=int, default=0,
+                    help="CTA target of the pages' planner formula (overrides --plan)")
+    ap.add_argument("--persistent", type=int, default=0,
+                    help="run the plan's CTA item list with this many persistent CTAs (FP8)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--kv-append", action="store_true",
                     help="time the FP8 paged KV append (decode-sized and prefill-sized batches)")
@@ -474,7 +478,10 @@ def main():
     # A sparse decode is planned over the compact range of its selection.
     plan_lens = [32 * topk] * B if is_sparse else lens
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    if args.plan == "pages" and w["target"] is not None:
+    if args.target > 0:
+        plan = mla.mla_decode_plan(plan_lens, H, q_len, sm_count=sm_count,
+                                   target_ctas=args.target)
+    elif args.plan == "pages" and w["target"] is not None:
         plan = mla.mla_decode_plan(plan_lens, H, q_len, target_ctas=w["target"])
     else:
         plan = mla.mla_decode_plan(plan_lens, H, q_len, sm_count=sm_count)
@@ -520,7 +527,8 @@ def main():
 
     # A plan with empty split slots (a skewed or ragged batch) launches the FP8
     # kernel over its CTA item list: exactly the CTAs that have work.
-    use_items = (not is_bf16) and bool(np.any(plan.splits < plan.max_splits))
+    use_items = (not is_bf16) and (bool(np.any(plan.splits < plan.max_splits))
+                                   or args.persistent > 0)
     items_h = mla.mla_decode_plan_items(plan.splits, H, q_len) if use_items else None
     items_d = torch.from_numpy(items_h).to(dev) if use_items else None
 
@@ -529,11 +537,12 @@ def main():
         c, s = a[:-1], a[-1]
         it = items_d if items is None else items
         if is_sparse:
-            mla.mla_decode_sparse(*c[:6], c[22], topk, *c[6:22], cta_items=it, stream=s)
+            mla.mla_decode_sparse(*c[:6], c[22], topk, *c[6:22], cta_items=it,
+                                  persistent_ctas=args.persistent, stream=s)
         elif is_bf16:  # BF16 Q and KV: no q/kv scales
             mla.mla_decode_bf16(*c[:14], *c[16:22], s)
         elif use_items:
-            mla.mla_decode_ex(*c[:22], cta_items=it, stream=s)
+            mla.mla_decode_ex(*c[:22], cta_items=it, persistent_ctas=args.persistent, stream=s)
         else:
             mla.mla_decode(*c[:22], s)
 
@@ -726,7 +735,9 @@ def main():
             "data": ("synthetic (seeded N(0,0.5^2) cast to "
                      f"{'BF16' if is_bf16 else 'E4M3'}, random pages)"),
             "config": {"workload": args.workload, "batch": B, "num_heads": H, "q_len": q_len,
-                       "kv_len": lens[0], "causal": w["causal"], "plan": args.plan,
+                       "kv_len": lens[0], "causal": w["causal"],
+                       "plan": f"target {args.target}" if args.target > 0 else args.plan,
+                       "persistent_ctas": args.persistent,
                        "splits": plan.splits.tolist()[:4] + (["..."] if B > 4 else []),
                        "kv_split": plan.kv_split, "kv_bytes": kv_bytes,
                        "cta_items": use_items,

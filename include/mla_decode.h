@@ -91,8 +91,8 @@ typedef enum {
  *              (tokens per split, a multiple of 128, splits*chunk >= L),
  *              *kv_split_out (merge thread groups: the largest of 16, 8, 4, 2,
  *              1 with at least two partials per group and
- *              batch * num_heads * q_len * groups <= 6 * sm_count, with
- *              sm_count 152 when <= 0) and
+ *              (num_heads * q_len * the requests with more than one split)
+ *              * groups <= 6 * sm_count, with sm_count 152 when <= 0) and
  *              *workspace_bytes_out for mla_decode with max(splits).
  */
 MLA_API int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t num_heads, int32_t q_len,
@@ -193,6 +193,14 @@ MLA_API int mla_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_
  * cta_items, num_ctas  NULL / 0, or the device copy of the item list of
  *     mla_decode_plan_items for this call's splits and its length: the
  *     split-KV kernel then launches exactly num_ctas CTAs.
+ * persistent_ctas  0, or (with an item list) the number of persistent CTAs
+ *     (issue #20510, "Repro 1": the run() argument is_persistent; plain
+ *     reading): min(persistent_ctas, num_ctas) CTAs are launched and CTA c
+ *     works on items c, c + grid, c + 2 grid, ... of the list, one after
+ *     another, loading the next item's Q and first KV tiles while it
+ *     finishes the current one, so each CTA's start-up is paid once.  The
+ *     results are the same numbers as with one CTA per item.  FP8 entry
+ *     points only (the BF16 ones return MLA_ERR_UNSUPPORTED).
  * Zero-initialise the structure: fields added later default to off.
  */
 typedef struct {
@@ -205,6 +213,7 @@ typedef struct {
   const int32_t* kv_bounds;
   const int32_t* cta_items;
   int32_t num_ctas;
+  int32_t persistent_ctas;
 } mla_decode_options_t;
 
 /* mla_decode with options (NULL options = mla_decode).  Same arguments,

@@ -61,7 +61,7 @@ class DecodeOptions(ctypes.Structure):
                 ("softmax_scale_dev", ctypes.c_void_p), ("output_scale", ctypes.c_float),
                 ("sinks", ctypes.c_void_p), ("query_lens", ctypes.c_void_p),
                 ("kv_bounds", ctypes.c_void_p), ("cta_items", ctypes.c_void_p),
-                ("num_ctas", ctypes.c_int32)]
+                ("num_ctas", ctypes.c_int32), ("persistent_ctas", ctypes.c_int32)]
 
 
 class MlaError(RuntimeError):
@@ -249,13 +249,16 @@ def mla_decode_ex(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req,
                   kv_scale, softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32=None,
                   out_f32_debug=None, *, q_scale_dev=None, kv_scale_dev=None,
                   softmax_scale_dev=None, output_scale: float = 1.0, sinks=None,
-                  query_lens=None, kv_bounds=None, cta_items=None, stream=None) -> None:
+                  query_lens=None, kv_bounds=None, cta_items=None, persistent_ctas: int = 0,
+                  stream=None) -> None:
     """mla_decode with device-side scales, an output scale, attention sinks,
     ragged query counts, key windows and a CTA item list (a device int32
-    tensor from mla_decode_plan_items)."""
+    tensor from mla_decode_plan_items), optionally run by persistent_ctas
+    CTAs that loop over the list."""
     opts = DecodeOptions(_ptr(q_scale_dev), _ptr(kv_scale_dev), _ptr(softmax_scale_dev),
                          float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds),
-                         _ptr(cta_items), 0 if cta_items is None else int(cta_items.numel()))
+                         _ptr(cta_items), 0 if cta_items is None else int(cta_items.numel()),
+                         int(persistent_ctas))
     lib = load_library()
     _check(lib.mla_decode_ex(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages), _ptr(page_table),
                              int(max_pages_per_req), _ptr(kv_lens), _ptr(splits), _ptr(chunks),
@@ -332,12 +335,13 @@ def mla_decode_sparse(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_
                       workspace_bytes, out_bf16, lse_f32=None, out_f32_debug=None, *,
                       q_scale_dev=None, kv_scale_dev=None, softmax_scale_dev=None,
                       output_scale: float = 1.0, sinks=None, query_lens=None, kv_bounds=None,
-                      cta_items=None, stream=None) -> None:
+                      cta_items=None, persistent_ctas: int = 0, stream=None) -> None:
     """Sparse decode over the selected pages block_idx [batch, topk] (plan with
     the compact lengths 32 * topk)."""
     opts = DecodeOptions(_ptr(q_scale_dev), _ptr(kv_scale_dev), _ptr(softmax_scale_dev),
                          float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds),
-                         _ptr(cta_items), 0 if cta_items is None else int(cta_items.numel()))
+                         _ptr(cta_items), 0 if cta_items is None else int(cta_items.numel()),
+                         int(persistent_ctas))
     lib = load_library()
     _check(lib.mla_decode_sparse(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages),
                                  _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),
@@ -445,7 +449,7 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
            kv_split: Optional[int] = None, want_f32: bool = False, stream=None,
            check_status: bool = True, sinks=None, output_scale: float = 1.0,
            device_scales: bool = False, query_lens=None, kv_bounds=None, block_idx=None,
-           use_items: Optional[bool] = None):
+           use_items: Optional[bool] = None, persistent_ctas: int = 0):
     """Plan, allocate outputs and a workspace with torch, and run mla_decode.
 
     q_fp8 uint8 [B, q, H, 576] and kv_pages_fp8 uint8 [P, 32, 576] (E4M3 codes)
@@ -455,7 +459,8 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
     [B, topk] (selected pages: mla_decode_sparse / mla_decode_bf16_sparse,
     planned on the compact lengths) restrict the visible keys.  use_items
     (default: when the plan has empty split slots) launches the split kernel
-    over the plan's CTA item list.  Returns (out_bf16, lse, out_f32 or None).
+    over the plan's CTA item list; persistent_ctas > 0 (FP8) runs that list
+    with that many persistent CTAs.  Returns (out_bf16, lse, out_f32 or None).
     """
     import torch
     dev = q_fp8.device
@@ -483,7 +488,7 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
               lens_d, splits_d, chunks_d, plan.max_splits, ks, batch, q_len, num_heads, causal)
     restricted = query_lens is not None or kv_bounds is not None or block_idx is not None
     if use_items is None:
-        use_items = bool(np.any(plan.splits < plan.max_splits))
+        use_items = bool(np.any(plan.splits < plan.max_splits)) or persistent_ctas > 0
     is_bf16 = q_fp8.dtype == torch.bfloat16
     items_d = None
     if use_items:
@@ -514,7 +519,7 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
                 mla_decode_bf16_sparse(*common[:6], bi_d, topk, *common[6:], sm_h, ws, ws_bytes,
                                        out, lse, out_f32, **extra)
     elif (sinks is None and output_scale == 1.0 and not device_scales and not restricted
-          and items_d is None):
+          and items_d is None and persistent_ctas == 0):
         mla_decode(*common, q_scale, kv_scale, softmax_scale, ws, ws_bytes, out, lse, out_f32,
                    stream)
     else:
@@ -531,7 +536,7 @@ def decode(q_fp8, kv_pages_fp8, page_table, kv_lens, *, num_heads: int, q_len: i
                      kv_scale_dev=None if dev_s is None else dev_s[1:2],
                      softmax_scale_dev=None if dev_s is None else dev_s[2:3],
                      output_scale=output_scale, sinks=sk, query_lens=ql_d, kv_bounds=kb_d,
-                     cta_items=items_d, stream=stream)
+                     cta_items=items_d, persistent_ctas=persistent_ctas, stream=stream)
         if bi_d is None:
             mla_decode_ex(*common, *host, ws, ws_bytes, out, lse, out_f32, **extra)
         else:

@@ -96,7 +96,7 @@ struct Cfg {
   // Reductions: tile maxima 16 NR B, row sums 32 NR B (double-buffered by
   // tile parity; 16 NR B, one buffer, with per-thread sums), references 4 NR B.
   static constexpr uint32_t kRedSumBytes = kWide ? 16 * NR : 32 * NR;
-  static constexpr uint32_t kAuxBytes = 176 + 20 * NR + kRedSumBytes + (kWide ? 4 * NR : 0);
+  static constexpr uint32_t kAuxBytes = 192 + 20 * NR + kRedSumBytes + (kWide ? 4 * NR : 0);
   static constexpr uint32_t kQBytes = NR * MLA_HEAD_DIM;
   // Three KV stages fit when P^T can live in the rope block of its own stage
   // (QK has consumed that block before P is written): NR = 16.  Otherwise two
@@ -118,11 +118,11 @@ struct Cfg {
   static constexpr int kBarOdone1 = kPInStage ? BAR_PFREE1 : BAR_FULL0 + 2;
   static_assert(kPInStage || NST == 2, "the third stage's barrier must be free");
   // aux: mbarriers, tmem slot, flags, reductions
-  static constexpr uint32_t kBars = kAux;               // 17 x 8 B
-  static constexpr uint32_t kTmemSlot = kAux + 136;     // 4 B
-  static constexpr uint32_t kFlags = kAux + 144;        // 3 x 4 B
-  static constexpr uint32_t kStageInfo = kAux + 160;    // NST x 4 B: rows loaded per page
-  static constexpr uint32_t kRedMax = kAux + 176;       // 4 x NR floats
+  static constexpr uint32_t kBars = kAux;               // 19 x 8 B
+  static constexpr uint32_t kTmemSlot = kAux + 152;     // 4 B
+  static constexpr uint32_t kFlags = kAux + 160;        // 3 x 4 B
+  static constexpr uint32_t kStageInfo = kAux + 176;    // NST x 4 B: rows loaded per page
+  static constexpr uint32_t kRedMax = kAux + 192;       // 4 x NR floats
   // Row owner r reads red_max[.][r] before writing alpha[r]: alpha reuses
   // red_max's first row.
   static constexpr uint32_t kAlpha = kRedMax;           // NR floats
@@ -181,95 +181,160 @@ __device__ __forceinline__ void zero_unloaded_rows(uint8_t* kvp, int lane, uint3
   }
 }
 
+// One work item of the split kernel: split `split` of request b, row group
+// grp, with the key range, scales and row counts every role derives the
+// same way.
+struct ItemInfo {
+  int b, split, grp, L, nsplit, q_b, tok_end, t0, win_lo, win_hi, row0, rows_here, rows_valid,
+      n_tiles;
+  bool sparse;
+  float c_log2, kv_scale;
+};
+
+// Item (b, split, grp): the plan checks (a bad plan is reported as
+// MLA_ERR_INVALID_ARG and gives false), then the split's token range in the
+// planned space (positions, or the compact range of a page selection), the
+// key window, the first tile (whole tiles below a dense window are skipped;
+// tiles stay aligned to the split start, so pages stay whole), the scales and
+// the row counts.
+template <bool kGather>
+__device__ __forceinline__ bool item_info(const DecodeParams& p, int b, int split, int grp,
+                                          ItemInfo& it) {
+  it.b = b;
+  it.split = split;
+  it.grp = grp;
+  it.L = p.kv_lens[b];
+  it.nsplit = p.splits[b];
+  const int chunk = p.chunks[b];
+  // With selected pages the split plan covers the compact range of the
+  // selection (32 * topk tokens); otherwise the key positions [0, L).
+  it.sparse = kGather && p.block_idx != nullptr;
+  const int Lspace = it.sparse ? p.topk * MLA_PAGE_SIZE : it.L;
+  it.q_b = p.query_lens ? p.query_lens[b] : p.q_len;  // this request's query tokens
+  const bool bad = it.L < 1 || it.q_b < 1 || it.q_b > p.q_len || (p.causal && it.L < it.q_b) ||
+                   it.nsplit > p.max_splits || chunk < kTileTokens ||
+                   (chunk % kTileTokens) != 0 ||
+                   static_cast<int64_t>(it.nsplit) * chunk < Lspace ||
+                   static_cast<int64_t>(it.nsplit - 1) * chunk >= Lspace ||
+                   static_cast<int64_t>(it.L) > static_cast<int64_t>(p.max_pages) * MLA_PAGE_SIZE;
+  if (bad) {
+    if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
+    return false;
+  }
+  const int tok_begin = split * chunk;
+  it.tok_end = min(Lspace, tok_begin + chunk);
+  // Key window in positions ([0, L) without one).
+  it.win_lo = 0;
+  it.win_hi = it.L;
+  if (kGather && p.kv_bounds) {
+    it.win_lo = max(0, p.kv_bounds[2 * b]);
+    it.win_hi = min(it.L, p.kv_bounds[2 * b + 1]);
+  }
+  it.t0 = tok_begin;
+  if (kGather && !it.sparse) {
+    it.tok_end = min(it.tok_end, it.win_hi);
+    if (it.win_lo >= it.tok_end)
+      it.t0 = it.tok_end;  // nothing of the window in this split
+    else if (it.win_lo > tok_begin)
+      it.t0 = tok_begin + (it.win_lo - tok_begin) / kTileTokens * kTileTokens;
+  }
+  it.c_log2 = p.c_log2;
+  it.kv_scale = p.kv_scale;
+  if (p.q_scale_dev || p.kv_scale_dev || p.sm_scale_dev) {
+    const float qs = p.q_scale_dev ? *p.q_scale_dev : p.q_scale_h;
+    it.kv_scale = p.kv_scale_dev ? *p.kv_scale_dev : p.kv_scale;
+    const float ss = p.sm_scale_dev ? *p.sm_scale_dev : p.sm_scale_h;
+    it.c_log2 = ss * qs * it.kv_scale * 1.4426950408889634f;
+  }
+  it.row0 = grp * p.rows_per_group;  // first row of this group
+  it.rows_here = min(p.rows_per_group, p.rows_per_req - it.row0);
+  // Rows of real query tokens (the others are padding slots of a shorter
+  // query block: no key is visible to them).
+  it.rows_valid = max(0, min(it.rows_here, it.q_b * p.num_heads - it.row0));
+  it.n_tiles = (it.rows_valid > 0 && it.tok_end > it.t0)
+                   ? (it.tok_end - it.t0 + kTileTokens - 1) / kTileTokens
+                   : 0;
+  return true;
+}
+
+// Decodes a CTA item-list entry; false (reported) for an item outside the
+// batch or the row groups.
+__device__ __forceinline__ bool decode_item(const DecodeParams& p, int it, int ngroups, int& b,
+                                            int& split, int& grp) {
+  b = it >> MLA_ITEM_B_SHIFT;
+  split = (it >> MLA_ITEM_S_SHIFT) & ((1 << (MLA_ITEM_B_SHIFT - MLA_ITEM_S_SHIFT)) - 1);
+  grp = it & ((1 << MLA_ITEM_S_SHIFT) - 1);
+  if (it < 0 || b >= p.batch || grp >= ngroups) {
+    if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
+    return false;
+  }
+  return true;
+}
+
 // kGather: the variant for restricted key sets (key windows, selected pages):
 // tiles may have pages that are not loaded, and every score is masked by its
 // key position.  The plain variant (kGather = false) covers full key ranges,
-// with or without ragged query counts.
-template <int NR, bool kGather, bool kItems>
+// with or without ragged query counts.  kMode: 0 the (request, split x row
+// group) grid, 1 the CTA item list (one item per CTA), 2 persistent CTAs
+// that each loop over items blockIdx.x, blockIdx.x + gridDim.x, ... of the
+// list, carrying every barrier phase from one item to the next so that the
+// next item's Q and first tiles load while the current one finishes.
+template <int NR, bool kGather, int kMode>
 __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     mla_split_kv_kernel(const __grid_constant__ CUtensorMap tm_kv_lat,
                         const __grid_constant__ CUtensorMap tm_kv_rope,
                         const __grid_constant__ CUtensorMap tm_q_lat,
                         const __grid_constant__ CUtensorMap tm_q_rope, const DecodeParams p) {
   using C = Cfg<NR>;
+  constexpr bool kPersist = kMode == 2;
   // Grid (request, split x row group), dispatched split-major: every
   // request's first splits go out before anyone's later ones, so the empty
   // slots of short requests (split >= splits[b], exiting at once) do not hold
   // back real work in a skewed batch; the row groups of one split are
   // `batch` CTAs apart and run in the same wave, so L2 serves their repeated
-  // reads of the same KV tiles.
+  // reads of the same KV tiles.  The item list holds exactly the CTAs that
+  // have work, in the same order.
   const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
-  int split, grp, b;
-  if constexpr (kItems) {
-    // Item list: exactly the CTAs that have work.
-    const int it = p.cta_items[blockIdx.x];
-    b = it >> MLA_ITEM_B_SHIFT;
-    split = (it >> MLA_ITEM_S_SHIFT) & ((1 << (MLA_ITEM_B_SHIFT - MLA_ITEM_S_SHIFT)) - 1);
-    grp = it & ((1 << MLA_ITEM_S_SHIFT) - 1);
-    if (it < 0 || b >= p.batch || grp >= ngroups) {
-      if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
-      return;
+  ItemInfo first{};
+  if constexpr (!kPersist) {
+    int b, split, grp;
+    if constexpr (kMode == 1) {
+      if (!decode_item(p, p.cta_items[blockIdx.x], ngroups, b, split, grp)) return;
+    } else {
+      split = blockIdx.y / ngroups;
+      grp = blockIdx.y - split * ngroups;
+      b = blockIdx.x;
     }
-  } else {
-    split = blockIdx.y / ngroups;
-    grp = blockIdx.y - split * ngroups;
-    b = blockIdx.x;
+    if (split >= p.splits[b]) return;  // empty split slot of a shorter request
+    if (!item_info<kGather>(p, b, split, grp, first)) return;
   }
-
-  // ---- plan checks (uniform over the CTA) -------------------------------
-  const int L = p.kv_lens[b];
-  const int nsplit = p.splits[b];
-  const int chunk = p.chunks[b];
-  if (split >= nsplit) return;  // empty split slot of a shorter request
-  // With selected pages the split plan covers the compact range of the
-  // selection (32 * topk tokens); otherwise the key positions [0, L).
-  const bool sparse = kGather && p.block_idx != nullptr;
-  const int Lspace = sparse ? p.topk * MLA_PAGE_SIZE : L;
-  const int q_b = p.query_lens ? p.query_lens[b] : p.q_len;  // this request's query tokens
-  {
-    const bool bad = L < 1 || q_b < 1 || q_b > p.q_len || (p.causal && L < q_b) ||
-                     nsplit > p.max_splits || chunk < kTileTokens ||
-                     (chunk % kTileTokens) != 0 ||
-                     static_cast<int64_t>(nsplit) * chunk < Lspace ||
-                     static_cast<int64_t>(nsplit - 1) * chunk >= Lspace ||
-                     static_cast<int64_t>(L) > static_cast<int64_t>(p.max_pages) * MLA_PAGE_SIZE;
-    if (bad) {
-      if (threadIdx.x == 0) report(p.status, MLA_ERR_INVALID_ARG);
-      return;
+  // The n-th item of this CTA: 2 = `it` holds it, 1 = skip it (reported),
+  // 0 = no more.  Every role walks the same sequence.
+  auto next_item = [&](int n, ItemInfo& it) -> int {
+    if constexpr (!kPersist) {
+      if (n > 0) return 0;
+      it = first;
+      return 2;
+    } else {
+      const int64_t idx = blockIdx.x + static_cast<int64_t>(n) * gridDim.x;
+      if (idx >= p.num_items) return 0;
+      int b, split, grp;
+      if (!decode_item(p, p.cta_items[idx], ngroups, b, split, grp)) return 1;
+      if (split >= p.splits[b]) return 1;
+      return item_info<kGather>(p, b, split, grp, it) ? 2 : 1;
     }
-  }
-  const int tok_begin = split * chunk;
-  int tok_end = min(Lspace, tok_begin + chunk);
-  // Key window in positions ([0, L) without one).
-  int win_lo = 0, win_hi = L;
-  if (kGather && p.kv_bounds) {
-    win_lo = max(0, p.kv_bounds[2 * b]);
-    win_hi = min(L, p.kv_bounds[2 * b + 1]);
-  }
-  // First tile of the split: whole tiles below a dense window are skipped
-  // (tiles stay aligned to the split start, so pages stay whole).
-  int t0 = tok_begin;
-  if (kGather && !sparse) {
-    tok_end = min(tok_end, win_hi);
-    if (win_lo >= tok_end)
-      t0 = tok_end;  // nothing of the window in this split
-    else if (win_lo > tok_begin)
-      t0 = tok_begin + (win_lo - tok_begin) / kTileTokens * kTileTokens;
-  }
-  float c_log2 = p.c_log2, kv_scale = p.kv_scale;
-  if (p.q_scale_dev || p.kv_scale_dev || p.sm_scale_dev) {
-    const float qs = p.q_scale_dev ? *p.q_scale_dev : p.q_scale_h;
-    kv_scale = p.kv_scale_dev ? *p.kv_scale_dev : p.kv_scale;
-    const float ss = p.sm_scale_dev ? *p.sm_scale_dev : p.sm_scale_h;
-    c_log2 = ss * qs * kv_scale * 1.4426950408889634f;
-  }
-  const int row0 = grp * p.rows_per_group;                       // first row of this group
-  const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
-  // Rows of real query tokens (the others are padding slots of a shorter
-  // query block: no key is visible to them).
-  const int rows_valid = max(0, min(rows_here, q_b * p.num_heads - row0));
-  const int n_tiles =
-      (rows_valid > 0 && tok_end > t0) ? (tok_end - t0 + kTileTokens - 1) / kTileTokens : 0;
+  };
+  // Binds an item's values to the names the role bodies use.
+#define MLA_ITEM_NAMES(it)                                                                    \
+  const int b = it.b, split = it.split, L = it.L, nsplit = it.nsplit, q_b = it.q_b;          \
+  const int tok_end = it.tok_end, t0 = it.t0, win_lo = it.win_lo, win_hi = it.win_hi;        \
+  const int row0 = it.row0, rows_here = it.rows_here, rows_valid = it.rows_valid;            \
+  const int n_tiles = it.n_tiles;                                                            \
+  const bool sparse = it.sparse;                                                             \
+  const float c_log2 = it.c_log2, kv_scale = it.kv_scale;                                    \
+  (void)b; (void)split; (void)L; (void)nsplit; (void)q_b; (void)tok_end; (void)t0;           \
+  (void)win_lo; (void)win_hi; (void)row0; (void)rows_here; (void)rows_valid; (void)n_tiles;   \
+  (void)sparse; (void)c_log2; (void)kv_scale
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -302,7 +367,12 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     mbar_init(bar(BAR_PFREE1), 1);
     mbar_init(bar(BAR_ODONE), 1);
     mbar_init(bar(C::kBarOdone1), 1);
-    mbar_init(bar(BAR_FINAL), C::kMmaWarps);  // one commit from each MMA warp
+    // Per item: the PV warp's commit after its last PV (every QK result has
+    // been consumed by then); Q free again after the QK warp's last QK; O^T
+    // read by the softmax warpgroups.
+    mbar_init(bar(BAR_FINAL), 1);
+    mbar_init(bar(BAR_QFREE), 1);
+    mbar_init(bar(BAR_OFREE), 128 * C::SWG);
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;
@@ -327,127 +397,153 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       tma_prefetch_desc(&tm_kv_rope);
       tma_prefetch_desc(&tm_q_lat);
       tma_prefetch_desc(&tm_q_rope);
-      const int qrow = b * p.rows_per_req + row0;
-      mbar_arrive_expect_tx(bar(BAR_QFULL), C::kQBytes);
-#pragma unroll
-      for (int d = 0; d < 4; ++d)
-        tma_load_2d(sbase + C::kQ + d * NR * 128, &tm_q_lat, d * 128, qrow, bar(BAR_QFULL));
-      tma_load_2d(sbase + C::kQ + 4 * NR * 128, &tm_q_rope, MLA_LATENT_DIM, qrow, bar(BAR_QFULL));
     }
     const uint64_t pol = l2_policy_evict_first();
-    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-    const int page0 = t0 / MLA_PAGE_SIZE;
-    const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
-    // Page ids of 8 tiles (32 pages) per window, one per lane; the next
-    // window is fetched a window ahead so its latency is hidden.  kGather
-    // also keeps, per page, the number of its rows to load (0: not loaded):
-    // compact page cp maps to logical page lp (cp itself, or the selection's
-    // entry), which is loaded when it holds keys inside the window and before
-    // the end of the split (dense) or of the request (selection).
-    int last_lp = -1;  // selection: the entry before this window (order check)
-    auto load_window = [&](int w, int& nv_out) -> int {
-      const int pi = page0 + w * 32 + lane;
-      int pg = 0;
-      nv_out = 0;
-      if constexpr (!kGather) {
-        if (pi < page_end) {
-          pg = pt[pi];
-          if (pg < 0 || pg >= p.num_pages) {
-            report(p.status, MLA_ERR_INVALID_ARG);
-            pg = 0;
-          }
-        }
-      } else {
-        int lp = -1;
-        if (pi < page_end) {
-          lp = pi;
-          if (sparse) lp = (pi < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + pi] : -1;
-        }
-        if (sparse) {
-          // Selected pages must be listed in increasing order, each once.
-          int prev = __shfl_up_sync(0xffffffffu, lp, 1);
-          if (lane == 0) prev = last_lp;
-          if (lp >= 0 && prev >= 0 && lp <= prev) report(p.status, MLA_ERR_INVALID_ARG);
-          last_lp = __shfl_sync(0xffffffffu, lp, 31);
-        }
-        const int64_t end_pos = sparse ? win_hi : tok_end;
-        const int64_t first = static_cast<int64_t>(lp) * MLA_PAGE_SIZE;
-        if (lp >= 0 && first < end_pos && first + MLA_PAGE_SIZE > win_lo) {
-          pg = pt[lp];
-          if (pg < 0 || pg >= p.num_pages) {
-            report(p.status, MLA_ERR_INVALID_ARG);
-            pg = 0;
-          }
-          nv_out = static_cast<int>(end_pos - first < MLA_PAGE_SIZE ? end_pos - first : MLA_PAGE_SIZE);
-        }
-      }
-      return pg;
-    };
-    int window_nv, window_next_nv;
-    int window = load_window(0, window_nv);
-    int window_next = load_window(1, window_next_nv);
     volatile uint32_t* stage_info = reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo);
-    int issued = 0;
+    int issued = 0;  // tiles issued, all items
     int st = 0, round = 0;
-    for (int i = 0; i < n_tiles; ++i) {
-      if (i > 0 && (i & 7) == 0) {
-        window = window_next;
-        window_nv = window_next_nv;
-        window_next = load_window((i >> 3) + 1, window_next_nv);
-      }
-      bool ok = !expired_here(p, WAIT_STAGE_FREE, i);
-      if (ok && round > 0)
-        ok = mbar_wait_abort(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles, abort_flag);
-      ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-      if (!ok) {
-        if (lane == 0) {
-          report(p.status, MLA_ERR_TIMEOUT);
-          *abort_flag = 1;
+    int nq = 0;      // items whose Q was loaded
+    bool ok = true;
+    for (int n = 0; ok && (kPersist || n == 0); ++n) {
+      ItemInfo item;
+      const int r = next_item(n, item);
+      if (r == 0) break;
+      if (r == 1) continue;
+      MLA_ITEM_NAMES(item);
+      // Q of this item, once the previous item's QKs are done with the buffer.
+      if (nq > 0) {
+        bool q_ok = mbar_wait_abort(bar(BAR_QFREE), (nq - 1) & 1, p.wait_cycles, abort_flag);
+        q_ok = __all_sync(0xffffffffu, q_ok && !*abort_flag);
+        if (!q_ok) {
+          if (lane == 0) {
+            report(p.status, MLA_ERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
         }
-        break;
       }
-      // Lane q (< 4) takes the id of the tile's page q.
-      const int src = (i & 7) * 4 + (lane & 3);
-      const int my_page = __shfl_sync(0xffffffffu, window, src);
-      const int tp0 = page0 + i * 4;
-      bool my_load;
-      uint32_t info = 0;
-      if constexpr (kGather) {
-        // Rows to load of pages 0-3, one byte each, for the QK warp (which
-        // zeroes the rest); published by the arrive below.
-        const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
-        my_load = my_nv > 0;
-        const int n1 = __shfl_sync(0xffffffffu, my_nv, 1);
-        const int n2 = __shfl_sync(0xffffffffu, my_nv, 2);
-        const int n3 = __shfl_sync(0xffffffffu, my_nv, 3);
-        info = static_cast<uint32_t>(my_nv) | (static_cast<uint32_t>(n1) << 8) |
-               (static_cast<uint32_t>(n2) << 16) | (static_cast<uint32_t>(n3) << 24);
-      } else {
-        my_load = tp0 + (lane & 3) < page_end;
-      }
-      const int nload = __popc(__ballot_sync(0xffffffffu, lane < 4 && my_load));
-      const uint32_t fb = bar(BAR_FULL0 + st);
       if (lane == 0) {
-        if constexpr (kGather) stage_info[st] = info;
-        mbar_arrive_expect_tx(fb, nload * kPageBytes);
-      }
-      __syncwarp();
-      // Lanes 0-3 issue one page each (5 boxes: 4 latent blocks + rope).
-      if (lane < 4 && my_load) {
-        const uint32_t kv = sbase + C::kKV + st * kTileBytes;
-        const int row = my_page * MLA_PAGE_SIZE;
+        const int qrow = b * p.rows_per_req + row0;
+        mbar_arrive_expect_tx(bar(BAR_QFULL), C::kQBytes);
 #pragma unroll
         for (int d = 0; d < 4; ++d)
-          tma_load_2d_hint(kv + d * kLatBlockBytes + lane * kPageLatBytes, &tm_kv_lat, d * 128,
-                           row, fb, pol);
-        tma_load_2d_hint(kv + kRopeOffset + lane * kPageRopeBytes, &tm_kv_rope, MLA_LATENT_DIM,
-                         row, fb, pol);
+          tma_load_2d(sbase + C::kQ + d * NR * 128, &tm_q_lat, d * 128, qrow, bar(BAR_QFULL));
+        tma_load_2d(sbase + C::kQ + 4 * NR * 128, &tm_q_rope, MLA_LATENT_DIM, qrow,
+                    bar(BAR_QFULL));
       }
-      __syncwarp();
-      issued = i + 1;
-      if (++st == C::NST) {
-        st = 0;
-        ++round;
+      ++nq;
+      const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+      const int page0 = t0 / MLA_PAGE_SIZE;
+      const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
+      // Page ids of 8 tiles (32 pages) per window, one per lane; the next
+      // window is fetched a window ahead so its latency is hidden.  kGather
+      // also keeps, per page, the number of its rows to load (0: not loaded):
+      // compact page cp maps to logical page lp (cp itself, or the selection's
+      // entry), which is loaded when it holds keys inside the window and before
+      // the end of the split (dense) or of the request (selection).
+      int last_lp = -1;  // selection: the entry before this window (order check)
+      auto load_window = [&](int w, int& nv_out) -> int {
+        const int pi = page0 + w * 32 + lane;
+        int pg = 0;
+        nv_out = 0;
+        if constexpr (!kGather) {
+          if (pi < page_end) {
+            pg = pt[pi];
+            if (pg < 0 || pg >= p.num_pages) {
+              report(p.status, MLA_ERR_INVALID_ARG);
+              pg = 0;
+            }
+          }
+        } else {
+          int lp = -1;
+          if (pi < page_end) {
+            lp = pi;
+            if (sparse) lp = (pi < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + pi] : -1;
+          }
+          if (sparse) {
+            // Selected pages must be listed in increasing order, each once.
+            int prev = __shfl_up_sync(0xffffffffu, lp, 1);
+            if (lane == 0) prev = last_lp;
+            if (lp >= 0 && prev >= 0 && lp <= prev) report(p.status, MLA_ERR_INVALID_ARG);
+            last_lp = __shfl_sync(0xffffffffu, lp, 31);
+          }
+          const int64_t end_pos = sparse ? win_hi : tok_end;
+          const int64_t first = static_cast<int64_t>(lp) * MLA_PAGE_SIZE;
+          if (lp >= 0 && first < end_pos && first + MLA_PAGE_SIZE > win_lo) {
+            pg = pt[lp];
+            if (pg < 0 || pg >= p.num_pages) {
+              report(p.status, MLA_ERR_INVALID_ARG);
+              pg = 0;
+            }
+            nv_out = static_cast<int>(end_pos - first < MLA_PAGE_SIZE ? end_pos - first : MLA_PAGE_SIZE);
+          }
+        }
+        return pg;
+      };
+      int window_nv, window_next_nv;
+      int window = load_window(0, window_nv);
+      int window_next = load_window(1, window_next_nv);
+      for (int i = 0; i < n_tiles; ++i) {
+        if (i > 0 && (i & 7) == 0) {
+          window = window_next;
+          window_nv = window_next_nv;
+          window_next = load_window((i >> 3) + 1, window_next_nv);
+        }
+        ok = !expired_here(p, WAIT_STAGE_FREE, i);
+        if (ok && round > 0)
+          ok = mbar_wait_abort(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles, abort_flag);
+        ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+        if (!ok) {
+          if (lane == 0) {
+            report(p.status, MLA_ERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          break;
+        }
+        // Lane q (< 4) takes the id of the tile's page q.
+        const int src = (i & 7) * 4 + (lane & 3);
+        const int my_page = __shfl_sync(0xffffffffu, window, src);
+        const int tp0 = page0 + i * 4;
+        bool my_load;
+        uint32_t info = 0;
+        if constexpr (kGather) {
+          // Rows to load of pages 0-3, one byte each, for the QK warp (which
+          // zeroes the rest); published by the arrive below.
+          const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
+          my_load = my_nv > 0;
+          const int n1 = __shfl_sync(0xffffffffu, my_nv, 1);
+          const int n2 = __shfl_sync(0xffffffffu, my_nv, 2);
+          const int n3 = __shfl_sync(0xffffffffu, my_nv, 3);
+          info = static_cast<uint32_t>(my_nv) | (static_cast<uint32_t>(n1) << 8) |
+                 (static_cast<uint32_t>(n2) << 16) | (static_cast<uint32_t>(n3) << 24);
+        } else {
+          my_load = tp0 + (lane & 3) < page_end;
+        }
+        const int nload = __popc(__ballot_sync(0xffffffffu, lane < 4 && my_load));
+        const uint32_t fb = bar(BAR_FULL0 + st);
+        if (lane == 0) {
+          if constexpr (kGather) stage_info[st] = info;
+          mbar_arrive_expect_tx(fb, nload * kPageBytes);
+        }
+        __syncwarp();
+        // Lanes 0-3 issue one page each (5 boxes: 4 latent blocks + rope).
+        if (lane < 4 && my_load) {
+          const uint32_t kv = sbase + C::kKV + st * kTileBytes;
+          const int row = my_page * MLA_PAGE_SIZE;
+#pragma unroll
+          for (int d = 0; d < 4; ++d)
+            tma_load_2d_hint(kv + d * kLatBlockBytes + lane * kPageLatBytes, &tm_kv_lat, d * 128,
+                             row, fb, pol);
+          tma_load_2d_hint(kv + kRopeOffset + lane * kPageRopeBytes, &tm_kv_rope, MLA_LATENT_DIM,
+                           row, fb, pol);
+        }
+        __syncwarp();
+        ++issued;
+        if (++st == C::NST) {
+          st = 0;
+          ++round;
+        }
       }
     }
     // Before the CTA can exit, the copies this warp issued must have landed
@@ -456,7 +552,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     if (lane == 0) {
       for (int k = max(0, issued - C::NST); k < issued; ++k)
         mbar_wait(bar(BAR_FULL0 + k % C::NST), (k / C::NST) & 1, kWaitLimitCycles);
-      mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
+      if (nq > 0) mbar_wait(bar(BAR_QFULL), (nq - 1) & 1, kWaitLimitCycles);
     }
     __syncwarp();
   } else if (warp == 1 || warp == 2) {
@@ -466,15 +562,16 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     // at these N (measured with a probe of the issue rate).
     constexpr uint32_t kIdQK = idesc_e4m3(128, NR, 0, 0);
     constexpr uint32_t kIdPV = idesc_e4m3(128, C::OW, 1, 1);
-    bool ok = (warp == 1) ? mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles) : true;
+    bool ok = true;
     auto fail = [&]() {
       if (lane == 0) {
         report(p.status, MLA_ERR_TIMEOUT);
         *abort_flag = 1;
       }
     };
-    // PV of tile j (KV in stage jst, P^T in buffer pb); lane 0 issues.
-    auto issue_pv = [&](int j, int jst, int pb) {
+    // PV of tile j of an item (tile g of the CTA, KV in stage jst, P^T in
+    // buffer pb); lane 0 issues.
+    auto issue_pv = [&](int j, int g, int jst, int pb) {
       tc_fence_after();
       const uint32_t kv = sbase + C::kKV + jst * kTileBytes;
       const uint32_t pbuf = C::kPInStage ? kv + kRopeOffset : sbase + C::kP + pb * C::kPBytes;
@@ -498,7 +595,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       }
       umma_commit(bar(BAR_EMPTY0 + jst));
       if (!C::kPInStage) umma_commit(bar(BAR_PFREE0 + pb));
-      umma_commit(bar((j & 1) ? C::kBarOdone1 : BAR_ODONE));
+      umma_commit(bar((g & 1) ? C::kBarOdone1 : BAR_ODONE));
     };
     // QK of tile i (KV in stage ist) into S buffer sb; lane 0 issues.
     auto issue_qk = [&](int ist, int sb) {
@@ -520,68 +617,102 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       }
       umma_commit(bar(BAR_SFULL0 + sb));
     };
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) fail();
     if (warp == 1) {
       // QK(j) once its tile has landed, its S^T buffer is free and PV(j - 2)
       // has completed (so the softmax's wait for PV(j - 1) stays within one
-      // phase of its barrier; QK(j) still overlaps PV(j - 1)).
-      int st = 0, round = 0;
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int sb = (C::NS == 2) ? (j & 1) : 0;
-        const int use = (C::NS == 2) ? (j >> 1) : j;
-        bool w = !expired_here(p, WAIT_TILE_FULL, j) &&
-                 mbar_wait_abort(bar(BAR_FULL0 + st), round & 1, p.wait_cycles, abort_flag);
-        if (w && use >= 1)
-          w = mbar_wait_abort(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles, abort_flag);
-        // The 96-row CTA needs no PV(j - 2) wait: its softmax waited for PV(i - 2)
-        // (the P^T buffer) before writing P(i - 1), which keeps its wait for
-        // PV(i - 1) within one phase; the tile's stage implies PV(j - 2) anyway.
-        if (w && j >= 2 && !C::kWide)
-          w = mbar_wait_abort(bar(((j - 2) & 1) ? C::kBarOdone1 : BAR_ODONE), ((j - 2) >> 1) & 1,
-                              p.wait_cycles, abort_flag);
-        w = __all_sync(0xffffffffu, w && !*abort_flag);
-        if (!w) {
-          ok = false;
-          break;
+      // phase of its barrier; QK(j) still overlaps PV(j - 1)).  Tile indices
+      // for buffers and phases count across the CTA's items (g).
+      int st = 0, round = 0, g = 0;
+      int nq = 0;  // items started
+      for (int n = 0; ok && (kPersist || n == 0); ++n) {
+        ItemInfo item;
+        const int r = next_item(n, item);
+        if (r == 0) break;
+        if (r == 1) continue;
+        MLA_ITEM_NAMES(item);
+        ++nq;
+        bool w = mbar_wait_abort(bar(BAR_QFULL), (nq - 1) & 1, p.wait_cycles, abort_flag);
+        ok = __all_sync(0xffffffffu, w && !*abort_flag);
+        for (int j = 0; ok && j < n_tiles; ++j, ++g) {
+          const int sb = (C::NS == 2) ? (g & 1) : 0;
+          const int use = (C::NS == 2) ? (g >> 1) : g;
+          w = !expired_here(p, WAIT_TILE_FULL, j) &&
+              mbar_wait_abort(bar(BAR_FULL0 + st), round & 1, p.wait_cycles, abort_flag);
+          if (w && use >= 1)
+            w = mbar_wait_abort(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles, abort_flag);
+          // The 96-row CTA needs no PV(g - 2) wait: its softmax waited for
+          // PV(g - 2) (the P^T buffer) before writing P(g - 1), which keeps its
+          // wait for PV(g - 1) within one phase; the tile's stage implies
+          // PV(g - 2) anyway.
+          if (w && g >= 2 && !C::kWide)
+            w = mbar_wait_abort(bar(((g - 2) & 1) ? C::kBarOdone1 : BAR_ODONE),
+                                ((g - 2) >> 1) & 1, p.wait_cycles, abort_flag);
+          w = __all_sync(0xffffffffu, w && !*abort_flag);
+          if (!w) {
+            ok = false;
+            break;
+          }
+          // Rows loaded per page, as the producer published them with the
+          // stage's full barrier (observed above).
+          const uint32_t info =
+              kGather ? *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st) : 0u;
+          zero_unloaded_rows<kGather>(base + C::kKV + st * kTileBytes, lane, info,
+                                      tok_end - (t0 + j * kTileTokens));
+          if (lane == 0) issue_qk(st, sb);
+          __syncwarp();
+          if (++st == C::NST) {
+            st = 0;
+            ++round;
+          }
         }
-        // Rows loaded per page, as the producer published them with the
-        // stage's full barrier (observed above).
-        const uint32_t info =
-            kGather ? *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st) : 0u;
-        zero_unloaded_rows<kGather>(base + C::kKV + st * kTileBytes, lane, info,
-                                    tok_end - (t0 + j * kTileTokens));
-        if (lane == 0) issue_qk(st, sb);
+        // Q is free for the next item once these QKs complete (also on the
+        // way out: the drain below waits for it).
+        if (lane == 0) umma_commit(bar(BAR_QFREE));
         __syncwarp();
-        if (++st == C::NST) {
-          st = 0;
-          ++round;
-        }
       }
+      if (!ok) fail();
+      // This warp's MMAs complete before the CTA releases TMEM.
+      if (nq > 0) mbar_wait(bar(BAR_QFREE), (nq - 1) & 1, kWaitLimitCycles);
     } else {
-      // PV(i) as soon as its P^T is ready.
-      int st = 0;
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int pb = (C::NPB == 1) ? 0 : (i & 1);
-        const int use = (C::NPB == 1) ? i : (i >> 1);
-        bool w = !expired_here(p, WAIT_P_FULL, i) &&
-                 mbar_wait_abort(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles, abort_flag);
-        w = __all_sync(0xffffffffu, w && !*abort_flag);
-        if (!w) {
-          ok = false;
-          break;
+      // PV(i) as soon as its P^T is ready; the first PV of an item overwrites
+      // O^T, so it waits until the softmax has read the previous item's.
+      int st = 0, g = 0;
+      int nq = 0;  // items started
+      for (int n = 0; ok && (kPersist || n == 0); ++n) {
+        ItemInfo item;
+        const int r = next_item(n, item);
+        if (r == 0) break;
+        if (r == 1) continue;
+        MLA_ITEM_NAMES(item);
+        ++nq;
+        if (nq > 1) {
+          const bool w =
+              mbar_wait_abort(bar(BAR_OFREE), (nq - 2) & 1, p.wait_cycles, abort_flag);
+          ok = __all_sync(0xffffffffu, w && !*abort_flag);
         }
-        if (lane == 0) issue_pv(i, st, pb);
+        for (int i = 0; ok && i < n_tiles; ++i, ++g) {
+          const int pb = (C::NPB == 1) ? 0 : (g & 1);
+          const int use = (C::NPB == 1) ? g : (g >> 1);
+          bool w = !expired_here(p, WAIT_P_FULL, i) &&
+                   mbar_wait_abort(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles, abort_flag);
+          w = __all_sync(0xffffffffu, w && !*abort_flag);
+          if (!w) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) issue_pv(i, g, st, pb);
+          __syncwarp();
+          if (++st == C::NST) st = 0;
+        }
+        // One commit after the item's last PV: the epilogue reads O^T after
+        // it (every QK result has been consumed by then).
+        if (lane == 0) umma_commit(bar(BAR_FINAL));
         __syncwarp();
-        if (++st == C::NST) st = 0;
       }
+      if (!ok) fail();
+      // This warp's MMAs complete before the CTA releases TMEM.
+      if (nq > 0) mbar_wait(bar(BAR_FINAL), (nq - 1) & 1, kWaitLimitCycles);
     }
-    if (!ok) fail();
-    // One commit after everything this warp issued: the epilogue reads O^T
-    // after it, and TMEM is released only after it.
-    if (lane == 0) umma_commit(bar(BAR_FINAL));
-    __syncwarp();
-    mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
   } else {
     // ===== softmax warpgroups (warps kSoftmaxWarp0 .. kSoftmaxWarp0 + 4*SWG - 1) =====
     // SWG warpgroups share each tile: warpgroup g owns rows [g*NRH, (g+1)*NRH)
@@ -597,325 +728,189 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     const int tok_lane = quad * 32 + lane;  // TMEM lane == token index within the tile
     const int sid = threadIdx.x - 32 * C::kSoftmaxWarp0;  // 0..NT-1, owner of row `sid` when < NR
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    float k_row = -INFINITY;  // owner state: reference (integer, log2 units)
-    float l_row = 0.0f;       // owner state: sum of weights relative to k_row - 8
-    // This thread's copy of its rows' references; the 96-row configuration
-    // reads its rows' thresholds and exponent offsets from shared memory
-    // instead (owners write them only between B1 and B2, when every thread
-    // has passed the tile's vote and none has reached its weights), which
-    // keeps the 48-row thread within its registers.
-    float kreg[C::kWide ? 1 : NRH];
-#pragma unroll
-    for (int k = 0; k < (C::kWide ? 1 : NRH); ++k) kreg[k] = -INFINITY;
-    // 96 rows: this thread's sums of its token's weights per row, relative to
-    // the row's current reference (reduced once, after the last tile).
-    float lsum[C::kWide ? NRH : 1];
-#pragma unroll
-    for (int k = 0; k < (C::kWide ? NRH : 1); ++k) lsum[k] = 0.0f;
-    const float c = c_log2;
-    // Smallest visibility limit over this group's rows (MTP verify: the first
-    // query token of the block sees the fewest keys).
-    const int qi_first = row0 / p.num_heads;
-    const int lim_min = p.causal ? min(tok_end, L - q_b + qi_first + 1) : tok_end;
-    const int my_row0 = row0 + rbase;  // first request row of this warpgroup
-    const int my_rows = max(0, min(NRH, rows_valid - rbase));
-    // Selection: logical page ids of 8 tiles' compact pages, one per lane
-    // (this warp's token page is page `quad` of its tile).
-    auto sel_window = [&](int w) -> int {
-      const int cp = t0 / MLA_PAGE_SIZE + w * 32 + lane;
-      return (cp < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + cp] : -1;
-    };
-    int sel_cur = -1, sel_next = -1;
-    if (sparse) {
-      sel_cur = sel_window(0);
-      sel_next = sel_window(1);
-    }
+    int g = 0;   // tiles of the CTA's earlier items (S^T / P^T buffer phases)
+    int nq = 0;  // items started
     bool ok = true;
-    // Scale the scores of tile i by c and mask them (-inf): rows past the real
-    // query rows, tokens past the split, and (MTP verify) tokens after the
-    // row's query position; with restricted key sets the key position decides.
-    auto scale_mask = [&](float (&t)[NRH], int i) {
-      const int tile_tok0 = t0 + i * kTileTokens;
-      const int j = tile_tok0 + tok_lane;
-      if constexpr (kGather) {
-        // Restricted key sets: the token's key position decides.
-        int64_t pos = j;
-        bool tok_ok = j < tok_end;
-        if (sparse) {
-          if (i > 0 && (i & 7) == 0) {
-            sel_cur = sel_next;
-            sel_next = sel_window((i >> 3) + 1);
-          }
-          const int lp = __shfl_sync(0xffffffffu, sel_cur, (i & 7) * 4 + quad);
-          pos = static_cast<int64_t>(lp) * MLA_PAGE_SIZE + lane;
-          tok_ok = tok_ok && lp >= 0;
-        }
-        tok_ok = tok_ok && pos >= win_lo && pos < win_hi;
-        int qi = my_row0 / p.num_heads;
-        int h = my_row0 - qi * p.num_heads;
+    for (int n = 0; kPersist || n == 0; ++n) {
+      ItemInfo item;
+      const int r = next_item(n, item);
+      if (r == 0) break;
+      if (r == 1) continue;
+      MLA_ITEM_NAMES(item);
+      ++nq;
+      float k_row = -INFINITY;  // owner state: reference (integer, log2 units)
+      float l_row = 0.0f;       // owner state: sum of weights relative to k_row - 8
+      // This thread's copy of its rows' references; the 96-row configuration
+      // reads its rows' thresholds and exponent offsets from shared memory
+      // instead (owners write them only between B1 and B2, when every thread
+      // has passed the tile's vote and none has reached its weights), which
+      // keeps the 48-row thread within its registers.
+      float kreg[C::kWide ? 1 : NRH];
 #pragma unroll
-        for (int k = 0; k < NRH; ++k) {
-          const bool vis = tok_ok && k < my_rows && (!p.causal || pos < L - q_b + qi + 1);
-          t[k] = vis ? t[k] * c : -INFINITY;
-          if (++h == p.num_heads) {
-            h = 0;
-            ++qi;
-          }
-        }
-      } else if (tile_tok0 + kTileTokens <= lim_min) {
+      for (int k = 0; k < (C::kWide ? 1 : NRH); ++k) kreg[k] = -INFINITY;
+      // 96 rows: this thread's sums of its token's weights per row, relative to
+      // the row's current reference (reduced once, after the last tile).
+      float lsum[C::kWide ? NRH : 1];
 #pragma unroll
-        for (int k = 0; k < NRH; ++k) t[k] = (k < my_rows) ? t[k] * c : -INFINITY;
-      } else {
-        int qi = my_row0 / p.num_heads;
-        int h = my_row0 - qi * p.num_heads;
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) {
-          const int lim = p.causal ? min(tok_end, L - q_b + qi + 1) : tok_end;
-          t[k] = (k < my_rows && j < lim) ? t[k] * c : -INFINITY;
-          if (++h == p.num_heads) {
-            h = 0;
-            ++qi;
-          }
-        }
+      for (int k = 0; k < (C::kWide ? NRH : 1); ++k) lsum[k] = 0.0f;
+      const float c = c_log2;
+      // Smallest visibility limit over this group's rows (MTP verify: the first
+      // query token of the block sees the fewest keys).
+      const int qi_first = row0 / p.num_heads;
+      const int lim_min = p.causal ? min(tok_end, L - q_b + qi_first + 1) : tok_end;
+      const int my_row0 = row0 + rbase;  // first request row of this warpgroup
+      const int my_rows = max(0, min(NRH, rows_valid - rbase));
+      // Selection: logical page ids of 8 tiles' compact pages, one per lane
+      // (this warp's token page is page `quad` of its tile).
+      auto sel_window = [&](int w) -> int {
+        const int cp = t0 / MLA_PAGE_SIZE + w * 32 + lane;
+        return (cp < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + cp] : -1;
+      };
+      int sel_cur = -1, sel_next = -1;
+      if (sparse) {
+        sel_cur = sel_window(0);
+        sel_next = sel_window(1);
       }
-    };
-    if constexpr (C::kWide) {
-      // 96 rows: each thread holds 48 rows of one token.  Per tile: load S^T
-      // and free it, scale and mask, vote on the rows' thresholds (k + 0.75,
-      // from shared memory), then weights from the rows' integer exponent
-      // offsets (softmax_weight_kc), the row sums of this thread, and P^T as
-      // hi and lo E4M3 terms through packed halves.
-      float* thr = kref;                                  // k + 0.75 per row
-      int* kci = reinterpret_cast<int*>(base + C::kKci);  // exponent offset per row
-      for (int i = 0; i < n_tiles; ++i) {
-        if (ok)
-          ok = !expired_here(p, WAIT_S_FULL, i) &&
-               mbar_wait_abort(bar(BAR_SFULL0), i & 1, p.wait_cycles, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
-        float t[NRH];
-        if (ok) {
-          tc_fence_after();
-          uint32_t r[NRH];
-#pragma unroll
-          for (int cc = 0; cc < NRH / 16; ++cc)
-            tmem_ld16(tmem + lane_addr + rbase + cc * 16,
-                      *reinterpret_cast<uint32_t(*)[16]>(&r[cc * 16]));
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
-          tc_fence_before();
-          mbar_arrive(bar(BAR_SFREE0));
-        } else {
-#pragma unroll
-          for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
-        }
-        if (!kGather && my_rows == NRH && t0 + i * kTileTokens + kTileTokens <= lim_min) {
-#pragma unroll
-          for (int k = 0; k < NRH; ++k) t[k] *= c;
-        } else {
-          scale_mask(t, i);
-        }
-        // Vote: does some score exceed its row's threshold?
-        bool over = false;
-#pragma unroll
-        for (int k4 = 0; k4 < NRH / 4; ++k4) {
-          const float4 th = *reinterpret_cast<const float4*>(thr + rbase + 4 * k4);
-          over |= (t[4 * k4] > th.x) | (t[4 * k4 + 1] > th.y) | (t[4 * k4 + 2] > th.z) |
-                  (t[4 * k4 + 3] > th.w);
-        }
-        const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
-        if (any_over) {
-          {
-            float tm[NRH];
-#pragma unroll
-            for (int k = 0; k < NRH; ++k) tm[k] = t[k];
-            warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
-          }
-          if (sid == 0) flags[0] = 0;
-          named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
-          if (sid < NR) {
-            const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
-                                   fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
-            float k_new = k_row;
-            if (mt > k_row + 0.75f) k_new = ceilf(mt);
-            float alpha = 1.0f;
-            if (k_new != k_row && k_row != -INFINITY) {
-              const int e = static_cast<int>(k_row - k_new);
-              alpha = (e < -126) ? 0.0f : pow2i(e);
-              flags[0] = 1;
+      // Scale the scores of tile i by c and mask them (-inf): rows past the real
+      // query rows, tokens past the split, and (MTP verify) tokens after the
+      // row's query position; with restricted key sets the key position decides.
+      auto scale_mask = [&](float (&t)[NRH], int i) {
+        const int tile_tok0 = t0 + i * kTileTokens;
+        const int j = tile_tok0 + tok_lane;
+        if constexpr (kGather) {
+          // Restricted key sets: the token's key position decides.
+          int64_t pos = j;
+          bool tok_ok = j < tok_end;
+          if (sparse) {
+            if (i > 0 && (i & 7) == 0) {
+              sel_cur = sel_next;
+              sel_next = sel_window((i >> 3) + 1);
             }
-            k_row = k_new;
-            thr[sid] = k_new + 0.75f;
-            kci[sid] = (k_new == -INFINITY) ? kKcNone
-                                            : 135 - 0x4B400000 - static_cast<int>(k_new);
-            alpha_s[sid] = alpha;
+            const int lp = __shfl_sync(0xffffffffu, sel_cur, (i & 7) * 4 + quad);
+            pos = static_cast<int64_t>(lp) * MLA_PAGE_SIZE + lane;
+            tok_ok = tok_ok && lp >= 0;
           }
-          named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
-          // This thread's sums follow their rows' references.
+          tok_ok = tok_ok && pos >= win_lo && pos < win_hi;
+          int qi = my_row0 / p.num_heads;
+          int h = my_row0 - qi * p.num_heads;
 #pragma unroll
-          for (int k = 0; k < NRH; ++k) lsum[k] *= alpha_s[rbase + k];
-          const bool corr = flags[0] != 0;
-          if (ok && corr && i > 0) {
-            // Rescale the O^T columns of rows whose reference moved (rare),
-            // once PV(i - 1) is done (its completion barrier is within one
-            // phase of the awaited one, as in the other configurations).
-            ok = mbar_wait_abort(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE),
-                                 ((i - 1) >> 1) & 1, p.wait_cycles, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
-              tc_fence_after();
-#pragma unroll 1
-              for (int d = 0; d < 4; ++d) {
+          for (int k = 0; k < NRH; ++k) {
+            const bool vis = tok_ok && k < my_rows && (!p.causal || pos < L - q_b + qi + 1);
+            t[k] = vis ? t[k] * c : -INFINITY;
+            if (++h == p.num_heads) {
+              h = 0;
+              ++qi;
+            }
+          }
+        } else if (tile_tok0 + kTileTokens <= lim_min) {
 #pragma unroll
-                for (int cc = 0; cc < NRH / 8; ++cc) {
-                  uint32_t r[8];
-                  const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + rbase + cc * 8;
-                  tmem_ld8(addr, r);
-                  tmem_ld_wait();
+          for (int k = 0; k < NRH; ++k) t[k] = (k < my_rows) ? t[k] * c : -INFINITY;
+        } else {
+          int qi = my_row0 / p.num_heads;
+          int h = my_row0 - qi * p.num_heads;
 #pragma unroll
-                  for (int k = 0; k < 8; ++k)
-                    r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[rbase + cc * 8 + k]);
-                  tmem_st8(addr, r);
-                }
+          for (int k = 0; k < NRH; ++k) {
+            const int lim = p.causal ? min(tok_end, L - q_b + qi + 1) : tok_end;
+            t[k] = (k < my_rows && j < lim) ? t[k] * c : -INFINITY;
+            if (++h == p.num_heads) {
+              h = 0;
+              ++qi;
+            }
+          }
+        }
+      };
+      if constexpr (C::kWide) {
+        // 96 rows: each thread holds 48 rows of one token.  Per tile: load S^T
+        // and free it, scale and mask, vote on the rows' thresholds (k + 0.75,
+        // from shared memory), then weights from the rows' integer exponent
+        // offsets (softmax_weight_kc), the row sums of this thread, and P^T as
+        // hi and lo E4M3 terms through packed halves.
+        float* thr = kref;                                  // k + 0.75 per row
+        int* kci = reinterpret_cast<int*>(base + C::kKci);  // exponent offset per row
+        for (int i = 0; i < n_tiles; ++i) {
+          if (ok)
+            ok = !expired_here(p, WAIT_S_FULL, i) &&
+                 mbar_wait_abort(bar(BAR_SFULL0), (g + i) & 1, p.wait_cycles, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
+          float t[NRH];
+          if (ok) {
+            tc_fence_after();
+            uint32_t r[NRH];
+#pragma unroll
+            for (int cc = 0; cc < NRH / 16; ++cc)
+              tmem_ld16(tmem + lane_addr + rbase + cc * 16,
+                        *reinterpret_cast<uint32_t(*)[16]>(&r[cc * 16]));
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
+            tc_fence_before();
+            mbar_arrive(bar(BAR_SFREE0));
+          } else {
+#pragma unroll
+            for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
+          }
+          if (!kGather && my_rows == NRH && t0 + i * kTileTokens + kTileTokens <= lim_min) {
+#pragma unroll
+            for (int k = 0; k < NRH; ++k) t[k] *= c;
+          } else {
+            scale_mask(t, i);
+          }
+          // Vote: does some score exceed its row's threshold?
+          bool over = false;
+#pragma unroll
+          for (int k4 = 0; k4 < NRH / 4; ++k4) {
+            const float4 th = *reinterpret_cast<const float4*>(thr + rbase + 4 * k4);
+            over |= (t[4 * k4] > th.x) | (t[4 * k4 + 1] > th.y) | (t[4 * k4 + 2] > th.z) |
+                    (t[4 * k4 + 3] > th.w);
+          }
+          const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
+          if (any_over) {
+            {
+              float tm[NRH];
+#pragma unroll
+              for (int k = 0; k < NRH; ++k) tm[k] = t[k];
+              warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
+            }
+            if (sid == 0) flags[0] = 0;
+            named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
+            if (sid < NR) {
+              const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
+                                     fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
+              float k_new = k_row;
+              if (mt > k_row + 0.75f) k_new = ceilf(mt);
+              float alpha = 1.0f;
+              if (k_new != k_row && k_row != -INFINITY) {
+                const int e = static_cast<int>(k_row - k_new);
+                alpha = (e < -126) ? 0.0f : pow2i(e);
+                flags[0] = 1;
               }
-              tmem_st_wait();
+              k_row = k_new;
+              thr[sid] = k_new + 0.75f;
+              kci[sid] = (k_new == -INFINITY) ? kKcNone
+                                              : 135 - 0x4B400000 - static_cast<int>(k_new);
+              alpha_s[sid] = alpha;
             }
-          }
-        }
-        // Weights 2^(t - k + 8) and this thread's row sums.
+            named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
+            // This thread's sums follow their rows' references.
 #pragma unroll
-        for (int k4 = 0; k4 < NRH / 4; ++k4) {
-          const int4 kc = *reinterpret_cast<const int4*>(kci + rbase + 4 * k4);
-          t[4 * k4] = softmax_weight_kc(t[4 * k4], kc.x);
-          t[4 * k4 + 1] = softmax_weight_kc(t[4 * k4 + 1], kc.y);
-          t[4 * k4 + 2] = softmax_weight_kc(t[4 * k4 + 2], kc.z);
-          t[4 * k4 + 3] = softmax_weight_kc(t[4 * k4 + 3], kc.w);
-        }
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) lsum[k] += t[k];
-        // P^T (one buffer): wait until PV(i - 1) has read it.
-        if (ok && expired_here(p, WAIT_P_FREE, i)) ok = false;
-        if (ok && i >= 1)
-          ok = mbar_wait_abort(bar(BAR_PFREE0), (i - 1) & 1, p.wait_cycles, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok && lane == 0) *abort_flag = 1;
-        if (ok) {
-          // MN-major [term][NR/16 row groups][128 tokens][16 rows]: one
-          // 16-byte store per term and 16-row group.
-          uint8_t* pbuf = base + C::kP;
-#pragma unroll
-          for (int g = 0; g < NRH / 16; ++g) {
-            uint32_t h[8], l[8];
-#pragma unroll
-            for (int m = 0; m < 8; ++m)
-              split_e4m3x2_h(t[g * 16 + 2 * m], t[g * 16 + 2 * m + 1], h[m], l[m]);
-            const uint4 vh = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
-                                        h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-            const uint4 vl = make_uint4(l[0] | (l[1] << 16), l[2] | (l[3] << 16),
-                                        l[4] | (l[5] << 16), l[6] | (l[7] << 16));
-            const uint32_t off = ((rbase >> 4) + g) * 2048 + tok_lane * 16;
-            *reinterpret_cast<uint4*>(pbuf + off) = vh;
-            *reinterpret_cast<uint4*>(pbuf + C::kPHalf + off) = vl;
-          }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(bar(BAR_PFULL0));
-        }
-      }
-    } else {
-      for (int i = 0; i < n_tiles; ++i) {
-        const int sb = (C::NS == 2) ? (i & 1) : 0;
-        const int use = (C::NS == 2) ? (i >> 1) : i;
-        if (ok)
-          ok = !expired_here(p, WAIT_S_FULL, i) &&
-               mbar_wait_abort(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
-        float t[NRH];
-        if (ok) {
-          tc_fence_after();
-          uint32_t r[NRH];
-#pragma unroll
-          for (int cc = 0; cc < NRH / 8; ++cc)
-            tmem_ld8(tmem + lane_addr + sb * NR + rbase + cc * 8,
-                     *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
-          tc_fence_before();
-          mbar_arrive(bar(BAR_SFREE0 + sb));
-        } else {
-#pragma unroll
-          for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
-        }
-        scale_mask(t, i);
-        // Reference check.  A row's reference k only has to bound its scores:
-        // with p = 2^(t - k + 8), E4M3 holds p up to 448 = 2^8.8, so any k with
-        // t <= k + 0.75 works.  One vote finds whether some score of the tile
-        // exceeds its row's reference; only then (always on the first tile)
-        // are the tile maxima reduced and references raised to ceil(max).
-        bool over = false;
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) over |= t[k] > kreg[k] + 0.75f;
-        const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
-        // Owners fold the previous tile's row sums (relative to its reference).
-        if (sid < NR && i > 0) {
-          const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
-          l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
-        }
-        if (any_over) {
-          {
-            float tm[NRH];
-#pragma unroll
-            for (int k = 0; k < NRH; ++k) tm[k] = t[k];
-            warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
-          }
-          // The correction flag: cleared before B1 (every read of its last
-          // value happened before this tile's vote), set by owners after B1,
-          // read by all after B2.
-          if (sid == 0) flags[0] = 0;
-          named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
-          if (sid < NR) {
-            const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
-                                   fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
-            float k_new = k_row;
-            if (mt > k_row + 0.75f) k_new = ceilf(mt);
-            float alpha = 1.0f;
-            if (k_new != k_row && k_row != -INFINITY) {
-              const int e = static_cast<int>(k_row - k_new);
-              alpha = (e < -126) ? 0.0f : pow2i(e);
-              flags[0] = 1;
-            }
-            l_row *= alpha;
-            k_row = k_new;
-            kref[sid] = k_new;
-            alpha_s[sid] = alpha;
-          }
-          named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
-#pragma unroll
-          for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
-          const bool corr = flags[0] != 0;
-          if (ok && corr && i > 0) {
-            // Rescale the O^T columns (hi and lo) of rows whose reference moved
-            // (rare), once PV(i-1) is done.  PV completions alternate between
-            // two barriers, and the one of PV(i-1)'s parity is within one phase
-            // of the awaited one: s_full(i) implies PV(i-2) completed (QK(i)
-            // waits for it) and PV(i+1) needs a later tile's P^T.
-            ok = mbar_wait_abort(bar(((i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE),
-                                 ((i - 1) >> 1) & 1, p.wait_cycles, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
-              tc_fence_after();
+            for (int k = 0; k < NRH; ++k) lsum[k] *= alpha_s[rbase + k];
+            const bool corr = flags[0] != 0;
+            if (ok && corr && i > 0) {
+              // Rescale the O^T columns of rows whose reference moved (rare),
+              // once PV(i - 1) is done (its completion barrier is within one
+              // phase of the awaited one, as in the other configurations).
+              ok = mbar_wait_abort(bar(((g + i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE),
+                                   ((g + i - 1) >> 1) & 1, p.wait_cycles, abort_flag);
+              ok = __all_sync(0xffffffffu, ok);
+              if (ok) {
+                tc_fence_after();
 #pragma unroll 1
-              for (int d = 0; d < 4; ++d) {
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int d = 0; d < 4; ++d) {
 #pragma unroll
                   for (int cc = 0; cc < NRH / 8; ++cc) {
                     uint32_t r[8];
-                    const uint32_t addr =
-                        tmem + lane_addr + C::kOCol + d * C::OW + half * NR + rbase + cc * 8;
+                    const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + rbase + cc * 8;
                     tmem_ld8(addr, r);
                     tmem_ld_wait();
 #pragma unroll
@@ -924,159 +919,317 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
                     tmem_st8(addr, r);
                   }
                 }
+                tmem_st_wait();
               }
-              tmem_st_wait();
             }
           }
-        }
-        // Weights 2^(t - k + 8), exact power-of-two scaling.
+          // Weights 2^(t - k + 8) and this thread's row sums.
 #pragma unroll
-        for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], kreg[k]);
-        // P^T as two E4M3 terms into shared memory, MN-major:
-        // [term][NR/16 row groups][128 tokens][16 rows]; this thread writes its
-        // token's bytes for rows rbase .. rbase + NRH, 16 (or 8) rows per store.
-        // P barriers (and buffers) alternate by tile parity; the PV issuer
-        // uses the same rule.
-        const int pb = i & 1;
-        const int puse = i >> 1;
-        if (ok && !C::kPInStage && expired_here(p, WAIT_P_FREE, i)) ok = false;
-        if (ok && !C::kPInStage && puse >= 1)
-          ok = mbar_wait_abort(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok && lane == 0) *abort_flag = 1;
-        if (ok) {
-          // P^T of tile i goes to the rope block of its KV stage (consumed by
-          // QK(i), which s_full(i) reports complete) or to a P buffer.
-          uint8_t* pbuf = C::kPInStage
-                              ? base + C::kKV + (i % C::NST) * kTileBytes + kRopeOffset
-                              : base + C::kP + pb * C::kPBytes;
-          if constexpr (NRH % 16 == 0) {
-            // Whole 16-row groups: one 16-byte store per term and group, the
-            // warp's 32 tokens covering 512 contiguous bytes (no bank conflict).
+          for (int k4 = 0; k4 < NRH / 4; ++k4) {
+            const int4 kc = *reinterpret_cast<const int4*>(kci + rbase + 4 * k4);
+            t[4 * k4] = softmax_weight_kc(t[4 * k4], kc.x);
+            t[4 * k4 + 1] = softmax_weight_kc(t[4 * k4 + 1], kc.y);
+            t[4 * k4 + 2] = softmax_weight_kc(t[4 * k4 + 2], kc.z);
+            t[4 * k4 + 3] = softmax_weight_kc(t[4 * k4 + 3], kc.w);
+          }
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) lsum[k] += t[k];
+          // P^T (one buffer): wait until PV(i - 1) has read it.
+          if (ok && expired_here(p, WAIT_P_FREE, i)) ok = false;
+          if (ok && g + i >= 1)
+            ok = mbar_wait_abort(bar(BAR_PFREE0), (g + i - 1) & 1, p.wait_cycles, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok && lane == 0) *abort_flag = 1;
+          if (ok) {
+            // MN-major [term][NR/16 row groups][128 tokens][16 rows]: one
+            // 16-byte store per term and 16-row group.
+            uint8_t* pbuf = base + C::kP;
 #pragma unroll
             for (int g = 0; g < NRH / 16; ++g) {
-              const int row = rbase + g * 16;
-              uint4 vh, vl;
-              split_e4m3x4(&t[g * 16 + 0], vh.x, vl.x);
-              split_e4m3x4(&t[g * 16 + 4], vh.y, vl.y);
-              split_e4m3x4(&t[g * 16 + 8], vh.z, vl.z);
-              split_e4m3x4(&t[g * 16 + 12], vh.w, vl.w);
-              const uint32_t off = (row >> 4) * 2048 + tok_lane * 16;
+              uint32_t h[8], l[8];
+#pragma unroll
+              for (int m = 0; m < 8; ++m)
+                split_e4m3x2_h(t[g * 16 + 2 * m], t[g * 16 + 2 * m + 1], h[m], l[m]);
+              const uint4 vh = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
+                                          h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+              const uint4 vl = make_uint4(l[0] | (l[1] << 16), l[2] | (l[3] << 16),
+                                          l[4] | (l[5] << 16), l[6] | (l[7] << 16));
+              const uint32_t off = ((rbase >> 4) + g) * 2048 + tok_lane * 16;
               *reinterpret_cast<uint4*>(pbuf + off) = vh;
               *reinterpret_cast<uint4*>(pbuf + C::kPHalf + off) = vl;
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(BAR_PFULL0));
+          }
+        }
+      } else {
+        for (int i = 0; i < n_tiles; ++i) {
+          const int sb = (C::NS == 2) ? ((g + i) & 1) : 0;
+          const int use = (C::NS == 2) ? ((g + i) >> 1) : (g + i);
+          if (ok)
+            ok = !expired_here(p, WAIT_S_FULL, i) &&
+                 mbar_wait_abort(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
+          float t[NRH];
+          if (ok) {
+            tc_fence_after();
+            uint32_t r[NRH];
+#pragma unroll
+            for (int cc = 0; cc < NRH / 8; ++cc)
+              tmem_ld8(tmem + lane_addr + sb * NR + rbase + cc * 8,
+                       *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
+            tc_fence_before();
+            mbar_arrive(bar(BAR_SFREE0 + sb));
           } else {
 #pragma unroll
-            for (int g = 0; g < NRH / 8; ++g) {
-              const int row = rbase + g * 8;
-              uint2 vh, vl;
-              split_e4m3x4(&t[g * 8 + 0], vh.x, vl.x);
-              split_e4m3x4(&t[g * 8 + 4], vh.y, vl.y);
-              const uint32_t off = (row >> 4) * 2048 + tok_lane * 16 + (row & 15);
-              *reinterpret_cast<uint2*>(pbuf + off) = vh;
-              *reinterpret_cast<uint2*>(pbuf + C::kPHalf + off) = vl;
+            for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
+          }
+          scale_mask(t, i);
+          // Reference check.  A row's reference k only has to bound its scores:
+          // with p = 2^(t - k + 8), E4M3 holds p up to 448 = 2^8.8, so any k with
+          // t <= k + 0.75 works.  One vote finds whether some score of the tile
+          // exceeds its row's reference; only then (always on the first tile)
+          // are the tile maxima reduced and references raised to ceil(max).
+          bool over = false;
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) over |= t[k] > kreg[k] + 0.75f;
+          const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
+          // Owners fold the previous tile's row sums (relative to its reference).
+          if (sid < NR && i > 0) {
+            const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
+            l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+          }
+          if (any_over) {
+            {
+              float tm[NRH];
+#pragma unroll
+              for (int k = 0; k < NRH; ++k) tm[k] = t[k];
+              warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
+            }
+            // The correction flag: cleared before B1 (every read of its last
+            // value happened before this tile's vote), set by owners after B1,
+            // read by all after B2.
+            if (sid == 0) flags[0] = 0;
+            named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
+            if (sid < NR) {
+              const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
+                                     fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
+              float k_new = k_row;
+              if (mt > k_row + 0.75f) k_new = ceilf(mt);
+              float alpha = 1.0f;
+              if (k_new != k_row && k_row != -INFINITY) {
+                const int e = static_cast<int>(k_row - k_new);
+                alpha = (e < -126) ? 0.0f : pow2i(e);
+                flags[0] = 1;
+              }
+              l_row *= alpha;
+              k_row = k_new;
+              kref[sid] = k_new;
+              alpha_s[sid] = alpha;
+            }
+            named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
+#pragma unroll
+            for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
+            const bool corr = flags[0] != 0;
+            if (ok && corr && i > 0) {
+              // Rescale the O^T columns (hi and lo) of rows whose reference moved
+              // (rare), once PV(i-1) is done.  PV completions alternate between
+              // two barriers, and the one of PV(i-1)'s parity is within one phase
+              // of the awaited one: s_full(i) implies PV(i-2) completed (QK(i)
+              // waits for it) and PV(i+1) needs a later tile's P^T.
+              ok = mbar_wait_abort(bar(((g + i - 1) & 1) ? C::kBarOdone1 : BAR_ODONE),
+                                   ((g + i - 1) >> 1) & 1, p.wait_cycles, abort_flag);
+              ok = __all_sync(0xffffffffu, ok);
+              if (ok) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int d = 0; d < 4; ++d) {
+#pragma unroll
+                  for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int cc = 0; cc < NRH / 8; ++cc) {
+                      uint32_t r[8];
+                      const uint32_t addr =
+                          tmem + lane_addr + C::kOCol + d * C::OW + half * NR + rbase + cc * 8;
+                      tmem_ld8(addr, r);
+                      tmem_ld_wait();
+#pragma unroll
+                      for (int k = 0; k < 8; ++k)
+                        r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[rbase + cc * 8 + k]);
+                      tmem_st8(addr, r);
+                    }
+                  }
+                }
+                tmem_st_wait();
+              }
             }
           }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(bar(BAR_PFULL0 + pb));
+          // Weights 2^(t - k + 8), exact power-of-two scaling.
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], kreg[k]);
+          // P^T as two E4M3 terms into shared memory, MN-major:
+          // [term][NR/16 row groups][128 tokens][16 rows]; this thread writes its
+          // token's bytes for rows rbase .. rbase + NRH, 16 (or 8) rows per store.
+          // P barriers (and buffers) alternate by tile parity; the PV issuer
+          // uses the same rule.
+          const int pb = (g + i) & 1;
+          const int puse = (g + i) >> 1;
+          if (ok && !C::kPInStage && expired_here(p, WAIT_P_FREE, i)) ok = false;
+          if (ok && !C::kPInStage && puse >= 1)
+            ok = mbar_wait_abort(bar(BAR_PFREE0 + pb), (puse - 1) & 1, p.wait_cycles, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok && lane == 0) *abort_flag = 1;
+          if (ok) {
+            // P^T of tile i goes to the rope block of its KV stage (consumed by
+            // QK(i), which s_full(i) reports complete) or to a P buffer.
+            uint8_t* pbuf = C::kPInStage
+                                ? base + C::kKV + ((g + i) % C::NST) * kTileBytes + kRopeOffset
+                                : base + C::kP + pb * C::kPBytes;
+            if constexpr (NRH % 16 == 0) {
+              // Whole 16-row groups: one 16-byte store per term and group, the
+              // warp's 32 tokens covering 512 contiguous bytes (no bank conflict).
+#pragma unroll
+              for (int g = 0; g < NRH / 16; ++g) {
+                const int row = rbase + g * 16;
+                uint4 vh, vl;
+                split_e4m3x4(&t[g * 16 + 0], vh.x, vl.x);
+                split_e4m3x4(&t[g * 16 + 4], vh.y, vl.y);
+                split_e4m3x4(&t[g * 16 + 8], vh.z, vl.z);
+                split_e4m3x4(&t[g * 16 + 12], vh.w, vl.w);
+                const uint32_t off = (row >> 4) * 2048 + tok_lane * 16;
+                *reinterpret_cast<uint4*>(pbuf + off) = vh;
+                *reinterpret_cast<uint4*>(pbuf + C::kPHalf + off) = vl;
+              }
+            } else {
+#pragma unroll
+              for (int g = 0; g < NRH / 8; ++g) {
+                const int row = rbase + g * 8;
+                uint2 vh, vl;
+                split_e4m3x4(&t[g * 8 + 0], vh.x, vl.x);
+                split_e4m3x4(&t[g * 8 + 4], vh.y, vl.y);
+                const uint32_t off = (row >> 4) * 2048 + tok_lane * 16 + (row & 15);
+                *reinterpret_cast<uint2*>(pbuf + off) = vh;
+                *reinterpret_cast<uint2*>(pbuf + C::kPHalf + off) = vl;
+              }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(BAR_PFULL0 + pb));
+          }
+          // Row sums of the unquantised weights, reduced per tile and folded in
+          // by the owners after the next tile's vote (double-buffered by tile
+          // parity).
+          warp_reduce_rows<NRH, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR + rbase);
         }
-        // Row sums of the unquantised weights, reduced per tile and folded in
-        // by the owners after the next tile's vote (double-buffered by tile
-        // parity).
-        warp_reduce_rows<NRH, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR + rbase);
       }
-    }
-    if (!ok && lane == 0) {
-      report(p.status, MLA_ERR_TIMEOUT);
-      *abort_flag = 1;
-    }
-    // ---- epilogue ----
-    if constexpr (C::kWide) {
-      // The per-thread sums, reduced over the 32 tokens of each warp; the
-      // owners add the four lane quadrants below.
-      warp_reduce_rows<NRH, false>(lsum, lane, red_sum + quad * NR + rbase);
-    }
-    named_bar_sync(kSoftmaxBarrier, NT);
-    const bool single = (nsplit == 1);
-    float* scale_s = alpha_s;
-    if (sid < NR) {
-      if (n_tiles > 0) {
-        const float* rs = red_sum + (C::kWide ? 0 : ((n_tiles - 1) & 1) * 4 * NR);
-        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+      if (!ok && lane == 0) {
+        report(p.status, MLA_ERR_TIMEOUT);
+        *abort_flag = 1;
       }
-      const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
-      const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + sid;
-      float sc = 0.0f;
-      if (sid < rows_here) {
-        if (single) {
-          // A sink is one more (zero-valued) key: it joins the denominator.
-          const float sink2 = p.sinks
-                                  ? p.sinks[(row0 + sid) % p.num_heads] * 1.4426950408889634f
-                                  : -INFINITY;
-          const float mm = fmaxf(l_row > 0.0f ? m_s : -INFINITY, sink2);
-          const float a = (l_row > 0.0f) ? exp2f(m_s - mm) : 0.0f;
-          const float den = l_row * a + (sink2 == -INFINITY ? 0.0f : exp2f(sink2 - mm));
-          const float ls = (den > 0.0f) ? 0.6931471805599453f * (mm + log2f(den)) : -INFINITY;
-          if (p.lse) p.lse[grow] = ls;
-          sc = (den > 0.0f) ? kv_scale * p.output_scale * a / den : 0.0f;
-        } else {
-          float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
-          ml[0] = m_s;
-          ml[1] = l_row;
-          sc = kv_scale;
+      // ---- epilogue ----
+      if constexpr (C::kWide) {
+        // The per-thread sums, reduced over the 32 tokens of each warp; the
+        // owners add the four lane quadrants below.
+        warp_reduce_rows<NRH, false>(lsum, lane, red_sum + quad * NR + rbase);
+      }
+      named_bar_sync(kSoftmaxBarrier, NT);
+      const bool single = (nsplit == 1);
+      float* scale_s = alpha_s;
+      if (sid < NR) {
+        if (n_tiles > 0) {
+          const float* rs = red_sum + (C::kWide ? 0 : ((n_tiles - 1) & 1) * 4 * NR);
+          l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+        }
+        const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
+        const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + sid;
+        float sc = 0.0f;
+        if (sid < rows_here) {
+          if (single) {
+            // A sink is one more (zero-valued) key: it joins the denominator.
+            const float sink2 = p.sinks
+                                    ? p.sinks[(row0 + sid) % p.num_heads] * 1.4426950408889634f
+                                    : -INFINITY;
+            const float mm = fmaxf(l_row > 0.0f ? m_s : -INFINITY, sink2);
+            const float a = (l_row > 0.0f) ? exp2f(m_s - mm) : 0.0f;
+            const float den = l_row * a + (sink2 == -INFINITY ? 0.0f : exp2f(sink2 - mm));
+            const float ls = (den > 0.0f) ? 0.6931471805599453f * (mm + log2f(den)) : -INFINITY;
+            if (p.lse) p.lse[grow] = ls;
+            sc = (den > 0.0f) ? kv_scale * p.output_scale * a / den : 0.0f;
+          } else {
+            float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
+            ml[0] = m_s;
+            ml[1] = l_row;
+            sc = kv_scale;
+          }
+        }
+        scale_s[sid] = sc;
+        // The 96-row configuration's thresholds and exponent offsets start the
+        // next item with no reference (every thread is past its last read).
+        if constexpr (C::kWide) {
+          kref[sid] = -INFINITY;
+          reinterpret_cast<int*>(base + C::kKci)[sid] = kKcNone;
         }
       }
-      scale_s[sid] = sc;
-    }
-    named_bar_sync(kSoftmaxBarrier, NT);
-    // Each MMA warp commits BAR_FINAL once, after its last MMA.
-    bool fin = !expired_here(p, WAIT_FINAL, 0) && mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
-    fin = __all_sync(0xffffffffu, fin);
-    if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
-    if (ok && fin && n_tiles > 0) {
-      tc_fence_after();
+      named_bar_sync(kSoftmaxBarrier, NT);
+      // The PV warp commits BAR_FINAL once per item, after its last PV.
+      bool fin = !expired_here(p, WAIT_FINAL, 0) &&
+                 mbar_wait(bar(BAR_FINAL), (nq - 1) & 1, p.wait_cycles);
+      fin = __all_sync(0xffffffffu, fin);
+      if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
+      if (ok && fin && n_tiles > 0) {
+        tc_fence_after();
 #pragma unroll 1
-      for (int d = 0; d < 4; ++d) {
-        const int dim = d * 128 + tok_lane;
+        for (int d = 0; d < 4; ++d) {
+          const int dim = d * 128 + tok_lane;
 #pragma unroll
-        for (int cc = 0; cc < NRH / 8; ++cc) {
-          uint32_t r[8], r2[8];
-          const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + rbase + cc * 8;
-          tmem_ld8(addr, r);
-          if constexpr (!C::kWide) tmem_ld8(addr + NR, r2);  // the lo term's product
-          tmem_ld_wait();
+          for (int cc = 0; cc < NRH / 8; ++cc) {
+            uint32_t r[8], r2[8];
+            const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + rbase + cc * 8;
+            tmem_ld8(addr, r);
+            if constexpr (!C::kWide) tmem_ld8(addr + NR, r2);  // the lo term's product
+            tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int row = rbase + cc * 8 + k;
-            if (row < rows_here) {
-              const float o = C::kWide ? __uint_as_float(r[k])
-                                       : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
-              const float v = o * scale_s[row];
-              const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
-              if (single) {
-                p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
-                if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = v;
-              } else {
-                p.ws_o[(grow * p.max_splits + split) * MLA_LATENT_DIM + dim] = v;
+            for (int k = 0; k < 8; ++k) {
+              const int row = rbase + cc * 8 + k;
+              if (row < rows_here) {
+                const float o = C::kWide ? __uint_as_float(r[k])
+                                         : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
+                const float v = o * scale_s[row];
+                const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
+                if (single) {
+                  p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
+                  if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = v;
+                } else {
+                  p.ws_o[(grow * p.max_splits + split) * MLA_LATENT_DIM + dim] = v;
+                }
               }
             }
           }
         }
-      }
-    } else if (ok && fin && n_tiles == 0 && single) {
-      // No key of this split is visible to any row here (padding query slots,
-      // an empty window or selection): O = 0.  Partials need only (-inf, 0),
-      // written above; the merge gives such slots weight 0 without reading O.
+      } else if (ok && fin && n_tiles == 0 && single) {
+        // No key of this split is visible to any row here (padding query slots,
+        // an empty window or selection): O = 0.  Partials need only (-inf, 0),
+        // written above; the merge gives such slots weight 0 without reading O.
 #pragma unroll 1
-      for (int d = 0; d < 4; ++d) {
-        const int dim = d * 128 + tok_lane;
-        for (int row = rbase; row < min(rows_here, rbase + NRH); ++row) {
-          const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
-          p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(0.0f);
-          if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = 0.0f;
+        for (int d = 0; d < 4; ++d) {
+          const int dim = d * 128 + tok_lane;
+          for (int row = rbase; row < min(rows_here, rbase + NRH); ++row) {
+            const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
+            p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(0.0f);
+            if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = 0.0f;
+          }
         }
       }
+      // O^T has been read: the next item's first PV may overwrite it.
+      tc_fence_before();
+      mbar_arrive(bar(BAR_OFREE));
+      g += n_tiles;
+      if (!ok) break;  // after a wait ran out the remaining items are not run
     }
   }
   tc_fence_before();
@@ -1088,6 +1241,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
   // This CTA's partials are written: the merge may start once every CTA is here.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+#undef MLA_ITEM_NAMES
 
 
 
@@ -1122,15 +1276,15 @@ static bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t bo
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NR, bool kGather, bool kItems>
+template <int NR, bool kGather, int kMode>
 static cudaError_t launch_split_t(const void* q, const void* kv, int64_t num_pages, int batch,
                                 int groups, int num_ctas, const DecodeParams& prm,
                                 cudaStream_t stream) {
   using C = Cfg<NR>;
   static std::atomic<uint64_t> attr_done{0};
   {
-    const cudaError_t e =
-        ensure_smem_attr(mla_split_kv_kernel<NR, kGather, kItems>, static_cast<int>(C::kSmemBytes), attr_done);
+    const cudaError_t e = ensure_smem_attr(mla_split_kv_kernel<NR, kGather, kMode>,
+                                           static_cast<int>(C::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap kv_lat, kv_rope, q_lat, q_rope;
@@ -1141,9 +1295,10 @@ static cudaError_t launch_split_t(const void* q, const void* kv, int64_t num_pag
       !make_map(&q_lat, q, q_rows, 128, NR, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&q_rope, q, q_rows, 64, NR, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  const dim3 grid = kItems ? dim3(num_ctas) : dim3(batch, prm.max_splits * groups);
-  mla_split_kv_kernel<NR, kGather, kItems><<<grid, C::kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat,
-                                                                     q_rope, prm);
+  // Persistent: num_ctas CTAs loop over the prm.num_items items of the list.
+  const dim3 grid = kMode != 0 ? dim3(num_ctas) : dim3(batch, prm.max_splits * groups);
+  mla_split_kv_kernel<NR, kGather, kMode>
+      <<<grid, C::kThreads, C::kSmemBytes, stream>>>(kv_lat, kv_rope, q_lat, q_rope, prm);
   return cudaGetLastError();
 }
 
@@ -1151,13 +1306,13 @@ template <int NR, bool kGather>
 static cudaError_t launch_split(const void* q, const void* kv, int64_t num_pages, int batch,
                                 int groups, int num_ctas, const DecodeParams& prm,
                                 cudaStream_t stream) {
-  // The item-list mapping is its own instantiation, so the grid variant's
-  // code is exactly what it is without it.
-  return prm.cta_items
-             ? launch_split_t<NR, kGather, true>(q, kv, num_pages, batch, groups, num_ctas, prm,
-                                                 stream)
-             : launch_split_t<NR, kGather, false>(q, kv, num_pages, batch, groups, num_ctas, prm,
-                                                  stream);
+  // The item-list mapping and the persistent loop are their own
+  // instantiations, so the grid variant's code is what it is without them.
+  if (!prm.cta_items)
+    return launch_split_t<NR, kGather, 0>(q, kv, num_pages, batch, groups, num_ctas, prm, stream);
+  if (num_ctas < prm.num_items)
+    return launch_split_t<NR, kGather, 2>(q, kv, num_pages, batch, groups, num_ctas, prm, stream);
+  return launch_split_t<NR, kGather, 1>(q, kv, num_pages, batch, groups, num_ctas, prm, stream);
 }
 
 std::atomic<long long> g_wait_cycles{0};
@@ -1277,6 +1432,7 @@ static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t n
   prm.block_idx = nullptr;
   prm.topk = 0;
   prm.cta_items = nullptr;
+  prm.num_items = 0;
   prm.batch = batch;
   dl->num_ctas = 0;
   {
@@ -1322,6 +1478,10 @@ static int apply_options(const mla_decode_options_t* o, const char* who, DecodeL
       return MLA_ERR_INVALID_ARG;
     }
   }
+  if (o->persistent_ctas < 0 || (o->persistent_ctas > 0 && !o->cta_items)) {
+    set_error(w + ": persistent_ctas needs a CTA item list and must be >= 0");
+    return MLA_ERR_INVALID_ARG;
+  }
   dl->prm.q_scale_dev = o->q_scale_dev;
   dl->prm.kv_scale_dev = o->kv_scale_dev;
   dl->prm.sm_scale_dev = o->softmax_scale_dev;
@@ -1330,7 +1490,12 @@ static int apply_options(const mla_decode_options_t* o, const char* who, DecodeL
   dl->prm.query_lens = o->query_lens;
   dl->prm.kv_bounds = o->kv_bounds;
   dl->prm.cta_items = o->cta_items;
-  dl->num_ctas = o->cta_items ? o->num_ctas : 0;
+  dl->prm.num_items = o->cta_items ? o->num_ctas : 0;
+  // Persistent CTAs: at most one per item.
+  dl->num_ctas = o->cta_items ? (o->persistent_ctas > 0 && o->persistent_ctas < o->num_ctas
+                                     ? o->persistent_ctas
+                                     : o->num_ctas)
+                              : 0;
   dl->mp.output_scale = o->output_scale;
   dl->mp.sinks = o->sinks;
   return MLA_OK;

@@ -1554,6 +1554,10 @@ static int decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t nu
       set_error(who + ": q/kv scales are FP8-only (BF16 Q and KV carry no scale)");
       return MLA_ERR_UNSUPPORTED;
     }
+    if (options->persistent_ctas != 0) {
+      set_error(who + ": persistent CTAs are FP8-only");
+      return MLA_ERR_UNSUPPORTED;
+    }
     if (options->cta_items) {
       const int64_t cap = static_cast<int64_t>(batch) * max_splits * rg.groups;
       if (options->num_ctas < 1 || options->num_ctas > cap) {
@@ -1568,6 +1572,7 @@ static int decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t nu
     prm.query_lens = options->query_lens;
     prm.kv_bounds = options->kv_bounds;
     prm.cta_items = options->cta_items;
+    prm.num_items = options->cta_items ? options->num_ctas : 0;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;

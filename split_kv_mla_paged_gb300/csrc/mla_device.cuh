@@ -52,8 +52,10 @@ struct DecodeParams {
   const int32_t* block_idx;
   int32_t topk;
   // Optional CTA item list (mla_decode_plan_items): CTA i works on item
-  // cta_items[i] of a 1-D grid; NULL = the (batch, splits x groups) grid.
+  // cta_items[i] of a 1-D grid, or (persistent CTAs) on items i, i + gridDim.x,
+  // ... < num_items; NULL = the (batch, splits x groups) grid.
   const int32_t* cta_items;
+  int32_t num_items;
   int32_t batch;
   long long wait_cycles;   // limit of the pipeline waits (drains always use the long limit)
   // Test hook (mla_debug_set_expire): (role << 24) | tile makes that one
@@ -67,12 +69,15 @@ struct DecodeParams {
   float* out_f32;
 };
 
-// Barrier indices inside the aux block.
+// Barrier indices inside the aux block.  The BF16 kernels use the first 17;
+// the FP8 kernel also has the per-item Q-free and O^T-free barriers of its
+// persistent mode.
 enum : int {
   BAR_FULL0 = 0, BAR_EMPTY0 = 3, BAR_QFULL = 6, BAR_SFULL0, BAR_SFULL1, BAR_SFREE0, BAR_SFREE1,
-  BAR_PFULL0, BAR_PFULL1, BAR_PFREE0, BAR_PFREE1, BAR_ODONE, BAR_FINAL, BAR_COUNT
+  BAR_PFULL0, BAR_PFULL1, BAR_PFREE0, BAR_PFREE1, BAR_ODONE, BAR_FINAL, BAR_QFREE, BAR_OFREE,
+  BAR_COUNT
 };
-static_assert(BAR_COUNT <= 17, "barrier slots");
+static_assert(BAR_FINAL < 17 && BAR_COUNT <= 19, "barrier slots");
 
 __device__ __forceinline__ void report(int* status, int code) {
   atomicCAS(status, 0, code);

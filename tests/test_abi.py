@@ -176,3 +176,20 @@ def test_bf16_item_lists_use_the_bf16_row_groups(lib):
     assert len(fp8) == sum(splits) and len(bf16) == 2 * sum(splits)
     groups = bf16 & ((1 << 5) - 1)
     assert sorted(set(groups.tolist())) == [0, 1]
+
+
+def test_persistent_ctas_host_checks(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 1.0, 1.0, 0.1, fake,
+            1 << 30, fake, None, None]
+    # Persistent CTAs need an item list; a negative count is refused.
+    opts = mla.DecodeOptions(None, None, None, 1.0, None, None, None, None, 0, 4)
+    assert lib.mla_decode_ex(*args, ctypes.byref(opts), None) == mla.MLA_ERR_INVALID_ARG
+    assert "persistent" in mla.mla_last_error()
+    opts = mla.DecodeOptions(None, None, None, 1.0, None, None, None, fake, 2, -1)
+    assert lib.mla_decode_ex(*args, ctypes.byref(opts), None) == mla.MLA_ERR_INVALID_ARG
+    # The BF16 entry points have no persistent mode.
+    opts = mla.DecodeOptions(None, None, None, 1.0, None, None, None, fake, 2, 4)
+    st = lib.mla_decode_bf16_ex(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 0.1,
+                                fake, 1 << 30, fake, None, None, ctypes.byref(opts), None)
+    assert st == mla.MLA_ERR_UNSUPPORTED and "persistent" in mla.mla_last_error()
