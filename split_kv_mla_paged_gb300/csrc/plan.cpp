@@ -145,14 +145,18 @@ extern "C" int mla_decode_plan(const int32_t* kv_lens, int32_t batch, int32_t nu
   // Merge thread groups (KvSplit): PR #20380 "Description" takes the largest
   // power of two up to the cap that still gives every group whole work and
   // keeps the grid within its CTA budget.  Here: the largest power of two up
-  // to 16 with at least two partials per group and rows x groups <= 6 x SMs
+  // to 16 with at least two partials per group and merged rows x groups <= 6 x SMs
   // (the merge runs rows x 4 CTAs of 32 threads per group, so this keeps it
   // near a third of the GPU's thread slots; past that, more groups add
   // threads but no parallel loads).  Fitted to the
   // merge-only sweep on GB300 (rows 12-768, 6-152 splits, every KvSplit):
   // within 5 % of the best KvSplit per point in total, against 14 % for
   // "about four partials per group".
-  const int64_t rows = static_cast<int64_t>(batch) * num_heads * q_len;
+  // Only the rows of requests with more than one split are merged (the
+  // others are written by the split kernel and their merge CTAs exit at once).
+  int64_t rows = 0;
+  for (int b = 0; b < batch; ++b)
+    if (splits_out[b] > 1) rows += static_cast<int64_t>(num_heads) * q_len;
   const int64_t budget = 6 * static_cast<int64_t>(sm_count > 0 ? sm_count : kDefaultSms);
   int32_t g = 16;
   while (g > 1 && (g * 2 > max_splits || rows * g > budget)) g >>= 1;

@@ -177,3 +177,12 @@ def test_merge_kv_split_rule(rows_hq, splits, expect):
     p = mla.mla_decode_plan([splits * 128], num_heads=H, q_len=q, sm_count=152,
                             target_ctas=splits)
     assert p.max_splits == splits and p.kv_split == expect
+
+
+def test_merge_kv_split_counts_only_merged_rows():
+    # A skewed batch: one long request (many splits) and short ones (one split
+    # each, written directly): only the long request's 96 rows are merged.
+    lens = [1048576] + [4096] * 7
+    p = mla.mla_decode_plan(lens, num_heads=12, q_len=8, sm_count=152)
+    assert p.splits[0] > 100 and np.all(p.splits[1:] == 1)
+    assert p.kv_split == 8  # 96 rows x 8 groups <= 912; 768 rows would give 1
