@@ -74,8 +74,9 @@ struct Cfg {
   static constexpr int NS = kWide ? 1 : 2;        // S^T buffers in TMEM
   static constexpr uint32_t kTmemUsed = NS * NR + 4 * OW;
   static_assert(kTmemUsed <= 512, "TMEM");
-  // Softmax warpgroups: two (each owning half the rows) from 32 rows up.
-  static constexpr int SWG = NR >= 32 ? 2 : 1;
+  // Softmax warpgroups: two (each owning half the rows) from 32 rows up,
+  // three (32 rows each) for the 96-row configuration.
+  static constexpr int SWG = kWide ? 3 : NR >= 32 ? 2 : 1;
   static constexpr int NRH = NR / SWG;
   static_assert(NRH % 8 == 0, "rows per softmax warpgroup");
   // Warp 0 TMA, warp 1 QK issuer (and TMEM owner), warp 2 PV issuer, then
@@ -84,7 +85,19 @@ struct Cfg {
   // MTP q8 B16 128K) than one warp polling both, and the polling loop lost
   // 4 % to any extra work in it.
   static constexpr int kMmaWarps = 2;
-  static constexpr int kSoftmaxWarp0 = 1 + kMmaWarps;
+  // 96 rows: an idle fourth warp makes warps 0-3 one warpgroup, so that
+  // setmaxnreg can move registers from it to the three softmax warpgroups:
+  // launched with 128 per thread (512 threads), warpgroup 0 drops to 56 and
+  // the softmax warpgroups rise to 152 (56 x 128 + 152 x 384 = 128 x 512).
+  // Measured against two softmax warpgroups of 48 rows at 168 registers
+  // (which spilled): MTP q8 B16 128K 371.6 -> 361.2 us, B1 45.1 -> 41.4 us,
+  // H96 q8 B1 1M 1332.7 -> 1305.7 us.
+  static constexpr int kIdleWarps = kWide ? 1 : 0;
+  static constexpr int kSoftmaxWarp0 = 1 + kMmaWarps + kIdleWarps;
+  static constexpr int kRegsLaunch = 128, kRegsLow = 56, kRegsHigh = 152;
+  static_assert(!kWide || (kRegsLow * 128 + kRegsHigh * 128 * SWG <= kRegsLaunch * 512 &&
+                           32 * kSoftmaxWarp0 + 128 * SWG == 512),
+                "register split");
   static constexpr int kThreads = 32 * kSoftmaxWarp0 + 128 * SWG;
   static constexpr uint32_t kTmemCols =
       kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
@@ -390,330 +403,336 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + C::kTmemSlot);
 
-  if (warp == 0) {
-    // ================= TMA producer =================
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_kv_lat);
-      tma_prefetch_desc(&tm_kv_rope);
-      tma_prefetch_desc(&tm_q_lat);
-      tma_prefetch_desc(&tm_q_rope);
-    }
-    const uint64_t pol = l2_policy_evict_first();
-    volatile uint32_t* stage_info = reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo);
-    int issued = 0;  // tiles issued, all items
-    int st = 0, round = 0;
-    int nq = 0;      // items whose Q was loaded
-    bool ok = true;
-    for (int n = 0; ok && (kPersist || n == 0); ++n) {
-      ItemInfo item;
-      const int r = next_item(n, item);
-      if (r == 0) break;
-      if (r == 1) continue;
-      MLA_ITEM_NAMES(item);
-      // Q of this item, once the previous item's QKs are done with the buffer.
-      if (nq > 0) {
-        bool q_ok = mbar_wait_abort(bar(BAR_QFREE), (nq - 1) & 1, p.wait_cycles, abort_flag);
-        q_ok = __all_sync(0xffffffffu, q_ok && !*abort_flag);
-        if (!q_ok) {
-          if (lane == 0) {
-            report(p.status, MLA_ERR_TIMEOUT);
-            *abort_flag = 1;
-          }
-          ok = false;
-          break;
-        }
-      }
+  if (warp < C::kSoftmaxWarp0) {
+    // Producer, MMA issuers (and the 96-row configuration's idle warp): one
+    // warpgroup, whose registers go to the softmax warpgroups.
+    if constexpr (C::kWide) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsLow));
+    if (warp == 0) {
+      // ================= TMA producer =================
       if (lane == 0) {
-        const int qrow = b * p.rows_per_req + row0;
-        mbar_arrive_expect_tx(bar(BAR_QFULL), C::kQBytes);
-#pragma unroll
-        for (int d = 0; d < 4; ++d)
-          tma_load_2d(sbase + C::kQ + d * NR * 128, &tm_q_lat, d * 128, qrow, bar(BAR_QFULL));
-        tma_load_2d(sbase + C::kQ + 4 * NR * 128, &tm_q_rope, MLA_LATENT_DIM, qrow,
-                    bar(BAR_QFULL));
+        tma_prefetch_desc(&tm_kv_lat);
+        tma_prefetch_desc(&tm_kv_rope);
+        tma_prefetch_desc(&tm_q_lat);
+        tma_prefetch_desc(&tm_q_rope);
       }
-      ++nq;
-      const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-      const int page0 = t0 / MLA_PAGE_SIZE;
-      const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
-      // Page ids of 8 tiles (32 pages) per window, one per lane; the next
-      // window is fetched a window ahead so its latency is hidden.  kGather
-      // also keeps, per page, the number of its rows to load (0: not loaded):
-      // compact page cp maps to logical page lp (cp itself, or the selection's
-      // entry), which is loaded when it holds keys inside the window and before
-      // the end of the split (dense) or of the request (selection).
-      int last_lp = -1;  // selection: the entry before this window (order check)
-      auto load_window = [&](int w, int& nv_out) -> int {
-        const int pi = page0 + w * 32 + lane;
-        int pg = 0;
-        nv_out = 0;
-        if constexpr (!kGather) {
-          if (pi < page_end) {
-            pg = pt[pi];
-            if (pg < 0 || pg >= p.num_pages) {
-              report(p.status, MLA_ERR_INVALID_ARG);
-              pg = 0;
-            }
-          }
-        } else {
-          int lp = -1;
-          if (pi < page_end) {
-            lp = pi;
-            if (sparse) lp = (pi < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + pi] : -1;
-          }
-          if (sparse) {
-            // Selected pages must be listed in increasing order, each once.
-            int prev = __shfl_up_sync(0xffffffffu, lp, 1);
-            if (lane == 0) prev = last_lp;
-            if (lp >= 0 && prev >= 0 && lp <= prev) report(p.status, MLA_ERR_INVALID_ARG);
-            last_lp = __shfl_sync(0xffffffffu, lp, 31);
-          }
-          const int64_t end_pos = sparse ? win_hi : tok_end;
-          const int64_t first = static_cast<int64_t>(lp) * MLA_PAGE_SIZE;
-          if (lp >= 0 && first < end_pos && first + MLA_PAGE_SIZE > win_lo) {
-            pg = pt[lp];
-            if (pg < 0 || pg >= p.num_pages) {
-              report(p.status, MLA_ERR_INVALID_ARG);
-              pg = 0;
-            }
-            nv_out = static_cast<int>(end_pos - first < MLA_PAGE_SIZE ? end_pos - first : MLA_PAGE_SIZE);
-          }
-        }
-        return pg;
-      };
-      int window_nv, window_next_nv;
-      int window = load_window(0, window_nv);
-      int window_next = load_window(1, window_next_nv);
-      for (int i = 0; i < n_tiles; ++i) {
-        if (i > 0 && (i & 7) == 0) {
-          window = window_next;
-          window_nv = window_next_nv;
-          window_next = load_window((i >> 3) + 1, window_next_nv);
-        }
-        ok = !expired_here(p, WAIT_STAGE_FREE, i);
-        if (ok && round > 0)
-          ok = mbar_wait_abort(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles, abort_flag);
-        ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-        if (!ok) {
-          if (lane == 0) {
-            report(p.status, MLA_ERR_TIMEOUT);
-            *abort_flag = 1;
-          }
-          break;
-        }
-        // Lane q (< 4) takes the id of the tile's page q.
-        const int src = (i & 7) * 4 + (lane & 3);
-        const int my_page = __shfl_sync(0xffffffffu, window, src);
-        const int tp0 = page0 + i * 4;
-        bool my_load;
-        uint32_t info = 0;
-        if constexpr (kGather) {
-          // Rows to load of pages 0-3, one byte each, for the QK warp (which
-          // zeroes the rest); published by the arrive below.
-          const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
-          my_load = my_nv > 0;
-          const int n1 = __shfl_sync(0xffffffffu, my_nv, 1);
-          const int n2 = __shfl_sync(0xffffffffu, my_nv, 2);
-          const int n3 = __shfl_sync(0xffffffffu, my_nv, 3);
-          info = static_cast<uint32_t>(my_nv) | (static_cast<uint32_t>(n1) << 8) |
-                 (static_cast<uint32_t>(n2) << 16) | (static_cast<uint32_t>(n3) << 24);
-        } else {
-          my_load = tp0 + (lane & 3) < page_end;
-        }
-        const int nload = __popc(__ballot_sync(0xffffffffu, lane < 4 && my_load));
-        const uint32_t fb = bar(BAR_FULL0 + st);
-        if (lane == 0) {
-          if constexpr (kGather) stage_info[st] = info;
-          mbar_arrive_expect_tx(fb, nload * kPageBytes);
-        }
-        __syncwarp();
-        // Lanes 0-3 issue one page each (5 boxes: 4 latent blocks + rope).
-        if (lane < 4 && my_load) {
-          const uint32_t kv = sbase + C::kKV + st * kTileBytes;
-          const int row = my_page * MLA_PAGE_SIZE;
-#pragma unroll
-          for (int d = 0; d < 4; ++d)
-            tma_load_2d_hint(kv + d * kLatBlockBytes + lane * kPageLatBytes, &tm_kv_lat, d * 128,
-                             row, fb, pol);
-          tma_load_2d_hint(kv + kRopeOffset + lane * kPageRopeBytes, &tm_kv_rope, MLA_LATENT_DIM,
-                           row, fb, pol);
-        }
-        __syncwarp();
-        ++issued;
-        if (++st == C::NST) {
-          st = 0;
-          ++round;
-        }
-      }
-    }
-    // Before the CTA can exit, the copies this warp issued must have landed
-    // (they have, unless a wait elsewhere ran out).  The full barrier of a
-    // stage is at most one phase behind the producer, so these waits are exact.
-    if (lane == 0) {
-      for (int k = max(0, issued - C::NST); k < issued; ++k)
-        mbar_wait(bar(BAR_FULL0 + k % C::NST), (k / C::NST) & 1, kWaitLimitCycles);
-      if (nq > 0) mbar_wait(bar(BAR_QFULL), (nq - 1) & 1, kWaitLimitCycles);
-    }
-    __syncwarp();
-  } else if (warp == 1 || warp == 2) {
-    // ================= MMA issuers: warp 1 QK, warp 2 PV =================
-    // Two issuing warps keep the tensor pipe fed with QK(i + 1) while PV(i)
-    // goes out: one warp issuing both left ~30 % of the pipe's rate unused
-    // at these N (measured with a probe of the issue rate).
-    constexpr uint32_t kIdQK = idesc_e4m3(128, NR, 0, 0);
-    constexpr uint32_t kIdPV = idesc_e4m3(128, C::OW, 1, 1);
-    bool ok = true;
-    auto fail = [&]() {
-      if (lane == 0) {
-        report(p.status, MLA_ERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-    };
-    // PV of tile j of an item (tile g of the CTA, KV in stage jst, P^T in
-    // buffer pb); lane 0 issues.
-    auto issue_pv = [&](int j, int g, int jst, int pb) {
-      tc_fence_after();
-      const uint32_t kv = sbase + C::kKV + jst * kTileBytes;
-      const uint32_t pbuf = C::kPInStage ? kv + kRopeOffset : sbase + C::kP + pb * C::kPBytes;
-#pragma unroll
-      for (int d = 0; d < 4; ++d) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = smem_desc(kv + d * kLatBlockBytes + ks * 4096, 16384, 1024,
-                                       kLayoutSW128);
-          const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
-          // B = P^T, MN-major: 16-row groups 2048 B apart (hi groups, then lo
-          // groups), 8-token groups 128 B apart.
-          const uint64_t bd = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
-          umma_f8(tmem + C::kOCol + d * C::OW, a, bd, kIdPV, acc);
-          if constexpr (C::kWide) {
-            // The lo term: a second MMA into the same O^T columns.
-            const uint64_t bl = smem_desc(pbuf + C::kPHalf + ks * 512, 128, 2048, kLayoutNone);
-            umma_f8(tmem + C::kOCol + d * C::OW, a, bl, kIdPV, 1u);
-          }
-        }
-      }
-      umma_commit(bar(BAR_EMPTY0 + jst));
-      if (!C::kPInStage) umma_commit(bar(BAR_PFREE0 + pb));
-      umma_commit(bar((g & 1) ? C::kBarOdone1 : BAR_ODONE));
-    };
-    // QK of tile i (KV in stage ist) into S buffer sb; lane 0 issues.
-    auto issue_qk = [&](int ist, int sb) {
-      tc_fence_after();
-      const uint32_t kv = sbase + C::kKV + ist * kTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < 18; ++kk) {
-        uint64_t a, bd;
-        if (kk < 16) {
-          const int d = kk >> 2, sub = kk & 3;
-          a = smem_desc(kv + d * kLatBlockBytes + sub * 32, 16, 1024, kLayoutSW128);
-          bd = smem_desc(sbase + C::kQ + d * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
-        } else {
-          const int sub = kk - 16;
-          a = smem_desc(kv + kRopeOffset + sub * 32, 16, 512, kLayoutSW64);
-          bd = smem_desc(sbase + C::kQ + 4 * NR * 128 + sub * 32, 16, 512, kLayoutSW64);
-        }
-        umma_f8(tmem + sb * NR, a, bd, kIdQK, kk > 0 ? 1u : 0u);
-      }
-      umma_commit(bar(BAR_SFULL0 + sb));
-    };
-    if (warp == 1) {
-      // QK(j) once its tile has landed, its S^T buffer is free and PV(j - 2)
-      // has completed (so the softmax's wait for PV(j - 1) stays within one
-      // phase of its barrier; QK(j) still overlaps PV(j - 1)).  Tile indices
-      // for buffers and phases count across the CTA's items (g).
-      int st = 0, round = 0, g = 0;
-      int nq = 0;  // items started
+      const uint64_t pol = l2_policy_evict_first();
+      volatile uint32_t* stage_info = reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo);
+      int issued = 0;  // tiles issued, all items
+      int st = 0, round = 0;
+      int nq = 0;      // items whose Q was loaded
+      bool ok = true;
       for (int n = 0; ok && (kPersist || n == 0); ++n) {
         ItemInfo item;
         const int r = next_item(n, item);
         if (r == 0) break;
         if (r == 1) continue;
         MLA_ITEM_NAMES(item);
-        ++nq;
-        bool w = mbar_wait_abort(bar(BAR_QFULL), (nq - 1) & 1, p.wait_cycles, abort_flag);
-        ok = __all_sync(0xffffffffu, w && !*abort_flag);
-        for (int j = 0; ok && j < n_tiles; ++j, ++g) {
-          const int sb = (C::NS == 2) ? (g & 1) : 0;
-          const int use = (C::NS == 2) ? (g >> 1) : g;
-          w = !expired_here(p, WAIT_TILE_FULL, j) &&
-              mbar_wait_abort(bar(BAR_FULL0 + st), round & 1, p.wait_cycles, abort_flag);
-          if (w && use >= 1)
-            w = mbar_wait_abort(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles, abort_flag);
-          // The 96-row CTA needs no PV(g - 2) wait: its softmax waited for
-          // PV(g - 2) (the P^T buffer) before writing P(g - 1), which keeps its
-          // wait for PV(g - 1) within one phase; the tile's stage implies
-          // PV(g - 2) anyway.
-          if (w && g >= 2 && !C::kWide)
-            w = mbar_wait_abort(bar(((g - 2) & 1) ? C::kBarOdone1 : BAR_ODONE),
-                                ((g - 2) >> 1) & 1, p.wait_cycles, abort_flag);
-          w = __all_sync(0xffffffffu, w && !*abort_flag);
-          if (!w) {
+        // Q of this item, once the previous item's QKs are done with the buffer.
+        if (nq > 0) {
+          bool q_ok = mbar_wait_abort(bar(BAR_QFREE), (nq - 1) & 1, p.wait_cycles, abort_flag);
+          q_ok = __all_sync(0xffffffffu, q_ok && !*abort_flag);
+          if (!q_ok) {
+            if (lane == 0) {
+              report(p.status, MLA_ERR_TIMEOUT);
+              *abort_flag = 1;
+            }
             ok = false;
             break;
           }
-          // Rows loaded per page, as the producer published them with the
-          // stage's full barrier (observed above).
-          const uint32_t info =
-              kGather ? *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st) : 0u;
-          zero_unloaded_rows<kGather>(base + C::kKV + st * kTileBytes, lane, info,
-                                      tok_end - (t0 + j * kTileTokens));
-          if (lane == 0) issue_qk(st, sb);
+        }
+        if (lane == 0) {
+          const int qrow = b * p.rows_per_req + row0;
+          mbar_arrive_expect_tx(bar(BAR_QFULL), C::kQBytes);
+#pragma unroll
+          for (int d = 0; d < 4; ++d)
+            tma_load_2d(sbase + C::kQ + d * NR * 128, &tm_q_lat, d * 128, qrow, bar(BAR_QFULL));
+          tma_load_2d(sbase + C::kQ + 4 * NR * 128, &tm_q_rope, MLA_LATENT_DIM, qrow,
+                      bar(BAR_QFULL));
+        }
+        ++nq;
+        const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+        const int page0 = t0 / MLA_PAGE_SIZE;
+        const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
+        // Page ids of 8 tiles (32 pages) per window, one per lane; the next
+        // window is fetched a window ahead so its latency is hidden.  kGather
+        // also keeps, per page, the number of its rows to load (0: not loaded):
+        // compact page cp maps to logical page lp (cp itself, or the selection's
+        // entry), which is loaded when it holds keys inside the window and before
+        // the end of the split (dense) or of the request (selection).
+        int last_lp = -1;  // selection: the entry before this window (order check)
+        auto load_window = [&](int w, int& nv_out) -> int {
+          const int pi = page0 + w * 32 + lane;
+          int pg = 0;
+          nv_out = 0;
+          if constexpr (!kGather) {
+            if (pi < page_end) {
+              pg = pt[pi];
+              if (pg < 0 || pg >= p.num_pages) {
+                report(p.status, MLA_ERR_INVALID_ARG);
+                pg = 0;
+              }
+            }
+          } else {
+            int lp = -1;
+            if (pi < page_end) {
+              lp = pi;
+              if (sparse) lp = (pi < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + pi] : -1;
+            }
+            if (sparse) {
+              // Selected pages must be listed in increasing order, each once.
+              int prev = __shfl_up_sync(0xffffffffu, lp, 1);
+              if (lane == 0) prev = last_lp;
+              if (lp >= 0 && prev >= 0 && lp <= prev) report(p.status, MLA_ERR_INVALID_ARG);
+              last_lp = __shfl_sync(0xffffffffu, lp, 31);
+            }
+            const int64_t end_pos = sparse ? win_hi : tok_end;
+            const int64_t first = static_cast<int64_t>(lp) * MLA_PAGE_SIZE;
+            if (lp >= 0 && first < end_pos && first + MLA_PAGE_SIZE > win_lo) {
+              pg = pt[lp];
+              if (pg < 0 || pg >= p.num_pages) {
+                report(p.status, MLA_ERR_INVALID_ARG);
+                pg = 0;
+              }
+              nv_out = static_cast<int>(end_pos - first < MLA_PAGE_SIZE ? end_pos - first : MLA_PAGE_SIZE);
+            }
+          }
+          return pg;
+        };
+        int window_nv, window_next_nv;
+        int window = load_window(0, window_nv);
+        int window_next = load_window(1, window_next_nv);
+        for (int i = 0; i < n_tiles; ++i) {
+          if (i > 0 && (i & 7) == 0) {
+            window = window_next;
+            window_nv = window_next_nv;
+            window_next = load_window((i >> 3) + 1, window_next_nv);
+          }
+          ok = !expired_here(p, WAIT_STAGE_FREE, i);
+          if (ok && round > 0)
+            ok = mbar_wait_abort(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles, abort_flag);
+          ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+          if (!ok) {
+            if (lane == 0) {
+              report(p.status, MLA_ERR_TIMEOUT);
+              *abort_flag = 1;
+            }
+            break;
+          }
+          // Lane q (< 4) takes the id of the tile's page q.
+          const int src = (i & 7) * 4 + (lane & 3);
+          const int my_page = __shfl_sync(0xffffffffu, window, src);
+          const int tp0 = page0 + i * 4;
+          bool my_load;
+          uint32_t info = 0;
+          if constexpr (kGather) {
+            // Rows to load of pages 0-3, one byte each, for the QK warp (which
+            // zeroes the rest); published by the arrive below.
+            const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
+            my_load = my_nv > 0;
+            const int n1 = __shfl_sync(0xffffffffu, my_nv, 1);
+            const int n2 = __shfl_sync(0xffffffffu, my_nv, 2);
+            const int n3 = __shfl_sync(0xffffffffu, my_nv, 3);
+            info = static_cast<uint32_t>(my_nv) | (static_cast<uint32_t>(n1) << 8) |
+                   (static_cast<uint32_t>(n2) << 16) | (static_cast<uint32_t>(n3) << 24);
+          } else {
+            my_load = tp0 + (lane & 3) < page_end;
+          }
+          const int nload = __popc(__ballot_sync(0xffffffffu, lane < 4 && my_load));
+          const uint32_t fb = bar(BAR_FULL0 + st);
+          if (lane == 0) {
+            if constexpr (kGather) stage_info[st] = info;
+            mbar_arrive_expect_tx(fb, nload * kPageBytes);
+          }
           __syncwarp();
+          // Lanes 0-3 issue one page each (5 boxes: 4 latent blocks + rope).
+          if (lane < 4 && my_load) {
+            const uint32_t kv = sbase + C::kKV + st * kTileBytes;
+            const int row = my_page * MLA_PAGE_SIZE;
+#pragma unroll
+            for (int d = 0; d < 4; ++d)
+              tma_load_2d_hint(kv + d * kLatBlockBytes + lane * kPageLatBytes, &tm_kv_lat, d * 128,
+                               row, fb, pol);
+            tma_load_2d_hint(kv + kRopeOffset + lane * kPageRopeBytes, &tm_kv_rope, MLA_LATENT_DIM,
+                             row, fb, pol);
+          }
+          __syncwarp();
+          ++issued;
           if (++st == C::NST) {
             st = 0;
             ++round;
           }
         }
-        // Q is free for the next item once these QKs complete (also on the
-        // way out: the drain below waits for it).
-        if (lane == 0) umma_commit(bar(BAR_QFREE));
-        __syncwarp();
       }
-      if (!ok) fail();
-      // This warp's MMAs complete before the CTA releases TMEM.
-      if (nq > 0) mbar_wait(bar(BAR_QFREE), (nq - 1) & 1, kWaitLimitCycles);
-    } else {
-      // PV(i) as soon as its P^T is ready; the first PV of an item overwrites
-      // O^T, so it waits until the softmax has read the previous item's.
-      int st = 0, g = 0;
-      int nq = 0;  // items started
-      for (int n = 0; ok && (kPersist || n == 0); ++n) {
-        ItemInfo item;
-        const int r = next_item(n, item);
-        if (r == 0) break;
-        if (r == 1) continue;
-        MLA_ITEM_NAMES(item);
-        ++nq;
-        if (nq > 1) {
-          const bool w =
-              mbar_wait_abort(bar(BAR_OFREE), (nq - 2) & 1, p.wait_cycles, abort_flag);
-          ok = __all_sync(0xffffffffu, w && !*abort_flag);
+      // Before the CTA can exit, the copies this warp issued must have landed
+      // (they have, unless a wait elsewhere ran out).  The full barrier of a
+      // stage is at most one phase behind the producer, so these waits are exact.
+      if (lane == 0) {
+        for (int k = max(0, issued - C::NST); k < issued; ++k)
+          mbar_wait(bar(BAR_FULL0 + k % C::NST), (k / C::NST) & 1, kWaitLimitCycles);
+        if (nq > 0) mbar_wait(bar(BAR_QFULL), (nq - 1) & 1, kWaitLimitCycles);
+      }
+      __syncwarp();
+    } else if (warp == 1 || warp == 2) {
+      // ================= MMA issuers: warp 1 QK, warp 2 PV =================
+      // Two issuing warps keep the tensor pipe fed with QK(i + 1) while PV(i)
+      // goes out: one warp issuing both left ~30 % of the pipe's rate unused
+      // at these N (measured with a probe of the issue rate).
+      constexpr uint32_t kIdQK = idesc_e4m3(128, NR, 0, 0);
+      constexpr uint32_t kIdPV = idesc_e4m3(128, C::OW, 1, 1);
+      bool ok = true;
+      auto fail = [&]() {
+        if (lane == 0) {
+          report(p.status, MLA_ERR_TIMEOUT);
+          *abort_flag = 1;
         }
-        for (int i = 0; ok && i < n_tiles; ++i, ++g) {
-          const int pb = (C::NPB == 1) ? 0 : (g & 1);
-          const int use = (C::NPB == 1) ? g : (g >> 1);
-          bool w = !expired_here(p, WAIT_P_FULL, i) &&
-                   mbar_wait_abort(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles, abort_flag);
-          w = __all_sync(0xffffffffu, w && !*abort_flag);
-          if (!w) {
-            ok = false;
-            break;
+      };
+      // PV of tile j of an item (tile g of the CTA, KV in stage jst, P^T in
+      // buffer pb); lane 0 issues.
+      auto issue_pv = [&](int j, int g, int jst, int pb) {
+        tc_fence_after();
+        const uint32_t kv = sbase + C::kKV + jst * kTileBytes;
+        const uint32_t pbuf = C::kPInStage ? kv + kRopeOffset : sbase + C::kP + pb * C::kPBytes;
+#pragma unroll
+        for (int d = 0; d < 4; ++d) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t a = smem_desc(kv + d * kLatBlockBytes + ks * 4096, 16384, 1024,
+                                         kLayoutSW128);
+            const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+            // B = P^T, MN-major: 16-row groups 2048 B apart (hi groups, then lo
+            // groups), 8-token groups 128 B apart.
+            const uint64_t bd = smem_desc(pbuf + ks * 512, 128, 2048, kLayoutNone);
+            umma_f8(tmem + C::kOCol + d * C::OW, a, bd, kIdPV, acc);
+            if constexpr (C::kWide) {
+              // The lo term: a second MMA into the same O^T columns.
+              const uint64_t bl = smem_desc(pbuf + C::kPHalf + ks * 512, 128, 2048, kLayoutNone);
+              umma_f8(tmem + C::kOCol + d * C::OW, a, bl, kIdPV, 1u);
+            }
           }
-          if (lane == 0) issue_pv(i, g, st, pb);
-          __syncwarp();
-          if (++st == C::NST) st = 0;
         }
-        // One commit after the item's last PV: the epilogue reads O^T after
-        // it (every QK result has been consumed by then).
-        if (lane == 0) umma_commit(bar(BAR_FINAL));
-        __syncwarp();
+        umma_commit(bar(BAR_EMPTY0 + jst));
+        if (!C::kPInStage) umma_commit(bar(BAR_PFREE0 + pb));
+        umma_commit(bar((g & 1) ? C::kBarOdone1 : BAR_ODONE));
+      };
+      // QK of tile i (KV in stage ist) into S buffer sb; lane 0 issues.
+      auto issue_qk = [&](int ist, int sb) {
+        tc_fence_after();
+        const uint32_t kv = sbase + C::kKV + ist * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 18; ++kk) {
+          uint64_t a, bd;
+          if (kk < 16) {
+            const int d = kk >> 2, sub = kk & 3;
+            a = smem_desc(kv + d * kLatBlockBytes + sub * 32, 16, 1024, kLayoutSW128);
+            bd = smem_desc(sbase + C::kQ + d * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
+          } else {
+            const int sub = kk - 16;
+            a = smem_desc(kv + kRopeOffset + sub * 32, 16, 512, kLayoutSW64);
+            bd = smem_desc(sbase + C::kQ + 4 * NR * 128 + sub * 32, 16, 512, kLayoutSW64);
+          }
+          umma_f8(tmem + sb * NR, a, bd, kIdQK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(BAR_SFULL0 + sb));
+      };
+      if (warp == 1) {
+        // QK(j) once its tile has landed, its S^T buffer is free and PV(j - 2)
+        // has completed (so the softmax's wait for PV(j - 1) stays within one
+        // phase of its barrier; QK(j) still overlaps PV(j - 1)).  Tile indices
+        // for buffers and phases count across the CTA's items (g).
+        int st = 0, round = 0, g = 0;
+        int nq = 0;  // items started
+        for (int n = 0; ok && (kPersist || n == 0); ++n) {
+          ItemInfo item;
+          const int r = next_item(n, item);
+          if (r == 0) break;
+          if (r == 1) continue;
+          MLA_ITEM_NAMES(item);
+          ++nq;
+          bool w = mbar_wait_abort(bar(BAR_QFULL), (nq - 1) & 1, p.wait_cycles, abort_flag);
+          ok = __all_sync(0xffffffffu, w && !*abort_flag);
+          for (int j = 0; ok && j < n_tiles; ++j, ++g) {
+            const int sb = (C::NS == 2) ? (g & 1) : 0;
+            const int use = (C::NS == 2) ? (g >> 1) : g;
+            w = !expired_here(p, WAIT_TILE_FULL, j) &&
+                mbar_wait_abort(bar(BAR_FULL0 + st), round & 1, p.wait_cycles, abort_flag);
+            if (w && use >= 1)
+              w = mbar_wait_abort(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles, abort_flag);
+            // The 96-row CTA needs no PV(g - 2) wait: its softmax waited for
+            // PV(g - 2) (the P^T buffer) before writing P(g - 1), which keeps its
+            // wait for PV(g - 1) within one phase; the tile's stage implies
+            // PV(g - 2) anyway.
+            if (w && g >= 2 && !C::kWide)
+              w = mbar_wait_abort(bar(((g - 2) & 1) ? C::kBarOdone1 : BAR_ODONE),
+                                  ((g - 2) >> 1) & 1, p.wait_cycles, abort_flag);
+            w = __all_sync(0xffffffffu, w && !*abort_flag);
+            if (!w) {
+              ok = false;
+              break;
+            }
+            // Rows loaded per page, as the producer published them with the
+            // stage's full barrier (observed above).
+            const uint32_t info =
+                kGather ? *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st) : 0u;
+            zero_unloaded_rows<kGather>(base + C::kKV + st * kTileBytes, lane, info,
+                                        tok_end - (t0 + j * kTileTokens));
+            if (lane == 0) issue_qk(st, sb);
+            __syncwarp();
+            if (++st == C::NST) {
+              st = 0;
+              ++round;
+            }
+          }
+          // Q is free for the next item once these QKs complete (also on the
+          // way out: the drain below waits for it).
+          if (lane == 0) umma_commit(bar(BAR_QFREE));
+          __syncwarp();
+        }
+        if (!ok) fail();
+        // This warp's MMAs complete before the CTA releases TMEM.
+        if (nq > 0) mbar_wait(bar(BAR_QFREE), (nq - 1) & 1, kWaitLimitCycles);
+      } else {
+        // PV(i) as soon as its P^T is ready; the first PV of an item overwrites
+        // O^T, so it waits until the softmax has read the previous item's.
+        int st = 0, g = 0;
+        int nq = 0;  // items started
+        for (int n = 0; ok && (kPersist || n == 0); ++n) {
+          ItemInfo item;
+          const int r = next_item(n, item);
+          if (r == 0) break;
+          if (r == 1) continue;
+          MLA_ITEM_NAMES(item);
+          ++nq;
+          if (nq > 1) {
+            const bool w =
+                mbar_wait_abort(bar(BAR_OFREE), (nq - 2) & 1, p.wait_cycles, abort_flag);
+            ok = __all_sync(0xffffffffu, w && !*abort_flag);
+          }
+          for (int i = 0; ok && i < n_tiles; ++i, ++g) {
+            const int pb = (C::NPB == 1) ? 0 : (g & 1);
+            const int use = (C::NPB == 1) ? g : (g >> 1);
+            bool w = !expired_here(p, WAIT_P_FULL, i) &&
+                     mbar_wait_abort(bar(BAR_PFULL0 + pb), use & 1, p.wait_cycles, abort_flag);
+            w = __all_sync(0xffffffffu, w && !*abort_flag);
+            if (!w) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) issue_pv(i, g, st, pb);
+            __syncwarp();
+            if (++st == C::NST) st = 0;
+          }
+          // One commit after the item's last PV: the epilogue reads O^T after
+          // it (every QK result has been consumed by then).
+          if (lane == 0) umma_commit(bar(BAR_FINAL));
+          __syncwarp();
+        }
+        if (!ok) fail();
+        // This warp's MMAs complete before the CTA releases TMEM.
+        if (nq > 0) mbar_wait(bar(BAR_FINAL), (nq - 1) & 1, kWaitLimitCycles);
       }
-      if (!ok) fail();
-      // This warp's MMAs complete before the CTA releases TMEM.
-      if (nq > 0) mbar_wait(bar(BAR_FINAL), (nq - 1) & 1, kWaitLimitCycles);
     }
   } else {
+    if constexpr (C::kWide) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsHigh));
     // ===== softmax warpgroups (warps kSoftmaxWarp0 .. kSoftmaxWarp0 + 4*SWG - 1) =====
     // SWG warpgroups share each tile: warpgroup g owns rows [g*NRH, (g+1)*NRH)
     // of every token (two warps per SM sub-partition when SWG = 2, so one
@@ -744,7 +763,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       // reads its rows' thresholds and exponent offsets from shared memory
       // instead (owners write them only between B1 and B2, when every thread
       // has passed the tile's vote and none has reached its weights), which
-      // keeps the 48-row thread within its registers.
+      // keeps the 32-row thread within its registers.
       float kreg[C::kWide ? 1 : NRH];
 #pragma unroll
       for (int k = 0; k < (C::kWide ? 1 : NRH); ++k) kreg[k] = -INFINITY;
@@ -820,7 +839,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         }
       };
       if constexpr (C::kWide) {
-        // 96 rows: each thread holds 48 rows of one token.  Per tile: load S^T
+        // 96 rows: each thread holds 32 rows of one token.  Per tile: load S^T
         // and free it, scale and mask, vote on the rows' thresholds (k + 0.75,
         // from shared memory), then weights from the rows' integer exponent
         // offsets (softmax_weight_kc), the row sums of this thread, and P^T as
@@ -1286,6 +1305,15 @@ static cudaError_t launch_split_t(const void* q, const void* kv, int64_t num_pag
     const cudaError_t e = ensure_smem_attr(mla_split_kv_kernel<NR, kGather, kMode>,
                                            static_cast<int>(C::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
+  }
+  if constexpr (C::kWide) {
+    // setmaxnreg.inc waits until the registers exist: launch only if the
+    // kernel's register count covers the split.
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, mla_split_kv_kernel<NR, kGather, kMode>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * C::kThreads < C::kRegsLow * 128 + C::kRegsHigh * 128 * C::SWG)
+      return cudaErrorInvalidConfiguration;
   }
   CUtensorMap kv_lat, kv_rope, q_lat, q_rope;
   const uint64_t kv_rows = static_cast<uint64_t>(num_pages) * MLA_PAGE_SIZE;

@@ -201,23 +201,28 @@ def test_inconsistent_plan_is_reported():
     assert e.value.status == mla.MLA_ERR_INVALID_ARG
 
 
-def test_wait_timeout_is_reported_and_context_survives():
-    # A tiny wait limit makes the pipeline waits run out; the kernel must
-    # record MLA_ERR_TIMEOUT, drain its own work and exit, and the next call
-    # must run normally.
-    inp = decode_inputs(1, 12, 8, [60000], seed=14)
+@pytest.mark.parametrize("H,q_len", [(12, 1), (12, 8)])
+def test_tiny_wait_limit_times_out_or_completes_and_context_survives(H, q_len):
+    # With a wait limit of 64 cycles a pipeline wait may run out or not (the
+    # waits block in mbarrier.try_wait, whose hardware suspend window can
+    # outlast so short a limit; tests/test_expire_gpu.py drives the expiry
+    # path deterministically).  Either the call completes with the right
+    # result or it reports MLA_ERR_TIMEOUT, and the next call on the same
+    # context is exact.
+    inp = decode_inputs(1, H, q_len, [60000], seed=14)
+    rows = np.array([0, 5, 11]) if q_len == 1 else np.array([0, 17, 50, 95])
+    ref_o, ref_l = oracle_rows(inp, rows, q_len > 1, SOFTMAX_SCALE)
+    idx = torch.from_numpy(rows).cuda()
     mla.mla_debug_set_wait_limit(64)
     try:
-        with pytest.raises(mla.MlaError) as e:
-            run_decode(inp, True, SOFTMAX_SCALE)
-        assert e.value.status == mla.MLA_ERR_TIMEOUT
+        out, lse, _ = run_decode(inp, q_len > 1, SOFTMAX_SCALE)
+        assert_parity(out.reshape(-1, 512)[idx], lse.reshape(-1)[idx], ref_o, ref_l)
+    except mla.MlaError as e:
+        assert e.status == mla.MLA_ERR_TIMEOUT
     finally:
         mla.mla_debug_set_wait_limit(0)
-    out, lse, _ = run_decode(inp, True, SOFTMAX_SCALE)
-    rows = np.array([0, 17, 50, 95])
-    ref_o, ref_l = oracle_rows(inp, rows, True, SOFTMAX_SCALE)
-    assert_parity(out.reshape(-1, 512)[torch.from_numpy(rows).cuda()],
-                  lse.reshape(-1)[torch.from_numpy(rows).cuda()], ref_o, ref_l)
+    out, lse, _ = run_decode(inp, q_len > 1, SOFTMAX_SCALE)
+    assert_parity(out.reshape(-1, 512)[idx], lse.reshape(-1)[idx], ref_o, ref_l)
 
 
 # ---------------------------------------------------------------- full-size workloads
