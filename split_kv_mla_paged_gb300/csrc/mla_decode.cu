@@ -107,9 +107,15 @@ struct Cfg {
   static constexpr uint32_t kPHalf = NR * kTileTokens;  // one E4M3 term of P^T
   static constexpr uint32_t kPBytes = 2 * kPHalf;       // hi + lo
   // Reductions: tile maxima 16 NR B, row sums 32 NR B (double-buffered by
-  // tile parity; 16 NR B, one buffer, with per-thread sums), references 4 NR B.
-  static constexpr uint32_t kRedSumBytes = kWide ? 16 * NR : 32 * NR;
-  static constexpr uint32_t kAuxBytes = 192 + 20 * NR + kRedSumBytes + (kWide ? 4 * NR : 0);
+  // tile parity; with per-thread sums, 96 rows, the once-per-item reduction
+  // shares the tile maxima's buffer), references 4 NR B.
+  static constexpr uint32_t kRedSumBytes = kWide ? 0 : 32 * NR;
+  // 96 rows: the KV stages are filled and released per block (rope, then the
+  // four 128-dim latent blocks), each with its own full and empty barrier.
+  static constexpr bool kBlockStages = kWide;
+  static constexpr uint32_t kBlkBarBytes = kBlockStages ? 2 * 2 * 5 * 8 : 0;
+  static constexpr uint32_t kAuxBytes =
+      192 + 20 * NR + kRedSumBytes + (kWide ? 4 * NR : 0) + kBlkBarBytes;
   static constexpr uint32_t kQBytes = NR * MLA_HEAD_DIM;
   // Three KV stages fit when P^T can live in the rope block of its own stage
   // (QK has consumed that block before P is written): NR = 16.  Otherwise two
@@ -139,12 +145,18 @@ struct Cfg {
   // Row owner r reads red_max[.][r] before writing alpha[r]: alpha reuses
   // red_max's first row.
   static constexpr uint32_t kAlpha = kRedMax;           // NR floats
-  static constexpr uint32_t kRedSum = kRedMax + 16 * NR;  // (2 x) 4 x NR floats
-  static constexpr uint32_t kKref = kRedSum + kRedSumBytes;  // NR floats
+  // (2 x) 4 x NR floats; 96 rows: the tile maxima's buffer.  Each warpgroup
+  // writes its own rows' slots of either, so one warpgroup's sums and
+  // another's tile maxima never meet.
+  static constexpr uint32_t kRedSum = kWide ? kRedMax : kRedMax + 16 * NR;
+  static constexpr uint32_t kKref = kRedMax + 16 * NR + kRedSumBytes;  // NR floats
   // 96 rows: kref holds each row's vote threshold k + 0.75, and kKci its
   // integer exponent offset for softmax_weight_kc (NR ints).
   static constexpr uint32_t kKci = kKref + 4 * NR;
-  static constexpr uint32_t kEnd = kKci + (kWide ? 4 * NR : 0);
+  // Block barriers: full (stage s, block b) at 8 (5 s + b), empty at 8 (10 + 5 s + b).
+  static constexpr uint32_t kBlkBars = kKci + (kWide ? 4 * NR : 0);
+  static_assert(kBlkBars % 8 == 0, "mbarrier alignment");
+  static constexpr uint32_t kEnd = kBlkBars + kBlkBarBytes;
   static_assert(kEnd - kAux <= kAuxBytes, "aux layout");
   static_assert(NR != 16 || NST == 3, "16-row CTAs must keep three KV stages");
   static constexpr uint32_t kSmemBytes = kEnd + 1024;   // + alignment slack
@@ -354,6 +366,14 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(base);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kBars + 8u * i; };
+  // Block barriers (kBlockStages): block b of stage s, b = 0..3 the latent
+  // blocks, 4 the rope block.
+  auto full_blk = [&](int st, int b) -> uint32_t { return sbase + C::kBlkBars + 8u * (5 * st + b); };
+  auto empty_blk = [&](int st, int b) -> uint32_t {
+    return sbase + C::kBlkBars + 8u * (10 + 5 * st + b);
+  };
+  (void)full_blk;
+  (void)empty_blk;
   volatile int* flags = reinterpret_cast<volatile int*>(base + C::kFlags);
   volatile int* abort_flag = flags + 2;
   float* red_max = reinterpret_cast<float*>(base + C::kRedMax);
@@ -368,6 +388,13 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     for (int k = 0; k < C::NST; ++k) {
       mbar_init(bar(BAR_FULL0 + k), 1);
       mbar_init(bar(BAR_EMPTY0 + k), 1);
+    }
+    if constexpr (C::kBlockStages) {
+      for (int k = 0; k < C::NST; ++k)
+        for (int b = 0; b < 5; ++b) {
+          mbar_init(full_blk(k, b), 1);
+          mbar_init(empty_blk(k, b), 1);
+        }
     }
     mbar_init(bar(BAR_QFULL), 1);
     mbar_init(bar(BAR_SFULL0), 1);
@@ -418,6 +445,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       const uint64_t pol = l2_policy_evict_first();
       volatile uint32_t* stage_info = reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo);
       int issued = 0;  // tiles issued, all items
+      int armed_part = 0;  // block stages: blocks out of a tile cut short by a failed wait
       int st = 0, round = 0;
       int nq = 0;      // items whose Q was loaded
       bool ok = true;
@@ -508,7 +536,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
             window_next = load_window((i >> 3) + 1, window_next_nv);
           }
           ok = !expired_here(p, WAIT_STAGE_FREE, i);
-          if (ok && round > 0)
+          if (ok && round > 0 && !C::kBlockStages)
             ok = mbar_wait_abort(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles, abort_flag);
           ok = __all_sync(0xffffffffu, ok && !*abort_flag);
           if (!ok) {
@@ -538,24 +566,65 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
             my_load = tp0 + (lane & 3) < page_end;
           }
           const int nload = __popc(__ballot_sync(0xffffffffu, lane < 4 && my_load));
-          const uint32_t fb = bar(BAR_FULL0 + st);
-          if (lane == 0) {
-            if constexpr (kGather) stage_info[st] = info;
-            mbar_arrive_expect_tx(fb, nload * kPageBytes);
-          }
-          __syncwarp();
-          // Lanes 0-3 issue one page each (5 boxes: 4 latent blocks + rope).
-          if (lane < 4 && my_load) {
-            const uint32_t kv = sbase + C::kKV + st * kTileBytes;
-            const int row = my_page * MLA_PAGE_SIZE;
+          const uint32_t kv = sbase + C::kKV + st * kTileBytes;
+          const int row = my_page * MLA_PAGE_SIZE;
+          if constexpr (C::kBlockStages) {
+            // Block by block as the previous tile of this stage releases them:
+            // the rope block after its QK, latent block d after its PV block d.
+            // The rows-loaded word goes out with the first block's barrier.
+            int armed = 0;  // blocks of this tile whose copies are out
+#pragma unroll 1
+            for (int bi = 0; bi < 5; ++bi) {
+              const int blk = (bi == 0) ? 4 : bi - 1;
+              if (round > 0) {
+                ok = mbar_wait_abort(empty_blk(st, blk), (round - 1) & 1, p.wait_cycles,
+                                     abort_flag);
+                ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+                if (!ok) break;
+              }
+              const uint32_t fb = full_blk(st, blk);
+              if (lane == 0) {
+                if (kGather && bi == 0) stage_info[st] = info;
+                mbar_arrive_expect_tx(fb, nload * (blk == 4 ? kPageRopeBytes : kPageLatBytes));
+              }
+              __syncwarp();
+              if (lane < 4 && my_load) {
+                if (blk == 4)
+                  tma_load_2d_hint(kv + kRopeOffset + lane * kPageRopeBytes, &tm_kv_rope,
+                                   MLA_LATENT_DIM, row, fb, pol);
+                else
+                  tma_load_2d_hint(kv + blk * kLatBlockBytes + lane * kPageLatBytes, &tm_kv_lat,
+                                   blk * 128, row, fb, pol);
+              }
+              __syncwarp();
+              ++armed;
+            }
+            if (!ok) {
+              if (lane == 0) {
+                report(p.status, MLA_ERR_TIMEOUT);
+                *abort_flag = 1;
+              }
+              armed_part = armed;  // drained below
+              break;
+            }
+          } else {
+            const uint32_t fb = bar(BAR_FULL0 + st);
+            if (lane == 0) {
+              if constexpr (kGather) stage_info[st] = info;
+              mbar_arrive_expect_tx(fb, nload * kPageBytes);
+            }
+            __syncwarp();
+            // Lanes 0-3 issue one page each (5 boxes: 4 latent blocks + rope).
+            if (lane < 4 && my_load) {
 #pragma unroll
-            for (int d = 0; d < 4; ++d)
-              tma_load_2d_hint(kv + d * kLatBlockBytes + lane * kPageLatBytes, &tm_kv_lat, d * 128,
-                               row, fb, pol);
-            tma_load_2d_hint(kv + kRopeOffset + lane * kPageRopeBytes, &tm_kv_rope, MLA_LATENT_DIM,
-                             row, fb, pol);
+              for (int d = 0; d < 4; ++d)
+                tma_load_2d_hint(kv + d * kLatBlockBytes + lane * kPageLatBytes, &tm_kv_lat,
+                                 d * 128, row, fb, pol);
+              tma_load_2d_hint(kv + kRopeOffset + lane * kPageRopeBytes, &tm_kv_rope,
+                               MLA_LATENT_DIM, row, fb, pol);
+            }
+            __syncwarp();
           }
-          __syncwarp();
           ++issued;
           if (++st == C::NST) {
             st = 0;
@@ -567,8 +636,21 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       // (they have, unless a wait elsewhere ran out).  The full barrier of a
       // stage is at most one phase behind the producer, so these waits are exact.
       if (lane == 0) {
-        for (int k = max(0, issued - C::NST); k < issued; ++k)
-          mbar_wait(bar(BAR_FULL0 + k % C::NST), (k / C::NST) & 1, kWaitLimitCycles);
+        for (int k = max(0, issued - C::NST); k < issued; ++k) {
+          if constexpr (C::kBlockStages) {
+            // Blocks of the stage re-armed for a tile cut short have landed
+            // for tile k (their release needed it); that tile's own blocks
+            // are one phase ahead, waited for after this loop.
+            const int skip = (k + C::NST == issued) ? armed_part : 0;
+            for (int bi = skip; bi < 5; ++bi)
+              mbar_wait(full_blk(k % C::NST, bi == 0 ? 4 : bi - 1), (k / C::NST) & 1,
+                        kWaitLimitCycles);
+          } else {
+            mbar_wait(bar(BAR_FULL0 + k % C::NST), (k / C::NST) & 1, kWaitLimitCycles);
+          }
+        }
+        for (int bi = 0; bi < armed_part; ++bi)
+          mbar_wait(full_blk(st, bi == 0 ? 4 : bi - 1), round & 1, kWaitLimitCycles);
         if (nq > 0) mbar_wait(bar(BAR_QFULL), (nq - 1) & 1, kWaitLimitCycles);
       }
       __syncwarp();
@@ -609,29 +691,34 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
               umma_f8(tmem + C::kOCol + d * C::OW, a, bl, kIdPV, 1u);
             }
           }
+          // Latent block d of the stage is free once these MMAs complete.
+          if constexpr (C::kBlockStages) umma_commit(empty_blk(jst, d));
         }
-        umma_commit(bar(BAR_EMPTY0 + jst));
+        if constexpr (!C::kBlockStages) umma_commit(bar(BAR_EMPTY0 + jst));
         if (!C::kPInStage) umma_commit(bar(BAR_PFREE0 + pb));
         umma_commit(bar((g & 1) ? C::kBarOdone1 : BAR_ODONE));
+      };
+      // One 32-dim K step of QK (KV in stage ist, S^T buffer sb): steps 0-15
+      // the latent blocks, 16-17 the rope block.
+      auto qk_step = [&](int ist, int sb, int kk, bool acc) {
+        const uint32_t kv = sbase + C::kKV + ist * kTileBytes;
+        uint64_t a, bd;
+        if (kk < 16) {
+          const int d = kk >> 2, sub = kk & 3;
+          a = smem_desc(kv + d * kLatBlockBytes + sub * 32, 16, 1024, kLayoutSW128);
+          bd = smem_desc(sbase + C::kQ + d * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
+        } else {
+          const int sub = kk - 16;
+          a = smem_desc(kv + kRopeOffset + sub * 32, 16, 512, kLayoutSW64);
+          bd = smem_desc(sbase + C::kQ + 4 * NR * 128 + sub * 32, 16, 512, kLayoutSW64);
+        }
+        umma_f8(tmem + sb * NR, a, bd, kIdQK, acc ? 1u : 0u);
       };
       // QK of tile i (KV in stage ist) into S buffer sb; lane 0 issues.
       auto issue_qk = [&](int ist, int sb) {
         tc_fence_after();
-        const uint32_t kv = sbase + C::kKV + ist * kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < 18; ++kk) {
-          uint64_t a, bd;
-          if (kk < 16) {
-            const int d = kk >> 2, sub = kk & 3;
-            a = smem_desc(kv + d * kLatBlockBytes + sub * 32, 16, 1024, kLayoutSW128);
-            bd = smem_desc(sbase + C::kQ + d * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
-          } else {
-            const int sub = kk - 16;
-            a = smem_desc(kv + kRopeOffset + sub * 32, 16, 512, kLayoutSW64);
-            bd = smem_desc(sbase + C::kQ + 4 * NR * 128 + sub * 32, 16, 512, kLayoutSW64);
-          }
-          umma_f8(tmem + sb * NR, a, bd, kIdQK, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 18; ++kk) qk_step(ist, sb, kk, kk > 0);
         umma_commit(bar(BAR_SFULL0 + sb));
       };
       if (warp == 1) {
@@ -653,8 +740,10 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           for (int j = 0; ok && j < n_tiles; ++j, ++g) {
             const int sb = (C::NS == 2) ? (g & 1) : 0;
             const int use = (C::NS == 2) ? (g >> 1) : g;
+            // Block stages: the rope block arrives first.
             w = !expired_here(p, WAIT_TILE_FULL, j) &&
-                mbar_wait_abort(bar(BAR_FULL0 + st), round & 1, p.wait_cycles, abort_flag);
+                mbar_wait_abort(C::kBlockStages ? full_blk(st, 4) : bar(BAR_FULL0 + st), round & 1,
+                                p.wait_cycles, abort_flag);
             if (w && use >= 1)
               w = mbar_wait_abort(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles, abort_flag);
             // The 96-row CTA needs no PV(g - 2) wait: its softmax waited for
@@ -673,10 +762,56 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
             // stage's full barrier (observed above).
             const uint32_t info =
                 kGather ? *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st) : 0u;
-            zero_unloaded_rows<kGather>(base + C::kKV + st * kTileBytes, lane, info,
-                                        tok_end - (t0 + j * kTileTokens));
-            if (lane == 0) issue_qk(st, sb);
-            __syncwarp();
+            const int valid = tok_end - (t0 + j * kTileTokens);
+            if constexpr (C::kBlockStages) {
+              // Rope steps first, then each latent block's four steps as it
+              // lands.  A tile with rows to zero (which span every block)
+              // waits for all of it first.
+              const bool partial = kGather ? (info != 0x20202020u) : (valid < kTileTokens);
+              if (partial) {
+                for (int blk = 0; w && blk < 4; ++blk)
+                  w = mbar_wait_abort(full_blk(st, blk), round & 1, p.wait_cycles, abort_flag);
+                w = __all_sync(0xffffffffu, w && !*abort_flag);
+                if (!w) {
+                  ok = false;
+                  break;
+                }
+                zero_unloaded_rows<kGather>(base + C::kKV + st * kTileBytes, lane, info, valid);
+              }
+              if (lane == 0) {
+                tc_fence_after();
+                qk_step(st, sb, 16, false);
+                qk_step(st, sb, 17, true);
+              }
+              __syncwarp();
+              for (int blk = 0; blk < 4; ++blk) {
+                if (!partial) {
+                  w = mbar_wait_abort(full_blk(st, blk), round & 1, p.wait_cycles, abort_flag);
+                  w = __all_sync(0xffffffffu, w && !*abort_flag);
+                  if (!w) break;
+                }
+                if (lane == 0) {
+                  tc_fence_after();
+#pragma unroll
+                  for (int sub = 0; sub < 4; ++sub) qk_step(st, sb, blk * 4 + sub, true);
+                }
+                __syncwarp();
+              }
+              if (!w) {
+                ok = false;
+                break;
+              }
+              // S^T is complete, and the rope block free, once these MMAs are.
+              if (lane == 0) {
+                umma_commit(bar(BAR_SFULL0 + sb));
+                umma_commit(empty_blk(st, 4));
+              }
+              __syncwarp();
+            } else {
+              zero_unloaded_rows<kGather>(base + C::kKV + st * kTileBytes, lane, info, valid);
+              if (lane == 0) issue_qk(st, sb);
+              __syncwarp();
+            }
             if (++st == C::NST) {
               st = 0;
               ++round;
@@ -745,7 +880,18 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     const int quad = warp & 3;
     const int rbase = ((warp - C::kSoftmaxWarp0) >> 2) * NRH;  // first row of this warpgroup
     const int tok_lane = quad * 32 + lane;  // TMEM lane == token index within the tile
-    const int sid = threadIdx.x - 32 * C::kSoftmaxWarp0;  // 0..NT-1, owner of row `sid` when < NR
+    const int sid = threadIdx.x - 32 * C::kSoftmaxWarp0;  // 0..NT-1
+    // Owner of a row's state (reference, sum): thread `sid` of row `sid` up to
+    // 48 rows; with 96 rows the first 32 threads of each warpgroup own its
+    // rows, so that a warpgroup's vote and reference update synchronise only
+    // its own 128 threads (named barriers per warpgroup).
+    const int wgi = (warp - C::kSoftmaxWarp0) >> 2;
+    const int own = C::kWide ? (((sid & 127) < NRH) ? rbase + (sid & 127) : -1)
+                             : (sid < NR ? sid : -1);
+    const uint32_t vote_bar = C::kWide ? kVoteBarrierWg0 + wgi : kVoteBarrier;
+    const uint32_t smx_bar = C::kWide ? kSoftmaxBarrierWg0 + wgi : kSoftmaxBarrier;
+    (void)vote_bar;
+    (void)smx_bar;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     int g = 0;   // tiles of the CTA's earlier items (S^T / P^T buffer phases)
     int nq = 0;  // items started
@@ -883,7 +1029,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
             over |= (t[4 * k4] > th.x) | (t[4 * k4 + 1] > th.y) | (t[4 * k4 + 2] > th.z) |
                     (t[4 * k4 + 3] > th.w);
           }
-          const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
+          const bool any_over = bar_sync_or(vote_bar, 128, over);
           if (any_over) {
             {
               float tm[NRH];
@@ -891,30 +1037,34 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
               for (int k = 0; k < NRH; ++k) tm[k] = t[k];
               warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
             }
-            if (sid == 0) flags[0] = 0;
-            named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
-            if (sid < NR) {
-              const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
-                                     fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
+            named_bar_sync(smx_bar, 128);  // B1: tile maxima ready
+            if (own >= 0) {
+              const float mt = fmaxf(fmaxf(red_max[own], red_max[NR + own]),
+                                     fmaxf(red_max[2 * NR + own], red_max[3 * NR + own]));
               float k_new = k_row;
               if (mt > k_row + 0.75f) k_new = ceilf(mt);
               float alpha = 1.0f;
               if (k_new != k_row && k_row != -INFINITY) {
                 const int e = static_cast<int>(k_row - k_new);
                 alpha = (e < -126) ? 0.0f : pow2i(e);
-                flags[0] = 1;
               }
               k_row = k_new;
-              thr[sid] = k_new + 0.75f;
-              kci[sid] = (k_new == -INFINITY) ? kKcNone
+              thr[own] = k_new + 0.75f;
+              kci[own] = (k_new == -INFINITY) ? kKcNone
                                               : 135 - 0x4B400000 - static_cast<int>(k_new);
-              alpha_s[sid] = alpha;
+              alpha_s[own] = alpha;
             }
-            named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
-            // This thread's sums follow their rows' references.
+            named_bar_sync(smx_bar, 128);  // B2: references ready
+            // This thread's sums follow their rows' references; a row whose
+            // reference moved needs its O^T columns rescaled (the same answer
+            // for every thread of the warpgroup).
+            bool corr = false;
 #pragma unroll
-            for (int k = 0; k < NRH; ++k) lsum[k] *= alpha_s[rbase + k];
-            const bool corr = flags[0] != 0;
+            for (int k = 0; k < NRH; ++k) {
+              const float al = alpha_s[rbase + k];
+              lsum[k] *= al;
+              corr |= al != 1.0f;
+            }
             if (ok && corr && i > 0) {
               // Rescale the O^T columns of rows whose reference moved (rare),
               // once PV(i - 1) is done (its completion barrier is within one
@@ -1159,19 +1309,19 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       named_bar_sync(kSoftmaxBarrier, NT);
       const bool single = (nsplit == 1);
       float* scale_s = alpha_s;
-      if (sid < NR) {
+      if (own >= 0) {
         if (n_tiles > 0) {
           const float* rs = red_sum + (C::kWide ? 0 : ((n_tiles - 1) & 1) * 4 * NR);
-          l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+          l_row += (rs[own] + rs[NR + own]) + (rs[2 * NR + own] + rs[3 * NR + own]);
         }
         const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
-        const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + sid;
+        const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + own;
         float sc = 0.0f;
-        if (sid < rows_here) {
+        if (own < rows_here) {
           if (single) {
             // A sink is one more (zero-valued) key: it joins the denominator.
             const float sink2 = p.sinks
-                                    ? p.sinks[(row0 + sid) % p.num_heads] * 1.4426950408889634f
+                                    ? p.sinks[(row0 + own) % p.num_heads] * 1.4426950408889634f
                                     : -INFINITY;
             const float mm = fmaxf(l_row > 0.0f ? m_s : -INFINITY, sink2);
             const float a = (l_row > 0.0f) ? exp2f(m_s - mm) : 0.0f;
@@ -1186,12 +1336,12 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
             sc = kv_scale;
           }
         }
-        scale_s[sid] = sc;
+        scale_s[own] = sc;
         // The 96-row configuration's thresholds and exponent offsets start the
         // next item with no reference (every thread is past its last read).
         if constexpr (C::kWide) {
-          kref[sid] = -INFINITY;
-          reinterpret_cast<int*>(base + C::kKci)[sid] = kKcNone;
+          kref[own] = -INFINITY;
+          reinterpret_cast<int*>(base + C::kKci)[own] = kKcNone;
         }
       }
       named_bar_sync(kSoftmaxBarrier, NT);

@@ -18,6 +18,9 @@ namespace mla {
 constexpr long long kWaitLimitCycles = 4000000000LL;  // about 2 s at 2 GHz
 constexpr uint32_t kSoftmaxBarrier = 1;
 constexpr uint32_t kVoteBarrier = 2;
+// 96-row configuration: per-warpgroup vote and reference barriers (3 each).
+constexpr uint32_t kVoteBarrierWg0 = 3;
+constexpr uint32_t kSoftmaxBarrierWg0 = 6;
 
 struct DecodeParams {
   const int32_t* page_table;
