@@ -62,8 +62,23 @@ def measured_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def algorithmic_flops(lens, H: int, q_len: int, causal: bool, sel=None) -> int:
+    """QK over 576 dims and PV over 512 for every visible (row, key) pair:
+    2 * 1088 flop each.  A causal MTP row (query token qi of q) sees the
+    first L - q + qi + 1 keys; with a page selection, only the selected keys
+    among them."""
+    pairs = 0
+    for b, L in enumerate(lens):
+        for qi in range(q_len):
+            n_tok = L - q_len + qi + 1 if causal else L
+            keys = selected_keys(sel[b], L, n_tok) if sel is not None else min(L, n_tok)
+            pairs += H * keys
+    return 2 * 1088 * pairs
 
 
 def recorded_traffic(workload: str):
@@ -708,10 +723,31 @@ def main():
     e2e_us = max_over_ranks((time.perf_counter() - t0) * 1e6 / args.e2e_steps, dev)
 
     # ---- roofline of the dominant kernel (split-KV) ----
+    # HBM-bound unless the flop per KV byte is above the ridge of the MMA
+    # type's peak (E4M3: twice the measured bf16 burst, the nominal ratio of
+    # the dense rates), as for H96 q8 (768 rows per request).
     split_avg_s = split_us * 1e-6
     achieved = kv_bytes / split_avg_s / 1e9
     peaks = measured_peaks()
     traffic = recorded_traffic(args.workload)
+    flops = algorithmic_flops(lens, H, q_len, w["causal"], sel0 if is_sparse else None)
+    mma_peak = peaks["bf16_tflops"] * (1.0 if is_bf16 else 2.0)
+    ridge = mma_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    intensity = flops / kv_bytes
+    tflops = flops / split_avg_s / 1e12
+    hbm_line = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"]}
+    tensor_line = {"bound": "tensor", "achieved": tflops, "peak": mma_peak, "unit": "TFLOP/s",
+                   "frac": tflops / mma_peak,
+                   "peak_note": ("measured bf16 burst" if is_bf16 else
+                                 "2 x measured bf16 burst (nominal E4M3 / bf16 dense ratio)")}
+    roof = dict(tensor_line if intensity >= ridge else hbm_line)
+    roof.update({"traffic": traffic, "peak_source": peaks["source"],
+                 "flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
+                 "other": {k: v for k, v in (hbm_line if intensity >= ridge else tensor_line).items()
+                           if k in ("bound", "achieved", "peak", "unit", "frac")},
+                 "kernel": ("mla_split_kv_bf16_kernel (timed with its merge)"
+                            if is_bf16 else "mla_split_kv_kernel")})
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_rows > 0:
@@ -749,11 +785,7 @@ def main():
             "aggregate_kv_gbs": world * kv_bytes / (us_per_call * 1e-6) / 1e9,
             "split_kernel_us": split_us,
             "merge_kernel_us": merge_us,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": traffic, "peak_source": peaks["source"],
-                         "kernel": ("mla_split_kv_bf16_kernel (timed with its merge)"
-                                    if is_bf16 else "mla_split_kv_kernel")},
+            "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

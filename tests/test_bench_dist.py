@@ -3,6 +3,7 @@ maximum over ranks and rank 0 alone prints."""
 import os
 import socket
 
+import numpy as np
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
@@ -54,3 +55,15 @@ def test_dist_env_defaults(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("LOCAL_RANK", "1")
     assert bench.dist_env() == (2, 1, 1)
+
+
+def test_algorithmic_flops_counts_visible_pairs():
+    # QK over 576 dims and PV over 512: 2 * 1088 flop per visible (row, key).
+    assert bench.algorithmic_flops([4096], 12, 1, False) == 2 * 1088 * 12 * 4096
+    # Causal MTP block of 4 over L = 10: query token qi sees 10 - 4 + qi + 1 keys.
+    assert bench.algorithmic_flops([10], 2, 4, True) == 2 * 1088 * 2 * (7 + 8 + 9 + 10)
+    # Selected pages 0 and 2 of a 100-token request: keys 0-31 and 64-95.
+    sel = np.array([[0, 2, -1]])
+    assert bench.algorithmic_flops([100], 1, 1, False, sel) == 2 * 1088 * 64
+    # A causal row of a 70-token request sees keys 0-31 and 64-69 of them.
+    assert bench.algorithmic_flops([70], 1, 1, True, np.array([[0, 2]])) == 2 * 1088 * 38
