@@ -107,3 +107,28 @@ def test_graph_replay_reads_new_device_scale():
                                           num_heads=12, causal=False, softmax_scale=sm_scale)
         assert_parity(out, lse, ref_o, ref_l, what=f"softmax_scale {sm_scale}")
     mla.mla_decode_status(ws, stream)
+
+
+# Negative and zero scales on every FP8 kernel configuration (12 rows -> the
+# 16-row CTA, 20 -> 32, 40 -> 48, 96 -> the 96-row CTA, whose softmax keeps
+# scores unscaled and applies the scale's sign and magnitude separately).
+@pytest.mark.parametrize("H,q_len,causal", [(12, 1, False), (20, 1, False), (10, 4, True),
+                                            (12, 8, True)])
+@pytest.mark.parametrize("scales", [
+    dict(softmax_scale=-SOFTMAX_SCALE),
+    dict(softmax_scale=0.0),
+    dict(softmax_scale=SOFTMAX_SCALE, q_scale=-1.3, kv_scale=0.6),
+    dict(softmax_scale=0.09, q_scale=1.1, kv_scale=-0.7),
+])
+def test_negative_and_zero_scales(H, q_len, causal, scales):
+    lens = [3000, 1100]
+    inp = decode_inputs(2, H, q_len, lens, seed=60 + H + q_len)
+    q, kv, pt = _dev(inp)
+    for target in (0, 6):
+        plan = mla.mla_decode_plan(lens, H, q_len, target_ctas=target) if target else None
+        out, lse, _ = mla.decode(q, kv, pt, inp.kv_lens, num_heads=H, q_len=q_len,
+                                 causal=causal, plan=plan, **scales)
+        torch.cuda.synchronize()
+        ref_o, ref_l = oracle.decode_rows(inp.q, inp.kv, inp.page_table, inp.kv_lens,
+                                          q_len=q_len, num_heads=H, causal=causal, **scales)
+        assert_parity(out, lse, ref_o, ref_l)
