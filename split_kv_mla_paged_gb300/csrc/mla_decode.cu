@@ -1352,30 +1352,39 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
       if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
       if (ok && fin && n_tiles > 0) {
         tc_fence_after();
+        // Per latent block: every column of this warpgroup's rows (and their
+        // lo products up to 48 rows) in one batch of TMEM loads and one wait,
+        // then the stores.  Row k of the warpgroup goes to base + k * stride.
+        const int64_t grow0 = static_cast<int64_t>(b) * p.rows_per_req + row0 + rbase;
+        const int64_t stride = single ? MLA_LATENT_DIM
+                                      : static_cast<int64_t>(p.max_splits) * MLA_LATENT_DIM;
+        float* const obase = single ? nullptr
+                                    : p.ws_o + (grow0 * p.max_splits + split) * MLA_LATENT_DIM;
+        const int nrow = min(NRH, rows_here - rbase);  // rows of this warpgroup to store
 #pragma unroll 1
         for (int d = 0; d < 4; ++d) {
           const int dim = d * 128 + tok_lane;
+          uint32_t r[NRH], r2[C::kWide ? 1 : NRH];
+          const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + rbase;
 #pragma unroll
           for (int cc = 0; cc < NRH / 8; ++cc) {
-            uint32_t r[8], r2[8];
-            const uint32_t addr = tmem + lane_addr + C::kOCol + d * C::OW + rbase + cc * 8;
-            tmem_ld8(addr, r);
-            if constexpr (!C::kWide) tmem_ld8(addr + NR, r2);  // the lo term's product
-            tmem_ld_wait();
+            tmem_ld8(addr + cc * 8, *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
+            if constexpr (!C::kWide)  // the lo term's product
+              tmem_ld8(addr + NR + cc * 8, *reinterpret_cast<uint32_t(*)[8]>(&r2[cc * 8]));
+          }
+          tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int row = rbase + cc * 8 + k;
-              if (row < rows_here) {
-                const float o = C::kWide ? __uint_as_float(r[k])
-                                         : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
-                const float v = o * scale_s[row];
-                const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
-                if (single) {
-                  p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
-                  if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = v;
-                } else {
-                  p.ws_o[(grow * p.max_splits + split) * MLA_LATENT_DIM + dim] = v;
-                }
+          for (int k = 0; k < NRH; ++k) {
+            if (k < nrow) {
+              const float o = C::kWide ? __uint_as_float(r[k])
+                                       : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
+              const float v = o * scale_s[rbase + k];
+              if (single) {
+                const int64_t off = (grow0 + k) * MLA_LATENT_DIM + dim;
+                p.out[off] = __float2bfloat16_rn(v);
+                if (p.out_f32) p.out_f32[off] = v;
+              } else {
+                obase[k * stride + dim] = v;
               }
             }
           }
