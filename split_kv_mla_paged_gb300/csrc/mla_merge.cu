@@ -18,8 +18,14 @@
 namespace mla {
 
 // The merge of one (row, quarter of the latent dims): G thread groups over
-// the row's partials, U loads in flight per group.
-template <int G, int U>
+// the row's partials, U loads in flight per group.  kMaxFirst: each group
+// first takes the maximum m over its slots and then accumulates
+// exp2(m_s - max) O_s with no running rescale, so its loads carry no
+// dependence on the previous slot (the same numbers as the running form:
+// every rescale there is an exact power of two for the split kernel's
+// integer maxima); it pays one more round trip per group and serves rows
+// whose groups hold many slots.
+template <int G, int U, bool kMaxFirst>
 __device__ __forceinline__ void merge_body(const MergeParams& p) {
   __shared__ float sm_m[G];
   __shared__ float sm_l[G];
@@ -40,7 +46,16 @@ __device__ __forceinline__ void merge_body(const MergeParams& p) {
   const float* po = p.po + static_cast<int64_t>(row) * p.stride_s * MLA_LATENT_DIM + dim;
   float m = -INFINITY, l = 0.0f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = g; s0 < ns; s0 += G * U) {
+  if constexpr (kMaxFirst) {
+    // Lane k reads the (m, l) of slots g + G k, g + G (k + 32), ...
+    for (int s = g + G * lane; s < ns; s += G * 32) {
+      const float2 ml = *reinterpret_cast<const float2*>(pml + s * 2);
+      if (ml.y > 0.0f) m = fmaxf(m, ml.x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  }
+  for (int s0 = g; (!kMaxFirst || m != -INFINITY) && s0 < ns; s0 += G * U) {
     float mu[U], lu[U];
     float4 ou[U];
 #pragma unroll
@@ -55,16 +70,25 @@ __device__ __forceinline__ void merge_body(const MergeParams& p) {
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (mu[u] == -INFINITY) continue;  // empty slot or padding: weight 0
-      const float m_new = fmaxf(m, mu[u]);
-      const float a = exp2_exact_int(m - m_new);
-      const float w = exp2_exact_int(mu[u] - m_new);
-      l = l * a + lu[u] * w;
-      o.x = o.x * a + ou[u].x * w;
-      o.y = o.y * a + ou[u].y * w;
-      o.z = o.z * a + ou[u].z * w;
-      o.w = o.w * a + ou[u].w * w;
-      m = m_new;
+      if (mu[u] == -INFINITY) continue;  // empty slot or padding: weight 0 (O unread)
+      if constexpr (kMaxFirst) {
+        const float w = exp2_exact_int(mu[u] - m);
+        l += lu[u] * w;
+        o.x += ou[u].x * w;
+        o.y += ou[u].y * w;
+        o.z += ou[u].z * w;
+        o.w += ou[u].w * w;
+      } else {
+        const float m_new = fmaxf(m, mu[u]);
+        const float a = exp2_exact_int(m - m_new);
+        const float w = exp2_exact_int(mu[u] - m_new);
+        l = l * a + lu[u] * w;
+        o.x = o.x * a + ou[u].x * w;
+        o.y = o.y * a + ou[u].y * w;
+        o.z = o.z * a + ou[u].z * w;
+        o.w = o.w * a + ou[u].w * w;
+        m = m_new;
+      }
     }
   }
   if (G > 1) {
@@ -117,16 +141,16 @@ __device__ __forceinline__ void merge_body(const MergeParams& p) {
     p.lse[row] = empty ? -INFINITY : 0.6931471805599453f * (mm + log2f(den));
 }
 
-template <int G>
+template <int G, bool kMaxFirst>
 __global__ void __launch_bounds__(32 * G) mla_merge_kernel(const MergeParams p) {
-  merge_body<G, 4>(p);
+  merge_body<G, 4, kMaxFirst>(p);
 }
 
 // Grids of more than two 512-thread CTAs per SM: three per SM (at most 40
 // registers, two loads in flight per group instead of four), so that the
 // grid fits one wave.
 __global__ void __launch_bounds__(512, 3) mla_merge_many_kernel(const MergeParams p) {
-  merge_body<16, 2>(p);
+  merge_body<16, 2, false>(p);
 }
 
 // The merge is launched as a programmatic dependent of whatever precedes it
@@ -136,6 +160,11 @@ __global__ void __launch_bounds__(512, 3) mla_merge_many_kernel(const MergeParam
 // kMany (16 groups only): the one-wave kernel for many-row grids.
 template <int G, bool kMany = false>
 static cudaError_t launch_merge_g(const MergeParams& mp, cudaStream_t stream) {
+  // The max-first form where groups hold at least 8 slots and the grid has at
+  // least 96 rows: on the GB300 merge-only sweep and the decode workloads it
+  // is faster there (MTP B2 128K 6.9 -> 5.9 us, sparse q8 8.8 -> 7.8 us) and
+  // slower for short groups or few rows (12 rows x 147 splits 5.0 -> 5.3 us).
+  const bool max_first = mp.rows >= 96 && mp.stride_s >= 8 * G;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(mp.rows, 4);  // rows on x: no 65535 limit
   cfg.blockDim = dim3(32 * G);
@@ -150,7 +179,8 @@ static cudaError_t launch_merge_g(const MergeParams& mp, cudaStream_t stream) {
   if constexpr (kMany) {
     return cudaLaunchKernelEx(&cfg, mla_merge_many_kernel, mp);
   } else {
-    return cudaLaunchKernelEx(&cfg, mla_merge_kernel<G>, mp);
+    return max_first ? cudaLaunchKernelEx(&cfg, mla_merge_kernel<G, true>, mp)
+                     : cudaLaunchKernelEx(&cfg, mla_merge_kernel<G, false>, mp);
   }
 }
 
