@@ -4,21 +4,17 @@
 // geometry: 512 latent + 64 rope, page size 32, BF16 output).
 //
 // Differences from the FP8 kernel (mla_decode.cu):
-//  * A token row is 1152 bytes, so a KV tile is 64 tokens (73,728 B, the same
-//    stage size as 128 FP8 tokens) in nine 64-element blocks (8 latent + 1
-//    rope), each [64 tokens][128 B] with the 128-byte swizzle.
-//  * QK is tcgen05.mma kind::f16 with M = 64 tokens: D row 16q + i lands in
-//    TMEM lane 32q + i, so each softmax warp (quadrant q) owns 16 tokens in
-//    its lanes 0-15.  K = 16 elements per instruction, 36 per tile.
+//  * A token row is 1152 bytes, in nine 64-element blocks (8 latent + 1
+//    rope) of 128 B, each staged with the 128-byte swizzle.
+//  * QK and PV are tcgen05.mma kind::f16 (K = 16 elements per instruction;
+//    A and B of one type, so Q is BF16 too and there are no q/kv scales).
 //  * P is BF16 (8 mantissa bits, so one term is enough: |err| <= 2^-9 of a
-//    weight), written MN-major into the rope block of its own stage, which QK
-//    has consumed.  PV is M = 128 latent dims (two 64-element swizzle atoms),
-//    N = rows, K = 16 tokens, 16 instructions per tile.
-//  * Q is BF16 too (kind::f16 takes A and B of one type); there are no q/kv
-//    scales.  Partials have the FP8 kernel's layout, so the merge is shared.
-//  * Row groups of at most 16 rows run a variant with Q in TMEM (see
-//    mla_split_kv_bf16_q16_kernel below); the description above is the
-//    kernel for 32 and 48 rows.
+//    weight).  Partials have the FP8 kernel's layout, so the merge is shared.
+//  * Row groups of at most 16 rows (mla_split_kv_bf16_q16_kernel) keep Q in
+//    TMEM and stream 64-token tiles (73,728 B) through three stages; 32- and
+//    48-row groups (mla_split_kv_bf16_wide_kernel) use the FP8 kernel's
+//    swapped layout with 128-token tiles (147,456 B: one stage, released
+//    block by block).
 //  * As in the FP8 kernel, warp 1 issues QK and warp 2 PV, and PV
 //    completions alternate between two barriers by tile parity.
 #include <cuda.h>
@@ -87,10 +83,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // a in the low half
   return *reinterpret_cast<uint32_t*>(&v);
 }
-
-// PV(i) completion of the 32/48-row kernel alternates between BAR_ODONE and
-// this slot (P^T lives in the KV stages, so the P^T-free barriers are unused).
-constexpr int kBarOdone1B = BAR_PFREE1;
 
 // Rows of a staged 64-token tile (two pages) that hold no loaded key: pages
 // not loaded (past the split's end, outside a window, an unused selection
@@ -162,7 +154,7 @@ struct SplitRange {
   bool sparse;
 };
 
-template <bool kGather>
+template <bool kGather, int kTile = kTokB>
 __device__ __forceinline__ bool split_range(const DecodeParams& p, int b, int split,
                                             SplitRange& r) {
   r.L = p.kv_lens[b];
@@ -195,7 +187,7 @@ __device__ __forceinline__ bool split_range(const DecodeParams& p, int b, int sp
     if (r.win_lo >= r.tok_end)
       r.t0 = r.tok_end;
     else if (r.win_lo > r.tok_begin)
-      r.t0 = r.tok_begin + (r.win_lo - r.tok_begin) / kTokB * kTokB;
+      r.t0 = r.tok_begin + (r.win_lo - r.tok_begin) / kTile * kTile;
   }
   return true;
 }
@@ -249,575 +241,6 @@ __device__ __forceinline__ int bf16_window_page(const DecodeParams& p, const Spl
     }
   }
   return pg;
-}
-
-template <int NR>
-struct CfgB {
-  static_assert(NR % 16 == 0 && NR >= 16 && NR <= kMaxRowsPerCta, "NR");
-  static constexpr int NS = 2;  // S^T buffers
-  static constexpr uint32_t kTmemUsed = NS * NR + 4 * NR;
-  static constexpr uint32_t kTmemCols =
-      kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
-      : kTmemUsed <= 256 ? 256 : 512;
-  static constexpr uint32_t kOCol = NS * NR;
-  static constexpr int SWG = NR >= 32 ? 2 : 1;
-  static constexpr int NRH = NR / SWG;
-  static_assert(NRH % 8 == 0, "rows per softmax warpgroup");
-  // Warp 0 TMA, warp 1 QK issuer (and TMEM owner), warp 2 PV issuer, then
-  // the softmax warpgroups.
-  static constexpr int kThreads = 96 + 128 * SWG;
-  static constexpr uint32_t kPBytes = NR * kTokB * 2;  // BF16 P^T, in the rope block
-  static_assert(kPBytes <= kBlkBytesB, "P^T must fit the rope block");
-  static constexpr int NST = 2;
-  static constexpr uint32_t kQBytes = NR * kRowBytesB;
-  static constexpr uint32_t kAuxBytes = 176 + 52 * NR;
-  static constexpr uint32_t kKV = 0;
-  static constexpr uint32_t kQ = NST * kTileBytesB;
-  static constexpr uint32_t kAux = kQ + kQBytes;
-  static constexpr uint32_t kBars = kAux;
-  static constexpr uint32_t kTmemSlot = kAux + 136;
-  static constexpr uint32_t kFlags = kAux + 144;
-  static constexpr uint32_t kStageInfo = kAux + 160;  // NST x 4 B: rows loaded per page
-  static constexpr uint32_t kRedMax = kAux + 176;
-  static constexpr uint32_t kAlpha = kRedMax;
-  static constexpr uint32_t kRedSum = kRedMax + 16 * NR;
-  static constexpr uint32_t kKref = kRedSum + 32 * NR;
-  static constexpr uint32_t kEnd = kKref + 4 * NR;
-  static_assert(kEnd - kAux <= kAuxBytes, "aux layout");
-  static constexpr uint32_t kSmemBytes = kEnd + 1024;
-  static_assert(kSmemBytes <= 232448u, "shared memory");
-};
-
-// kGather: the variant for restricted key sets (key windows, selected pages),
-// where tiles may hold pages that are not loaded and every score is masked by
-// its key position; kItems: the CTA item list instead of the full grid.
-template <int NR, bool kGather, bool kItems>
-__global__ void __launch_bounds__(CfgB<NR>::kThreads, 1)
-    mla_split_kv_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
-                             const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
-  using C = CfgB<NR>;
-  const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
-  int b, split, grp;
-  if (!cta_coords<kItems>(p, ngroups, b, split, grp)) return;
-  if (split >= p.splits[b]) return;  // empty split slot of a shorter request
-  SplitRange sr;
-  if (!split_range<kGather>(p, b, split, sr)) return;
-  const int L = sr.L, nsplit = sr.nsplit, q_b = sr.q_b, tok_end = sr.tok_end, t0 = sr.t0;
-  const bool sparse = sr.sparse;
-  const float c_log2 =
-      p.sm_scale_dev ? *p.sm_scale_dev * 1.4426950408889634f : p.c_log2;
-  const int row0 = grp * p.rows_per_group;
-  const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
-  // Rows of real query tokens (the others are padding slots of a shorter
-  // query block: no key is visible to them).
-  const int rows_valid = max(0, min(rows_here, q_b * p.num_heads - row0));
-  const int n_tiles =
-      (rows_valid > 0 && tok_end > t0) ? (tok_end - t0 + kTokB - 1) / kTokB : 0;
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = smem_u32(base);
-  auto bar = [&](int i) -> uint32_t { return sbase + C::kBars + 8u * i; };
-  volatile int* flags = reinterpret_cast<volatile int*>(base + C::kFlags);
-  volatile int* abort_flag = flags + 2;
-  float* red_max = reinterpret_cast<float*>(base + C::kRedMax);
-  float* red_sum = reinterpret_cast<float*>(base + C::kRedSum);
-  float* kref = reinterpret_cast<float*>(base + C::kKref);
-  float* alpha_s = reinterpret_cast<float*>(base + C::kAlpha);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < C::NST; ++k) {
-      mbar_init(bar(BAR_FULL0 + k), 1);
-      mbar_init(bar(BAR_EMPTY0 + k), 1);
-    }
-    mbar_init(bar(BAR_QFULL), 1);
-    mbar_init(bar(BAR_SFULL0), 1);
-    mbar_init(bar(BAR_SFULL1), 1);
-    mbar_init(bar(BAR_SFREE0), 128 * C::SWG);
-    mbar_init(bar(BAR_SFREE1), 128 * C::SWG);
-    mbar_init(bar(BAR_PFULL0), 128 * C::SWG);
-    mbar_init(bar(BAR_PFULL1), 128 * C::SWG);
-    mbar_init(bar(BAR_ODONE), 1);
-    mbar_init(bar(kBarOdone1B), 1);
-    mbar_init(bar(BAR_FINAL), 2);  // one commit from each MMA warp
-    flags[0] = 0;
-    flags[1] = 0;
-    flags[2] = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(sbase + C::kTmemSlot, C::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + C::kTmemSlot);
-
-  if (warp == 0) {
-    // ================= TMA producer =================
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_kv);
-      tma_prefetch_desc(&tm_q);
-      const int qrow = b * p.rows_per_req + row0;
-      mbar_arrive_expect_tx(bar(BAR_QFULL), C::kQBytes);
-#pragma unroll
-      for (int d = 0; d < 9; ++d)
-        tma_load_2d(sbase + C::kQ + d * NR * 128, &tm_q, d * 64, qrow, bar(BAR_QFULL));
-    }
-    const uint64_t pol = l2_policy_evict_first();
-    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-    const int page0 = t0 / MLA_PAGE_SIZE;
-    const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
-    // Page ids of 16 tiles (32 pages) per window, one per lane, fetched a
-    // window ahead, with the rows of each page to load (0: not loaded).
-    int last_lp = -1;
-    int window_nv, window_next_nv;
-    int window = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, 0, lane, last_lp,
-                                           window_nv);
-    int window_next = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, 1, lane, last_lp,
-                                                window_next_nv);
-    volatile uint32_t* stage_info = reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo);
-    int issued = 0;
-    int st = 0, round = 0;
-    for (int i = 0; i < n_tiles; ++i) {
-      if (i > 0 && (i & 15) == 0) {
-        window = window_next;
-        window_nv = window_next_nv;
-        window_next = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, (i >> 4) + 1,
-                                                lane, last_lp, window_next_nv);
-      }
-      bool ok = !expired_here(p, WAIT_STAGE_FREE, i);
-      if (ok && round > 0)
-        ok = mbar_wait_abort(bar(BAR_EMPTY0 + st), (round - 1) & 1, p.wait_cycles, abort_flag);
-      ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-      if (!ok) {
-        if (lane == 0) {
-          report(p.status, MLA_ERR_TIMEOUT);
-          *abort_flag = 1;
-        }
-        break;
-      }
-      // Lane q (< 2) takes the id and the rows to load of the tile's page q;
-      // the rows per page go to the QK warp (which zeroes the rest) with the
-      // stage's full barrier.
-      const int src = (i & 15) * 2 + (lane & 1);
-      const int my_page = __shfl_sync(0xffffffffu, window, src);
-      const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
-      const int nv1 = __shfl_sync(0xffffffffu, my_nv, 1);
-      const bool my_load = my_nv > 0;
-      const int nload = __popc(__ballot_sync(0xffffffffu, lane < 2 && my_load));
-      const uint32_t fb = bar(BAR_FULL0 + st);
-      if (lane == 0) {
-        if constexpr (kGather)
-          stage_info[st] = static_cast<uint32_t>(my_nv) | (static_cast<uint32_t>(nv1) << 8);
-        mbar_arrive_expect_tx(fb, nload * kPageBytesB);
-      }
-      __syncwarp();
-      if (lane < 2 && my_load) {
-        const uint32_t kv = sbase + C::kKV + st * kTileBytesB;
-        const int row = my_page * MLA_PAGE_SIZE;
-#pragma unroll
-        for (int d = 0; d < 9; ++d)
-          tma_load_2d_hint(kv + d * kBlkBytesB + lane * kPageBlkBytesB, &tm_kv, d * 64, row, fb,
-                           pol);
-      }
-      __syncwarp();
-      issued = i + 1;
-      if (++st == C::NST) {
-        st = 0;
-        ++round;
-      }
-    }
-    if (lane == 0) {
-      for (int k = max(0, issued - C::NST); k < issued; ++k)
-        mbar_wait(bar(BAR_FULL0 + k % C::NST), (k / C::NST) & 1, kWaitLimitCycles);
-      mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
-    }
-    __syncwarp();
-  } else if (warp == 1 || warp == 2) {
-    // ================= MMA issuers: warp 1 QK, warp 2 PV =================
-    constexpr uint32_t kIdQK = idesc_bf16(64, NR, 0, 0);
-    constexpr uint32_t kIdPV = idesc_bf16(128, NR, 1, 1);
-    bool ok = (warp == 1) ? mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles) : true;
-    auto fail = [&]() {
-      if (lane == 0) {
-        report(p.status, MLA_ERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-    };
-    // PV of tile j (KV in stage jst; P^T in its rope block).
-    auto issue_pv = [&](int j, int jst) {
-      tc_fence_after();
-      const uint32_t kv = sbase + C::kKV + jst * kTileBytesB;
-      const uint32_t pbuf = kv + kRopeOffB;
-#pragma unroll
-      for (int d = 0; d < 4; ++d) {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          // A = V^T, MN-major: 64-element atoms 8 KB apart (latent blocks 2d,
-          // 2d + 1), 8-token groups 1 KB apart; 16 tokens per instruction.
-          const uint64_t a = smem_desc(kv + 2 * d * kBlkBytesB + ks * 2048, kBlkBytesB, 1024,
-                                       kLayoutSW128);
-          // B = P^T, MN-major, no swizzle: 8-row groups 1 KB apart, 8-token
-          // groups 128 B apart.
-          const uint64_t bd = smem_desc(pbuf + ks * 256, 128, 1024, kLayoutNone);
-          umma_bf16(tmem + C::kOCol + d * NR, a, bd, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
-        }
-      }
-      umma_commit(bar(BAR_EMPTY0 + jst));
-      umma_commit(bar((j & 1) ? kBarOdone1B : BAR_ODONE));
-    };
-    // QK of a tile (KV in stage ist) into S buffer sb.
-    auto issue_qk = [&](int ist, int sb) {
-      tc_fence_after();
-      const uint32_t kv = sbase + C::kKV + ist * kTileBytesB;
-#pragma unroll
-      for (int kk = 0; kk < 36; ++kk) {
-        const int d = kk >> 2, sub = kk & 3;
-        const uint64_t a = smem_desc(kv + d * kBlkBytesB + sub * 32, 16, 1024, kLayoutSW128);
-        const uint64_t bd =
-            smem_desc(sbase + C::kQ + d * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
-        umma_bf16(tmem + sb * NR, a, bd, kIdQK, kk > 0 ? 1u : 0u);
-      }
-      umma_commit(bar(BAR_SFULL0 + sb));
-    };
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) fail();
-    if (warp == 1) {
-      // QK(j) once its tile has landed, its S^T buffer is free and PV(j - 2)
-      // has completed (two stages: the tile's stage was freed by PV(j - 2)
-      // anyway; the wait keeps the softmax's PV(j - 1) wait exact).
-      int st = 0, round = 0;
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int use = j >> 1;
-        bool w = !expired_here(p, WAIT_TILE_FULL, j) &&
-                 mbar_wait_abort(bar(BAR_FULL0 + st), round & 1, p.wait_cycles, abort_flag);
-        if (w && use >= 1)
-          w = mbar_wait_abort(bar(BAR_SFREE0 + (j & 1)), (use - 1) & 1, p.wait_cycles,
-                              abort_flag);
-        if (w && j >= 2)
-          w = mbar_wait_abort(bar(((j - 2) & 1) ? kBarOdone1B : BAR_ODONE), ((j - 2) >> 1) & 1,
-                              p.wait_cycles, abort_flag);
-        w = __all_sync(0xffffffffu, w && !*abort_flag);
-        if (!w) {
-          ok = false;
-          break;
-        }
-        // Rows loaded per page, as the producer published them with the
-        // stage's full barrier (observed above).
-        const uint32_t info =
-            kGather ? *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo + 4 * st) : 0u;
-        zero_unloaded_rows_bf16<kGather>(base + C::kKV + st * kTileBytesB, lane, info,
-                                         tok_end - (t0 + j * kTokB));
-        if (lane == 0) issue_qk(st, j & 1);
-        __syncwarp();
-        if (++st == C::NST) {
-          st = 0;
-          ++round;
-        }
-      }
-    } else {
-      // PV(i) as soon as its P^T is ready.
-      int st = 0;
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        bool w = !expired_here(p, WAIT_P_FULL, i) &&
-                 mbar_wait_abort(bar(BAR_PFULL0 + (i & 1)), (i >> 1) & 1, p.wait_cycles,
-                                 abort_flag);
-        w = __all_sync(0xffffffffu, w && !*abort_flag);
-        if (!w) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) issue_pv(i, st);
-        __syncwarp();
-        if (++st == C::NST) st = 0;
-      }
-    }
-    if (!ok) fail();
-    if (lane == 0) umma_commit(bar(BAR_FINAL));
-    __syncwarp();
-    mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
-  } else {
-    // ================= softmax warpgroups =================
-    // As in the FP8 kernel, with the M = 64 S^T layout: warp quadrant q
-    // holds tokens 16q .. 16q + 15 in its lanes 0-15; lanes 16-31 carry no
-    // token (their scores are -inf and their weights 0).
-    constexpr int NRH = C::NRH;
-    constexpr int NT = 128 * C::SWG;
-    const int quad = warp & 3;
-    const int rbase = ((warp - 3) >> 2) * NRH;
-    const bool has_tok = lane < 16;
-    const int tok = quad * 16 + lane;       // token index within the tile (when has_tok)
-    const int dim_lane = quad * 32 + lane;  // TMEM lane for O^T (M = 128 layout)
-    const int sid = threadIdx.x - 96;
-    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    float k_row = -INFINITY;
-    float l_row = 0.0f;
-    float kreg[NRH];
-#pragma unroll
-    for (int k = 0; k < NRH; ++k) kreg[k] = -INFINITY;
-    const float c = c_log2;
-    const int qi_first = row0 / p.num_heads;
-    const int lim_min = p.causal ? min(tok_end, L - q_b + qi_first + 1) : tok_end;
-    const int my_row0 = row0 + rbase;
-    const int my_rows = max(0, min(NRH, rows_valid - rbase));
-    // Selection: logical page ids of 16 tiles' compact pages, one per lane
-    // (this thread's token lies in page quad / 2 of its tile).
-    auto sel_window = [&](int w) -> int {
-      const int cp = t0 / MLA_PAGE_SIZE + w * 32 + lane;
-      return (cp < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + cp] : -1;
-    };
-    int sel_cur = -1, sel_next = -1;
-    if (sparse) {
-      sel_cur = sel_window(0);
-      sel_next = sel_window(1);
-    }
-    bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int sb = i & 1;
-      const int use = i >> 1;
-      if (ok)
-        ok = !expired_here(p, WAIT_S_FULL, i) &&
-             mbar_wait_abort(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
-      float t[NRH];
-      if (ok) {
-        tc_fence_after();
-        uint32_t r[NRH];
-#pragma unroll
-        for (int cc = 0; cc < NRH / 8; ++cc)
-          tmem_ld8(tmem + lane_addr + sb * NR + rbase + cc * 8,
-                   *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
-        tc_fence_before();
-        mbar_arrive(bar(BAR_SFREE0 + sb));
-      } else {
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
-      }
-      const int tile_tok0 = t0 + i * kTokB;
-      const int j = tile_tok0 + tok;
-      if constexpr (kGather) {
-        // Restricted key sets: the token's key position decides.
-        int64_t pos = j;
-        bool tok_ok = has_tok && j < tok_end;
-        if (sparse) {
-          if (i > 0 && (i & 15) == 0) {
-            sel_cur = sel_next;
-            sel_next = sel_window((i >> 4) + 1);
-          }
-          const int lp = __shfl_sync(0xffffffffu, sel_cur, (i & 15) * 2 + (quad >> 1));
-          pos = static_cast<int64_t>(lp) * MLA_PAGE_SIZE + (quad & 1) * 16 + lane;
-          tok_ok = tok_ok && lp >= 0;
-        }
-        tok_ok = tok_ok && pos >= sr.win_lo && pos < sr.win_hi;
-        int qi = my_row0 / p.num_heads;
-        int h = my_row0 - qi * p.num_heads;
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) {
-          const bool vis = tok_ok && k < my_rows && (!p.causal || pos < L - q_b + qi + 1);
-          t[k] = vis ? t[k] * c : -INFINITY;
-          if (++h == p.num_heads) {
-            h = 0;
-            ++qi;
-          }
-        }
-      } else if (tile_tok0 + kTokB <= lim_min) {
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) t[k] = (has_tok && k < my_rows) ? t[k] * c : -INFINITY;
-      } else {
-        int qi = my_row0 / p.num_heads;
-        int h = my_row0 - qi * p.num_heads;
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) {
-          const int lim = p.causal ? min(tok_end, L - q_b + qi + 1) : tok_end;
-          t[k] = (has_tok && k < my_rows && j < lim) ? t[k] * c : -INFINITY;
-          if (++h == p.num_heads) {
-            h = 0;
-            ++qi;
-          }
-        }
-      }
-      bool over = false;
-#pragma unroll
-      for (int k = 0; k < NRH; ++k) over |= t[k] > kreg[k] + 0.75f;
-      const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
-      if (sid < NR && i > 0) {
-        const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
-        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
-      }
-      if (any_over) {
-        {
-          float tm[NRH];
-#pragma unroll
-          for (int k = 0; k < NRH; ++k) tm[k] = t[k];
-          warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
-        }
-        if (sid == 0) flags[0] = 0;
-        named_bar_sync(kSoftmaxBarrier, NT);
-        if (sid < NR) {
-          const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
-                                 fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
-          float k_new = k_row;
-          if (mt > k_row + 0.75f) k_new = ceilf(mt);
-          float alpha = 1.0f;
-          if (k_new != k_row && k_row != -INFINITY) {
-            const int e = static_cast<int>(k_row - k_new);
-            alpha = (e < -126) ? 0.0f : pow2i(e);
-            flags[0] = 1;
-          }
-          l_row *= alpha;
-          k_row = k_new;
-          kref[sid] = k_new;
-          alpha_s[sid] = alpha;
-        }
-        named_bar_sync(kSoftmaxBarrier, NT);
-#pragma unroll
-        for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
-        const bool corr = flags[0] != 0;
-        if (ok && corr && i > 0) {
-          // PV(i - 1) done; PV completions alternate between two barriers
-          // and the one of PV(i - 1)'s parity is within one phase of it.
-          ok = mbar_wait_abort(bar(((i - 1) & 1) ? kBarOdone1B : BAR_ODONE),
-                               ((i - 1) >> 1) & 1, p.wait_cycles, abort_flag);
-          ok = __all_sync(0xffffffffu, ok);
-          if (ok) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int d = 0; d < 4; ++d) {
-#pragma unroll
-              for (int cc = 0; cc < NRH / 8; ++cc) {
-                uint32_t r[8];
-                const uint32_t addr = tmem + lane_addr + C::kOCol + d * NR + rbase + cc * 8;
-                tmem_ld8(addr, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[rbase + cc * 8 + k]);
-                tmem_st8(addr, r);
-              }
-            }
-            tmem_st_wait();
-          }
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<(C::SWG > 1)>(t[k], kreg[k]);
-      if (ok) {
-        // P^T (BF16) into the rope block of this tile's stage, MN-major:
-        // [NR/8 row groups][64 tokens][8 rows].
-        uint8_t* pbuf = base + C::kKV + (i % C::NST) * kTileBytesB + kRopeOffB;
-        if (has_tok) {
-#pragma unroll
-          for (int g = 0; g < NRH / 8; ++g) {
-            uint4 v;
-            v.x = pack_bf16x2(t[g * 8 + 0], t[g * 8 + 1]);
-            v.y = pack_bf16x2(t[g * 8 + 2], t[g * 8 + 3]);
-            v.z = pack_bf16x2(t[g * 8 + 4], t[g * 8 + 5]);
-            v.w = pack_bf16x2(t[g * 8 + 6], t[g * 8 + 7]);
-            *reinterpret_cast<uint4*>(pbuf + ((rbase >> 3) + g) * 1024 + tok * 16) = v;
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar(BAR_PFULL0 + (i & 1)));
-      }
-      warp_reduce_rows<NRH, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR + rbase);
-    }
-    if (!ok && lane == 0) {
-      report(p.status, MLA_ERR_TIMEOUT);
-      *abort_flag = 1;
-    }
-    // ---- epilogue (as in the FP8 kernel; O^T has NR columns per block) ----
-    named_bar_sync(kSoftmaxBarrier, NT);
-    const bool single = (nsplit == 1);
-    float* scale_s = alpha_s;
-    if (sid < NR) {
-      if (n_tiles > 0) {
-        const float* rs = red_sum + ((n_tiles - 1) & 1) * 4 * NR;
-        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
-      }
-      const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
-      const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + sid;
-      float sc = 0.0f;
-      if (sid < rows_here) {
-        if (single) {
-          // A sink is one more (zero-valued) key: it joins the denominator.
-          const float sink2 = p.sinks
-                                  ? p.sinks[(row0 + sid) % p.num_heads] * 1.4426950408889634f
-                                  : -INFINITY;
-          const float mm = fmaxf(l_row > 0.0f ? m_s : -INFINITY, sink2);
-          const float a = (l_row > 0.0f) ? exp2f(m_s - mm) : 0.0f;
-          const float den = l_row * a + (sink2 == -INFINITY ? 0.0f : exp2f(sink2 - mm));
-          if (p.lse)
-            p.lse[grow] = (den > 0.0f) ? 0.6931471805599453f * (mm + log2f(den)) : -INFINITY;
-          sc = (den > 0.0f) ? p.output_scale * a / den : 0.0f;
-        } else {
-          float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
-          ml[0] = m_s;
-          ml[1] = l_row;
-          sc = 1.0f;
-        }
-      }
-      scale_s[sid] = sc;
-    }
-    named_bar_sync(kSoftmaxBarrier, NT);
-    bool fin = !expired_here(p, WAIT_FINAL, 0) && mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
-    fin = __all_sync(0xffffffffu, fin);
-    if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
-    if (ok && fin && n_tiles > 0) {
-      tc_fence_after();
-#pragma unroll 1
-      for (int d = 0; d < 4; ++d) {
-        const int dim = d * 128 + dim_lane;
-#pragma unroll
-        for (int cc = 0; cc < NRH / 8; ++cc) {
-          uint32_t r[8];
-          tmem_ld8(tmem + lane_addr + C::kOCol + d * NR + rbase + cc * 8, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int row = rbase + cc * 8 + k;
-            if (row < rows_here) {
-              const float v = __uint_as_float(r[k]) * scale_s[row];
-              const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
-              if (single) {
-                p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
-                if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = v;
-              } else {
-                p.ws_o[(grow * p.max_splits + split) * MLA_LATENT_DIM + dim] = v;
-              }
-            }
-          }
-        }
-      }
-    } else if (ok && fin && n_tiles == 0 && single) {
-      // Only padding query slots here: O = 0 (partials need only (-inf, 0)).
-      for (int d = 0; d < 4; ++d) {
-        const int dim = d * 128 + dim_lane;
-        for (int row = rbase; row < min(rows_here, rbase + NRH); ++row) {
-          const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
-          p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(0.0f);
-          if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = 0.0f;
-        }
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
-  }
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -1372,6 +795,686 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------------------------------
+// 32- and 48-row groups with 128-token tiles
+// ---------------------------------------------------------------------------
+// The swapped layout of the FP8 kernel (M = 128 tokens, TMEM lane = token,
+// every lane of a softmax warp holds a token) with BF16 operands.  A 128-token
+// BF16 tile is 147,456 B, so the CTA holds one KV stage next to Q^T and two
+// P^T buffers, and releases it block by block: the rope block once QK has
+// read it, latent blocks 2d and 2d + 1 once PV's latent group d has, with a
+// full and an empty barrier per block; the producer refills each block for
+// the next tile as soon as it is free and QK issues each block's steps as
+// they land.  QK: 36 `kind::f16` instructions (K = 16) of N = NR per tile;
+// PV: 4 latent groups x 8 token slices of N = NR; P in one BF16 term, in its
+// own double buffer; S^T double-buffered in TMEM.
+namespace bw {
+constexpr int kTok = 128;                                  // tokens per tile
+constexpr uint32_t kBlk = kTok * 128;                      // 16,384: one 64-element block
+constexpr uint32_t kTile = 9 * kBlk;                       // 147,456: 8 latent blocks + rope
+constexpr int kRopeBlk = 8;
+}  // namespace bw
+
+template <int NR>
+struct CfgW {
+  static_assert(NR == 32 || NR == 48, "NR");
+  static constexpr int NS = 2;                     // S^T buffers
+  static constexpr uint32_t kOCol = NS * NR;       // O^T: 4 latent groups x NR columns
+  static constexpr uint32_t kTmemUsed = NS * NR + 4 * NR;
+  static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+  static constexpr int SWG = 2;
+  static constexpr int NRH = NR / SWG;
+  static_assert(NRH % 8 == 0, "rows per softmax warpgroup");
+  static constexpr int kThreads = 96 + 128 * SWG;
+  static constexpr uint32_t kQBytes = NR * kRowBytesB;
+  static constexpr uint32_t kPBytes = NR * bw::kTok * 2;  // one BF16 P^T buffer
+  static constexpr uint32_t kKV = 0;
+  static constexpr uint32_t kQ = bw::kTile;
+  static constexpr uint32_t kP = kQ + kQBytes;            // two P^T buffers
+  static constexpr uint32_t kAux = kP + 2 * kPBytes;
+  static_assert(kQ % 1024 == 0 && kP % 1024 == 0 && kAux % 1024 == 0, "alignment");
+  // aux: 19 mbarriers, TMEM slot, flags, rows loaded per page, reductions,
+  // then 18 block barriers (full: 8 b, empty: 8 (9 + b)).
+  static constexpr uint32_t kBars = kAux;
+  static constexpr uint32_t kTmemSlot = kAux + 152;
+  static constexpr uint32_t kFlags = kAux + 160;
+  static constexpr uint32_t kStageInfo = kAux + 176;
+  static constexpr uint32_t kRedMax = kAux + 192;  // 4 x NR floats (alpha reuses row 0)
+  static constexpr uint32_t kAlpha = kRedMax;
+  static constexpr uint32_t kRedSum = kRedMax + 16 * NR;  // 2 x 4 x NR floats
+  static constexpr uint32_t kKref = kRedSum + 32 * NR;
+  static constexpr uint32_t kBlkBars = kKref + 4 * NR;
+  static_assert(kBlkBars % 8 == 0, "mbarrier alignment");
+  static constexpr uint32_t kEnd = kBlkBars + 18 * 8;
+  static constexpr uint32_t kSmemBytes = kEnd + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448u, "shared memory");
+};
+// PV completions alternate between BAR_ODONE and this slot (the stage's
+// full/empty barriers are the block barriers).
+constexpr int kBarOdone1W = BAR_FULL0;
+
+// Rows of a staged 128-token tile (four pages) that hold no loaded key; the
+// warp zeroes all 1152 bytes of each (nine 128-byte blocks, 16 KB apart).
+// kGather: `info` holds the rows loaded per page (byte q for page q);
+// otherwise the first `valid` rows of the tile are keys of the split.
+template <bool kGather>
+__device__ __forceinline__ void zero_unloaded_rows_w(uint8_t* kvp, int lane, uint32_t info,
+                                                     int valid) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  auto zero_rows = [&](int r0, int nrow) {
+    for (int idx = lane; idx < nrow * 72; idx += 32) {
+      const int r = r0 + idx / 72;
+      const int c = idx % 72;
+      *reinterpret_cast<uint4*>(kvp + (c / 8) * bw::kBlk + r * 128 + (c % 8) * 16) = z;
+    }
+  };
+  bool any = false;
+  if constexpr (kGather) {
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      const int nv = static_cast<int>((info >> (8 * q)) & 0xFFu);
+      if (nv < MLA_PAGE_SIZE) {
+        zero_rows(q * MLA_PAGE_SIZE + nv, MLA_PAGE_SIZE - nv);
+        any = true;
+      }
+    }
+  } else if (valid < bw::kTok) {
+    zero_rows(valid, bw::kTok - valid);
+    any = true;
+  }
+  if (any) {
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+}
+
+template <int NR, bool kGather, bool kItems>
+__global__ void __launch_bounds__(CfgW<NR>::kThreads, 1)
+    mla_split_kv_bf16_wide_kernel(const __grid_constant__ CUtensorMap tm_kv,
+                                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+  using C = CfgW<NR>;
+  using bw::kTok;
+  const int ngroups = (p.rows_per_req + p.rows_per_group - 1) / p.rows_per_group;
+  int b, split, grp;
+  if (!cta_coords<kItems>(p, ngroups, b, split, grp)) return;
+  if (split >= p.splits[b]) return;  // empty split slot of a shorter request
+  SplitRange sr;
+  if (!split_range<kGather, kTok>(p, b, split, sr)) return;
+  const int L = sr.L, nsplit = sr.nsplit, q_b = sr.q_b, tok_end = sr.tok_end, t0 = sr.t0;
+  const bool sparse = sr.sparse;
+  const float c_log2 =
+      p.sm_scale_dev ? *p.sm_scale_dev * 1.4426950408889634f : p.c_log2;
+  const int row0 = grp * p.rows_per_group;
+  const int rows_here = min(p.rows_per_group, p.rows_per_req - row0);
+  // Rows of real query tokens (the others are padding slots of a shorter
+  // query block: no key is visible to them).
+  const int rows_valid = max(0, min(rows_here, q_b * p.num_heads - row0));
+  const int n_tiles =
+      (rows_valid > 0 && tok_end > t0) ? (tok_end - t0 + kTok - 1) / kTok : 0;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(base);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBars + 8u * i; };
+  // Block b of the stage: b = 0..7 latent blocks of 64 elements, 8 rope.
+  auto full_blk = [&](int blk) -> uint32_t { return sbase + C::kBlkBars + 8u * blk; };
+  auto empty_blk = [&](int blk) -> uint32_t { return sbase + C::kBlkBars + 8u * (9 + blk); };
+  volatile int* flags = reinterpret_cast<volatile int*>(base + C::kFlags);
+  volatile int* abort_flag = flags + 2;
+  float* red_max = reinterpret_cast<float*>(base + C::kRedMax);
+  float* red_sum = reinterpret_cast<float*>(base + C::kRedSum);
+  float* kref = reinterpret_cast<float*>(base + C::kKref);
+  float* alpha_s = reinterpret_cast<float*>(base + C::kAlpha);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < 9; ++k) {
+      mbar_init(full_blk(k), 1);
+      mbar_init(empty_blk(k), 1);
+    }
+    mbar_init(bar(BAR_QFULL), 1);
+    mbar_init(bar(BAR_SFULL0), 1);
+    mbar_init(bar(BAR_SFULL1), 1);
+    mbar_init(bar(BAR_SFREE0), 128 * C::SWG);
+    mbar_init(bar(BAR_SFREE1), 128 * C::SWG);
+    mbar_init(bar(BAR_PFULL0), 128 * C::SWG);
+    mbar_init(bar(BAR_PFULL1), 128 * C::SWG);
+    mbar_init(bar(BAR_PFREE0), 1);
+    mbar_init(bar(BAR_PFREE1), 1);
+    mbar_init(bar(BAR_ODONE), 1);
+    mbar_init(bar(kBarOdone1W), 1);
+    mbar_init(bar(BAR_FINAL), 2);  // one commit from each MMA warp
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + C::kTmemSlot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + C::kTmemSlot);
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_kv);
+      tma_prefetch_desc(&tm_q);
+      const int qrow = b * p.rows_per_req + row0;
+      mbar_arrive_expect_tx(bar(BAR_QFULL), C::kQBytes);
+#pragma unroll
+      for (int d = 0; d < 9; ++d)
+        tma_load_2d(sbase + C::kQ + d * NR * 128, &tm_q, d * 64, qrow, bar(BAR_QFULL));
+    }
+    const uint64_t pol = l2_policy_evict_first();
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+    const int page0 = t0 / MLA_PAGE_SIZE;
+    const int page_end = (tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;  // exclusive
+    // Page ids of 8 tiles (32 pages) per window, one per lane, fetched a
+    // window ahead, with the rows of each page to load (0: not loaded).
+    int last_lp = -1;
+    int window_nv, window_next_nv;
+    int window = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, 0, lane, last_lp,
+                                           window_nv);
+    int window_next = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, 1, lane, last_lp,
+                                                window_next_nv);
+    volatile uint32_t* stage_info = reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo);
+    int issued = 0;       // tiles whose nine blocks are out
+    int armed_part = 0;   // blocks out of a tile cut short by a failed wait
+    for (int i = 0; i < n_tiles; ++i) {
+      if (i > 0 && (i & 7) == 0) {
+        window = window_next;
+        window_nv = window_next_nv;
+        window_next = bf16_window_page<kGather>(p, sr, pt, b, page0, page_end, (i >> 3) + 1,
+                                                lane, last_lp, window_next_nv);
+      }
+      bool ok = !expired_here(p, WAIT_STAGE_FREE, i);
+      ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+      if (!ok) {
+        if (lane == 0) {
+          report(p.status, MLA_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      // Lane q (< 4) takes the id and the rows to load of the tile's page q;
+      // the rows per page go to the QK warp (which zeroes the rest) with the
+      // rope block's full barrier.
+      const int src = (i & 7) * 4 + (lane & 3);
+      const int my_page = __shfl_sync(0xffffffffu, window, src);
+      const int my_nv = __shfl_sync(0xffffffffu, window_nv, src);
+      const int nv1 = __shfl_sync(0xffffffffu, my_nv, 1);
+      const int nv2 = __shfl_sync(0xffffffffu, my_nv, 2);
+      const int nv3 = __shfl_sync(0xffffffffu, my_nv, 3);
+      const bool my_load = my_nv > 0;
+      const int nload = __popc(__ballot_sync(0xffffffffu, lane < 4 && my_load));
+      const uint32_t kv = sbase + C::kKV;
+      const int row = my_page * MLA_PAGE_SIZE;
+      // Rope first (free once QK(i - 1) is done), then latent blocks 0-7
+      // as PV(i - 1) releases them.
+      int armed = 0;
+#pragma unroll 1
+      for (int bi = 0; bi < 9; ++bi) {
+        const int blk = (bi == 0) ? bw::kRopeBlk : bi - 1;
+        if (i > 0) {
+          ok = mbar_wait_abort(empty_blk(blk), (i - 1) & 1, p.wait_cycles, abort_flag);
+          ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+          if (!ok) break;
+        }
+        const uint32_t fb = full_blk(blk);
+        if (lane == 0) {
+          if (kGather && bi == 0)
+            stage_info[0] = static_cast<uint32_t>(my_nv) | (static_cast<uint32_t>(nv1) << 8) |
+                            (static_cast<uint32_t>(nv2) << 16) |
+                            (static_cast<uint32_t>(nv3) << 24);
+          mbar_arrive_expect_tx(fb, nload * (MLA_PAGE_SIZE * 128));
+        }
+        __syncwarp();
+        if (lane < 4 && my_load)
+          tma_load_2d_hint(kv + blk * bw::kBlk + lane * (MLA_PAGE_SIZE * 128), &tm_kv, blk * 64,
+                           row, fb, pol);
+        __syncwarp();
+        ++armed;
+      }
+      if (!ok) {
+        if (lane == 0) {
+          report(p.status, MLA_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        armed_part = armed;  // drained below
+        break;
+      }
+      issued = i + 1;
+    }
+    // Before the CTA exits, the copies this warp issued land: the last full
+    // tile's blocks (those a cut-short tile re-armed have landed for it: their
+    // release needed them), then the cut-short tile's armed blocks.
+    if (lane == 0) {
+      if (issued > 0) {
+        const int k = issued - 1;
+        for (int bi = armed_part; bi < 9; ++bi)
+          mbar_wait(full_blk(bi == 0 ? bw::kRopeBlk : bi - 1), k & 1, kWaitLimitCycles);
+      }
+      for (int bi = 0; bi < armed_part; ++bi)
+        mbar_wait(full_blk(bi == 0 ? bw::kRopeBlk : bi - 1), issued & 1, kWaitLimitCycles);
+      mbar_wait(bar(BAR_QFULL), 0, kWaitLimitCycles);
+    }
+    __syncwarp();
+  } else if (warp == 1 || warp == 2) {
+    // ================= MMA issuers: warp 1 QK, warp 2 PV =================
+    constexpr uint32_t kIdQK = idesc_bf16(128, NR, 0, 0);
+    constexpr uint32_t kIdPV = idesc_bf16(128, NR, 1, 1);
+    bool ok = (warp == 1) ? mbar_wait(bar(BAR_QFULL), 0, p.wait_cycles) : true;
+    auto fail = [&]() {
+      if (lane == 0) {
+        report(p.status, MLA_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    };
+    // Four K = 16 steps of QK over block blk of the stage into S buffer sb.
+    auto qk_block = [&](int blk, int sb, bool first) {
+      tc_fence_after();
+#pragma unroll
+      for (int sub = 0; sub < 4; ++sub) {
+        const uint64_t a = smem_desc(sbase + C::kKV + blk * bw::kBlk + sub * 32, 16, 1024,
+                                     kLayoutSW128);
+        const uint64_t bd =
+            smem_desc(sbase + C::kQ + blk * NR * 128 + sub * 32, 16, 1024, kLayoutSW128);
+        umma_bf16(tmem + sb * NR, a, bd, kIdQK, (first && sub == 0) ? 0u : 1u);
+      }
+    };
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) fail();
+    if (warp == 1) {
+      // QK(j): the rope steps once the rope block has landed and S buffer
+      // j & 1 is free, then each latent block's steps as it lands (all of
+      // them first when the tile has rows to zero, which span every block).
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int sb = j & 1;
+        const int use = j >> 1;
+        bool w = !expired_here(p, WAIT_TILE_FULL, j) &&
+                 mbar_wait_abort(full_blk(bw::kRopeBlk), j & 1, p.wait_cycles, abort_flag);
+        if (w && use >= 1)
+          w = mbar_wait_abort(bar(BAR_SFREE0 + sb), (use - 1) & 1, p.wait_cycles, abort_flag);
+        w = __all_sync(0xffffffffu, w && !*abort_flag);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        const uint32_t info =
+            kGather ? *reinterpret_cast<volatile uint32_t*>(base + C::kStageInfo) : 0u;
+        const int valid = tok_end - (t0 + j * kTok);
+        const bool partial = kGather ? (info != 0x20202020u) : (valid < kTok);
+        if (partial) {
+          for (int blk = 0; w && blk < 8; ++blk)
+            w = mbar_wait_abort(full_blk(blk), j & 1, p.wait_cycles, abort_flag);
+          w = __all_sync(0xffffffffu, w && !*abort_flag);
+          if (!w) {
+            ok = false;
+            break;
+          }
+          zero_unloaded_rows_w<kGather>(base + C::kKV, lane, info, valid);
+        }
+        if (lane == 0) qk_block(bw::kRopeBlk, sb, true);
+        __syncwarp();
+        for (int blk = 0; blk < 8; ++blk) {
+          if (!partial) {
+            w = mbar_wait_abort(full_blk(blk), j & 1, p.wait_cycles, abort_flag);
+            w = __all_sync(0xffffffffu, w && !*abort_flag);
+            if (!w) break;
+          }
+          if (lane == 0) qk_block(blk, sb, false);
+          __syncwarp();
+        }
+        if (!w) {
+          ok = false;
+          break;
+        }
+        // S^T is complete, and the rope block free, once these MMAs are.
+        if (lane == 0) {
+          umma_commit(bar(BAR_SFULL0 + sb));
+          umma_commit(empty_blk(bw::kRopeBlk));
+        }
+        __syncwarp();
+      }
+    } else {
+      // PV(i) as soon as its P^T is ready; latent group d (blocks 2d, 2d + 1)
+      // is released when its MMAs complete.
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int pb = i & 1;
+        bool w = !expired_here(p, WAIT_P_FULL, i) &&
+                 mbar_wait_abort(bar(BAR_PFULL0 + pb), (i >> 1) & 1, p.wait_cycles,
+                                 abort_flag);
+        w = __all_sync(0xffffffffu, w && !*abort_flag);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t pbuf = sbase + C::kP + pb * C::kPBytes;
+#pragma unroll
+          for (int d = 0; d < 4; ++d) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              // A = V^T, MN-major: 64-element atoms 16 KB apart (latent blocks
+              // 2d, 2d + 1), 8-token groups 1 KB apart; 16 tokens per step.
+              const uint64_t a = smem_desc(sbase + C::kKV + 2 * d * bw::kBlk + ks * 2048,
+                                           bw::kBlk, 1024, kLayoutSW128);
+              // B = P^T, MN-major, no swizzle: 8-row groups 2 KB apart, 8-token
+              // groups 128 B apart.
+              const uint64_t bd = smem_desc(pbuf + ks * 256, 128, 2048, kLayoutNone);
+              umma_bf16(tmem + C::kOCol + d * NR, a, bd, kIdPV, (i > 0 || ks > 0) ? 1u : 0u);
+            }
+            umma_commit(empty_blk(2 * d));
+            umma_commit(empty_blk(2 * d + 1));
+          }
+          umma_commit(bar(BAR_PFREE0 + pb));
+          umma_commit(bar((i & 1) ? kBarOdone1W : BAR_ODONE));
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok) fail();
+    if (lane == 0) umma_commit(bar(BAR_FINAL));
+    __syncwarp();
+    mbar_wait(bar(BAR_FINAL), 0, kWaitLimitCycles);
+  } else {
+    // ================= softmax warpgroups =================
+    // As in the FP8 kernel's 32/48-row configurations: TMEM lane = token of
+    // the tile, warpgroup g owns rows [g * NRH, (g + 1) * NRH) of every token.
+    constexpr int NRH = C::NRH;
+    constexpr int NT = 128 * C::SWG;
+    const int quad = warp & 3;
+    const int rbase = ((warp - 3) >> 2) * NRH;
+    const int tok = quad * 32 + lane;  // token within the tile == TMEM lane == O^T lane
+    const int sid = threadIdx.x - 96;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    float k_row = -INFINITY;
+    float l_row = 0.0f;
+    float kreg[NRH];
+#pragma unroll
+    for (int k = 0; k < NRH; ++k) kreg[k] = -INFINITY;
+    const float c = c_log2;
+    const int qi_first = row0 / p.num_heads;
+    const int lim_min = p.causal ? min(tok_end, L - q_b + qi_first + 1) : tok_end;
+    const int my_row0 = row0 + rbase;
+    const int my_rows = max(0, min(NRH, rows_valid - rbase));
+    // Selection: logical page ids of 8 tiles' compact pages, one per lane
+    // (this warp's tokens are page `quad` of the tile).
+    auto sel_window = [&](int w) -> int {
+      const int cp = t0 / MLA_PAGE_SIZE + w * 32 + lane;
+      return (cp < p.topk) ? p.block_idx[static_cast<int64_t>(b) * p.topk + cp] : -1;
+    };
+    int sel_cur = -1, sel_next = -1;
+    if (sparse) {
+      sel_cur = sel_window(0);
+      sel_next = sel_window(1);
+    }
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int sb = i & 1;
+      const int use = i >> 1;
+      if (ok)
+        ok = !expired_here(p, WAIT_S_FULL, i) &&
+             mbar_wait_abort(bar(BAR_SFULL0 + sb), use & 1, p.wait_cycles, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok && lane == 0) *abort_flag = 1;  // the other roles stop waiting
+      float t[NRH];
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[NRH];
+#pragma unroll
+        for (int cc = 0; cc < NRH / 8; ++cc)
+          tmem_ld8(tmem + lane_addr + sb * NR + rbase + cc * 8,
+                   *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) t[k] = __uint_as_float(r[k]);
+        tc_fence_before();
+        mbar_arrive(bar(BAR_SFREE0 + sb));
+      } else {
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) t[k] = 0.0f;
+      }
+      const int tile_tok0 = t0 + i * kTok;
+      const int j = tile_tok0 + tok;
+      if constexpr (kGather) {
+        // Restricted key sets: the token's key position decides.
+        int64_t pos = j;
+        bool tok_ok = j < tok_end;
+        if (sparse) {
+          if (i > 0 && (i & 7) == 0) {
+            sel_cur = sel_next;
+            sel_next = sel_window((i >> 3) + 1);
+          }
+          const int lp = __shfl_sync(0xffffffffu, sel_cur, (i & 7) * 4 + quad);
+          pos = static_cast<int64_t>(lp) * MLA_PAGE_SIZE + lane;
+          tok_ok = tok_ok && lp >= 0;
+        }
+        tok_ok = tok_ok && pos >= sr.win_lo && pos < sr.win_hi;
+        int qi = my_row0 / p.num_heads;
+        int h = my_row0 - qi * p.num_heads;
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) {
+          const bool vis = tok_ok && k < my_rows && (!p.causal || pos < L - q_b + qi + 1);
+          t[k] = vis ? t[k] * c : -INFINITY;
+          if (++h == p.num_heads) {
+            h = 0;
+            ++qi;
+          }
+        }
+      } else if (tile_tok0 + kTok <= lim_min) {
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) t[k] = (k < my_rows) ? t[k] * c : -INFINITY;
+      } else {
+        int qi = my_row0 / p.num_heads;
+        int h = my_row0 - qi * p.num_heads;
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) {
+          const int lim = p.causal ? min(tok_end, L - q_b + qi + 1) : tok_end;
+          t[k] = (k < my_rows && j < lim) ? t[k] * c : -INFINITY;
+          if (++h == p.num_heads) {
+            h = 0;
+            ++qi;
+          }
+        }
+      }
+      // Reference check and update as in the FP8 kernel (integer references
+      // k with t <= k + 0.75; exact power-of-two rescales of l and O^T).
+      bool over = false;
+#pragma unroll
+      for (int k = 0; k < NRH; ++k) over |= t[k] > kreg[k] + 0.75f;
+      const bool any_over = bar_sync_or(kVoteBarrier, NT, over);
+      if (sid < NR && i > 0) {
+        const float* rs = red_sum + ((i - 1) & 1) * 4 * NR;
+        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+      }
+      if (any_over) {
+        {
+          float tm[NRH];
+#pragma unroll
+          for (int k = 0; k < NRH; ++k) tm[k] = t[k];
+          warp_reduce_rows<NRH, true>(tm, lane, red_max + quad * NR + rbase);
+        }
+        if (sid == 0) flags[0] = 0;
+        named_bar_sync(kSoftmaxBarrier, NT);  // B1: tile maxima ready
+        if (sid < NR) {
+          const float mt = fmaxf(fmaxf(red_max[sid], red_max[NR + sid]),
+                                 fmaxf(red_max[2 * NR + sid], red_max[3 * NR + sid]));
+          float k_new = k_row;
+          if (mt > k_row + 0.75f) k_new = ceilf(mt);
+          float alpha = 1.0f;
+          if (k_new != k_row && k_row != -INFINITY) {
+            const int e = static_cast<int>(k_row - k_new);
+            alpha = (e < -126) ? 0.0f : pow2i(e);
+            flags[0] = 1;
+          }
+          l_row *= alpha;
+          k_row = k_new;
+          kref[sid] = k_new;
+          alpha_s[sid] = alpha;
+        }
+        named_bar_sync(kSoftmaxBarrier, NT);  // B2: references ready
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) kreg[k] = kref[rbase + k];
+        const bool corr = flags[0] != 0;
+        if (ok && corr && i > 0) {
+          // PV(i - 1) done (S^T(i) implies PV(i - 1) released every latent
+          // block, so its completion barrier is within one phase).
+          ok = mbar_wait_abort(bar(((i - 1) & 1) ? kBarOdone1W : BAR_ODONE), ((i - 1) >> 1) & 1,
+                               p.wait_cycles, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int d = 0; d < 4; ++d) {
+#pragma unroll
+              for (int cc = 0; cc < NRH / 8; ++cc) {
+                uint32_t r[8];
+                const uint32_t addr = tmem + lane_addr + C::kOCol + d * NR + rbase + cc * 8;
+                tmem_ld8(addr, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha_s[rbase + cc * 8 + k]);
+                tmem_st8(addr, r);
+              }
+            }
+            tmem_st_wait();
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NRH; ++k) t[k] = softmax_weight<true>(t[k], kreg[k]);
+      // P^T buffer i & 1: free once PV(i - 2) is done.
+      const int pb = i & 1;
+      if (ok && expired_here(p, WAIT_P_FREE, i)) ok = false;
+      if (ok && i >= 2)
+        ok = mbar_wait_abort(bar(BAR_PFREE0 + pb), ((i >> 1) - 1) & 1, p.wait_cycles,
+                             abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok && lane == 0) *abort_flag = 1;
+      if (ok) {
+        // P^T (BF16), MN-major: [NR/8 row groups][128 tokens][8 rows].
+        uint8_t* pbuf = base + C::kP + pb * C::kPBytes;
+#pragma unroll
+        for (int g = 0; g < NRH / 8; ++g) {
+          uint4 v;
+          v.x = pack_bf16x2(t[g * 8 + 0], t[g * 8 + 1]);
+          v.y = pack_bf16x2(t[g * 8 + 2], t[g * 8 + 3]);
+          v.z = pack_bf16x2(t[g * 8 + 4], t[g * 8 + 5]);
+          v.w = pack_bf16x2(t[g * 8 + 6], t[g * 8 + 7]);
+          *reinterpret_cast<uint4*>(pbuf + ((rbase >> 3) + g) * 2048 + tok * 16) = v;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(BAR_PFULL0 + pb));
+      }
+      warp_reduce_rows<NRH, false>(t, lane, red_sum + (i & 1) * 4 * NR + quad * NR + rbase);
+    }
+    if (!ok && lane == 0) {
+      report(p.status, MLA_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // ---- epilogue (as in the FP8 kernel; O^T has NR columns per group) ----
+    named_bar_sync(kSoftmaxBarrier, NT);
+    const bool single = (nsplit == 1);
+    float* scale_s = alpha_s;
+    if (sid < NR) {
+      if (n_tiles > 0) {
+        const float* rs = red_sum + ((n_tiles - 1) & 1) * 4 * NR;
+        l_row += (rs[sid] + rs[NR + sid]) + (rs[2 * NR + sid] + rs[3 * NR + sid]);
+      }
+      const float m_s = (k_row == -INFINITY) ? -INFINITY : k_row - 8.0f;
+      const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + sid;
+      float sc = 0.0f;
+      if (sid < rows_here) {
+        if (single) {
+          // A sink is one more (zero-valued) key: it joins the denominator.
+          const float sink2 = p.sinks
+                                  ? p.sinks[(row0 + sid) % p.num_heads] * 1.4426950408889634f
+                                  : -INFINITY;
+          const float mm = fmaxf(l_row > 0.0f ? m_s : -INFINITY, sink2);
+          const float a = (l_row > 0.0f) ? exp2f(m_s - mm) : 0.0f;
+          const float den = l_row * a + (sink2 == -INFINITY ? 0.0f : exp2f(sink2 - mm));
+          if (p.lse)
+            p.lse[grow] = (den > 0.0f) ? 0.6931471805599453f * (mm + log2f(den)) : -INFINITY;
+          sc = (den > 0.0f) ? p.output_scale * a / den : 0.0f;
+        } else {
+          float* ml = p.ws_ml + (grow * p.max_splits + split) * 2;
+          ml[0] = m_s;
+          ml[1] = l_row;
+          sc = 1.0f;
+        }
+      }
+      scale_s[sid] = sc;
+    }
+    named_bar_sync(kSoftmaxBarrier, NT);
+    bool fin = !expired_here(p, WAIT_FINAL, 0) && mbar_wait(bar(BAR_FINAL), 0, p.wait_cycles);
+    fin = __all_sync(0xffffffffu, fin);
+    if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
+    if (ok && fin && n_tiles > 0) {
+      tc_fence_after();
+      // Per latent group: this warpgroup's NRH columns in one batch of TMEM
+      // loads, then the stores (row k of the warpgroup at base + k * stride).
+      const int64_t grow0 = static_cast<int64_t>(b) * p.rows_per_req + row0 + rbase;
+      const int64_t stride = single ? MLA_LATENT_DIM
+                                    : static_cast<int64_t>(p.max_splits) * MLA_LATENT_DIM;
+      float* const obase =
+          single ? nullptr : p.ws_o + (grow0 * p.max_splits + split) * MLA_LATENT_DIM;
+      const int nrow = min(NRH, rows_here - rbase);
+#pragma unroll 1
+      for (int d = 0; d < 4; ++d) {
+        const int dim = d * 128 + tok;
+        uint32_t r[NRH];
+#pragma unroll
+        for (int cc = 0; cc < NRH / 8; ++cc)
+          tmem_ld8(tmem + lane_addr + C::kOCol + d * NR + rbase + cc * 8,
+                   *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) {
+          if (k < nrow) {
+            const float v = __uint_as_float(r[k]) * scale_s[rbase + k];
+            if (single) {
+              const int64_t off = (grow0 + k) * MLA_LATENT_DIM + dim;
+              p.out[off] = __float2bfloat16_rn(v);
+              if (p.out_f32) p.out_f32[off] = v;
+            } else {
+              obase[k * stride + dim] = v;
+            }
+          }
+        }
+      }
+    } else if (ok && fin && n_tiles == 0 && single) {
+      // No key of this split is visible to any row here: O = 0 (partials
+      // need only (-inf, 0)).
+      for (int d = 0; d < 4; ++d) {
+        const int dim = d * 128 + tok;
+        for (int row = rbase; row < min(rows_here, rbase + NRH); ++row) {
+          const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + row;
+          p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(0.0f);
+          if (p.out_f32) p.out_f32[grow * MLA_LATENT_DIM + dim] = 0.0f;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2-D BF16 view [rows, 576] with a (64, box_y) box, 128-byte swizzle.
 static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t box_y) {
   auto enc = encode_fn();
@@ -1386,13 +1489,13 @@ static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint32
 }
 
 template <int NR, bool kGather, bool kItems>
-static cudaError_t launch_split_bf16_t(const void* q, const void* kv, int64_t num_pages,
-                                       int batch, int groups, int num_ctas,
-                                       const DecodeParams& prm, cudaStream_t stream) {
-  using C = CfgB<NR>;
+static cudaError_t launch_split_bf16_w_t(const void* q, const void* kv, int64_t num_pages,
+                                         int batch, int groups, int num_ctas,
+                                         const DecodeParams& prm, cudaStream_t stream) {
+  using C = CfgW<NR>;
   static std::atomic<uint64_t> attr_done{0};
   {
-    const cudaError_t e = ensure_smem_attr(mla_split_kv_bf16_kernel<NR, kGather, kItems>,
+    const cudaError_t e = ensure_smem_attr(mla_split_kv_bf16_wide_kernel<NR, kGather, kItems>,
                                            static_cast<int>(C::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
   }
@@ -1402,7 +1505,7 @@ static cudaError_t launch_split_bf16_t(const void* q, const void* kv, int64_t nu
       !make_map_bf16(&tm_q, q, static_cast<uint64_t>(batch) * prm.rows_per_req, NR))
     return cudaErrorInvalidValue;
   const dim3 grid = kItems ? dim3(num_ctas) : dim3(batch, prm.max_splits * groups);
-  mla_split_kv_bf16_kernel<NR, kGather, kItems>
+  mla_split_kv_bf16_wide_kernel<NR, kGather, kItems>
       <<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_kv, tm_q, prm);
   return cudaGetLastError();
 }
@@ -1449,14 +1552,14 @@ static cudaError_t launch_split_bf16(const void* q, const void* kv, int64_t num_
                                                           num_ctas, prm, stream);
   } else {
     if (gather)
-      return items ? launch_split_bf16_t<NR, true, true>(q, kv, num_pages, batch, groups,
-                                                          num_ctas, prm, stream)
-                   : launch_split_bf16_t<NR, true, false>(q, kv, num_pages, batch, groups,
-                                                           num_ctas, prm, stream);
-    return items ? launch_split_bf16_t<NR, false, true>(q, kv, num_pages, batch, groups,
-                                                         num_ctas, prm, stream)
-                 : launch_split_bf16_t<NR, false, false>(q, kv, num_pages, batch, groups,
-                                                          num_ctas, prm, stream);
+      return items ? launch_split_bf16_w_t<NR, true, true>(q, kv, num_pages, batch, groups,
+                                                            num_ctas, prm, stream)
+                   : launch_split_bf16_w_t<NR, true, false>(q, kv, num_pages, batch, groups,
+                                                             num_ctas, prm, stream);
+    return items ? launch_split_bf16_w_t<NR, false, true>(q, kv, num_pages, batch, groups,
+                                                           num_ctas, prm, stream)
+                 : launch_split_bf16_w_t<NR, false, false>(q, kv, num_pages, batch, groups,
+                                                            num_ctas, prm, stream);
   }
 }
 

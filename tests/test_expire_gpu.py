@@ -5,8 +5,8 @@ MLA_ERR_TIMEOUT in the workspace status word, stops its other roles, lets its
 own copies and MMAs finish, frees TMEM and exits, and the context stays usable.
 The test hook mla_debug_set_expire makes one chosen wait (role, tile) read as
 expired without any real stall, so the path runs in every configuration: the
-16/32/48/96-row FP8 kernels and the 16-row (Q in TMEM) and 48-row BF16
-kernels, for each role whose wait the configuration has.  After each expired
+16/32/48/96-row FP8 kernels and the 16-row (Q in TMEM), 32-row and 48-row
+BF16 kernels, for each role whose wait the configuration has.  After each expired
 call the next call on the same context must match the oracle.
 """
 import numpy as np
@@ -33,7 +33,10 @@ CONFIGS = {
     "fp8_96rows": ("e4m3", 12, 8, 4000, True, (STAGE_FREE, TILE_FULL, P_FULL, S_FULL, P_FREE,
                                                FINAL)),
     "bf16_16rows": ("bf16", 12, 1, 4000, False, (STAGE_FREE, TILE_FULL, P_FULL, S_FULL, FINAL)),
-    "bf16_48rows": ("bf16", 12, 4, 4000, True, (STAGE_FREE, TILE_FULL, P_FULL, S_FULL, FINAL)),
+    "bf16_48rows": ("bf16", 12, 4, 4000, True, (STAGE_FREE, TILE_FULL, P_FULL, S_FULL, P_FREE,
+                                                FINAL)),
+    "bf16_32rows": ("bf16", 16, 2, 4000, True, (STAGE_FREE, TILE_FULL, P_FULL, S_FULL, P_FREE,
+                                                FINAL)),
 }
 CASES = [(name, role) for name, cfg in CONFIGS.items() for role in cfg[5]]
 
