@@ -31,8 +31,11 @@
 //    partial, is the same for any split plan up to exact scaling.
 //  * Warp roles: warp 0 issues TMA, warp 1 issues the QK tcgen05.mma (and
 //    owns TMEM), warp 2 the PV ones, and the next four warps (eight from 32
-//    rows up; TMEM lane quadrant = warp % 4) run the softmax, the rare O
-//    correction and the epilogue.
+//    rows up; for 96 rows an idle warp 3, then twelve; TMEM lane quadrant =
+//    warp % 4) run the softmax, the rare O correction and the epilogue.
+//  * The 96-row configuration fills and releases its two KV stages block by
+//    block (rope, then the four latent blocks), so a tile's load overlaps the
+//    previous tile's PV.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
