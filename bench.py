@@ -672,55 +672,102 @@ def main():
     del graphs, g_floor
 
     # ---- end to end through the public API with host buffers ----
+    # Each call copies its inputs (Q, page table, plan arrays, selection or
+    # item list) from pinned host memory and reads its output and LSE back.
+    # Two schedules are timed: "serial" (copies and call in order on one
+    # stream) and "overlapped" (the copies of call k + 1 on a second stream
+    # into the other of two device input sets while call k computes, the
+    # double buffering of a serving loop: call k waits for its own copies, and
+    # copies into a set wait until the call that last read it is done).  The
+    # second costs more host work per call, so it pays only where the call's
+    # device time hides it; the line reports the faster and both values.
     q_h = inp.q.cpu().pin_memory()
     pt_h = inp.page_table.cpu().pin_memory()
     meta_h = torch.tensor(np.stack([np.asarray(lens, np.int32), plan.splits, plan.chunks]),
                           dtype=torch.int32).pin_memory()
-    meta_d = torch.empty_like(meta_h, device=dev)
-    q_d = torch.empty_like(inp.q)
-    pt_d = torch.empty_like(inp.page_table)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    e2e_args = list(args_common)
-    e2e_args[0], e2e_args[3] = q_d, pt_d
-    e2e_args[5], e2e_args[6], e2e_args[7] = meta_d[0], meta_d[1], meta_d[2]
+    sel_h = sels[0].cpu().pin_memory() if is_sparse else None
+    it_h = torch.from_numpy(items_h).pin_memory() if use_items else None
     h2d = q_h.numel() * q_h.element_size() + pt_h.numel() * 4 + meta_h.numel() * 4
     if is_sparse:
-        sel_h = sels[0].cpu().pin_memory()
-        sel_d = torch.empty_like(sels[0])
-        e2e_args[22] = sel_d
         h2d += sel_h.numel() * 4
     if use_items:
-        it_h = torch.from_numpy(items_h).pin_memory()
-        it_d = torch.empty_like(items_d)
         h2d += it_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    sets = []
+    for _ in range(2):
+        st = {"q": torch.empty_like(inp.q), "pt": torch.empty_like(inp.page_table),
+              "meta": torch.empty_like(meta_h, device=dev),
+              "sel": torch.empty_like(sels[0]) if is_sparse else None,
+              "it": torch.empty_like(items_d) if use_items else None,
+              "copied": torch.cuda.Event(), "used": torch.cuda.Event()}
+        a_ = list(args_common)
+        a_[0], a_[3] = st["q"], st["pt"]
+        a_[5], a_[6], a_[7] = st["meta"][0], st["meta"][1], st["meta"][2]
+        if is_sparse:
+            a_[22] = st["sel"]
+        st["args"] = a_
+        sets.append(st)
+    copy_stream = torch.cuda.Stream(device=dev)
+    n_e2e = [0]
 
-    def e2e_step():
+    def e2e_step_serial():
+        st = sets[0]
         p = (mla.mla_decode_plan(plan_lens, H, q_len, sm_count=sm_count)
              if args.plan == "gb300" else plan)
         del p
-        q_d.copy_(q_h, non_blocking=True)
-        pt_d.copy_(pt_h, non_blocking=True)
-        meta_d.copy_(meta_h, non_blocking=True)
-        if is_sparse:
-            sel_d.copy_(sel_h, non_blocking=True)
         if use_items:
             mla.mla_decode_plan_items(plan.splits, H, q_len)  # host cost of the item list
-            it_d.copy_(it_h, non_blocking=True)
-        decode_call(*e2e_args, stream, items=it_d if use_items else None)
+        st["q"].copy_(q_h, non_blocking=True)
+        st["pt"].copy_(pt_h, non_blocking=True)
+        st["meta"].copy_(meta_h, non_blocking=True)
+        if is_sparse:
+            st["sel"].copy_(sel_h, non_blocking=True)
+        if use_items:
+            st["it"].copy_(it_h, non_blocking=True)
+        decode_call(*st["args"], stream, items=st["it"] if use_items else None)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-    e2e_us = max_over_ranks((time.perf_counter() - t0) * 1e6 / args.e2e_steps, dev)
+    def e2e_step_overlapped():
+        st = sets[n_e2e[0] & 1]
+        p = (mla.mla_decode_plan(plan_lens, H, q_len, sm_count=sm_count)
+             if args.plan == "gb300" else plan)
+        del p
+        if use_items:
+            mla.mla_decode_plan_items(plan.splits, H, q_len)  # host cost of the item list
+        with torch.cuda.stream(copy_stream):
+            if n_e2e[0] >= 2:
+                copy_stream.wait_event(st["used"])
+            st["q"].copy_(q_h, non_blocking=True)
+            st["pt"].copy_(pt_h, non_blocking=True)
+            st["meta"].copy_(meta_h, non_blocking=True)
+            if is_sparse:
+                st["sel"].copy_(sel_h, non_blocking=True)
+            if use_items:
+                st["it"].copy_(it_h, non_blocking=True)
+            st["copied"].record(copy_stream)
+        stream.wait_event(st["copied"])
+        decode_call(*st["args"], stream, items=st["it"] if use_items else None)
+        st["used"].record(stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        n_e2e[0] += 1
+
+    e2e_sched = {}
+    for name, step in (("serial", e2e_step_serial), ("overlapped", e2e_step_overlapped)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            for _ in range(args.e2e_steps):
+                step()
+            torch.cuda.synchronize(dev)
+        e2e_sched[name] = max_over_ranks((time.perf_counter() - t0) * 1e6 / args.e2e_steps, dev)
+    e2e_best = min(e2e_sched, key=e2e_sched.get)
+    e2e_us = e2e_sched[e2e_best]
 
     # ---- roofline of the dominant kernel (split-KV) ----
     # HBM-bound unless the flop per KV byte is above the ridge of the MMA
@@ -788,7 +835,9 @@ def main():
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "schedule": e2e_best, "serial_us": e2e_sched["serial"],
+                    "overlapped_us": e2e_sched["overlapped"]},
             "gpu_launches": K * (2 if plan.max_splits > 1 else 1),
             "replays": ({"n": len(rep_us), "p10_us": float(np.percentile(rep_us, 10)),
                          "median_us": float(np.median(rep_us)),
