@@ -1364,6 +1364,13 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         float* const obase = single ? nullptr
                                     : p.ws_o + (grow0 * p.max_splits + split) * MLA_LATENT_DIM;
         const int nrow = min(NRH, rows_here - rbase);  // rows of this warpgroup to store
+        // With a P^T buffer to spare (free after the item's last PV), each
+        // warp turns its 32 dims x 8 rows at a time around through 1 KB of it,
+        // so that a lane stores 4 contiguous dims of a row (16 B of a partial,
+        // 8 B of BF16 output) instead of one dim of each of four rows.
+        float* const scr = reinterpret_cast<float*>(base + C::kP) +
+                           (warp - C::kSoftmaxWarp0) * 256;
+        constexpr bool transpose = !C::kPInStage;
 #pragma unroll 1
         for (int d = 0; d < 4; ++d) {
           const int dim = d * 128 + tok_lane;
@@ -1376,6 +1383,42 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
               tmem_ld8(addr + NR + cc * 8, *reinterpret_cast<uint32_t(*)[8]>(&r2[cc * 8]));
           }
           tmem_ld_wait();
+          if (transpose) {
+            const int dim4 = d * 128 + quad * 32 + (lane & 7) * 4;  // this lane's 4 dims
+#pragma unroll
+            for (int c8 = 0; c8 < NRH / 8; ++c8) {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const int k = c8 * 8 + kk;
+                const float o = C::kWide ? __uint_as_float(r[k])
+                                         : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
+                scr[kk * 32 + lane] = o * scale_s[rbase + k];
+              }
+              __syncwarp();
+#pragma unroll
+              for (int m = 0; m < 2; ++m) {
+                const int kk = m * 4 + (lane >> 3);
+                const float4 v4 = *reinterpret_cast<const float4*>(scr + kk * 32 + (lane & 7) * 4);
+                const int k = c8 * 8 + kk;
+                if (k < nrow) {
+                  if (single) {
+                    const int64_t off = (grow0 + k) * MLA_LATENT_DIM + dim4;
+                    __nv_bfloat162 lo2 = __floats2bfloat162_rn(v4.x, v4.y);
+                    __nv_bfloat162 hi2 = __floats2bfloat162_rn(v4.z, v4.w);
+                    uint2 packed;
+                    packed.x = *reinterpret_cast<uint32_t*>(&lo2);
+                    packed.y = *reinterpret_cast<uint32_t*>(&hi2);
+                    *reinterpret_cast<uint2*>(p.out + off) = packed;
+                    if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + off) = v4;
+                  } else {
+                    *reinterpret_cast<float4*>(obase + k * stride + dim4) = v4;
+                  }
+                }
+              }
+              __syncwarp();
+            }
+            continue;
+          }
 #pragma unroll
           for (int k = 0; k < NRH; ++k) {
             if (k < nrow) {
@@ -1406,6 +1449,9 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           }
         }
       }
+      // Persistent CTAs: every warp is done with its P^T scratch before any
+      // writes the next item's P^T.
+      if (kPersist && !C::kPInStage) named_bar_sync(kSoftmaxBarrier, NT);
       // O^T has been read: the next item's first PV may overwrite it.
       tc_fence_before();
       mbar_arrive(bar(BAR_OFREE));
