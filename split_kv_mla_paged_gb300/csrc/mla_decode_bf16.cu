@@ -1430,9 +1430,13 @@ __global__ void __launch_bounds__(CfgW<NR>::kThreads, 1)
       float* const obase =
           single ? nullptr : p.ws_o + (grow0 * p.max_splits + split) * MLA_LATENT_DIM;
       const int nrow = min(NRH, rows_here - rbase);
+      // Each warp turns its 32 dims x 8 rows at a time around through 1 KB of
+      // the P^T buffers (free after the last PV), so that a lane stores 4
+      // contiguous dims of a row (16 B of a partial, 8 B of BF16 output).
+      float* const scr = reinterpret_cast<float*>(base + C::kP) + (warp - 3) * 256;
 #pragma unroll 1
       for (int d = 0; d < 4; ++d) {
-        const int dim = d * 128 + tok;
+        const int dim4 = d * 128 + quad * 32 + (lane & 7) * 4;  // this lane's 4 dims
         uint32_t r[NRH];
 #pragma unroll
         for (int cc = 0; cc < NRH / 8; ++cc)
@@ -1440,17 +1444,32 @@ __global__ void __launch_bounds__(CfgW<NR>::kThreads, 1)
                    *reinterpret_cast<uint32_t(*)[8]>(&r[cc * 8]));
         tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < NRH; ++k) {
-          if (k < nrow) {
-            const float v = __uint_as_float(r[k]) * scale_s[rbase + k];
-            if (single) {
-              const int64_t off = (grow0 + k) * MLA_LATENT_DIM + dim;
-              p.out[off] = __float2bfloat16_rn(v);
-              if (p.out_f32) p.out_f32[off] = v;
-            } else {
-              obase[k * stride + dim] = v;
+        for (int c8 = 0; c8 < NRH / 8; ++c8) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            scr[kk * 32 + lane] = __uint_as_float(r[c8 * 8 + kk]) * scale_s[rbase + c8 * 8 + kk];
+          __syncwarp();
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const int kk = m * 4 + (lane >> 3);
+            const float4 v4 = *reinterpret_cast<const float4*>(scr + kk * 32 + (lane & 7) * 4);
+            const int k = c8 * 8 + kk;
+            if (k < nrow) {
+              if (single) {
+                const int64_t off = (grow0 + k) * MLA_LATENT_DIM + dim4;
+                __nv_bfloat162 lo2 = __floats2bfloat162_rn(v4.x, v4.y);
+                __nv_bfloat162 hi2 = __floats2bfloat162_rn(v4.z, v4.w);
+                uint2 packed;
+                packed.x = *reinterpret_cast<uint32_t*>(&lo2);
+                packed.y = *reinterpret_cast<uint32_t*>(&hi2);
+                *reinterpret_cast<uint2*>(p.out + off) = packed;
+                if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + off) = v4;
+              } else {
+                *reinterpret_cast<float4*>(obase + k * stride + dim4) = v4;
+              }
             }
           }
+          __syncwarp();
         }
       }
     } else if (ok && fin && n_tiles == 0 && single) {
