@@ -1383,7 +1383,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
               tmem_ld8(addr + NR + cc * 8, *reinterpret_cast<uint32_t(*)[8]>(&r2[cc * 8]));
           }
           tmem_ld_wait();
-          if (transpose) {
+          if constexpr (transpose) {
             const int dim4 = d * 128 + quad * 32 + (lane & 7) * 4;  // this lane's 4 dims
 #pragma unroll
             for (int c8 = 0; c8 < NRH / 8; ++c8) {
@@ -1417,20 +1417,20 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
               }
               __syncwarp();
             }
-            continue;
-          }
+          } else {
 #pragma unroll
-          for (int k = 0; k < NRH; ++k) {
-            if (k < nrow) {
-              const float o = C::kWide ? __uint_as_float(r[k])
-                                       : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
-              const float v = o * scale_s[rbase + k];
-              if (single) {
-                const int64_t off = (grow0 + k) * MLA_LATENT_DIM + dim;
-                p.out[off] = __float2bfloat16_rn(v);
-                if (p.out_f32) p.out_f32[off] = v;
-              } else {
-                obase[k * stride + dim] = v;
+            for (int k = 0; k < NRH; ++k) {
+              if (k < nrow) {
+                const float o = C::kWide ? __uint_as_float(r[k])
+                                         : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
+                const float v = o * scale_s[rbase + k];
+                if (single) {
+                  const int64_t off = (grow0 + k) * MLA_LATENT_DIM + dim;
+                  p.out[off] = __float2bfloat16_rn(v);
+                  if (p.out_f32) p.out_f32[off] = v;
+                } else {
+                  obase[k * stride + dim] = v;
+                }
               }
             }
           }
