@@ -1371,6 +1371,12 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
         float* const scr = reinterpret_cast<float*>(base + C::kP) +
                            (warp - C::kSoftmaxWarp0) * 256;
         constexpr bool transpose = !C::kPInStage;
+        // The rows' scales in registers: read from shared memory inside the
+        // store loops, each would wait behind the previous row's stores (the
+        // compiler cannot tell the two shared-memory pointers apart).
+        float sc_r[NRH];
+#pragma unroll
+        for (int k = 0; k < NRH; ++k) sc_r[k] = scale_s[rbase + k];
 #pragma unroll 1
         for (int d = 0; d < 4; ++d) {
           const int dim = d * 128 + tok_lane;
@@ -1392,7 +1398,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
                 const int k = c8 * 8 + kk;
                 const float o = C::kWide ? __uint_as_float(r[k])
                                          : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
-                scr[kk * 32 + lane] = o * scale_s[rbase + k];
+                scr[kk * 32 + lane] = o * sc_r[k];
               }
               __syncwarp();
 #pragma unroll
@@ -1423,7 +1429,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
               if (k < nrow) {
                 const float o = C::kWide ? __uint_as_float(r[k])
                                          : __uint_as_float(r[k]) + __uint_as_float(r2[k]);
-                const float v = o * scale_s[rbase + k];
+                const float v = o * sc_r[k];
                 if (single) {
                   const int64_t off = (grow0 + k) * MLA_LATENT_DIM + dim;
                   p.out[off] = __float2bfloat16_rn(v);

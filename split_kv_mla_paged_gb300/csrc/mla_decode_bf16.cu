@@ -754,6 +754,10 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
     if (!fin && lane == 0) report(p.status, MLA_ERR_TIMEOUT);
     if (ok && fin && n_tiles > 0) {
       tc_fence_after();
+      // The rows' scales in registers, not re-read after every store.
+      float sc_r[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) sc_r[k] = scale_s[k];
 #pragma unroll 1
       for (int d = 0; d < 4; ++d) {
         const int dim = d * 128 + lidx;
@@ -763,7 +767,7 @@ __global__ void __launch_bounds__(q16::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           if (k < rows_here) {
-            const float v = __uint_as_float(r[k]) * scale_s[k];
+            const float v = __uint_as_float(r[k]) * sc_r[k];
             const int64_t grow = static_cast<int64_t>(b) * p.rows_per_req + row0 + k;
             if (single) {
               p.out[grow * MLA_LATENT_DIM + dim] = __float2bfloat16_rn(v);
@@ -1434,6 +1438,11 @@ __global__ void __launch_bounds__(CfgW<NR>::kThreads, 1)
       // the P^T buffers (free after the last PV), so that a lane stores 4
       // contiguous dims of a row (16 B of a partial, 8 B of BF16 output).
       float* const scr = reinterpret_cast<float*>(base + C::kP) + (warp - 3) * 256;
+      // The rows' scales in registers: read from shared memory inside the
+      // store loop, each would wait behind the previous row's stores.
+      float sc_r[NRH];
+#pragma unroll
+      for (int k = 0; k < NRH; ++k) sc_r[k] = scale_s[rbase + k];
 #pragma unroll 1
       for (int d = 0; d < 4; ++d) {
         const int dim4 = d * 128 + quad * 32 + (lane & 7) * 4;  // this lane's 4 dims
@@ -1447,7 +1456,7 @@ __global__ void __launch_bounds__(CfgW<NR>::kThreads, 1)
         for (int c8 = 0; c8 < NRH / 8; ++c8) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            scr[kk * 32 + lane] = __uint_as_float(r[c8 * 8 + kk]) * scale_s[rbase + c8 * 8 + kk];
+            scr[kk * 32 + lane] = __uint_as_float(r[c8 * 8 + kk]) * sc_r[c8 * 8 + kk];
           __syncwarp();
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
