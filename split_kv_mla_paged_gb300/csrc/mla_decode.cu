@@ -419,10 +419,13 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
     flags[0] = 0;
     flags[1] = 0;
     flags[2] = 0;
-    for (int r = 0; r < NR; ++r) kref[r] = -INFINITY;
-    if constexpr (C::kWide)
-      for (int r = 0; r < NR; ++r) reinterpret_cast<int*>(base + C::kKci)[r] = kKcNone;
     fence_mbar_init();
+  }
+  // Rows start with no reference (every thread takes a few, next to thread
+  // 0's barrier set-up).
+  for (int r = threadIdx.x; r < NR; r += C::kThreads) {
+    kref[r] = -INFINITY;
+    if constexpr (C::kWide) reinterpret_cast<int*>(base + C::kKci)[r] = kKcNone;
   }
   if (warp == 1) {
     tmem_alloc(sbase + C::kTmemSlot, C::kTmemCols);
