@@ -364,6 +364,18 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
   (void)win_lo; (void)win_hi; (void)row0; (void)rows_here; (void)rows_valid; (void)n_tiles;   \
   (void)sparse; (void)c_log2; (void)kv_scale
 
+  // One item per CTA with contiguous pages: the producer's first page-id
+  // window is read before the set-up below, so that its latency overlaps it.
+  int pre_window = 0;
+  if constexpr (!kPersist && !kGather) {
+    if ((threadIdx.x >> 5) == 0) {
+      const int pi = first.t0 / MLA_PAGE_SIZE + static_cast<int>(threadIdx.x & 31);
+      if (pi < (first.tok_end + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE)
+        pre_window = p.page_table[static_cast<int64_t>(first.b) * p.max_pages + pi];
+    }
+  }
+  (void)pre_window;
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -500,7 +512,7 @@ __global__ void __launch_bounds__(Cfg<NR>::kThreads, 1)
           nv_out = 0;
           if constexpr (!kGather) {
             if (pi < page_end) {
-              pg = pt[pi];
+              pg = (!kPersist && w == 0) ? pre_window : pt[pi];
               if (pg < 0 || pg >= p.num_pages) {
                 report(p.status, MLA_ERR_INVALID_ARG);
                 pg = 0;
