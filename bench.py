@@ -547,33 +547,39 @@ def main():
     items_h = mla.mla_decode_plan_items(plan.splits, H, q_len) if use_items else None
     items_d = torch.from_numpy(items_h).to(dev) if use_items else None
 
-    def decode_call(*a, items=None):
+    def decode_call(*a, items=None, phases=mla.PHASE_ALL):
         # a = one call's 22 arguments (+ the page selection), then the stream
         c, s = a[:-1], a[-1]
         it = items_d if items is None else items
         if is_sparse:
             mla.mla_decode_sparse(*c[:6], c[22], topk, *c[6:22], cta_items=it,
-                                  persistent_ctas=args.persistent, stream=s)
+                                  persistent_ctas=args.persistent, phases=phases, stream=s)
         elif is_bf16:  # BF16 Q and KV: no q/kv scales
-            mla.mla_decode_bf16(*c[:14], *c[16:22], s)
+            if phases == mla.PHASE_ALL:
+                mla.mla_decode_bf16(*c[:14], *c[16:22], s)
+            else:
+                mla.mla_decode_bf16_ex(*c[:14], *c[16:22], phases=phases, stream=s)
         elif use_items:
-            mla.mla_decode_ex(*c[:22], cta_items=it, persistent_ctas=args.persistent, stream=s)
+            mla.mla_decode_ex(*c[:22], cta_items=it, persistent_ctas=args.persistent,
+                              phases=phases, stream=s)
         else:
             mla.mla_decode(*c[:22], s)
 
+    # The two phases of the same calls alone, for per-kernel durations: the
+    # split-KV kernel, then the merge of the partials it left (the phase entry
+    # points for plain calls, the options' phases for the others).
     def split_call(*a):
         if is_bf16 or is_sparse or use_items:
-            decode_call(*a)
+            decode_call(*a, phases=mla.PHASE_SPLIT)
         else:
             mla.mla_decode_splitkv(*a[:22], a[-1])
 
     def merge_call(*a):
-        mla.mla_decode_merge(*a[:22], a[-1])
+        if is_bf16 or is_sparse or use_items:
+            decode_call(*a, phases=mla.PHASE_MERGE)
+        else:
+            mla.mla_decode_merge(*a[:22], a[-1])
 
-    # The BF16, sparse and item-list calls have no separate phases: their
-    # "split" graph is the whole call (an upper bound on the split kernel's
-    # time), and the merge is the shared merge kernel on the same workspace
-    # and plan.
     phases = (("full", decode_call), ("split", split_call), ("merge", merge_call))
 
     with torch.cuda.stream(stream):

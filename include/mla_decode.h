@@ -201,8 +201,20 @@ MLA_API int mla_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_
  *     finishes the current one, so each CTA's start-up is paid once.  The
  *     results are the same numbers as with one CTA per item.  FP8 entry
  *     points only (the BF16 ones return MLA_ERR_UNSUPPORTED).
+ * phases  MLA_PHASE_ALL (0): the split-KV kernel, then the merge.
+ *     MLA_PHASE_SPLIT: the split-KV kernel only (requests with one split get
+ *     their final output, the others partials in the workspace).
+ *     MLA_PHASE_MERGE: the merge only, of the partials that a MLA_PHASE_SPLIT
+ *     call with the same arguments left in the workspace.  The two enqueued
+ *     one after the other on one stream are the whole call, as
+ *     mla_decode_splitkv and mla_decode_merge are for mla_decode (to time
+ *     the kernels one by one, or to run other work between them).  Other
+ *     values: MLA_ERR_INVALID_ARG.
  * Zero-initialise the structure: fields added later default to off.
  */
+#define MLA_PHASE_ALL 0
+#define MLA_PHASE_SPLIT 1
+#define MLA_PHASE_MERGE 2
 typedef struct {
   const float* q_scale_dev;
   const float* kv_scale_dev;
@@ -214,6 +226,7 @@ typedef struct {
   const int32_t* cta_items;
   int32_t num_ctas;
   int32_t persistent_ctas;
+  int32_t phases;
 } mla_decode_options_t;
 
 /* mla_decode with options (NULL options = mla_decode).  Same arguments,

@@ -61,7 +61,12 @@ class DecodeOptions(ctypes.Structure):
                 ("softmax_scale_dev", ctypes.c_void_p), ("output_scale", ctypes.c_float),
                 ("sinks", ctypes.c_void_p), ("query_lens", ctypes.c_void_p),
                 ("kv_bounds", ctypes.c_void_p), ("cta_items", ctypes.c_void_p),
-                ("num_ctas", ctypes.c_int32), ("persistent_ctas", ctypes.c_int32)]
+                ("num_ctas", ctypes.c_int32), ("persistent_ctas", ctypes.c_int32),
+                ("phases", ctypes.c_int32)]
+
+
+# mla_decode_options_t.phases: both phases, the split-KV kernel only, the merge only.
+PHASE_ALL, PHASE_SPLIT, PHASE_MERGE = 0, 1, 2
 
 
 class MlaError(RuntimeError):
@@ -250,15 +255,16 @@ def mla_decode_ex(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_req,
                   out_f32_debug=None, *, q_scale_dev=None, kv_scale_dev=None,
                   softmax_scale_dev=None, output_scale: float = 1.0, sinks=None,
                   query_lens=None, kv_bounds=None, cta_items=None, persistent_ctas: int = 0,
-                  stream=None) -> None:
+                  phases: int = PHASE_ALL, stream=None) -> None:
     """mla_decode with device-side scales, an output scale, attention sinks,
     ragged query counts, key windows and a CTA item list (a device int32
     tensor from mla_decode_plan_items), optionally run by persistent_ctas
-    CTAs that loop over the list."""
+    CTAs that loop over the list; phases selects the split-KV kernel or the
+    merge alone."""
     opts = DecodeOptions(_ptr(q_scale_dev), _ptr(kv_scale_dev), _ptr(softmax_scale_dev),
                          float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds),
                          _ptr(cta_items), 0 if cta_items is None else int(cta_items.numel()),
-                         int(persistent_ctas))
+                         int(persistent_ctas), int(phases))
     lib = load_library()
     _check(lib.mla_decode_ex(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages), _ptr(page_table),
                              int(max_pages_per_req), _ptr(kv_lens), _ptr(splits), _ptr(chunks),
@@ -290,13 +296,13 @@ def mla_decode_bf16_ex(q_bf16, kv_pages_bf16, num_pages, page_table, max_pages_p
                        softmax_scale, workspace, workspace_bytes, out_bf16, lse_f32=None,
                        out_f32_debug=None, *, softmax_scale_dev=None, output_scale: float = 1.0,
                        sinks=None, query_lens=None, kv_bounds=None, cta_items=None,
-                       stream=None) -> None:
+                       phases: int = PHASE_ALL, stream=None) -> None:
     """mla_decode_bf16 with a device softmax scale, output scale, sinks,
     ragged query counts, key windows and a CTA item list (a device int32
-    tensor from mla_decode_plan_items_bf16)."""
+    tensor from mla_decode_plan_items_bf16); phases as for mla_decode_ex."""
     opts = DecodeOptions(None, None, _ptr(softmax_scale_dev), float(output_scale), _ptr(sinks),
                          _ptr(query_lens), _ptr(kv_bounds), _ptr(cta_items),
-                         0 if cta_items is None else int(cta_items.numel()))
+                         0 if cta_items is None else int(cta_items.numel()), 0, int(phases))
     lib = load_library()
     _check(lib.mla_decode_bf16_ex(_ptr(q_bf16), _ptr(kv_pages_bf16), int(num_pages),
                                   _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),
@@ -312,12 +318,13 @@ def mla_decode_bf16_sparse(q_bf16, kv_pages_bf16, num_pages, page_table, max_pag
                            q_len, num_heads, causal, softmax_scale, workspace, workspace_bytes,
                            out_bf16, lse_f32=None, out_f32_debug=None, *, softmax_scale_dev=None,
                            output_scale: float = 1.0, sinks=None, query_lens=None,
-                           kv_bounds=None, cta_items=None, stream=None) -> None:
+                           kv_bounds=None, cta_items=None, phases: int = PHASE_ALL,
+                           stream=None) -> None:
     """BF16 sparse decode over the selected pages block_idx [batch, topk]
     (plan with the compact lengths 32 * topk)."""
     opts = DecodeOptions(None, None, _ptr(softmax_scale_dev), float(output_scale), _ptr(sinks),
                          _ptr(query_lens), _ptr(kv_bounds), _ptr(cta_items),
-                         0 if cta_items is None else int(cta_items.numel()))
+                         0 if cta_items is None else int(cta_items.numel()), 0, int(phases))
     lib = load_library()
     _check(lib.mla_decode_bf16_sparse(_ptr(q_bf16), _ptr(kv_pages_bf16), int(num_pages),
                                       _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),
@@ -335,13 +342,14 @@ def mla_decode_sparse(q_fp8, kv_pages_fp8, num_pages, page_table, max_pages_per_
                       workspace_bytes, out_bf16, lse_f32=None, out_f32_debug=None, *,
                       q_scale_dev=None, kv_scale_dev=None, softmax_scale_dev=None,
                       output_scale: float = 1.0, sinks=None, query_lens=None, kv_bounds=None,
-                      cta_items=None, persistent_ctas: int = 0, stream=None) -> None:
+                      cta_items=None, persistent_ctas: int = 0, phases: int = PHASE_ALL,
+                      stream=None) -> None:
     """Sparse decode over the selected pages block_idx [batch, topk] (plan with
     the compact lengths 32 * topk)."""
     opts = DecodeOptions(_ptr(q_scale_dev), _ptr(kv_scale_dev), _ptr(softmax_scale_dev),
                          float(output_scale), _ptr(sinks), _ptr(query_lens), _ptr(kv_bounds),
                          _ptr(cta_items), 0 if cta_items is None else int(cta_items.numel()),
-                         int(persistent_ctas))
+                         int(persistent_ctas), int(phases))
     lib = load_library()
     _check(lib.mla_decode_sparse(_ptr(q_fp8), _ptr(kv_pages_fp8), int(num_pages),
                                  _ptr(page_table), int(max_pages_per_req), _ptr(kv_lens),

@@ -1600,6 +1600,7 @@ struct DecodeLaunch {
   int kv_split;
   int max_splits;
   int num_ctas;  // length of prm.cta_items (0 without an item list)
+  int phases = MLA_PHASE_ALL;
 };
 
 static int prepare_decode(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
@@ -1739,6 +1740,11 @@ static int apply_options(const mla_decode_options_t* o, const char* who, DecodeL
     set_error(w + ": persistent_ctas needs a CTA item list and must be >= 0");
     return MLA_ERR_INVALID_ARG;
   }
+  if (o->phases != MLA_PHASE_ALL && o->phases != MLA_PHASE_SPLIT && o->phases != MLA_PHASE_MERGE) {
+    set_error(w + ": phases must be MLA_PHASE_ALL, MLA_PHASE_SPLIT or MLA_PHASE_MERGE");
+    return MLA_ERR_INVALID_ARG;
+  }
+  dl->phases = o->phases;
   dl->prm.q_scale_dev = o->q_scale_dev;
   dl->prm.kv_scale_dev = o->kv_scale_dev;
   dl->prm.sm_scale_dev = o->softmax_scale_dev;
@@ -1798,6 +1804,16 @@ static int launch_decode_merge(const DecodeLaunch& dl, cudaStream_t st) {
   return MLA_OK;
 }
 
+// The phases an options structure asks for (both by default).
+static int launch_decode_phases(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
+                                const DecodeLaunch& dl, cudaStream_t st) {
+  if (dl.phases != MLA_PHASE_MERGE) {
+    const int rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
+    if (rc != MLA_OK) return rc;
+  }
+  return dl.phases == MLA_PHASE_SPLIT ? MLA_OK : launch_decode_merge(dl, st);
+}
+
 }  // namespace mla
 
 #define MLA_DECODE_ARGS                                                                     \
@@ -1834,10 +1850,8 @@ extern "C" int mla_decode_ex(const void* q_fp8, const void* kv_pages_fp8, int64_
   if (rc != MLA_OK) return rc;
   rc = apply_options(options, "mla_decode_ex", &dl);
   if (rc != MLA_OK) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
-  if (rc != MLA_OK) return rc;
-  return launch_decode_merge(dl, st);
+  return launch_decode_phases(q_fp8, kv_pages_fp8, num_pages, dl,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int mla_decode_sparse(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,
@@ -1865,10 +1879,8 @@ extern "C" int mla_decode_sparse(const void* q_fp8, const void* kv_pages_fp8, in
   dl.prm.topk = topk;
   rc = apply_options(options, "mla_decode_sparse", &dl);
   if (rc != MLA_OK) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  rc = launch_decode_split(q_fp8, kv_pages_fp8, num_pages, dl, st);
-  if (rc != MLA_OK) return rc;
-  return launch_decode_merge(dl, st);
+  return launch_decode_phases(q_fp8, kv_pages_fp8, num_pages, dl,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int mla_decode_splitkv(const void* q_fp8, const void* kv_pages_fp8, int64_t num_pages,

@@ -1676,6 +1676,7 @@ static int decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t nu
   prm.topk = topk;
   prm.batch = batch;
   int num_ctas = 0;
+  int phases = MLA_PHASE_ALL;
   if (options) {
     if (!std::isfinite(options->output_scale)) {
       set_error(who + ": output_scale must be finite");
@@ -1688,6 +1689,11 @@ static int decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t nu
     if (options->persistent_ctas != 0) {
       set_error(who + ": persistent CTAs are FP8-only");
       return MLA_ERR_UNSUPPORTED;
+    }
+    phases = options->phases;
+    if (phases != MLA_PHASE_ALL && phases != MLA_PHASE_SPLIT && phases != MLA_PHASE_MERGE) {
+      set_error(who + ": phases must be MLA_PHASE_ALL, MLA_PHASE_SPLIT or MLA_PHASE_MERGE");
+      return MLA_ERR_INVALID_ARG;
     }
     if (options->cta_items) {
       const int64_t cap = static_cast<int64_t>(batch) * max_splits * rg.groups;
@@ -1706,26 +1712,28 @@ static int decode_bf16(const void* q_bf16, const void* kv_pages_bf16, int64_t nu
     prm.num_items = options->cta_items ? options->num_ctas : 0;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  switch (rg.nr) {
-    case 16:
-      e = launch_split_bf16<16>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, num_ctas,
-                                prm, st);
-      break;
-    case 32:
-      e = launch_split_bf16<32>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, num_ctas,
-                                prm, st);
-      break;
-    case 48:
-      e = launch_split_bf16<48>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, num_ctas,
-                                prm, st);
-      break;
-    default:
-      set_error(who + ": internal row grouping error");
-      return MLA_ERR_UNSUPPORTED;
+  cudaError_t e = cudaSuccess;
+  if (phases != MLA_PHASE_MERGE) {
+    switch (rg.nr) {
+      case 16:
+        e = launch_split_bf16<16>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, num_ctas,
+                                  prm, st);
+        break;
+      case 32:
+        e = launch_split_bf16<32>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, num_ctas,
+                                  prm, st);
+        break;
+      case 48:
+        e = launch_split_bf16<48>(q_bf16, kv_pages_bf16, num_pages, batch, rg.groups, num_ctas,
+                                  prm, st);
+        break;
+      default:
+        set_error(who + ": internal row grouping error");
+        return MLA_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return cuda_fail((who + ": split-KV launch").c_str(), e);
   }
-  if (e != cudaSuccess) return cuda_fail((who + ": split-KV launch").c_str(), e);
-  if (max_splits > 1) {
+  if (max_splits > 1 && phases != MLA_PHASE_SPLIT) {
     MergeParams mp = {};
     mp.po = prm.ws_o;
     mp.pml = prm.ws_ml;

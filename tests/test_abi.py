@@ -5,6 +5,7 @@ No compute call here: host-side argument checks return before any CUDA call.
 import ctypes
 import os
 import re
+import subprocess
 
 import numpy as np
 import pytest
@@ -193,3 +194,40 @@ def test_persistent_ctas_host_checks(lib):
     st = lib.mla_decode_bf16_ex(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 0.1,
                                 fake, 1 << 30, fake, None, None, ctypes.byref(opts), None)
     assert st == mla.MLA_ERR_UNSUPPORTED and "persistent" in mla.mla_last_error()
+
+
+def test_phases_are_checked(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0, 1.0, 1.0, 0.1, fake,
+            1 << 30, fake, None, None]
+    for bad in (-1, 3):
+        opts = mla.DecodeOptions(None, None, None, 1.0, None, None, None, None, 0, 0, bad)
+        assert lib.mla_decode_ex(*args, ctypes.byref(opts), None) == mla.MLA_ERR_INVALID_ARG
+        assert "phases" in mla.mla_last_error()
+        st = lib.mla_decode_sparse(*args[:6], fake, 8, *args[6:], ctypes.byref(opts), None)
+        assert st == mla.MLA_ERR_INVALID_ARG and "phases" in mla.mla_last_error()
+        st = lib.mla_decode_bf16_ex(fake, fake, 4, fake, 4, fake, fake, fake, 2, 2, 1, 1, 12, 0,
+                                    0.1, fake, 1 << 30, fake, None, None, ctypes.byref(opts),
+                                    None)
+        assert st == mla.MLA_ERR_INVALID_ARG and "phases" in mla.mla_last_error()
+
+
+def test_options_struct_matches_the_header(tmp_path):
+    # The binding's ctypes mirror of mla_decode_options_t against the C
+    # compiler's layout of the header's structure.
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "mla_decode.h"\n'
+        "int main(void) {\n"
+        '  printf("%zu", sizeof(mla_decode_options_t));\n'
+        + "".join(f'  printf(" %zu", offsetof(mla_decode_options_t, {name}));\n'
+                  for name, _ in mla.DecodeOptions._fields_)
+        + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [ctypes.sizeof(mla.DecodeOptions)] + [getattr(mla.DecodeOptions, name).offset
+                                                 for name, _ in mla.DecodeOptions._fields_]
+    assert got == want
