@@ -271,6 +271,11 @@ _add("bf16_h12_q1_l1m_b16", batch=16, num_heads=12, q_len=1, kv_lens=[1048576] *
 for _q in (1, 8):
     _add(f"sparse_h12_q{_q}_l1m_b16_top256", batch=16, num_heads=12, q_len=_q,
          kv_lens=[1048576] * 16, causal=(_q > 1), target=None, seed=6, topk=256)
+# The same selections in 128K-key requests: the same CTAs and tiles over a
+# 1.2 GB pool (a size for full-set profiler captures).
+for _q in (1, 8):
+    _add(f"sparse_h12_q{_q}_l128k_b16_top256", batch=16, num_heads=12, q_len=_q,
+         kv_lens=[131072] * 16, causal=(_q > 1), target=None, seed=6, topk=256)
 
 
 def workload_inputs(name: str, device: str | torch.device = "cpu",
