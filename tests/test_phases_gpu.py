@@ -1,8 +1,8 @@
 """GPU: an options call split into its two phases (mla_decode_options_t.phases:
 the split-KV kernel, then the merge, enqueued one after the other on one
-stream) writes the same bytes as the whole call, on the FP8 item-list, FP8
-sparse, BF16 and BF16 sparse entry points, for batches that mix one-split and
-many-split requests."""
+stream) writes the same bytes as the whole call, on the FP8 grid, item-list,
+persistent, sparse, BF16 and BF16 sparse paths, for batches that mix one-split
+and many-split requests."""
 import numpy as np
 import pytest
 import torch
@@ -45,6 +45,12 @@ def _run(kind, inp, lens, H, q_len, causal, sel, phase_seq):
         if kind == "fp8_items":
             mla.mla_decode_ex(*common, 1.0, 1.0, SOFTMAX_SCALE, ws, ws_bytes, out, lse, o32,
                               cta_items=items, phases=ph)
+        elif kind == "fp8_persistent":
+            mla.mla_decode_ex(*common, 1.0, 1.0, SOFTMAX_SCALE, ws, ws_bytes, out, lse, o32,
+                              cta_items=items, persistent_ctas=16, phases=ph)
+        elif kind == "fp8_grid":
+            mla.mla_decode_ex(*common, 1.0, 1.0, SOFTMAX_SCALE, ws, ws_bytes, out, lse, o32,
+                              output_scale=0.5, phases=ph)
         elif kind == "fp8_sparse":
             mla.mla_decode_sparse(*common[:6], sel_d, sel.shape[1], *common[6:], 1.0, 1.0,
                                   SOFTMAX_SCALE, ws, ws_bytes, out, lse, o32, phases=ph)
@@ -59,7 +65,8 @@ def _run(kind, inp, lens, H, q_len, causal, sel, phase_seq):
     return plan, out, lse, o32
 
 
-@pytest.mark.parametrize("kind", ["fp8_items", "fp8_sparse", "bf16", "bf16_sparse"])
+@pytest.mark.parametrize("kind", ["fp8_grid", "fp8_items", "fp8_persistent", "fp8_sparse", "bf16",
+                                  "bf16_sparse"])
 @pytest.mark.parametrize("H,q_len,lens", [
     (12, 1, [9000, 100, 3000]),
     (12, 8, [6000, 200]),
